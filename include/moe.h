@@ -1,0 +1,221 @@
+/*
+ * moe.h -- C ABI of the GB300 (sm_103a) quantized MoE decode-layer library.
+ *
+ * The layer is the decode step of a top-k mixture-of-experts FFN over affine
+ * group-quantised expert weights, as described by:
+ *   - PureDrive-35B-A3B-MLX model card (huggingface.co), "Summary": 256
+ *     experts, top-8 plus a shared expert, 6-bit experts, 8-bit shared
+ *     weights; "How it works": a verify pass of 1 + draft rows reads the
+ *     weights once and every row is identical to a one-row decode; fused
+ *     add + RMSNorm;
+ *   - flash-moe (ja.news.hada.io topic 27758), "FMA最適化デクォントカーネル":
+ *     dequantised weight = code * scale + bias; "Metal Compute Shaders":
+ *     dequant mat-vec, SwiGLU, RMS normalisation, MoE combine + residual +
+ *     gate; "Deferred GPU Expert Compute": combine, norm and residual stay on
+ *     the GPU and feed the next layer.
+ *
+ * Per token row m (rows never interact):
+ *   hn      = x_m / sqrt(mean(x_m^2) + eps) * gamma
+ *   logits  = W_r hn ;  p = softmax(logits) ;  top-k of p (ties: lower id),
+ *             w_i = p_i / sum_topk p
+ *   y_e     = W_d,e (silu(W_g,e hn) * (W_u,e hn))           (each selected e)
+ *   sigma   = sigmoid(w_sg . hn) ; y_s = shared-expert FFN of hn
+ *   out_m   = bf16(x_m + sum_i w_i y_i + sigma y_s)
+ *   outn_m  = bf16(out_m / sqrt(mean(out_m^2) + eps) * gamma_next)
+ * Every matrix is stored as groups of 64 consecutive elements along its input
+ * (contraction) axis, w = q * s + b with a b-bit code q and bf16 s, b.
+ *
+ * Conventions for every call:
+ *   - Return value: a moe_status.  No call throws, aborts or exits.
+ *   - Memory: the library never allocates device memory.  The caller owns
+ *     every device buffer (weights, workspace, inputs, outputs) and keeps it
+ *     alive while a handle or an enqueued call uses it.  Handles are small
+ *     host structs (malloc) that borrow those device pointers.
+ *   - Pointers named *_dev are device pointers; everything else is host.
+ *     bf16 values travel as uint16_t bit patterns.
+ *   - Streams: calls taking a stream only enqueue work on it and return;
+ *     errors raised while the kernels run are read with moe_stream_status().
+ *   - Sizes: H, I, I_shared multiples of 64 (H >= 256), E <= 512, k <= min(E, 32),
+ *     routed/shared bits in {4, 6, 8}, router bits in {0 (fp32), 8}.
+ */
+#ifndef MOE_H
+#define MOE_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+/* Same type as cudaStream_t; NULL is the legacy default stream. */
+typedef struct CUstream_st *moe_stream_t;
+
+typedef enum moe_status {
+    MOE_OK = 0,
+    MOE_ERR_INVALID_ARG = 1,      /* NULL pointer, negative size, inconsistent descriptors */
+    MOE_ERR_UNSUPPORTED = 2,      /* sizes or bit widths outside the supported set */
+    MOE_ERR_BUFFER_TOO_SMALL = 3, /* weight blob or workspace smaller than the *_size query */
+    MOE_ERR_CUDA = 4,             /* a CUDA runtime call failed; see moe_last_cuda_error() */
+    MOE_ERR_TIMEOUT = 5,          /* a device-side wait gave up (the kernel returned early) */
+    MOE_ERR_DEVICE = 6            /* a device-side check failed (bounds build) */
+} moe_status;
+
+/* Shape and storage of one layer. */
+typedef struct moe_layer_desc {
+    int H;            /* hidden size */
+    int I;            /* routed expert intermediate size */
+    int E;            /* routed experts */
+    int k;            /* experts kept per row */
+    int routed_bits;  /* 4, 6 or 8 */
+    int shared_bits;  /* 4, 6 or 8 (ignored when has_shared == 0) */
+    int router_bits;  /* 0 = fp32 router rows, 8 = 8-bit groups; also used for the shared-gate vector */
+    int has_shared;   /* 1 = a sigmoid-gated shared expert is present */
+    int I_shared;     /* shared expert intermediate size (has_shared == 1) */
+    float eps;        /* RMSNorm epsilon */
+} moe_layer_desc;
+
+/* One source matrix [rows, cols] in canonical form, device pointers:
+ * either codes (uint8, one code per byte, row-major) + scales + biases (bf16,
+ * [rows, cols/64]), or fp32 weights w (row-major) which the packer quantises:
+ *   s = bf16((max - min) / (2^b - 1)), b = bf16(min),
+ *   q = clamp(rint((w - b) / s), 0, 2^b - 1)  (fp32 arithmetic, q = 0 when s == 0).
+ * A router with router_bits == 0 must be given as fp32 w and stays fp32. */
+typedef struct moe_src_matrix {
+    const uint8_t *codes_dev;
+    const uint16_t *scales_dev;
+    const uint16_t *biases_dev;
+    const float *w_dev;
+} moe_src_matrix;
+
+/* All source tensors of one layer (device pointers). */
+typedef struct moe_src_layer {
+    moe_src_matrix gate;         /* [E * I, H]: expert e rows e*I .. e*I + I - 1 */
+    moe_src_matrix up;           /* [E * I, H] */
+    moe_src_matrix down;         /* [E * H, I] */
+    moe_src_matrix shared_gate;  /* [I_shared, H] */
+    moe_src_matrix shared_up;    /* [I_shared, H] */
+    moe_src_matrix shared_down;  /* [H, I_shared] */
+    moe_src_matrix router;       /* [E, H] */
+    moe_src_matrix sgate;        /* [1, H] shared-expert gate vector */
+    const uint16_t *gamma_dev;       /* [H] RMSNorm weight of this layer's input */
+    const uint16_t *gamma_next_dev;  /* [H] RMSNorm weight applied to the output, or NULL */
+} moe_src_layer;
+
+typedef struct moe_layer moe_layer;
+typedef struct moe_stack moe_stack;
+
+/* Tensor ids for moe_export_canonical. */
+enum {
+    MOE_T_ROUTER = 0, MOE_T_SGATE = 1, MOE_T_GATE = 2, MOE_T_UP = 3, MOE_T_DOWN = 4,
+    MOE_T_SHARED_GATE = 5, MOE_T_SHARED_UP = 6, MOE_T_SHARED_DOWN = 7
+};
+
+/* Bytes of the packed device blob of one layer (codes as LSB-first bit
+ * streams, per-group bf16 scale and bias, rows padded to 16 bytes).
+ * Errors: MOE_ERR_INVALID_ARG (NULL), MOE_ERR_UNSUPPORTED (sizes/bits). */
+int moe_pack_size(const moe_layer_desc *desc, size_t *weight_bytes);
+
+/* Affine group quantisation / packing into the device layout (flash-moe,
+ * "FMA最適化デクォントカーネル": w = code * scale + bias; group 64 along the
+ * input axis).  Reads the canonical sources in `src`, writes the blob at
+ * dst_dev (dst_bytes >= moe_pack_size), enqueued on `stream`, and returns a
+ * handle in *out that borrows dst_dev.  The sources may be freed once the
+ * stream has passed this call.
+ * Errors: INVALID_ARG, UNSUPPORTED, BUFFER_TOO_SMALL, CUDA. */
+int moe_pack_weights(const moe_layer_desc *desc, const moe_src_layer *src, void *dst_dev,
+                     size_t dst_bytes, moe_layer **out, moe_stream_t stream);
+
+/* Frees the handle (not the blob).  NULL is a no-op. */
+void moe_layer_destroy(moe_layer *layer);
+
+/* Writes one quantised matrix of a packed layer back in canonical form
+ * (codes one per byte, bf16 scales and biases) to device buffers sized like
+ * the moe_src_matrix of that tensor; `expert` selects the routed expert for
+ * MOE_T_GATE/UP/DOWN.  Errors: INVALID_ARG, UNSUPPORTED (fp32 router), CUDA. */
+int moe_export_canonical(const moe_layer *layer, int tensor_id, int expert, uint8_t *codes_dev,
+                         uint16_t *scales_dev, uint16_t *biases_dev, moe_stream_t stream);
+
+/* Scratch bytes needed by the decode calls for up to max_M rows per call
+ * (logits, expert activations, inter-layer activations and a control block).
+ * The same workspace serves every call on one stream; calls that run at the
+ * same time on the GPU need separate workspaces. */
+int moe_workspace_size(const moe_layer_desc *desc, int max_M, size_t *ws_bytes);
+
+/* Zeroes the workspace control block (grid-barrier state and status word).
+ * Call once after allocating a workspace, and again after any call reported
+ * MOE_ERR_TIMEOUT or MOE_ERR_DEVICE. */
+int moe_workspace_init(void *ws_dev, size_t ws_bytes, moe_stream_t stream);
+
+/* Router only (RMSNorm, router mat-vec, softmax, top-k, renormalisation) for
+ * M rows of x_dev [M, H] bf16.  Writes idx_dev [M, k] int32 (descending
+ * weight, ties to the lower expert id) and w_dev [M, k] fp32 (sums to 1 per
+ * row).  PureDrive model card, "Summary": the full top-8 of 256 is kept.
+ * Errors: INVALID_ARG, UNSUPPORTED (M < 1 or M > max_M of the workspace),
+ * BUFFER_TOO_SMALL, CUDA. */
+int moe_router_topk(const moe_layer *layer, const uint16_t *x_dev, int M, int32_t *idx_dev,
+                    float *w_dev, void *ws_dev, size_t ws_bytes, moe_stream_t stream);
+
+/* One layer for M rows of x_dev [M, H] bf16: writes out_dev [M, H] (bf16
+ * residual stream) and, when out_normed_dev != NULL, the fused next RMSNorm
+ * out_normed_dev [M, H] (needs gamma_next).  out_dev may alias x_dev.  Each
+ * selected expert's weights are streamed from memory once for all the rows
+ * that chose it (model card, "How it works": the verify pass reads its
+ * weights once), and row m of the result does not depend on the other rows.
+ * Errors: INVALID_ARG, UNSUPPORTED, BUFFER_TOO_SMALL, CUDA. */
+int moe_decode_layer(const moe_layer *layer, const uint16_t *x_dev, int M, uint16_t *out_dev,
+                     uint16_t *out_normed_dev, void *ws_dev, size_t ws_bytes, moe_stream_t stream);
+
+/* A stack of L layers with identical descriptors: x_{l+1} = out_l.  The
+ * handle borrows the layer handles.  flash-moe, "Deferred GPU Expert
+ * Compute": combine, norm and residual stay on the GPU and feed the next
+ * layer; here the whole stack runs in one persistent launch (per 64 layers
+ * and per chunk of rows) with no host round trip between layers.
+ * Errors: INVALID_ARG (NULL, L < 1, descriptors differ). */
+int moe_stack_create(moe_layer *const *layers, int L, moe_stack **out);
+
+/* Runs the stack on x_dev [M, H]; writes the last layer's out_dev [M, H] and,
+ * when out_normed_dev != NULL, its fused next RMSNorm.  out_dev may alias x_dev.
+ * Errors: as moe_decode_layer. */
+int moe_stack_forward(moe_stack *stack, const uint16_t *x_dev, int M, uint16_t *out_dev,
+                      uint16_t *out_normed_dev, void *ws_dev, size_t ws_bytes, moe_stream_t stream);
+
+/* moe_stack_forward from host buffers: copies x_host [M, H] to the device
+ * (into the workspace, which must be sized for M rows), runs the stack,
+ * copies out_host [M, H] back and synchronises the stream.  Pinned host
+ * memory gives the fastest copies.  Returns the stream status. */
+int moe_stack_forward_host(moe_stack *stack, const uint16_t *x_host, int M, uint16_t *out_host,
+                           void *ws_dev, size_t ws_bytes, moe_stream_t stream);
+
+/* Frees the stack handle (not the layers).  NULL is a no-op. */
+void moe_stack_destroy(moe_stack *stack);
+
+/* Synchronises `stream` and returns MOE_OK, MOE_ERR_TIMEOUT or MOE_ERR_DEVICE
+ * from the workspace status word (or MOE_ERR_CUDA). */
+int moe_stream_status(void *ws_dev, size_t ws_bytes, moe_stream_t stream);
+
+/* Test hook: the next decode calls make CTA `cta` skip its arrival at the
+ * first grid barrier (-1 = off) and give every device wait `timeout_ns`
+ * (<= 0 restores the default of 2 s).  Used to check that a wait that runs
+ * out returns MOE_ERR_TIMEOUT instead of hanging. */
+int moe_debug_set(int skip_cta, long long timeout_ns);
+
+/* Human-readable name of a status code (static string). */
+const char *moe_status_str(int status);
+
+/* The last CUDA error code seen by the library on this host thread (0 = none). */
+int moe_last_cuda_error(void);
+
+/* Host-side check of the code-extraction tables the kernels use (no GPU
+ * needed): returns the number of mismatching codes, 0 when consistent. */
+int moe_selftest_host(void);
+
+/* Number of kernel launches the library enqueued on this host thread since
+ * the last reset (reset = 1 zeroes it after reading). */
+long long moe_launch_count(int reset);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* MOE_H */

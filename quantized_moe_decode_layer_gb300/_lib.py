@@ -1,0 +1,97 @@
+"""ctypes view of libmoe.so (include/moe.h).  Argument marshalling only.
+
+The library must exist (built by quantized_moe_decode_layer_gb300.build or
+__graft_entry__.build()); there is no fallback of any kind.
+"""
+from __future__ import annotations
+
+import ctypes as C
+import os
+
+HERE = os.path.dirname(os.path.abspath(__file__))
+LIB_PATH = os.path.join(HERE, "libmoe.so")
+
+MOE_OK = 0
+STATUS = {0: "MOE_OK", 1: "MOE_ERR_INVALID_ARG", 2: "MOE_ERR_UNSUPPORTED", 3: "MOE_ERR_BUFFER_TOO_SMALL",
+          4: "MOE_ERR_CUDA", 5: "MOE_ERR_TIMEOUT", 6: "MOE_ERR_DEVICE"}
+T_ROUTER, T_SGATE, T_GATE, T_UP, T_DOWN, T_SHARED_GATE, T_SHARED_UP, T_SHARED_DOWN = range(8)
+
+# every symbol include/moe.h declares
+SYMBOLS = ["moe_pack_size", "moe_pack_weights", "moe_layer_destroy", "moe_export_canonical",
+           "moe_workspace_size", "moe_workspace_init", "moe_router_topk", "moe_decode_layer",
+           "moe_stack_create", "moe_stack_forward", "moe_stack_forward_host", "moe_stack_destroy",
+           "moe_stream_status", "moe_debug_set", "moe_status_str", "moe_last_cuda_error",
+           "moe_selftest_host", "moe_launch_count"]
+
+
+class MoeError(RuntimeError):
+    def __init__(self, fn: str, code: int):
+        self.code = code
+        super().__init__(f"{fn} failed: {STATUS.get(code, code)} (cuda error {last_cuda_error()})")
+
+
+class LayerDesc(C.Structure):
+    _fields_ = [("H", C.c_int), ("I", C.c_int), ("E", C.c_int), ("k", C.c_int),
+                ("routed_bits", C.c_int), ("shared_bits", C.c_int), ("router_bits", C.c_int),
+                ("has_shared", C.c_int), ("I_shared", C.c_int), ("eps", C.c_float)]
+
+
+class SrcMatrix(C.Structure):
+    _fields_ = [("codes_dev", C.c_void_p), ("scales_dev", C.c_void_p), ("biases_dev", C.c_void_p),
+                ("w_dev", C.c_void_p)]
+
+
+class SrcLayer(C.Structure):
+    _fields_ = [("gate", SrcMatrix), ("up", SrcMatrix), ("down", SrcMatrix),
+                ("shared_gate", SrcMatrix), ("shared_up", SrcMatrix), ("shared_down", SrcMatrix),
+                ("router", SrcMatrix), ("sgate", SrcMatrix),
+                ("gamma_dev", C.c_void_p), ("gamma_next_dev", C.c_void_p)]
+
+
+_lib = None
+
+
+def lib():
+    """Load libmoe.so; raise if it was not built."""
+    global _lib
+    if _lib is None:
+        if not os.path.exists(LIB_PATH):
+            raise RuntimeError(f"{LIB_PATH} is missing: build it with "
+                               "`python -c 'import __graft_entry__ as g; g.build()'`")
+        L = C.CDLL(LIB_PATH)
+        vp, i, sz = C.c_void_p, C.c_int, C.c_size_t
+        sig = {
+            "moe_pack_size": (i, [C.POINTER(LayerDesc), C.POINTER(sz)]),
+            "moe_pack_weights": (i, [C.POINTER(LayerDesc), C.POINTER(SrcLayer), vp, sz, C.POINTER(vp), vp]),
+            "moe_layer_destroy": (None, [vp]),
+            "moe_export_canonical": (i, [vp, i, i, vp, vp, vp, vp]),
+            "moe_workspace_size": (i, [C.POINTER(LayerDesc), i, C.POINTER(sz)]),
+            "moe_workspace_init": (i, [vp, sz, vp]),
+            "moe_router_topk": (i, [vp, vp, i, vp, vp, vp, sz, vp]),
+            "moe_decode_layer": (i, [vp, vp, i, vp, vp, vp, sz, vp]),
+            "moe_stack_create": (i, [C.POINTER(vp), i, C.POINTER(vp)]),
+            "moe_stack_forward": (i, [vp, vp, i, vp, vp, vp, sz, vp]),
+            "moe_stack_forward_host": (i, [vp, vp, i, vp, vp, sz, vp]),
+            "moe_stack_destroy": (None, [vp]),
+            "moe_stream_status": (i, [vp, sz, vp]),
+            "moe_debug_set": (i, [i, C.c_longlong]),
+            "moe_status_str": (C.c_char_p, [i]),
+            "moe_last_cuda_error": (i, []),
+            "moe_selftest_host": (i, []),
+            "moe_launch_count": (C.c_longlong, [i]),
+        }
+        for name, (res, args) in sig.items():
+            f = getattr(L, name)
+            f.restype = res
+            f.argtypes = args
+        _lib = L
+    return _lib
+
+
+def check(fn: str, rc: int) -> None:
+    if rc != MOE_OK:
+        raise MoeError(fn, rc)
+
+
+def last_cuda_error() -> int:
+    return int(lib().moe_last_cuda_error()) if _lib is not None else 0

@@ -1,0 +1,238 @@
+"""Thin Python binding over the C ABI: torch provides device memory and
+streams, every step of the layer runs in libmoe.so's kernels."""
+from __future__ import annotations
+
+import ctypes as C
+
+import torch
+
+from . import _lib
+from ._lib import LayerDesc, SrcLayer, SrcMatrix, check, lib
+
+
+def _ptr(t) -> int | None:
+    if t is None:
+        return None
+    assert t.is_cuda and t.is_contiguous(), "device tensors must be contiguous CUDA tensors"
+    return t.data_ptr()
+
+
+def _stream(stream=None) -> int:
+    s = stream if stream is not None else torch.cuda.current_stream()
+    return s.cuda_stream
+
+
+def make_desc(H, I, E, k, routed_bits, shared_bits=8, router_bits=8, has_shared=True, I_shared=0,
+              eps=1e-6) -> LayerDesc:
+    return LayerDesc(H, I, E, k, routed_bits, shared_bits, router_bits, 1 if has_shared else 0,
+                     I_shared if has_shared else 0, eps)
+
+
+def desc_from_shape(shape) -> LayerDesc:
+    """moe_layer_desc of a synth.LayerShape-like object."""
+    return make_desc(shape.H, shape.I, shape.E, shape.k, shape.routed_bits, shape.shared_bits,
+                     shape.router_bits, shape.has_shared, shape.I_shared, shape.eps)
+
+
+def pack_size(desc: LayerDesc) -> int:
+    n = C.c_size_t()
+    check("moe_pack_size", lib().moe_pack_size(C.byref(desc), C.byref(n)))
+    return n.value
+
+
+def workspace_size(desc: LayerDesc, max_M: int) -> int:
+    n = C.c_size_t()
+    check("moe_workspace_size", lib().moe_workspace_size(C.byref(desc), max_M, C.byref(n)))
+    return n.value
+
+
+def _bits16(t):
+    if t is None:
+        return None
+    return t.contiguous().view(torch.int16) if t.dtype == torch.bfloat16 else t.contiguous()
+
+
+def _src_matrix(d) -> tuple[SrcMatrix, list]:
+    """d: dict with codes/scales/biases (canonical) or 'w' (fp32), or a tensor (fp32)."""
+    keep = []
+    if d is None:
+        return SrcMatrix(), keep
+    if isinstance(d, torch.Tensor):
+        d = {"w": d}
+    m = SrcMatrix()
+    if d.get("codes") is not None:
+        c, s, b = d["codes"].contiguous(), _bits16(d["scales"]), _bits16(d["biases"])
+        keep += [c, s, b]
+        m.codes_dev, m.scales_dev, m.biases_dev = _ptr(c), _ptr(s), _ptr(b)
+    if d.get("w") is not None:
+        w = d["w"].contiguous().float()
+        keep.append(w)
+        m.w_dev = _ptr(w)
+    return m, keep
+
+
+class Layer:
+    """One packed layer: owns the device blob (a torch uint8 tensor) and the
+    C handle that borrows it."""
+
+    def __init__(self, desc: LayerDesc, src: dict, device="cuda", stream=None):
+        self.desc = desc
+        self.nbytes = pack_size(desc)
+        self.blob = torch.empty(self.nbytes, dtype=torch.uint8, device=device)
+        keep = []
+        sl = SrcLayer()
+
+        def flat(d, rows):
+            if d is None or isinstance(d, torch.Tensor):
+                return d
+            return {k: (v.reshape(rows, -1) if isinstance(v, torch.Tensor) else v) for k, v in d.items()}
+
+        E, I, H = desc.E, desc.I, desc.H
+        for name, d in (("gate", flat(src["gate"], E * I)), ("up", flat(src["up"], E * I)),
+                        ("down", flat(src["down"], E * H)), ("router", src["router"])):
+            m, k = _src_matrix(d)
+            keep += k
+            setattr(sl, name, m)
+        if desc.has_shared:
+            for name in ("shared_gate", "shared_up", "shared_down", "sgate"):
+                m, k = _src_matrix(src[name])
+                keep += k
+                setattr(sl, name, m)
+        g = _bits16(src["gamma"])
+        keep.append(g)
+        sl.gamma_dev = _ptr(g)
+        gn = _bits16(src.get("gamma_next"))
+        if gn is not None:
+            keep.append(gn)
+            sl.gamma_next_dev = _ptr(gn)
+        h = C.c_void_p()
+        check("moe_pack_weights", lib().moe_pack_weights(C.byref(desc), C.byref(sl), _ptr(self.blob),
+                                                         self.nbytes, C.byref(h), _stream(stream)))
+        self.handle = h
+        # the sources must outlive the enqueued pack kernels
+        torch.cuda.current_stream().synchronize() if stream is None else stream.synchronize()
+        del keep
+
+    def export(self, tensor_id: int, expert: int = 0, stream=None):
+        """Canonical (codes, scales bf16, biases bf16) of one packed matrix."""
+        d = self.desc
+        rows, cols = {
+            _lib.T_ROUTER: (d.E, d.H), _lib.T_SGATE: (1, d.H), _lib.T_GATE: (d.I, d.H), _lib.T_UP: (d.I, d.H),
+            _lib.T_DOWN: (d.H, d.I), _lib.T_SHARED_GATE: (d.I_shared, d.H), _lib.T_SHARED_UP: (d.I_shared, d.H),
+            _lib.T_SHARED_DOWN: (d.H, d.I_shared)}[tensor_id]
+        dev = self.blob.device
+        codes = torch.empty((rows, cols), dtype=torch.uint8, device=dev)
+        s = torch.empty((rows, cols // 64), dtype=torch.int16, device=dev)
+        b = torch.empty((rows, cols // 64), dtype=torch.int16, device=dev)
+        check("moe_export_canonical", lib().moe_export_canonical(self.handle, tensor_id, expert, _ptr(codes),
+                                                                 _ptr(s), _ptr(b), _stream(stream)))
+        return codes, s.view(torch.bfloat16), b.view(torch.bfloat16)
+
+    def __del__(self):
+        try:
+            if getattr(self, "handle", None):
+                lib().moe_layer_destroy(self.handle)
+                self.handle = None
+        except Exception:
+            pass
+
+
+class Workspace:
+    """Scratch for the decode calls (allocated by torch, zeroed control block)."""
+
+    def __init__(self, desc: LayerDesc, max_M: int, device="cuda", stream=None):
+        self.nbytes = workspace_size(desc, max_M)
+        self.buf = torch.empty(self.nbytes, dtype=torch.uint8, device=device)
+        assert self.buf.data_ptr() % 256 == 0
+        self.max_M = max_M
+        self.init(stream)
+
+    def init(self, stream=None):
+        check("moe_workspace_init", lib().moe_workspace_init(_ptr(self.buf), self.nbytes, _stream(stream)))
+
+    @property
+    def ptr(self) -> int:
+        return self.buf.data_ptr()
+
+    def status(self, stream=None) -> int:
+        """Synchronise and return the device status (0 = MOE_OK)."""
+        return int(lib().moe_stream_status(self.ptr, self.nbytes, _stream(stream)))
+
+
+def router_topk(layer: Layer, x: torch.Tensor, ws: Workspace, stream=None):
+    M = x.shape[0]
+    idx = torch.empty((M, layer.desc.k), dtype=torch.int32, device=x.device)
+    w = torch.empty((M, layer.desc.k), dtype=torch.float32, device=x.device)
+    check("moe_router_topk", lib().moe_router_topk(layer.handle, _ptr(_bits16(x)), M, _ptr(idx), _ptr(w),
+                                                   ws.ptr, ws.nbytes, _stream(stream)))
+    return idx, w
+
+
+def decode_layer(layer: Layer, x: torch.Tensor, ws: Workspace, out=None, normed: bool = False, stream=None):
+    """out (and out_normed when normed) bf16 [M, H]."""
+    M = x.shape[0]
+    if out is None:
+        out = torch.empty_like(x)
+    on = torch.empty_like(x) if normed else None
+    check("moe_decode_layer", lib().moe_decode_layer(layer.handle, _ptr(_bits16(x)), M, _ptr(_bits16(out)),
+                                                     _ptr(_bits16(on)) if on is not None else None,
+                                                     ws.ptr, ws.nbytes, _stream(stream)))
+    return (out, on) if normed else out
+
+
+class Stack:
+    def __init__(self, layers):
+        self.layers = list(layers)
+        arr = (C.c_void_p * len(self.layers))(*[l.handle.value for l in self.layers])
+        h = C.c_void_p()
+        check("moe_stack_create", lib().moe_stack_create(arr, len(self.layers), C.byref(h)))
+        self.handle = h
+
+    def forward(self, x: torch.Tensor, ws: Workspace, out=None, normed: bool = False, stream=None):
+        M = x.shape[0]
+        if out is None:
+            out = torch.empty_like(x)
+        on = torch.empty_like(x) if normed else None
+        check("moe_stack_forward", lib().moe_stack_forward(self.handle, _ptr(_bits16(x)), M, _ptr(_bits16(out)),
+                                                           _ptr(_bits16(on)) if on is not None else None,
+                                                           ws.ptr, ws.nbytes, _stream(stream)))
+        return (out, on) if normed else out
+
+    def forward_host(self, x_host: torch.Tensor, out_host: torch.Tensor, ws: Workspace, stream=None):
+        """Host buffers in and out (copies inside the call); synchronises."""
+        assert not x_host.is_cuda and not out_host.is_cuda
+        M = x_host.shape[0]
+        check("moe_stack_forward_host",
+              lib().moe_stack_forward_host(self.handle, _bits16(x_host).data_ptr(), M, _bits16(out_host).data_ptr(),
+                                           ws.ptr, ws.nbytes, _stream(stream)))
+        return out_host
+
+    def __del__(self):
+        try:
+            if getattr(self, "handle", None):
+                lib().moe_stack_destroy(self.handle)
+                self.handle = None
+        except Exception:
+            pass
+
+
+def debug_set(skip_cta: int = -1, timeout_ns: int = 0) -> None:
+    check("moe_debug_set", lib().moe_debug_set(skip_cta, timeout_ns))
+
+
+def launch_count(reset: bool = False) -> int:
+    return int(lib().moe_launch_count(1 if reset else 0))
+
+
+def layer_src_from_synth(L: dict) -> dict:
+    """Source-tensor dict for Layer() from synth.make_layer's canonical dict."""
+    src = {"gate": L["gate"], "up": L["up"], "down": L["down"], "gamma": L["gamma"],
+           "gamma_next": L.get("gamma_next")}
+    sh = L["shape"]
+    src["router"] = {"w": L["router_w"]}
+    if sh.has_shared:
+        src["shared_gate"] = L["shared_gate"]
+        src["shared_up"] = L["shared_up"]
+        src["shared_down"] = L["shared_down"]
+        src["sgate"] = {"w": L["sgate_w"].reshape(1, -1)}
+    return src

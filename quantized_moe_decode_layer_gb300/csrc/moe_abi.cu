@@ -1,0 +1,369 @@
+// Host side of the C ABI declared in include/moe.h: argument checks,
+// blob/workspace layouts, row chunking and kernel launches.  No device
+// memory is allocated here.
+#include <cstdio>
+#include <cstdlib>
+#include <cstring>
+
+#include "moe_internal.h"
+#include "moe_unpack.cuh"
+
+namespace moe {
+
+namespace {
+thread_local int t_last_cuda_error = 0;
+thread_local long long t_launches = 0;
+int g_skip_cta = -1;
+long long g_timeout_ns = 2000000000LL;
+
+bool width_ok(int K)
+{
+    if (K <= 0 || K % kGroup) return false;
+    return K == 64 || K == 128 || K == 256 || K % 512 == 0;
+}
+
+bool bits_ok(int b) { return b == 4 || b == 6 || b == 8; }
+
+int check_status_word(void *ws)
+{
+    int st = 0;
+    cudaError_t e = cudaMemcpy(&st, reinterpret_cast<uint8_t *>(ws) + offsetof(Ctrl, status), sizeof st,
+                               cudaMemcpyDeviceToHost);
+    if (e != cudaSuccess) { note_cuda_error((int)e); return MOE_ERR_CUDA; }
+    if (st & kStatusTimeout) return MOE_ERR_TIMEOUT;
+    if (st) return MOE_ERR_DEVICE;
+    return MOE_OK;
+}
+}  // namespace
+
+void note_cuda_error(int err) { t_last_cuda_error = err; }
+void note_launch() { ++t_launches; }
+
+int rows_per_launch(int H)
+{
+    int r = 16384 / H;
+    if (r > kMaxRows) r = kMaxRows;
+    return r < 1 ? 1 : r;
+}
+
+bool make_geo(const moe_layer_desc &d, Geo &g)
+{
+    if (d.H < 256 || !width_ok(d.H) || !width_ok(d.I) || d.I > d.H) return false;
+    if (d.E < 1 || d.E > kMaxE || d.k < 1 || d.k > d.E || d.k > kMaxK) return false;
+    if (!bits_ok(d.routed_bits)) return false;
+    if (!(d.router_bits == 0 || bits_ok(d.router_bits))) return false;
+    if (d.has_shared != 0 && d.has_shared != 1) return false;
+    if (d.has_shared && (!bits_ok(d.shared_bits) || !width_ok(d.I_shared) || d.I_shared > d.H)) return false;
+    if (!(d.eps > 0.0f)) return false;
+    memset(&g, 0, sizeof g);
+    g.H = d.H; g.I = d.I; g.E = d.E; g.k = d.k;
+    g.has_shared = d.has_shared;
+    g.Is = d.has_shared ? d.I_shared : 0;
+    g.rb = d.routed_bits;
+    g.sb = d.has_shared ? d.shared_bits : 8;
+    g.qb = d.router_bits;
+    g.Er = d.E + d.has_shared;
+    g.eps = d.eps;
+    g.rr_bytes = row_bytes(g.H, g.qb);
+    g.g_bytes = row_bytes(g.H, g.rb);
+    g.d_bytes = row_bytes(g.I, g.rb);
+    g.sg_bytes = d.has_shared ? row_bytes(g.H, g.sb) : 0;
+    g.sd_bytes = d.has_shared ? row_bytes(g.Is, g.sb) : 0;
+    size_t o = 0;
+    auto put = [&](size_t bytes) { o = align_up(o, 256); size_t r = o; o += bytes; return r; };
+    g.off_router = put((size_t)g.Er * g.rr_bytes);
+    g.off_gamma = put((size_t)g.H * 2);
+    g.off_gamma_next = put((size_t)g.H * 2);
+    g.off_gu = put((size_t)g.E * g.I * 2 * g.g_bytes);
+    g.off_down = put((size_t)g.E * g.H * g.d_bytes);
+    g.off_sgu = put(d.has_shared ? (size_t)g.Is * 2 * g.sg_bytes : 0);
+    g.off_sdown = put(d.has_shared ? (size_t)g.H * g.sd_bytes : 0);
+    g.total = align_up(o, 256);
+    return true;
+}
+
+void make_ws_layout(const Geo &g, int max_M, WsLayout &w)
+{
+    const int R = rows_per_launch(g.H);
+    w.maxr = R;
+    w.max_slots = g.E < R * g.k ? g.E : R * g.k;
+    w.max_M = max_M;
+    size_t o = kCtrlBytes;
+    auto put = [&](size_t bytes) { o = align_up(o, 256); size_t r = o; o += bytes; return r; };
+    w.off_logits = put((size_t)R * g.Er * 4);
+    w.off_act = put((size_t)w.max_slots * R * g.I * 4);
+    w.off_act_s = put((size_t)R * (g.Is ? g.Is : 1) * 4);
+    w.off_ping = put((size_t)2 * R * g.H * 2);
+    w.off_stage_in = put((size_t)max_M * g.H * 2);
+    w.off_stage_out = put((size_t)max_M * g.H * 2);
+    w.total = align_up(o, 256);
+}
+
+namespace {
+
+int prepare(const moe_layer *layer, int M, void *ws, size_t ws_bytes, KParams &kp, int &R)
+{
+    if (!layer || !ws || M < 1) return MOE_ERR_INVALID_ARG;
+    if ((reinterpret_cast<uintptr_t>(ws) & 255) != 0) return MOE_ERR_INVALID_ARG;
+    memset(&kp, 0, sizeof kp);
+    kp.g = layer->geo;
+    make_ws_layout(kp.g, M, kp.ws_l);
+    if (ws_bytes < kp.ws_l.total) return MOE_ERR_BUFFER_TOO_SMALL;
+    R = kp.ws_l.maxr;
+    kp.ws = reinterpret_cast<uint8_t *>(ws);
+    kp.timeout_ns = g_timeout_ns;
+    kp.skip_cta = g_skip_cta;
+    return MOE_OK;
+}
+
+int plan_for(KParams &kp, int mc)
+{
+    const int sms = device_sms();
+    if (sms <= 0) return MOE_ERR_CUDA;
+    if (!make_plan(kp.g, mc, sms, kp.p)) return MOE_ERR_UNSUPPORTED;
+    kp.M = mc;
+    return MOE_OK;
+}
+
+bool aligned16(const void *p) { return (reinterpret_cast<uintptr_t>(p) & 15) == 0; }
+
+}  // namespace
+}  // namespace moe
+
+using namespace moe;
+
+extern "C" {
+
+int moe_pack_size(const moe_layer_desc *desc, size_t *weight_bytes)
+{
+    if (!desc || !weight_bytes) return MOE_ERR_INVALID_ARG;
+    Geo g;
+    if (!make_geo(*desc, g)) return MOE_ERR_UNSUPPORTED;
+    *weight_bytes = g.total;
+    return MOE_OK;
+}
+
+int moe_pack_weights(const moe_layer_desc *desc, const moe_src_layer *src, void *dst_dev, size_t dst_bytes,
+                     moe_layer **out, moe_stream_t stream)
+{
+    if (!desc || !src || !dst_dev || !out) return MOE_ERR_INVALID_ARG;
+    *out = nullptr;
+    Geo g;
+    if (!make_geo(*desc, g)) return MOE_ERR_UNSUPPORTED;
+    if (dst_bytes < g.total) return MOE_ERR_BUFFER_TOO_SMALL;
+    if ((reinterpret_cast<uintptr_t>(dst_dev) & 255) != 0) return MOE_ERR_INVALID_ARG;
+    if (!src->gamma_dev) return MOE_ERR_INVALID_ARG;
+    moe_layer *L = static_cast<moe_layer *>(calloc(1, sizeof(moe_layer)));
+    if (!L) return MOE_ERR_INVALID_ARG;
+    L->desc = *desc;
+    L->geo = g;
+    L->base = static_cast<uint8_t *>(dst_dev);
+    L->bytes = dst_bytes;
+    L->ptrs.router = L->base + g.off_router;
+    L->ptrs.gu = L->base + g.off_gu;
+    L->ptrs.down = L->base + g.off_down;
+    L->ptrs.sgu = g.has_shared ? L->base + g.off_sgu : nullptr;
+    L->ptrs.sdown = g.has_shared ? L->base + g.off_sdown : nullptr;
+    L->ptrs.gamma = reinterpret_cast<const uint16_t *>(L->base + g.off_gamma);
+    L->ptrs.gamma_next = src->gamma_next_dev ? reinterpret_cast<const uint16_t *>(L->base + g.off_gamma_next) : nullptr;
+    const int rc = launch_pack(*L, *src, reinterpret_cast<cudaStream_t>(stream));
+    if (rc != MOE_OK) {
+        free(L);
+        return rc;
+    }
+    *out = L;
+    return MOE_OK;
+}
+
+void moe_layer_destroy(moe_layer *layer) { free(layer); }
+
+int moe_export_canonical(const moe_layer *layer, int tensor_id, int expert, uint8_t *codes_dev,
+                         uint16_t *scales_dev, uint16_t *biases_dev, moe_stream_t stream)
+{
+    if (!layer || !codes_dev || !scales_dev || !biases_dev) return MOE_ERR_INVALID_ARG;
+    return launch_export(*layer, tensor_id, expert, codes_dev, scales_dev, biases_dev,
+                         reinterpret_cast<cudaStream_t>(stream));
+}
+
+int moe_workspace_size(const moe_layer_desc *desc, int max_M, size_t *ws_bytes)
+{
+    if (!desc || !ws_bytes || max_M < 1) return MOE_ERR_INVALID_ARG;
+    Geo g;
+    if (!make_geo(*desc, g)) return MOE_ERR_UNSUPPORTED;
+    WsLayout w;
+    make_ws_layout(g, max_M, w);
+    *ws_bytes = w.total;
+    return MOE_OK;
+}
+
+int moe_workspace_init(void *ws_dev, size_t ws_bytes, moe_stream_t stream)
+{
+    if (!ws_dev || ws_bytes < (size_t)kCtrlBytes) return MOE_ERR_INVALID_ARG;
+    cudaError_t e = cudaMemsetAsync(ws_dev, 0, kCtrlBytes, reinterpret_cast<cudaStream_t>(stream));
+    if (e != cudaSuccess) { note_cuda_error((int)e); return MOE_ERR_CUDA; }
+    return MOE_OK;
+}
+
+int moe_router_topk(const moe_layer *layer, const uint16_t *x_dev, int M, int32_t *idx_dev, float *w_dev,
+                    void *ws_dev, size_t ws_bytes, moe_stream_t stream)
+{
+    if (!x_dev || !idx_dev || !w_dev || !aligned16(x_dev)) return MOE_ERR_INVALID_ARG;
+    KParams kp;
+    int R;
+    int rc = prepare(layer, M, ws_dev, ws_bytes, kp, R);
+    if (rc) return rc;
+    kp.mode = kModeRouter;
+    kp.L = 1;
+    kp.layer[0] = layer->ptrs;
+    const int H = kp.g.H, k = kp.g.k;
+    for (int c0 = 0; c0 < M; c0 += R) {
+        const int mc = M - c0 < R ? M - c0 : R;
+        if ((rc = plan_for(kp, mc))) return rc;
+        kp.x = x_dev + (size_t)c0 * H;
+        kp.idx_out = idx_dev + (size_t)c0 * k;
+        kp.w_out = w_dev + (size_t)c0 * k;
+        if ((rc = launch_decode(kp, reinterpret_cast<cudaStream_t>(stream)))) return rc;
+    }
+    return MOE_OK;
+}
+
+int moe_decode_layer(const moe_layer *layer, const uint16_t *x_dev, int M, uint16_t *out_dev,
+                     uint16_t *out_normed_dev, void *ws_dev, size_t ws_bytes, moe_stream_t stream)
+{
+    if (!x_dev || !out_dev || !aligned16(x_dev) || !aligned16(out_dev)) return MOE_ERR_INVALID_ARG;
+    if (out_normed_dev && (!layer || !layer->ptrs.gamma_next)) return MOE_ERR_INVALID_ARG;
+    KParams kp;
+    int R;
+    int rc = prepare(layer, M, ws_dev, ws_bytes, kp, R);
+    if (rc) return rc;
+    kp.mode = kModeLayers;
+    kp.L = 1;
+    kp.layer[0] = layer->ptrs;
+    const int H = kp.g.H;
+    for (int c0 = 0; c0 < M; c0 += R) {
+        const int mc = M - c0 < R ? M - c0 : R;
+        if ((rc = plan_for(kp, mc))) return rc;
+        kp.x = x_dev + (size_t)c0 * H;
+        kp.out = out_dev + (size_t)c0 * H;
+        kp.out_normed = out_normed_dev ? out_normed_dev + (size_t)c0 * H : nullptr;
+        if ((rc = launch_decode(kp, reinterpret_cast<cudaStream_t>(stream)))) return rc;
+    }
+    return MOE_OK;
+}
+
+int moe_stack_create(moe_layer *const *layers, int L, moe_stack **out)
+{
+    if (!layers || L < 1 || !out) return MOE_ERR_INVALID_ARG;
+    *out = nullptr;
+    for (int l = 0; l < L; ++l) {
+        if (!layers[l]) return MOE_ERR_INVALID_ARG;
+        if (memcmp(&layers[l]->desc, &layers[0]->desc, sizeof(moe_layer_desc)) != 0) return MOE_ERR_INVALID_ARG;
+    }
+    moe_stack *s = static_cast<moe_stack *>(calloc(1, sizeof(moe_stack)));
+    if (!s) return MOE_ERR_INVALID_ARG;
+    s->layers = static_cast<moe_layer **>(calloc((size_t)L, sizeof(moe_layer *)));
+    if (!s->layers) { free(s); return MOE_ERR_INVALID_ARG; }
+    memcpy(s->layers, layers, sizeof(moe_layer *) * (size_t)L);
+    s->L = L;
+    *out = s;
+    return MOE_OK;
+}
+
+int moe_stack_forward(moe_stack *stack, const uint16_t *x_dev, int M, uint16_t *out_dev, uint16_t *out_normed_dev,
+                      void *ws_dev, size_t ws_bytes, moe_stream_t stream)
+{
+    if (!stack || !x_dev || !out_dev || !aligned16(x_dev) || !aligned16(out_dev)) return MOE_ERR_INVALID_ARG;
+    const moe_layer *last = stack->layers[stack->L - 1];
+    if (out_normed_dev && !last->ptrs.gamma_next) return MOE_ERR_INVALID_ARG;
+    KParams kp;
+    int R;
+    int rc = prepare(stack->layers[0], M, ws_dev, ws_bytes, kp, R);
+    if (rc) return rc;
+    kp.mode = kModeLayers;
+    const int H = kp.g.H;
+    for (int c0 = 0; c0 < M; c0 += R) {
+        const int mc = M - c0 < R ? M - c0 : R;
+        if ((rc = plan_for(kp, mc))) return rc;
+        for (int l0 = 0; l0 < stack->L; l0 += kMaxLayers) {
+            const int nl = stack->L - l0 < kMaxLayers ? stack->L - l0 : kMaxLayers;
+            kp.L = nl;
+            for (int i = 0; i < nl; ++i) kp.layer[i] = stack->layers[l0 + i]->ptrs;
+            kp.x = l0 == 0 ? x_dev + (size_t)c0 * H : out_dev + (size_t)c0 * H;
+            kp.out = out_dev + (size_t)c0 * H;
+            const bool final_group = l0 + nl == stack->L;
+            kp.out_normed = final_group && out_normed_dev ? out_normed_dev + (size_t)c0 * H : nullptr;
+            if ((rc = launch_decode(kp, reinterpret_cast<cudaStream_t>(stream)))) return rc;
+        }
+    }
+    return MOE_OK;
+}
+
+int moe_stack_forward_host(moe_stack *stack, const uint16_t *x_host, int M, uint16_t *out_host, void *ws_dev,
+                           size_t ws_bytes, moe_stream_t stream)
+{
+    if (!stack || !x_host || !out_host || !ws_dev || M < 1) return MOE_ERR_INVALID_ARG;
+    Geo g = stack->layers[0]->geo;
+    WsLayout w;
+    make_ws_layout(g, M, w);
+    if (ws_bytes < w.total) return MOE_ERR_BUFFER_TOO_SMALL;
+    cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
+    uint16_t *din = reinterpret_cast<uint16_t *>(static_cast<uint8_t *>(ws_dev) + w.off_stage_in);
+    uint16_t *dout = reinterpret_cast<uint16_t *>(static_cast<uint8_t *>(ws_dev) + w.off_stage_out);
+    const size_t bytes = (size_t)M * g.H * 2;
+    cudaError_t e = cudaMemcpyAsync(din, x_host, bytes, cudaMemcpyHostToDevice, st);
+    if (e != cudaSuccess) { note_cuda_error((int)e); return MOE_ERR_CUDA; }
+    int rc = moe_stack_forward(stack, din, M, dout, nullptr, ws_dev, ws_bytes, stream);
+    if (rc) return rc;
+    e = cudaMemcpyAsync(out_host, dout, bytes, cudaMemcpyDeviceToHost, st);
+    if (e != cudaSuccess) { note_cuda_error((int)e); return MOE_ERR_CUDA; }
+    return moe_stream_status(ws_dev, ws_bytes, stream);
+}
+
+void moe_stack_destroy(moe_stack *stack)
+{
+    if (!stack) return;
+    free(stack->layers);
+    free(stack);
+}
+
+int moe_stream_status(void *ws_dev, size_t ws_bytes, moe_stream_t stream)
+{
+    if (!ws_dev || ws_bytes < (size_t)kCtrlBytes) return MOE_ERR_INVALID_ARG;
+    cudaError_t e = cudaStreamSynchronize(reinterpret_cast<cudaStream_t>(stream));
+    if (e != cudaSuccess) { note_cuda_error((int)e); return MOE_ERR_CUDA; }
+    return check_status_word(ws_dev);
+}
+
+int moe_debug_set(int skip_cta, long long timeout_ns)
+{
+    g_skip_cta = skip_cta;
+    g_timeout_ns = timeout_ns > 0 ? timeout_ns : 2000000000LL;
+    return MOE_OK;
+}
+
+const char *moe_status_str(int status)
+{
+    switch (status) {
+    case MOE_OK: return "MOE_OK";
+    case MOE_ERR_INVALID_ARG: return "MOE_ERR_INVALID_ARG";
+    case MOE_ERR_UNSUPPORTED: return "MOE_ERR_UNSUPPORTED";
+    case MOE_ERR_BUFFER_TOO_SMALL: return "MOE_ERR_BUFFER_TOO_SMALL";
+    case MOE_ERR_CUDA: return "MOE_ERR_CUDA";
+    case MOE_ERR_TIMEOUT: return "MOE_ERR_TIMEOUT";
+    case MOE_ERR_DEVICE: return "MOE_ERR_DEVICE";
+    default: return "MOE_ERR_UNKNOWN";
+    }
+}
+
+int moe_last_cuda_error(void) { return t_last_cuda_error; }
+
+long long moe_launch_count(int reset)
+{
+    const long long n = t_launches;
+    if (reset) t_launches = 0;
+    return n;
+}
+
+int moe_selftest_host(void) { return unpack_selftest_host(); }
+
+}  // extern "C"

@@ -1,0 +1,146 @@
+// Internal definitions shared by the host ABI (moe_abi.cu), the packer
+// (moe_pack.cu) and the decode kernel (moe_layer.cu).  Not part of the ABI.
+#pragma once
+
+#include <cuda_runtime.h>
+
+#include <cstddef>
+#include <cstdint>
+
+#include "../../include/moe.h"
+
+namespace moe {
+
+constexpr int kGroup = 64;          // affine group along the contraction axis
+constexpr int kSub = 16;            // codes per sub-group (one lane step)
+constexpr int kConsumerWarps = 8;   // compute warps per CTA
+constexpr int kThreads = (kConsumerWarps + 1) * 32;  // + one TMA producer warp
+constexpr int kMaxRows = 8;         // token rows per launch (larger M is chunked)
+constexpr int kMaxLayers = 64;      // layers per persistent launch
+constexpr int kMaxStages = 64;      // ring stages (mbarrier pairs)
+constexpr int kMaxE = 512;
+constexpr int kMaxK = 32;
+constexpr int kCtrlBytes = 512;     // control block at the start of the workspace
+constexpr int kSmemMax = 232448;    // dynamic shared memory per CTA on sm_100-class parts
+
+// Status word bits (workspace control block).
+constexpr int kStatusTimeout = 1;
+constexpr int kStatusBounds = 2;
+
+__host__ __device__ constexpr size_t align_up(size_t v, size_t a) { return (v + a - 1) / a * a; }
+
+// Bytes of one packed row of K inputs: LSB-first code stream, then one
+// 32-bit word (scale | bias << 16) per 64-group, padded to 16 bytes.
+// bits == 0: K fp32 values.
+__host__ __device__ constexpr int row_bytes(int K, int bits)
+{
+    return bits == 0 ? (int)align_up((size_t)K * 4, 16)
+                     : (int)align_up((size_t)K * bits / 8 + (size_t)(K / kGroup) * 4, 16);
+}
+
+// Geometry of a layer: sizes, row sizes, blob offsets, launch plan.
+struct Geo {
+    int H, I, E, k, Is;
+    int has_shared, rb, sb, qb;     // routed / shared / router bits
+    int Er;                         // router rows = E + has_shared (last = shared gate)
+    int rr_bytes;                   // router row
+    int g_bytes;                    // routed gate (or up) row, K = H
+    int d_bytes;                    // routed down row, K = I
+    int sg_bytes;                   // shared gate (or up) row, K = H
+    int sd_bytes;                   // shared down row, K = Is
+    float eps;
+    // blob offsets (bytes)
+    size_t off_router, off_gamma, off_gamma_next, off_gu, off_down, off_sgu, off_sdown, total;
+};
+
+// Per-layer device pointers inside the packed blob.
+struct LayerPtrs {
+    const uint8_t *router;
+    const uint8_t *gu;       // E * I units of (gate row, up row)
+    const uint8_t *down;     // E * H rows
+    const uint8_t *sgu;      // I_shared units
+    const uint8_t *sdown;    // H rows
+    const uint16_t *gamma;
+    const uint16_t *gamma_next;  // NULL when absent
+};
+
+// Workspace layout (offsets from the workspace base).
+struct WsLayout {
+    int maxr;                // rows per launch
+    int max_slots;           // distinct routed experts per launch
+    size_t off_logits, off_act, off_act_s, off_ping, off_stage_in, off_stage_out, total;
+    int max_M;               // rows the host-staging area holds
+};
+
+struct Ctrl {                // first kCtrlBytes of the workspace
+    unsigned count;          // grid barrier arrivals
+    unsigned pad0[31];
+    unsigned gen;            // grid barrier generation (own 128-byte line)
+    unsigned pad1[31];
+    int status;              // kStatus* bits
+    int where;               // debug: which wait gave up
+    int pad2[62];
+};
+static_assert(sizeof(Ctrl) <= kCtrlBytes, "control block");
+
+// Launch plan of the persistent kernel.
+struct Plan {
+    int P;                   // CTAs (one per SM)
+    int S;                   // stage bytes
+    int NS;                  // ring stages
+    int maxr;                // rows per launch
+    int max_slots;
+    int hrows;               // output rows per CTA (upper bound)
+    int smem_bytes;
+};
+
+enum Mode { kModeLayers = 0, kModeRouter = 1 };
+
+struct KParams {
+    Geo g;
+    Plan p;
+    int L;                   // layers in this launch
+    LayerPtrs layer[kMaxLayers];
+    const uint16_t *x;       // [M, H] input of the first layer
+    int M;
+    uint16_t *out;           // [M, H] output of the last layer
+    uint16_t *out_normed;    // [M, H] or NULL
+    int32_t *idx_out;        // router mode
+    float *w_out;            // router mode
+    int mode;
+    uint8_t *ws;             // workspace base
+    WsLayout ws_l;
+    long long timeout_ns;
+    int skip_cta;
+};
+
+bool make_geo(const moe_layer_desc &d, Geo &g);
+void make_ws_layout(const Geo &g, int max_M, WsLayout &w);
+bool make_plan(const Geo &g, int maxr, int num_sms, Plan &p);
+int rows_per_launch(int H);
+int device_sms();
+
+}  // namespace moe
+
+struct moe_layer {
+    moe_layer_desc desc;
+    moe::Geo geo;
+    uint8_t *base;
+    size_t bytes;
+    moe::LayerPtrs ptrs;
+};
+
+struct moe_stack {
+    int L;
+    moe_layer **layers;
+};
+
+// Host-side entry points of the kernels (moe_layer.cu, moe_pack.cu).
+namespace moe {
+int launch_decode(const KParams &kp, cudaStream_t stream);
+int launch_pack(const moe_layer &L, const moe_src_layer &src, cudaStream_t stream);
+int launch_export(const moe_layer &L, int tensor_id, int expert, uint8_t *codes, uint16_t *scales,
+                  uint16_t *biases, cudaStream_t stream);
+void note_cuda_error(int err);
+void note_launch();
+}  // namespace moe

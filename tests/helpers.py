@@ -1,0 +1,61 @@
+"""Shared helpers for the tests: seeded inputs with the routing margin the
+parity checks need, oracle views and the element-wise tolerance."""
+from __future__ import annotations
+
+import numpy as np
+import torch
+
+import oracle
+import synth
+
+MARGIN = 1e-3          # top-k logit gap every parity row must have (oracle logits)
+ATOL, RTOL = 2e-3, 1e-2  # |gpu - ref| <= ATOL + RTOL * |ref| on the bf16 outputs
+
+
+def to_device(L: dict, dev) -> dict:
+    out = {}
+    for k, v in L.items():
+        if isinstance(v, dict):
+            out[k] = {kk: (vv.to(dev) if isinstance(vv, torch.Tensor) else vv) for kk, vv in v.items()}
+        elif isinstance(v, torch.Tensor):
+            out[k] = v.to(dev)
+        else:
+            out[k] = v
+    return out
+
+
+def bits_np(x: torch.Tensor) -> np.ndarray:
+    return synth.bf16_bits(x.detach().cpu()).numpy().view(np.uint16)
+
+
+def rows_with_margin(shape, lay: oracle.Layer, seed: int, M: int, correlation: float = 0.0,
+                     gamma=None, max_attempts: int = 200) -> torch.Tensor:
+    """bf16 rows [M, H] whose oracle top-k logit gaps are all >= MARGIN.
+    A row that fails is redrawn from its next attempt stream (row 0 as well,
+    which changes every correlated row)."""
+    attempts = [0] * M
+    for _ in range(max_attempts):
+        x = synth.make_rows(shape, seed, M, gamma=gamma, correlation=correlation, attempts=attempts)
+        r = lay.route(bits_np(x))
+        bad = [m for m in range(M) if r["margin"][m] < MARGIN]
+        if not bad:
+            return x
+        for m in bad:
+            attempts[m] += 1
+    raise RuntimeError("could not draw rows with the routing margin")
+
+
+def assert_close(got: np.ndarray, ref: np.ndarray, what: str):
+    got = np.asarray(got, np.float64)
+    ref = np.asarray(ref, np.float64)
+    err = np.abs(got - ref)
+    tol = ATOL + RTOL * np.abs(ref)
+    bad = err > tol
+    if bad.any():
+        i = np.argwhere(bad)[0]
+        raise AssertionError(f"{what}: {bad.sum()} of {bad.size} elements outside tolerance; first at "
+                             f"{tuple(i)}: got {got[tuple(i)]}, ref {ref[tuple(i)]}, max err {err.max()}")
+
+
+def bf16_tensor_to_f64(t: torch.Tensor) -> np.ndarray:
+    return t.detach().float().cpu().numpy().astype(np.float64)

@@ -1,0 +1,83 @@
+"""The C-ABI library without a GPU: it loads, exports every symbol that
+include/moe.h declares, checks its arguments, and sizes blobs/workspaces."""
+import ctypes as C
+import os
+import re
+
+import pytest
+
+import synth
+import quantized_moe_decode_layer_gb300 as moe
+from quantized_moe_decode_layer_gb300 import _lib
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+
+
+def declared_functions():
+    text = open(os.path.join(ROOT, "include", "moe.h")).read()
+    text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
+    return sorted(set(re.findall(r"\b(moe_[a-z_0-9]+)\s*\(", text)))
+
+
+def test_exports_every_declared_symbol():
+    L = moe.lib()
+    names = declared_functions()
+    assert len(names) >= 15
+    for n in names:
+        assert hasattr(L, n), n
+    assert set(names) == set(_lib.SYMBOLS)
+
+
+def test_unpack_tables_selftest():
+    assert moe.lib().moe_selftest_host() == 0
+
+
+def test_status_strings():
+    L = moe.lib()
+    for code, name in _lib.STATUS.items():
+        assert L.moe_status_str(code).decode() == name
+
+
+@pytest.mark.parametrize("shape,per_expert", [(synth.A35B, 2_555_904), (synth.B397, 7_077_888)])
+def test_pack_size_counts(shape, per_expert):
+    """Blob = router + gammas + experts + shared expert; no per-row padding at
+    these widths, so the expert bytes are exactly the algorithmic ones."""
+    d = moe.desc_from_shape(shape)
+    total = moe.pack_size(d)
+    H, I, E, Is = shape.H, shape.I, shape.E, shape.I_shared
+    expert = 2 * I * (H * shape.routed_bits // 8 + H // 64 * 4) + H * (I * shape.routed_bits // 8 + I // 64 * 4)
+    assert expert == per_expert
+    shared = 2 * Is * (H + H // 64 * 4) + H * (Is + Is // 64 * 4)
+    router = (E + 1) * (H + H // 64 * 4)
+    assert total >= E * expert + shared + router + 4 * H
+    assert total - (E * expert + shared + router + 4 * H) < 8 * 256
+
+
+def test_argument_errors():
+    L = moe.lib()
+    d = moe.desc_from_shape(synth.TINY)
+    n = C.c_size_t()
+    assert L.moe_pack_size(None, C.byref(n)) == 1
+    bad = moe.make_desc(256, 128, 16, 2, 5, router_bits=0, has_shared=False)
+    assert L.moe_pack_size(C.byref(bad), C.byref(n)) == 2
+    bad = moe.make_desc(256, 128, 16, 17, 4, router_bits=0, has_shared=False)   # k > E
+    assert L.moe_pack_size(C.byref(bad), C.byref(n)) == 2
+    bad = moe.make_desc(320, 128, 16, 2, 4, router_bits=0, has_shared=False)   # H not 256/multiple of 512
+    assert L.moe_pack_size(C.byref(bad), C.byref(n)) == 2
+    bad = moe.make_desc(256, 512, 16, 2, 4, router_bits=0, has_shared=False)   # I > H
+    assert L.moe_pack_size(C.byref(bad), C.byref(n)) == 2
+    assert L.moe_workspace_size(C.byref(d), 0, C.byref(n)) == 1
+    h = C.c_void_p()
+    src = _lib.SrcLayer()
+    assert L.moe_pack_weights(C.byref(d), C.byref(src), None, 0, C.byref(h), None) == 1
+    assert L.moe_pack_weights(C.byref(d), C.byref(src), C.c_void_p(256), 16, C.byref(h), None) == 3
+    assert L.moe_decode_layer(None, None, 1, None, None, None, 0, None) == 1
+    assert L.moe_router_topk(None, None, 1, None, None, None, 0, None) == 1
+    assert L.moe_stack_create(None, 0, C.byref(h)) == 1
+    L.moe_layer_destroy(None)
+    L.moe_stack_destroy(None)
+
+
+def test_workspace_sizes_grow_with_rows():
+    d = moe.desc_from_shape(synth.A35B)
+    assert moe.workspace_size(d, 1) < moe.workspace_size(d, 8) < moe.workspace_size(d, 32)

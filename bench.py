@@ -1,0 +1,392 @@
+#!/usr/bin/env python3
+"""Benchmark of the quantized MoE decode layer on GB300.
+
+Workload (one step): one forward of the 40-layer stack of 35B-A3B-shaped MoE
+FFN layers (H=2048, E=256, top-8, I=512, 6-bit routed experts, 8-bit shared
+expert and router, group 64) at M=1 token row, each layer with its own
+weights (40 distinct layer sets, 26.3 GB resident in HBM, so L2 cannot hold
+the working set).  The stack runs as one persistent kernel launch.
+
+Metric: achieved HBM GB/s on the unique bytes a step touches (each selected
+expert once, shared expert, router, gamma, activations) and microseconds per
+layer.  M=4 (1 token + 3 correlated draft rows) is reported alongside.
+
+--impl reference times the fp64 CPU oracle on the host cores on a bounded
+sample of the same workload (the reference arm of this tier).
+"""
+from __future__ import annotations
+
+import argparse
+import hashlib
+import json
+import os
+import subprocess
+import sys
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+METRIC = "MoE layer µs/token & achieved HBM GB/s vs 8 TB/s (35B-A3B shape, M=1 and M=4)"
+LAYERS = 40
+CORR_M4 = 0.6
+
+
+def parse():
+    p = argparse.ArgumentParser()
+    p.add_argument("--gpus", type=int, default=1)
+    p.add_argument("--steps", type=int, default=400)
+    p.add_argument("--warmup", type=int, default=10)
+    p.add_argument("--impl", default="ours", choices=["ours", "reference"])
+    p.add_argument("--layers", type=int, default=LAYERS)
+    p.add_argument("--no-m4", action="store_true")
+    p.add_argument("--cpu-seconds", type=float, default=12.0)
+    return p.parse_args()
+
+
+def dist_env():
+    ws = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    return ws, rank, local
+
+
+def unique_bytes(shape, U: int, M: int) -> int:
+    """Algorithmic bytes of one layer call: U selected experts once each, the
+    shared expert, all router rows (+ shared-gate row), gamma, x in, out."""
+    import quantized_moe_decode_layer_gb300 as moe  # noqa: F401
+    H, I, E, Is = shape.H, shape.I, shape.E, shape.I_shared
+    rb, sb, qb = shape.routed_bits, shape.shared_bits, shape.router_bits
+
+    def row(K, b):
+        return K * b // 8 + K // 64 * 4 if b else K * 4
+
+    expert = 2 * I * row(H, rb) + H * row(I, rb)
+    shared = (2 * Is * row(H, sb) + H * row(Is, sb)) if shape.has_shared else 0
+    router = (E + (1 if shape.has_shared else 0)) * row(H, qb)
+    return U * expert + shared + router + 2 * H + 2 * M * H * 2
+
+
+def source_hash() -> str:
+    h = hashlib.sha256()
+    csrc = os.path.join(ROOT, "quantized_moe_decode_layer_gb300", "csrc")
+    for f in sorted(os.listdir(csrc)):
+        h.update(open(os.path.join(csrc, f), "rb").read())
+    return h.hexdigest()[:16]
+
+
+def load_peaks():
+    try:
+        return json.load(open(os.path.join(ROOT, "MEASURED_PEAKS.json"))), "measured"
+    except Exception:
+        return {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0}, "fallback"
+
+
+def load_traffic():
+    """Per-launch DRAM bytes from the committed ncu summary, if it was taken
+    on the current kernel source."""
+    try:
+        t = json.load(open(os.path.join(ROOT, "profiles", "traffic.json")))
+        if t.get("source_hash") == source_hash():
+            return t
+    except Exception:
+        pass
+    return None
+
+
+class Clocks:
+    """nvidia-smi samples during the timed region."""
+
+    def __init__(self, index: int):
+        self.index = index
+        self.proc = None
+        self.path = f"/tmp/moe_clocks_{os.getpid()}.csv"
+
+    def __enter__(self):
+        q = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+             "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+             "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+        try:
+            self.f = open(self.path, "w")
+            self.proc = subprocess.Popen(["nvidia-smi", f"--id={self.index}", f"--query-gpu={q}",
+                                          "--format=csv,noheader,nounits", "-lms", "100"],
+                                         stdout=self.f, stderr=subprocess.DEVNULL)
+        except Exception:
+            self.proc = None
+        time.sleep(0.3)
+        return self
+
+    def __exit__(self, *a):
+        if self.proc:
+            self.proc.terminate()
+            try:
+                self.proc.wait(timeout=5)
+            except Exception:
+                self.proc.kill()
+            self.f.close()
+
+    def summary(self):
+        rows = []
+        try:
+            for line in open(self.path):
+                parts = [p.strip() for p in line.split(",")]
+                if len(parts) >= 9 and parts[1].isdigit():
+                    rows.append(parts)
+        except Exception:
+            pass
+        if not rows:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["unavailable"], "samples": 0}
+        mhz = sorted(int(r[1]) for r in rows)
+        reasons = set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        for r in rows:
+            for n, v in zip(names, r[5:9]):
+                if v.lower().startswith("active"):
+                    reasons.add(n)
+        return {"sm_mhz": mhz[len(mhz) // 2], "sm_max_mhz": int(rows[0][2]), "reasons": sorted(reasons),
+                "samples": len(rows)}
+
+
+def build_stack(shape, n_layers, dev, seed0=1000):
+    import torch
+    import synth
+    import quantized_moe_decode_layer_gb300 as moe
+    desc = moe.desc_from_shape(shape)
+    layers = []
+    for l in range(n_layers):
+        L = synth.make_layer(shape, seed0 + l, device=dev)
+        layers.append(moe.Layer(desc, moe.layer_src_from_synth(L)))
+        del L
+    torch.cuda.synchronize()
+    torch.cuda.empty_cache()
+    return desc, layers
+
+
+def measure_U(layers, x, ws):
+    """Distinct experts per layer along the stack for input x (untimed)."""
+    import torch
+    import quantized_moe_decode_layer_gb300 as moe
+    Us = []
+    h = x
+    for lyr in layers:
+        idx, _ = moe.router_topk(lyr, h, ws)
+        Us.append(int(torch.unique(idx).numel()))
+        h = moe.decode_layer(lyr, h, ws)
+    return Us
+
+
+def time_stack(st, x, ws, steps, warmup, stream):
+    import torch
+    import quantized_moe_decode_layer_gb300 as moe
+    out = torch.empty_like(x)
+    for _ in range(warmup):
+        st.forward(x, ws, out=out, stream=stream)
+    torch.cuda.synchronize()
+    ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(steps)]
+    moe.launch_count(reset=True)
+    t0 = torch.cuda.Event(enable_timing=True)
+    t1 = torch.cuda.Event(enable_timing=True)
+    t0.record(stream)
+    for i in range(steps):
+        ev[i][0].record(stream)
+        st.forward(x, ws, out=out, stream=stream)
+        ev[i][1].record(stream)
+    t1.record(stream)
+    torch.cuda.synchronize()
+    launches = moe.launch_count(reset=True)
+    per = sorted(a.elapsed_time(b) for a, b in ev)
+    total_ms = t0.elapsed_time(t1)
+    assert ws.status(stream) == 0
+    return total_ms, per, launches
+
+
+def run_ours(args):
+    import numpy as np
+    import torch
+    import torch.distributed as td
+    import synth
+    import quantized_moe_decode_layer_gb300 as moe
+
+    world, rank, local = dist_env()
+    torch.cuda.set_device(local)
+    dev = torch.device("cuda", local)
+    if world > 1:
+        td.init_process_group("nccl", device_id=dev)
+    shape = synth.A35B
+    desc, layers = build_stack(shape, args.layers, dev)
+    st = moe.Stack(layers)
+    stream = torch.cuda.current_stream()
+
+    def barrier():
+        if world > 1:
+            td.barrier()
+        torch.cuda.synchronize()
+
+    # M = 1 (headline)
+    x1 = synth.make_rows(shape, 5, 1, gamma=None).to(dev)
+    ws = moe.Workspace(desc, 4)
+    U1 = measure_U(layers, x1, ws)
+    bytes1 = sum(unique_bytes(shape, u, 1) for u in U1)
+    barrier()
+    with Clocks(local) as clk:
+        barrier()
+        total_ms, per, launches = time_stack(st, x1, ws, args.steps, args.warmup, stream)
+        barrier()
+    clocks = clk.summary()
+    t = torch.tensor([total_ms], device=dev)
+    if world > 1:
+        td.all_reduce(t, op=td.ReduceOp.MAX)
+    total_ms = float(t.item())
+    ms_step = total_ms / args.steps
+    value = world * bytes1 * args.steps / (total_ms * 1e-3) / 1e9
+    us_layer = ms_step * 1e3 / args.layers
+
+    # roofline of the dominant (only) kernel: one launch per step
+    peaks, peak_kind = load_peaks()
+    med_ms = per[len(per) // 2]
+    mean_ms = sum(per) / len(per)
+    achieved = bytes1 / (mean_ms * 1e-3) / 1e9
+    traffic = load_traffic()
+    roof = {"bound": "hbm", "achieved": round(achieved, 1), "peak": peaks["hbm_gbs"], "unit": "GB/s",
+            "frac": round(achieved / peaks["hbm_gbs"], 4), "peak_kind": peak_kind,
+            "traffic": (traffic["bytes_per_launch"] if traffic else None),
+            "algorithmic_bytes": bytes1, "launch_ms_mean": round(mean_ms, 5), "launch_ms_median": round(med_ms, 5)}
+
+    # end to end through the C ABI with host buffers (copies inside the call)
+    xh = x1.cpu().pin_memory()
+    oh = torch.empty_like(xh).pin_memory()
+    for _ in range(args.warmup):
+        st.forward_host(xh, oh, ws)
+    e_steps = max(10, args.steps // 4)
+    barrier()
+    t0 = time.perf_counter()
+    for _ in range(e_steps):
+        st.forward_host(xh, oh, ws)
+    e_s = time.perf_counter() - t0
+    te = torch.tensor([e_s], device=dev)
+    if world > 1:
+        td.all_reduce(te, op=td.ReduceOp.MAX)
+    e_s = float(te.item())
+    e2e = {"value": round(world * bytes1 * e_steps / e_s / 1e9, 1), "unit": "GB/s",
+           "h2d_bytes_per_step": int(x1.numel() * 2), "d2h_bytes_per_step": int(x1.numel() * 2),
+           "us_per_layer": round(e_s / e_steps * 1e6 / args.layers, 3)}
+
+    # M = 4: one token + 3 correlated draft rows
+    m4 = None
+    if not args.no_m4:
+        x4 = synth.make_rows(shape, 6, 4, correlation=CORR_M4).to(dev)
+        U4 = measure_U(layers, x4, ws)
+        bytes4 = sum(unique_bytes(shape, u, 4) for u in U4)
+        s4 = max(20, args.steps // 2)
+        tm4, per4, _ = time_stack(st, x4, ws, s4, args.warmup, stream)
+        mean4 = sum(per4) / len(per4)
+        m4 = {"us_per_layer": round(tm4 / s4 * 1e3 / args.layers, 3),
+              "gbs": round(bytes4 / (mean4 * 1e-3) / 1e9, 1),
+              "frac": round(bytes4 / (mean4 * 1e-3) / 1e9 / peaks["hbm_gbs"], 4),
+              "mean_U": round(float(np.mean(U4)), 2), "bytes_per_step": bytes4}
+
+    # single-layer calls (one launch per layer) over the 40 rotating layer sets
+    single = None
+    if rank == 0:
+        out = torch.empty_like(x1)
+        for lyr in layers[:4]:
+            moe.decode_layer(lyr, x1, ws, out=out)
+        torch.cuda.synchronize()
+        reps = 5
+        a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        a.record()
+        for _ in range(reps):
+            for lyr in layers:
+                moe.decode_layer(lyr, x1, ws, out=out)
+        b.record()
+        torch.cuda.synchronize()
+        single = round(a.elapsed_time(b) * 1e3 / (reps * len(layers)), 3)
+
+    cpu = cpu_baseline(args, shape, dev) if rank == 0 else None
+    if rank == 0:
+        line = {
+            "metric": METRIC, "value": round(value, 1), "unit": "GB/s", "n_gpus": world, "steps": args.steps,
+            "warmup": args.warmup, "ms_per_step": round(ms_step, 5), "higher_is_better": True,
+            "scaling": "weak", "vs_baseline": None, "dtype": "f32", "data": "synthetic",
+            "config": {"workload": f"35B-A3B-shaped MoE FFN stack, {args.layers} distinct layer sets, M=1",
+                       "H": 2048, "E": 256, "k": 8, "I": 512, "I_shared": 512, "routed_bits": 6,
+                       "shared_bits": 8, "router_bits": 8, "group": 64, "M": 1, "layers": args.layers,
+                       "resident_weight_GB": round(sum(l.nbytes for l in layers) / 1e9, 2),
+                       "l2": "weights rotate over 40 layer sets (26 GB) > L2; no flush",
+                       "parallelism": f"replicas x{world}"},
+            "us_per_layer": round(us_layer, 3), "fraction_of_8TBs": round(value / world / 8000.0, 4),
+            "single_layer_call_us": single, "m4": m4, "roofline": roof, "e2e": e2e,
+            "gpu_launches": launches, "clocks": clocks, "cpu_baseline": cpu,
+        }
+        print(json.dumps(line), flush=True)
+    if world > 1:
+        td.barrier()
+        td.destroy_process_group()
+
+
+def cpu_baseline(args, shape, dev=None):
+    """The oracle, as it stands, on a bounded sample of the workload: whole
+    layers of the stack at M=1 (fp64, one host core)."""
+    import numpy as np
+    import torch
+    import oracle
+    import synth
+    t_budget = args.cpu_seconds
+    n_done, bytes_done, elapsed = 0, 0, 0.0
+    x = synth.bf16_bits(synth.make_rows(shape, 5, 1)).numpy().view(np.uint16)
+    l = 0
+    while elapsed < t_budget and l < args.layers:
+        L = synth.make_layer(shape, 1000 + l, device=dev if dev is not None else "cpu")
+        lay = oracle.Layer(L)
+        r = lay.route(x)
+        for e in set(int(v) for v in r["idx"].ravel()):
+            lay.expert(e)
+        del L
+        if dev is not None:
+            torch.cuda.empty_cache()
+        t0 = time.perf_counter()
+        res = lay.forward(x, normed=False)
+        elapsed += time.perf_counter() - t0
+        bytes_done += unique_bytes(shape, len(set(res["idx"].ravel().tolist())), 1)
+        n_done += 1
+        x = res["out"]
+        l += 1
+    return {"value": round(bytes_done / elapsed / 1e9, 6), "unit": "GB/s", "cores": 1, "kind": "oracle",
+            "sample": f"{n_done} chained layers of the a35b stack at M=1 ({elapsed:.1f} s of oracle time)",
+            "us_per_layer": round(elapsed / n_done * 1e6, 1)}
+
+
+def run_reference(args):
+    world, rank, local = dist_env()
+    if rank != 0:
+        return
+    import synth
+    import torch
+    dev = None
+    if torch.cuda.is_available():
+        torch.cuda.set_device(local)
+        dev = torch.device("cuda", local)
+    shape = synth.A35B
+    for _ in range(max(0, min(args.warmup, 1))):
+        pass
+    cb = cpu_baseline(args, shape, dev)
+    line = {"impl": "reference", "metric": METRIC, "value": cb["value"], "unit": "GB/s", "n_gpus": world,
+            "steps": args.steps, "warmup": args.warmup, "ms_per_step": round(cb["us_per_layer"] * args.layers / 1e3, 3),
+            "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
+            "config": {"workload": f"35B-A3B-shaped MoE FFN stack, {args.layers} distinct layer sets, M=1",
+                       "M": 1, "layers": args.layers},
+            "cpu_baseline": cb,
+            "e2e": {"value": cb["value"], "unit": "GB/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
+    print(json.dumps(line), flush=True)
+
+
+def main():
+    args = parse()
+    if args.impl == "reference":
+        run_reference(args)
+    else:
+        run_ours(args)
+
+
+if __name__ == "__main__":
+    main()

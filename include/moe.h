@@ -200,6 +200,14 @@ int moe_stream_status(void *ws_dev, size_t ws_bytes, moe_stream_t stream);
  * out returns MOE_ERR_TIMEOUT instead of hanging. */
 int moe_debug_set(int skip_cta, long long timeout_ns);
 
+/* Diagnostic hook: while set, every decode launch records globaltimer
+ * stamps (ns) into trace_dev: [CTA][layer][24] as uint64 for the first
+ * min(layers, 64) layers of a launch, followed by a per-warp timeline of two
+ * CTAs, [2][64][16][16]; bytes must cover (SMs * 64 * 24 + 2 * 64 * 256) * 8.
+ * NULL turns it off.  The stamps show where the time of
+ * each layer goes (per phase, per CTA). */
+int moe_debug_trace(void *trace_dev, size_t bytes);
+
 /* Human-readable name of a status code (static string). */
 const char *moe_status_str(int status);
 

@@ -14,6 +14,7 @@ namespace {
 thread_local int t_last_cuda_error = 0;
 thread_local long long t_launches = 0;
 int g_skip_cta = -1;
+unsigned long long *g_trace = nullptr;
 long long g_timeout_ns = 2000000000LL;
 
 bool width_ok(int K)
@@ -48,12 +49,13 @@ int rows_per_launch(int H)
 
 bool make_geo(const moe_layer_desc &d, Geo &g)
 {
-    if (d.H < 256 || !width_ok(d.H) || !width_ok(d.I) || d.I > d.H) return false;
+    if (d.H < 256 || !width_ok(d.H) || !width_ok(d.I) || d.I > d.H || d.I > 1024) return false;
     if (d.E < 1 || d.E > kMaxE || d.k < 1 || d.k > d.E || d.k > kMaxK) return false;
     if (!bits_ok(d.routed_bits)) return false;
     if (!(d.router_bits == 0 || bits_ok(d.router_bits))) return false;
     if (d.has_shared != 0 && d.has_shared != 1) return false;
-    if (d.has_shared && (!bits_ok(d.shared_bits) || !width_ok(d.I_shared) || d.I_shared > d.H)) return false;
+    if (d.has_shared && (!bits_ok(d.shared_bits) || !width_ok(d.I_shared) || d.I_shared > d.H || d.I_shared > 1024))
+        return false;
     if (!(d.eps > 0.0f)) return false;
     memset(&g, 0, sizeof g);
     g.H = d.H; g.I = d.I; g.E = d.E; g.k = d.k;
@@ -113,6 +115,7 @@ int prepare(const moe_layer *layer, int M, void *ws, size_t ws_bytes, KParams &k
     kp.ws = reinterpret_cast<uint8_t *>(ws);
     kp.timeout_ns = g_timeout_ns;
     kp.skip_cta = g_skip_cta;
+    kp.trace = g_trace;
     return MOE_OK;
 }
 
@@ -338,6 +341,15 @@ int moe_debug_set(int skip_cta, long long timeout_ns)
 {
     g_skip_cta = skip_cta;
     g_timeout_ns = timeout_ns > 0 ? timeout_ns : 2000000000LL;
+    return MOE_OK;
+}
+
+int moe_debug_trace(void *trace_dev, size_t bytes)
+{
+    const int sms = device_sms();
+    if (trace_dev && (sms <= 0 || bytes < ((size_t)sms * kMaxLayers * kTraceEvents + 2 * kMaxLayers * 16 * 16) * 8))
+        return MOE_ERR_BUFFER_TOO_SMALL;
+    g_trace = static_cast<unsigned long long *>(trace_dev);
     return MOE_OK;
 }
 

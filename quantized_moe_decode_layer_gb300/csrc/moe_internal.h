@@ -13,14 +13,16 @@ namespace moe {
 
 constexpr int kGroup = 64;          // affine group along the contraction axis
 constexpr int kSub = 16;            // codes per sub-group (one lane step)
-constexpr int kConsumerWarps = 8;   // compute warps per CTA
+constexpr int kConsumerWarps = 15;  // compute warps per CTA (16 warps: 128 registers per thread)
 constexpr int kThreads = (kConsumerWarps + 1) * 32;  // + one TMA producer warp
+constexpr int kProducerLanes = 5;   // lanes of the producer warp issuing bulk copies
 constexpr int kMaxRows = 8;         // token rows per launch (larger M is chunked)
 constexpr int kMaxLayers = 64;      // layers per persistent launch
 constexpr int kMaxStages = 64;      // ring stages (mbarrier pairs)
 constexpr int kMaxE = 512;
 constexpr int kMaxK = 32;
-constexpr int kCtrlBytes = 512;     // control block at the start of the workspace
+constexpr int kCtrlBytes = 2048;    // control block at the start of the workspace
+constexpr int kFlagsOffset = 512;   // per-slot activation-ready counters (uint32 each) inside it
 constexpr int kSmemMax = 232448;    // dynamic shared memory per CTA on sm_100-class parts
 
 // Status word bits (workspace control block).
@@ -73,15 +75,16 @@ struct WsLayout {
 };
 
 struct Ctrl {                // first kCtrlBytes of the workspace
-    unsigned count;          // grid barrier arrivals
+    unsigned count;          // grid-barrier arrivals since the launch began (reset at its end)
     unsigned pad0[31];
-    unsigned gen;            // grid barrier generation (own 128-byte line)
+    unsigned exit;           // CTAs finished with their barriers (own 128-byte line)
     unsigned pad1[31];
     int status;              // kStatus* bits
     int where;               // debug: which wait gave up
     int pad2[62];
 };
-static_assert(sizeof(Ctrl) <= kCtrlBytes, "control block");
+static_assert(sizeof(Ctrl) <= kFlagsOffset, "control block");
+static_assert(kFlagsOffset + 4 * kMaxRows * kMaxK <= kCtrlBytes, "activation-ready counters");
 
 // Launch plan of the persistent kernel.
 struct Plan {
@@ -112,7 +115,10 @@ struct KParams {
     WsLayout ws_l;
     long long timeout_ns;
     int skip_cta;
+    unsigned long long *trace;   // optional per-CTA phase timestamps (ns), NULL = off
 };
+
+constexpr int kTraceEvents = 24; // events recorded per (CTA, layer)
 
 bool make_geo(const moe_layer_desc &d, Geo &g);
 void make_ws_layout(const Geo &g, int max_M, WsLayout &w);

@@ -47,7 +47,26 @@ __host__ __device__ __forceinline__ float code_at(uint32_t v)
     return u2f((v & kMask) | kExp) - u2f(kExp);
 }
 
+// Raw form: the float 2^(23-P) + q (no subtraction yet) and its offset
+// 2^(23-P); packed two-lane FADD then removes the offsets of a pair at once.
+template <int BITS, int P>
+__host__ __device__ __forceinline__ float code_raw(uint32_t v)
+{
+    static_assert(P + BITS <= 23, "code must sit inside the mantissa");
+    constexpr uint32_t kMask = ((1u << BITS) - 1u) << P;
+    constexpr uint32_t kExp = (uint32_t)(150 - P) << 23;
+    return u2f((v & kMask) | kExp);
+}
+
+template <int P>
+__host__ __device__ __forceinline__ float code_off()
+{
+    return u2f((uint32_t)(150 - P) << 23);
+}
+
 // Codes 4t .. 4t+3 of a 16-code sub-group held in w[] (BITS/2 words).
+// get4 gives exact floats; raw4 gives code_raw values f and offsets o with
+// f - o the codes.
 template <int BITS>
 struct Unpack;
 
@@ -71,6 +90,23 @@ struct Unpack<4> {
             q[3] = code_at<4, 16>(s);
         }
     }
+    template <int T>
+    __host__ __device__ __forceinline__ static void raw4(const uint32_t *w, float *f, float *o)
+    {
+        const uint32_t v = w[T >> 1];
+        if ((T & 1) == 0) {
+            f[0] = code_raw<4, 0>(v); o[0] = code_off<0>();
+            f[1] = code_raw<4, 4>(v); o[1] = code_off<4>();
+            f[2] = code_raw<4, 8>(v); o[2] = code_off<8>();
+            f[3] = code_raw<4, 12>(v); o[3] = code_off<12>();
+        } else {
+            const uint32_t s = v >> 12;
+            f[0] = code_raw<4, 16>(v); o[0] = code_off<16>();
+            f[1] = code_raw<4, 8>(s); o[1] = code_off<8>();
+            f[2] = code_raw<4, 12>(s); o[2] = code_off<12>();
+            f[3] = code_raw<4, 16>(s); o[3] = code_off<16>();
+        }
+    }
 };
 
 template <>
@@ -85,6 +121,16 @@ struct Unpack<8> {
         q[1] = code_at<8, 8>(v);
         q[2] = code_at<8, 0>(s);
         q[3] = code_at<8, 8>(s);
+    }
+    template <int T>
+    __host__ __device__ __forceinline__ static void raw4(const uint32_t *w, float *f, float *o)
+    {
+        const uint32_t v = w[T];
+        const uint32_t s = v >> 16;
+        f[0] = code_raw<8, 0>(v); o[0] = code_off<0>();
+        f[1] = code_raw<8, 8>(v); o[1] = code_off<8>();
+        f[2] = code_raw<8, 0>(s); o[2] = code_off<0>();
+        f[3] = code_raw<8, 8>(s); o[3] = code_off<8>();
     }
 };
 
@@ -123,6 +169,35 @@ struct Unpack<6> {
             q[3] = code_at<6, 14>(s2);
         }
     }
+    template <int T>
+    __host__ __device__ __forceinline__ static void raw4(const uint32_t *w, float *f, float *o)
+    {
+        if (T == 0) {
+            const uint32_t s0 = w[0] >> 12;
+            f[0] = code_raw<6, 0>(w[0]); o[0] = code_off<0>();
+            f[1] = code_raw<6, 6>(w[0]); o[1] = code_off<6>();
+            f[2] = code_raw<6, 12>(w[0]); o[2] = code_off<12>();
+            f[3] = code_raw<6, 6>(s0); o[3] = code_off<6>();
+        } else if (T == 1) {
+            const uint32_t s0 = w[0] >> 12;
+            f[0] = code_raw<6, 12>(s0); o[0] = code_off<12>();
+            f[1] = code_raw<6, 0>(funnel_r(w[0], w[1], 30)); o[1] = code_off<0>();
+            f[2] = code_raw<6, 4>(w[1]); o[2] = code_off<4>();
+            f[3] = code_raw<6, 10>(w[1]); o[3] = code_off<10>();
+        } else if (T == 2) {
+            const uint32_t s1 = w[1] >> 12;
+            f[0] = code_raw<6, 16>(w[1]); o[0] = code_off<16>();
+            f[1] = code_raw<6, 10>(s1); o[1] = code_off<10>();
+            f[2] = code_raw<6, 0>(funnel_r(w[1], w[2], 28)); o[2] = code_off<0>();
+            f[3] = code_raw<6, 2>(w[2]); o[3] = code_off<2>();
+        } else {
+            const uint32_t s2 = w[2] >> 12;
+            f[0] = code_raw<6, 8>(w[2]); o[0] = code_off<8>();
+            f[1] = code_raw<6, 14>(w[2]); o[1] = code_off<14>();
+            f[2] = code_raw<6, 8>(s2); o[2] = code_off<8>();
+            f[3] = code_raw<6, 14>(s2); o[3] = code_off<14>();
+        }
+    }
 };
 
 // Host check of the tables above against a plain bit-by-bit extraction.
@@ -143,7 +218,16 @@ inline int unpack_selftest_host()
             } else {
                 Unpack<8>::get4<0>(w, q); Unpack<8>::get4<1>(w, q + 4); Unpack<8>::get4<2>(w, q + 8); Unpack<8>::get4<3>(w, q + 12);
             }
+            float fr[16], of[16];
+            if (bits == 4) {
+                Unpack<4>::raw4<0>(w, fr, of); Unpack<4>::raw4<1>(w, fr + 4, of + 4); Unpack<4>::raw4<2>(w, fr + 8, of + 8); Unpack<4>::raw4<3>(w, fr + 12, of + 12);
+            } else if (bits == 6) {
+                Unpack<6>::raw4<0>(w, fr, of); Unpack<6>::raw4<1>(w, fr + 4, of + 4); Unpack<6>::raw4<2>(w, fr + 8, of + 8); Unpack<6>::raw4<3>(w, fr + 12, of + 12);
+            } else {
+                Unpack<8>::raw4<0>(w, fr, of); Unpack<8>::raw4<1>(w, fr + 4, of + 4); Unpack<8>::raw4<2>(w, fr + 8, of + 8); Unpack<8>::raw4<3>(w, fr + 12, of + 12);
+            }
             for (int i = 0; i < 16; ++i) {
+                if (fr[i] - of[i] != q[i]) ++bad;
                 uint32_t v = 0;
                 for (int t = 0; t < bits; ++t) {
                     const int pos = i * bits + t;

@@ -190,6 +190,33 @@ int moe_stack_forward_host(moe_stack *stack, const uint16_t *x_host, int M, uint
 /* Frees the stack handle (not the layers).  NULL is a no-op. */
 void moe_stack_destroy(moe_stack *stack);
 
+/* moe_decode_layer without a caller-provided workspace, for callers that
+ * cannot allocate device memory at the point of the call: code enqueued
+ * while a stream is being captured into a CUDA graph (cudaMalloc is not
+ * allowed there), plug-ins that run inside another framework's memory pool
+ * and may not grow it, and latency-critical paths that must not take an
+ * allocation's implicit synchronisation.  The pages describing the method
+ * have no counterpart of this call; it exists for such callers only.
+ *
+ * The scratch lives in a fixed array of MOE_NOALLOC_SCRATCH_BYTES of device
+ * memory inside the library (every GPU that loads the library holds it
+ * until the process exits).  Layers and row counts whose moe_workspace_size
+ * exceeds it are rejected with MOE_ERR_BUFFER_TOO_SMALL before anything is
+ * enqueued.  Inputs and outputs are as for moe_decode_layer.
+ *
+ * - The first call on a device looks up the array's device address on that
+ *   device (once); make that first call outside any stream capture.
+ * - Each call clears the array's control block on `stream` before its
+ *   kernels, so an earlier failed call does not affect it.
+ * - Every call on a device shares the one array: calls that can overlap on
+ *   the GPU (different streams without ordering between them) race and give
+ *   wrong results.  Order them on one stream.
+ * - No device memory is allocated or freed by this call.
+ * Errors: as moe_decode_layer, plus BUFFER_TOO_SMALL (scratch too small). */
+#define MOE_NOALLOC_SCRATCH_BYTES (4u << 20)
+int moe_decode_layer_noalloc(const moe_layer *layer, const uint16_t *x_dev, int M, uint16_t *out_dev,
+                             uint16_t *out_normed_dev, moe_stream_t stream);
+
 /* Synchronises `stream` and returns MOE_OK, MOE_ERR_TIMEOUT or MOE_ERR_DEVICE
  * from the workspace status word (or MOE_ERR_CUDA). */
 int moe_stream_status(void *ws_dev, size_t ws_bytes, moe_stream_t stream);

@@ -337,6 +337,53 @@ int moe_stream_status(void *ws_dev, size_t ws_bytes, moe_stream_t stream)
     return check_status_word(ws_dev);
 }
 
+}  // extern "C"
+
+namespace {
+
+// Scratch of moe_decode_layer_noalloc: one fixed array per device, shared by
+// every call on that device.  Its host-side name is only a handle for the
+// runtime; the kernels get the device address looked up below.
+static __device__ __align__(256) uint8_t g_noalloc_scratch[MOE_NOALLOC_SCRATCH_BYTES];
+
+void *g_noalloc_ptr[64];
+
+// Device address of the array on the current device, looked up once per device.
+int noalloc_scratch(void **out)
+{
+    int dev = 0;
+    cudaError_t e = cudaGetDevice(&dev);
+    if (e != cudaSuccess || dev < 0 || dev >= 64) { note_cuda_error((int)e); return MOE_ERR_CUDA; }
+    if (!g_noalloc_ptr[dev]) {
+        void *p = nullptr;
+        e = cudaGetSymbolAddress(&p, g_noalloc_scratch);
+        if (e != cudaSuccess || !p) { note_cuda_error((int)e); return MOE_ERR_CUDA; }
+        g_noalloc_ptr[dev] = p;
+    }
+    *out = g_noalloc_ptr[dev];
+    return MOE_OK;
+}
+
+}  // namespace
+
+extern "C" {
+
+int moe_decode_layer_noalloc(const moe_layer *layer, const uint16_t *x_dev, int M, uint16_t *out_dev,
+                             uint16_t *out_normed_dev, moe_stream_t stream)
+{
+    if (!layer || M < 1) return MOE_ERR_INVALID_ARG;
+    WsLayout w;
+    make_ws_layout(layer->geo, M, w);
+    if (w.total > (size_t)MOE_NOALLOC_SCRATCH_BYTES) return MOE_ERR_BUFFER_TOO_SMALL;
+    void *ws = nullptr;
+    int rc = noalloc_scratch(&ws);
+    if (rc) return rc;
+    // the control block (barrier counters, status, ready counters) starts at zero
+    cudaError_t e = cudaMemsetAsync(ws, 0, kCtrlBytes, reinterpret_cast<cudaStream_t>(stream));
+    if (e != cudaSuccess) { note_cuda_error((int)e); return MOE_ERR_CUDA; }
+    return moe_decode_layer(layer, x_dev, M, out_dev, out_normed_dev, ws, (size_t)MOE_NOALLOC_SCRATCH_BYTES, stream);
+}
+
 int moe_debug_set(int skip_cta, long long timeout_ns)
 {
     g_skip_cta = skip_cta;

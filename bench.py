@@ -52,19 +52,9 @@ def dist_env():
 
 
 def unique_bytes(shape, U: int, M: int) -> int:
-    """Algorithmic bytes of one layer call: U selected experts once each, the
-    shared expert, all router rows (+ shared-gate row), gamma, x in, out."""
-    import quantized_moe_decode_layer_gb300 as moe  # noqa: F401
-    H, I, E, Is = shape.H, shape.I, shape.E, shape.I_shared
-    rb, sb, qb = shape.routed_bits, shape.shared_bits, shape.router_bits
-
-    def row(K, b):
-        return K * b // 8 + K // 64 * 4 if b else K * 4
-
-    expert = 2 * I * row(H, rb) + H * row(I, rb)
-    shared = (2 * Is * row(H, sb) + H * row(Is, sb)) if shape.has_shared else 0
-    router = (E + (1 if shape.has_shared else 0)) * row(H, qb)
-    return U * expert + shared + router + 2 * H + 2 * M * H * 2
+    """Algorithmic bytes of one layer call (see accounting.unique_bytes)."""
+    from quantized_moe_decode_layer_gb300.accounting import unique_bytes as ub
+    return ub(shape, U, M)
 
 
 def source_hash() -> str:

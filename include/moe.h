@@ -221,11 +221,12 @@ int moe_decode_layer_noalloc(const moe_layer *layer, const uint16_t *x_dev, int 
  * from the workspace status word (or MOE_ERR_CUDA). */
 int moe_stream_status(void *ws_dev, size_t ws_bytes, moe_stream_t stream);
 
-/* Test hook: the next decode calls make CTA `cta` skip its arrival at the
- * first grid barrier (-1 = off) and give every device wait `timeout_ns`
- * (<= 0 restores the default of 2 s).  Used to check that a wait that runs
- * out returns MOE_ERR_TIMEOUT instead of hanging. */
-int moe_debug_set(int skip_cta, long long timeout_ns);
+/* Test hook: the next decode calls leave router logit `skip_row` (an expert
+ * index; -1 = off) of their first layer unpublished, so that every CTA's
+ * wait for it runs out, and give every device wait `timeout_ns` (<= 0
+ * restores the default of 2 s).  Used to check that a wait that runs out
+ * returns MOE_ERR_TIMEOUT instead of hanging. */
+int moe_debug_set(int skip_row, long long timeout_ns);
 
 /* Diagnostic hook: while set, every decode launch records globaltimer
  * stamps (ns) into trace_dev: [CTA][layer][24] as uint64 for the first

@@ -216,8 +216,8 @@ class Stack:
             pass
 
 
-def debug_set(skip_cta: int = -1, timeout_ns: int = 0) -> None:
-    check("moe_debug_set", lib().moe_debug_set(skip_cta, timeout_ns))
+def debug_set(skip_row: int = -1, timeout_ns: int = 0) -> None:
+    check("moe_debug_set", lib().moe_debug_set(skip_row, timeout_ns))
 
 
 def launch_count(reset: bool = False) -> int:

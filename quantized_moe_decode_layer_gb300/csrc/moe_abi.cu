@@ -13,14 +13,17 @@ namespace moe {
 namespace {
 thread_local int t_last_cuda_error = 0;
 thread_local long long t_launches = 0;
-int g_skip_cta = -1;
+int g_skip_row = -1;
 unsigned long long *g_trace = nullptr;
 long long g_timeout_ns = 2000000000LL;
 
+// Contraction widths 64 * 2^j up to 64 * 32 * kMaxGPL: a row splits into
+// whole groups over 1, 2, 4, ..., 32 lanes.
 bool width_ok(int K)
 {
-    if (K <= 0 || K % kGroup) return false;
-    return K == 64 || K == 128 || K == 256 || K % 512 == 0;
+    for (int w = kGroup; w <= kGroup * 32 * kMaxGPL; w *= 2)
+        if (K == w) return true;
+    return false;
 }
 
 bool bits_ok(int b) { return b == 4 || b == 6 || b == 8; }
@@ -92,10 +95,11 @@ void make_ws_layout(const Geo &g, int max_M, WsLayout &w)
     w.max_M = max_M;
     size_t o = kCtrlBytes;
     auto put = [&](size_t bytes) { o = align_up(o, 256); size_t r = o; o += bytes; return r; };
-    w.off_logits = put((size_t)R * g.Er * 4);
-    w.off_act = put((size_t)w.max_slots * R * g.I * 4);
-    w.off_act_s = put((size_t)R * (g.Is ? g.Is : 1) * 4);
-    w.off_ping = put((size_t)2 * R * g.H * 2);
+    // buffers CTAs exchange hold tagged 8-byte words (value | tag << 32)
+    w.off_logits = put((size_t)R * g.Er * 8);
+    w.off_act = put((size_t)w.max_slots * R * g.I * 8);
+    w.off_act_s = put((size_t)R * (g.Is ? g.Is : 1) * 8);
+    w.off_ping = put((size_t)2 * R * (g.H / 2) * 8);
     w.off_stage_in = put((size_t)max_M * g.H * 2);
     w.off_stage_out = put((size_t)max_M * g.H * 2);
     w.total = align_up(o, 256);
@@ -114,7 +118,7 @@ int prepare(const moe_layer *layer, int M, void *ws, size_t ws_bytes, KParams &k
     R = kp.ws_l.maxr;
     kp.ws = reinterpret_cast<uint8_t *>(ws);
     kp.timeout_ns = g_timeout_ns;
-    kp.skip_cta = g_skip_cta;
+    kp.skip_row = g_skip_row;
     kp.trace = g_trace;
     return MOE_OK;
 }
@@ -384,9 +388,9 @@ int moe_decode_layer_noalloc(const moe_layer *layer, const uint16_t *x_dev, int 
     return moe_decode_layer(layer, x_dev, M, out_dev, out_normed_dev, ws, (size_t)MOE_NOALLOC_SCRATCH_BYTES, stream);
 }
 
-int moe_debug_set(int skip_cta, long long timeout_ns)
+int moe_debug_set(int skip_row, long long timeout_ns)
 {
-    g_skip_cta = skip_cta;
+    g_skip_row = skip_row;
     g_timeout_ns = timeout_ns > 0 ? timeout_ns : 2000000000LL;
     return MOE_OK;
 }

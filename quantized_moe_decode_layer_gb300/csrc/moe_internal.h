@@ -21,6 +21,7 @@ constexpr int kMaxLayers = 64;      // layers per persistent launch
 constexpr int kMaxStages = 64;      // ring stages (mbarrier pairs)
 constexpr int kMaxE = 512;
 constexpr int kMaxK = 32;
+constexpr int kMaxGPL = 4;          // 64-groups per lane of a row: K <= 32 * 64 * kMaxGPL
 constexpr int kCtrlBytes = 2048;    // control block at the start of the workspace
 constexpr int kFlagsOffset = 512;   // per-slot activation-ready counters (uint32 each) inside it
 constexpr int kSmemMax = 232448;    // dynamic shared memory per CTA on sm_100-class parts
@@ -94,6 +95,8 @@ struct Plan {
     int maxr;                // rows per launch
     int max_slots;
     int hrows;               // output rows per CTA (upper bound)
+    int pb_bytes;            // prefetch buffer (gamma, router rows, shared units of a layer)
+    int act_pairs;           // (slot, row) activation vectors the staging buffer holds
     int smem_bytes;
 };
 
@@ -114,7 +117,8 @@ struct KParams {
     uint8_t *ws;             // workspace base
     WsLayout ws_l;
     long long timeout_ns;
-    int skip_cta;
+    int skip_row;            // debug: router logit row left unpublished in layer 0 (-1 = none)
+    unsigned epoch;          // tags of this launch: epoch + layer + 1 (set at launch)
     unsigned long long *trace;   // optional per-CTA phase timestamps (ns), NULL = off
 };
 

@@ -1,38 +1,55 @@
 // Persistent decode kernel of the quantized MoE FFN layer (and of a stack of
 // such layers) for sm_103a.
 //
-// One CTA per SM: 16 compute warps and one producer warp.  Eight lanes of the
-// producer warp stream every weight byte the CTA needs through a ring of
-// shared-memory stages with 1-D bulk copies (cp.async.bulk completing on
-// mbarrier transaction counts); several issuing lanes are needed because one
-// thread cannot issue small bulk copies fast enough to fill HBM.  Each stage
-// is consumed by one compute warp, which dequantises in registers and
-// accumulates in fp32.  Per layer:
+// One CTA per SM: 15 compute warps and one producer warp.  The producer
+// streams weights into shared memory with 1-D bulk copies
+// (cp.async.bulk ... mbarrier::complete_tx): five lanes feed a ring of
+// stages holding the routed experts (and the shared expert's down rows), each
+// stage consumed by one compute warp; a sixth lane fills a prefetch buffer
+// with the next layer's RMSNorm weight, router rows and shared-expert gate/up
+// units, which do not depend on routing and are therefore loaded while the
+// current layer still runs.  Per layer:
 //
 //   P0  every CTA: RMSNorm of the M input rows into shared memory
 //       (flash-moe, "Metal Compute Shaders": RMS normalisation)
 //   P1  router rows (plus the shared-expert gate row) and the shared
-//       expert's gate/up units, split over the CTAs          -> grid barrier
+//       expert's gate/up units of this CTA, from the prefetch buffer
+//                                                           -> grid barrier
 //   R   every CTA: softmax + top-k + renormalisation per row and the list of
 //       distinct selected experts with the rows that chose each
 //       (PureDrive model card, "Summary": the full top-8 of 256 is kept)
-//   P1b the shared expert's down rows of this CTA's output slice (weights
-//       prefetched before routing is known)
+//   P1b the shared expert's down rows of this CTA's output slice
 //   P2  gate/up units of the selected experts, each expert streamed once for
 //       all the rows that chose it (model card, "How it works": the verify
-//       pass reads its weights once), SwiGLU                 -> grid barrier
+//       pass reads its weights once), SwiGLU; per-expert release counters
 //   P3  down rows of every selected expert for this CTA's output slice
 //   C   weighted combine + sigmoid-gated shared expert + residual, bf16
 //       (flash-moe: "MoE combine + residual + gate")         -> grid barrier
 //   N   the fused next RMSNorm of the bf16 output (model card: fused
 //       add+RMSNorm), or the next layer's P0.
 //
+// Dequantisation (moe_unpack.cuh).  A lane takes one 64-code group of a
+// weight row.  A masked code read as a float is the subnormal
+// q * 2^(p - 149); the activations sit in shared memory multiplied by
+// 2^100, so a paired FFMA2 of masked codes against them accumulates
+// q * x * 2^(p - 49) as exact fp32 products.  Codes are accumulated per bit
+// position ("class") and each class sum is scaled back once per group: one
+// LOP3 and half an FFMA2 per weight.  With several token rows the codes are
+// first turned into q * 2^-23 by one paired multiply and reused for every
+// row.  The affine terms are factored per group:
+// sum_j (q_j s + b) x_j = s * sum_j q_j x_j + b * sum_j x_j.
+//
 // Determinism: no float atomics; every sum has a fixed order that depends
 // only on the row itself, so row m of an M-row call equals a 1-row call.
 #include <cuda_bf16.h>
 
+#include <unistd.h>
+
+#include <atomic>
 #include <cfloat>
-#include <type_traits>
+#include <chrono>
+#include <climits>
+#include <mutex>
 
 #include "moe_internal.h"
 #include "moe_unpack.cuh"
@@ -42,16 +59,16 @@ namespace {
 
 constexpr int NCW = kConsumerWarps;
 constexpr int NCT = NCW * 32;
-constexpr int NP = kProducerLanes;
-constexpr int kCandCap = 64;
-constexpr int kRedChunks = 8;        // per-row partial sums in the RMSNorm reduction
+constexpr int NP = kProducerLanes;   // lanes issuing ring stages; lane NP fills the prefetch buffer
 constexpr unsigned FULLMASK = 0xffffffffu;
+constexpr float kXScale = 0x1p100f;  // arranged vectors hold x * 2^100
+constexpr float kFmScale = 0x1p-77f; // (q 2^-23) (x 2^100) -> q x
 
 // ------------------------------------------------------------ shared layout
 
 struct SmemLayout {
     int bar, flags, slot_e, slot_mask, slot_rowbase, sigma, eslot, emask, topv, tope, topw;
-    int row_w, row_pair, cand_v, cand_e, red, xs, xsum, ybuf, ysh, target, ring, total;
+    int row_w, row_pair, red, p1v, pair_src, pend, xs, xsum, act, asum, ybuf, ysh, target, pb, ring, total;
 };
 
 __host__ __device__ inline int take(int &o, int bytes, int align)
@@ -62,12 +79,17 @@ __host__ __device__ inline int take(int &o, int bytes, int align)
     return r;
 }
 
+__host__ __device__ inline int imax_of(const Geo &g) { return g.Is > g.I ? g.Is : g.I; }
+
+// Router rows / shared units taken by one CTA at most.
+__host__ __device__ inline int per_cta(int n, int P) { return (n + P - 1) / P; }
+
 __host__ __device__ inline SmemLayout carve(const Geo &g, const Plan &p)
 {
     SmemLayout L;
     int o = 0;
-    const int ms = p.max_slots;
-    L.bar = take(o, (2 * p.NS + 1) * 8, 8);
+    const int ms = p.max_slots, Im = imax_of(g);
+    L.bar = take(o, (2 * p.NS + 3) * 8, 8);
     L.flags = take(o, 16 * 4, 16);
     L.slot_e = take(o, ms * 4, 4);
     L.slot_mask = take(o, ms * 4, 4);
@@ -80,20 +102,22 @@ __host__ __device__ inline SmemLayout carve(const Geo &g, const Plan &p)
     L.topw = take(o, kMaxRows * kMaxK * 4, 4);
     L.row_w = take(o, kMaxRows * kMaxK * 4, 4);
     L.row_pair = take(o, kMaxRows * kMaxK * 4, 4);
-    L.cand_v = take(o, kMaxRows * kCandCap * 4, 4);
-    L.cand_e = take(o, kMaxRows * kCandCap * 4, 4);
-    L.red = take(o, kMaxRows * (kRedChunks + 1) * 4, 4);
+    L.red = take(o, kMaxRows * (NCW + 1) * 4, 4);
+    L.p1v = take(o, 2 * per_cta(g.Is > 0 ? g.Is : 1, p.P) * p.maxr * 4, 4);
+    L.pair_src = take(o, p.act_pairs * 4, 4);
+    L.pend = take(o, NCW * ms * 4, 4);
     L.xs = take(o, p.maxr * g.H * 4, 16);
-    L.xsum = take(o, p.maxr * (g.H / kSub) * 4, 16);
+    L.xsum = take(o, p.maxr * (g.H / kGroup) * 4, 16);
+    L.act = take(o, p.act_pairs * Im * 4, 16);
+    L.asum = take(o, p.act_pairs * (Im / kGroup) * 4, 16);
     L.ybuf = take(o, p.maxr * g.k * p.hrows * 4, 16);
     L.ysh = take(o, p.hrows * kMaxRows * 4, 16);
     L.target = take(o, ms * 4, 16);
+    L.pb = take(o, p.pb_bytes, 128);
     L.ring = take(o, p.NS * p.S, 128);
     L.total = o;
     return L;
 }
-
-__host__ __device__ inline int lanes_per_row(int K) { return K / kSub < 32 ? K / kSub : 32; }
 
 // ------------------------------------------------------------------- PTX
 
@@ -141,10 +165,23 @@ __device__ __forceinline__ bool mbar_try_wait_sleep(uint64_t *bar, unsigned pari
     return ok != 0;
 }
 
+// L2 policy for the weight stream: every weight byte is read once per pass,
+// so its lines go first when L2 needs room; the kernel's code, activations,
+// logits and counters then stay resident instead of being pushed out to
+// HBM by the 26 GB of weights that pass through L2 on every stack forward.
+__device__ __forceinline__ uint64_t evict_first_policy()
+{
+    uint64_t pol;
+    asm volatile("createpolicy.fractional.L2::evict_first.b64 %0, 1.0;" : "=l"(pol));
+    return pol;
+}
+
 __device__ __forceinline__ void bulk_load(void *dst, const void *src, unsigned bytes, uint64_t *bar)
 {
-    asm volatile("cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];"
-                 ::"r"(smem_u32(dst)), "l"(src), "r"(bytes), "r"(smem_u32(bar)) : "memory");
+    asm volatile("cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes.L2::cache_hint"
+                 " [%0], [%1], %2, [%3], %4;"
+                 ::"r"(smem_u32(dst)), "l"(src), "r"(bytes), "r"(smem_u32(bar)), "l"(evict_first_policy())
+                 : "memory");
 }
 
 __device__ __forceinline__ unsigned long long now_ns()
@@ -173,6 +210,11 @@ __device__ __forceinline__ void red_release_add(unsigned *p, unsigned v)
     asm volatile("red.release.gpu.global.add.u32 [%0], %1;" ::"l"(p), "r"(v) : "memory");
 }
 
+__device__ __forceinline__ void red_relaxed_add(unsigned *p, unsigned v)
+{
+    asm volatile("red.relaxed.gpu.global.add.u32 [%0], %1;" ::"l"(p), "r"(v) : "memory");
+}
+
 __device__ __forceinline__ unsigned atom_add_acqrel(unsigned *p, unsigned v)
 {
     unsigned old;
@@ -190,6 +232,24 @@ __device__ __forceinline__ unsigned ld_acquire(const unsigned *p)
 __device__ __forceinline__ void st_relaxed(unsigned *p, unsigned v)
 {
     asm volatile("st.relaxed.gpu.global.u32 [%0], %1;" ::"l"(p), "r"(v) : "memory");
+}
+
+// Tagged words: a 32-bit payload (an fp32 value, or two bf16 values) with
+// the 32-bit tag of the layer that wrote it, stored and loaded as one
+// 64-bit access.  A reader that sees its own layer's tag has the value; no
+// separate flag, counter or barrier is needed to publish data between CTAs.
+__device__ __forceinline__ unsigned layer_tag(const KParams &kp, int l) { return kp.epoch + (unsigned)l + 1u; }
+
+__device__ __forceinline__ void st_tag(uint64_t *p, uint32_t payload, unsigned tag)
+{
+    asm volatile("st.relaxed.gpu.global.b64 [%0], %1;" ::"l"(p), "l"(((uint64_t)tag << 32) | payload) : "memory");
+}
+
+__device__ __forceinline__ uint64_t ld_tag(const uint64_t *p)
+{
+    uint64_t v;
+    asm volatile("ld.relaxed.gpu.global.b64 %0, [%1];" : "=l"(v) : "l"(p) : "memory");
+    return v;
 }
 
 __device__ __forceinline__ float bf2f(uint16_t b) { return __uint_as_float((uint32_t)b << 16); }
@@ -228,7 +288,7 @@ __device__ __forceinline__ void wstamp(const KParams &kp, int l, int ev)
 // ----------------------------------------------------------- CTA state
 
 struct Sh {
-    uint64_t *full, *empty, *route;
+    uint64_t *full, *empty, *route, *pb_full, *pb_empty;
     int *flags;          // [0] abort, [1] U
     int *slot_e;
     uint32_t *slot_mask;
@@ -241,17 +301,21 @@ struct Sh {
     float *topw;
     float *row_w;        // [kMaxRows][kMaxK]  by expert id
     int *row_pair;
-    float *cand_v;       // [kMaxRows][kCandCap]
-    int *cand_e;
-    float *red;          // [kMaxRows][kRedChunks + 1]
-    float *xs;           // arranged hn rows
-    float *xsum;         // per-16 sums of xs
+    float *red;          // [kMaxRows][NCW + 1] RMSNorm partial sums, then 1/rms
+    float *p1v;          // [shared rows of this CTA][maxr] gate / up values
+    int *pair_src;       // [act_pairs] slot * kMaxRows + row of each staged pair
+    int *pend;           // [NCW][max_slots] activation units a warp has yet to publish
+    float4 *xs;          // [maxr][H / 4] arranged hn * 2^100
+    float *xsum;         // [maxr][H / 64] group sums of hn
+    float4 *act;         // [act_pairs][K / 4] arranged activations * 2^100
+    float *asum;         // [act_pairs][K / 64]
     float *ybuf;         // [pair][hrows] routed expert outputs of this CTA's slice
     float *ysh;          // [hrows][kMaxRows] shared expert outputs
     unsigned *target;    // [max_slots] activation-ready count each slot must reach this layer
     unsigned *act_done;  // [max_slots] global activation-ready counters (workspace)
+    uint8_t *pb;
     uint8_t *ring;
-    int NS, S, hrows;
+    int NS, S, hrows, act_pairs;
     long long timeout_ns;
     Ctrl *ctrl;
 };
@@ -301,6 +365,28 @@ __device__ bool wait_count(const Sh &sh, const unsigned *ctr, unsigned target, i
     return __shfl_sync(FULLMASK, ok ? 1 : 0, 0) != 0;
 }
 
+// Loads tagged word p until it carries `tag`; returns its payload.  Bounded:
+// on timeout (or when another thread gave up) raises the abort flag and
+// returns 0; callers check aborted() at their next CTA barrier.
+__device__ uint32_t poll_tag(const Sh &sh, const uint64_t *p, unsigned tag, int where)
+{
+    uint64_t v = ld_tag(p);
+    if ((unsigned)(v >> 32) == tag) return (uint32_t)v;
+    const unsigned long long t0 = now_ns();
+    for (unsigned it = 1;; ++it) {
+        __nanosleep(32);
+        v = ld_tag(p);
+        if ((unsigned)(v >> 32) == tag) return (uint32_t)v;
+        if ((it & 15) == 0) {
+            if (aborted(sh)) return 0u;
+            if (now_ns() - t0 > (unsigned long long)sh.timeout_ns) {
+                raise_abort(sh, where);
+                return 0u;
+            }
+        }
+    }
+}
+
 // Grid-wide barrier over the compute warps of every CTA.  The arrival
 // counter grows monotonically during a launch (barrier b waits for
 // (b + 1) * gridDim.x arrivals) and is reset by the last CTA to finish.
@@ -310,7 +396,7 @@ __device__ bool grid_sync(const KParams &kp, const Sh &sh, int &nsync)
     if (threadIdx.x == 0) {
         Ctrl *ctrl = sh.ctrl;
         const unsigned target = (unsigned)(nsync + 1) * gridDim.x;
-        if (!(kp.skip_cta == (int)blockIdx.x && nsync == 0)) red_release_add(&ctrl->count, 1u);
+        red_release_add(&ctrl->count, 1u);
         if (ld_acquire(&ctrl->count) < target) {
             const unsigned long long t0 = now_ns();
             for (unsigned it = 1;; ++it) {
@@ -326,13 +412,13 @@ __device__ bool grid_sync(const KParams &kp, const Sh &sh, int &nsync)
     return !cbar_or(aborted(sh));
 }
 
-__device__ void kernel_exit(const Sh &sh, int sh_max_slots_for_reset)
+__device__ void kernel_exit(const Sh &sh, int max_slots)
 {
     if (threadIdx.x == 0 && !aborted(sh)) {
         Ctrl *ctrl = sh.ctrl;
         const unsigned old = atom_add_acqrel(&ctrl->exit, 1u);
         if (old == gridDim.x - 1) {
-            for (int i = 0; i < sh_max_slots_for_reset; ++i) st_relaxed(&sh.act_done[i], 0u);
+            for (int i = 0; i < max_slots; ++i) st_relaxed(&sh.act_done[i], 0u);
             st_relaxed(&ctrl->count, 0u);
             st_relaxed(&ctrl->exit, 0u);
         }
@@ -345,169 +431,308 @@ __device__ __forceinline__ void split(int n, int P, int c, int &a, int &b)
     b = (int)((long long)n * (c + 1) / P);
 }
 
-// ------------------------------------------------------ dot-product kernels
-
-// Arranged float4 index of (sub-group sg, quarter t) for vectors of K inputs:
-// lanes holding consecutive sub-groups read consecutive float4s.  LPR is a
-// power of two (16-input sub-groups per row, capped at 32).
-__device__ __forceinline__ int arr_index(int sg, int t, int LPR)
+// This CTA's output rows [h0, h1): whole pairs of rows, so that a row pair of
+// bf16 outputs goes out as one tagged word.
+__device__ __forceinline__ void hslice(int H, int &h0, int &h1)
 {
-    return ((sg & ~(LPR - 1)) << 2) + t * LPR + (sg & (LPR - 1));
+    split(H / 2, gridDim.x, blockIdx.x, h0, h1);
+    h0 *= 2;
+    h1 *= 2;
+}
+
+// ------------------------------------------------------ dequant + dot kernels
+
+__device__ __forceinline__ int ilog2(int x) { return 31 - __clz(x); }
+
+// Arranged vectors: for K inputs in G = K / 64 groups, float4 number
+// t * G + g holds inputs 64 g + 4 t .. 64 g + 4 t + 3 (times 2^100), so the
+// lanes of a warp, one group each, read consecutive float4s.
+
+// Codes of group g of a packed row (64 codes, 8 * BITS bytes).
+// Shared-memory loads by 32-bit shared address: the row kernels are not
+// inlined into the kernel, so generic pointers would not be known to point
+// to shared memory.
+__device__ __forceinline__ uint4 lds4(uint32_t a)
+{
+    uint4 v;
+    asm("ld.shared.v4.u32 {%0, %1, %2, %3}, [%4];" : "=r"(v.x), "=r"(v.y), "=r"(v.z), "=r"(v.w) : "r"(a));
+    return v;
+}
+__device__ __forceinline__ float4 ldsf4(uint32_t a)
+{
+    float4 v;
+    asm("ld.shared.v4.f32 {%0, %1, %2, %3}, [%4];" : "=f"(v.x), "=f"(v.y), "=f"(v.z), "=f"(v.w) : "r"(a));
+    return v;
+}
+__device__ __forceinline__ uint32_t lds1(uint32_t a)
+{
+    uint32_t v;
+    asm("ld.shared.u32 %0, [%1];" : "=r"(v) : "r"(a));
+    return v;
+}
+__device__ __forceinline__ float ldsf1(uint32_t a)
+{
+    float v;
+    asm("ld.shared.f32 %0, [%1];" : "=f"(v) : "r"(a));
+    return v;
 }
 
 template <int BITS>
-__device__ __forceinline__ void load_codes(const uint8_t *row, int sg, uint32_t (&w)[4])
+__device__ __forceinline__ void load_group(uint32_t row, int g, uint32_t (&w)[2 * BITS])
 {
-    if (BITS == 4) {
-        const uint2 v = *reinterpret_cast<const uint2 *>(row + sg * 8);
-        w[0] = v.x; w[1] = v.y; w[2] = 0; w[3] = 0;
-    } else if (BITS == 6) {
-        const uint32_t *p = reinterpret_cast<const uint32_t *>(row + sg * 12);
-        w[0] = p[0]; w[1] = p[1]; w[2] = p[2]; w[3] = 0;
-    } else {
-        const uint4 v = *reinterpret_cast<const uint4 *>(row + sg * 16);
-        w[0] = v.x; w[1] = v.y; w[2] = v.z; w[3] = v.w;
+#pragma unroll
+    for (int i = 0; i < BITS / 2; ++i) {
+        const uint4 v = lds4(row + g * 8 * BITS + 16 * i);
+        w[4 * i] = v.x; w[4 * i + 1] = v.y; w[4 * i + 2] = v.z; w[4 * i + 3] = v.w;
     }
 }
 
-__device__ __forceinline__ void scale_bias(const uint8_t *row, int K, int bits, int sg, float &s, float &b)
+__device__ __forceinline__ void scale_bias(uint32_t row, int K, int bits, int g, float &s, float &b)
 {
-    const uint32_t sbw = *reinterpret_cast<const uint32_t *>(row + K * bits / 8 + (sg >> 2) * 4);
+    const uint32_t sbw = lds1(row + K * bits / 8 + g * 4);
     s = __uint_as_float(sbw << 16);
     b = __uint_as_float(sbw & 0xFFFF0000u);
 }
 
-// Codes 4T .. 4T+3 of NROWS weight rows as two exact float pairs per row
-// (packed two-lane FADD removes the exponent offsets).
-template <int BITS, int NROWS, int T>
-__device__ __forceinline__ void codes4(const uint32_t (&w)[NROWS][4], float2 (&qa)[NROWS], float2 (&qb)[NROWS])
+__device__ __forceinline__ float2 xpair(const float4 &x, int half)
 {
-#pragma unroll
-    for (int n = 0; n < NROWS; ++n) {
-        float f[4], o[4];
-        Unpack<BITS>::template raw4<T>(w[n], f, o);
-        qa[n] = __fadd2_rn(make_float2(f[0], f[1]), make_float2(-o[0], -o[1]));
-        qb[n] = __fadd2_rn(make_float2(f[2], f[3]), make_float2(-o[2], -o[3]));
-    }
+    return half ? make_float2(x.z, x.w) : make_float2(x.x, x.y);
 }
 
-// Sub-group sg (16 inputs) of NROWS weight rows against NR activation rows
-// arranged in shared memory: acc[n][r] += s_g * sum(q x) + b_g * sum(x), the
-// per-group affine factoring of sum_j (q_j s + b) x_j.  Two-lane FMAs keep
-// codes 0, 2 and 1, 3 of each quarter in separate partial sums.
-template <int BITS, int NR, int NROWS, int T>
-__device__ __forceinline__ void quarter_s(const uint32_t (&w)[NROWS][4], const float4 *xs4, const int (&xoff)[NR],
-                                          int ai, int LPR, float2 (&S)[NROWS][NR])
+// First pair of class c (pairs of one class share both positions).
+template <typename PT>
+__host__ __device__ constexpr int first_of_class(int c)
 {
-    float2 qa[NROWS], qb[NROWS];
-    codes4<BITS, NROWS, T>(w, qa, qb);
-#pragma unroll
-    for (int r = 0; r < NR; ++r) {
-        const float4 x = xs4[xoff[r] + ai + T * LPR];
-        const float2 xa = make_float2(x.x, x.y), xb = make_float2(x.z, x.w);
-#pragma unroll
-        for (int n = 0; n < NROWS; ++n) {
-            S[n][r] = __ffma2_rn(qa[n], xa, S[n][r]);
-            S[n][r] = __ffma2_rn(qb[n], xb, S[n][r]);
-        }
-    }
+    int i0 = 0;
+    for (int i = 7; i >= 0; --i)
+        if (PT::cls(i) == c) i0 = i;
+    return i0;
 }
 
-template <int BITS, int NR, int NROWS>
-__device__ __forceinline__ void qdot_sub(const uint8_t *const (&wr)[NROWS], int K, int sg, const float4 *xs4,
-                                         const float *xsum, const int (&xoff)[NR], const int (&soff)[NR],
-                                         int LPR, float (&acc)[NROWS][NR])
+// Chunk order of a lane.  At 8 and 4 bits a group is 64 or 32 bytes, so
+// the same 16-byte chunk of neighbouring lanes' groups falls on the same
+// shared-memory banks; each lane starts at a different chunk instead.  (At
+// 6 bits the 48-byte stride already spreads the banks.)
+template <int BITS>
+__device__ __forceinline__ int chunk_rot(int g)
 {
-    const int ai = arr_index(sg, 0, LPR);
-    if constexpr (BITS == 0) {
-#pragma unroll
-        for (int n = 0; n < NROWS; ++n) {
-            const float4 *wp = reinterpret_cast<const float4 *>(wr[n] + sg * 64);
-            float S[NR];
-#pragma unroll
-            for (int r = 0; r < NR; ++r) S[r] = 0.f;
-#pragma unroll
-            for (int t = 0; t < 4; ++t) {
-                const float4 wv = wp[t];
-#pragma unroll
-                for (int r = 0; r < NR; ++r) {
-                    const float4 x = xs4[xoff[r] + ai + t * LPR];
-                    S[r] = fmaf(wv.x, x.x, S[r]);
-                    S[r] = fmaf(wv.y, x.y, S[r]);
-                    S[r] = fmaf(wv.z, x.z, S[r]);
-                    S[r] = fmaf(wv.w, x.w, S[r]);
-                }
-            }
-#pragma unroll
-            for (int r = 0; r < NR; ++r) acc[n][r] += S[r];
-        }
-    } else {
-        uint32_t w[NROWS][4];
-        float s[NROWS], b[NROWS];
-#pragma unroll
-        for (int n = 0; n < NROWS; ++n) {
-            load_codes<BITS>(wr[n], sg, w[n]);
-            scale_bias(wr[n], K, BITS, sg, s[n], b[n]);
-        }
-        float2 S[NROWS][NR];
-#pragma unroll
-        for (int n = 0; n < NROWS; ++n)
-#pragma unroll
-            for (int r = 0; r < NR; ++r) S[n][r] = make_float2(0.f, 0.f);
-        quarter_s<BITS, NR, NROWS, 0>(w, xs4, xoff, ai, LPR, S);
-        quarter_s<BITS, NR, NROWS, 1>(w, xs4, xoff, ai, LPR, S);
-        quarter_s<BITS, NR, NROWS, 2>(w, xs4, xoff, ai, LPR, S);
-        quarter_s<BITS, NR, NROWS, 3>(w, xs4, xoff, ai, LPR, S);
-#pragma unroll
-        for (int r = 0; r < NR; ++r) {
-            const float xsm = xsum[soff[r] + sg];
+    return BITS == 8 ? (g >> 1) & 3 : BITS == 4 ? (g >> 2) & 1 : 0;
+}
+
+__device__ __forceinline__ uint2 lds2(uint32_t a)
+{
+    uint2 v;
+    asm("ld.shared.v2.u32 {%0, %1}, [%2];" : "=r"(v.x), "=r"(v.y) : "r"(a));
+    return v;
+}
+
+// Visits the 4 sub-groups of group g of NROWS rows: f(sg, parity, words[n])
+// with words[n] the sub-group's BITS/2 code words of row n and parity a
+// compile-time visit parity (0, 1).  Two sub-groups per loop trip, the loop
+// not unrolled: the kernel's code then stays small enough to remain in the
+// instruction caches between layers.
+template <int BITS, int NROWS, typename F>
+__device__ __forceinline__ void for_subgroups(const uint32_t (&rp)[NROWS], int g, F &&f)
+{
+    if constexpr (BITS == 6) {
+        // 24 bytes (two sub-groups) per trip; lanes 8 .. 15 of each half warp
+        // start with the other pair so that 8-byte loads spread the banks
+        const int rot = (g >> 3) & 1;
+#pragma unroll 1
+        for (int j = 0; j < 2; ++j) {
+            const int jj = j ^ rot;
+            uint32_t w[NROWS][6];
 #pragma unroll
             for (int n = 0; n < NROWS; ++n) {
-                acc[n][r] = fmaf(s[n], S[n][r].x + S[n][r].y, acc[n][r]);
-                acc[n][r] = fmaf(b[n], xsm, acc[n][r]);
+                const uint32_t a = rp[n] + g * 48 + 24 * jj;
+                const uint2 v0 = lds2(a), v1 = lds2(a + 8), v2 = lds2(a + 16);
+                w[n][0] = v0.x; w[n][1] = v0.y; w[n][2] = v1.x; w[n][3] = v1.y; w[n][4] = v2.x; w[n][5] = v2.y;
             }
+            const uint32_t *w0[NROWS], *w1[NROWS];
+#pragma unroll
+            for (int n = 0; n < NROWS; ++n) { w0[n] = &w[n][0]; w1[n] = &w[n][3]; }
+            f(2 * jj, 0, w0);
+            f(2 * jj + 1, 1, w1);
+        }
+    } else if constexpr (BITS == 8) {
+        // one 16-byte chunk per sub-group, two per trip
+        const int rot = chunk_rot<8>(g);
+#pragma unroll 1
+        for (int j = 0; j < 2; ++j) {
+            const int c0 = (2 * j + rot) & 3, c1 = (2 * j + 1 + rot) & 3;
+            uint32_t w[NROWS][8];
+#pragma unroll
+            for (int n = 0; n < NROWS; ++n) {
+                const uint4 v0 = lds4(rp[n] + g * 64 + 16 * c0), v1 = lds4(rp[n] + g * 64 + 16 * c1);
+                w[n][0] = v0.x; w[n][1] = v0.y; w[n][2] = v0.z; w[n][3] = v0.w;
+                w[n][4] = v1.x; w[n][5] = v1.y; w[n][6] = v1.z; w[n][7] = v1.w;
+            }
+            const uint32_t *w0[NROWS], *w1[NROWS];
+#pragma unroll
+            for (int n = 0; n < NROWS; ++n) { w0[n] = &w[n][0]; w1[n] = &w[n][4]; }
+            f(c0, 0, w0);
+            f(c1, 1, w1);
+        }
+    } else {
+        // 4 bits: a 16-byte chunk holds two sub-groups
+        const int rot = chunk_rot<4>(g);
+#pragma unroll 1
+        for (int j = 0; j < 2; ++j) {
+            const int c = (j + rot) & 1;
+            uint32_t w[NROWS][4];
+#pragma unroll
+            for (int n = 0; n < NROWS; ++n) {
+                const uint4 v = lds4(rp[n] + g * 32 + 16 * c);
+                w[n][0] = v.x; w[n][1] = v.y; w[n][2] = v.z; w[n][3] = v.w;
+            }
+            const uint32_t *w0[NROWS], *w1[NROWS];
+#pragma unroll
+            for (int n = 0; n < NROWS; ++n) { w0[n] = &w[n][0]; w1[n] = &w[n][2]; }
+            f(2 * c, 0, w0);
+            f(2 * c + 1, 1, w1);
         }
     }
 }
 
-// The same against NR activation rows held in registers (16 values of the
-// lane's sub-group and their sum per row).
-template <int BITS, int NR, int NROWS>
-__device__ __forceinline__ void rdot_sub(const uint8_t *const (&wr)[NROWS], int K, int sg, const float (&a)[NR][16],
-                                         const float (&as)[NR], float (&acc)[NROWS][NR])
+// acc[n][r] += dot(row n, group g) . x_r for NROWS weight rows and NR token
+// rows, with per-class accumulators (split by visit parity at 4 and 8 bits,
+// which have few classes, for more independent chains).  The codes are
+// extracted once for all token rows; each token row's arithmetic is the
+// same whatever NR is, so a row's result does not depend on the other rows
+// of the call (row-exact).
+template <int BITS, int NROWS, int NR>
+__device__ __forceinline__ void grp_cls(const uint32_t (&rp)[NROWS], int g, int K, int G, const uint32_t (&xq)[NR],
+                                        const float (&xsum)[NR], float (&acc)[NROWS][NR])
 {
-    uint32_t w[NROWS][4];
+    using PT = Pairs<BITS>;
+    constexpr int NC = PT::NC, NA = BITS == 6 ? NC : 2 * NC;
     float s[NROWS], b[NROWS];
 #pragma unroll
-    for (int n = 0; n < NROWS; ++n) {
-        load_codes<BITS>(wr[n], sg, w[n]);
-        scale_bias(wr[n], K, BITS, sg, s[n], b[n]);
-    }
-    float2 S[NROWS][NR];
+    for (int n = 0; n < NROWS; ++n) scale_bias(rp[n], K, BITS, g, s[n], b[n]);
+    float2 A[NROWS][NR][NA];
 #pragma unroll
     for (int n = 0; n < NROWS; ++n)
 #pragma unroll
-        for (int r = 0; r < NR; ++r) S[n][r] = make_float2(0.f, 0.f);
-    float2 qa[NROWS], qb[NROWS];
-#define MOE_RQ(T)                                                                                 \
-    codes4<BITS, NROWS, T>(w, qa, qb);                                                            \
-    _Pragma("unroll") for (int r = 0; r < NR; ++r) {                                              \
-        const float2 xa = make_float2(a[r][4 * T], a[r][4 * T + 1]);                              \
-        const float2 xb = make_float2(a[r][4 * T + 2], a[r][4 * T + 3]);                          \
-        _Pragma("unroll") for (int n = 0; n < NROWS; ++n) {                                       \
-            S[n][r] = __ffma2_rn(qa[n], xa, S[n][r]);                                             \
-            S[n][r] = __ffma2_rn(qb[n], xb, S[n][r]);                                             \
-        }                                                                                         \
+        for (int r = 0; r < NR; ++r)
+#pragma unroll
+            for (int c = 0; c < NA; ++c) A[n][r][c] = make_float2(0.f, 0.f);
+    const uint32_t G16 = G * 16;
+    for_subgroups<BITS, NROWS>(rp, g, [&](int sg, int step, const uint32_t *const (&ws)[NROWS]) {
+        float4 xv[NR][4];
+#pragma unroll
+        for (int r = 0; r < NR; ++r)
+#pragma unroll
+            for (int t = 0; t < 4; ++t) xv[r][t] = ldsf4(xq[r] + g * 16 + (4 * sg + t) * G16);
+        const int half = NA > NC ? step * NC : 0;
+#pragma unroll
+        for (int n = 0; n < NROWS; ++n)
+            PT::each(ws[n], [&](int i, float a, float bb) {
+                const float2 q = make_float2(a, bb);
+#pragma unroll
+                for (int r = 0; r < NR; ++r)
+                    A[n][r][PT::cls(i) + half] =
+                        __ffma2_rn(q, xpair(xv[r][i >> 1], i & 1), A[n][r][PT::cls(i) + half]);
+            });
+    });
+#pragma unroll
+    for (int n = 0; n < NROWS; ++n)
+#pragma unroll
+        for (int r = 0; r < NR; ++r) {
+            float t = 0.f;
+#pragma unroll
+            for (int c = 0; c < NA; ++c) {
+                const int i0 = first_of_class<PT>(c % NC);
+                t = fmaf(A[n][r][c].x, __uint_as_float(cls_bits(PT::pa(i0))), t);
+                t = fmaf(A[n][r][c].y, __uint_as_float(cls_bits(PT::pb(i0))), t);
+            }
+            acc[n][r] = fmaf(s[n], t, fmaf(b[n], xsum[r], acc[n][r]));
+        }
+}
+
+// fp32 rows (a router given in fp32): K floats per row.
+template <int NROWS, int NR>
+__device__ __forceinline__ void grp_f32(const uint32_t (&rp)[NROWS], int g, int G,
+                                        const uint32_t (&xq)[NR], float (&acc)[NROWS][NR])
+{
+#pragma unroll
+    for (int n = 0; n < NROWS; ++n) {
+        float S[NR];
+#pragma unroll
+        for (int r = 0; r < NR; ++r) S[r] = 0.f;
+#pragma unroll 4
+        for (int t = 0; t < 16; ++t) {
+            const float4 wq = ldsf4(rp[n] + (g * 16 + t) * 16);
+#pragma unroll
+            for (int r = 0; r < NR; ++r) {
+                const float4 x = ldsf4(xq[r] + (t * G + g) * 16);
+                S[r] = fmaf(wq.x, x.x, fmaf(wq.y, x.y, fmaf(wq.z, x.z, fmaf(wq.w, x.w, S[r]))));
+            }
+        }
+#pragma unroll
+        for (int r = 0; r < NR; ++r) acc[n][r] = fmaf(S[r], 0x1p-100f, acc[n][r]);
     }
-    MOE_RQ(0) MOE_RQ(1) MOE_RQ(2) MOE_RQ(3)
-#undef MOE_RQ
+}
+
+// A warp computes rows [0, nrows) (row i at base + i * rstride, K inputs
+// at BITS bits) against NR arranged token vectors.  Lanes split a row's
+// groups (LPR lanes per row, GPL groups per lane); each lane takes NROWS
+// consecutive rows.  emit(first_row, acc) runs on the first lane of each
+// row group with the complete sums of rows first_row .. first_row+NROWS-1
+// (rows at or past nrows hold repeats of the last row and must be ignored).
+template <int BITS, int NROWS, int NR, typename F>
+__device__ __forceinline__ void warp_rows(const uint8_t *base, int rstride, int nrows, int K,
+                                          const uint32_t (&xq)[NR], const float (&xsg)[NR][kMaxGPL],
+                                          F &&emit)
+{
+    const int lane = threadIdx.x & 31;
+    const uint32_t sbase = smem_u32(base);
+    // K and G are powers of two: shifts instead of divisions
+    const int G = K >> 6, lgG = ilog2(G), lgL = lgG < 5 ? lgG : 5;
+    const int LPR = 1 << lgL, GPL = G >> lgL, RPP = 32 >> lgL;
+    const int lg = lane & (LPR - 1), lr = lane >> lgL;
+    for (int r0 = 0; r0 < nrows; r0 += RPP * NROWS) {
+        const int rb = r0 + lr * NROWS;
+        uint32_t rp[NROWS];
+#pragma unroll
+        for (int n = 0; n < NROWS; ++n) rp[n] = sbase + (uint32_t)(min(rb + n, nrows - 1) * rstride);
+        float acc[NROWS][NR];
+#pragma unroll
+        for (int n = 0; n < NROWS; ++n)
+#pragma unroll
+            for (int r = 0; r < NR; ++r) acc[n][r] = 0.f;
+        if (rb < nrows) {
+            for (int j = 0; j < GPL; ++j) {
+                const int g = lg + LPR * j;
+                if constexpr (BITS == 0) {
+                    grp_f32<NROWS, NR>(rp, g, G, xq, acc);
+                } else {
+                    float xs[NR];
+#pragma unroll
+                    for (int r = 0; r < NR; ++r) xs[r] = xsg[r][j];
+                    grp_cls<BITS, NROWS, NR>(rp, g, K, G, xq, xs, acc);
+                }
+            }
+        }
+        for (int o = LPR >> 1; o >= 1; o >>= 1)
+#pragma unroll
+            for (int n = 0; n < NROWS; ++n)
+#pragma unroll
+                for (int r = 0; r < NR; ++r) acc[n][r] += __shfl_xor_sync(FULLMASK, acc[n][r], o);
+        if (lg == 0 && rb < nrows) emit(rb, acc);
+    }
+}
+
+// Per-lane group sums of NR arranged vectors (sums[soff[r] + g] layout).
+template <int NR>
+__device__ __forceinline__ void lane_gsums(uint32_t sums, const int (&soff)[NR], int K, float (&xsg)[NR][kMaxGPL])
+{
+    const int lane = threadIdx.x & 31;
+    const int G = K >> 6, lgG = ilog2(G), lgL = lgG < 5 ? lgG : 5;
+    const int LPR = 1 << lgL, GPL = G >> lgL, lg = lane & (LPR - 1);
 #pragma unroll
     for (int r = 0; r < NR; ++r)
 #pragma unroll
-        for (int n = 0; n < NROWS; ++n) {
-            acc[n][r] = fmaf(s[n], S[n][r].x + S[n][r].y, acc[n][r]);
-            acc[n][r] = fmaf(b[n], as[r], acc[n][r]);
-        }
+        for (int j = 0; j < kMaxGPL; ++j) xsg[r][j] = j < GPL ? ldsf1(sums + 4 * (soff[r] + lg + LPR * j)) : 0.f;
 }
 
 // Token rows first .. first + NR - 1 of a row mask (in set-bit order),
@@ -529,613 +754,627 @@ __device__ __forceinline__ void rows_of_group(uint32_t mask, int first, int (&ro
     }
 }
 
-__device__ __forceinline__ int nr_bucket(int n) { return n <= 1 ? 1 : 2; }
-
-template <int N, int NR>
-__device__ __forceinline__ void lane_reduce(float (&acc)[N][NR], int LPR)
-{
-    for (int o = LPR / 2; o >= 1; o >>= 1)
-#pragma unroll
-        for (int n = 0; n < N; ++n)
-#pragma unroll
-            for (int r = 0; r < NR; ++r) acc[n][r] += __shfl_xor_sync(FULLMASK, acc[n][r], o);
-}
-
-// Gate/up units (gate row, up row) of one stage for NR token rows of hn, NU
-// units per lane group at a time -> act[m * mstride + j0 + u] = silu(g) * up.
-template <int BITS, int NR, int NU>
-__device__ void gu_pass(const Sh &sh, const uint8_t *stage, int cnt, int rowb, int H, const int (&rows)[NR],
-                        int nvalid, float *act, int mstride, int j0)
-{
-    const int lane = threadIdx.x & 31;
-    const int LPR = lanes_per_row(H), RPP = 32 / LPR, nsg = H / kSub;
-    int xoff[NR], soff[NR];
-#pragma unroll
-    for (int r = 0; r < NR; ++r) { xoff[r] = rows[r] * (H / 4); soff[r] = rows[r] * nsg; }
-    const float4 *xs4 = reinterpret_cast<const float4 *>(sh.xs);
-    for (int u0 = 0; u0 < cnt; u0 += RPP * NU) {
-        const int ub = u0 + (lane / LPR) * NU;
-        const uint8_t *wr[2 * NU];
-#pragma unroll
-        for (int i = 0; i < NU; ++i) {
-            const int u = ub + i < cnt ? ub + i : 0;
-            wr[2 * i] = stage + (size_t)u * 2 * rowb;
-            wr[2 * i + 1] = wr[2 * i] + rowb;
-        }
-        float acc[2 * NU][NR];
-#pragma unroll
-        for (int n = 0; n < 2 * NU; ++n)
-#pragma unroll
-            for (int r = 0; r < NR; ++r) acc[n][r] = 0.f;
-        if (ub < cnt)
-            for (int sg = lane % LPR; sg < nsg; sg += LPR)
-                qdot_sub<BITS, NR, 2 * NU>(wr, H, sg, xs4, sh.xsum, xoff, soff, LPR, acc);
-        lane_reduce<2 * NU, NR>(acc, LPR);
-        if (lane % LPR == 0) {
-#pragma unroll
-            for (int i = 0; i < NU; ++i)
-                if (ub + i < cnt) {
-#pragma unroll
-                    for (int r = 0; r < NR; ++r)
-                        if (r < nvalid) {
-                            const float g = acc[2 * i][r], up = acc[2 * i + 1][r];
-                            act[(size_t)rows[r] * mstride + j0 + ub + i] = g / (1.0f + expf(-g)) * up;
-                        }
-                }
-        }
-    }
-}
-
-// Router rows of one stage, NU rows per lane group at a time -> logits[m * Er + e0 + u].
-template <int BITS, int NR, int NU>
-__device__ void router_pass(const Sh &sh, const uint8_t *stage, int cnt, int rowb, int H, const int (&rows)[NR],
-                            int nvalid, float *logits, int Er, int e0)
-{
-    const int lane = threadIdx.x & 31;
-    const int LPR = lanes_per_row(H), RPP = 32 / LPR, nsg = H / kSub;
-    int xoff[NR], soff[NR];
-#pragma unroll
-    for (int r = 0; r < NR; ++r) { xoff[r] = rows[r] * (H / 4); soff[r] = rows[r] * nsg; }
-    const float4 *xs4 = reinterpret_cast<const float4 *>(sh.xs);
-    for (int u0 = 0; u0 < cnt; u0 += RPP * NU) {
-        const int ub = u0 + (lane / LPR) * NU;
-        const uint8_t *wr[NU];
-#pragma unroll
-        for (int i = 0; i < NU; ++i) wr[i] = stage + (size_t)(ub + i < cnt ? ub + i : 0) * rowb;
-        float acc[NU][NR];
-#pragma unroll
-        for (int n = 0; n < NU; ++n)
-#pragma unroll
-            for (int r = 0; r < NR; ++r) acc[n][r] = 0.f;
-        if (ub < cnt)
-            for (int sg = lane % LPR; sg < nsg; sg += LPR)
-                qdot_sub<BITS, NR, NU>(wr, H, sg, xs4, sh.xsum, xoff, soff, LPR, acc);
-        lane_reduce<NU, NR>(acc, LPR);
-        if (lane % LPR == 0) {
-#pragma unroll
-            for (int i = 0; i < NU; ++i)
-                if (ub + i < cnt) {
-#pragma unroll
-                    for (int r = 0; r < NR; ++r)
-                        if (r < nvalid) logits[(size_t)rows[r] * Er + e0 + ub + i] = acc[i][r];
-                }
-        }
-    }
-}
-
-// Down rows [rs, rs + cnt) (relative to the CTA's first output) of one
-// expert for NR token rows whose activations (K inputs each) the warp keeps
-// in registers: lane l holds sub-groups l mod LPR (+ LPR * i, i < SPL); NU
-// rows per lane group at a time.  Output of token row r, row h:
-// y[yoff[r] + h * ystride].
-template <int BITS, int NR, int SPL, int NU>
-__device__ void dn_pass(const uint8_t *stage, int rs, int cnt, int rowb, int K, const int (&rows)[NR], int nvalid,
-                        const float *act, int mstride, float *y, const int (&yoff)[NR], int ystride)
-{
-    const int lane = threadIdx.x & 31;
-    const int LPR = lanes_per_row(K), RPP = 32 / LPR;
-    float a[SPL][NR][16], as[SPL][NR];
-#pragma unroll
-    for (int i = 0; i < SPL; ++i) {
-        const int sg = lane % LPR + LPR * i;
-#pragma unroll
-        for (int r = 0; r < NR; ++r) {
-            const float4 *src = reinterpret_cast<const float4 *>(act + (size_t)rows[r] * mstride + sg * kSub);
-            float s = 0.f;
-#pragma unroll
-            for (int t = 0; t < 4; ++t) {
-                const float4 v = __ldcg(src + t);
-                a[i][r][4 * t] = v.x; a[i][r][4 * t + 1] = v.y; a[i][r][4 * t + 2] = v.z; a[i][r][4 * t + 3] = v.w;
-                s += (v.x + v.y) + (v.z + v.w);
-            }
-            as[i][r] = s;
-        }
-    }
-    for (int h0 = 0; h0 < cnt; h0 += RPP * NU) {
-        const int hb = h0 + (lane / LPR) * NU;
-        const uint8_t *wr[NU];
-#pragma unroll
-        for (int j = 0; j < NU; ++j) wr[j] = stage + (size_t)(hb + j < cnt ? hb + j : 0) * rowb;
-        float acc[NU][NR];
-#pragma unroll
-        for (int j = 0; j < NU; ++j)
-#pragma unroll
-            for (int r = 0; r < NR; ++r) acc[j][r] = 0.f;
-        if (hb < cnt) {
-#pragma unroll
-            for (int i = 0; i < SPL; ++i)
-                rdot_sub<BITS, NR, NU>(wr, K, lane % LPR + LPR * i, a[i], as[i], acc);
-        }
-        lane_reduce<NU, NR>(acc, LPR);
-        if (lane % LPR == 0) {
-#pragma unroll
-            for (int j = 0; j < NU; ++j)
-                if (hb + j < cnt) {
-#pragma unroll
-                    for (int r = 0; r < NR; ++r)
-                        if (r < nvalid) y[yoff[r] + (rs + hb + j) * ystride] = acc[j][r];
-                }
-        }
-    }
-}
-
-#define MOE_CASE(BV, RV, CALL) \
-    case (BV) * 16 + (RV): { constexpr int B_ = (BV), R_ = (RV); CALL; } break;
-#define MOE_CASES_NR(BV, CALL) MOE_CASE(BV, 1, CALL) MOE_CASE(BV, 2, CALL)
-
-// Expert matrices: 4, 6 or 8 bits.
-#define MOE_DISPATCH(BITSV, NRV, CALL)                                            \
-    do {                                                                          \
-        switch ((BITSV) * 16 + (NRV)) {                                           \
-            MOE_CASES_NR(4, CALL) MOE_CASES_NR(6, CALL) MOE_CASES_NR(8, CALL)     \
-        default: break;                                                           \
-        }                                                                         \
-    } while (0)
-
-// Router rows: fp32 (0) or 4, 6, 8 bits.
-#define MOE_DISPATCH_ROUTER(BITSV, NRV, CALL)                                                       \
-    do {                                                                                            \
-        switch ((BITSV) * 16 + (NRV)) {                                                             \
-            MOE_CASES_NR(0, CALL) MOE_CASES_NR(4, CALL) MOE_CASES_NR(6, CALL) MOE_CASES_NR(8, CALL) \
-        default: break;                                                                             \
-        }                                                                                           \
-    } while (0)
-
-// Token rows of a mask in groups of up to `gmax`: f(first, NR bucket).
+// Row groups of a mask: pairs, then a single row.
 template <typename F>
-__device__ __forceinline__ void for_row_groups(uint32_t mask, int gmax, F &&f)
+__device__ __forceinline__ void for_row_groups(uint32_t mask, F &&f)
 {
     const int n = __popc(mask);
-    for (int g0 = 0; g0 < n; g0 += gmax) f(g0, nr_bucket(min(gmax, n - g0)));
+    int g0 = 0;
+    for (; n - g0 >= 2; g0 += 2) f(g0, 2);
+    if (n - g0 == 1) f(g0, 1);
 }
 
-// One token row: two units (four weight rows) per lane group at a time;
-// several token rows: one unit at a time.
-__device__ void gu_stage(const Sh &sh, int bits, const uint8_t *stage, int cnt, int rowb, int H, uint32_t mask,
-                         float *act, int mstride, int j0)
-{
-    for_row_groups(mask, 2, [&](int g0, int nr) {
-        MOE_DISPATCH(bits, nr, ({
-            int rows[R_], nv;
-            rows_of_group<R_>(mask, g0, rows, nv);
-            // two units at a time for one token row; an odd last unit alone
-            const int even = R_ == 1 ? (cnt & ~1) : 0;
-            if (even) gu_pass<B_, R_, 2>(sh, stage, even, rowb, H, rows, nv, act, mstride, j0);
-            if (cnt > even)
-                gu_pass<B_, R_, 1>(sh, stage + (size_t)even * 2 * rowb, cnt - even, rowb, H, rows, nv, act, mstride,
-                                   j0 + even);
-        }));
-    });
-}
+// The warp-level row kernels below are separate (not inlined) functions,
+// one per (bits, token rows): each gets its own register allocation, and a
+// call is made once per stage and row group, not per weight.
 
-__device__ void router_stage(const Sh &sh, int bits, const uint8_t *stage, int cnt, int rowb, int H, uint32_t mask,
-                             float *logits, int Er, int e0)
+// Gate/up units [0, cnt) at `units` (unit u: gate row then up row, row
+// bytes rowb, K = H inputs) for token rows g0 .. of `mask` against hn:
+// dst[m * ld + u] = silu(gate) * up.
+template <int B, int R>
+__device__ __forceinline__ void gu_k_body(const float4 *xs, const float *xsum, int H, const uint8_t *units, int cnt,
+                                  int rowb, uint32_t mask, int g0, uint64_t *dst, int ld, unsigned tag)
 {
-    for_row_groups(mask, 2, [&](int g0, int nr) {
-        MOE_DISPATCH_ROUTER(bits, nr, ({
-            int rows[R_], nv;
-            rows_of_group<R_>(mask, g0, rows, nv);
-            const int even = R_ == 1 ? (cnt & ~1) : 0;
-            if (even) router_pass<B_, R_, 2>(sh, stage, even, rowb, H, rows, nv, logits, Er, e0);
-            if (cnt > even)
-                router_pass<B_, R_, 1>(sh, stage + (size_t)even * rowb, cnt - even, rowb, H, rows, nv, logits, Er,
-                                       e0 + even);
-        }));
-    });
-}
-
-// Down rows of one stage for every row group of `mask`.  Routed experts
-// write ybuf[(pair0 + r) * hrows + h]; the shared expert writes
-// ysh[h * kMaxRows + m].
-__device__ void dn_stage(const Sh &sh, int bits, const uint8_t *stage, int rs, int cnt, int rowb, int K, uint32_t mask,
-                         const float *act, int mstride, bool shared, int pair0)
-{
-    const int spl = (K / kSub) / lanes_per_row(K);   // 1 or 2 (K <= 1024)
-    const int gmax = 2 / spl;
-    for_row_groups(mask, gmax, [&](int g0, int nr) {
-        auto run = [&](auto spl_c) {
-            constexpr int SPLV = decltype(spl_c)::value;
-            MOE_DISPATCH(bits, nr, ({
-                if constexpr (R_ * SPLV <= 2) {
-                    int rows[R_], nv;
-                    rows_of_group<R_>(mask, g0, rows, nv);
-                    int yoff[R_];
+    const int G = H / kGroup;
+    int rows[R], nv;
+    rows_of_group<R>(mask, g0, rows, nv);
+    uint32_t xq[R];
+    int soff[R];
 #pragma unroll
-                    for (int r = 0; r < R_; ++r)
-                        yoff[r] = shared ? rows[r] : (pair0 + g0 + (r < nv ? r : nv - 1)) * sh.hrows;
-                    float *y = shared ? sh.ysh : sh.ybuf;
-                    const int ys = shared ? kMaxRows : 1;
-                    const int RPPv = 32 / lanes_per_row(K);
-                    // pairs of rows per lane group; a leftover row alone
-                    const int even = cnt - cnt % (2 * RPPv);
-                    if (even) dn_pass<B_, R_, SPLV, 2>(stage, rs, even, rowb, K, rows, nv, act, mstride, y, yoff, ys);
-                    if (cnt > even)
-                        dn_pass<B_, R_, SPLV, 1>(stage + (size_t)even * rowb, rs + even, cnt - even, rowb, K, rows, nv,
-                                                 act, mstride, y, yoff, ys);
-                }
-            }));
-        };
-        if (spl == 1) run(std::integral_constant<int, 1>{});
-        else run(std::integral_constant<int, 2>{});
+    for (int r = 0; r < R; ++r) { xq[r] = smem_u32(xs) + (uint32_t)(rows[r] * H * 4); soff[r] = rows[r] * G; }
+    float xsg[R][kMaxGPL];
+    lane_gsums<R>(smem_u32(xsum), soff, H, xsg);
+    constexpr int NROWS = R == 1 ? 4 : 2;   // whole units (gate and up row) per lane
+    warp_rows<B, NROWS, R>(units, rowb, 2 * cnt, H, xq, xsg, [&](int rb, const float (&acc)[NROWS][R]) {
+#pragma unroll
+        for (int k2 = 0; k2 < NROWS; k2 += 2) {
+            if (rb + k2 + 1 < 2 * cnt) {
+#pragma unroll
+                for (int r = 0; r < R; ++r)
+                    if (r < nv) {
+                        const float gt = acc[k2][r], up = acc[k2 + 1][r];
+                        st_tag(dst + (size_t)rows[r] * ld + ((rb + k2) >> 1),
+                               __float_as_uint(gt / (1.0f + expf(-gt)) * up), tag);
+                    }
+            }
+        }
+    });
+}
+
+// One row of K = H inputs (a router row, or a gate or up row of a shared
+// unit) for token rows g0 .. of `mask`: dst[m * ms] = row . hn_m.
+template <int B, int R>
+__device__ __forceinline__ void one_k_body(const float4 *xs, const float *xsum, int H, const uint8_t *row, uint32_t mask,
+                                   int g0, void *dst, int ms, unsigned tag)
+{
+    const int G = H / kGroup;
+    int rows[R], nv;
+    rows_of_group<R>(mask, g0, rows, nv);
+    uint32_t xq[R];
+    int soff[R];
+#pragma unroll
+    for (int r = 0; r < R; ++r) { xq[r] = smem_u32(xs) + (uint32_t)(rows[r] * H * 4); soff[r] = rows[r] * G; }
+    float xsg[R][kMaxGPL];
+    lane_gsums<R>(smem_u32(xsum), soff, H, xsg);
+    warp_rows<B, 1, R>(row, 0, 1, H, xq, xsg, [&](int, const float (&acc)[1][R]) {
+#pragma unroll
+        for (int r = 0; r < R; ++r)
+            if (r < nv) {
+                if (tag) st_tag(static_cast<uint64_t *>(dst) + (size_t)rows[r] * ms, __float_as_uint(acc[0][r]), tag);
+                else static_cast<float *>(dst)[(size_t)rows[r] * ms] = acc[0][r];
+            }
+    });
+}
+
+// Down rows [0, cnt) (K inputs each) against the staged activation pairs
+// pair0 + t, t = g0 .. (t < popc(mask)): dst[h * hs + t * ts].
+template <int B, int R>
+__device__ __forceinline__ void dn_k_body(const float4 *act, const float *asum, int K, const uint8_t *rows0, int cnt,
+                                  int rowb, uint32_t mask, int pair0, int g0, float *dst, int hs, int ts)
+{
+    const int Gi = K / kGroup, n = __popc(mask);
+    int tp[R];
+    int nv = 0;
+#pragma unroll
+    for (int r = 0; r < R; ++r) {
+        tp[r] = g0 + r < n ? g0 + r : n - 1;
+        nv += g0 + r < n ? 1 : 0;
+    }
+    uint32_t xq[R];
+    int soff[R];
+#pragma unroll
+    for (int r = 0; r < R; ++r) {
+        xq[r] = smem_u32(act) + (uint32_t)((pair0 + tp[r]) * K * 4);
+        soff[r] = (pair0 + tp[r]) * Gi;
+    }
+    float xsg[R][kMaxGPL];
+    lane_gsums<R>(smem_u32(asum), soff, K, xsg);
+    constexpr int NROWS = R == 1 ? 2 : 1;   // (down rows: any count)
+    warp_rows<B, NROWS, R>(rows0, rowb, cnt, K, xq, xsg, [&](int rb, const float (&acc)[NROWS][R]) {
+#pragma unroll
+        for (int k2 = 0; k2 < NROWS; ++k2)
+            if (rb + k2 < cnt) {
+#pragma unroll
+                for (int r = 0; r < R; ++r)
+                    if (r < nv) dst[(size_t)(rb + k2) * hs + (size_t)tp[r] * ts] = acc[k2][r];
+            }
+    });
+}
+
+// Out-of-line entry points of the row kernels (one per instantiation).
+template <int B, int R>
+__device__ __noinline__ void gu_k(const float4 *xs, const float *xsum, int H, const uint8_t *units, int cnt,
+                                  int rowb, uint32_t mask, int g0, uint64_t *dst, int ld, unsigned tag)
+{
+    gu_k_body<B, R>(xs, xsum, H, units, cnt, rowb, mask, g0, dst, ld, tag);
+}
+template <int B, int R>
+__device__ __noinline__ void one_k(const float4 *xs, const float *xsum, int H, const uint8_t *row, uint32_t mask,
+                                   int g0, void *dst, int ms, unsigned tag)
+{
+    one_k_body<B, R>(xs, xsum, H, row, mask, g0, dst, ms, tag);
+}
+template <int B, int R>
+__device__ __noinline__ void dn_k(const float4 *act, const float *asum, int K, const uint8_t *rows0, int cnt,
+                                  int rowb, uint32_t mask, int pair0, int g0, float *dst, int hs, int ts)
+{
+    dn_k_body<B, R>(act, asum, K, rows0, cnt, rowb, mask, pair0, g0, dst, hs, ts);
+}
+
+// Dispatch on (bits, row-group size): code = bits * 8 + nr.
+#define MOE_RK_CASES(FN, ARGS)                                                                   \
+    case 4 * 8 + 1: FN<4, 1> ARGS; break;                                                        \
+    case 4 * 8 + 2: FN<4, 2> ARGS; break;                                                        \
+    case 6 * 8 + 1: FN<6, 1> ARGS; break;                                                        \
+    case 6 * 8 + 2: FN<6, 2> ARGS; break;                                                        \
+    case 8 * 8 + 1: FN<8, 1> ARGS; break;                                                        \
+    case 8 * 8 + 2: FN<8, 2> ARGS; break;
+
+__device__ __noinline__ void gu_units(const Sh &sh, int H, int bits, const uint8_t *units, int cnt, int rowb,
+                                         uint32_t mask, uint64_t *dst, int ld, unsigned tag)
+{
+    for_row_groups(mask, [&](int g0, int nr) {
+        switch (bits * 8 + nr) {
+            MOE_RK_CASES(gu_k, (sh.xs, sh.xsum, H, units, cnt, rowb, mask, g0, dst, ld, tag))
+        default: break;
+        }
+    });
+}
+
+__device__ __noinline__ void one_row(const Sh &sh, int H, int bits, const uint8_t *row, uint32_t mask,
+                                        void *dst, int ms, unsigned tag)
+{
+    for_row_groups(mask, [&](int g0, int nr) {
+        switch (bits * 8 + nr) {
+            MOE_RK_CASES(one_k, (sh.xs, sh.xsum, H, row, mask, g0, dst, ms, tag))
+        case 0 * 8 + 1: one_k<0, 1>(sh.xs, sh.xsum, H, row, mask, g0, dst, ms, tag); break;
+        case 0 * 8 + 2: one_k<0, 2>(sh.xs, sh.xsum, H, row, mask, g0, dst, ms, tag); break;
+        default: break;
+        }
+    });
+}
+
+__device__ __noinline__ void dn_rows(const Sh &sh, int bits, const uint8_t *rows0, int cnt, int rowb, int K,
+                                        uint32_t mask, int pair0, float *dst, int hs, int ts)
+{
+    for_row_groups(mask, [&](int g0, int nr) {
+        switch (bits * 8 + nr) {
+            MOE_RK_CASES(dn_k, (sh.act, sh.asum, K, rows0, cnt, rowb, mask, pair0, g0, dst, hs, ts))
+        default: break;
+        }
     });
 }
 
 // ------------------------------------------------------------ P0: RMSNorm
 
-// Per-row sums of squares of M bf16 rows of x (global) into red[], and,
-// when `stage` is set, the raw values copied into xs in the arranged layout.
-// Then rinv = 1 / sqrt(mean(x^2) + eps) -> red[kMaxRows * kRedChunks + m].
-__device__ void rms_rows(const KParams &kp, const Sh &sh, const uint16_t *x, bool stage)
+// hn rows of x (bf16 [M, H], global) -> xs (arranged, * 2^100) and group
+// sums; 1 / rms of row m -> red[m * (NCW + 1) + NCW].  A thread item is 8
+// consecutive inputs (one 16-byte load); H / 8 is a multiple of 32, so the
+// 32 items of a warp belong to one row.
+__device__ void build_hn(const KParams &kp, const Sh &sh, const void *x, unsigned xtag, const uint16_t *gamma)
 {
-    const int H = kp.g.H, M = kp.M, tid = threadIdx.x, lane = tid & 31;
-    const int nsg = H / kSub, width = nsg < 32 ? nsg : 32, chunks = nsg / width;
-    const int LPR = lanes_per_row(H);
-    // pairs are visited in rounds of NCT; all lanes of a warp share a round
-    for (int p0 = 0; p0 < M * nsg; p0 += NCT) {
-        const int p = p0 + tid;
+    const int H = kp.g.H, M = kp.M, G = H / kGroup, tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+    const int per_row = H / 8, lpr = ilog2(per_row), total = M * per_row;
+    for (int m = lane; m < M; m += 32) sh.red[m * (NCW + 1) + warp] = 0.f;
+    __syncwarp();
+    // pass 1: sums of squares per (row, warp); raw values into xs
+    for (int base = 0; base < total; base += NCT) {
+        const int it = base + tid;
         float ss = 0.f;
-        if (p < M * nsg) {
-            const int m = p / nsg, sg = p % nsg;
-            const uint4 *xv = reinterpret_cast<const uint4 *>(x + (size_t)m * H + sg * kSub);
-            float4 *xs4 = reinterpret_cast<float4 *>(sh.xs + (size_t)m * H);
+        if (it < total) {
+            const int m = it >> lpr, c = it & (per_row - 1);
+            uint32_t aw[4];
+            if (xtag) {
+                // the previous layer's output: tagged bf16 pairs
+                const uint64_t *xp = static_cast<const uint64_t *>(x) + (size_t)m * (H / 2) + 4 * c;
 #pragma unroll
-            for (int h = 0; h < 2; ++h) {
-                const uint4 a = __ldcg(xv + h);
-                const uint32_t aw[4] = {a.x, a.y, a.z, a.w};
-                float f[8];
-#pragma unroll
-                for (int j = 0; j < 4; ++j) {
-                    f[2 * j] = __uint_as_float(aw[j] << 16);
-                    f[2 * j + 1] = __uint_as_float(aw[j] & 0xFFFF0000u);
-                }
-#pragma unroll
-                for (int j = 0; j < 8; ++j) ss = fmaf(f[j], f[j], ss);
-                if (stage) {
-                    xs4[arr_index(sg, 2 * h, LPR)] = make_float4(f[0], f[1], f[2], f[3]);
-                    xs4[arr_index(sg, 2 * h + 1, LPR)] = make_float4(f[4], f[5], f[6], f[7]);
-                }
+                for (int j = 0; j < 4; ++j) aw[j] = poll_tag(sh, xp + j, xtag, 40);
+            } else {
+                const uint4 a = __ldcg(reinterpret_cast<const uint4 *>(static_cast<const uint16_t *>(x) + (size_t)m * H) + c);
+                aw[0] = a.x; aw[1] = a.y; aw[2] = a.z; aw[3] = a.w;
             }
+            float f[8];
+#pragma unroll
+            for (int j = 0; j < 4; ++j) {
+                f[2 * j] = __uint_as_float(aw[j] << 16);
+                f[2 * j + 1] = __uint_as_float(aw[j] & 0xFFFF0000u);
+            }
+#pragma unroll
+            for (int j = 0; j < 8; ++j) ss = fmaf(f[j], f[j], ss);
+            // inputs 8c .. 8c+7: group c / 8, quads 2 (c % 8) and 2 (c % 8) + 1
+            const int g = c >> 3, t = (c & 7) * 2;
+            float4 *row = sh.xs + (size_t)m * (H / 4);
+            row[t * G + g] = make_float4(f[0], f[1], f[2], f[3]);
+            row[(t + 1) * G + g] = make_float4(f[4], f[5], f[6], f[7]);
         }
-        // sum over the `width` lanes that share a row chunk
-        for (int o = width / 2; o >= 1; o >>= 1) ss += __shfl_xor_sync(FULLMASK, ss, o);
-        if (p < M * nsg && (lane % width) == 0) {
-            const int m = p / nsg, chunk = (p % nsg) / width;
-            sh.red[m * kRedChunks + chunk] = ss;
-        }
+        ss = warp_sum(ss);
+        const int wfirst = base + warp * 32;
+        if (lane == 0 && wfirst < total) sh.red[(wfirst >> lpr) * (NCW + 1) + warp] += ss;
     }
     cbar();
     if (tid < M) {
         float t = 0.f;
-        for (int c = 0; c < chunks; ++c) t += sh.red[tid * kRedChunks + c];
-        sh.red[kMaxRows * kRedChunks + tid] = rsqrtf(t / (float)H + kp.g.eps);
+        for (int w = 0; w < NCW; ++w) t += sh.red[tid * (NCW + 1) + w];
+        sh.red[tid * (NCW + 1) + NCW] = rsqrtf(t / (float)H + kp.g.eps);
     }
     cbar();
-}
-
-// hn = x * rinv * gamma in the arranged layout, with per-16 sums.
-__device__ void build_hn(const KParams &kp, const Sh &sh, const uint16_t *x, const uint16_t *gamma)
-{
-    const int H = kp.g.H, M = kp.M, tid = threadIdx.x;
-    rms_rows(kp, sh, x, true);
-    const int nsg = H / kSub, LPR = lanes_per_row(H);
-    for (int p = tid; p < M * nsg; p += NCT) {
-        const int m = p / nsg, sg = p % nsg;
-        const float rinv = sh.red[kMaxRows * kRedChunks + m];
-        const uint4 *gv = reinterpret_cast<const uint4 *>(gamma + sg * kSub);
-        float4 *xs4 = reinterpret_cast<float4 *>(sh.xs + (size_t)m * H);
-        float s = 0.f;
+    // pass 2: scale by rinv * gamma * 2^100; group sums of hn
+    for (int base = 0; base < total; base += NCT) {
+        const int it = base + tid;
+        float gs = 0.f;
+        if (it < total) {
+            const int m = it >> lpr, c = it & (per_row - 1);
+            const float rinv = sh.red[m * (NCW + 1) + NCW];
+            const uint4 gv = *reinterpret_cast<const uint4 *>(gamma + c * 8);
+            const uint32_t gw[4] = {gv.x, gv.y, gv.z, gv.w};
+            const int g = c >> 3, t = (c & 7) * 2;
+            float4 *row = sh.xs + (size_t)m * (H / 4);
+            const float4 a = row[t * G + g], b = row[(t + 1) * G + g];
+            float h[8] = {a.x, a.y, a.z, a.w, b.x, b.y, b.z, b.w};
 #pragma unroll
-        for (int h = 0; h < 2; ++h) {
-            const uint4 g = __ldg(gv + h);
-            const uint32_t gw[4] = {g.x, g.y, g.z, g.w};
-            float4 a = xs4[arr_index(sg, 2 * h, LPR)], b = xs4[arr_index(sg, 2 * h + 1, LPR)];
-            a.x = a.x * rinv * __uint_as_float(gw[0] << 16);
-            a.y = a.y * rinv * __uint_as_float(gw[0] & 0xFFFF0000u);
-            a.z = a.z * rinv * __uint_as_float(gw[1] << 16);
-            a.w = a.w * rinv * __uint_as_float(gw[1] & 0xFFFF0000u);
-            b.x = b.x * rinv * __uint_as_float(gw[2] << 16);
-            b.y = b.y * rinv * __uint_as_float(gw[2] & 0xFFFF0000u);
-            b.z = b.z * rinv * __uint_as_float(gw[3] << 16);
-            b.w = b.w * rinv * __uint_as_float(gw[3] & 0xFFFF0000u);
-            s += ((a.x + a.y) + (a.z + a.w)) + ((b.x + b.y) + (b.z + b.w));
-            xs4[arr_index(sg, 2 * h, LPR)] = a;
-            xs4[arr_index(sg, 2 * h + 1, LPR)] = b;
+            for (int j = 0; j < 4; ++j) {
+                h[2 * j] = h[2 * j] * rinv * __uint_as_float(gw[j] << 16);
+                h[2 * j + 1] = h[2 * j + 1] * rinv * __uint_as_float(gw[j] & 0xFFFF0000u);
+            }
+#pragma unroll
+            for (int j = 0; j < 8; ++j) gs += h[j];
+            row[t * G + g] = make_float4(h[0] * kXScale, h[1] * kXScale, h[2] * kXScale, h[3] * kXScale);
+            row[(t + 1) * G + g] = make_float4(h[4] * kXScale, h[5] * kXScale, h[6] * kXScale, h[7] * kXScale);
         }
-        sh.xsum[m * nsg + sg] = s;
+        // 8 consecutive items make a group
+        gs += __shfl_xor_sync(FULLMASK, gs, 4);
+        gs += __shfl_xor_sync(FULLMASK, gs, 2);
+        gs += __shfl_xor_sync(FULLMASK, gs, 1);
+        if (it < total && (it & 7) == 0) {
+            const int m = it >> lpr, c = it & (per_row - 1);
+            sh.xsum[m * G + (c >> 3)] = gs;
+        }
     }
     for (int e = tid; e < kp.g.E; e += NCT) sh.emask[e] = 0u;
     cbar();
 }
 
+// Activations (fp32 rows in global memory) of `n` staged pairs: pair p =
+// src(p)[0 .. K), arranged, * 2^100, with group sums.  A thread item is 4
+// consecutive inputs; 16 items make a group.
+// Threads [t0, t0 + nt) of the compute warps take part (whole warps).  The
+// sources are tagged fp32 words; each is waited for until it carries `tag`.
+template <typename F>
+__device__ __forceinline__ void stage_acts(const Sh &sh, int n, int K, int t0, int nt, unsigned tag, F &&src)
+{
+    const int per = K / 4, lgp = ilog2(per), G = K / kGroup, total = n * per, tid = threadIdx.x - t0;
+    for (int base = 0; base < total; base += nt) {
+        const int it = base + tid;
+        float gs = 0.f;
+        if (it < total) {
+            const int p = it >> lgp, c = it & (per - 1);
+            const uint64_t *sp = src(p) + 4 * c;
+            float4 v;
+            v.x = __uint_as_float(poll_tag(sh, sp, tag, 41));
+            v.y = __uint_as_float(poll_tag(sh, sp + 1, tag, 41));
+            v.z = __uint_as_float(poll_tag(sh, sp + 2, tag, 41));
+            v.w = __uint_as_float(poll_tag(sh, sp + 3, tag, 41));
+            gs = (v.x + v.y) + (v.z + v.w);
+            sh.act[(size_t)p * per + (c & 15) * G + (c >> 4)] =
+                make_float4(v.x * kXScale, v.y * kXScale, v.z * kXScale, v.w * kXScale);
+        }
+#pragma unroll
+        for (int o = 8; o >= 1; o >>= 1) gs += __shfl_xor_sync(FULLMASK, gs, o);
+        if (it < total && (it & 15) == 0) {
+            const int p = it >> lgp, c = it & (per - 1);
+            sh.asum[p * G + (c >> 4)] = gs;
+        }
+    }
+}
+
 // ------------------------------------------------------------- R: routing
 
-// Order-preserving map of a float to an unsigned key (larger float, larger key).
+// Order-preserving map of a float to an unsigned key (larger float, larger
+// key) and back.
 __device__ __forceinline__ uint32_t fkey(float v)
 {
     const uint32_t u = __float_as_uint(v);
     return (u & 0x80000000u) ? ~u : (u | 0x80000000u);
 }
+__device__ __forceinline__ float unkey(uint32_t k)
+{
+    return __uint_as_float((k & 0x80000000u) ? (k & 0x7FFFFFFFu) : ~k);
+}
 
 // Top-k of one row by a warp, keyed on (logit descending, expert id
-// ascending).  T = the k-th largest of the 32 lane maxima (a lower bound of
-// the k-th largest logit) by an MSB-first radix search with ballots; the
-// candidates at or above T (at least k of them) go to shared memory and are
-// ranked exactly.  No step depends on a chain of shuffles.
+// ascending): k rounds of the warp-wide best (redux.sync) of the lanes'
+// best remaining logits, the winning lane dropping it.  Exact ties between
+// lanes go to the lower expert id.  Needs k <= NPL.
 template <int NPL>
-__device__ void topk_row_t(const KParams &kp, const Sh &sh, int m, const float *logits)
+__device__ __noinline__ void topk_row_t(const KParams &kp, const Sh &sh, int m, const uint64_t *logits, unsigned tag)
 {
     const int lane = threadIdx.x & 31;
     const int E = kp.g.E, k = kp.g.k, Er = kp.g.Er;
-    float v[NPL];
+    uint32_t key[NPL];
 #pragma unroll
     for (int i = 0; i < NPL; ++i) {
         const int e = lane + 32 * i;
-        v[i] = e < E ? __ldcg(logits + (size_t)m * Er + e) : -FLT_MAX;
+        key[i] = e < E ? fkey(__uint_as_float(poll_tag(sh, logits + (size_t)m * Er + e, tag, 42))) : 0u;
     }
-    const float lsg = kp.g.has_shared ? __ldcg(logits + (size_t)m * Er + E) : 0.f;
-    float bv = v[0];
+    const float lsg = kp.g.has_shared ? __uint_as_float(poll_tag(sh, logits + (size_t)m * Er + E, tag, 42)) : 0.f;
+    uint32_t rk = 0u;   // this lane's entry of the result: round r == lane
+    int re = 0;
+#pragma unroll 1
+    for (int r = 0; r < k; ++r) {
+        // the lane's best remaining key (max tree), then its lowest index
+        uint32_t t[NPL];
 #pragma unroll
-    for (int i = 1; i < NPL; ++i) bv = fmaxf(bv, v[i]);
-    // k-th largest lane maximum (ties counted with multiplicity)
-    const uint32_t key = (lane < E) ? fkey(bv) : 0u;
-    uint32_t prefix = 0;
+        for (int i = 0; i < NPL; ++i) t[i] = key[i];
 #pragma unroll
-    for (int b = 31; b >= 0; --b) {
-        const uint32_t trial = prefix | (1u << b);
-        if (__popc(__ballot_sync(FULLMASK, key >= trial)) >= k) prefix = trial;
-    }
-    // candidates: every logit >= T; at least k of them
-    unsigned bal[NPL];
-    int C = 0;
+        for (int w = NPL >> 1; w > 0; w >>= 1)
 #pragma unroll
-    for (int i = 0; i < NPL; ++i) {
-        bal[i] = __ballot_sync(FULLMASK, lane + 32 * i < E && fkey(v[i]) >= prefix);
-        C += __popc(bal[i]);
-    }
-    float *topv = sh.topv + m * kMaxK;
-    int *tope = sh.tope + m * kMaxK;
-    if (C <= kCandCap) {
-        float *cv = sh.cand_v + m * kCandCap;
-        int *ce = sh.cand_e + m * kCandCap;
-        int base = 0;
+            for (int i = 0; i < w; ++i) t[i] = max(t[i], t[i + w]);
+        const uint32_t bk = t[0];
+        int bi = NPL - 1;
 #pragma unroll
-        for (int i = 0; i < NPL; ++i) {
-            if ((bal[i] >> lane) & 1u) {
-                const int pos = base + __popc(bal[i] & ((1u << lane) - 1u));
-                cv[pos] = v[i];
-                ce[pos] = lane + 32 * i;
-            }
-            base += __popc(bal[i]);
-        }
-        __syncwarp();
-        for (int c = lane; c < C; c += 32) {
-            const float a = cv[c];
-            const int ea = ce[c];
-            int r = 0;
-            for (int c2 = 0; c2 < C; ++c2) {
-                const float b = cv[c2];
-                r += (b > a || (b == a && ce[c2] < ea)) ? 1 : 0;
-            }
-            if (r < k) { topv[r] = a; tope[r] = ea; }
-        }
-    } else {
-        // many ties at the threshold: k rounds of warp arg-max (exact)
-        unsigned taken = 0;
-        for (int r = 0; r < k; ++r) {
-            float lv = -FLT_MAX;
-            int le = 0x7fffffff, li = -1;
+        for (int i = NPL - 2; i >= 0; --i) bi = key[i] == bk ? i : bi;
+        const uint32_t wk = __reduce_max_sync(FULLMASK, bk);
+        const unsigned bal = __ballot_sync(FULLMASK, bk == wk);
+        const int mye = lane + 32 * bi;
+        const int we = __popc(bal) == 1 ? __shfl_sync(FULLMASK, mye, __ffs(bal) - 1)
+                                        : (int)__reduce_min_sync(FULLMASK, bk == wk ? (unsigned)mye : 0xFFFFFFFFu);
+        if (lane == r) { rk = wk; re = we; }
+        if (mye == we) {
 #pragma unroll
-            for (int i = 0; i < NPL; ++i) {
-                const int e = lane + 32 * i;
-                if (e < E && !(taken >> i & 1u) && (v[i] > lv || (v[i] == lv && e < le))) { lv = v[i]; le = e; li = i; }
-            }
-            float gv = lv;
-            int ge = le;
-#pragma unroll
-            for (int o = 16; o >= 1; o >>= 1) {
-                const float ov = __shfl_xor_sync(FULLMASK, gv, o);
-                const int oe = __shfl_xor_sync(FULLMASK, ge, o);
-                if (ov > gv || (ov == gv && oe < ge)) { gv = ov; ge = oe; }
-            }
-            if (ge == le && li >= 0) taken |= 1u << li;
-            if (lane == 0) { topv[r] = gv; tope[r] = ge < E ? ge : 0; }
+            for (int i = 0; i < NPL; ++i) key[i] = i == bi ? 0u : key[i];
         }
     }
-    __syncwarp();
     // renormalised softmax weights over the k kept logits (the full softmax
     // probabilities divided by their top-k sum)
+    const float vmax = unkey(__shfl_sync(FULLMASK, rk, 0));
+    const float ev = lane < k ? expf(unkey(rk) - vmax) : 0.f;
+    const float z = warp_sum(ev);
+    // rank of the lane's expert id among the k kept ones
+    int r = 0;
+#pragma unroll
+    for (int j = 0; j < NPL; ++j) {
+        const int ej = __shfl_sync(FULLMASK, re, j);
+        r += (j < k && ej < re) ? 1 : 0;
+    }
+    if (lane < k) {
+        const float wv = ev / z;
+        sh.topv[m * kMaxK + lane] = unkey(rk);
+        sh.tope[m * kMaxK + lane] = re;
+        sh.topw[m * kMaxK + lane] = wv;
+        // the same k entries ordered by expert id (combine order of the row)
+        sh.row_w[m * kMaxK + r] = wv;
+        sh.row_pair[m * kMaxK + r] = re;   // expert id for now; pair index after the slot list
+    }
+    if (lane == 0) sh.sigma[m] = kp.g.has_shared ? 1.0f / (1.0f + expf(-lsg)) : 0.f;
+}
+
+// k larger than a lane's share of the logits: k rounds of a warp-wide max
+// (redux.sync) of the lanes' best remaining keys, the lowest expert id
+// breaking exact ties.
+template <int NPL>
+__device__ __noinline__ void topk_row_rounds(const KParams &kp, const Sh &sh, int m, const uint64_t *logits, unsigned tag)
+{
+    const int lane = threadIdx.x & 31;
+    const int E = kp.g.E, k = kp.g.k, Er = kp.g.Er;
+    uint32_t key[NPL];
+#pragma unroll
+    for (int i = 0; i < NPL; ++i) {
+        const int e = lane + 32 * i;
+        key[i] = e < E ? fkey(__uint_as_float(poll_tag(sh, logits + (size_t)m * Er + e, tag, 42))) : 0u;
+    }
+    const float lsg = kp.g.has_shared ? __uint_as_float(poll_tag(sh, logits + (size_t)m * Er + E, tag, 42)) : 0.f;
+    float *topv = sh.topv + m * kMaxK;
+    int *tope = sh.tope + m * kMaxK;
+#pragma unroll 1
+    for (int r = 0; r < k; ++r) {
+        uint32_t bk = key[0];
+        int bi = 0;
+#pragma unroll
+        for (int i = 1; i < NPL; ++i)
+            if (key[i] > bk) { bk = key[i]; bi = i; }
+        const uint32_t wk = __reduce_max_sync(FULLMASK, bk);
+        const unsigned bal = __ballot_sync(FULLMASK, bk == wk);
+        const unsigned mye = (unsigned)(lane + 32 * bi);
+        unsigned we;
+        if (__popc(bal) == 1) we = __shfl_sync(FULLMASK, mye, __ffs(bal) - 1);
+        else we = __reduce_min_sync(FULLMASK, bk == wk ? mye : 0xFFFFFFFFu);
+        if (mye == we) {
+#pragma unroll
+            for (int i = 0; i < NPL; ++i)
+                if (i == bi) key[i] = 0u;
+        }
+        if (lane == 0) { topv[r] = unkey(wk); tope[r] = (int)we < E ? (int)we : 0; }
+    }
+    __syncwarp();
     const float vmax = topv[0];
     const float ev = lane < k ? expf(topv[lane] - vmax) : 0.f;
     const float z = warp_sum(ev);
     if (lane < k) {
         const float wv = ev / z;
         sh.topw[m * kMaxK + lane] = wv;
-        // the same k entries ordered by expert id (combine order of the row)
         const int e = tope[lane];
         int r = 0;
         for (int j = 0; j < k; ++j) r += tope[j] < e ? 1 : 0;
         sh.row_w[m * kMaxK + r] = wv;
-        sh.row_pair[m * kMaxK + r] = e;   // expert id for now; pair index after the slot list
+        sh.row_pair[m * kMaxK + r] = e;
     }
     if (lane == 0) sh.sigma[m] = kp.g.has_shared ? 1.0f / (1.0f + expf(-lsg)) : 0.f;
 }
 
-__device__ void topk_row(const KParams &kp, const Sh &sh, int m, const float *logits)
+__device__ void topk_row(const KParams &kp, const Sh &sh, int m, const uint64_t *logits, unsigned tag)
 {
     const int E = kp.g.E;
-    if (E <= 64) topk_row_t<2>(kp, sh, m, logits);
-    else if (E <= 256) topk_row_t<8>(kp, sh, m, logits);
-    else topk_row_t<16>(kp, sh, m, logits);
+    const int k = kp.g.k;
+    if (E <= 64 && k <= 2) topk_row_t<2>(kp, sh, m, logits, tag);
+    else if (E <= 256 && k <= 8) topk_row_t<8>(kp, sh, m, logits, tag);
+    else if (k <= 16) topk_row_t<16>(kp, sh, m, logits, tag);
+    else topk_row_rounds<16>(kp, sh, m, logits, tag);
 }
 
-__device__ void route(const KParams &kp, const Sh &sh, const float *logits, int l)
+// Named barrier over the first nw compute warps (the routing warps).
+__device__ __forceinline__ void rbar(int nw) { asm volatile("bar.sync 2, %0;" ::"r"(nw * 32) : "memory"); }
+
+// Routing, run by the first max(M, 1) compute warps only (one per token
+// row); the other warps work meanwhile.  Ends by telling the producer that
+// the slot table of layer l is ready.
+__device__ void route(const KParams &kp, const Sh &sh, const uint64_t *logits, int l)
 {
+    const unsigned tag = layer_tag(kp, l);
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     const int E = kp.g.E, k = kp.g.k, M = kp.M;
     if (M == 1) {
         // one row: the slots are its k experts in id order
-        if (warp == 0) {
-            topk_row(kp, sh, 0, logits);
-            if (threadIdx.x == 0) stamp(kp, l, 12);
-            __syncwarp();
-            if (lane < k) {
-                const int e = sh.row_pair[lane];
-                sh.slot_e[lane] = e;
-                sh.slot_mask[lane] = 1u;
-                sh.slot_rowbase[lane] = lane;
-                sh.row_pair[lane] = lane;
-                if (kp.mode == kModeRouter && blockIdx.x == 0) {
-                    kp.idx_out[lane] = sh.tope[lane];
-                    kp.w_out[lane] = sh.topw[lane];
-                }
-            }
-            if (lane == 0) {
-                sh.flags[1] = k;
-                sh.slot_rowbase[k] = k;
-                stamp(kp, l, 13);
-            }
-            for (int t = lane; t < k; t += 32) sh.target[t] += (unsigned)kp.g.I;
-        }
-        cbar();
-        return;
-    }
-    if (warp < M) topk_row(kp, sh, warp, logits);
-    if (threadIdx.x == 0) stamp(kp, l, 12);
-    cbar();
-    if (warp == 0) {
-        for (int t = lane; t < M * k; t += 32) {
-            const int e = sh.tope[(t / k) * kMaxK + t % k];
-            atomicOr(&sh.emask[e < E ? e : 0], 1u << (t / k));
-        }
+        topk_row(kp, sh, 0, logits, tag);
+        if (threadIdx.x == 0) stamp(kp, l, 12);
         __syncwarp();
-        int base = 0;
-        for (int c0 = 0; c0 < E; c0 += 32) {
-            const int e = c0 + lane;
-            const uint32_t mk = e < E ? sh.emask[e] : 0u;
-            const unsigned bal = __ballot_sync(FULLMASK, mk != 0u);
-            if (mk) {
-                const int pos = base + __popc(bal & ((1u << lane) - 1u));
-                sh.slot_e[pos] = e;
-                sh.slot_mask[pos] = mk;
-                sh.eslot[e] = pos;
+        if (lane < k) {
+            const int e = sh.row_pair[lane];
+            sh.slot_e[lane] = e;
+            sh.slot_mask[lane] = 1u;
+            sh.slot_rowbase[lane] = lane;
+            sh.row_pair[lane] = lane;
+            if (kp.mode == kModeRouter && blockIdx.x == 0) {
+                kp.idx_out[lane] = sh.tope[lane];
+                kp.w_out[lane] = sh.topw[lane];
             }
-            base += __popc(bal);
-        }
-        __syncwarp();
-        // slot-row pair bases: prefix sums of popc(mask) over the slots
-        int run = 0;
-        for (int s0 = 0; s0 < base; s0 += 32) {
-            const int s = s0 + lane;
-            const int pc = s < base ? __popc(sh.slot_mask[s]) : 0;
-            int inc = pc;
-#pragma unroll
-            for (int o = 1; o < 32; o <<= 1) {
-                const int t = __shfl_up_sync(FULLMASK, inc, o);
-                if (lane >= o) inc += t;
-            }
-            if (s < base) sh.slot_rowbase[s] = run + inc - pc;
-            run += __shfl_sync(FULLMASK, inc, 31);
         }
         if (lane == 0) {
-            sh.flags[1] = base;
-            sh.slot_rowbase[base] = run;
+            sh.flags[1] = k;
+            sh.slot_rowbase[k] = k;
+            stamp(kp, l, 13);
         }
-        for (int t = lane; t < base; t += 32) sh.target[t] += (unsigned)kp.g.I;
+        for (int t = lane; t < k; t += 32) sh.target[t] += (unsigned)kp.g.I;
         __syncwarp();
-        for (int t = lane; t < M * k; t += 32) {
-            const int m = t / k, j = t % k;
-            const int e = sh.row_pair[m * kMaxK + j];
-            const int s = sh.eslot[e < E ? e : 0];
-            sh.row_pair[m * kMaxK + j] = sh.slot_rowbase[s] + __popc(sh.slot_mask[s] & ((1u << m) - 1u));
-            if (kp.mode == kModeRouter && blockIdx.x == 0) {
-                kp.idx_out[m * k + j] = sh.tope[m * kMaxK + j];
-                kp.w_out[m * k + j] = sh.topw[m * kMaxK + j];
-            }
-        }
-        if (threadIdx.x == 0) stamp(kp, l, 13);
+        if (lane == 0 && kp.mode == kModeLayers) mbar_arrive(sh.route, 1);
+        return;
     }
-    cbar();
+    topk_row(kp, sh, warp, logits, tag);
+    if (threadIdx.x == 0) stamp(kp, l, 12);
+    rbar(M);
+    if (warp != 0) return;
+    for (int t = lane; t < M * k; t += 32) {
+        const int e = sh.tope[(t / k) * kMaxK + t % k];
+        atomicOr(&sh.emask[e < E ? e : 0], 1u << (t / k));
+    }
+    __syncwarp();
+    int base = 0;
+    for (int c0 = 0; c0 < E; c0 += 32) {
+        const int e = c0 + lane;
+        const uint32_t em = e < E ? sh.emask[e] : 0u;
+        const unsigned bal = __ballot_sync(FULLMASK, em != 0u);
+        if (em) {
+            const int pos = base + __popc(bal & ((1u << lane) - 1u));
+            sh.slot_e[pos] = e;
+            sh.slot_mask[pos] = em;
+            sh.eslot[e] = pos;
+        }
+        base += __popc(bal);
+    }
+    __syncwarp();
+    // slot-row pair bases: prefix sums of popc(mask) over the slots
+    int run = 0;
+    for (int s0 = 0; s0 < base; s0 += 32) {
+        const int s = s0 + lane;
+        const int pc = s < base ? __popc(sh.slot_mask[s]) : 0;
+        int inc = pc;
+#pragma unroll
+        for (int o = 1; o < 32; o <<= 1) {
+            const int t = __shfl_up_sync(FULLMASK, inc, o);
+            if (lane >= o) inc += t;
+        }
+        if (s < base) sh.slot_rowbase[s] = run + inc - pc;
+        run += __shfl_sync(FULLMASK, inc, 31);
+    }
+    if (lane == 0) {
+        sh.flags[1] = base;
+        sh.slot_rowbase[base] = run;
+    }
+    for (int t = lane; t < base; t += 32) sh.target[t] += (unsigned)kp.g.I;
+    __syncwarp();
+    for (int t = lane; t < M * k; t += 32) {
+        const int m = t / k, j = t % k;
+        const int e = sh.row_pair[m * kMaxK + j];
+        const int s = sh.eslot[e < E ? e : 0];
+        sh.row_pair[m * kMaxK + j] = sh.slot_rowbase[s] + __popc(sh.slot_mask[s] & ((1u << m) - 1u));
+        if (kp.mode == kModeRouter && blockIdx.x == 0) {
+            kp.idx_out[m * k + j] = sh.tope[m * kMaxK + j];
+            kp.w_out[m * k + j] = sh.topw[m * kMaxK + j];
+        }
+    }
+    if (threadIdx.x == 0) stamp(kp, l, 13);
+    __syncwarp();
+    if (lane == 0 && kp.mode == kModeLayers) mbar_arrive(sh.route, 1);
 }
 
 // ---------------------------------------------------------- workspace views
 
+// Workspace buffers shared between CTAs, all of tagged words.
 struct Ws {
-    float *logits;   // [maxr][Er]
-    float *act;      // [max_slots][maxr][I]
-    float *act_s;    // [maxr][Is]
-    uint16_t *ping[2];
+    uint64_t *logits;   // [maxr][Er] fp32
+    uint64_t *act;      // [max_slots][maxr][I] fp32
+    uint64_t *act_s;    // [maxr][Is] fp32
+    uint64_t *ping[2];  // [maxr][H / 2] bf16 pairs: outputs of the layers before the last
 };
 
 __device__ __forceinline__ Ws ws_views(const KParams &kp)
 {
     Ws w;
-    w.logits = reinterpret_cast<float *>(kp.ws + kp.ws_l.off_logits);
-    w.act = reinterpret_cast<float *>(kp.ws + kp.ws_l.off_act);
-    w.act_s = reinterpret_cast<float *>(kp.ws + kp.ws_l.off_act_s);
-    w.ping[0] = reinterpret_cast<uint16_t *>(kp.ws + kp.ws_l.off_ping);
-    w.ping[1] = w.ping[0] + (size_t)kp.ws_l.maxr * kp.g.H;
+    w.logits = reinterpret_cast<uint64_t *>(kp.ws + kp.ws_l.off_logits);
+    w.act = reinterpret_cast<uint64_t *>(kp.ws + kp.ws_l.off_act);
+    w.act_s = reinterpret_cast<uint64_t *>(kp.ws + kp.ws_l.off_act_s);
+    w.ping[0] = reinterpret_cast<uint64_t *>(kp.ws + kp.ws_l.off_ping);
+    w.ping[1] = w.ping[0] + (size_t)kp.ws_l.maxr * (kp.g.H / 2);
     return w;
 }
 
 // ------------------------------------------------------------- schedules
 
-// Stage schedule shared by the producer and the compute warps: `f` gets
-// (src, bytes, slot-or-kind, first, count) of each stage in order.
-template <typename F>
-__device__ __forceinline__ void sched_p1(const KParams &kp, const LayerPtrs &Lp, F &&f)
+// Prefetch buffer of one layer: gamma, this CTA's router rows, then as many
+// of its shared units as fit (the rest go through the ring as P1 stages).
+// Prefetch buffer of one layer: gamma, this CTA's router rows, the shared
+// expert's down rows of its output slice (when they fit) and as many of its
+// shared gate/up units as fit; the rest go through the ring.
+struct PbPlan {
+    int ra, rb;        // router rows
+    int ua, ub;        // shared units of this CTA
+    int upb;           // units held in the buffer: [ua, ua + upb)
+    int h0, nh;        // output slice (shared down rows h0 .. h0 + nh)
+    int dpb;           // shared down rows held in the buffer: nh or 0
+    int off_router, off_sdown, off_units, bytes;
+};
+
+__device__ __forceinline__ PbPlan pb_plan(const KParams &kp)
 {
     const Geo &g = kp.g;
-    const int P = gridDim.x, c = blockIdx.x, S = kp.p.S;
-    int a, b;
-    split(g.Er, P, c, a, b);
-    const int cr = S / g.rr_bytes;
-    for (int r = a; r < b; r += cr) {
-        const int n = min(cr, b - r);
-        f(Lp.router + (size_t)r * g.rr_bytes, n * g.rr_bytes, 0, r, n);
-    }
-    if (kp.mode == kModeLayers && g.has_shared) {
-        split(g.Is, P, c, a, b);
-        const int ub = 2 * g.sg_bytes;
-        const int cu = max(1, min(S / ub, (b - a + NCW - 1) / NCW));
-        for (int j = a; j < b; j += cu) {
-            const int n = min(cu, b - j);
-            f(Lp.sgu + (size_t)j * ub, n * ub, 1, j, n);
-        }
+    PbPlan b;
+    split(g.Er, gridDim.x, blockIdx.x, b.ra, b.rb);
+    int h1;
+    hslice(g.H, b.h0, h1);
+    b.nh = h1 - b.h0;
+    b.ua = b.ub = 0;
+    const bool sh_on = kp.mode == kModeLayers && g.has_shared;
+    if (sh_on) split(g.Is, gridDim.x, blockIdx.x, b.ua, b.ub);
+    b.off_router = (int)align_up((size_t)g.H * 2, 16);
+    b.off_sdown = b.off_router + (b.rb - b.ra) * g.rr_bytes;
+    b.dpb = sh_on && b.off_sdown + b.nh * g.sd_bytes <= kp.p.pb_bytes ? b.nh : 0;
+    b.off_units = b.off_sdown + b.dpb * g.sd_bytes;
+    const int ub2 = 2 * g.sg_bytes;
+    const int room = kp.p.pb_bytes - b.off_units;
+    b.upb = ub2 > 0 ? min(b.ub - b.ua, max(0, room / ub2)) : 0;
+    b.bytes = b.off_units + b.upb * ub2;
+    return b;
+}
+
+// Ring stages of a layer, in order: P1 units that did not fit the prefetch
+// buffer, P1b shared down rows, P2 routed gate/up units, P3 routed down
+// rows.  `f` gets (src, bytes, slot-or-kind, first, count).
+// The P1 overflow is counted in shared-expert rows (row 2u is the gate row
+// of unit u, row 2u + 1 its up row); `first` is relative to the CTA's rows.
+template <typename F>
+__device__ __forceinline__ void sched_p1x(const KParams &kp, const LayerPtrs &Lp, F &&f)
+{
+    const Geo &g = kp.g;
+    if (kp.mode != kModeLayers || !g.has_shared || g.sg_bytes == 0) return;
+    const PbPlan b = pb_plan(kp);
+    const int cr = max(1, kp.p.S / g.sg_bytes);
+    for (int r = 2 * (b.ua + b.upb); r < 2 * b.ub; r += cr) {
+        const int n = min(cr, 2 * b.ub - r);
+        f(Lp.sgu + (size_t)r * g.sg_bytes, n * g.sg_bytes, -2, r - 2 * b.ua, n);
     }
 }
 
+// Shared down rows that did not fit the prefetch buffer.
 template <typename F>
 __device__ __forceinline__ void sched_p1b(const KParams &kp, const LayerPtrs &Lp, F &&f)
 {
     const Geo &g = kp.g;
     if (kp.mode != kModeLayers || !g.has_shared) return;
-    int h0, h1;
-    split(g.H, gridDim.x, blockIdx.x, h0, h1);
-    const int nh = h1 - h0;
-    const int cd = max(1, min(kp.p.S / g.sd_bytes, (nh + 6) / 7));
-    for (int r = 0; r < nh; r += cd) {
-        const int n = min(cd, nh - r);
-        f(Lp.sdown + (size_t)(h0 + r) * g.sd_bytes, n * g.sd_bytes, -1, r, n);
+    const PbPlan b = pb_plan(kp);
+    if (b.dpb) return;
+    const int cd = max(1, min(kp.p.S / g.sd_bytes, (b.nh + 1) / 2));
+    for (int r = 0; r < b.nh; r += cd) {
+        const int n = min(cd, b.nh - r);
+        f(Lp.sdown + (size_t)(b.h0 + r) * g.sd_bytes, n * g.sd_bytes, -1, r, n);
     }
 }
 
@@ -1147,6 +1386,8 @@ __device__ __forceinline__ void sched_p2(const KParams &kp, const Sh &sh, const 
     const int ub = 2 * g.g_bytes;
     int a, b;
     split(U * g.I, gridDim.x, blockIdx.x, a, b);
+    // about one stage per compute warp, an even number of units (a lane
+    // takes two at a time) where the stage size allows
     const int cu = max(1, min(kp.p.S / ub, 2 * ((b - a + 2 * NCW - 1) / (2 * NCW))));
     for (int n = a; n < b;) {
         const int s = n / g.I, j = n % g.I;
@@ -1162,12 +1403,11 @@ __device__ __forceinline__ void sched_p3(const KParams &kp, const Sh &sh, const 
     const Geo &g = kp.g;
     const int U = sh.flags[1];
     int h0, h1;
-    split(g.H, gridDim.x, blockIdx.x, h0, h1);
+    hslice(g.H, h0, h1);
     const int nh = h1 - h0;
-    const int pieces = max(1, (NCW + U - 1) / max(1, U));
-    int cd = max(1, min(kp.p.S / g.d_bytes, (nh + pieces - 1) / pieces));
-    if (cd > 1 && (cd & 1)) ++cd;
-    cd = min(cd, kp.p.S / g.d_bytes);
+    // about one stage per compute warp over the layer
+    const int per_slot = max(1, (NCW + U - 1) / max(1, U));
+    const int cd = max(1, min(kp.p.S / g.d_bytes, (nh + per_slot - 1) / per_slot));
     for (int s = 0; s < U; ++s) {
         const int e = sh.slot_e[s];
         for (int r = 0; r < nh; r += cd) {
@@ -1192,7 +1432,7 @@ __device__ __forceinline__ bool issue(const Sh &sh, unsigned q, const uint8_t *s
     return true;
 }
 
-__device__ __forceinline__ void producer(const KParams &kp, const Sh &sh, int lane)
+__device__ __forceinline__ void ring_producer(const KParams &kp, const Sh &sh, int lane)
 {
     unsigned q = 0;
     bool ok = true;
@@ -1200,17 +1440,19 @@ __device__ __forceinline__ void producer(const KParams &kp, const Sh &sh, int la
         if (ok && (int)(q % NP) == lane) ok = issue(sh, q, src, bytes);
         ++q;
     };
-    for (int l = 0; l < kp.L && ok; ++l) {
-        const LayerPtrs &Lp = kp.layer[l];
-        sched_p1(kp, Lp, each);
-        sched_p1b(kp, Lp, each);
-        if (!ok || kp.mode == kModeRouter) break;
-        if (lane == 0) stamp(kp, l, 9);
-        if (!wait_bar(sh, sh.route, (unsigned)l & 1u, 2)) break;
-        if (lane == 0) stamp(kp, l, 10);
-        sched_p2(kp, sh, Lp, each);
-        sched_p3(kp, sh, Lp, each);
-        if (lane == 0) stamp(kp, l, 11);
+    if (kp.mode == kModeLayers) {
+        for (int l = 0; l < kp.L && ok; ++l) {
+            const LayerPtrs &Lp = kp.layer[l];
+            sched_p1x(kp, Lp, each);
+            if (!ok) break;
+            if (lane == 0) stamp(kp, l, 9);
+            if (!wait_bar(sh, sh.route, (unsigned)l & 1u, 2)) break;
+            if (lane == 0) stamp(kp, l, 10);
+            sched_p2(kp, sh, Lp, each);
+            sched_p1b(kp, Lp, each);
+            sched_p3(kp, sh, Lp, each);
+            if (lane == 0) stamp(kp, l, 11);
+        }
     }
     // Let this lane's copies still in flight land before the CTA can exit.
     const unsigned first = q > (unsigned)sh.NS ? q - (unsigned)sh.NS : 0u;
@@ -1219,6 +1461,39 @@ __device__ __forceinline__ void producer(const KParams &kp, const Sh &sh, int la
         const int slot = (int)(t % (unsigned)sh.NS);
         const unsigned long long t0 = now_ns();
         while (!mbar_try_wait(&sh.full[slot], (t / (unsigned)sh.NS) & 1u))
+            if (now_ns() - t0 > (unsigned long long)sh.timeout_ns) break;
+    }
+}
+
+// The prefetch lane: layer l's buffer is loaded once every compute warp is
+// done with layer l - 1's P1.
+__device__ __forceinline__ void pb_producer(const KParams &kp, const Sh &sh)
+{
+    const Geo &g = kp.g;
+    const PbPlan b = pb_plan(kp);
+    int issued = 0;
+    for (int l = 0; l < kp.L; ++l) {
+        if (l > 0 && !wait_bar(sh, sh.pb_empty, (unsigned)(l - 1) & 1u, 3)) break;
+        if (aborted(sh)) break;
+        const LayerPtrs &Lp = kp.layer[l];
+        mbar_expect_tx(sh.pb_full, (unsigned)b.bytes);
+        bulk_load(sh.pb, Lp.gamma, (unsigned)(g.H * 2), sh.pb_full);
+        if (b.rb > b.ra)
+            bulk_load(sh.pb + b.off_router, Lp.router + (size_t)b.ra * g.rr_bytes,
+                      (unsigned)((b.rb - b.ra) * g.rr_bytes), sh.pb_full);
+        if (b.dpb > 0)
+            bulk_load(sh.pb + b.off_sdown, Lp.sdown + (size_t)b.h0 * g.sd_bytes, (unsigned)(b.dpb * g.sd_bytes),
+                      sh.pb_full);
+        if (b.upb > 0)
+            bulk_load(sh.pb + b.off_units, Lp.sgu + (size_t)b.ua * 2 * g.sg_bytes,
+                      (unsigned)(b.upb * 2 * g.sg_bytes), sh.pb_full);
+        issued = l + 1;
+        if (kp.mode == kModeRouter) break;
+    }
+    // the last buffer issued must land before the CTA can exit
+    if (issued > 0) {
+        const unsigned long long t0 = now_ns();
+        while (!mbar_try_wait(sh.pb_full, (unsigned)(issued - 1) & 1u))
             if (now_ns() - t0 > (unsigned long long)sh.timeout_ns) break;
     }
 }
@@ -1245,26 +1520,66 @@ __device__ __forceinline__ void consume(const Sh &sh, unsigned &q, int where, F 
     if ((threadIdx.x & 31) == 0) mbar_arrive(&sh.empty[slot], 1);
 }
 
-__device__ void phase1(const KParams &kp, const Sh &sh, const LayerPtrs &Lp, unsigned &q, const Ws &w)
+// P1: router rows and shared gate/up rows of this CTA from the prefetch
+// buffer (warp w takes rows w, w + NCW, ...), then any units that came
+// through the ring.  Router rows -> logits; shared units -> act_s.
+__device__ void phase1(const KParams &kp, const Sh &sh, const LayerPtrs &Lp, unsigned &q, const Ws &w, int l)
 {
     const Geo &g = kp.g;
     const uint32_t all = (1u << kp.M) - 1u;
-    sched_p1(kp, Lp, [&](const uint8_t *, int, int kind, int first, int n) {
+    const int warp = threadIdx.x >> 5, maxr = kp.p.maxr;
+    const PbPlan b = pb_plan(kp);
+    const int nr = b.rb - b.ra, nrows = nr + 2 * b.upb;
+    wstamp(kp, l, 14);
+    for (int i = warp; i < nrows; i += NCW) {
+        if (i < nr) {
+            // (debug switch: one logit of layer 0 stays unpublished)
+            if (!(l == 0 && kp.skip_row == b.ra + i))
+                one_row(sh, g.H, g.qb, sh.pb + b.off_router + (size_t)i * g.rr_bytes, all, w.logits + b.ra + i, g.Er,
+                        layer_tag(kp, l));
+        } else {
+            const int j = i - nr;   // gate row of unit j / 2, or its up row
+            one_row(sh, g.H, g.sb, sh.pb + b.off_units + (size_t)j * g.sg_bytes, all, sh.p1v + j * maxr, 1, 0u);
+        }
+    }
+    wstamp(kp, l, 15);
+    // rows past the buffer (large shared experts) come through the ring
+    sched_p1x(kp, Lp, [&](const uint8_t *, int, int, int first, int n) {
         consume(sh, q, 10, [&](const uint8_t *st) {
-            if (kind == 0) router_stage(sh, g.qb, st, n, g.rr_bytes, g.H, all, w.logits, g.Er, first);
-            else gu_stage(sh, g.sb, st, n, g.sg_bytes, g.H, all, w.act_s, g.Is, first);
+            for (int i = 0; i < n; ++i)
+                one_row(sh, g.H, g.sb, st + (size_t)i * g.sg_bytes, all, sh.p1v + (first + i) * maxr, 1, 0u);
         });
     });
+    cbar();
+    // SwiGLU of the CTA's units
+    for (int t = threadIdx.x; t < (b.ub - b.ua) * kp.M; t += NCT) {
+        const int u = t / kp.M, m = t % kp.M;
+        const float gt = sh.p1v[(2 * u) * maxr + m], up = sh.p1v[(2 * u + 1) * maxr + m];
+        st_tag(w.act_s + (size_t)m * g.Is + b.ua + u, __float_as_uint(gt / (1.0f + expf(-gt)) * up), layer_tag(kp, l));
+    }
 }
 
-__device__ void phase1b(const KParams &kp, const Sh &sh, const LayerPtrs &Lp, unsigned &q, const Ws &w, int l)
+// Shared down rows held in the prefetch buffer, by compute warps w0 .. NCW-1
+// in chunks of 8 rows.
+__device__ void shared_down_pb(const KParams &kp, const Sh &sh, int w0)
+{
+    const Geo &g = kp.g;
+    const uint32_t all = (1u << kp.M) - 1u;
+    const PbPlan b = pb_plan(kp);
+    const int warp = threadIdx.x >> 5;
+    for (int r0 = (warp - w0) * 8; r0 < b.dpb; r0 += (NCW - w0) * 8)
+        dn_rows(sh, g.sb, sh.pb + b.off_sdown + (size_t)r0 * g.sd_bytes, min(8, b.dpb - r0), g.sd_bytes, g.Is, all, 0,
+                sh.ysh + r0 * kMaxRows, kMaxRows, 1);
+}
+
+__device__ void phase1b(const KParams &kp, const Sh &sh, const LayerPtrs &Lp, unsigned &q, int l)
 {
     const Geo &g = kp.g;
     const uint32_t all = (1u << kp.M) - 1u;
     int tc = 0;
     sched_p1b(kp, Lp, [&](const uint8_t *, int, int, int first, int n) {
         consume(sh, q, 15, [&](const uint8_t *st) {
-            dn_stage(sh, g.sb, st, first, n, g.sd_bytes, g.Is, all, w.act_s, g.Is, true, 0);
+            dn_rows(sh, g.sb, st, n, g.sd_bytes, g.Is, all, 0, sh.ysh + first * kMaxRows, kMaxRows, 1);
         }, kp.trace ? &kp : nullptr, l, &tc, 11, 1);
     });
 }
@@ -1273,116 +1588,210 @@ __device__ void phase2(const KParams &kp, const Sh &sh, const LayerPtrs &Lp, uns
 {
     const Geo &g = kp.g;
     const int maxr = kp.ws_l.maxr;
+    const unsigned tag = layer_tag(kp, l);
     int tc = 0;
     sched_p2(kp, sh, Lp, [&](const uint8_t *, int, int s, int first, int n) {
         consume(sh, q, 20, [&](const uint8_t *st) {
-            gu_stage(sh, g.rb, st, n, g.g_bytes, g.H, sh.slot_mask[s], w.act + (size_t)s * maxr * g.I, g.I, first);
-            // publish: n more activation units of slot s are in global memory
-            // (the warp barrier orders every lane's stores before lane 0's release)
-            __syncwarp();
-            if ((threadIdx.x & 31) == 0) red_release_add(&sh.act_done[s], (unsigned)n);
+            uint64_t *act = w.act + (size_t)s * maxr * g.I;
+            gu_units(sh, g.H, g.rb, st, n, g.g_bytes, sh.slot_mask[s], act + first, g.I, tag);
         }, kp.trace ? &kp : nullptr, l, &tc, 2, 1);
     });
 }
 
-__device__ void phase3(const KParams &kp, const Sh &sh, const LayerPtrs &Lp, unsigned &q, const Ws &w, int l)
+// P3 in rounds of consecutive slots whose activation pairs fit the staging
+// buffer; the producer issued the down stages slot by slot, so the stages of
+// a round are consumed in issue order.
+__device__ bool phase3(const KParams &kp, const Sh &sh, const LayerPtrs &Lp, unsigned &q, const Ws &w, int l)
 {
     const Geo &g = kp.g;
-    const int maxr = kp.ws_l.maxr;
+    const int maxr = kp.ws_l.maxr, U = sh.flags[1];
     int tc = 0;
-    sched_p3(kp, sh, Lp, [&](const uint8_t *, int, int s, int first, int n) {
-        consume(sh, q, 30, [&](const uint8_t *st) {
-            if (!wait_count(sh, &sh.act_done[s], sh.target[s], 35)) return;
-            dn_stage(sh, g.rb, st, first, n, g.d_bytes, g.I, sh.slot_mask[s], w.act + (size_t)s * maxr * g.I, g.I,
-                     false, sh.slot_rowbase[s]);
-        }, kp.trace ? &kp : nullptr, l, &tc, 7, 1);
-    });
+    for (int s0 = 0; s0 < U;) {
+        int s1 = s0, pairs = 0;
+        while (s1 < U && pairs + __popc(sh.slot_mask[s1]) <= sh.act_pairs) pairs += __popc(sh.slot_mask[s1++]);
+        if (s1 == s0) s1 = s0 + 1;   // cannot happen: act_pairs >= maxr >= popc of any mask
+        const int pbase = sh.slot_rowbase[s0], npairs = sh.slot_rowbase[s1] - pbase;
+        // pair -> (slot, row) table of the round
+        if (threadIdx.x < 32) {
+            for (int s = s0 + (int)threadIdx.x; s < s1; s += 32) {
+                uint32_t mask = sh.slot_mask[s];
+                for (int p = sh.slot_rowbase[s] - pbase; mask; mask &= mask - 1, ++p)
+                    sh.pair_src[p] = s * kMaxRows + (__ffs(mask) - 1);
+            }
+        }
+        cbar();
+        // the round's activations, waited for word by word (tagged)
+        stage_acts(sh, npairs, g.I, 0, NCT, layer_tag(kp, l), [&](int p) -> const uint64_t * {
+            const int ps = sh.pair_src[p];
+            return w.act + ((size_t)(ps / kMaxRows) * maxr + ps % kMaxRows) * g.I;
+        });
+        if (cbar_or(aborted(sh))) return false;
+        sched_p3(kp, sh, Lp, [&](const uint8_t *, int, int s, int first, int n) {
+            if (s < s0 || s >= s1) return;
+            consume(sh, q, 30, [&](const uint8_t *st) {
+                const int pr = sh.slot_rowbase[s];
+                dn_rows(sh, g.rb, st, n, g.d_bytes, g.I, sh.slot_mask[s], pr - pbase,
+                        sh.ybuf + pr * sh.hrows + first, 1, sh.hrows);
+            }, kp.trace ? &kp : nullptr, l, &tc, 7, 1);
+        });
+        cbar();
+        s0 = s1;
+    }
+    return true;
 }
 
-// out = x + sum_j w_j y_j (expert-id order) + sigma y_shared, for this
-// CTA's outputs; thread t holds output (hl, m) = (t / M, t % M).
-__device__ void combine(const KParams &kp, const Sh &sh, float xres, uint16_t *xout)
+// out = x + sum_j w_j y_j (expert-id order) + sigma y_shared for this CTA's
+// outputs; thread t holds the row pair (2 pl, 2 pl + 1) of token row m,
+// t = pl * M + m, with residuals xr.  Outputs of layers before the last go
+// out as tagged bf16 pairs, the last one as plain bf16.
+__device__ void combine(const KParams &kp, const Sh &sh, const float (&xr)[2], uint64_t *tagged, unsigned tag,
+                        uint16_t *plain)
 {
     const Geo &g = kp.g;
     const int M = kp.M, k = g.k, t = threadIdx.x;
     int h0, h1;
-    split(g.H, gridDim.x, blockIdx.x, h0, h1);
-    const int nh = h1 - h0;
-    if (t < nh * M) {
-        const int hl = t / M, m = t % M;
-        float acc = 0.f;
-        for (int j = 0; j < k; ++j)
-            acc = fmaf(sh.row_w[m * kMaxK + j], sh.ybuf[sh.row_pair[m * kMaxK + j] * sh.hrows + hl], acc);
-        if (g.has_shared) acc = fmaf(sh.sigma[m], sh.ysh[hl * kMaxRows + m], acc);
-        xout[(size_t)m * g.H + h0 + hl] = f2bf(xres + acc);
+    hslice(g.H, h0, h1);
+    const int np = (h1 - h0) / 2;
+    if (t < np * M) {
+        const int pl = t / M, m = t % M;
+        uint32_t o[2];
+#pragma unroll
+        for (int hh = 0; hh < 2; ++hh) {
+            const int hl = 2 * pl + hh;
+            float acc = 0.f;
+            for (int j = 0; j < k; ++j)
+                acc = fmaf(sh.row_w[m * kMaxK + j], sh.ybuf[sh.row_pair[m * kMaxK + j] * sh.hrows + hl], acc);
+            if (g.has_shared) acc = fmaf(sh.sigma[m], sh.ysh[hl * kMaxRows + m], acc);
+            o[hh] = f2bf(xr[hh] + acc);
+        }
+        const uint32_t pair = o[0] | (o[1] << 16);
+        if (tagged) st_tag(tagged + (size_t)m * (g.H / 2) + h0 / 2 + pl, pair, tag);
+        else *reinterpret_cast<uint32_t *>(plain + (size_t)m * g.H + h0 + 2 * pl) = pair;
     }
 }
 
 // out_n = bf16(out * rinv * gamma_next) for this CTA's outputs.
-__device__ void write_normed(const KParams &kp, const Sh &sh, const uint16_t *out, const uint16_t *gamma_next)
+__device__ __noinline__ void write_normed(const KParams &kp, const Sh &sh, const uint16_t *out, const uint16_t *gamma_next)
 {
     const Geo &g = kp.g;
-    rms_rows(kp, sh, out, false);
+    const int H = g.H, M = kp.M, tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+    for (int m = lane; m < M; m += 32) sh.red[m * (NCW + 1) + warp] = 0.f;
+    __syncwarp();
+    const int per_row = H / 8, total = M * per_row;
+    for (int base = 0; base < total; base += NCT) {
+        const int it = base + tid;
+        float ss = 0.f;
+        if (it < total) {
+            const int m = it / per_row;
+            const uint4 a = __ldcg(reinterpret_cast<const uint4 *>(out + (size_t)m * H) + it % per_row);
+            const uint32_t aw[4] = {a.x, a.y, a.z, a.w};
+#pragma unroll
+            for (int j = 0; j < 4; ++j) {
+                const float lo = __uint_as_float(aw[j] << 16), hi = __uint_as_float(aw[j] & 0xFFFF0000u);
+                ss = fmaf(lo, lo, fmaf(hi, hi, ss));
+            }
+        }
+        ss = warp_sum(ss);
+        const int wfirst = base + warp * 32;
+        if (lane == 0 && wfirst < total) sh.red[(wfirst / per_row) * (NCW + 1) + warp] += ss;
+    }
+    cbar();
+    if (tid < M) {
+        float t = 0.f;
+        for (int w2 = 0; w2 < NCW; ++w2) t += sh.red[tid * (NCW + 1) + w2];
+        sh.red[tid * (NCW + 1) + NCW] = rsqrtf(t / (float)H + g.eps);
+    }
+    cbar();
     int h0, h1;
-    split(g.H, gridDim.x, blockIdx.x, h0, h1);
-    const int nh = h1 - h0, M = kp.M;
-    for (int t = threadIdx.x; t < nh * M; t += NCT) {
+    hslice(H, h0, h1);
+    const int nh = h1 - h0;
+    for (int t = tid; t < nh * M; t += NCT) {
         const int hl = t / M, m = t % M;
-        const size_t idx = (size_t)m * g.H + h0 + hl;
-        const float v = bf2f(__ldcg(out + idx)) * sh.red[kMaxRows * kRedChunks + m] * bf2f(gamma_next[h0 + hl]);
+        const size_t idx = (size_t)m * H + h0 + hl;
+        const float v = bf2f(__ldcg(out + idx)) * sh.red[m * (NCW + 1) + NCW] * bf2f(gamma_next[h0 + hl]);
         kp.out_normed[idx] = f2bf(v);
     }
 }
 
+// No grid barrier between layers or phases: every piece of data one CTA
+// publishes for others (router logits, shared and routed activations, the
+// layer output) is a tagged word, and readers wait on the words themselves.
+// (A word is rewritten only after every reader of its previous value is
+// done: CTA A writes layer l + 1's copy only after its P0 of layer l + 1,
+// which read every CTA's layer-l output, written after that CTA's last
+// read of layer l.)  One barrier remains, before the fused final RMSNorm.
 __device__ __forceinline__ void compute(const KParams &kp, const Sh &sh)
 {
     const Ws w = ws_views(kp);
     unsigned q = 0;
     int nsync = 0;
     int h0, h1;
-    split(kp.g.H, gridDim.x, blockIdx.x, h0, h1);
-    const int nh = h1 - h0;
+    hslice(kp.g.H, h0, h1);
+    const int np = (h1 - h0) / 2, M = kp.M, H = kp.g.H;
+    const int warp = threadIdx.x >> 5;
     for (int l = 0; l < kp.L; ++l) {
         const LayerPtrs &Lp = kp.layer[l];
         const bool last = l == kp.L - 1;
-        const uint16_t *xin = l == 0 ? kp.x : w.ping[(l - 1) & 1];
-        uint16_t *xout = last ? kp.out : w.ping[l & 1];
+        const unsigned xtag = l == 0 ? 0u : layer_tag(kp, l - 1);
+        const void *xin = l == 0 ? static_cast<const void *>(kp.x) : static_cast<const void *>(w.ping[(l - 1) & 1]);
         const bool t0 = threadIdx.x == 0;
         if (t0) stamp(kp, l, 0);
-        build_hn(kp, sh, xin, Lp.gamma);
+        // layer l's gamma, router rows and shared units
+        const bool pb_ok = wait_bar(sh, sh.pb_full, (unsigned)l & 1u, 5);
+        if (cbar_or(!pb_ok)) return;
+        build_hn(kp, sh, xin, xtag, reinterpret_cast<const uint16_t *>(sh.pb));
+        if (cbar_or(aborted(sh))) return;
         if (t0) stamp(kp, l, 1);
-        phase1(kp, sh, Lp, q, w);
+        phase1(kp, sh, Lp, q, w, l);
         if (t0) stamp(kp, l, 2);
-        if (!grid_sync(kp, sh, nsync)) return;
         if (t0) stamp(kp, l, 3);
-        route(kp, sh, w.logits, l);
+        // the first M warps route (waiting on every CTA's logits); the others
+        // stage the shared expert's activations (waiting on every CTA's
+        // units) and run its down rows from the prefetch buffer meanwhile
+        if (warp < M) {
+            route(kp, sh, w.logits, l);
+        } else if (kp.mode == kModeLayers && kp.g.has_shared) {
+            stage_acts(sh, M, kp.g.Is, M * 32, NCT - M * 32, layer_tag(kp, l),
+                       [&](int p) -> const uint64_t * { return w.act_s + (size_t)p * kp.g.Is; });
+            asm volatile("bar.sync 3, %0;" ::"r"(NCT - M * 32) : "memory");
+            shared_down_pb(kp, sh, M);
+        }
+        if (cbar_or(aborted(sh))) return;
+        // every warp is done with the prefetch buffer of layer l
+        if ((threadIdx.x & 31) == 0) mbar_arrive(sh.pb_empty, 1);
         if (t0) stamp(kp, l, 4);
         if (kp.mode == kModeRouter) break;
-        if (t0) mbar_arrive(sh.route, 1);
-        // residual of this thread's output, read while the weights stream
-        float xres = 0.f;
-        if ((int)threadIdx.x < nh * kp.M) {
-            const int hl = threadIdx.x / kp.M, m = threadIdx.x % kp.M;
-            xres = bf2f(__ldcg(xin + (size_t)m * kp.g.H + h0 + hl));
+        // residuals of this thread's output pair, read while the weights stream
+        float xr[2] = {0.f, 0.f};
+        if ((int)threadIdx.x < np * M) {
+            const int pl = threadIdx.x / M, m = threadIdx.x % M;
+            uint32_t pair;
+            if (l == 0) pair = *reinterpret_cast<const uint32_t *>(kp.x + (size_t)m * H + h0 + 2 * pl);
+            else pair = poll_tag(sh, w.ping[(l - 1) & 1] + (size_t)m * (H / 2) + h0 / 2 + pl, xtag, 43);
+            xr[0] = bf2f((uint16_t)(pair & 0xFFFFu));
+            xr[1] = bf2f((uint16_t)(pair >> 16));
         }
         wstamp(kp, l, 0);
-        phase1b(kp, sh, Lp, q, w, l);
         wstamp(kp, l, 1);
         phase2(kp, sh, Lp, q, w, l);
         wstamp(kp, l, 5);
         if (t0) stamp(kp, l, 5);
+        // shared down rows that came through the ring
+        phase1b(kp, sh, Lp, q, l);
+        // the staging buffer is reused: every warp is done with the shared rows
+        cbar();
         if (t0) stamp(kp, l, 6);
         wstamp(kp, l, 6);
-        phase3(kp, sh, Lp, q, w, l);
+        if (!phase3(kp, sh, Lp, q, w, l)) return;
         wstamp(kp, l, 10);
         if (cbar_or(aborted(sh))) return;
-        combine(kp, sh, xres, xout);
+        combine(kp, sh, xr, last ? nullptr : w.ping[l & 1], layer_tag(kp, l), kp.out);
         if (t0) stamp(kp, l, 7);
-        if (!last || kp.out_normed) {
+        if (last && kp.out_normed) {
             if (!grid_sync(kp, sh, nsync)) return;
+            write_normed(kp, sh, kp.out, Lp.gamma_next);
         }
         if (t0) stamp(kp, l, 8);
-        if (last && kp.out_normed) write_normed(kp, sh, xout, Lp.gamma_next);
     }
     kernel_exit(sh, kp.p.max_slots);
 }
@@ -1396,6 +1805,8 @@ __global__ void __launch_bounds__(kThreads, 1) moe_decode_kernel(const __grid_co
     sh.full = bars;
     sh.empty = bars + kp.p.NS;
     sh.route = bars + 2 * kp.p.NS;
+    sh.pb_full = bars + 2 * kp.p.NS + 1;
+    sh.pb_empty = bars + 2 * kp.p.NS + 2;
     sh.flags = reinterpret_cast<int *>(smem + L.flags);
     sh.slot_e = reinterpret_cast<int *>(smem + L.slot_e);
     sh.slot_mask = reinterpret_cast<uint32_t *>(smem + L.slot_mask);
@@ -1408,19 +1819,24 @@ __global__ void __launch_bounds__(kThreads, 1) moe_decode_kernel(const __grid_co
     sh.topw = reinterpret_cast<float *>(smem + L.topw);
     sh.row_w = reinterpret_cast<float *>(smem + L.row_w);
     sh.row_pair = reinterpret_cast<int *>(smem + L.row_pair);
-    sh.cand_v = reinterpret_cast<float *>(smem + L.cand_v);
-    sh.cand_e = reinterpret_cast<int *>(smem + L.cand_e);
     sh.red = reinterpret_cast<float *>(smem + L.red);
-    sh.xs = reinterpret_cast<float *>(smem + L.xs);
+    sh.p1v = reinterpret_cast<float *>(smem + L.p1v);
+    sh.pair_src = reinterpret_cast<int *>(smem + L.pair_src);
+    sh.pend = reinterpret_cast<int *>(smem + L.pend);
+    sh.xs = reinterpret_cast<float4 *>(smem + L.xs);
     sh.xsum = reinterpret_cast<float *>(smem + L.xsum);
+    sh.act = reinterpret_cast<float4 *>(smem + L.act);
+    sh.asum = reinterpret_cast<float *>(smem + L.asum);
     sh.ybuf = reinterpret_cast<float *>(smem + L.ybuf);
     sh.ysh = reinterpret_cast<float *>(smem + L.ysh);
     sh.target = reinterpret_cast<unsigned *>(smem + L.target);
     sh.act_done = reinterpret_cast<unsigned *>(kp.ws + kFlagsOffset);
+    sh.pb = smem + L.pb;
     sh.ring = smem + L.ring;
     sh.NS = kp.p.NS;
     sh.S = kp.p.S;
     sh.hrows = kp.p.hrows;
+    sh.act_pairs = kp.p.act_pairs;
     sh.timeout_ns = kp.timeout_ns;
     sh.ctrl = reinterpret_cast<Ctrl *>(kp.ws);
     if (threadIdx.x == 0) {
@@ -1429,15 +1845,19 @@ __global__ void __launch_bounds__(kThreads, 1) moe_decode_kernel(const __grid_co
             mbar_init(&sh.empty[i], 1);
         }
         mbar_init(sh.route, 1);
+        mbar_init(sh.pb_full, 1);
+        mbar_init(sh.pb_empty, NCW);
         sh.flags[0] = 0;
         sh.flags[1] = 0;
         for (int i = 0; i < kp.p.max_slots; ++i) sh.target[i] = 0u;
+        for (int i = 0; i < NCW * kp.p.max_slots; ++i) sh.pend[i] = 0;
         asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
     }
     __syncthreads();
     if (threadIdx.x >= NCT) {
         const int lane = threadIdx.x - NCT;
-        if (lane < NP) producer(kp, sh, lane);
+        if (lane < NP) ring_producer(kp, sh, lane);
+        else if (lane == NP) pb_producer(kp, sh);
         return;
     }
     compute(kp, sh);
@@ -1446,33 +1866,82 @@ __global__ void __launch_bounds__(kThreads, 1) moe_decode_kernel(const __grid_co
 int g_num_sms[64];
 bool g_attr_set[64];
 
+// Tag ranges of successive launches: 64 tags each (one per layer), from a
+// start drawn from the clock and the process id, so that words a previous
+// process left in reused device memory are unlikely to match.
+unsigned next_epoch()
+{
+    static std::atomic<unsigned> counter{0u};
+    static std::once_flag once;
+    std::call_once(once, [] {
+        const unsigned long long t = (unsigned long long)std::chrono::steady_clock::now().time_since_epoch().count();
+        counter.store((unsigned)((t ^ (t >> 32) ^ ((unsigned long long)getpid() << 16)) & ~63ull));
+    });
+    unsigned e = counter.fetch_add(64u);
+    if (e == 0u - 64u) e = counter.fetch_add(64u);   // tags epoch + 1 .. epoch + 64 never wrap to 0
+    return e;
+}
+
 }  // namespace
 
+// Shared memory of a launch: small tables, hn rows, the activation staging
+// buffer (act_pairs pairs), the prefetch buffer and the ring.  The ring gets
+// up to ring_target first (enough bytes in flight to cover the HBM latency
+// at one SM's share of the bandwidth), then the prefetch buffer up to one
+// layer's P1 rows, then staging pairs up to every pair of a launch, then
+// the ring takes whatever is left.
 bool make_plan(const Geo &g, int maxr, int num_sms, Plan &p)
 {
     p.P = num_sms;
     p.maxr = maxr;
     p.max_slots = g.E < maxr * g.k ? g.E : maxr * g.k;
-    p.hrows = (g.H + num_sms - 1) / num_sms;
-    int maxi = g.rr_bytes;
-    if (2 * g.g_bytes > maxi) maxi = 2 * g.g_bytes;
+    p.hrows = 2 * ((g.H / 2 + num_sms - 1) / num_sms);   // whole row pairs per CTA
+    int maxi = 2 * g.g_bytes;
     if (g.d_bytes > maxi) maxi = g.d_bytes;
     if (g.has_shared) {
-        if (2 * g.sg_bytes > maxi) maxi = 2 * g.sg_bytes;
+        if (g.sg_bytes > maxi) maxi = g.sg_bytes;
         if (g.sd_bytes > maxi) maxi = g.sd_bytes;
     }
+    const int Im = imax_of(g);
+    const int pair_bytes = Im * 4 + (Im / kGroup) * 4 + 4;
+    const int pb_min = (int)align_up((size_t)g.H * 2, 16) + per_cta(g.Er, num_sms) * g.rr_bytes;
+    const int pb_all = pb_min + (g.has_shared ? per_cta(g.Is, num_sms) * 2 * g.sg_bytes : 0);
+    const int pairs_all = maxr * g.k + maxr;
+    const int ring_target = 96 * 1024;
     // Every stage has one consumer warp: stage q goes to warp q % NCW, and a
     // warp waits on stage q only after it waited on stage q - NS of the same
     // slot (mbarrier parity tells apart only the current and previous phase),
     // so NS is a multiple of NCW (and of NP, for the issuing lanes).
     static_assert(NCW % NP == 0, "producer lanes must divide the ring depth");
-    for (int ns = 2 * NCW; ns >= NCW; ns -= NCW) {
-        p.NS = ns;
-        p.S = 16;
-        const int fixed = carve(g, p).ring;
-        int S = (kSmemMax - fixed - 256) / ns;
+    p.NS = 2 * NCW;
+    p.S = 0;
+    p.pb_bytes = 0;
+    p.act_pairs = 0;
+    const int fixed = carve(g, p).total;
+    int room = kSmemMax - 2048 - fixed - pb_min - maxr * pair_bytes;
+    if (room < NCW * maxi) return false;
+    const int ring_want = ring_target > NCW * maxi ? ring_target : NCW * maxi;
+    int ring = room < ring_want ? room : ring_want;
+    room -= ring;
+    int pb_extra = pb_all - pb_min;
+    if (pb_extra > room) pb_extra = room;
+    p.pb_bytes = pb_min + pb_extra;
+    room -= pb_extra;
+    int more_pairs = room / pair_bytes;
+    if (more_pairs > pairs_all - maxr) more_pairs = pairs_all - maxr;
+    p.act_pairs = maxr + more_pairs;
+    room -= more_pairs * pair_bytes;
+    ring += room;
+    // stages of at least two gate/up units if the ring allows it
+    const int want = 4 * g.g_bytes > maxi ? 4 * g.g_bytes : maxi;
+    int ns_pick = 0;
+    for (int ns = 2 * NCW; ns >= NCW && !ns_pick; ns -= NCW)
+        if (ring / ns >= want) ns_pick = ns;
+    for (int ns = ns_pick ? ns_pick : 2 * NCW; ns >= NCW; ns -= NCW) {
+        int S = ring / ns;
         S -= S % 16;
         if (S < maxi) continue;
+        p.NS = ns;
         p.S = S;
         p.smem_bytes = carve(g, p).total;
         if (p.smem_bytes <= kSmemMax) return true;
@@ -1500,7 +1969,11 @@ int launch_decode(const KParams &kp, cudaStream_t stream)
     attr[0].val.cooperative = 1;
     cfg.attrs = attr;
     cfg.numAttrs = 1;
-    e = cudaLaunchKernelEx(&cfg, moe_decode_kernel, kp);
+    // a fresh tag range for this launch: words left in the workspace by
+    // earlier launches never carry one of its tags
+    KParams kl = kp;
+    kl.epoch = next_epoch();
+    e = cudaLaunchKernelEx(&cfg, moe_decode_kernel, kl);
     note_launch();
     if (e != cudaSuccess) { note_cuda_error((int)e); return MOE_ERR_CUDA; }
     return MOE_OK;

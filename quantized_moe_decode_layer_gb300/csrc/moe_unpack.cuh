@@ -1,19 +1,23 @@
-// Exact conversion of packed b-bit codes to fp32, 16 codes (one sub-group)
-// at a time, from the LSB-first bit stream of the device layout.
+// Packed b-bit codes as floats without an integer-to-float conversion.
 //
-// Method: IEEE-754 bit construction (the same idea as the "magic number"
-// int-to-float conversions used for quantised GEMMs, e.g. Kim et al. 2022,
-// "Who Says Elephants Can't Run"): for a code q sitting at bit position p of
-// a 32-bit word, OR-ing the word (masked to the code) with the exponent field
-// (150 - p) << 23 gives the float 2^(23-p) + q exactly, because q << p then
-// lies inside the 23-bit mantissa with unit weight 2^(23-p-23+p) = 1.
-// Subtracting the constant 2^(23-p) returns q exactly.  Choosing the exponent
-// per bit position avoids shifting each code down to bit 0: one LOP3-style
-// AND/OR plus one FADD per code, plus one shift per few codes.
+// A code q at bit position p < 23 of a 32-bit word, with every other bit
+// masked off, is read as the IEEE-754 single q * 2^(p - 149) (a subnormal for
+// the positions used here, exact).  The decode kernel multiplies it by the
+// activation stored times 2^100, which gives q * x * 2^(p - 49) as an exact
+// fp32 product, and scales each per-position ("class") sum back by
+// 2^(49 - p); or it first multiplies the masked code by 2^(126 - p) to get
+// q * 2^-23.  Either way one bitwise AND (a LOP3) per code is the only
+// integer work, plus one shift for every few codes that sit above bit 22.
+// (The idea of building floats from code bits is the one behind the
+// "magic number" conversions of quantised GEMM kernels, e.g. Kim et al.
+// 2022, "Who Says Elephants Can't Run".)
+//
+// A 16-code sub-group of the canonical LSB-first stream (BITS/2 words) is
+// read as 8 pairs: pair i = codes (2i, 2i+1), at positions (pa(i), pb(i)),
+// accumulated in class cls(i).
 #pragma once
 
 #include <cstdint>
-#include <initializer_list>
 
 namespace moe {
 
@@ -37,171 +41,156 @@ __host__ __device__ __forceinline__ uint32_t funnel_r(uint32_t lo, uint32_t hi, 
 #endif
 }
 
-// Code of `BITS` bits at position P of v, as an exact float.
-template <int BITS, int P>
-__host__ __device__ __forceinline__ float code_at(uint32_t v)
-{
-    static_assert(P + BITS <= 23, "code must sit inside the mantissa");
-    constexpr uint32_t kMask = ((1u << BITS) - 1u) << P;
-    constexpr uint32_t kExp = (uint32_t)(150 - P) << 23;
-    return u2f((v & kMask) | kExp) - u2f(kExp);
-}
+__host__ __device__ __forceinline__ float mk(uint32_t v, uint32_t m) { return u2f(v & m); }
 
-// Raw form: the float 2^(23-P) + q (no subtraction yet) and its offset
-// 2^(23-P); packed two-lane FADD then removes the offsets of a pair at once.
-template <int BITS, int P>
-__host__ __device__ __forceinline__ float code_raw(uint32_t v)
-{
-    static_assert(P + BITS <= 23, "code must sit inside the mantissa");
-    constexpr uint32_t kMask = ((1u << BITS) - 1u) << P;
-    constexpr uint32_t kExp = (uint32_t)(150 - P) << 23;
-    return u2f((v & kMask) | kExp);
-}
+// 2^(49 - p): brings a class sum of (masked code) * (x * 2^100) back to q x.
+__host__ __device__ constexpr uint32_t cls_bits(int p) { return (uint32_t)(49 - p + 127) << 23; }
+// 2^(126 - p): turns a masked code into q * 2^-23.
+__host__ __device__ constexpr uint32_t fm_bits(int p) { return (uint32_t)(126 - p + 127) << 23; }
 
-template <int P>
-__host__ __device__ __forceinline__ float code_off()
-{
-    return u2f((uint32_t)(150 - P) << 23);
-}
+struct Pair2 { float a, b; };
 
-// Codes 4t .. 4t+3 of a 16-code sub-group held in w[] (BITS/2 words).
-// get4 gives exact floats; raw4 gives code_raw values f and offsets o with
-// f - o the codes.
+template <int BITS> struct Pairs;
+
+template <> struct Pairs<6> {
+    // code c at stream bits [6c, 6c + 6); codes 3, 4, 9, 14, 15 are read
+    // after a 12-bit shift of their word, codes 5 and 10 (which straddle two
+    // words) after a funnel shift
+    static constexpr int NC = 7;
+    __host__ __device__ static constexpr int pa(int i)
+    {
+        return i == 0 ? 0 : i == 1 ? 12 : i == 2 ? 12 : i == 3 ? 4 : i == 4 ? 16 : i == 5 ? 0 : 8;
+    }
+    __host__ __device__ static constexpr int pb(int i)
+    {
+        return i == 0 ? 6 : i == 1 ? 6 : i == 2 ? 0 : i == 3 ? 10 : i == 4 ? 10 : i == 5 ? 2 : 14;
+    }
+    __host__ __device__ static constexpr int cls(int i) { return i < 7 ? i : 6; }
+    template <typename F>
+    __host__ __device__ __forceinline__ static void each(const uint32_t *w, F &&f)
+    {
+        const uint32_t s0 = w[0] >> 12, s1 = w[1] >> 12, s2 = w[2] >> 12;
+        const uint32_t f5 = funnel_r(w[0], w[1], 30), f10 = funnel_r(w[1], w[2], 28);
+        constexpr uint32_t M = 0x3Fu;
+        f(0, mk(w[0], M), mk(w[0], M << 6));
+        f(1, mk(w[0], M << 12), mk(s0, M << 6));
+        f(2, mk(s0, M << 12), mk(f5, M));
+        f(3, mk(w[1], M << 4), mk(w[1], M << 10));
+        f(4, mk(w[1], M << 16), mk(s1, M << 10));
+        f(5, mk(f10, M), mk(w[2], M << 2));
+        f(6, mk(w[2], M << 8), mk(w[2], M << 14));
+        f(7, mk(s2, M << 8), mk(s2, M << 14));
+    }
+    template <typename P2>
+    __host__ __device__ __forceinline__ static void get(const uint32_t *w, P2 (&p)[8])
+    {
+        const uint32_t s0 = w[0] >> 12, s1 = w[1] >> 12, s2 = w[2] >> 12;
+        const uint32_t f5 = funnel_r(w[0], w[1], 30), f10 = funnel_r(w[1], w[2], 28);
+        constexpr uint32_t M = 0x3Fu;
+        p[0] = {mk(w[0], M), mk(w[0], M << 6)};
+        p[1] = {mk(w[0], M << 12), mk(s0, M << 6)};
+        p[2] = {mk(s0, M << 12), mk(f5, M)};
+        p[3] = {mk(w[1], M << 4), mk(w[1], M << 10)};
+        p[4] = {mk(w[1], M << 16), mk(s1, M << 10)};
+        p[5] = {mk(f10, M), mk(w[2], M << 2)};
+        p[6] = {mk(w[2], M << 8), mk(w[2], M << 14)};
+        p[7] = {mk(s2, M << 8), mk(s2, M << 14)};
+    }
+};
+
+template <> struct Pairs<8> {
+    // word j: codes 4j .. 4j+3, one per byte; the high half shifted down
+    static constexpr int NC = 1;
+    __host__ __device__ static constexpr int pa(int) { return 0; }
+    __host__ __device__ static constexpr int pb(int) { return 8; }
+    __host__ __device__ static constexpr int cls(int) { return 0; }
+    template <typename F>
+    __host__ __device__ __forceinline__ static void each(const uint32_t *w, F &&f)
+    {
+#pragma unroll
+        for (int j = 0; j < 4; ++j) {
+            const uint32_t v = w[j], s = v >> 16;
+            f(2 * j, mk(v, 0xFFu), mk(v, 0xFF00u));
+            f(2 * j + 1, mk(s, 0xFFu), mk(s, 0xFF00u));
+        }
+    }
+    template <typename P2>
+    __host__ __device__ __forceinline__ static void get(const uint32_t *w, P2 (&p)[8])
+    {
+#pragma unroll
+        for (int j = 0; j < 4; ++j) {
+            const uint32_t v = w[j], s = v >> 16;
+            p[2 * j] = {mk(v, 0xFFu), mk(v, 0xFF00u)};
+            p[2 * j + 1] = {mk(s, 0xFFu), mk(s, 0xFF00u)};
+        }
+    }
+};
+
+template <> struct Pairs<4> {
+    // word j: codes 8j .. 8j+7, low nibble first; the high half shifted down
+    static constexpr int NC = 2;
+    __host__ __device__ static constexpr int pa(int i) { return (i & 1) ? 8 : 0; }
+    __host__ __device__ static constexpr int pb(int i) { return (i & 1) ? 12 : 4; }
+    __host__ __device__ static constexpr int cls(int i) { return i & 1; }
+    template <typename F>
+    __host__ __device__ __forceinline__ static void each(const uint32_t *w, F &&f)
+    {
+#pragma unroll
+        for (int j = 0; j < 2; ++j) {
+            const uint32_t v = w[j], s = v >> 16;
+            f(4 * j, mk(v, 0xFu), mk(v, 0xF0u));
+            f(4 * j + 1, mk(v, 0xF00u), mk(v, 0xF000u));
+            f(4 * j + 2, mk(s, 0xFu), mk(s, 0xF0u));
+            f(4 * j + 3, mk(s, 0xF00u), mk(s, 0xF000u));
+        }
+    }
+    template <typename P2>
+    __host__ __device__ __forceinline__ static void get(const uint32_t *w, P2 (&p)[8])
+    {
+#pragma unroll
+        for (int j = 0; j < 2; ++j) {
+            const uint32_t v = w[j], s = v >> 16;
+            p[4 * j] = {mk(v, 0xFu), mk(v, 0xF0u)};
+            p[4 * j + 1] = {mk(v, 0xF00u), mk(v, 0xF000u)};
+            p[4 * j + 2] = {mk(s, 0xFu), mk(s, 0xF0u)};
+            p[4 * j + 3] = {mk(s, 0xF00u), mk(s, 0xF000u)};
+        }
+    }
+};
+
+// Host check of the tables above against a plain bit-by-bit extraction of
+// the stream: every masked code times 2^(149 - p) must be the code, the
+// class of a pair must fix both positions, and the scale constants must be
+// the powers of two they stand for.  Returns the number of mismatches.
 template <int BITS>
-struct Unpack;
-
-template <>
-struct Unpack<4> {
-    // word i holds codes 8i .. 8i+7 at bits 0, 4, ..., 28
-    template <int T>
-    __host__ __device__ __forceinline__ static void get4(const uint32_t *w, float *q)
-    {
-        const uint32_t v = w[T >> 1];
-        if ((T & 1) == 0) {
-            q[0] = code_at<4, 0>(v);
-            q[1] = code_at<4, 4>(v);
-            q[2] = code_at<4, 8>(v);
-            q[3] = code_at<4, 12>(v);
-        } else {
-            const uint32_t s = v >> 12;   // codes 5, 6, 7 of the word move to 8, 12, 16
-            q[0] = code_at<4, 16>(v);
-            q[1] = code_at<4, 8>(s);
-            q[2] = code_at<4, 12>(s);
-            q[3] = code_at<4, 16>(s);
+inline int pairs_selftest_one(const uint32_t *w)
+{
+    using PT = Pairs<BITS>;
+    int bad = 0;
+    Pair2 p[8];
+    PT::get(w, p);
+    for (int c = 0; c < 16; ++c) {
+        uint32_t v = 0;
+        for (int t = 0; t < BITS; ++t) {
+            const int pos = c * BITS + t;
+            v |= ((w[pos >> 5] >> (pos & 31)) & 1u) << t;
         }
+        const int i = c / 2;
+        const int pos = (c & 1) ? PT::pb(i) : PT::pa(i);
+        const float m = (c & 1) ? p[i].b : p[i].a;
+        // exact: multiply by 2^(149 - pos) in two power-of-two steps
+        const double q = (double)m * 0x1p100 * (double)(1ull << (49 - pos));
+        if (q != (double)v) ++bad;
+        if ((double)u2f(fm_bits(pos)) * (double)m != (double)v * 0x1p-23) ++bad;
     }
-    template <int T>
-    __host__ __device__ __forceinline__ static void raw4(const uint32_t *w, float *f, float *o)
-    {
-        const uint32_t v = w[T >> 1];
-        if ((T & 1) == 0) {
-            f[0] = code_raw<4, 0>(v); o[0] = code_off<0>();
-            f[1] = code_raw<4, 4>(v); o[1] = code_off<4>();
-            f[2] = code_raw<4, 8>(v); o[2] = code_off<8>();
-            f[3] = code_raw<4, 12>(v); o[3] = code_off<12>();
-        } else {
-            const uint32_t s = v >> 12;
-            f[0] = code_raw<4, 16>(v); o[0] = code_off<16>();
-            f[1] = code_raw<4, 8>(s); o[1] = code_off<8>();
-            f[2] = code_raw<4, 12>(s); o[2] = code_off<12>();
-            f[3] = code_raw<4, 16>(s); o[3] = code_off<16>();
-        }
-    }
-};
+    for (int i = 0; i < 8; ++i)
+        for (int j = 0; j < 8; ++j)
+            if (PT::cls(i) == PT::cls(j) && (PT::pa(i) != PT::pa(j) || PT::pb(i) != PT::pb(j))) ++bad;
+    for (int pos = 0; pos < 23; ++pos)
+        if ((double)u2f(cls_bits(pos)) != (double)(1ull << (49 - pos))) ++bad;
+    return bad;
+}
 
-template <>
-struct Unpack<8> {
-    // word i holds codes 4i .. 4i+3, one per byte
-    template <int T>
-    __host__ __device__ __forceinline__ static void get4(const uint32_t *w, float *q)
-    {
-        const uint32_t v = w[T];
-        const uint32_t s = v >> 16;
-        q[0] = code_at<8, 0>(v);
-        q[1] = code_at<8, 8>(v);
-        q[2] = code_at<8, 0>(s);
-        q[3] = code_at<8, 8>(s);
-    }
-    template <int T>
-    __host__ __device__ __forceinline__ static void raw4(const uint32_t *w, float *f, float *o)
-    {
-        const uint32_t v = w[T];
-        const uint32_t s = v >> 16;
-        f[0] = code_raw<8, 0>(v); o[0] = code_off<0>();
-        f[1] = code_raw<8, 8>(v); o[1] = code_off<8>();
-        f[2] = code_raw<8, 0>(s); o[2] = code_off<0>();
-        f[3] = code_raw<8, 8>(s); o[3] = code_off<8>();
-    }
-};
-
-template <>
-struct Unpack<6> {
-    // 16 codes in 96 bits: code i at stream bits 6i .. 6i+5.  Word 0 holds
-    // codes 0-4 and the low 2 bits of code 5; word 1 the high 4 bits of
-    // code 5, codes 6-9 and the low 4 bits of code 10; word 2 the high 2 bits
-    // of code 10 and codes 11-15.
-    template <int T>
-    __host__ __device__ __forceinline__ static void get4(const uint32_t *w, float *q)
-    {
-        if (T == 0) {          // codes 0..3
-            const uint32_t s0 = w[0] >> 12;
-            q[0] = code_at<6, 0>(w[0]);
-            q[1] = code_at<6, 6>(w[0]);
-            q[2] = code_at<6, 12>(w[0]);
-            q[3] = code_at<6, 6>(s0);
-        } else if (T == 1) {   // codes 4..7
-            const uint32_t s0 = w[0] >> 12;
-            q[0] = code_at<6, 12>(s0);
-            q[1] = code_at<6, 0>(funnel_r(w[0], w[1], 30));
-            q[2] = code_at<6, 4>(w[1]);
-            q[3] = code_at<6, 10>(w[1]);
-        } else if (T == 2) {   // codes 8..11
-            const uint32_t s1 = w[1] >> 12;
-            q[0] = code_at<6, 16>(w[1]);
-            q[1] = code_at<6, 10>(s1);
-            q[2] = code_at<6, 0>(funnel_r(w[1], w[2], 28));
-            q[3] = code_at<6, 2>(w[2]);
-        } else {               // codes 12..15
-            const uint32_t s2 = w[2] >> 12;
-            q[0] = code_at<6, 8>(w[2]);
-            q[1] = code_at<6, 14>(w[2]);
-            q[2] = code_at<6, 8>(s2);
-            q[3] = code_at<6, 14>(s2);
-        }
-    }
-    template <int T>
-    __host__ __device__ __forceinline__ static void raw4(const uint32_t *w, float *f, float *o)
-    {
-        if (T == 0) {
-            const uint32_t s0 = w[0] >> 12;
-            f[0] = code_raw<6, 0>(w[0]); o[0] = code_off<0>();
-            f[1] = code_raw<6, 6>(w[0]); o[1] = code_off<6>();
-            f[2] = code_raw<6, 12>(w[0]); o[2] = code_off<12>();
-            f[3] = code_raw<6, 6>(s0); o[3] = code_off<6>();
-        } else if (T == 1) {
-            const uint32_t s0 = w[0] >> 12;
-            f[0] = code_raw<6, 12>(s0); o[0] = code_off<12>();
-            f[1] = code_raw<6, 0>(funnel_r(w[0], w[1], 30)); o[1] = code_off<0>();
-            f[2] = code_raw<6, 4>(w[1]); o[2] = code_off<4>();
-            f[3] = code_raw<6, 10>(w[1]); o[3] = code_off<10>();
-        } else if (T == 2) {
-            const uint32_t s1 = w[1] >> 12;
-            f[0] = code_raw<6, 16>(w[1]); o[0] = code_off<16>();
-            f[1] = code_raw<6, 10>(s1); o[1] = code_off<10>();
-            f[2] = code_raw<6, 0>(funnel_r(w[1], w[2], 28)); o[2] = code_off<0>();
-            f[3] = code_raw<6, 2>(w[2]); o[3] = code_off<2>();
-        } else {
-            const uint32_t s2 = w[2] >> 12;
-            f[0] = code_raw<6, 8>(w[2]); o[0] = code_off<8>();
-            f[1] = code_raw<6, 14>(w[2]); o[1] = code_off<14>();
-            f[2] = code_raw<6, 8>(s2); o[2] = code_off<8>();
-            f[3] = code_raw<6, 14>(s2); o[3] = code_off<14>();
-        }
-    }
-};
-
-// Host check of the tables above against a plain bit-by-bit extraction.
-// Returns the number of mismatching codes over a fixed pseudo-random set.
 inline int unpack_selftest_host()
 {
     int bad = 0;
@@ -209,33 +198,9 @@ inline int unpack_selftest_host()
     for (int rep = 0; rep < 2000; ++rep) {
         uint32_t w[4];
         for (int i = 0; i < 4; ++i) { seed = seed * 1664525u + 1013904223u; w[i] = seed ^ (seed >> 13); }
-        for (int bits : {4, 6, 8}) {
-            float q[16];
-            if (bits == 4) {
-                Unpack<4>::get4<0>(w, q); Unpack<4>::get4<1>(w, q + 4); Unpack<4>::get4<2>(w, q + 8); Unpack<4>::get4<3>(w, q + 12);
-            } else if (bits == 6) {
-                Unpack<6>::get4<0>(w, q); Unpack<6>::get4<1>(w, q + 4); Unpack<6>::get4<2>(w, q + 8); Unpack<6>::get4<3>(w, q + 12);
-            } else {
-                Unpack<8>::get4<0>(w, q); Unpack<8>::get4<1>(w, q + 4); Unpack<8>::get4<2>(w, q + 8); Unpack<8>::get4<3>(w, q + 12);
-            }
-            float fr[16], of[16];
-            if (bits == 4) {
-                Unpack<4>::raw4<0>(w, fr, of); Unpack<4>::raw4<1>(w, fr + 4, of + 4); Unpack<4>::raw4<2>(w, fr + 8, of + 8); Unpack<4>::raw4<3>(w, fr + 12, of + 12);
-            } else if (bits == 6) {
-                Unpack<6>::raw4<0>(w, fr, of); Unpack<6>::raw4<1>(w, fr + 4, of + 4); Unpack<6>::raw4<2>(w, fr + 8, of + 8); Unpack<6>::raw4<3>(w, fr + 12, of + 12);
-            } else {
-                Unpack<8>::raw4<0>(w, fr, of); Unpack<8>::raw4<1>(w, fr + 4, of + 4); Unpack<8>::raw4<2>(w, fr + 8, of + 8); Unpack<8>::raw4<3>(w, fr + 12, of + 12);
-            }
-            for (int i = 0; i < 16; ++i) {
-                if (fr[i] - of[i] != q[i]) ++bad;
-                uint32_t v = 0;
-                for (int t = 0; t < bits; ++t) {
-                    const int pos = i * bits + t;
-                    v |= ((w[pos >> 5] >> (pos & 31)) & 1u) << t;
-                }
-                if (q[i] != (float)v) ++bad;
-            }
-        }
+        bad += pairs_selftest_one<4>(w);
+        bad += pairs_selftest_one<6>(w);
+        bad += pairs_selftest_one<8>(w);
     }
     return bad;
 }

@@ -233,9 +233,9 @@ def test_stack_host_buffers():
 # -------------------------------------------------------------------- waits
 
 def test_barrier_timeout_returns_status():
-    """A CTA that never arrives makes the grid barrier run out: the call
-    returns MOE_ERR_TIMEOUT instead of hanging, and the workspace works again
-    after moe_workspace_init."""
+    """A router logit that is never published makes every CTA's wait for it
+    run out: the call returns MOE_ERR_TIMEOUT instead of hanging, and the
+    workspace works again after moe_workspace_init."""
     shape = synth.TINY
     L, layer, lay = cached(shape, 7)
     x = rows_with_margin(shape, lay, 79, 1).to(DEV)
@@ -243,7 +243,7 @@ def test_barrier_timeout_returns_status():
     good = moe.decode_layer(layer, x, ws)
     assert ws.status() == 0
     try:
-        moe.debug_set(skip_cta=3, timeout_ns=50_000_000)
+        moe.debug_set(skip_row=3, timeout_ns=50_000_000)
         moe.decode_layer(layer, x, ws)
         assert ws.status() == 5
     finally:

@@ -96,7 +96,7 @@ void make_ws_layout(const Geo &g, int max_M, WsLayout &w)
     size_t o = kCtrlBytes;
     auto put = [&](size_t bytes) { o = align_up(o, 256); size_t r = o; o += bytes; return r; };
     // buffers CTAs exchange hold tagged 8-byte words (value | tag << 32)
-    w.off_logits = put((size_t)R * g.Er * 8);
+    w.off_logits = put((size_t)kLogitCopies * R * g.Er * 8);
     w.off_act = put((size_t)w.max_slots * R * g.I * 8);
     w.off_act_s = put((size_t)R * (g.Is ? g.Is : 1) * 8);
     w.off_ping = put((size_t)2 * R * (g.H / 2) * 8);

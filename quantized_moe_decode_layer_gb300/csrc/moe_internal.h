@@ -15,15 +15,14 @@ constexpr int kGroup = 64;          // affine group along the contraction axis
 constexpr int kSub = 16;            // codes per sub-group (one lane step)
 constexpr int kConsumerWarps = 15;  // compute warps per CTA (16 warps: 128 registers per thread)
 constexpr int kThreads = (kConsumerWarps + 1) * 32;  // + one TMA producer warp
-constexpr int kProducerLanes = 5;   // lanes of the producer warp issuing bulk copies
 constexpr int kMaxRows = 8;         // token rows per launch (larger M is chunked)
 constexpr int kMaxLayers = 64;      // layers per persistent launch
 constexpr int kMaxStages = 64;      // ring stages (mbarrier pairs)
 constexpr int kMaxE = 512;
 constexpr int kMaxK = 32;
 constexpr int kMaxGPL = 4;          // 64-groups per lane of a row: K <= 32 * 64 * kMaxGPL
+constexpr int kLogitCopies = 8;     // copies of the router logits in the workspace (readers spread over them)
 constexpr int kCtrlBytes = 2048;    // control block at the start of the workspace
-constexpr int kFlagsOffset = 512;   // per-slot activation-ready counters (uint32 each) inside it
 constexpr int kSmemMax = 232448;    // dynamic shared memory per CTA on sm_100-class parts
 
 // Status word bits (workspace control block).
@@ -84,8 +83,7 @@ struct Ctrl {                // first kCtrlBytes of the workspace
     int where;               // debug: which wait gave up
     int pad2[62];
 };
-static_assert(sizeof(Ctrl) <= kFlagsOffset, "control block");
-static_assert(kFlagsOffset + 4 * kMaxRows * kMaxK <= kCtrlBytes, "activation-ready counters");
+static_assert(sizeof(Ctrl) <= kCtrlBytes, "control block");
 
 // Launch plan of the persistent kernel.
 struct Plan {

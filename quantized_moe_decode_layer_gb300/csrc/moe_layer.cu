@@ -59,16 +59,33 @@ namespace {
 
 constexpr int NCW = kConsumerWarps;
 constexpr int NCT = NCW * 32;
-constexpr int NP = kProducerLanes;   // lanes issuing ring stages; lane NP fills the prefetch buffer
 constexpr unsigned FULLMASK = 0xffffffffu;
 constexpr float kXScale = 0x1p100f;  // arranged vectors hold x * 2^100
 constexpr float kFmScale = 0x1p-77f; // (q 2^-23) (x 2^100) -> q x
 
 // ------------------------------------------------------------ shared layout
 
+// Per-CTA constants of a launch, computed once into shared memory: this
+// CTA's router rows, shared gate/up units and output slice, and what its
+// prefetch buffer holds.  The prefetch buffer of a layer is gamma, the
+// router rows, the shared expert's down rows of the output slice (when they
+// fit) and as many of the shared units as fit; the rest go through the ring.
+struct CtaPlan {
+    int ra, rb;        // router rows
+    int ua, ub;        // shared units of this CTA
+    int upb;           // units held in the buffer: [ua, ua + upb)
+    int h0, nh;        // output slice (whole row pairs): rows h0 .. h0 + nh
+    int dpb;           // shared down rows held in the buffer: nh or 0
+    int off_router, off_sdown, off_units, bytes;
+};
+
+// Bytes reserved for the CTA's Sh (pointers into shared memory and launch
+// constants), which lives in shared memory itself.
+constexpr int kShBytes = 512;
+
 struct SmemLayout {
-    int bar, flags, slot_e, slot_mask, slot_rowbase, sigma, eslot, emask, topv, tope, topw;
-    int row_w, row_pair, red, p1v, pair_src, pend, xs, xsum, act, asum, ybuf, ysh, target, pb, ring, total;
+    int shs, cplan, bar, flags, slot_e, slot_mask, slot_rowbase, sigma, eslot, emask, topv, tope, topw;
+    int row_w, row_pair, red, lscr, p1v, pair_src, xs, xsum, act, asum, ybuf, ysh, pb, ring, total;
 };
 
 __host__ __device__ inline int take(int &o, int bytes, int align)
@@ -89,6 +106,8 @@ __host__ __device__ inline SmemLayout carve(const Geo &g, const Plan &p)
     SmemLayout L;
     int o = 0;
     const int ms = p.max_slots, Im = imax_of(g);
+    L.shs = take(o, kShBytes, 16);
+    L.cplan = take(o, (int)sizeof(CtaPlan), 16);
     L.bar = take(o, (2 * p.NS + 3) * 8, 8);
     L.flags = take(o, 16 * 4, 16);
     L.slot_e = take(o, ms * 4, 4);
@@ -103,16 +122,15 @@ __host__ __device__ inline SmemLayout carve(const Geo &g, const Plan &p)
     L.row_w = take(o, kMaxRows * kMaxK * 4, 4);
     L.row_pair = take(o, kMaxRows * kMaxK * 4, 4);
     L.red = take(o, kMaxRows * (NCW + 1) * 4, 4);
+    L.lscr = take(o, NCW * kMaxRows * 4, 4);
     L.p1v = take(o, 2 * per_cta(g.Is > 0 ? g.Is : 1, p.P) * p.maxr * 4, 4);
     L.pair_src = take(o, p.act_pairs * 4, 4);
-    L.pend = take(o, NCW * ms * 4, 4);
     L.xs = take(o, p.maxr * g.H * 4, 16);
     L.xsum = take(o, p.maxr * (g.H / kGroup) * 4, 16);
     L.act = take(o, p.act_pairs * Im * 4, 16);
     L.asum = take(o, p.act_pairs * (Im / kGroup) * 4, 16);
     L.ybuf = take(o, p.maxr * g.k * p.hrows * 4, 16);
     L.ysh = take(o, p.hrows * kMaxRows * 4, 16);
-    L.target = take(o, ms * 4, 16);
     L.pb = take(o, p.pb_bytes, 128);
     L.ring = take(o, p.NS * p.S, 128);
     L.total = o;
@@ -152,6 +170,17 @@ __device__ __forceinline__ bool mbar_try_wait(uint64_t *bar, unsigned parity)
     return ok != 0;
 }
 
+// Non-blocking test of an mbarrier phase.
+__device__ __forceinline__ bool mbar_test(uint64_t *bar, unsigned parity)
+{
+    uint32_t ok;
+    asm volatile("{\n\t.reg .pred p;\n\t"
+                 "mbarrier.test_wait.parity.shared::cta.b64 p, [%1], %2;\n\t"
+                 "selp.u32 %0, 1, 0, p;\n\t}"
+                 : "=r"(ok) : "r"(smem_u32(bar)), "r"(parity) : "memory");
+    return ok != 0;
+}
+
 // The same, letting the hardware suspend the thread for up to `ns`
 // nanoseconds while the phase is incomplete (waiting warps then take no
 // issue slots from the computing ones).
@@ -182,6 +211,13 @@ __device__ __forceinline__ void bulk_load(void *dst, const void *src, unsigned b
                  " [%0], [%1], %2, [%3], %4;"
                  ::"r"(smem_u32(dst)), "l"(src), "r"(bytes), "r"(smem_u32(bar)), "l"(evict_first_policy())
                  : "memory");
+}
+
+// Starts moving `bytes` (a multiple of 16; src 16-byte aligned) from global
+// memory into L2, with no completion signal.
+__device__ __forceinline__ void prefetch_l2(const void *src, unsigned bytes)
+{
+    asm volatile("cp.async.bulk.prefetch.L2.global [%0], %1;" ::"l"(src), "r"(bytes) : "memory");
 }
 
 __device__ __forceinline__ unsigned long long now_ns()
@@ -252,6 +288,12 @@ __device__ __forceinline__ uint64_t ld_tag(const uint64_t *p)
     return v;
 }
 
+// Two adjacent tagged words (p 16-byte aligned) in one access.
+__device__ __forceinline__ void ld_tag2(const uint64_t *p, uint64_t &a, uint64_t &b)
+{
+    asm volatile("ld.relaxed.gpu.global.v2.b64 {%0, %1}, [%2];" : "=l"(a), "=l"(b) : "l"(p) : "memory");
+}
+
 __device__ __forceinline__ float bf2f(uint16_t b) { return __uint_as_float((uint32_t)b << 16); }
 
 __device__ __forceinline__ uint16_t f2bf(float v)
@@ -288,6 +330,7 @@ __device__ __forceinline__ void wstamp(const KParams &kp, int l, int ev)
 // ----------------------------------------------------------- CTA state
 
 struct Sh {
+    const CtaPlan *cp;
     uint64_t *full, *empty, *route, *pb_full, *pb_empty;
     int *flags;          // [0] abort, [1] U
     int *slot_e;
@@ -302,23 +345,23 @@ struct Sh {
     float *row_w;        // [kMaxRows][kMaxK]  by expert id
     int *row_pair;
     float *red;          // [kMaxRows][NCW + 1] RMSNorm partial sums, then 1/rms
+    float *lscr;         // [NCW][kMaxRows] a warp's router logits before they go out
     float *p1v;          // [shared rows of this CTA][maxr] gate / up values
     int *pair_src;       // [act_pairs] slot * kMaxRows + row of each staged pair
-    int *pend;           // [NCW][max_slots] activation units a warp has yet to publish
     float4 *xs;          // [maxr][H / 4] arranged hn * 2^100
     float *xsum;         // [maxr][H / 64] group sums of hn
     float4 *act;         // [act_pairs][K / 4] arranged activations * 2^100
     float *asum;         // [act_pairs][K / 64]
     float *ybuf;         // [pair][hrows] routed expert outputs of this CTA's slice
     float *ysh;          // [hrows][kMaxRows] shared expert outputs
-    unsigned *target;    // [max_slots] activation-ready count each slot must reach this layer
-    unsigned *act_done;  // [max_slots] global activation-ready counters (workspace)
     uint8_t *pb;
     uint8_t *ring;
     int NS, S, hrows, act_pairs;
     long long timeout_ns;
     Ctrl *ctrl;
 };
+static_assert(sizeof(Sh) <= kShBytes, "Sh does not fit its shared-memory slot");
+
 
 __device__ __forceinline__ bool aborted(const Sh &sh) { return *(volatile int *)&sh.flags[0] != 0; }
 
@@ -346,37 +389,18 @@ __device__ bool wait_bar(const Sh &sh, uint64_t *bar, unsigned parity, int where
     }
 }
 
-// Bounded wait (lane 0 polls, the warp follows) until a global counter
-// reaches `target`; false on timeout or abort.
-__device__ bool wait_count(const Sh &sh, const unsigned *ctr, unsigned target, int where)
-{
-    bool ok = true;
-    if ((threadIdx.x & 31) == 0 && ld_acquire(ctr) < target) {
-        const unsigned long long t0 = now_ns();
-        for (unsigned it = 1;; ++it) {
-            __nanosleep(64);   // many warps poll: keep the L2 traffic low
-            if (ld_acquire(ctr) >= target) break;
-            if ((it & 31) == 0) {
-                if (aborted(sh)) { ok = false; break; }
-                if (now_ns() - t0 > (unsigned long long)sh.timeout_ns) { raise_abort(sh, where); ok = false; break; }
-            }
-        }
-    }
-    return __shfl_sync(FULLMASK, ok ? 1 : 0, 0) != 0;
-}
-
 // Loads tagged word p until it carries `tag`; returns its payload.  Bounded:
 // on timeout (or when another thread gave up) raises the abort flag and
-// returns 0; callers check aborted() at their next CTA barrier.
-__device__ uint32_t poll_tag(const Sh &sh, const uint64_t *p, unsigned tag, int where)
+// returns 0; callers check aborted() at their next CTA barrier.  Kept out of
+// line: it runs only for data that is not there at the first look.
+__device__ __noinline__ uint32_t poll_tag_slow(const Sh &sh, const uint64_t *p, unsigned tag, int where)
 {
-    uint64_t v = ld_tag(p);
-    if ((unsigned)(v >> 32) == tag) return (uint32_t)v;
     const unsigned long long t0 = now_ns();
+#pragma unroll 1
     for (unsigned it = 1;; ++it) {
-        __nanosleep(32);
-        v = ld_tag(p);
+        const uint64_t v = ld_tag(p);
         if ((unsigned)(v >> 32) == tag) return (uint32_t)v;
+        __nanosleep(32);
         if ((it & 15) == 0) {
             if (aborted(sh)) return 0u;
             if (now_ns() - t0 > (unsigned long long)sh.timeout_ns) {
@@ -385,6 +409,66 @@ __device__ uint32_t poll_tag(const Sh &sh, const uint64_t *p, unsigned tag, int 
             }
         }
     }
+}
+
+__device__ __forceinline__ uint32_t poll_tag(const Sh &sh, const uint64_t *p, unsigned tag, int where)
+{
+    const uint64_t v = ld_tag(p);
+    if ((unsigned)(v >> 32) == tag) return (uint32_t)v;
+    return poll_tag_slow(sh, p, tag, where);
+}
+
+// Bookkeeping of a bounded poll: false once the wait ran out (the abort flag
+// is then raised) or another thread gave up.  `it` counts failed rounds.
+__device__ __forceinline__ bool poll_more(const Sh &sh, unsigned it, unsigned long long &t0, int where)
+{
+    if (it == 1) t0 = now_ns();
+    else if ((it & 15) == 0) {
+        if (aborted(sh)) return false;
+        if (now_ns() - t0 > (unsigned long long)sh.timeout_ns) {
+            raise_abort(sh, where);
+            return false;
+        }
+    }
+    __nanosleep(32);
+    return true;
+}
+
+// Two items of four consecutive tagged words each (pa, pb 16-byte aligned;
+// null for no item): payloads into a and b.  All eight words are loaded
+// together; while some are missing, the lane polls the first missing one
+// alone (many CTAs poll the same words: fewer requests while waiting) and
+// then loads all eight again.  Bounded (poll_more); payloads are 0 after a
+// timeout.
+__device__ __forceinline__ void poll_tag8(const Sh &sh, const uint64_t *pa, const uint64_t *pb, unsigned tag, int where,
+                                          uint32_t (&a)[4], uint32_t (&b)[4])
+{
+    const uint64_t none = (uint64_t)tag << 32;
+    uint64_t v[8];
+    unsigned long long t0 = 0;
+    unsigned it = 0;
+#pragma unroll 1
+    for (;;) {
+#pragma unroll
+        for (int j = 0; j < 8; ++j) v[j] = none;
+        if (pa) { ld_tag2(pa, v[0], v[1]); ld_tag2(pa + 2, v[2], v[3]); }
+        if (pb) { ld_tag2(pb, v[4], v[5]); ld_tag2(pb + 2, v[6], v[7]); }
+        const uint64_t *pm = nullptr;
+#pragma unroll
+        for (int j = 7; j >= 0; --j)
+            if ((unsigned)(v[j] >> 32) != tag) pm = j < 4 ? pa + j : pb + (j - 4);
+        if (!pm) break;
+        bool more = true;
+#pragma unroll 1
+        while ((more = poll_more(sh, ++it, t0, where)) && (unsigned)(ld_tag(pm) >> 32) != tag) {}
+        if (!more) {
+#pragma unroll
+            for (int j = 0; j < 8; ++j) v[j] = 0;
+            break;
+        }
+    }
+#pragma unroll
+    for (int j = 0; j < 4; ++j) { a[j] = (uint32_t)v[j]; b[j] = (uint32_t)v[4 + j]; }
 }
 
 // Grid-wide barrier over the compute warps of every CTA.  The arrival
@@ -412,23 +496,24 @@ __device__ bool grid_sync(const KParams &kp, const Sh &sh, int &nsync)
     return !cbar_or(aborted(sh));
 }
 
-__device__ void kernel_exit(const Sh &sh, int max_slots)
+__device__ void kernel_exit(const Sh &sh)
 {
     if (threadIdx.x == 0 && !aborted(sh)) {
         Ctrl *ctrl = sh.ctrl;
         const unsigned old = atom_add_acqrel(&ctrl->exit, 1u);
         if (old == gridDim.x - 1) {
-            for (int i = 0; i < max_slots; ++i) st_relaxed(&sh.act_done[i], 0u);
             st_relaxed(&ctrl->count, 0u);
             st_relaxed(&ctrl->exit, 0u);
         }
     }
 }
 
+// Part c of P of n items: [n c / P, n (c + 1) / P).  n P < 2^32 (the host
+// plan checks the largest n).
 __device__ __forceinline__ void split(int n, int P, int c, int &a, int &b)
 {
-    a = (int)((long long)n * c / P);
-    b = (int)((long long)n * (c + 1) / P);
+    a = (int)((unsigned)n * (unsigned)c / (unsigned)P);
+    b = (int)((unsigned)n * (unsigned)(c + 1) / (unsigned)P);
 }
 
 // This CTA's output rows [h0, h1): whole pairs of rows, so that a row pair of
@@ -881,6 +966,151 @@ __device__ __noinline__ void dn_k(const float4 *act, const float *asum, int K, c
     dn_k_body<B, R>(act, asum, K, rows0, cnt, rowb, mask, pair0, g0, dst, hs, ts);
 }
 
+// ---------------------------------------------- one token vector in registers
+//
+// When a call has one token vector (one row of the mask) and a row has at
+// most 32 groups (K <= 2048), each lane of a row keeps its group's 64 inputs
+// in registers and the warp walks the rows: per row only the codes, scale and
+// bias are read from shared memory, and the loop body is small enough to run
+// from the innermost instruction cache after the first row.  The arithmetic
+// per row is that of grp_cls with NR = 1 (same sub-group visit order, same
+// class accumulators, same lane reduction), so a row's result is bit-for-bit
+// the one the general kernels give.
+
+// Sub-group of group g visited at position v (0 .. 3) by for_subgroups.
+template <int BITS>
+__device__ __forceinline__ int visit_sg(int g, int v)
+{
+    if constexpr (BITS == 6) return 2 * ((v >> 1) ^ ((g >> 3) & 1)) + (v & 1);
+    else if constexpr (BITS == 8) return (v + chunk_rot<8>(g)) & 3;
+    else return 2 * (((v >> 1) + chunk_rot<4>(g)) & 1) + (v & 1);
+}
+
+// The lane's inputs of group g of an arranged vector at shared address xq,
+// in visit order: x[4 v + t] = inputs 64 g + 4 (4 sg + t) .., sg = visit_sg(g, v).
+template <int BITS>
+__device__ __forceinline__ void load_x1(uint32_t xq, int g, int G, float4 (&x)[16])
+{
+#pragma unroll
+    for (int v = 0; v < 4; ++v) {
+        const int sg = visit_sg<BITS>(g, v);
+#pragma unroll
+        for (int t = 0; t < 4; ++t) x[4 * v + t] = ldsf4(xq + g * 16 + (4 * sg + t) * G * 16);
+    }
+}
+
+// The lane's part of row . x (group g), before the reduction over the lanes
+// of the row: exactly grp_cls<BITS, 1, 1> on a zero accumulator.
+template <int BITS>
+__device__ __forceinline__ float dot1(uint32_t row, int g, int K, const float4 (&x)[16], float xsum)
+{
+    using PT = Pairs<BITS>;
+    constexpr int NC = PT::NC, NA = BITS == 6 ? NC : 2 * NC;
+    float s, b;
+    scale_bias(row, K, BITS, g, s, b);
+    float2 A[NA];
+#pragma unroll
+    for (int c = 0; c < NA; ++c) A[c] = make_float2(0.f, 0.f);
+#pragma unroll
+    for (int v = 0; v < 4; ++v) {
+        const int sg = visit_sg<BITS>(g, v);
+        uint32_t w[BITS / 2];
+        if constexpr (BITS == 6) {
+            // 12 bytes at row + 48 g + 12 sg: 8-byte aligned for even sg
+            const uint32_t a = row + g * 48 + 12 * sg;
+            if (sg & 1) {
+                w[0] = lds1(a);
+                const uint2 p = lds2(a + 4);
+                w[1] = p.x; w[2] = p.y;
+            } else {
+                const uint2 p = lds2(a);
+                w[0] = p.x; w[1] = p.y;
+                w[2] = lds1(a + 8);
+            }
+        } else if constexpr (BITS == 8) {
+            const uint4 p = lds4(row + g * 64 + 16 * sg);
+            w[0] = p.x; w[1] = p.y; w[2] = p.z; w[3] = p.w;
+        } else {
+            const uint2 p = lds2(row + g * 32 + 8 * sg);
+            w[0] = p.x; w[1] = p.y;
+        }
+        const int half = NA > NC ? (v & 1) * NC : 0;
+        PT::each(w, [&](int i, float a, float bb) {
+            A[PT::cls(i) + half] = __ffma2_rn(make_float2(a, bb), xpair(x[4 * v + (i >> 1)], i & 1), A[PT::cls(i) + half]);
+        });
+    }
+    float t = 0.f;
+#pragma unroll
+    for (int c = 0; c < NA; ++c) {
+        const int i0 = first_of_class<PT>(c % NC);
+        t = fmaf(A[c].x, __uint_as_float(cls_bits(PT::pa(i0))), t);
+        t = fmaf(A[c].y, __uint_as_float(cls_bits(PT::pb(i0))), t);
+    }
+    return fmaf(s, t, fmaf(b, xsum, 0.f));
+}
+
+// Rows against one token vector: the warp takes rows r0 + RPP i (lanes
+// lg of a row group, RPP = 32 / LPR row groups) of nrows at rows + r * rstride
+// (shared memory), each of K inputs.  emit(r, value) runs on the first lane
+// of the row group with the complete dot product of row r.
+template <int BITS, typename F>
+__device__ __forceinline__ void rows1(uint32_t rows, int rstride, int nrows, int K, uint32_t xq, uint32_t xsq, F &&emit)
+{
+    const int lane = threadIdx.x & 31;
+    const int G = K >> 6, lgL = ilog2(G), LPR = 1 << lgL, RPP = 32 >> lgL;
+    const int g = lane & (LPR - 1), lr = lane >> lgL;
+    float4 x[16];
+    load_x1<BITS>(xq, g, G, x);
+    const float xsum = ldsf1(xsq + 4 * g);
+#pragma unroll 1
+    for (int r0 = 0; r0 < nrows; r0 += RPP) {
+        const int r = r0 + lr;
+        float acc = dot1<BITS>(rows + (uint32_t)(min(r, nrows - 1) * rstride), g, K, x, xsum);
+#pragma unroll 1
+        for (int o = LPR >> 1; o >= 1; o >>= 1) acc += __shfl_xor_sync(FULLMASK, acc, o);
+        if (g == 0 && r < nrows) emit(r, acc);
+    }
+}
+
+// Gate/up units [0, cnt) (unit u: gate row 2u, up row 2u + 1) against one
+// token vector: dst[u] = silu(gate) * up, tagged.  A row group takes a whole
+// unit.
+template <int BITS>
+__device__ __noinline__ void gu1(uint32_t units, int cnt, int rowb, int H, uint32_t xq, uint32_t xsq, uint64_t *dst,
+                                 unsigned tag)
+{
+    const int lane = threadIdx.x & 31;
+    const int G = H >> 6, lgL = ilog2(G), LPR = 1 << lgL, RPP = 32 >> lgL;
+    const int g = lane & (LPR - 1), lr = lane >> lgL;
+    float4 x[16];
+    load_x1<BITS>(xq, g, G, x);
+    const float xsum = ldsf1(xsq + 4 * g);
+#pragma unroll 1
+    for (int u0 = 0; u0 < cnt; u0 += RPP) {
+        const uint32_t ru = units + (uint32_t)(2 * min(u0 + lr, cnt - 1) * rowb);
+        float gt = 0.f, up = 0.f;
+#pragma unroll 1
+        for (int k = 0; k < 2; ++k) {
+            const float v = dot1<BITS>(ru + k * rowb, g, H, x, xsum);
+            if (k) up = v;
+            else gt = v;
+        }
+#pragma unroll 1
+        for (int o = LPR >> 1; o >= 1; o >>= 1) {
+            gt += __shfl_xor_sync(FULLMASK, gt, o);
+            up += __shfl_xor_sync(FULLMASK, up, o);
+        }
+        if (g == 0 && u0 + lr < cnt) st_tag(dst + u0 + lr, __float_as_uint(gt / (1.0f + expf(-gt)) * up), tag);
+    }
+}
+
+// Rows [0, cnt) against one vector: dst[r * ds] = row r . x (plain fp32).
+template <int BITS>
+__device__ __noinline__ void plain1(uint32_t rows, int cnt, int rowb, int K, uint32_t xq, uint32_t xsq, float *dst, int ds)
+{
+    rows1<BITS>(rows, rowb, cnt, K, xq, xsq, [&](int r, float v) { dst[(size_t)r * ds] = v; });
+}
+
 // Dispatch on (bits, row-group size): code = bits * 8 + nr.
 #define MOE_RK_CASES(FN, ARGS)                                                                   \
     case 4 * 8 + 1: FN<4, 1> ARGS; break;                                                        \
@@ -893,6 +1123,15 @@ __device__ __noinline__ void dn_k(const float4 *act, const float *asum, int K, c
 __device__ __noinline__ void gu_units(const Sh &sh, int H, int bits, const uint8_t *units, int cnt, int rowb,
                                          uint32_t mask, uint64_t *dst, int ld, unsigned tag)
 {
+    if (__popc(mask) == 1 && H <= 32 * kGroup && bits != 0) {
+        const int m = __ffs(mask) - 1;
+        const uint32_t xq = smem_u32(sh.xs) + (uint32_t)(m * H * 4), xsq = smem_u32(sh.xsum) + (uint32_t)(m * (H / kGroup) * 4);
+        uint64_t *d = dst + (size_t)m * ld;
+        if (bits == 6) gu1<6>(smem_u32(units), cnt, rowb, H, xq, xsq, d, tag);
+        else if (bits == 8) gu1<8>(smem_u32(units), cnt, rowb, H, xq, xsq, d, tag);
+        else gu1<4>(smem_u32(units), cnt, rowb, H, xq, xsq, d, tag);
+        return;
+    }
     for_row_groups(mask, [&](int g0, int nr) {
         switch (bits * 8 + nr) {
             MOE_RK_CASES(gu_k, (sh.xs, sh.xsum, H, units, cnt, rowb, mask, g0, dst, ld, tag))
@@ -904,6 +1143,15 @@ __device__ __noinline__ void gu_units(const Sh &sh, int H, int bits, const uint8
 __device__ __noinline__ void one_row(const Sh &sh, int H, int bits, const uint8_t *row, uint32_t mask,
                                         void *dst, int ms, unsigned tag)
 {
+    if (__popc(mask) == 1 && H <= 32 * kGroup && bits != 0 && tag == 0u) {
+        const int m = __ffs(mask) - 1;
+        const uint32_t xq = smem_u32(sh.xs) + (uint32_t)(m * H * 4), xsq = smem_u32(sh.xsum) + (uint32_t)(m * (H / kGroup) * 4);
+        float *d = static_cast<float *>(dst) + (size_t)m * ms;
+        if (bits == 6) plain1<6>(smem_u32(row), 1, 0, H, xq, xsq, d, 0);
+        else if (bits == 8) plain1<8>(smem_u32(row), 1, 0, H, xq, xsq, d, 0);
+        else plain1<4>(smem_u32(row), 1, 0, H, xq, xsq, d, 0);
+        return;
+    }
     for_row_groups(mask, [&](int g0, int nr) {
         switch (bits * 8 + nr) {
             MOE_RK_CASES(one_k, (sh.xs, sh.xsum, H, row, mask, g0, dst, ms, tag))
@@ -917,6 +1165,13 @@ __device__ __noinline__ void one_row(const Sh &sh, int H, int bits, const uint8_
 __device__ __noinline__ void dn_rows(const Sh &sh, int bits, const uint8_t *rows0, int cnt, int rowb, int K,
                                         uint32_t mask, int pair0, float *dst, int hs, int ts)
 {
+    if (__popc(mask) == 1 && K <= 32 * kGroup && bits != 0) {
+        const uint32_t xq = smem_u32(sh.act) + (uint32_t)(pair0 * K * 4), xsq = smem_u32(sh.asum) + (uint32_t)(pair0 * (K / kGroup) * 4);
+        if (bits == 6) plain1<6>(smem_u32(rows0), cnt, rowb, K, xq, xsq, dst, hs);
+        else if (bits == 8) plain1<8>(smem_u32(rows0), cnt, rowb, K, xq, xsq, dst, hs);
+        else plain1<4>(smem_u32(rows0), cnt, rowb, K, xq, xsq, dst, hs);
+        return;
+    }
     for_row_groups(mask, [&](int g0, int nr) {
         switch (bits * 8 + nr) {
             MOE_RK_CASES(dn_k, (sh.act, sh.asum, K, rows0, cnt, rowb, mask, pair0, g0, dst, hs, ts))
@@ -935,24 +1190,15 @@ __device__ void build_hn(const KParams &kp, const Sh &sh, const void *x, unsigne
 {
     const int H = kp.g.H, M = kp.M, G = H / kGroup, tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
     const int per_row = H / 8, lpr = ilog2(per_row), total = M * per_row;
+#pragma unroll 1
     for (int m = lane; m < M; m += 32) sh.red[m * (NCW + 1) + warp] = 0.f;
     __syncwarp();
-    // pass 1: sums of squares per (row, warp); raw values into xs
-    for (int base = 0; base < total; base += NCT) {
-        const int it = base + tid;
+    // pass 1: sums of squares per (row, warp); raw values into xs.  Two
+    // items per thread and round, both loads in flight before either is used.
+    auto item = [&](int it, const uint32_t (&aw)[4]) {
         float ss = 0.f;
         if (it < total) {
             const int m = it >> lpr, c = it & (per_row - 1);
-            uint32_t aw[4];
-            if (xtag) {
-                // the previous layer's output: tagged bf16 pairs
-                const uint64_t *xp = static_cast<const uint64_t *>(x) + (size_t)m * (H / 2) + 4 * c;
-#pragma unroll
-                for (int j = 0; j < 4; ++j) aw[j] = poll_tag(sh, xp + j, xtag, 40);
-            } else {
-                const uint4 a = __ldcg(reinterpret_cast<const uint4 *>(static_cast<const uint16_t *>(x) + (size_t)m * H) + c);
-                aw[0] = a.x; aw[1] = a.y; aw[2] = a.z; aw[3] = a.w;
-            }
             float f[8];
 #pragma unroll
             for (int j = 0; j < 4; ++j) {
@@ -968,17 +1214,37 @@ __device__ void build_hn(const KParams &kp, const Sh &sh, const void *x, unsigne
             row[(t + 1) * G + g] = make_float4(f[4], f[5], f[6], f[7]);
         }
         ss = warp_sum(ss);
-        const int wfirst = base + warp * 32;
+        const int wfirst = it - lane;
         if (lane == 0 && wfirst < total) sh.red[(wfirst >> lpr) * (NCW + 1) + warp] += ss;
+    };
+#pragma unroll 1
+    for (int base = 0; base < total; base += 2 * NCT) {
+        const int ia = base + tid, ib = ia + NCT;
+        uint32_t a[4] = {0u, 0u, 0u, 0u}, b[4] = {0u, 0u, 0u, 0u};
+        if (xtag) {
+            // the previous layer's output: tagged bf16 pairs
+            const uint64_t *xt = static_cast<const uint64_t *>(x);
+            const uint64_t *pa = ia < total ? xt + (size_t)(ia >> lpr) * (H / 2) + 4 * (ia & (per_row - 1)) : nullptr;
+            const uint64_t *pb = ib < total ? xt + (size_t)(ib >> lpr) * (H / 2) + 4 * (ib & (per_row - 1)) : nullptr;
+            poll_tag8(sh, pa, pb, xtag, 40, a, b);
+        } else {
+            const uint4 *xp = reinterpret_cast<const uint4 *>(x);
+            if (ia < total) { const uint4 v = __ldcg(xp + ia); a[0] = v.x; a[1] = v.y; a[2] = v.z; a[3] = v.w; }
+            if (ib < total) { const uint4 v = __ldcg(xp + ib); b[0] = v.x; b[1] = v.y; b[2] = v.z; b[3] = v.w; }
+        }
+        item(ia, a);
+        if (base + NCT < total) item(ib, b);
     }
     cbar();
     if (tid < M) {
         float t = 0.f;
+#pragma unroll 1
         for (int w = 0; w < NCW; ++w) t += sh.red[tid * (NCW + 1) + w];
         sh.red[tid * (NCW + 1) + NCW] = rsqrtf(t / (float)H + kp.g.eps);
     }
     cbar();
     // pass 2: scale by rinv * gamma * 2^100; group sums of hn
+#pragma unroll 1
     for (int base = 0; base < total; base += NCT) {
         const int it = base + tid;
         float gs = 0.f;
@@ -1010,6 +1276,7 @@ __device__ void build_hn(const KParams &kp, const Sh &sh, const void *x, unsigne
             sh.xsum[m * G + (c >> 3)] = gs;
         }
     }
+#pragma unroll 1
     for (int e = tid; e < kp.g.E; e += NCT) sh.emask[e] = 0u;
     cbar();
 }
@@ -1023,17 +1290,12 @@ template <typename F>
 __device__ __forceinline__ void stage_acts(const Sh &sh, int n, int K, int t0, int nt, unsigned tag, F &&src)
 {
     const int per = K / 4, lgp = ilog2(per), G = K / kGroup, total = n * per, tid = threadIdx.x - t0;
-    for (int base = 0; base < total; base += nt) {
-        const int it = base + tid;
+    auto item = [&](int it, const uint32_t (&u)[4]) {
         float gs = 0.f;
         if (it < total) {
             const int p = it >> lgp, c = it & (per - 1);
-            const uint64_t *sp = src(p) + 4 * c;
-            float4 v;
-            v.x = __uint_as_float(poll_tag(sh, sp, tag, 41));
-            v.y = __uint_as_float(poll_tag(sh, sp + 1, tag, 41));
-            v.z = __uint_as_float(poll_tag(sh, sp + 2, tag, 41));
-            v.w = __uint_as_float(poll_tag(sh, sp + 3, tag, 41));
+            const float4 v = make_float4(__uint_as_float(u[0]), __uint_as_float(u[1]), __uint_as_float(u[2]),
+                                         __uint_as_float(u[3]));
             gs = (v.x + v.y) + (v.z + v.w);
             sh.act[(size_t)p * per + (c & 15) * G + (c >> 4)] =
                 make_float4(v.x * kXScale, v.y * kXScale, v.z * kXScale, v.w * kXScale);
@@ -1044,6 +1306,17 @@ __device__ __forceinline__ void stage_acts(const Sh &sh, int n, int K, int t0, i
             const int p = it >> lgp, c = it & (per - 1);
             sh.asum[p * G + (c >> 4)] = gs;
         }
+    };
+    // two items per thread and round, both loads in flight before either is used
+#pragma unroll 1
+    for (int base = 0; base < total; base += 2 * nt) {
+        const int ia = base + tid, ib = ia + nt;
+        const uint64_t *pa = ia < total ? src(ia >> lgp) + 4 * (ia & (per - 1)) : nullptr;
+        const uint64_t *pb = ib < total ? src(ib >> lgp) + 4 * (ib & (per - 1)) : nullptr;
+        uint32_t a[4], b[4];
+        poll_tag8(sh, pa, pb, tag, 41, a, b);
+        item(ia, a);
+        if (base + nt < total) item(ib, b);
     }
 }
 
@@ -1061,27 +1334,52 @@ __device__ __forceinline__ float unkey(uint32_t k)
     return __uint_as_float((k & 0x80000000u) ? (k & 0x7FFFFFFFu) : ~k);
 }
 
-// Top-k of one row by a warp, keyed on (logit descending, expert id
-// ascending): k rounds of the warp-wide best (redux.sync) of the lanes'
-// best remaining logits, the winning lane dropping it.  Exact ties between
-// lanes go to the lower expert id.  Needs k <= NPL.
+// Top-k of router row m by one warp, keyed on (logit descending, expert id
+// ascending); lane `lane` holds experts lane + 32 i.  k rounds: the warp-wide
+// largest of the lanes' best remaining keys (redux.sync); the lane holding
+// it at its lowest index drops it and records it.  Exact ties between lanes
+// (several lanes hold the largest key) go to the lowest expert id.
+// Writes topv/tope/topw (selection order), row_w/row_pair (expert-id order;
+// row_pair holds the expert id until the slot table is built) and sigma.
 template <int NPL>
 __device__ __noinline__ void topk_row_t(const KParams &kp, const Sh &sh, int m, const uint64_t *logits, unsigned tag)
 {
     const int lane = threadIdx.x & 31;
-    const int E = kp.g.E, k = kp.g.k, Er = kp.g.Er;
+    const int E = kp.g.E, k = kp.g.k;
+    // this CTA's copy of the logits
+    const uint64_t *row = logits + ((size_t)(blockIdx.x % kLogitCopies) * kp.ws_l.maxr + m) * kp.g.Er;
+    // the lane's logits and the shared expert's gate logit, all loaded
+    // together; while some are missing the lane polls the first missing one
+    // alone (every CTA polls these words), then loads them all again
+    const uint64_t none = (uint64_t)tag << 32;
+    uint64_t v[NPL + 1];
+    unsigned long long t0 = 0;
+    unsigned it = 0;
+#pragma unroll 1
+    for (;;) {
+#pragma unroll
+        for (int i = 0; i < NPL; ++i) v[i] = lane + 32 * i < E ? ld_tag(row + lane + 32 * i) : none;
+        v[NPL] = kp.g.has_shared ? ld_tag(row + E) : none;
+        const uint64_t *pm = nullptr;
+#pragma unroll
+        for (int i = NPL; i >= 0; --i)
+            if ((unsigned)(v[i] >> 32) != tag) pm = i < NPL ? row + lane + 32 * i : row + E;
+        bool more = true;
+        if (pm) {
+#pragma unroll 1
+            while ((more = poll_more(sh, ++it, t0, 42)) && (unsigned)(ld_tag(pm) >> 32) != tag) {}
+        }
+        if (!__any_sync(FULLMASK, pm != nullptr) || !__all_sync(FULLMASK, more)) break;
+    }
+    if (threadIdx.x == 0) stamp(kp, (int)(tag - kp.epoch - 1u), 15);
     uint32_t key[NPL];
 #pragma unroll
-    for (int i = 0; i < NPL; ++i) {
-        const int e = lane + 32 * i;
-        key[i] = e < E ? fkey(__uint_as_float(poll_tag(sh, logits + (size_t)m * Er + e, tag, 42))) : 0u;
-    }
-    const float lsg = kp.g.has_shared ? __uint_as_float(poll_tag(sh, logits + (size_t)m * Er + E, tag, 42)) : 0.f;
-    uint32_t rk = 0u;   // this lane's entry of the result: round r == lane
-    int re = 0;
+    for (int i = 0; i < NPL; ++i) key[i] = lane + 32 * i < E ? fkey(__uint_as_float((uint32_t)v[i])) : 0u;
+    const float lsg = __uint_as_float((uint32_t)v[NPL]);
+    float *topv = sh.topv + m * kMaxK;
+    int *tope = sh.tope + m * kMaxK;
 #pragma unroll 1
     for (int r = 0; r < k; ++r) {
-        // the lane's best remaining key (max tree), then its lowest index
         uint32_t t[NPL];
 #pragma unroll
         for (int i = 0; i < NPL; ++i) t[i] = key[i];
@@ -1089,92 +1387,36 @@ __device__ __noinline__ void topk_row_t(const KParams &kp, const Sh &sh, int m, 
         for (int w = NPL >> 1; w > 0; w >>= 1)
 #pragma unroll
             for (int i = 0; i < w; ++i) t[i] = max(t[i], t[i + w]);
-        const uint32_t bk = t[0];
-        int bi = NPL - 1;
+        const uint32_t wk = __reduce_max_sync(FULLMASK, t[0]);
+        // the lane's lowest index holding wk (NPL if none)
+        int bi = NPL;
 #pragma unroll
-        for (int i = NPL - 2; i >= 0; --i) bi = key[i] == bk ? i : bi;
-        const uint32_t wk = __reduce_max_sync(FULLMASK, bk);
-        const unsigned bal = __ballot_sync(FULLMASK, bk == wk);
-        const int mye = lane + 32 * bi;
-        const int we = __popc(bal) == 1 ? __shfl_sync(FULLMASK, mye, __ffs(bal) - 1)
-                                        : (int)__reduce_min_sync(FULLMASK, bk == wk ? (unsigned)mye : 0xFFFFFFFFu);
-        if (lane == r) { rk = wk; re = we; }
-        if (mye == we) {
+        for (int i = NPL - 1; i >= 0; --i) bi = key[i] == wk ? i : bi;
+        const unsigned bal = __ballot_sync(FULLMASK, bi < NPL);
+        int wl = __ffs(bal) - 1;
+        if (bal & (bal - 1u)) {
+            const unsigned we = __reduce_min_sync(FULLMASK, bi < NPL ? (unsigned)(lane + 32 * bi) : 0xFFFFFFFFu);
+            wl = (int)(we & 31u);
+        }
+        if (lane == wl) {
 #pragma unroll
             for (int i = 0; i < NPL; ++i) key[i] = i == bi ? 0u : key[i];
+            topv[r] = unkey(wk);
+            tope[r] = lane + 32 * bi;
         }
-    }
-    // renormalised softmax weights over the k kept logits (the full softmax
-    // probabilities divided by their top-k sum)
-    const float vmax = unkey(__shfl_sync(FULLMASK, rk, 0));
-    const float ev = lane < k ? expf(unkey(rk) - vmax) : 0.f;
-    const float z = warp_sum(ev);
-    // rank of the lane's expert id among the k kept ones
-    int r = 0;
-#pragma unroll
-    for (int j = 0; j < NPL; ++j) {
-        const int ej = __shfl_sync(FULLMASK, re, j);
-        r += (j < k && ej < re) ? 1 : 0;
-    }
-    if (lane < k) {
-        const float wv = ev / z;
-        sh.topv[m * kMaxK + lane] = unkey(rk);
-        sh.tope[m * kMaxK + lane] = re;
-        sh.topw[m * kMaxK + lane] = wv;
-        // the same k entries ordered by expert id (combine order of the row)
-        sh.row_w[m * kMaxK + r] = wv;
-        sh.row_pair[m * kMaxK + r] = re;   // expert id for now; pair index after the slot list
-    }
-    if (lane == 0) sh.sigma[m] = kp.g.has_shared ? 1.0f / (1.0f + expf(-lsg)) : 0.f;
-}
-
-// k larger than a lane's share of the logits: k rounds of a warp-wide max
-// (redux.sync) of the lanes' best remaining keys, the lowest expert id
-// breaking exact ties.
-template <int NPL>
-__device__ __noinline__ void topk_row_rounds(const KParams &kp, const Sh &sh, int m, const uint64_t *logits, unsigned tag)
-{
-    const int lane = threadIdx.x & 31;
-    const int E = kp.g.E, k = kp.g.k, Er = kp.g.Er;
-    uint32_t key[NPL];
-#pragma unroll
-    for (int i = 0; i < NPL; ++i) {
-        const int e = lane + 32 * i;
-        key[i] = e < E ? fkey(__uint_as_float(poll_tag(sh, logits + (size_t)m * Er + e, tag, 42))) : 0u;
-    }
-    const float lsg = kp.g.has_shared ? __uint_as_float(poll_tag(sh, logits + (size_t)m * Er + E, tag, 42)) : 0.f;
-    float *topv = sh.topv + m * kMaxK;
-    int *tope = sh.tope + m * kMaxK;
-#pragma unroll 1
-    for (int r = 0; r < k; ++r) {
-        uint32_t bk = key[0];
-        int bi = 0;
-#pragma unroll
-        for (int i = 1; i < NPL; ++i)
-            if (key[i] > bk) { bk = key[i]; bi = i; }
-        const uint32_t wk = __reduce_max_sync(FULLMASK, bk);
-        const unsigned bal = __ballot_sync(FULLMASK, bk == wk);
-        const unsigned mye = (unsigned)(lane + 32 * bi);
-        unsigned we;
-        if (__popc(bal) == 1) we = __shfl_sync(FULLMASK, mye, __ffs(bal) - 1);
-        else we = __reduce_min_sync(FULLMASK, bk == wk ? mye : 0xFFFFFFFFu);
-        if (mye == we) {
-#pragma unroll
-            for (int i = 0; i < NPL; ++i)
-                if (i == bi) key[i] = 0u;
-        }
-        if (lane == 0) { topv[r] = unkey(wk); tope[r] = (int)we < E ? (int)we : 0; }
     }
     __syncwarp();
-    const float vmax = topv[0];
-    const float ev = lane < k ? expf(topv[lane] - vmax) : 0.f;
+    // renormalised softmax weights over the k kept logits (the full softmax
+    // probabilities divided by their top-k sum)
+    const float ev = lane < k ? expf(topv[lane] - topv[0]) : 0.f;
     const float z = warp_sum(ev);
     if (lane < k) {
         const float wv = ev / z;
-        sh.topw[m * kMaxK + lane] = wv;
         const int e = tope[lane];
         int r = 0;
+#pragma unroll 1
         for (int j = 0; j < k; ++j) r += tope[j] < e ? 1 : 0;
+        sh.topw[m * kMaxK + lane] = wv;
         sh.row_w[m * kMaxK + r] = wv;
         sh.row_pair[m * kMaxK + r] = e;
     }
@@ -1184,104 +1426,98 @@ __device__ __noinline__ void topk_row_rounds(const KParams &kp, const Sh &sh, in
 __device__ void topk_row(const KParams &kp, const Sh &sh, int m, const uint64_t *logits, unsigned tag)
 {
     const int E = kp.g.E;
-    const int k = kp.g.k;
-    if (E <= 64 && k <= 2) topk_row_t<2>(kp, sh, m, logits, tag);
-    else if (E <= 256 && k <= 8) topk_row_t<8>(kp, sh, m, logits, tag);
-    else if (k <= 16) topk_row_t<16>(kp, sh, m, logits, tag);
-    else topk_row_rounds<16>(kp, sh, m, logits, tag);
+    if (E <= 64) topk_row_t<2>(kp, sh, m, logits, tag);
+    else if (E <= 256) topk_row_t<8>(kp, sh, m, logits, tag);
+    else topk_row_t<16>(kp, sh, m, logits, tag);
 }
 
 // Named barrier over the first nw compute warps (the routing warps).
 __device__ __forceinline__ void rbar(int nw) { asm volatile("bar.sync 2, %0;" ::"r"(nw * 32) : "memory"); }
 
-// Routing, run by the first max(M, 1) compute warps only (one per token
-// row); the other warps work meanwhile.  Ends by telling the producer that
-// the slot table of layer l is ready.
+// Routing, run by the first M compute warps only (one per token row); the
+// other warps work meanwhile.  Builds the slot table (the distinct experts
+// of the M rows in id order, each with the mask of rows that chose it and
+// the index of its first activation pair) and turns row_pair into pair
+// indices; ends by telling the producer that the table of layer l is ready.
 __device__ void route(const KParams &kp, const Sh &sh, const uint64_t *logits, int l)
 {
     const unsigned tag = layer_tag(kp, l);
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     const int E = kp.g.E, k = kp.g.k, M = kp.M;
-    if (M == 1) {
-        // one row: the slots are its k experts in id order
-        topk_row(kp, sh, 0, logits, tag);
-        if (threadIdx.x == 0) stamp(kp, l, 12);
-        __syncwarp();
-        if (lane < k) {
-            const int e = sh.row_pair[lane];
-            sh.slot_e[lane] = e;
-            sh.slot_mask[lane] = 1u;
-            sh.slot_rowbase[lane] = lane;
-            sh.row_pair[lane] = lane;
-            if (kp.mode == kModeRouter && blockIdx.x == 0) {
-                kp.idx_out[lane] = sh.tope[lane];
-                kp.w_out[lane] = sh.topw[lane];
-            }
-        }
-        if (lane == 0) {
-            sh.flags[1] = k;
-            sh.slot_rowbase[k] = k;
-            stamp(kp, l, 13);
-        }
-        for (int t = lane; t < k; t += 32) sh.target[t] += (unsigned)kp.g.I;
-        __syncwarp();
-        if (lane == 0 && kp.mode == kModeLayers) mbar_arrive(sh.route, 1);
-        return;
-    }
     topk_row(kp, sh, warp, logits, tag);
     if (threadIdx.x == 0) stamp(kp, l, 12);
-    rbar(M);
+    if (M > 1) rbar(M);
     if (warp != 0) return;
-    for (int t = lane; t < M * k; t += 32) {
-        const int e = sh.tope[(t / k) * kMaxK + t % k];
-        atomicOr(&sh.emask[e < E ? e : 0], 1u << (t / k));
-    }
-    __syncwarp();
-    int base = 0;
-    for (int c0 = 0; c0 < E; c0 += 32) {
-        const int e = c0 + lane;
-        const uint32_t em = e < E ? sh.emask[e] : 0u;
-        const unsigned bal = __ballot_sync(FULLMASK, em != 0u);
-        if (em) {
-            const int pos = base + __popc(bal & ((1u << lane) - 1u));
-            sh.slot_e[pos] = e;
-            sh.slot_mask[pos] = em;
-            sh.eslot[e] = pos;
+    int U, npairs;
+    if (M == 1) {
+        // one row: the slots are its k experts in id order
+#pragma unroll 1
+        for (int j = lane; j < k; j += 32) {
+            sh.slot_e[j] = sh.row_pair[j];
+            sh.slot_mask[j] = 1u;
+            sh.slot_rowbase[j] = j;
+            sh.row_pair[j] = j;
         }
-        base += __popc(bal);
-    }
-    __syncwarp();
-    // slot-row pair bases: prefix sums of popc(mask) over the slots
-    int run = 0;
-    for (int s0 = 0; s0 < base; s0 += 32) {
-        const int s = s0 + lane;
-        const int pc = s < base ? __popc(sh.slot_mask[s]) : 0;
-        int inc = pc;
+        U = npairs = k;
+    } else {
+#pragma unroll 1
+        for (int m = 0; m < M; ++m)
+#pragma unroll 1
+            for (int j = lane; j < k; j += 32) atomicOr(&sh.emask[sh.tope[m * kMaxK + j]], 1u << m);
+        __syncwarp();
+        U = 0;
+#pragma unroll 1
+        for (int c0 = 0; c0 < E; c0 += 32) {
+            const int e = c0 + lane;
+            const uint32_t em = e < E ? sh.emask[e] : 0u;
+            const unsigned bal = __ballot_sync(FULLMASK, em != 0u);
+            if (em) {
+                const int pos = U + __popc(bal & ((1u << lane) - 1u));
+                sh.slot_e[pos] = e;
+                sh.slot_mask[pos] = em;
+                sh.eslot[e] = pos;
+            }
+            U += __popc(bal);
+        }
+        __syncwarp();
+        // pair bases: prefix sums of popc(mask) over the slots
+        npairs = 0;
+#pragma unroll 1
+        for (int s0 = 0; s0 < U; s0 += 32) {
+            const int s = s0 + lane;
+            const int pc = s < U ? __popc(sh.slot_mask[s]) : 0;
+            int inc = pc;
 #pragma unroll
-        for (int o = 1; o < 32; o <<= 1) {
-            const int t = __shfl_up_sync(FULLMASK, inc, o);
-            if (lane >= o) inc += t;
+            for (int o = 1; o < 32; o <<= 1) {
+                const int t = __shfl_up_sync(FULLMASK, inc, o);
+                if (lane >= o) inc += t;
+            }
+            if (s < U) sh.slot_rowbase[s] = npairs + inc - pc;
+            npairs += __shfl_sync(FULLMASK, inc, 31);
         }
-        if (s < base) sh.slot_rowbase[s] = run + inc - pc;
-        run += __shfl_sync(FULLMASK, inc, 31);
+        __syncwarp();
+#pragma unroll 1
+        for (int m = 0; m < M; ++m)
+#pragma unroll 1
+            for (int j = lane; j < k; j += 32) {
+                const int s = sh.eslot[sh.row_pair[m * kMaxK + j]];
+                sh.row_pair[m * kMaxK + j] = sh.slot_rowbase[s] + __popc(sh.slot_mask[s] & ((1u << m) - 1u));
+            }
+    }
+    if (kp.mode == kModeRouter && blockIdx.x == 0) {
+#pragma unroll 1
+        for (int m = 0; m < M; ++m)
+#pragma unroll 1
+            for (int j = lane; j < k; j += 32) {
+                kp.idx_out[m * k + j] = sh.tope[m * kMaxK + j];
+                kp.w_out[m * k + j] = sh.topw[m * kMaxK + j];
+            }
     }
     if (lane == 0) {
-        sh.flags[1] = base;
-        sh.slot_rowbase[base] = run;
+        sh.flags[1] = U;
+        sh.slot_rowbase[U] = npairs;
+        stamp(kp, l, 13);
     }
-    for (int t = lane; t < base; t += 32) sh.target[t] += (unsigned)kp.g.I;
-    __syncwarp();
-    for (int t = lane; t < M * k; t += 32) {
-        const int m = t / k, j = t % k;
-        const int e = sh.row_pair[m * kMaxK + j];
-        const int s = sh.eslot[e < E ? e : 0];
-        sh.row_pair[m * kMaxK + j] = sh.slot_rowbase[s] + __popc(sh.slot_mask[s] & ((1u << m) - 1u));
-        if (kp.mode == kModeRouter && blockIdx.x == 0) {
-            kp.idx_out[m * k + j] = sh.tope[m * kMaxK + j];
-            kp.w_out[m * k + j] = sh.topw[m * kMaxK + j];
-        }
-    }
-    if (threadIdx.x == 0) stamp(kp, l, 13);
     __syncwarp();
     if (lane == 0 && kp.mode == kModeLayers) mbar_arrive(sh.route, 1);
 }
@@ -1290,7 +1526,7 @@ __device__ void route(const KParams &kp, const Sh &sh, const uint64_t *logits, i
 
 // Workspace buffers shared between CTAs, all of tagged words.
 struct Ws {
-    uint64_t *logits;   // [maxr][Er] fp32
+    uint64_t *logits;   // [kLogitCopies][maxr][Er] fp32 (each CTA reads copy blockIdx % kLogitCopies)
     uint64_t *act;      // [max_slots][maxr][I] fp32
     uint64_t *act_s;    // [maxr][Is] fp32
     uint64_t *ping[2];  // [maxr][H / 2] bf16 pairs: outputs of the layers before the last
@@ -1309,24 +1545,10 @@ __device__ __forceinline__ Ws ws_views(const KParams &kp)
 
 // ------------------------------------------------------------- schedules
 
-// Prefetch buffer of one layer: gamma, this CTA's router rows, then as many
-// of its shared units as fit (the rest go through the ring as P1 stages).
-// Prefetch buffer of one layer: gamma, this CTA's router rows, the shared
-// expert's down rows of its output slice (when they fit) and as many of its
-// shared gate/up units as fit; the rest go through the ring.
-struct PbPlan {
-    int ra, rb;        // router rows
-    int ua, ub;        // shared units of this CTA
-    int upb;           // units held in the buffer: [ua, ua + upb)
-    int h0, nh;        // output slice (shared down rows h0 .. h0 + nh)
-    int dpb;           // shared down rows held in the buffer: nh or 0
-    int off_router, off_sdown, off_units, bytes;
-};
-
-__device__ __forceinline__ PbPlan pb_plan(const KParams &kp)
+// This CTA's plan (run once, by one thread, into shared memory).
+__device__ void cta_plan(const KParams &kp, CtaPlan &b)
 {
     const Geo &g = kp.g;
-    PbPlan b;
     split(g.Er, gridDim.x, blockIdx.x, b.ra, b.rb);
     int h1;
     hslice(g.H, b.h0, h1);
@@ -1342,21 +1564,21 @@ __device__ __forceinline__ PbPlan pb_plan(const KParams &kp)
     const int room = kp.p.pb_bytes - b.off_units;
     b.upb = ub2 > 0 ? min(b.ub - b.ua, max(0, room / ub2)) : 0;
     b.bytes = b.off_units + b.upb * ub2;
-    return b;
 }
 
 // Ring stages of a layer, in order: P1 units that did not fit the prefetch
-// buffer, P1b shared down rows, P2 routed gate/up units, P3 routed down
-// rows.  `f` gets (src, bytes, slot-or-kind, first, count).
+// buffer, P2 routed gate/up units, P1b shared down rows that did not fit it,
+// P3 routed down rows.  `f` gets (src, bytes, slot-or-kind, first, count).
 // The P1 overflow is counted in shared-expert rows (row 2u is the gate row
 // of unit u, row 2u + 1 its up row); `first` is relative to the CTA's rows.
 template <typename F>
-__device__ __forceinline__ void sched_p1x(const KParams &kp, const LayerPtrs &Lp, F &&f)
+__device__ __forceinline__ void sched_p1x(const KParams &kp, const Sh &sh, const LayerPtrs &Lp, F &&f)
 {
     const Geo &g = kp.g;
     if (kp.mode != kModeLayers || !g.has_shared || g.sg_bytes == 0) return;
-    const PbPlan b = pb_plan(kp);
-    const int cr = max(1, kp.p.S / g.sg_bytes);
+    const CtaPlan &b = *sh.cp;
+    const int cr = max(1, sh.S / g.sg_bytes);
+#pragma unroll 1
     for (int r = 2 * (b.ua + b.upb); r < 2 * b.ub; r += cr) {
         const int n = min(cr, 2 * b.ub - r);
         f(Lp.sgu + (size_t)r * g.sg_bytes, n * g.sg_bytes, -2, r - 2 * b.ua, n);
@@ -1365,13 +1587,14 @@ __device__ __forceinline__ void sched_p1x(const KParams &kp, const LayerPtrs &Lp
 
 // Shared down rows that did not fit the prefetch buffer.
 template <typename F>
-__device__ __forceinline__ void sched_p1b(const KParams &kp, const LayerPtrs &Lp, F &&f)
+__device__ __forceinline__ void sched_p1b(const KParams &kp, const Sh &sh, const LayerPtrs &Lp, F &&f)
 {
     const Geo &g = kp.g;
     if (kp.mode != kModeLayers || !g.has_shared) return;
-    const PbPlan b = pb_plan(kp);
+    const CtaPlan &b = *sh.cp;
     if (b.dpb) return;
-    const int cd = max(1, min(kp.p.S / g.sd_bytes, (b.nh + 1) / 2));
+    const int cd = max(1, min(sh.S / g.sd_bytes, (b.nh + 1) / 2));
+#pragma unroll 1
     for (int r = 0; r < b.nh; r += cd) {
         const int n = min(cd, b.nh - r);
         f(Lp.sdown + (size_t)(b.h0 + r) * g.sd_bytes, n * g.sd_bytes, -1, r, n);
@@ -1388,12 +1611,15 @@ __device__ __forceinline__ void sched_p2(const KParams &kp, const Sh &sh, const 
     split(U * g.I, gridDim.x, blockIdx.x, a, b);
     // about one stage per compute warp, an even number of units (a lane
     // takes two at a time) where the stage size allows
-    const int cu = max(1, min(kp.p.S / ub, 2 * ((b - a + 2 * NCW - 1) / (2 * NCW))));
+    const int cu = max(1, min(sh.S / ub, 2 * ((b - a + 2 * NCW - 1) / (2 * NCW))));
+    int s = (int)((unsigned)a / (unsigned)g.I), j = a - s * g.I;
+#pragma unroll 1
     for (int n = a; n < b;) {
-        const int s = n / g.I, j = n % g.I;
-        const int cnt = min(cu, min(b, (s + 1) * g.I) - n);
+        const int cnt = min(cu, min(b - n, g.I - j));
         f(Lp.gu + ((size_t)sh.slot_e[s] * g.I + j) * ub, cnt * ub, s, j, cnt);
         n += cnt;
+        j += cnt;
+        if (j == g.I) { j = 0; ++s; }
     }
 }
 
@@ -1402,14 +1628,14 @@ __device__ __forceinline__ void sched_p3(const KParams &kp, const Sh &sh, const 
 {
     const Geo &g = kp.g;
     const int U = sh.flags[1];
-    int h0, h1;
-    hslice(g.H, h0, h1);
-    const int nh = h1 - h0;
+    const int h0 = sh.cp->h0, nh = sh.cp->nh;
     // about one stage per compute warp over the layer
     const int per_slot = max(1, (NCW + U - 1) / max(1, U));
-    const int cd = max(1, min(kp.p.S / g.d_bytes, (nh + per_slot - 1) / per_slot));
+    const int cd = max(1, min(sh.S / g.d_bytes, (nh + per_slot - 1) / per_slot));
+#pragma unroll 1
     for (int s = 0; s < U; ++s) {
         const int e = sh.slot_e[s];
+#pragma unroll 1
         for (int r = 0; r < nh; r += cd) {
             const int n = min(cd, nh - r);
             f(Lp.down + ((size_t)e * g.H + h0 + r) * g.d_bytes, n * g.d_bytes, s, r, n);
@@ -1417,146 +1643,258 @@ __device__ __forceinline__ void sched_p3(const KParams &kp, const Sh &sh, const 
     }
 }
 
-// ------------------------------------------------------------- producer
+// ------------------------------------------------------------- the ring
 
-// Lane `lane` issues the stages q with q % NP == lane.  NS is a multiple of
-// NP, so the lane itself issued the previous round of the slot it reuses.
-__device__ __forceinline__ bool issue(const Sh &sh, unsigned q, const uint8_t *src, int bytes)
+// Position of stage q in the ring: slot q % NS, phase parity (q / NS) & 1,
+// and q modulo the number of consumer warps (its owner), advanced one stage
+// at a time without dividing.
+struct Cursor {
+    int slot;
+    unsigned par;
+    int turn;
+    bool reuse;   // the slot held an earlier stage (q >= NS)
+};
+
+__device__ __forceinline__ Cursor cursor0() { return Cursor{0, 0u, 0, false}; }
+
+__device__ __forceinline__ void cursor_next(Cursor &c, int NS)
 {
-    const int slot = (int)(q % (unsigned)sh.NS);
-    const unsigned n = q / (unsigned)sh.NS;
-    if (n > 0 && !wait_bar(sh, &sh.empty[slot], (n - 1) & 1u, 1)) return false;
-    if (aborted(sh)) return false;
-    mbar_expect_tx(&sh.full[slot], (unsigned)bytes);
-    bulk_load(sh.ring + (size_t)slot * sh.S, src, (unsigned)bytes, &sh.full[slot]);
-    return true;
+    if (++c.slot == NS) { c.slot = 0; c.par ^= 1u; c.reuse = true; }
+    if (++c.turn == NCW) c.turn = 0;
 }
 
-__device__ __forceinline__ void ring_producer(const KParams &kp, const Sh &sh, int lane)
+// One batch of at most NS stages (no two in the same slot), one per lane of
+// the producer warp: each lane with a stage waits until the consumer released
+// the previous stage of its slot, then starts the bulk copy.  The lanes poll
+// together, so the copies go out as fast as slots free up and no lane's wait
+// holds up another's issue.  False on timeout or abort (the same for every
+// lane).
+__device__ __noinline__ bool issue_batch(const Sh &sh, bool pending, int slot, unsigned par, bool reuse,
+                                         const uint8_t *src, int bytes)
 {
-    unsigned q = 0;
-    bool ok = true;
-    auto each = [&](const uint8_t *src, int bytes, int, int, int) {
-        if (ok && (int)(q % NP) == lane) ok = issue(sh, q, src, bytes);
-        ++q;
-    };
+    unsigned long long t0 = 0;
+#pragma unroll 1
+    for (unsigned it = 1;; ++it) {
+        if (pending && (!reuse || mbar_test(&sh.empty[slot], par ^ 1u))) {
+            mbar_expect_tx(&sh.full[slot], (unsigned)bytes);
+            bulk_load(sh.ring + (size_t)slot * sh.S, src, (unsigned)bytes, &sh.full[slot]);
+            pending = false;
+        }
+        if (!__any_sync(FULLMASK, pending)) return true;
+        const bool go = poll_more(sh, it, t0, 1);
+        if (!__all_sync(FULLMASK, go)) return false;
+    }
+}
+
+// Every stage of one schedule pass (`sched` enumerates them in ring order),
+// in batches of NS stages: stage base + j of a batch goes to lane j.
+template <typename Sched>
+__device__ __forceinline__ bool issue_pass(const Sh &sh, Cursor &c, int lane, Sched &&sched)
+{
+    const Cursor start = c;
+#pragma unroll 1
+    for (int base = 0;; base += sh.NS) {
+        Cursor cur = start;
+        int idx = 0;
+        const uint8_t *src = nullptr;
+        int bytes = 0, slot = 0;
+        unsigned par = 0u;
+        bool reuse = false;
+        sched([&](const uint8_t *s, int b, int, int, int) {
+            if (idx - base == lane && lane < sh.NS) {
+                src = s;
+                bytes = b;
+                slot = cur.slot;
+                par = cur.par;
+                reuse = cur.reuse;
+            }
+            ++idx;
+            cursor_next(cur, sh.NS);
+        });
+        c = cur;
+        if (base >= idx) return true;
+        if (!issue_batch(sh, src != nullptr, slot, par, reuse, src, bytes)) return false;
+        if (base + sh.NS >= idx) return true;
+    }
+}
+
+// Layer l's prefetch buffer (see CtaPlan) into sh.pb.
+__device__ __forceinline__ void pb_issue(const KParams &kp, const Sh &sh, int l)
+{
+    const Geo &g = kp.g;
+    const CtaPlan &b = *sh.cp;
+    const LayerPtrs &Lp = kp.layer[l];
+    mbar_expect_tx(sh.pb_full, (unsigned)b.bytes);
+    bulk_load(sh.pb, Lp.gamma, (unsigned)(g.H * 2), sh.pb_full);
+    if (b.rb > b.ra)
+        bulk_load(sh.pb + b.off_router, Lp.router + (size_t)b.ra * g.rr_bytes, (unsigned)((b.rb - b.ra) * g.rr_bytes),
+                  sh.pb_full);
+    if (b.dpb > 0)
+        bulk_load(sh.pb + b.off_sdown, Lp.sdown + (size_t)b.h0 * g.sd_bytes, (unsigned)(b.dpb * g.sd_bytes), sh.pb_full);
+    if (b.upb > 0)
+        bulk_load(sh.pb + b.off_units, Lp.sgu + (size_t)b.ua * 2 * g.sg_bytes, (unsigned)(b.upb * 2 * g.sg_bytes),
+                  sh.pb_full);
+}
+
+// The producer warp (all 32 lanes, in step).  Lane 0 fills the prefetch
+// buffer: layer 0's at once, layer l + 1's once layer l's routed gate/up
+// stages are on their way and every compute warp is done with layer l's
+// buffer.  Per layer the copies go out in the order the layer needs them:
+// shared rows past the buffer, then (after routing) the routed gate/up
+// stages, the next layer's buffer, an L2 prefetch of every routed down stage
+// (the ring holds only part of a layer), the shared down rows past the
+// buffer and the routed down stages.
+__device__ __forceinline__ void producer(const KParams &kp, const Sh &sh, int lane)
+{
+    Cursor c = cursor0();
+    int pb_issued = 1;
+    if (lane == 0) pb_issue(kp, sh, 0);
     if (kp.mode == kModeLayers) {
-        for (int l = 0; l < kp.L && ok; ++l) {
+#pragma unroll 1
+        for (int l = 0; l < kp.L; ++l) {
             const LayerPtrs &Lp = kp.layer[l];
-            sched_p1x(kp, Lp, each);
-            if (!ok) break;
+            if (!issue_pass(sh, c, lane, [&](auto &&f) { sched_p1x(kp, sh, Lp, f); })) break;
             if (lane == 0) stamp(kp, l, 9);
             if (!wait_bar(sh, sh.route, (unsigned)l & 1u, 2)) break;
             if (lane == 0) stamp(kp, l, 10);
-            sched_p2(kp, sh, Lp, each);
-            sched_p1b(kp, Lp, each);
-            sched_p3(kp, sh, Lp, each);
+            if (!issue_pass(sh, c, lane, [&](auto &&f) { sched_p2(kp, sh, Lp, f); })) break;
+            if (lane == 0) stamp(kp, l, 14);
+            if (l + 1 < kp.L) {
+                if (!wait_bar(sh, sh.pb_empty, (unsigned)l & 1u, 3)) break;
+                if (lane == 0 && !aborted(sh)) pb_issue(kp, sh, l + 1);
+                pb_issued = l + 2;
+            }
+            int turn = 0;
+            sched_p3(kp, sh, Lp, [&](const uint8_t *src, int bytes, int, int, int) {
+                if (turn == lane) prefetch_l2(src, (unsigned)bytes);
+                if (++turn == 32) turn = 0;
+            });
+            if (!issue_pass(sh, c, lane, [&](auto &&f) { sched_p1b(kp, sh, Lp, f); })) break;
+            if (!issue_pass(sh, c, lane, [&](auto &&f) { sched_p3(kp, sh, Lp, f); })) break;
             if (lane == 0) stamp(kp, l, 11);
+            if (aborted(sh)) break;
         }
     }
-    // Let this lane's copies still in flight land before the CTA can exit.
-    const unsigned first = q > (unsigned)sh.NS ? q - (unsigned)sh.NS : 0u;
-    for (unsigned t = first; t < q; ++t) {
-        if ((int)(t % NP) != lane) continue;
-        const int slot = (int)(t % (unsigned)sh.NS);
+    // Let the copies still in flight land before the CTA can exit: slot s
+    // was last filled in the cursor's round if s < c.slot, else in the round
+    // before (if there was one).  Lane 0 waits for the last prefetch buffer.
+    if (lane == 0) {
         const unsigned long long t0 = now_ns();
-        while (!mbar_try_wait(&sh.full[slot], (t / (unsigned)sh.NS) & 1u))
+#pragma unroll 1
+        while (!mbar_try_wait(sh.pb_full, (unsigned)(pb_issued - 1) & 1u))
             if (now_ns() - t0 > (unsigned long long)sh.timeout_ns) break;
     }
-}
-
-// The prefetch lane: layer l's buffer is loaded once every compute warp is
-// done with layer l - 1's P1.
-__device__ __forceinline__ void pb_producer(const KParams &kp, const Sh &sh)
-{
-    const Geo &g = kp.g;
-    const PbPlan b = pb_plan(kp);
-    int issued = 0;
-    for (int l = 0; l < kp.L; ++l) {
-        if (l > 0 && !wait_bar(sh, sh.pb_empty, (unsigned)(l - 1) & 1u, 3)) break;
-        if (aborted(sh)) break;
-        const LayerPtrs &Lp = kp.layer[l];
-        mbar_expect_tx(sh.pb_full, (unsigned)b.bytes);
-        bulk_load(sh.pb, Lp.gamma, (unsigned)(g.H * 2), sh.pb_full);
-        if (b.rb > b.ra)
-            bulk_load(sh.pb + b.off_router, Lp.router + (size_t)b.ra * g.rr_bytes,
-                      (unsigned)((b.rb - b.ra) * g.rr_bytes), sh.pb_full);
-        if (b.dpb > 0)
-            bulk_load(sh.pb + b.off_sdown, Lp.sdown + (size_t)b.h0 * g.sd_bytes, (unsigned)(b.dpb * g.sd_bytes),
-                      sh.pb_full);
-        if (b.upb > 0)
-            bulk_load(sh.pb + b.off_units, Lp.sgu + (size_t)b.ua * 2 * g.sg_bytes,
-                      (unsigned)(b.upb * 2 * g.sg_bytes), sh.pb_full);
-        issued = l + 1;
-        if (kp.mode == kModeRouter) break;
-    }
-    // the last buffer issued must land before the CTA can exit
-    if (issued > 0) {
+#pragma unroll 1
+    for (int s = lane; s < sh.NS; s += 32) {
+        const bool cur = s < c.slot;
+        if (!cur && !c.reuse) continue;
+        const unsigned par = cur ? c.par : c.par ^ 1u;
         const unsigned long long t0 = now_ns();
-        while (!mbar_try_wait(sh.pb_full, (unsigned)(issued - 1) & 1u))
+#pragma unroll 1
+        while (!mbar_try_wait(&sh.full[s], par))
             if (now_ns() - t0 > (unsigned long long)sh.timeout_ns) break;
     }
 }
 
 // -------------------------------------------------------- compute warps
 
+// Trace bookkeeping of one phase's stages (diagnostic stamps of the first
+// `tmax` stages a warp takes, at events tbase, tbase + 1, tbase + 2).
+struct StageTrace {
+    const KParams *kp;
+    int l, count, base, max;
+};
+
 // Stage q belongs to warp q % NCW (NS is a multiple of NCW, so the warp
 // itself consumed the previous round of the slot before it waits on this one).
 template <typename F>
-__device__ __forceinline__ void consume(const Sh &sh, unsigned &q, int where, F &&f, const KParams *tk = nullptr,
-                                        int tl = 0, int *tcount = nullptr, int tbase = 0, int tmax = 0)
+__device__ __forceinline__ void consume(const Sh &sh, Cursor &c, int where, F &&f, StageTrace *tr = nullptr)
 {
-    const unsigned me = q++;
-    if ((int)(me % NCW) != (int)(threadIdx.x >> 5)) return;
-    const int slot = (int)(me % (unsigned)sh.NS);
-    const bool st = tk && *tcount < tmax;
-    if (st) wstamp(*tk, tl, tbase);
-    if (!aborted(sh) && wait_bar(sh, &sh.full[slot], (me / (unsigned)sh.NS) & 1u, where)) {
-        if (st) wstamp(*tk, tl, tbase + 1);
+    const bool mine = c.turn == (int)(threadIdx.x >> 5);
+    const int slot = c.slot;
+    const unsigned par = c.par;
+    cursor_next(c, sh.NS);
+    if (!mine) return;
+    const bool st = tr && tr->kp && tr->count < tr->max;
+    if (st) wstamp(*tr->kp, tr->l, tr->base);
+    if (!aborted(sh) && wait_bar(sh, &sh.full[slot], par, where)) {
+        if (st) wstamp(*tr->kp, tr->l, tr->base + 1);
         f(sh.ring + (size_t)slot * sh.S);
     }
     __syncwarp();
-    if (st) { wstamp(*tk, tl, tbase + 2); ++*tcount; }
+    if (st) { wstamp(*tr->kp, tr->l, tr->base + 2); ++tr->count; }
     if ((threadIdx.x & 31) == 0) mbar_arrive(&sh.empty[slot], 1);
 }
 
-// P1: router rows and shared gate/up rows of this CTA from the prefetch
-// buffer (warp w takes rows w, w + NCW, ...), then any units that came
-// through the ring.  Router rows -> logits; shared units -> act_s.
-__device__ void phase1(const KParams &kp, const Sh &sh, const LayerPtrs &Lp, unsigned &q, const Ws &w, int l)
+// P1 and routing.  The first M compute warps route (one token row each),
+// waiting on every CTA's router logits; the other warps compute this CTA's
+// router rows first and its shared gate/up rows from the prefetch buffer
+// after them (so that the logits every CTA waits for go out first), then the
+// SwiGLU of the CTA's shared units.  Shared rows past the buffer come through
+// the ring; their stages go to every compute warp in turn, so when there are
+// any the SwiGLU waits for the routing warps as well.
+__device__ void phase1(const KParams &kp, const Sh &sh, const LayerPtrs &Lp, Cursor &q, const Ws &w, int l)
 {
     const Geo &g = kp.g;
     const uint32_t all = (1u << kp.M) - 1u;
-    const int warp = threadIdx.x >> 5, maxr = kp.p.maxr;
-    const PbPlan b = pb_plan(kp);
+    const int warp = threadIdx.x >> 5, maxr = kp.p.maxr, M = kp.M;
+    const CtaPlan &b = *sh.cp;
     const int nr = b.rb - b.ra, nrows = nr + 2 * b.upb;
+    const bool ring_rows = b.ub - b.ua > b.upb;
     wstamp(kp, l, 14);
-    for (int i = warp; i < nrows; i += NCW) {
-        if (i < nr) {
-            // (debug switch: one logit of layer 0 stays unpublished)
-            if (!(l == 0 && kp.skip_row == b.ra + i))
-                one_row(sh, g.H, g.qb, sh.pb + b.off_router + (size_t)i * g.rr_bytes, all, w.logits + b.ra + i, g.Er,
-                        layer_tag(kp, l));
-        } else {
-            const int j = i - nr;   // gate row of unit j / 2, or its up row
-            one_row(sh, g.H, g.sb, sh.pb + b.off_units + (size_t)j * g.sg_bytes, all, sh.p1v + j * maxr, 1, 0u);
+    if (warp < M) {
+        route(kp, sh, w.logits, l);
+    } else {
+#pragma unroll 1
+        for (int i = warp - M; i < nrows; i += NCW - M) {
+            if (i < nr) {
+                // the M logits of router row e, then their copies out
+                const int e = b.ra + i;
+                float *lv = sh.lscr + warp * kMaxRows;
+                one_row(sh, g.H, g.qb, sh.pb + b.off_router + (size_t)i * g.rr_bytes, all, lv, 1, 0u);
+                __syncwarp();
+                const int lane = threadIdx.x & 31;
+                // (debug switch: one logit of layer 0 stays unpublished)
+                if (!(l == 0 && kp.skip_row == e))
+#pragma unroll 1
+                    for (int t = lane; t < kLogitCopies * M; t += 32) {
+                        const int c = t / M, m = t - c * M;
+                        st_tag(w.logits + ((size_t)c * kp.ws_l.maxr + m) * g.Er + e, __float_as_uint(lv[m]), layer_tag(kp, l));
+                    }
+                __syncwarp();
+            } else {
+                const int j = i - nr;   // gate row of unit j / 2, or its up row
+                one_row(sh, g.H, g.sb, sh.pb + b.off_units + (size_t)j * g.sg_bytes, all, sh.p1v + j * maxr, 1, 0u);
+            }
         }
     }
     wstamp(kp, l, 15);
-    // rows past the buffer (large shared experts) come through the ring
-    sched_p1x(kp, Lp, [&](const uint8_t *, int, int, int first, int n) {
-        consume(sh, q, 10, [&](const uint8_t *st) {
-            for (int i = 0; i < n; ++i)
-                one_row(sh, g.H, g.sb, st + (size_t)i * g.sg_bytes, all, sh.p1v + (first + i) * maxr, 1, 0u);
+    if (kp.mode != kModeLayers) return;
+    int t0 = M * 32, nt = NCT - M * 32;
+    if (ring_rows) {
+        sched_p1x(kp, sh, Lp, [&](const uint8_t *, int, int, int first, int n) {
+            consume(sh, q, 10, [&](const uint8_t *st) {
+#pragma unroll 1
+                for (int i = 0; i < n; ++i)
+                    one_row(sh, g.H, g.sb, st + (size_t)i * g.sg_bytes, all, sh.p1v + (first + i) * maxr, 1, 0u);
+            });
         });
-    });
-    cbar();
-    // SwiGLU of the CTA's units
-    for (int t = threadIdx.x; t < (b.ub - b.ua) * kp.M; t += NCT) {
-        const int u = t / kp.M, m = t % kp.M;
-        const float gt = sh.p1v[(2 * u) * maxr + m], up = sh.p1v[(2 * u + 1) * maxr + m];
-        st_tag(w.act_s + (size_t)m * g.Is + b.ua + u, __float_as_uint(gt / (1.0f + expf(-gt)) * up), layer_tag(kp, l));
+        cbar();
+        t0 = 0;
+        nt = NCT;
+    } else {
+        if (warp < M) return;
+        asm volatile("bar.sync 3, %0;" ::"r"(nt) : "memory");
     }
+    // SwiGLU of the CTA's shared units
+    const unsigned tag = layer_tag(kp, l);
+#pragma unroll 1
+    for (int m = 0; m < M; ++m)
+#pragma unroll 1
+        for (int u = (int)threadIdx.x - t0; u >= 0 && u < b.ub - b.ua; u += nt) {
+            const float gt = sh.p1v[(2 * u) * maxr + m], up = sh.p1v[(2 * u + 1) * maxr + m];
+            st_tag(w.act_s + (size_t)m * g.Is + b.ua + u, __float_as_uint(gt / (1.0f + expf(-gt)) * up), tag);
+        }
 }
 
 // Shared down rows held in the prefetch buffer, by compute warps w0 .. NCW-1
@@ -1565,56 +1903,61 @@ __device__ void shared_down_pb(const KParams &kp, const Sh &sh, int w0)
 {
     const Geo &g = kp.g;
     const uint32_t all = (1u << kp.M) - 1u;
-    const PbPlan b = pb_plan(kp);
+    const CtaPlan &b = *sh.cp;
     const int warp = threadIdx.x >> 5;
+#pragma unroll 1
     for (int r0 = (warp - w0) * 8; r0 < b.dpb; r0 += (NCW - w0) * 8)
         dn_rows(sh, g.sb, sh.pb + b.off_sdown + (size_t)r0 * g.sd_bytes, min(8, b.dpb - r0), g.sd_bytes, g.Is, all, 0,
                 sh.ysh + r0 * kMaxRows, kMaxRows, 1);
 }
 
-__device__ void phase1b(const KParams &kp, const Sh &sh, const LayerPtrs &Lp, unsigned &q, int l)
+__device__ void phase1b(const KParams &kp, const Sh &sh, const LayerPtrs &Lp, Cursor &q, int l)
 {
     const Geo &g = kp.g;
     const uint32_t all = (1u << kp.M) - 1u;
-    int tc = 0;
-    sched_p1b(kp, Lp, [&](const uint8_t *, int, int, int first, int n) {
+    StageTrace tr{kp.trace ? &kp : nullptr, l, 0, 11, 1};
+    sched_p1b(kp, sh, Lp, [&](const uint8_t *, int, int, int first, int n) {
         consume(sh, q, 15, [&](const uint8_t *st) {
             dn_rows(sh, g.sb, st, n, g.sd_bytes, g.Is, all, 0, sh.ysh + first * kMaxRows, kMaxRows, 1);
-        }, kp.trace ? &kp : nullptr, l, &tc, 11, 1);
+        }, &tr);
     });
 }
 
-__device__ void phase2(const KParams &kp, const Sh &sh, const LayerPtrs &Lp, unsigned &q, const Ws &w, int l)
+__device__ void phase2(const KParams &kp, const Sh &sh, const LayerPtrs &Lp, Cursor &q, const Ws &w, int l)
 {
     const Geo &g = kp.g;
     const int maxr = kp.ws_l.maxr;
     const unsigned tag = layer_tag(kp, l);
-    int tc = 0;
+    StageTrace tr{kp.trace ? &kp : nullptr, l, 0, 2, 1};
     sched_p2(kp, sh, Lp, [&](const uint8_t *, int, int s, int first, int n) {
         consume(sh, q, 20, [&](const uint8_t *st) {
             uint64_t *act = w.act + (size_t)s * maxr * g.I;
             gu_units(sh, g.H, g.rb, st, n, g.g_bytes, sh.slot_mask[s], act + first, g.I, tag);
-        }, kp.trace ? &kp : nullptr, l, &tc, 2, 1);
+        }, &tr);
     });
 }
 
 // P3 in rounds of consecutive slots whose activation pairs fit the staging
 // buffer; the producer issued the down stages slot by slot, so the stages of
 // a round are consumed in issue order.
-__device__ bool phase3(const KParams &kp, const Sh &sh, const LayerPtrs &Lp, unsigned &q, const Ws &w, int l)
+__device__ bool phase3(const KParams &kp, const Sh &sh, const LayerPtrs &Lp, Cursor &q, const Ws &w, int l)
 {
     const Geo &g = kp.g;
     const int maxr = kp.ws_l.maxr, U = sh.flags[1];
-    int tc = 0;
+    StageTrace tr{kp.trace ? &kp : nullptr, l, 0, 7, 1};
+#pragma unroll 1
     for (int s0 = 0; s0 < U;) {
         int s1 = s0, pairs = 0;
+#pragma unroll 1
         while (s1 < U && pairs + __popc(sh.slot_mask[s1]) <= sh.act_pairs) pairs += __popc(sh.slot_mask[s1++]);
         if (s1 == s0) s1 = s0 + 1;   // cannot happen: act_pairs >= maxr >= popc of any mask
         const int pbase = sh.slot_rowbase[s0], npairs = sh.slot_rowbase[s1] - pbase;
         // pair -> (slot, row) table of the round
         if (threadIdx.x < 32) {
+#pragma unroll 1
             for (int s = s0 + (int)threadIdx.x; s < s1; s += 32) {
                 uint32_t mask = sh.slot_mask[s];
+#pragma unroll 1
                 for (int p = sh.slot_rowbase[s] - pbase; mask; mask &= mask - 1, ++p)
                     sh.pair_src[p] = s * kMaxRows + (__ffs(mask) - 1);
             }
@@ -1632,7 +1975,7 @@ __device__ bool phase3(const KParams &kp, const Sh &sh, const LayerPtrs &Lp, uns
                 const int pr = sh.slot_rowbase[s];
                 dn_rows(sh, g.rb, st, n, g.d_bytes, g.I, sh.slot_mask[s], pr - pbase,
                         sh.ybuf + pr * sh.hrows + first, 1, sh.hrows);
-            }, kp.trace ? &kp : nullptr, l, &tc, 7, 1);
+            }, &tr);
         });
         cbar();
         s0 = s1;
@@ -1649,9 +1992,7 @@ __device__ void combine(const KParams &kp, const Sh &sh, const float (&xr)[2], u
 {
     const Geo &g = kp.g;
     const int M = kp.M, k = g.k, t = threadIdx.x;
-    int h0, h1;
-    hslice(g.H, h0, h1);
-    const int np = (h1 - h0) / 2;
+    const int h0 = sh.cp->h0, np = sh.cp->nh / 2;
     if (t < np * M) {
         const int pl = t / M, m = t % M;
         uint32_t o[2];
@@ -1659,6 +2000,7 @@ __device__ void combine(const KParams &kp, const Sh &sh, const float (&xr)[2], u
         for (int hh = 0; hh < 2; ++hh) {
             const int hl = 2 * pl + hh;
             float acc = 0.f;
+#pragma unroll 1
             for (int j = 0; j < k; ++j)
                 acc = fmaf(sh.row_w[m * kMaxK + j], sh.ybuf[sh.row_pair[m * kMaxK + j] * sh.hrows + hl], acc);
             if (g.has_shared) acc = fmaf(sh.sigma[m], sh.ysh[hl * kMaxRows + m], acc);
@@ -1675,9 +2017,11 @@ __device__ __noinline__ void write_normed(const KParams &kp, const Sh &sh, const
 {
     const Geo &g = kp.g;
     const int H = g.H, M = kp.M, tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+#pragma unroll 1
     for (int m = lane; m < M; m += 32) sh.red[m * (NCW + 1) + warp] = 0.f;
     __syncwarp();
     const int per_row = H / 8, total = M * per_row;
+#pragma unroll 1
     for (int base = 0; base < total; base += NCT) {
         const int it = base + tid;
         float ss = 0.f;
@@ -1698,13 +2042,13 @@ __device__ __noinline__ void write_normed(const KParams &kp, const Sh &sh, const
     cbar();
     if (tid < M) {
         float t = 0.f;
+#pragma unroll 1
         for (int w2 = 0; w2 < NCW; ++w2) t += sh.red[tid * (NCW + 1) + w2];
         sh.red[tid * (NCW + 1) + NCW] = rsqrtf(t / (float)H + g.eps);
     }
     cbar();
-    int h0, h1;
-    hslice(H, h0, h1);
-    const int nh = h1 - h0;
+    const int h0 = sh.cp->h0, nh = sh.cp->nh;
+#pragma unroll 1
     for (int t = tid; t < nh * M; t += NCT) {
         const int hl = t / M, m = t % M;
         const size_t idx = (size_t)m * H + h0 + hl;
@@ -1723,12 +2067,11 @@ __device__ __noinline__ void write_normed(const KParams &kp, const Sh &sh, const
 __device__ __forceinline__ void compute(const KParams &kp, const Sh &sh)
 {
     const Ws w = ws_views(kp);
-    unsigned q = 0;
+    Cursor q = cursor0();
     int nsync = 0;
-    int h0, h1;
-    hslice(kp.g.H, h0, h1);
-    const int np = (h1 - h0) / 2, M = kp.M, H = kp.g.H;
+    const int h0 = sh.cp->h0, np = sh.cp->nh / 2, M = kp.M, H = kp.g.H;
     const int warp = threadIdx.x >> 5;
+#pragma unroll 1
     for (int l = 0; l < kp.L; ++l) {
         const LayerPtrs &Lp = kp.layer[l];
         const bool last = l == kp.L - 1;
@@ -1745,12 +2088,10 @@ __device__ __forceinline__ void compute(const KParams &kp, const Sh &sh)
         phase1(kp, sh, Lp, q, w, l);
         if (t0) stamp(kp, l, 2);
         if (t0) stamp(kp, l, 3);
-        // the first M warps route (waiting on every CTA's logits); the others
-        // stage the shared expert's activations (waiting on every CTA's
-        // units) and run its down rows from the prefetch buffer meanwhile
-        if (warp < M) {
-            route(kp, sh, w.logits, l);
-        } else if (kp.mode == kModeLayers && kp.g.has_shared) {
+        // while the routed weights come in, the non-routing warps stage the
+        // shared expert's activations (waiting on every CTA's units) and run
+        // its down rows from the prefetch buffer
+        if (warp >= M && kp.mode == kModeLayers && kp.g.has_shared) {
             stage_acts(sh, M, kp.g.Is, M * 32, NCT - M * 32, layer_tag(kp, l),
                        [&](int p) -> const uint64_t * { return w.act_s + (size_t)p * kp.g.Is; });
             asm volatile("bar.sync 3, %0;" ::"r"(NCT - M * 32) : "memory");
@@ -1793,53 +2134,57 @@ __device__ __forceinline__ void compute(const KParams &kp, const Sh &sh)
         }
         if (t0) stamp(kp, l, 8);
     }
-    kernel_exit(sh, kp.p.max_slots);
+    kernel_exit(sh);
 }
 
 __global__ void __launch_bounds__(kThreads, 1) moe_decode_kernel(const __grid_constant__ KParams kp)
 {
     extern __shared__ __align__(128) uint8_t smem[];
     const SmemLayout L = carve(kp.g, kp.p);
-    Sh sh;
-    uint64_t *bars = reinterpret_cast<uint64_t *>(smem + L.bar);
-    sh.full = bars;
-    sh.empty = bars + kp.p.NS;
-    sh.route = bars + 2 * kp.p.NS;
-    sh.pb_full = bars + 2 * kp.p.NS + 1;
-    sh.pb_empty = bars + 2 * kp.p.NS + 2;
-    sh.flags = reinterpret_cast<int *>(smem + L.flags);
-    sh.slot_e = reinterpret_cast<int *>(smem + L.slot_e);
-    sh.slot_mask = reinterpret_cast<uint32_t *>(smem + L.slot_mask);
-    sh.slot_rowbase = reinterpret_cast<int *>(smem + L.slot_rowbase);
-    sh.sigma = reinterpret_cast<float *>(smem + L.sigma);
-    sh.eslot = reinterpret_cast<int *>(smem + L.eslot);
-    sh.emask = reinterpret_cast<uint32_t *>(smem + L.emask);
-    sh.topv = reinterpret_cast<float *>(smem + L.topv);
-    sh.tope = reinterpret_cast<int *>(smem + L.tope);
-    sh.topw = reinterpret_cast<float *>(smem + L.topw);
-    sh.row_w = reinterpret_cast<float *>(smem + L.row_w);
-    sh.row_pair = reinterpret_cast<int *>(smem + L.row_pair);
-    sh.red = reinterpret_cast<float *>(smem + L.red);
-    sh.p1v = reinterpret_cast<float *>(smem + L.p1v);
-    sh.pair_src = reinterpret_cast<int *>(smem + L.pair_src);
-    sh.pend = reinterpret_cast<int *>(smem + L.pend);
-    sh.xs = reinterpret_cast<float4 *>(smem + L.xs);
-    sh.xsum = reinterpret_cast<float *>(smem + L.xsum);
-    sh.act = reinterpret_cast<float4 *>(smem + L.act);
-    sh.asum = reinterpret_cast<float *>(smem + L.asum);
-    sh.ybuf = reinterpret_cast<float *>(smem + L.ybuf);
-    sh.ysh = reinterpret_cast<float *>(smem + L.ysh);
-    sh.target = reinterpret_cast<unsigned *>(smem + L.target);
-    sh.act_done = reinterpret_cast<unsigned *>(kp.ws + kFlagsOffset);
-    sh.pb = smem + L.pb;
-    sh.ring = smem + L.ring;
-    sh.NS = kp.p.NS;
-    sh.S = kp.p.S;
-    sh.hrows = kp.p.hrows;
-    sh.act_pairs = kp.p.act_pairs;
-    sh.timeout_ns = kp.timeout_ns;
-    sh.ctrl = reinterpret_cast<Ctrl *>(kp.ws);
+    // The CTA's Sh lives in shared memory: every function reaches it through
+    // a reference, with no copy in local memory.
+    Sh &sh = *reinterpret_cast<Sh *>(smem + L.shs);
     if (threadIdx.x == 0) {
+        CtaPlan *cplan = reinterpret_cast<CtaPlan *>(smem + L.cplan);
+        cta_plan(kp, *cplan);
+        sh.cp = cplan;
+        uint64_t *bars = reinterpret_cast<uint64_t *>(smem + L.bar);
+        sh.full = bars;
+        sh.empty = bars + kp.p.NS;
+        sh.route = bars + 2 * kp.p.NS;
+        sh.pb_full = bars + 2 * kp.p.NS + 1;
+        sh.pb_empty = bars + 2 * kp.p.NS + 2;
+        sh.flags = reinterpret_cast<int *>(smem + L.flags);
+        sh.slot_e = reinterpret_cast<int *>(smem + L.slot_e);
+        sh.slot_mask = reinterpret_cast<uint32_t *>(smem + L.slot_mask);
+        sh.slot_rowbase = reinterpret_cast<int *>(smem + L.slot_rowbase);
+        sh.sigma = reinterpret_cast<float *>(smem + L.sigma);
+        sh.eslot = reinterpret_cast<int *>(smem + L.eslot);
+        sh.emask = reinterpret_cast<uint32_t *>(smem + L.emask);
+        sh.topv = reinterpret_cast<float *>(smem + L.topv);
+        sh.tope = reinterpret_cast<int *>(smem + L.tope);
+        sh.topw = reinterpret_cast<float *>(smem + L.topw);
+        sh.row_w = reinterpret_cast<float *>(smem + L.row_w);
+        sh.row_pair = reinterpret_cast<int *>(smem + L.row_pair);
+        sh.red = reinterpret_cast<float *>(smem + L.red);
+        sh.lscr = reinterpret_cast<float *>(smem + L.lscr);
+        sh.p1v = reinterpret_cast<float *>(smem + L.p1v);
+        sh.pair_src = reinterpret_cast<int *>(smem + L.pair_src);
+        sh.xs = reinterpret_cast<float4 *>(smem + L.xs);
+        sh.xsum = reinterpret_cast<float *>(smem + L.xsum);
+        sh.act = reinterpret_cast<float4 *>(smem + L.act);
+        sh.asum = reinterpret_cast<float *>(smem + L.asum);
+        sh.ybuf = reinterpret_cast<float *>(smem + L.ybuf);
+        sh.ysh = reinterpret_cast<float *>(smem + L.ysh);
+        sh.pb = smem + L.pb;
+        sh.ring = smem + L.ring;
+        sh.NS = kp.p.NS;
+        sh.S = kp.p.S;
+        sh.hrows = kp.p.hrows;
+        sh.act_pairs = kp.p.act_pairs;
+        sh.timeout_ns = kp.timeout_ns;
+        sh.ctrl = reinterpret_cast<Ctrl *>(kp.ws);
+#pragma unroll 1
         for (int i = 0; i < kp.p.NS; ++i) {
             mbar_init(&sh.full[i], 1);
             mbar_init(&sh.empty[i], 1);
@@ -1849,15 +2194,12 @@ __global__ void __launch_bounds__(kThreads, 1) moe_decode_kernel(const __grid_co
         mbar_init(sh.pb_empty, NCW);
         sh.flags[0] = 0;
         sh.flags[1] = 0;
-        for (int i = 0; i < kp.p.max_slots; ++i) sh.target[i] = 0u;
-        for (int i = 0; i < NCW * kp.p.max_slots; ++i) sh.pend[i] = 0;
         asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
     }
     __syncthreads();
     if (threadIdx.x >= NCT) {
         const int lane = threadIdx.x - NCT;
-        if (lane < NP) ring_producer(kp, sh, lane);
-        else if (lane == NP) pb_producer(kp, sh);
+        producer(kp, sh, lane);
         return;
     }
     compute(kp, sh);
@@ -1911,8 +2253,9 @@ bool make_plan(const Geo &g, int maxr, int num_sms, Plan &p)
     // Every stage has one consumer warp: stage q goes to warp q % NCW, and a
     // warp waits on stage q only after it waited on stage q - NS of the same
     // slot (mbarrier parity tells apart only the current and previous phase),
-    // so NS is a multiple of NCW (and of NP, for the issuing lanes).
-    static_assert(NCW % NP == 0, "producer lanes must divide the ring depth");
+    // so NS is a multiple of NCW.  A batch of the producer takes NS <= 32
+    // stages, one per lane.
+    static_assert(2 * NCW <= 32, "ring depth above the producer warp's width");
     p.NS = 2 * NCW;
     p.S = 0;
     p.pb_bytes = 0;
@@ -1935,8 +2278,10 @@ bool make_plan(const Geo &g, int maxr, int num_sms, Plan &p)
     // stages of at least two gate/up units if the ring allows it
     const int want = 4 * g.g_bytes > maxi ? 4 * g.g_bytes : maxi;
     int ns_pick = 0;
+#pragma unroll 1
     for (int ns = 2 * NCW; ns >= NCW && !ns_pick; ns -= NCW)
         if (ring / ns >= want) ns_pick = ns;
+#pragma unroll 1
     for (int ns = ns_pick ? ns_pick : 2 * NCW; ns >= NCW; ns -= NCW) {
         int S = ring / ns;
         S -= S % 16;

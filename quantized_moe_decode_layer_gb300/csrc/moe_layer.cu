@@ -1737,13 +1737,13 @@ __device__ __forceinline__ void pb_issue(const KParams &kp, const Sh &sh, int l)
 }
 
 // The producer warp (all 32 lanes, in step).  Lane 0 fills the prefetch
-// buffer: layer 0's at once, layer l + 1's once layer l's routed gate/up
-// stages are on their way and every compute warp is done with layer l's
-// buffer.  Per layer the copies go out in the order the layer needs them:
-// shared rows past the buffer, then (after routing) the routed gate/up
-// stages, the next layer's buffer, an L2 prefetch of every routed down stage
-// (the ring holds only part of a layer), the shared down rows past the
-// buffer and the routed down stages.
+// buffer: layer 0's at once, layer l + 1's once layer l's stages are all
+// issued and every compute warp is done with layer l's buffer.  Per layer
+// the copies go out in the order the layer needs them: shared rows past the
+// buffer, then (after routing) the routed gate/up stages, an L2 prefetch of
+// every routed down stage (the ring holds only part of a layer), the shared
+// down rows past the buffer, the routed down stages and the next layer's
+// buffer.
 __device__ __forceinline__ void producer(const KParams &kp, const Sh &sh, int lane)
 {
     Cursor c = cursor0();
@@ -1759,11 +1759,6 @@ __device__ __forceinline__ void producer(const KParams &kp, const Sh &sh, int la
             if (lane == 0) stamp(kp, l, 10);
             if (!issue_pass(sh, c, lane, [&](auto &&f) { sched_p2(kp, sh, Lp, f); })) break;
             if (lane == 0) stamp(kp, l, 14);
-            if (l + 1 < kp.L) {
-                if (!wait_bar(sh, sh.pb_empty, (unsigned)l & 1u, 3)) break;
-                if (lane == 0 && !aborted(sh)) pb_issue(kp, sh, l + 1);
-                pb_issued = l + 2;
-            }
             int turn = 0;
             sched_p3(kp, sh, Lp, [&](const uint8_t *src, int bytes, int, int, int) {
                 if (turn == lane) prefetch_l2(src, (unsigned)bytes);
@@ -1772,6 +1767,11 @@ __device__ __forceinline__ void producer(const KParams &kp, const Sh &sh, int la
             if (!issue_pass(sh, c, lane, [&](auto &&f) { sched_p1b(kp, sh, Lp, f); })) break;
             if (!issue_pass(sh, c, lane, [&](auto &&f) { sched_p3(kp, sh, Lp, f); })) break;
             if (lane == 0) stamp(kp, l, 11);
+            if (l + 1 < kp.L) {
+                if (!wait_bar(sh, sh.pb_empty, (unsigned)l & 1u, 3)) break;
+                if (lane == 0 && !aborted(sh)) pb_issue(kp, sh, l + 1);
+                pb_issued = l + 2;
+            }
             if (aborted(sh)) break;
         }
     }
@@ -1897,17 +1897,17 @@ __device__ void phase1(const KParams &kp, const Sh &sh, const LayerPtrs &Lp, Cur
         }
 }
 
-// Shared down rows held in the prefetch buffer, by compute warps w0 .. NCW-1
-// in chunks of 8 rows.
+// Shared down rows held in the prefetch buffer, spread over compute warps
+// w0 .. NCW-1 in equal chunks.
 __device__ void shared_down_pb(const KParams &kp, const Sh &sh, int w0)
 {
     const Geo &g = kp.g;
     const uint32_t all = (1u << kp.M) - 1u;
     const CtaPlan &b = *sh.cp;
-    const int warp = threadIdx.x >> 5;
-#pragma unroll 1
-    for (int r0 = (warp - w0) * 8; r0 < b.dpb; r0 += (NCW - w0) * 8)
-        dn_rows(sh, g.sb, sh.pb + b.off_sdown + (size_t)r0 * g.sd_bytes, min(8, b.dpb - r0), g.sd_bytes, g.Is, all, 0,
+    const int warp = threadIdx.x >> 5, nw = NCW - w0, ch = (b.dpb + nw - 1) / nw;
+    const int r0 = (warp - w0) * ch;
+    if (warp >= w0 && ch > 0 && r0 < b.dpb)
+        dn_rows(sh, g.sb, sh.pb + b.off_sdown + (size_t)r0 * g.sd_bytes, min(ch, b.dpb - r0), g.sd_bytes, g.Is, all, 0,
                 sh.ysh + r0 * kMaxRows, kMaxRows, 1);
 }
 
@@ -2070,7 +2070,6 @@ __device__ __forceinline__ void compute(const KParams &kp, const Sh &sh)
     Cursor q = cursor0();
     int nsync = 0;
     const int h0 = sh.cp->h0, np = sh.cp->nh / 2, M = kp.M, H = kp.g.H;
-    const int warp = threadIdx.x >> 5;
 #pragma unroll 1
     for (int l = 0; l < kp.L; ++l) {
         const LayerPtrs &Lp = kp.layer[l];
@@ -2088,21 +2087,13 @@ __device__ __forceinline__ void compute(const KParams &kp, const Sh &sh)
         phase1(kp, sh, Lp, q, w, l);
         if (t0) stamp(kp, l, 2);
         if (t0) stamp(kp, l, 3);
-        // while the routed weights come in, the non-routing warps stage the
-        // shared expert's activations (waiting on every CTA's units) and run
-        // its down rows from the prefetch buffer
-        if (warp >= M && kp.mode == kModeLayers && kp.g.has_shared) {
-            stage_acts(sh, M, kp.g.Is, M * 32, NCT - M * 32, layer_tag(kp, l),
-                       [&](int p) -> const uint64_t * { return w.act_s + (size_t)p * kp.g.Is; });
-            asm volatile("bar.sync 3, %0;" ::"r"(NCT - M * 32) : "memory");
-            shared_down_pb(kp, sh, M);
-        }
         if (cbar_or(aborted(sh))) return;
-        // every warp is done with the prefetch buffer of layer l
-        if ((threadIdx.x & 31) == 0) mbar_arrive(sh.pb_empty, 1);
         if (t0) stamp(kp, l, 4);
-        if (kp.mode == kModeRouter) break;
-        // residuals of this thread's output pair, read while the weights stream
+        if (kp.mode == kModeRouter) {
+            if ((threadIdx.x & 31) == 0) mbar_arrive(sh.pb_empty, 1);
+            break;
+        }
+        // residuals of this thread's output pair
         float xr[2] = {0.f, 0.f};
         if ((int)threadIdx.x < np * M) {
             const int pl = threadIdx.x / M, m = threadIdx.x % M;
@@ -2117,9 +2108,19 @@ __device__ __forceinline__ void compute(const KParams &kp, const Sh &sh)
         phase2(kp, sh, Lp, q, w, l);
         wstamp(kp, l, 5);
         if (t0) stamp(kp, l, 5);
-        // shared down rows that came through the ring
-        phase1b(kp, sh, Lp, q, l);
-        // the staging buffer is reused: every warp is done with the shared rows
+        // The shared expert's down rows, off the routed path: its activations
+        // (waited for from every CTA) into the staging buffer, then the rows
+        // held in the prefetch buffer and any that came through the ring.
+        if (kp.g.has_shared) {
+            stage_acts(sh, M, kp.g.Is, 0, NCT, layer_tag(kp, l),
+                       [&](int p) -> const uint64_t * { return w.act_s + (size_t)p * kp.g.Is; });
+            cbar();
+            shared_down_pb(kp, sh, 0);
+            phase1b(kp, sh, Lp, q, l);
+        }
+        // every warp is done with the prefetch buffer of layer l, and with
+        // the staging buffer (reused by P3)
+        if ((threadIdx.x & 31) == 0) mbar_arrive(sh.pb_empty, 1);
         cbar();
         if (t0) stamp(kp, l, 6);
         wstamp(kp, l, 6);

@@ -13,7 +13,7 @@ namespace moe {
 
 constexpr int kGroup = 64;          // affine group along the contraction axis
 constexpr int kSub = 16;            // codes per sub-group (one lane step)
-constexpr int kConsumerWarps = 15;  // compute warps per CTA (16 warps: 128 registers per thread)
+constexpr int kConsumerWarps = 8;   // compute warps per CTA (9 warps in all: up to 224 registers per thread)
 constexpr int kThreads = (kConsumerWarps + 1) * 32;  // + one TMA producer warp
 constexpr int kMaxRows = 8;         // token rows per launch (larger M is chunked)
 constexpr int kMaxLayers = 64;      // layers per persistent launch

@@ -1,32 +1,37 @@
 // Persistent decode kernel of the quantized MoE FFN layer (and of a stack of
 // such layers) for sm_103a.
 //
-// One CTA per SM: 15 compute warps and one producer warp.  The producer
+// One CTA per SM: eight compute warps and one producer warp.  The producer
 // streams weights into shared memory with 1-D bulk copies
-// (cp.async.bulk ... mbarrier::complete_tx): five lanes feed a ring of
-// stages holding the routed experts (and the shared expert's down rows), each
-// stage consumed by one compute warp; a sixth lane fills a prefetch buffer
-// with the next layer's RMSNorm weight, router rows and shared-expert gate/up
-// units, which do not depend on routing and are therefore loaded while the
-// current layer still runs.  Per layer:
+// (cp.async.bulk ... mbarrier::complete_tx): a ring of stages holding the
+// routed experts (and shared-expert rows that do not fit elsewhere), each
+// stage consumed by one compute warp, issued one lane per stage so that the
+// copies of a layer go out together; and a prefetch buffer with the next
+// layer's RMSNorm weight, router rows and shared-expert rows, which do not
+// depend on routing and are therefore loaded while the current layer still
+// runs.  Per layer:
 //
 //   P0  every CTA: RMSNorm of the M input rows into shared memory
 //       (flash-moe, "Metal Compute Shaders": RMS normalisation)
-//   P1  router rows (plus the shared-expert gate row) and the shared
-//       expert's gate/up units of this CTA, from the prefetch buffer
-//                                                           -> grid barrier
-//   R   every CTA: softmax + top-k + renormalisation per row and the list of
-//       distinct selected experts with the rows that chose each
-//       (PureDrive model card, "Summary": the full top-8 of 256 is kept)
-//   P1b the shared expert's down rows of this CTA's output slice
+//   P1  this CTA's router rows (plus the shared-expert gate row), published
+//       first, then its shared-expert gate/up units and their SwiGLU; the
+//       first M warps meanwhile wait for every CTA's logits and route:
+//       softmax + top-k + renormalisation per row and the list of distinct
+//       selected experts with the rows that chose each (PureDrive model
+//       card, "Summary": the full top-8 of 256 is kept)
 //   P2  gate/up units of the selected experts, each expert streamed once for
 //       all the rows that chose it (model card, "How it works": the verify
-//       pass reads its weights once), SwiGLU; per-expert release counters
+//       pass reads its weights once), SwiGLU
+//   S   the shared expert's down rows of this CTA's output slice
 //   P3  down rows of every selected expert for this CTA's output slice
 //   C   weighted combine + sigmoid-gated shared expert + residual, bf16
-//       (flash-moe: "MoE combine + residual + gate")         -> grid barrier
+//       (flash-moe: "MoE combine + residual + gate")
 //   N   the fused next RMSNorm of the bf16 output (model card: fused
 //       add+RMSNorm), or the next layer's P0.
+//
+// CTAs exchange data (router logits, activations, layer outputs) as tagged
+// words in global memory that readers poll; there is no grid barrier
+// between phases or layers.
 //
 // Dequantisation (moe_unpack.cuh).  A lane takes one 64-code group of a
 // weight row.  A masked code read as a float is the subnormal
@@ -34,10 +39,8 @@
 // 2^100, so a paired FFMA2 of masked codes against them accumulates
 // q * x * 2^(p - 49) as exact fp32 products.  Codes are accumulated per bit
 // position ("class") and each class sum is scaled back once per group: one
-// LOP3 and half an FFMA2 per weight.  With several token rows the codes are
-// first turned into q * 2^-23 by one paired multiply and reused for every
-// row.  The affine terms are factored per group:
-// sum_j (q_j s + b) x_j = s * sum_j q_j x_j + b * sum_j x_j.
+// LOP3 and half an FFMA2 per weight and token row.  The affine terms are
+// factored per group: sum_j (q_j s + b) x_j = s * sum_j q_j x_j + b * sum_j x_j.
 //
 // Determinism: no float atomics; every sum has a fixed order that depends
 // only on the row itself, so row m of an M-row call equals a 1-row call.
@@ -317,7 +320,7 @@ __device__ __forceinline__ void stamp(const KParams &kp, int l, int ev)
 }
 
 // Per-warp timeline (lane 0 of each compute warp) of CTAs 0 and gridDim/2,
-// stored after the per-CTA stamps: [2][kMaxLayers][16 warps][16 events].
+// stored after the per-CTA stamps: [2][kMaxLayers][16 warp slots][16 events].
 __device__ __forceinline__ void wstamp(const KParams &kp, int l, int ev)
 {
     if (!kp.trace || l >= kMaxLayers || (threadIdx.x & 31) != 0) return;
@@ -1826,13 +1829,15 @@ __device__ __forceinline__ void consume(const Sh &sh, Cursor &c, int where, F &&
     if ((threadIdx.x & 31) == 0) mbar_arrive(&sh.empty[slot], 1);
 }
 
-// P1 and routing.  The first M compute warps route (one token row each),
-// waiting on every CTA's router logits; the other warps compute this CTA's
-// router rows first and its shared gate/up rows from the prefetch buffer
-// after them (so that the logits every CTA waits for go out first), then the
-// SwiGLU of the CTA's shared units.  Shared rows past the buffer come through
-// the ring; their stages go to every compute warp in turn, so when there are
-// any the SwiGLU waits for the routing warps as well.
+// P1 and routing.  With M at most half the compute warps, the first M warps
+// route (one token row each), waiting on every CTA's router logits, while
+// the other warps compute this CTA's router rows first and its shared
+// gate/up rows from the prefetch buffer after them (so that the logits every
+// CTA waits for go out first), then the SwiGLU of the CTA's shared units.
+// With more rows, every warp computes rows first and the first M route
+// after.  Shared rows past the buffer come through the ring; their stages go
+// to every compute warp in turn, so when there are any the SwiGLU waits for
+// the routing warps as well.
 __device__ void phase1(const KParams &kp, const Sh &sh, const LayerPtrs &Lp, Cursor &q, const Ws &w, int l)
 {
     const Geo &g = kp.g;
@@ -1841,12 +1846,14 @@ __device__ void phase1(const KParams &kp, const Sh &sh, const LayerPtrs &Lp, Cur
     const CtaPlan &b = *sh.cp;
     const int nr = b.rb - b.ra, nrows = nr + 2 * b.upb;
     const bool ring_rows = b.ub - b.ua > b.upb;
+    const bool early = 2 * M <= NCW;
+    const int w0 = early ? M : 0;   // first warp computing rows
     wstamp(kp, l, 14);
-    if (warp < M) {
+    if (early && warp < M) {
         route(kp, sh, w.logits, l);
     } else {
 #pragma unroll 1
-        for (int i = warp - M; i < nrows; i += NCW - M) {
+        for (int i = warp - w0; i < nrows; i += NCW - w0) {
             if (i < nr) {
                 // the M logits of router row e, then their copies out
                 const int e = b.ra + i;
@@ -1859,7 +1866,8 @@ __device__ void phase1(const KParams &kp, const Sh &sh, const LayerPtrs &Lp, Cur
 #pragma unroll 1
                     for (int t = lane; t < kLogitCopies * M; t += 32) {
                         const int c = t / M, m = t - c * M;
-                        st_tag(w.logits + ((size_t)c * kp.ws_l.maxr + m) * g.Er + e, __float_as_uint(lv[m]), layer_tag(kp, l));
+                        st_tag(w.logits + ((size_t)c * kp.ws_l.maxr + m) * g.Er + e, __float_as_uint(lv[m]),
+                               layer_tag(kp, l));
                     }
                 __syncwarp();
             } else {
@@ -1869,17 +1877,23 @@ __device__ void phase1(const KParams &kp, const Sh &sh, const LayerPtrs &Lp, Cur
         }
     }
     wstamp(kp, l, 15);
-    if (kp.mode != kModeLayers) return;
-    int t0 = M * 32, nt = NCT - M * 32;
-    if (ring_rows) {
-        sched_p1x(kp, sh, Lp, [&](const uint8_t *, int, int, int first, int n) {
-            consume(sh, q, 10, [&](const uint8_t *st) {
-#pragma unroll 1
-                for (int i = 0; i < n; ++i)
-                    one_row(sh, g.H, g.sb, st + (size_t)i * g.sg_bytes, all, sh.p1v + (first + i) * maxr, 1, 0u);
-            });
-        });
+    if (!early) {
         cbar();
+        if (warp < M) route(kp, sh, w.logits, l);
+    }
+    if (kp.mode != kModeLayers) return;
+    int t0 = w0 * 32, nt = NCT - w0 * 32;
+    if (ring_rows || !early) {
+        if (ring_rows) {
+            sched_p1x(kp, sh, Lp, [&](const uint8_t *, int, int, int first, int n) {
+                consume(sh, q, 10, [&](const uint8_t *st) {
+#pragma unroll 1
+                    for (int i = 0; i < n; ++i)
+                        one_row(sh, g.H, g.sb, st + (size_t)i * g.sg_bytes, all, sh.p1v + (first + i) * maxr, 1, 0u);
+                });
+            });
+            cbar();
+        }
         t0 = 0;
         nt = NCT;
     } else {

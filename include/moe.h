@@ -242,8 +242,10 @@ const char *moe_status_str(int status);
 /* The last CUDA error code seen by the library on this host thread (0 = none). */
 int moe_last_cuda_error(void);
 
-/* Host-side check of the code-extraction tables the kernels use (no GPU
- * needed): returns the number of mismatching codes, 0 when consistent. */
+/* Host-side checks (no GPU needed): the code-extraction tables the kernels
+ * use, and the launch plans of the test shapes against the invariants the
+ * kernel relies on (ring depth, stage and buffer sizes, shared-memory limit).
+ * Returns the number of violations, 0 when consistent. */
 int moe_selftest_host(void);
 
 /* Number of kernel launches the library enqueued on this host thread since

@@ -134,6 +134,53 @@ int plan_for(KParams &kp, int mc)
 
 bool aligned16(const void *p) { return (reinterpret_cast<uintptr_t>(p) & 15) == 0; }
 
+// Launch plans of the three test shapes (and of the 35B geometry at every
+// routed width) for every row count of a launch and several SM counts,
+// checked against what the kernel relies on: the ring depth a multiple of
+// the compute warps and within one producer batch, stages that hold any
+// single bulk copy, the shared-memory limit, a staging buffer that holds
+// every row of a slot, a prefetch buffer that holds gamma and the router
+// rows, whole output row pairs per CTA, and 32-bit products in the work
+// split.  Returns the number of violations.
+int plan_selftest_host()
+{
+    const moe_layer_desc shapes[] = {
+        {256, 128, 16, 2, 4, 8, 0, 0, 0, 1e-6f},
+        {2048, 512, 256, 8, 6, 8, 8, 1, 512, 1e-6f},
+        {2048, 512, 256, 8, 4, 8, 8, 1, 512, 1e-6f},
+        {2048, 512, 256, 8, 8, 8, 8, 1, 512, 1e-6f},
+        {4096, 1024, 512, 10, 4, 8, 8, 1, 1024, 1e-6f},
+    };
+    const int sm_counts[] = {132, 148, 152, 160, 170};
+    int bad = 0;
+    for (const moe_layer_desc &d : shapes) {
+        Geo g;
+        if (!make_geo(d, g)) { ++bad; continue; }
+        const int R = rows_per_launch(g.H);
+        int maxi = 2 * g.g_bytes;
+        if (g.d_bytes > maxi) maxi = g.d_bytes;
+        if (g.sg_bytes > maxi) maxi = g.sg_bytes;
+        if (g.sd_bytes > maxi) maxi = g.sd_bytes;
+        for (int sms : sm_counts)
+            for (int mc = 1; mc <= R; ++mc) {
+                Plan p;
+                if (!make_plan(g, mc, sms, p)) { ++bad; continue; }
+                if (p.NS % kConsumerWarps != 0 || p.NS > 32 || p.NS > kMaxStages) ++bad;
+                if (p.S % 16 != 0 || p.S < maxi) ++bad;
+                if (p.smem_bytes > kSmemMax) ++bad;
+                if (p.act_pairs < p.maxr) ++bad;
+                const int rows_cta = (g.Er + sms - 1) / sms;
+                if (p.pb_bytes < (int)align_up((size_t)g.H * 2, 16) + rows_cta * g.rr_bytes) ++bad;
+                if (p.hrows % 2 != 0 || (long long)p.hrows * sms < g.H) ++bad;
+                const long long lim = 1ll << 32;
+                const long long ns[] = {g.Er, g.Is, (long long)p.max_slots * g.I, g.H / 2};
+                for (long long n : ns)
+                    if (n * sms >= lim) ++bad;
+            }
+    }
+    return bad;
+}
+
 }  // namespace
 }  // namespace moe
 
@@ -427,6 +474,6 @@ long long moe_launch_count(int reset)
     return n;
 }
 
-int moe_selftest_host(void) { return unpack_selftest_host(); }
+int moe_selftest_host(void) { return unpack_selftest_host() + plan_selftest_host(); }
 
 }  // extern "C"

@@ -28,7 +28,9 @@ def test_exports_every_declared_symbol():
     assert set(names) == set(_lib.SYMBOLS)
 
 
-def test_unpack_tables_selftest():
+def test_host_selftest():
+    """The code-extraction tables and the launch plans of the test shapes
+    (every row count, several SM counts) meet the kernel's invariants."""
     assert moe.lib().moe_selftest_host() == 0
 
 

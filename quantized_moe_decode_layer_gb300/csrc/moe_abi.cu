@@ -100,6 +100,7 @@ void make_ws_layout(const Geo &g, int max_M, WsLayout &w)
     w.off_act = put((size_t)w.max_slots * R * g.I * 8);
     w.off_act_s = put((size_t)R * (g.Is ? g.Is : 1) * 8);
     w.off_ping = put((size_t)2 * R * (g.H / 2) * 8);
+    w.off_y = put((size_t)R * g.k * g.H * 8);
     w.off_stage_in = put((size_t)max_M * g.H * 2);
     w.off_stage_out = put((size_t)max_M * g.H * 2);
     w.total = align_up(o, 256);

@@ -70,7 +70,7 @@ struct LayerPtrs {
 struct WsLayout {
     int maxr;                // rows per launch
     int max_slots;           // distinct routed experts per launch
-    size_t off_logits, off_act, off_act_s, off_ping, off_stage_in, off_stage_out, total;
+    size_t off_logits, off_act, off_act_s, off_ping, off_y, off_stage_in, off_stage_out, total;
     int max_M;               // rows the host-staging area holds
 };
 

@@ -88,7 +88,7 @@ constexpr int kShBytes = 512;
 
 struct SmemLayout {
     int shs, cplan, bar, flags, slot_e, slot_mask, slot_rowbase, sigma, eslot, emask, topv, tope, topw;
-    int row_w, row_pair, red, lscr, p1v, pair_src, xs, xsum, act, asum, ybuf, ysh, pb, ring, total;
+    int row_w, row_pair, red, lscr, p1v, pair_src, xs, xsum, act, asum, ysh, pb, ring, total;
 };
 
 __host__ __device__ inline int take(int &o, int bytes, int align)
@@ -132,7 +132,6 @@ __host__ __device__ inline SmemLayout carve(const Geo &g, const Plan &p)
     L.xsum = take(o, p.maxr * (g.H / kGroup) * 4, 16);
     L.act = take(o, p.act_pairs * Im * 4, 16);
     L.asum = take(o, p.act_pairs * (Im / kGroup) * 4, 16);
-    L.ybuf = take(o, p.maxr * g.k * p.hrows * 4, 16);
     L.ysh = take(o, p.hrows * kMaxRows * 4, 16);
     L.pb = take(o, p.pb_bytes, 128);
     L.ring = take(o, p.NS * p.S, 128);
@@ -355,7 +354,6 @@ struct Sh {
     float *xsum;         // [maxr][H / 64] group sums of hn
     float4 *act;         // [act_pairs][K / 4] arranged activations * 2^100
     float *asum;         // [act_pairs][K / 64]
-    float *ybuf;         // [pair][hrows] routed expert outputs of this CTA's slice
     float *ysh;          // [hrows][kMaxRows] shared expert outputs
     uint8_t *pb;
     uint8_t *ring;
@@ -469,6 +467,40 @@ __device__ __forceinline__ void poll_tag8(const Sh &sh, const uint64_t *pa, cons
             for (int j = 0; j < 8; ++j) v[j] = 0;
             break;
         }
+    }
+#pragma unroll
+    for (int j = 0; j < 4; ++j) { a[j] = (uint32_t)v[j]; b[j] = (uint32_t)v[4 + j]; }
+}
+
+// Four pairs of consecutive tagged words (each pointer 16-byte aligned; null
+// for none): payloads of (p0, p1) into a, of (p2, p3) into b.  All loaded
+// together; while some are missing, the first missing one is polled alone,
+// then all are loaded again.  Bounded (poll_more).
+__device__ __forceinline__ void poll_pairs4(const Sh &sh, const uint64_t *p0, const uint64_t *p1, const uint64_t *p2,
+                                            const uint64_t *p3, unsigned tag, int where, uint32_t (&a)[4],
+                                            uint32_t (&b)[4])
+{
+    const uint64_t none = (uint64_t)tag << 32;
+    const uint64_t *const p[4] = {p0, p1, p2, p3};
+    uint64_t v[8];
+    unsigned long long t0 = 0;
+    unsigned it = 0;
+#pragma unroll 1
+    for (;;) {
+#pragma unroll
+        for (int j = 0; j < 4; ++j) {
+            v[2 * j] = v[2 * j + 1] = none;
+            if (p[j]) ld_tag2(p[j], v[2 * j], v[2 * j + 1]);
+        }
+        const uint64_t *pm = nullptr;
+#pragma unroll
+        for (int j = 7; j >= 0; --j)
+            if ((unsigned)(v[j] >> 32) != tag) pm = p[j >> 1] + (j & 1);
+        if (!pm) break;
+        bool more = true;
+#pragma unroll 1
+        while ((more = poll_more(sh, ++it, t0, where)) && (unsigned)(ld_tag(pm) >> 32) != tag) {}
+        if (!more) break;
     }
 #pragma unroll
     for (int j = 0; j < 4; ++j) { a[j] = (uint32_t)v[j]; b[j] = (uint32_t)v[4 + j]; }
@@ -914,11 +946,18 @@ __device__ __forceinline__ void one_k_body(const float4 *xs, const float *xsum, 
     });
 }
 
+// Stores v at element i of dst: a plain fp32 array, or (tag != 0) tagged words.
+__device__ __forceinline__ void put_out(void *dst, size_t i, float v, unsigned tag)
+{
+    if (tag) st_tag(static_cast<uint64_t *>(dst) + i, __float_as_uint(v), tag);
+    else static_cast<float *>(dst)[i] = v;
+}
+
 // Down rows [0, cnt) (K inputs each) against the staged activation pairs
-// pair0 + t, t = g0 .. (t < popc(mask)): dst[h * hs + t * ts].
+// pair0 + t, t = g0 .. (t < popc(mask)): dst[h * hs + t * ts] (see put_out).
 template <int B, int R>
 __device__ __forceinline__ void dn_k_body(const float4 *act, const float *asum, int K, const uint8_t *rows0, int cnt,
-                                  int rowb, uint32_t mask, int pair0, int g0, float *dst, int hs, int ts)
+                                  int rowb, uint32_t mask, int pair0, int g0, void *dst, int hs, int ts, unsigned tag)
 {
     const int Gi = K / kGroup, n = __popc(mask);
     int tp[R];
@@ -944,7 +983,7 @@ __device__ __forceinline__ void dn_k_body(const float4 *act, const float *asum, 
             if (rb + k2 < cnt) {
 #pragma unroll
                 for (int r = 0; r < R; ++r)
-                    if (r < nv) dst[(size_t)(rb + k2) * hs + (size_t)tp[r] * ts] = acc[k2][r];
+                    if (r < nv) put_out(dst, (size_t)(rb + k2) * hs + (size_t)tp[r] * ts, acc[k2][r], tag);
             }
     });
 }
@@ -964,9 +1003,9 @@ __device__ __noinline__ void one_k(const float4 *xs, const float *xsum, int H, c
 }
 template <int B, int R>
 __device__ __noinline__ void dn_k(const float4 *act, const float *asum, int K, const uint8_t *rows0, int cnt,
-                                  int rowb, uint32_t mask, int pair0, int g0, float *dst, int hs, int ts)
+                                  int rowb, uint32_t mask, int pair0, int g0, void *dst, int hs, int ts, unsigned tag)
 {
-    dn_k_body<B, R>(act, asum, K, rows0, cnt, rowb, mask, pair0, g0, dst, hs, ts);
+    dn_k_body<B, R>(act, asum, K, rows0, cnt, rowb, mask, pair0, g0, dst, hs, ts, tag);
 }
 
 // ---------------------------------------------- one token vector in registers
@@ -1107,11 +1146,12 @@ __device__ __noinline__ void gu1(uint32_t units, int cnt, int rowb, int H, uint3
     }
 }
 
-// Rows [0, cnt) against one vector: dst[r * ds] = row r . x (plain fp32).
+// Rows [0, cnt) against one vector: dst[r * ds] = row r . x (see put_out).
 template <int BITS>
-__device__ __noinline__ void plain1(uint32_t rows, int cnt, int rowb, int K, uint32_t xq, uint32_t xsq, float *dst, int ds)
+__device__ __noinline__ void plain1(uint32_t rows, int cnt, int rowb, int K, uint32_t xq, uint32_t xsq, void *dst, int ds,
+                                    unsigned tag)
 {
-    rows1<BITS>(rows, rowb, cnt, K, xq, xsq, [&](int r, float v) { dst[(size_t)r * ds] = v; });
+    rows1<BITS>(rows, rowb, cnt, K, xq, xsq, [&](int r, float v) { put_out(dst, (size_t)r * ds, v, tag); });
 }
 
 // Dispatch on (bits, row-group size): code = bits * 8 + nr.
@@ -1150,9 +1190,9 @@ __device__ __noinline__ void one_row(const Sh &sh, int H, int bits, const uint8_
         const int m = __ffs(mask) - 1;
         const uint32_t xq = smem_u32(sh.xs) + (uint32_t)(m * H * 4), xsq = smem_u32(sh.xsum) + (uint32_t)(m * (H / kGroup) * 4);
         float *d = static_cast<float *>(dst) + (size_t)m * ms;
-        if (bits == 6) plain1<6>(smem_u32(row), 1, 0, H, xq, xsq, d, 0);
-        else if (bits == 8) plain1<8>(smem_u32(row), 1, 0, H, xq, xsq, d, 0);
-        else plain1<4>(smem_u32(row), 1, 0, H, xq, xsq, d, 0);
+        if (bits == 6) plain1<6>(smem_u32(row), 1, 0, H, xq, xsq, d, 0, 0u);
+        else if (bits == 8) plain1<8>(smem_u32(row), 1, 0, H, xq, xsq, d, 0, 0u);
+        else plain1<4>(smem_u32(row), 1, 0, H, xq, xsq, d, 0, 0u);
         return;
     }
     for_row_groups(mask, [&](int g0, int nr) {
@@ -1165,19 +1205,21 @@ __device__ __noinline__ void one_row(const Sh &sh, int H, int bits, const uint8_
     });
 }
 
+// dst[h * hs + t * ts] for down row h and the staged pair pair0 + t (t the
+// rank of a row in `mask`): plain fp32, or tagged words when tag != 0.
 __device__ __noinline__ void dn_rows(const Sh &sh, int bits, const uint8_t *rows0, int cnt, int rowb, int K,
-                                        uint32_t mask, int pair0, float *dst, int hs, int ts)
+                                        uint32_t mask, int pair0, void *dst, int hs, int ts, unsigned tag)
 {
     if (__popc(mask) == 1 && K <= 32 * kGroup && bits != 0) {
         const uint32_t xq = smem_u32(sh.act) + (uint32_t)(pair0 * K * 4), xsq = smem_u32(sh.asum) + (uint32_t)(pair0 * (K / kGroup) * 4);
-        if (bits == 6) plain1<6>(smem_u32(rows0), cnt, rowb, K, xq, xsq, dst, hs);
-        else if (bits == 8) plain1<8>(smem_u32(rows0), cnt, rowb, K, xq, xsq, dst, hs);
-        else plain1<4>(smem_u32(rows0), cnt, rowb, K, xq, xsq, dst, hs);
+        if (bits == 6) plain1<6>(smem_u32(rows0), cnt, rowb, K, xq, xsq, dst, hs, tag);
+        else if (bits == 8) plain1<8>(smem_u32(rows0), cnt, rowb, K, xq, xsq, dst, hs, tag);
+        else plain1<4>(smem_u32(rows0), cnt, rowb, K, xq, xsq, dst, hs, tag);
         return;
     }
     for_row_groups(mask, [&](int g0, int nr) {
         switch (bits * 8 + nr) {
-            MOE_RK_CASES(dn_k, (sh.act, sh.asum, K, rows0, cnt, rowb, mask, pair0, g0, dst, hs, ts))
+            MOE_RK_CASES(dn_k, (sh.act, sh.asum, K, rows0, cnt, rowb, mask, pair0, g0, dst, hs, ts, tag))
         default: break;
         }
     });
@@ -1287,12 +1329,12 @@ __device__ void build_hn(const KParams &kp, const Sh &sh, const void *x, unsigne
 // Activations (fp32 rows in global memory) of `n` staged pairs: pair p =
 // src(p)[0 .. K), arranged, * 2^100, with group sums.  A thread item is 4
 // consecutive inputs; 16 items make a group.
-// Threads [t0, t0 + nt) of the compute warps take part (whole warps).  The
+// nt threads of whole compute warps take part, the calling one as number tid.  The
 // sources are tagged fp32 words; each is waited for until it carries `tag`.
 template <typename F>
-__device__ __forceinline__ void stage_acts(const Sh &sh, int n, int K, int t0, int nt, unsigned tag, F &&src)
+__device__ __forceinline__ void stage_acts(const Sh &sh, int n, int K, int tid, int nt, unsigned tag, F &&src)
 {
-    const int per = K / 4, lgp = ilog2(per), G = K / kGroup, total = n * per, tid = threadIdx.x - t0;
+    const int per = K / 4, lgp = ilog2(per), G = K / kGroup, total = n * per;
     auto item = [&](int it, const uint32_t (&u)[4]) {
         float gs = 0.f;
         if (it < total) {
@@ -1533,6 +1575,7 @@ struct Ws {
     uint64_t *act;      // [max_slots][maxr][I] fp32
     uint64_t *act_s;    // [maxr][Is] fp32
     uint64_t *ping[2];  // [maxr][H / 2] bf16 pairs: outputs of the layers before the last
+    uint64_t *y;        // [maxr * k][H] fp32 routed expert outputs, by pair
 };
 
 __device__ __forceinline__ Ws ws_views(const KParams &kp)
@@ -1543,6 +1586,7 @@ __device__ __forceinline__ Ws ws_views(const KParams &kp)
     w.act_s = reinterpret_cast<uint64_t *>(kp.ws + kp.ws_l.off_act_s);
     w.ping[0] = reinterpret_cast<uint64_t *>(kp.ws + kp.ws_l.off_ping);
     w.ping[1] = w.ping[0] + (size_t)kp.ws_l.maxr * (kp.g.H / 2);
+    w.y = reinterpret_cast<uint64_t *>(kp.ws + kp.ws_l.off_y);
     return w;
 }
 
@@ -1626,22 +1670,50 @@ __device__ __forceinline__ void sched_p2(const KParams &kp, const Sh &sh, const 
     }
 }
 
+// P3 of this CTA: the slots whose gate/up units it computed in P2 (one or
+// two: a CTA's unit range is shorter than an expert since U < P), and for
+// each the share of the slot's H down rows in proportion to the share of
+// the slot's units it computed (unit range [u0, u1) of I: rows
+// [H u0 / I, H u1 / I)), so that the activations a CTA waits for come from
+// the few CTAs that share its expert, not from every CTA, and the down work
+// follows the gate/up work.
+struct P3Part {
+    int s;        // slot
+    int r0, r1;   // down rows [r0, r1)
+};
+
+__device__ __forceinline__ int p3_parts(const KParams &kp, const Sh &sh, P3Part (&pt)[2])
+{
+    const int U = sh.flags[1], I = kp.g.I, H = kp.g.H, P = gridDim.x, c = blockIdx.x;
+    const int n = U * I;   // n P < 2^32 (the host plan checks it)
+    int a, b;
+    split(n, P, c, a, b);
+    int cnt = 0;
+#pragma unroll 1
+    for (int s = a / I; b > a && s <= (b - 1) / I && cnt < 2; ++s) {
+        const int u0 = max(a, s * I) - s * I, u1 = min(b, (s + 1) * I) - s * I;
+        const int r0 = (int)((unsigned)H * (unsigned)u0 / (unsigned)I), r1 = (int)((unsigned)H * (unsigned)u1 / (unsigned)I);
+        if (r1 > r0) pt[cnt++] = P3Part{s, r0, r1};
+    }
+    return cnt;
+}
+
 template <typename F>
 __device__ __forceinline__ void sched_p3(const KParams &kp, const Sh &sh, const LayerPtrs &Lp, F &&f)
 {
     const Geo &g = kp.g;
-    const int U = sh.flags[1];
-    const int h0 = sh.cp->h0, nh = sh.cp->nh;
+    P3Part pt[2];
+    const int np = p3_parts(kp, sh, pt);
     // about one stage per compute warp over the layer
-    const int per_slot = max(1, (NCW + U - 1) / max(1, U));
-    const int cd = max(1, min(sh.S / g.d_bytes, (nh + per_slot - 1) / per_slot));
+    const int per_part = max(1, (NCW + np - 1) / max(1, np));
 #pragma unroll 1
-    for (int s = 0; s < U; ++s) {
-        const int e = sh.slot_e[s];
+    for (int i = 0; i < np; ++i) {
+        const int e = sh.slot_e[pt[i].s], nr = pt[i].r1 - pt[i].r0;
+        const int cd = max(1, min(sh.S / g.d_bytes, (nr + per_part - 1) / per_part));
 #pragma unroll 1
-        for (int r = 0; r < nh; r += cd) {
-            const int n = min(cd, nh - r);
-            f(Lp.down + ((size_t)e * g.H + h0 + r) * g.d_bytes, n * g.d_bytes, s, r, n);
+        for (int r = pt[i].r0; r < pt[i].r1; r += cd) {
+            const int n = min(cd, pt[i].r1 - r);
+            f(Lp.down + ((size_t)e * g.H + r) * g.d_bytes, n * g.d_bytes, pt[i].s, r, n);
         }
     }
 }
@@ -1911,6 +1983,26 @@ __device__ void phase1(const KParams &kp, const Sh &sh, const LayerPtrs &Lp, Cur
         }
 }
 
+// The shared expert's down rows held in the prefetch buffer, by the `nw`
+// warps that finished their routed gate/up stages first (those with one
+// stage fewer than the others; all warps when every warp has as many), this
+// one as number `rank`: they stage the shared activations (published in P1)
+// among themselves and split the rows.
+__device__ void shared_down_light(const KParams &kp, const Sh &sh, const Ws &w, int l, int rank, int nw)
+{
+    const Geo &g = kp.g;
+    const int M = kp.M, lane = threadIdx.x & 31;
+    stage_acts(sh, M, g.Is, rank * 32 + lane, nw * 32, layer_tag(kp, l),
+               [&](int p) -> const uint64_t * { return w.act_s + (size_t)p * g.Is; });
+    asm volatile("bar.sync 4, %0;" ::"r"(nw * 32) : "memory");
+    const uint32_t all = (1u << M) - 1u;
+    const CtaPlan &b = *sh.cp;
+    const int ch = (b.dpb + nw - 1) / nw, r0 = rank * ch;
+    if (r0 < b.dpb)
+        dn_rows(sh, g.sb, sh.pb + b.off_sdown + (size_t)r0 * g.sd_bytes, min(ch, b.dpb - r0), g.sd_bytes, g.Is, all, 0,
+                sh.ysh + r0 * kMaxRows, kMaxRows, 1, 0u);
+}
+
 // Shared down rows held in the prefetch buffer, spread over compute warps
 // w0 .. NCW-1 in equal chunks.
 __device__ void shared_down_pb(const KParams &kp, const Sh &sh, int w0)
@@ -1922,7 +2014,7 @@ __device__ void shared_down_pb(const KParams &kp, const Sh &sh, int w0)
     const int r0 = (warp - w0) * ch;
     if (warp >= w0 && ch > 0 && r0 < b.dpb)
         dn_rows(sh, g.sb, sh.pb + b.off_sdown + (size_t)r0 * g.sd_bytes, min(ch, b.dpb - r0), g.sd_bytes, g.Is, all, 0,
-                sh.ysh + r0 * kMaxRows, kMaxRows, 1);
+                sh.ysh + r0 * kMaxRows, kMaxRows, 1, 0u);
 }
 
 __device__ void phase1b(const KParams &kp, const Sh &sh, const LayerPtrs &Lp, Cursor &q, int l)
@@ -1932,18 +2024,23 @@ __device__ void phase1b(const KParams &kp, const Sh &sh, const LayerPtrs &Lp, Cu
     StageTrace tr{kp.trace ? &kp : nullptr, l, 0, 11, 1};
     sched_p1b(kp, sh, Lp, [&](const uint8_t *, int, int, int first, int n) {
         consume(sh, q, 15, [&](const uint8_t *st) {
-            dn_rows(sh, g.sb, st, n, g.sd_bytes, g.Is, all, 0, sh.ysh + first * kMaxRows, kMaxRows, 1);
+            dn_rows(sh, g.sb, st, n, g.sd_bytes, g.Is, all, 0, sh.ysh + first * kMaxRows, kMaxRows, 1, 0u);
         }, &tr);
     });
 }
 
-__device__ void phase2(const KParams &kp, const Sh &sh, const LayerPtrs &Lp, Cursor &q, const Ws &w, int l)
+// P2.  Returns the number of stages and the turn of the first one.
+__device__ void phase2(const KParams &kp, const Sh &sh, const LayerPtrs &Lp, Cursor &q, const Ws &w, int l, int &n2,
+                       int &turn0)
 {
     const Geo &g = kp.g;
     const int maxr = kp.ws_l.maxr;
     const unsigned tag = layer_tag(kp, l);
     StageTrace tr{kp.trace ? &kp : nullptr, l, 0, 2, 1};
+    n2 = 0;
+    turn0 = q.turn;
     sched_p2(kp, sh, Lp, [&](const uint8_t *, int, int s, int first, int n) {
+        ++n2;
         consume(sh, q, 20, [&](const uint8_t *st) {
             uint64_t *act = w.act + (size_t)s * maxr * g.I;
             gu_units(sh, g.H, g.rb, st, n, g.g_bytes, sh.slot_mask[s], act + first, g.I, tag);
@@ -1951,79 +2048,88 @@ __device__ void phase2(const KParams &kp, const Sh &sh, const LayerPtrs &Lp, Cur
     });
 }
 
-// P3 in rounds of consecutive slots whose activation pairs fit the staging
-// buffer; the producer issued the down stages slot by slot, so the stages of
-// a round are consumed in issue order.
+// P3: per part (see p3_parts), the slot's activations from the CTAs that
+// computed them (tagged, waited for), then the part's down stages; the
+// outputs go to the workspace as tagged words, y[pair][h] for pair =
+// slot_rowbase[s] + rank of the row in the slot's mask.
 __device__ bool phase3(const KParams &kp, const Sh &sh, const LayerPtrs &Lp, Cursor &q, const Ws &w, int l)
 {
     const Geo &g = kp.g;
-    const int maxr = kp.ws_l.maxr, U = sh.flags[1];
+    const int maxr = kp.ws_l.maxr;
+    const unsigned tag = layer_tag(kp, l);
     StageTrace tr{kp.trace ? &kp : nullptr, l, 0, 7, 1};
+    P3Part pt[2];
+    const int np = p3_parts(kp, sh, pt);
 #pragma unroll 1
-    for (int s0 = 0; s0 < U;) {
-        int s1 = s0, pairs = 0;
-#pragma unroll 1
-        while (s1 < U && pairs + __popc(sh.slot_mask[s1]) <= sh.act_pairs) pairs += __popc(sh.slot_mask[s1++]);
-        if (s1 == s0) s1 = s0 + 1;   // cannot happen: act_pairs >= maxr >= popc of any mask
-        const int pbase = sh.slot_rowbase[s0], npairs = sh.slot_rowbase[s1] - pbase;
-        // pair -> (slot, row) table of the round
-        if (threadIdx.x < 32) {
-#pragma unroll 1
-            for (int s = s0 + (int)threadIdx.x; s < s1; s += 32) {
-                uint32_t mask = sh.slot_mask[s];
-#pragma unroll 1
-                for (int p = sh.slot_rowbase[s] - pbase; mask; mask &= mask - 1, ++p)
-                    sh.pair_src[p] = s * kMaxRows + (__ffs(mask) - 1);
-            }
-        }
+    for (int i = 0; i < np; ++i) {
+        const int s = pt[i].s;
+        const uint32_t mask = sh.slot_mask[s];
         cbar();
-        // the round's activations, waited for word by word (tagged)
-        stage_acts(sh, npairs, g.I, 0, NCT, layer_tag(kp, l), [&](int p) -> const uint64_t * {
-            const int ps = sh.pair_src[p];
-            return w.act + ((size_t)(ps / kMaxRows) * maxr + ps % kMaxRows) * g.I;
+        // pair p of the slot: token row __fns(mask, 0, p + 1)
+        stage_acts(sh, __popc(mask), g.I, threadIdx.x, NCT, tag, [&](int p) -> const uint64_t * {
+            return w.act + ((size_t)s * maxr + __fns(mask, 0, p + 1)) * g.I;
         });
         if (cbar_or(aborted(sh))) return false;
-        sched_p3(kp, sh, Lp, [&](const uint8_t *, int, int s, int first, int n) {
-            if (s < s0 || s >= s1) return;
+        uint64_t *y = w.y + (size_t)sh.slot_rowbase[s] * g.H;
+        sched_p3(kp, sh, Lp, [&](const uint8_t *, int, int ss, int first, int n) {
+            if (ss != s) return;
             consume(sh, q, 30, [&](const uint8_t *st) {
-                const int pr = sh.slot_rowbase[s];
-                dn_rows(sh, g.rb, st, n, g.d_bytes, g.I, sh.slot_mask[s], pr - pbase,
-                        sh.ybuf + pr * sh.hrows + first, 1, sh.hrows);
+                dn_rows(sh, g.rb, st, n, g.d_bytes, g.I, mask, 0, y + first, 1, g.H, tag);
             }, &tr);
         });
-        cbar();
-        s0 = s1;
     }
+    cbar();
     return true;
 }
 
 // out = x + sum_j w_j y_j (expert-id order) + sigma y_shared for this CTA's
 // outputs; thread t holds the row pair (2 pl, 2 pl + 1) of token row m,
-// t = pl * M + m, with residuals xr.  Outputs of layers before the last go
-// out as tagged bf16 pairs, the last one as plain bf16.
-__device__ void combine(const KParams &kp, const Sh &sh, const float (&xr)[2], uint64_t *tagged, unsigned tag,
+// t = pl * M + m, with residuals xr.  The routed outputs y_j come from the
+// CTAs that computed them (tagged words, waited for; eight experts' pairs
+// loaded at a time).  Outputs of layers before the last go out as tagged
+// bf16 pairs, the last one as plain bf16.
+__device__ void combine(const KParams &kp, const Sh &sh, const Ws &w, int l, const float (&xr)[2], uint64_t *tagged,
                         uint16_t *plain)
 {
     const Geo &g = kp.g;
     const int M = kp.M, k = g.k, t = threadIdx.x;
     const int h0 = sh.cp->h0, np = sh.cp->nh / 2;
-    if (t < np * M) {
-        const int pl = t / M, m = t % M;
-        uint32_t o[2];
-#pragma unroll
-        for (int hh = 0; hh < 2; ++hh) {
-            const int hl = 2 * pl + hh;
-            float acc = 0.f;
+    const unsigned tag = layer_tag(kp, l);
+    if (t >= np * M) return;
+    const int pl = t / M, m = t % M;
+    float acc[2] = {0.f, 0.f};
 #pragma unroll 1
-            for (int j = 0; j < k; ++j)
-                acc = fmaf(sh.row_w[m * kMaxK + j], sh.ybuf[sh.row_pair[m * kMaxK + j] * sh.hrows + hl], acc);
-            if (g.has_shared) acc = fmaf(sh.sigma[m], sh.ysh[hl * kMaxRows + m], acc);
-            o[hh] = f2bf(xr[hh] + acc);
-        }
-        const uint32_t pair = o[0] | (o[1] << 16);
-        if (tagged) st_tag(tagged + (size_t)m * (g.H / 2) + h0 / 2 + pl, pair, tag);
-        else *reinterpret_cast<uint32_t *>(plain + (size_t)m * g.H + h0 + 2 * pl) = pair;
+    for (int j0 = 0; j0 < k; j0 += 8) {
+        const int nj = min(8, k - j0);
+        uint32_t a[4], b[4], c[4], d[4];
+        const uint64_t *p[8];
+#pragma unroll
+        for (int jj = 0; jj < 8; ++jj)
+            p[jj] = jj < nj ? w.y + (size_t)sh.row_pair[m * kMaxK + j0 + jj] * g.H + h0 + 2 * pl : nullptr;
+        // four experts' word pairs per poll: (p0, p1) and (p2, p3), then the next four
+        poll_pairs4(sh, p[0], p[1], p[2], p[3], tag, 47, a, b);
+        poll_pairs4(sh, p[4], p[5], p[6], p[7], tag, 47, c, d);
+        const uint32_t v[16] = {a[0], a[1], a[2], a[3], b[0], b[1], b[2], b[3],
+                                c[0], c[1], c[2], c[3], d[0], d[1], d[2], d[3]};
+#pragma unroll
+        for (int jj = 0; jj < 8; ++jj)
+            if (jj < nj) {
+                const float wv = sh.row_w[m * kMaxK + j0 + jj];
+                acc[0] = fmaf(wv, __uint_as_float(v[2 * jj]), acc[0]);
+                acc[1] = fmaf(wv, __uint_as_float(v[2 * jj + 1]), acc[1]);
+            }
     }
+    uint32_t o[2];
+#pragma unroll
+    for (int hh = 0; hh < 2; ++hh) {
+        const int hl = 2 * pl + hh;
+        float r = acc[hh];
+        if (g.has_shared) r = fmaf(sh.sigma[m], sh.ysh[hl * kMaxRows + m], r);
+        o[hh] = f2bf(xr[hh] + r);
+    }
+    const uint32_t pair = o[0] | (o[1] << 16);
+    if (tagged) st_tag(tagged + (size_t)m * (g.H / 2) + h0 / 2 + pl, pair, tag);
+    else *reinterpret_cast<uint32_t *>(plain + (size_t)m * g.H + h0 + 2 * pl) = pair;
 }
 
 // out_n = bf16(out * rinv * gamma_next) for this CTA's outputs.
@@ -2084,6 +2190,7 @@ __device__ __forceinline__ void compute(const KParams &kp, const Sh &sh)
     Cursor q = cursor0();
     int nsync = 0;
     const int h0 = sh.cp->h0, np = sh.cp->nh / 2, M = kp.M, H = kp.g.H;
+    const int warp = threadIdx.x >> 5;
 #pragma unroll 1
     for (int l = 0; l < kp.L; ++l) {
         const LayerPtrs &Lp = kp.layer[l];
@@ -2119,14 +2226,20 @@ __device__ __forceinline__ void compute(const KParams &kp, const Sh &sh)
         }
         wstamp(kp, l, 0);
         wstamp(kp, l, 1);
-        phase2(kp, sh, Lp, q, w, l);
+        int n2 = 0, turn0 = 0;
+        phase2(kp, sh, Lp, q, w, l, n2, turn0);
         wstamp(kp, l, 5);
         if (t0) stamp(kp, l, 5);
         // The shared expert's down rows, off the routed path: its activations
         // (waited for from every CTA) into the staging buffer, then the rows
         // held in the prefetch buffer and any that came through the ring.
-        if (kp.g.has_shared) {
-            stage_acts(sh, M, kp.g.Is, 0, NCT, layer_tag(kp, l),
+        if (kp.g.has_shared && sh.cp->dpb == sh.cp->nh) {
+            // the warps done with P2 first take the shared expert's down rows
+            const int r0 = n2 % NCW, d = (warp - turn0 + NCW) % NCW;
+            const int nw = r0 == 0 ? NCW : NCW - r0;
+            if (r0 == 0 || d >= r0) shared_down_light(kp, sh, w, l, r0 == 0 ? d : d - r0, nw);
+        } else if (kp.g.has_shared) {
+            stage_acts(sh, M, kp.g.Is, threadIdx.x, NCT, layer_tag(kp, l),
                        [&](int p) -> const uint64_t * { return w.act_s + (size_t)p * kp.g.Is; });
             cbar();
             shared_down_pb(kp, sh, 0);
@@ -2141,7 +2254,7 @@ __device__ __forceinline__ void compute(const KParams &kp, const Sh &sh)
         if (!phase3(kp, sh, Lp, q, w, l)) return;
         wstamp(kp, l, 10);
         if (cbar_or(aborted(sh))) return;
-        combine(kp, sh, xr, last ? nullptr : w.ping[l & 1], layer_tag(kp, l), kp.out);
+        combine(kp, sh, w, l, xr, last ? nullptr : w.ping[l & 1], kp.out);
         if (t0) stamp(kp, l, 7);
         if (last && kp.out_normed) {
             if (!grid_sync(kp, sh, nsync)) return;
@@ -2189,7 +2302,6 @@ __global__ void __launch_bounds__(kThreads, 1) moe_decode_kernel(const __grid_co
         sh.xsum = reinterpret_cast<float *>(smem + L.xsum);
         sh.act = reinterpret_cast<float4 *>(smem + L.act);
         sh.asum = reinterpret_cast<float *>(smem + L.asum);
-        sh.ybuf = reinterpret_cast<float *>(smem + L.ybuf);
         sh.ysh = reinterpret_cast<float *>(smem + L.ysh);
         sh.pb = smem + L.pb;
         sh.ring = smem + L.ring;

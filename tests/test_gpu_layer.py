@@ -13,7 +13,7 @@ import synth
 import quantized_moe_decode_layer_gb300 as moe
 from quantized_moe_decode_layer_gb300 import _lib
 
-from helpers import assert_close, bf16_tensor_to_f64, bits_np, rows_with_margin, to_device
+from helpers import MARGIN, assert_close, bf16_tensor_to_f64, bits_np, rows_with_margin, to_device
 
 pytestmark = pytest.mark.gpu
 DEV = "cuda"
@@ -252,3 +252,46 @@ def test_barrier_timeout_returns_status():
     again = moe.decode_layer(layer, x, ws)
     assert ws.status() == 0
     assert torch.equal(again.view(torch.int16), good.view(torch.int16))
+
+
+def _rows_with_distinct_margin(shape, lay, seed, gamma=None, max_attempts=200):
+    """One bf16 row whose oracle logits, as a set of distinct values, are at
+    least MARGIN apart down to the (k+1)-th largest expert: exact ties stay
+    exact in both precisions, and no two distinct values can swap."""
+    for a in range(max_attempts):
+        x = synth.make_rows(shape, seed, 1, gamma=gamma, attempts=[a])
+        lg = lay.route(bits_np(x))["logits"][0]
+        d = np.unique(np.sort(lg)[::-1][:shape.k + 2])
+        if len(d) < 2 or np.min(np.diff(d)) >= MARGIN:
+            return x
+    raise RuntimeError("could not draw a row with distinct-value margins")
+
+
+@pytest.mark.parametrize("shape,period", [(synth.TINY, 2), (synth.A35B, 2), (synth.A35B, 4)])
+def test_router_topk_exact_ties(shape, period):
+    """Repeated router rows make logits tie exactly; the top k must list tied
+    experts by ascending id, as the oracle does.  Period 2 at a35b: experts
+    2j and 2j + 1 share a row (pairs of ties among few candidates).  Period 2
+    at tiny and 4 at a35b: expert e uses row e % period; at a35b every lane
+    of the routing warp then holds equal keys and 64 experts tie at the top
+    (the many-ties path)."""
+    L = synth.make_layer(shape, 23, device=DEV)
+    rw = L["router_w"]
+    E = shape.E
+    if period == 2 and shape.E > 16:
+        src = torch.arange(E, device=rw.device) // 2 * 2     # pairs (2j, 2j + 1)
+    else:
+        src = torch.arange(E, device=rw.device) % period
+    L["router_w"] = rw[src].contiguous()
+    layer = moe.Layer(moe.desc_from_shape(shape), moe.layer_src_from_synth(L))
+    lay = oracle.Layer(L)
+    x = _rows_with_distinct_margin(shape, lay, 31, gamma=L["gamma"] if shape.zipf else None)
+    ref = lay.route(bits_np(x))
+    ws = moe.Workspace(layer.desc, 1)
+    idx, w = moe.router_topk(layer, x.to(DEV), ws)
+    assert ws.status() == 0
+    assert np.array_equal(idx.cpu().numpy(), ref["idx"])
+    assert np.allclose(w.cpu().numpy(), ref["w"], rtol=1e-4, atol=1e-6)
+    # the tie structure is really there: some selected experts share a logit
+    lg = ref["logits"][0][ref["idx"][0]]
+    assert len(np.unique(lg)) < shape.k

@@ -88,7 +88,7 @@ constexpr int kShBytes = 512;
 
 struct SmemLayout {
     int shs, cplan, bar, flags, slot_e, slot_mask, slot_rowbase, sigma, eslot, emask, topv, tope, topw;
-    int row_w, row_pair, red, lscr, tks, p1v, pair_src, xs, xsum, act, asum, ysh, pb, ring, total;
+    int row_w, row_pair, red, lscr, p1v, pair_src, xs, xsum, act, asum, ysh, pb, ring, total;
 };
 
 __host__ __device__ inline int take(int &o, int bytes, int align)
@@ -126,7 +126,6 @@ __host__ __device__ inline SmemLayout carve(const Geo &g, const Plan &p)
     L.row_pair = take(o, kMaxRows * kMaxK * 4, 4);
     L.red = take(o, kMaxRows * (NCW + 1) * 4, 4);
     L.lscr = take(o, NCW * kMaxRows * 4, 4);
-    L.tks = take(o, p.maxr * 64 * 4, 16);
     L.p1v = take(o, 2 * per_cta(g.Is > 0 ? g.Is : 1, p.P) * p.maxr * 4, 4);
     L.pair_src = take(o, p.act_pairs * 4, 4);
     L.xs = take(o, p.maxr * g.H * 4, 16);
@@ -349,7 +348,6 @@ struct Sh {
     int *row_pair;
     float *red;          // [kMaxRows][NCW + 1] RMSNorm partial sums, then 1/rms
     float *lscr;         // [NCW][kMaxRows] a warp's router logits before they go out
-    uint32_t *tks;       // [maxr][64] top-k scratch of each routing warp
     float *p1v;          // [shared rows of this CTA][maxr] gate / up values
     int *pair_src;       // [act_pairs] slot * kMaxRows + row of each staged pair
     float4 *xs;          // [maxr][H / 4] arranged hn * 2^100
@@ -1382,10 +1380,10 @@ __device__ __forceinline__ float unkey(uint32_t k)
 }
 
 // Top-k of router row m by one warp, keyed on (logit descending, expert id
-// ascending); lane `lane` holds experts lane + 32 i.  A threshold from the
-// lanes' largest keys leaves a few candidates (at least k), which rank
-// themselves against each other in one pass; when more than 32 tie at the
-// threshold, k rounds of the warp-wide largest remaining key instead.
+// ascending); lane `lane` holds experts lane + 32 i.  k rounds: the warp-wide
+// largest of the lanes' best remaining keys (redux.sync); the lane holding
+// it at its lowest index drops it and records it.  Exact ties between lanes
+// (several lanes hold the largest key) go to the lowest expert id.
 // Writes topv/tope/topw (selection order), row_w/row_pair (expert-id order;
 // row_pair holds the expert id until the slot table is built) and sigma.
 template <int NPL>
@@ -1425,85 +1423,31 @@ __device__ __noinline__ void topk_row_t(const KParams &kp, const Sh &sh, int m, 
     const float lsg = __uint_as_float((uint32_t)v[NPL]);
     float *topv = sh.topv + m * kMaxK;
     int *tope = sh.tope + m * kMaxK;
-    // Threshold T: the k-th largest of the 32 lanes' largest keys, the
-    // smallest lane maximum with fewer than k lane maxima strictly above it.
-    // The k lanes at or above T hold k distinct experts with keys >= T, so
-    // all of the top k have keys >= T; ranked among those candidates alone,
-    // each of the top k gets its rank among all E.  The warp's scratch holds
-    // the 32 lane maxima, then the candidates.
-    uint32_t *scr = sh.tks + m * 64;
-    uint32_t mx = key[0];
-#pragma unroll
-    for (int i = 1; i < NPL; ++i) mx = max(mx, key[i]);
-    scr[lane] = mx;
-    __syncwarp();
-    int rk = 0;
-#pragma unroll
-    for (int j = 0; j < 32; j += 4) {
-        const uint4 q = *reinterpret_cast<const uint4 *>(scr + j);
-        rk += (q.x > mx ? 1 : 0) + (q.y > mx ? 1 : 0) + (q.z > mx ? 1 : 0) + (q.w > mx ? 1 : 0);
-    }
-    const uint32_t T = __reduce_min_sync(FULLMASK, rk < k ? mx : 0xFFFFFFFFu);
-    // candidate (lane, i) goes to slot (candidates of columns < i) + (lanes
-    // below with a candidate in column i)
-    const unsigned below = (1u << lane) - 1u;
-    int C = 0, pos[NPL];
-#pragma unroll
-    for (int i = 0; i < NPL; ++i) {
-        const unsigned b = __ballot_sync(FULLMASK, key[i] >= T);
-        pos[i] = C + __popc(b & below);
-        C += __popc(b);
-    }
-    __syncwarp();
-    if (C <= 32) {
-        uint2 *cand = reinterpret_cast<uint2 *>(scr);
-#pragma unroll
-        for (int i = 0; i < NPL; ++i)
-            if (key[i] >= T) cand[pos[i]] = make_uint2(key[i], (uint32_t)(lane + 32 * i));
-        __syncwarp();
-        // a candidate's rank: how many others precede it in (key
-        // descending, expert ascending)
-        if (lane < C) {
-            const uint2 me = cand[lane];
-            int r = 0;
 #pragma unroll 1
-            for (int j = 0; j < C; ++j) {
-                const uint2 ot = cand[j];
-                r += (ot.x > me.x || (ot.x == me.x && ot.y < me.y)) ? 1 : 0;
-            }
-            if (r < k) {
-                topv[r] = unkey(me.x);
-                tope[r] = (int)me.y;
-            }
+    for (int r = 0; r < k; ++r) {
+        uint32_t t[NPL];
+#pragma unroll
+        for (int i = 0; i < NPL; ++i) t[i] = key[i];
+#pragma unroll
+        for (int w = NPL >> 1; w > 0; w >>= 1)
+#pragma unroll
+            for (int i = 0; i < w; ++i) t[i] = max(t[i], t[i + w]);
+        const uint32_t wk = __reduce_max_sync(FULLMASK, t[0]);
+        // the lane's lowest index holding wk (NPL if none)
+        int bi = NPL;
+#pragma unroll
+        for (int i = NPL - 1; i >= 0; --i) bi = key[i] == wk ? i : bi;
+        const unsigned bal = __ballot_sync(FULLMASK, bi < NPL);
+        int wl = __ffs(bal) - 1;
+        if (bal & (bal - 1u)) {
+            const unsigned we = __reduce_min_sync(FULLMASK, bi < NPL ? (unsigned)(lane + 32 * bi) : 0xFFFFFFFFu);
+            wl = (int)(we & 31u);
         }
-    } else {
-        // many keys tie at T: k rounds of the warp-wide best remaining key;
-        // exact ties between lanes go to the lowest expert id
-#pragma unroll 1
-        for (int r = 0; r < k; ++r) {
-            uint32_t t[NPL];
+        if (lane == wl) {
 #pragma unroll
-            for (int i = 0; i < NPL; ++i) t[i] = key[i];
-#pragma unroll
-            for (int w = NPL >> 1; w > 0; w >>= 1)
-#pragma unroll
-                for (int i = 0; i < w; ++i) t[i] = max(t[i], t[i + w]);
-            const uint32_t wk = __reduce_max_sync(FULLMASK, t[0]);
-            int bi = NPL;
-#pragma unroll
-            for (int i = NPL - 1; i >= 0; --i) bi = key[i] == wk ? i : bi;
-            const unsigned bal = __ballot_sync(FULLMASK, bi < NPL);
-            int wl = __ffs(bal) - 1;
-            if (bal & (bal - 1u)) {
-                const unsigned we = __reduce_min_sync(FULLMASK, bi < NPL ? (unsigned)(lane + 32 * bi) : 0xFFFFFFFFu);
-                wl = (int)(we & 31u);
-            }
-            if (lane == wl) {
-#pragma unroll
-                for (int i = 0; i < NPL; ++i) key[i] = i == bi ? 0u : key[i];
-                topv[r] = unkey(wk);
-                tope[r] = lane + 32 * bi;
-            }
+            for (int i = 0; i < NPL; ++i) key[i] = i == bi ? 0u : key[i];
+            topv[r] = unkey(wk);
+            tope[r] = lane + 32 * bi;
         }
     }
     __syncwarp();
@@ -2352,7 +2296,6 @@ __global__ void __launch_bounds__(kThreads, 1) moe_decode_kernel(const __grid_co
         sh.row_pair = reinterpret_cast<int *>(smem + L.row_pair);
         sh.red = reinterpret_cast<float *>(smem + L.red);
         sh.lscr = reinterpret_cast<float *>(smem + L.lscr);
-        sh.tks = reinterpret_cast<uint32_t *>(smem + L.tks);
         sh.p1v = reinterpret_cast<float *>(smem + L.p1v);
         sh.pair_src = reinterpret_cast<int *>(smem + L.pair_src);
         sh.xs = reinterpret_cast<float4 *>(smem + L.xs);

@@ -39,7 +39,7 @@ def parse():
     p.add_argument("--warmup", type=int, default=10)
     p.add_argument("--impl", default="ours", choices=["ours", "reference"])
     p.add_argument("--layers", type=int, default=LAYERS)
-    p.add_argument("--no-m4", action="store_true")
+    p.add_argument("--no-m4", action="store_true", help="M=1 only: no M=4 line and no M sweep")
     p.add_argument("--cpu-seconds", type=float, default=12.0)
     return p.parse_args()
 
@@ -275,6 +275,45 @@ def run_ours(args):
               "frac": round(bytes4 / (mean4 * 1e-3) / 1e9 / peaks["hbm_gbs"], 4),
               "mean_U": round(float(np.mean(U4)), 2), "bytes_per_step": bytes4}
 
+    # the stack over M in {1, 2, 4, 8, 32} independent token rows (M above 8
+    # runs as launches of 8 rows; the bytes are still each selected expert
+    # once per step, so re-reads across launches count against GB/s)
+    sweep = None
+    if not args.no_m4:
+        sweep = {}
+        wsw = moe.Workspace(desc, 32)
+        for M in (1, 2, 4, 8, 32):
+            xm = synth.make_rows(shape, 40 + M, M).to(dev)
+            Um = measure_U(layers, xm, wsw)
+            bm = sum(unique_bytes(shape, u, M) for u in Um)
+            sm = max(10, args.steps // 10)
+            tmm, perm, _ = time_stack(st, xm, wsw, sm, args.warmup, stream)
+            s_step = tmm / sm * 1e-3
+            sweep[str(M)] = {"tokens_per_s": round(M / s_step, 1), "us_per_layer": round(s_step * 1e6 / args.layers, 3),
+                             "gbs": round(bm / s_step / 1e9, 1), "mean_U": round(float(np.mean(Um)), 2),
+                             "launches_per_step": -(-M // min(8, 16384 // shape.H))}
+        del wsw
+
+    # the 397B-shaped layer at M=1: a stack over 15 distinct layer sets (55 GB)
+    b397 = None
+    if not args.no_m4:
+        shb = synth.B397
+        descb, layb = build_stack(shb, 15, dev, seed0=3000)
+        stb = moe.Stack(layb)
+        xb = synth.make_rows(shb, 8, 1).to(dev)
+        wsb = moe.Workspace(descb, 1)
+        Ub = measure_U(layb, xb, wsb)
+        bb = sum(unique_bytes(shb, u, 1) for u in Ub)
+        sb = max(20, args.steps // 4)
+        tmb, perb, _ = time_stack(stb, xb, wsb, sb, args.warmup, stream)
+        meanb = sum(perb) / len(perb)
+        b397 = {"layers": 15, "us_per_layer": round(tmb / sb * 1e3 / 15, 3),
+                "gbs": round(bb / (meanb * 1e-3) / 1e9, 1),
+                "frac": round(bb / (meanb * 1e-3) / 1e9 / peaks["hbm_gbs"], 4),
+                "resident_weight_GB": round(sum(l.nbytes for l in layb) / 1e9, 2), "bytes_per_step": bb}
+        del stb, layb, wsb
+        torch.cuda.empty_cache()
+
     # single-layer calls (one launch per layer) over the 40 rotating layer sets
     single = None
     if rank == 0:
@@ -305,7 +344,7 @@ def run_ours(args):
                        "l2": "weights rotate over 40 layer sets (26 GB) > L2; no flush",
                        "parallelism": f"replicas x{world}"},
             "us_per_layer": round(us_layer, 3), "fraction_of_8TBs": round(value / world / 8000.0, 4),
-            "single_layer_call_us": single, "m4": m4, "roofline": roof, "e2e": e2e,
+            "single_layer_call_us": single, "m4": m4, "sweep": sweep, "b397": b397, "roofline": roof, "e2e": e2e,
             "gpu_launches": launches, "clocks": clocks, "cpu_baseline": cpu,
         }
         print(json.dumps(line), flush=True)

@@ -190,6 +190,46 @@ def time_stack(st, x, ws, steps, warmup, stream):
     return total_ms, per, launches
 
 
+def tc_measure(layers, desc, shape, dev, M, warmup):
+    """Time moe_gate_up_tc over the layer sets for M routed rows: one call per
+    layer (its distinct experts with their row masks), CUDA events around the
+    whole pass.  Bytes: the gate/up rows of each call's experts once; flops:
+    2 * 2I * H per (expert, row) pair."""
+    import numpy as np
+    import torch
+    import synth
+    import quantized_moe_decode_layer_gb300 as moe
+    ws = moe.Workspace(desc, M)
+    x = synth.make_rows(shape, 40 + M, M).to(dev)
+    from quantized_moe_decode_layer_gb300.profile_case import tc_routing
+    cases = tc_routing(layers, x, ws)
+    acts = [torch.zeros((int(ex.numel()), M, shape.I), dtype=torch.float32, device=dev) for ex, _, _ in cases]
+    err = torch.zeros(1, dtype=torch.int32, device=dev)
+    for _ in range(max(1, warmup)):
+        for (ex, mk, hn), act, lyr in zip(cases, acts, layers):
+            moe.gate_up_tc(lyr, hn, ex, mk, act=act, err=err)
+    torch.cuda.synchronize()
+    reps = 5
+    a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    a.record()
+    for _ in range(reps):
+        for (ex, mk, hn), act, lyr in zip(cases, acts, layers):
+            moe.gate_up_tc(lyr, hn, ex, mk, act=act, err=err)
+    b.record()
+    torch.cuda.synchronize()
+    assert int(err.item()) == 0
+    per_call_s = a.elapsed_time(b) * 1e-3 / (reps * len(layers))
+    U = np.array([int(ex.numel()) for ex, _, _ in cases])
+    pairs = np.array([sum(bin(int(m) & 0xFFFFFFFF).count("1") for m in mk.cpu().tolist()) for _, mk, _ in cases])
+    unit_bytes = 2 * (shape.H * shape.routed_bits // 8 + shape.H // 64 * 4)
+    bytes_call = float(np.mean(U)) * shape.I * unit_bytes
+    flops_call = float(np.mean(pairs)) * 2 * (2 * shape.I) * shape.H
+    return {"M": M, "us_per_call": round(per_call_s * 1e6, 3), "mean_U": round(float(np.mean(U)), 2),
+            "rows_per_expert": round(float(np.mean(pairs / U)), 2),
+            "gbs": round(bytes_call / per_call_s / 1e9, 1), "tflops": round(flops_call / per_call_s / 1e12, 2),
+            "calls": reps * len(layers)}
+
+
 def run_ours(args):
     import numpy as np
     import torch
@@ -294,6 +334,13 @@ def run_ours(args):
                              "launches_per_step": -(-M // min(8, 16384 // shape.H))}
         del wsw
 
+    # the grouped gate/up on the tensor cores (moe_gate_up_tc) for the M=32
+    # rows' experts, layer after layer over the 40 layer sets (2 GB of gate/up
+    # weights in all, so L2 holds none of a call's weights from the call before)
+    tc = None
+    if not args.no_m4:
+        tc = {str(M): tc_measure(layers, desc, shape, dev, M, args.warmup) for M in (8, 32)}
+
     # the 397B-shaped layer at M=1: a stack over 15 distinct layer sets (55 GB)
     b397 = None
     if not args.no_m4:
@@ -344,7 +391,7 @@ def run_ours(args):
                        "l2": "weights rotate over 40 layer sets (26 GB) > L2; no flush",
                        "parallelism": f"replicas x{world}"},
             "us_per_layer": round(us_layer, 3), "fraction_of_8TBs": round(value / world / 8000.0, 4),
-            "single_layer_call_us": single, "m4": m4, "sweep": sweep, "b397": b397, "roofline": roof, "e2e": e2e,
+            "single_layer_call_us": single, "m4": m4, "sweep": sweep, "tc_gate_up": tc, "b397": b397, "roofline": roof, "e2e": e2e,
             "gpu_launches": launches, "clocks": clocks, "cpu_baseline": cpu,
         }
         print(json.dumps(line), flush=True)

@@ -236,6 +236,30 @@ int moe_debug_set(int skip_row, long long timeout_ns);
  * each layer goes (per phase, per CTA). */
 int moe_debug_trace(void *trace_dev, size_t bytes);
 
+/* Grouped gate/up of routed experts on the tensor cores (tcgen05 MMAs,
+ * fp32 accumulators in tensor memory): the first half of each selected
+ * expert's FFN for every token row that chose it, when many rows share an
+ * expert (flash-moe, "Metal Compute Shaders": dequant mat-vec and SwiGLU;
+ * PureDrive-35B-A3B model card, "How it works": one read of the weights for
+ * all rows).  Not used by moe_decode_layer or the stack, which stay on the
+ * FMA pipes; it is the measured alternative for many rows per expert.
+ *
+ *   for u < U, e = experts_dev[u], each row m < M with bit m of masks_dev[u]:
+ *     act_dev[(u * M + m) * I + j] = silu(W_gate,e[j] . hn_m) * (W_up,e[j] . hn_m)
+ *
+ * hn_dev: fp32 [M][H], rows already normalised (device).  experts_dev int32 [U]
+ * and masks_dev uint32 [U] (device).  act_dev: fp32 [U][M][I] (device); entries
+ * of rows outside a mask are not written (mask bits at or above M are
+ * ignored).  M <= 32.  Arithmetic: each weight
+ * is rounded once to bf16 (w = q * s + b in fp32, round to nearest even);
+ * each input is split into two bf16 halves (hi = bf16(x), lo = bf16(x - hi));
+ * products accumulate in fp32.  err_dev (device int) is set to 1 if a device
+ * wait runs out (see moe_debug_set); the caller clears it.
+ * Errors: INVALID_ARG (NULL pointer, M < 1, U < 0), UNSUPPORTED (M > 32),
+ * CUDA (launch failed). */
+int moe_gate_up_tc(const moe_layer *layer, const float *hn_dev, int M, const int32_t *experts_dev,
+                   const uint32_t *masks_dev, int U, float *act_dev, int *err_dev, moe_stream_t stream);
+
 /* Human-readable name of a status code (static string). */
 const char *moe_status_str(int status);
 

@@ -180,6 +180,24 @@ def decode_layer(layer: Layer, x: torch.Tensor, ws: Workspace, out=None, normed:
     return (out, on) if normed else out
 
 
+def gate_up_tc(layer: Layer, hn: torch.Tensor, experts: torch.Tensor, masks: torch.Tensor, act=None,
+               err=None, stream=None):
+    """Grouped gate/up + SwiGLU on the tensor cores (moe_gate_up_tc).
+
+    hn fp32 [M, H] (normalised rows), experts int32 [U], masks int32 [U] (bit m
+    = row m) on the device.  Returns (act fp32 [U, M, I], err int32 [1]);
+    entries of rows outside a mask are left as they were in `act` (zeros when
+    it is allocated here)."""
+    M, U, I = hn.shape[0], experts.shape[0], layer.desc.I
+    if act is None:
+        act = torch.zeros((U, M, I), dtype=torch.float32, device=hn.device)
+    if err is None:
+        err = torch.zeros(1, dtype=torch.int32, device=hn.device)
+    check("moe_gate_up_tc", lib().moe_gate_up_tc(layer.handle, _ptr(hn.contiguous()), M, _ptr(experts), _ptr(masks),
+                                                 U, _ptr(act), _ptr(err), _stream(stream)))
+    return act, err
+
+
 class Stack:
     def __init__(self, layers):
         self.layers = list(layers)

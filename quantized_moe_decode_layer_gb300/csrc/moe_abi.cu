@@ -452,6 +452,18 @@ int moe_debug_trace(void *trace_dev, size_t bytes)
     return MOE_OK;
 }
 
+int moe_gate_up_tc(const moe_layer *layer, const float *hn_dev, int M, const int32_t *experts_dev,
+                   const uint32_t *masks_dev, int U, float *act_dev, int *err_dev, moe_stream_t stream)
+{
+    if (!layer || !hn_dev || !experts_dev || !masks_dev || !act_dev || !err_dev || M < 1 || U < 0)
+        return MOE_ERR_INVALID_ARG;
+    if (M > 32 || layer->geo.I % 64 != 0 || layer->geo.H % 64 != 0 || !bits_ok(layer->geo.rb))
+        return MOE_ERR_UNSUPPORTED;
+    if (U == 0) return MOE_OK;
+    return launch_gate_up_tc(*layer, hn_dev, M, experts_dev, masks_dev, U, act_dev, err_dev, g_timeout_ns,
+                             reinterpret_cast<cudaStream_t>(stream));
+}
+
 const char *moe_status_str(int status)
 {
     switch (status) {

@@ -149,6 +149,8 @@ int launch_decode(const KParams &kp, cudaStream_t stream);
 int launch_pack(const moe_layer &L, const moe_src_layer &src, cudaStream_t stream);
 int launch_export(const moe_layer &L, int tensor_id, int expert, uint8_t *codes, uint16_t *scales,
                   uint16_t *biases, cudaStream_t stream);
+int launch_gate_up_tc(const moe_layer &L, const float *hn, int M, const int32_t *experts, const uint32_t *masks, int U,
+                      float *act, int *err, long long timeout_ns, cudaStream_t stream);
 void note_cuda_error(int err);
 void note_launch();
 }  // namespace moe

@@ -1,0 +1,337 @@
+// Grouped gate/up projection of the routed experts on the 5th-generation
+// tensor cores (tcgen05, accumulators in tensor memory): the grouped-GEMM
+// regime that appears when many token rows share an expert.  Not on the decode
+// path: the decode kernel keeps every step on the FMA pipes, where each token
+// row's result is bitwise the one-row result; this kernel stands beside it
+// as a measured alternative for M up to 32.
+//
+// What it computes (the expert FFN's first half as the pages state it:
+// dequantised weight w = q * s + b per group of 64 along the input axis, then
+// SwiGLU): for each listed expert e and each token row m in its mask,
+//   act[u][m][j] = silu(W_gate,e[j] . hn[m]) * (W_up,e[j] . hn[m]).
+//
+// Layout and arithmetic:
+//   - One CTA per (expert, tile of 128 consecutive gate/up rows = 64 units).
+//     The tile is the MMA's M = 128 dimension.
+//   - The token rows are the N dimension: N = 64 = 32 rows of the high bf16
+//     halves of hn, then 32 rows of the low halves (hn - bf16(hn)), so the
+//     activations keep ~16 significant bits.  The weights are rounded once to
+//     bf16 (w = fma(q, s, b) in fp32, then round-to-nearest-even).
+//   - K runs over the input axis in chunks of 64 (one quantisation group):
+//     each of the CTA's 256 threads dequantises half a group of one tile row
+//     into shared memory and writes 16 inputs of the token-row chunk next to
+//     it, and one thread issues 4 MMAs of K = 16 into the same fp32
+//     accumulator in tensor memory.  The codes of chunk c + 2 and the inputs
+//     of chunk c + 1 load while chunk c is converted.
+//     Two chunk buffers alternate; an MMA batch's commit arrives on the
+//     buffer's mbarrier, which the next writers of that buffer wait on.
+//   - Shared-memory tiles use the no-swizzle K-major canonical layout: 8x16-
+//     byte core matrices of 128 contiguous bytes, 128 B apart along K and
+//     1024 B apart along M/N.
+//   - Epilogue: warp w < 4 reads tensor-memory lanes 32w .. 32w + 31 (its rows),
+//     adds the high and low columns, and gate/up neighbours (rows 2j, 2j + 1)
+//     meet through one shuffle for SwiGLU.
+// Every wait is bounded; a wait that runs out sets *err and the CTA skips
+// the rest of its work, still freeing its tensor memory.
+
+#include <cuda_runtime.h>
+#include <cuda_bf16.h>
+#include <stdint.h>
+
+#include "moe_internal.h"
+
+namespace moe {
+namespace {
+
+constexpr int kTcRows = 128;      // weight rows per tile (MMA M)
+constexpr int kTcTok = 32;        // token rows per call at most
+constexpr int kTcN = 2 * kTcTok;  // MMA N: high halves, then low halves
+constexpr int kTcK = 64;          // input elements per chunk (one group)
+constexpr int kTcThreads = 256;
+constexpr int kTileA = kTcRows * kTcK * 2;  // bytes of a weight chunk (16 KB)
+constexpr int kTileB = kTcN * kTcK * 2;     // bytes of a token chunk (8 KB)
+constexpr int kTcSmem = 2 * kTileA + 2 * kTileB + 64;
+constexpr uint32_t kTmemCols = 64;          // fp32 accumulator columns (= N)
+
+__device__ __forceinline__ uint32_t su32(const void *p) { return (uint32_t)__cvta_generic_to_shared(p); }
+
+// Byte offset of element (r, k) of a [rows x 64] bf16 tile in the no-swizzle
+// K-major layout (core matrix = 8 rows x 8 elements, 128 contiguous bytes).
+__device__ __forceinline__ uint32_t canon(int r, int k)
+{
+    return (uint32_t)((r >> 3) * 1024 + (k >> 3) * 128 + (r & 7) * 16 + (k & 7) * 2);
+}
+
+// Shared-memory matrix descriptor: start address, leading-dimension byte
+// offset (between core matrices along K: 128), stride-dimension byte offset
+// (between 8-row groups: 1024), descriptor version 1, no swizzle.
+__device__ __forceinline__ uint64_t smem_desc(uint32_t addr)
+{
+    return (uint64_t)((addr & 0x3FFFFu) >> 4) | ((uint64_t)(128u >> 4) << 16) | ((uint64_t)(1024u >> 4) << 32) |
+           (1ull << 46);
+}
+
+// Instruction descriptor of kind::f16: fp32 accumulator, bf16 A and B, both
+// K-major, N = kTcN, M = kTcRows.
+constexpr uint32_t kIdesc = (1u << 4) | (1u << 7) | (1u << 10) | ((uint32_t)(kTcN >> 3) << 17) |
+                            ((uint32_t)(kTcRows >> 4) << 24);
+
+__device__ __forceinline__ bool mbar_wait_bounded(uint32_t bar, unsigned parity, long long timeout_ns)
+{
+    unsigned long long t0;
+    asm volatile("mov.u64 %0, %%globaltimer;" : "=l"(t0));
+#pragma unroll 1
+    for (;;) {
+        uint32_t done;
+        asm volatile("{ .reg .pred p; mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2; selp.u32 %0, 1, 0, p; }"
+                     : "=r"(done)
+                     : "r"(bar), "r"(parity)
+                     : "memory");
+        if (done) return true;
+        unsigned long long t;
+        asm volatile("mov.u64 %0, %%globaltimer;" : "=l"(t));
+        if ((long long)(t - t0) > timeout_ns) return false;
+    }
+}
+
+__device__ __forceinline__ uint32_t pack_bf16(float a, float b)
+{
+    const uint32_t lo = __bfloat16_as_ushort(__float2bfloat16_rn(a));
+    const uint32_t hi = __bfloat16_as_ushort(__float2bfloat16_rn(b));
+    return lo | (hi << 16);
+}
+
+// Code k (0 .. 31) of half a group's LSB-first code stream, held in the
+// BITS words w (32 codes of BITS bits).
+template <int BITS>
+__device__ __forceinline__ uint32_t code_at(const uint32_t (&w)[BITS], int k)
+{
+    const int bit = k * BITS, wi = bit >> 5, off = bit & 31;
+    uint32_t v = w[wi] >> off;
+    if (off + BITS > 32) v |= w[wi + 1] << (32 - off);
+    return v & ((1u << BITS) - 1u);
+}
+
+template <int BITS>
+__global__ void __launch_bounds__(kTcThreads, 1)
+gate_up_tc_kernel(const uint8_t *__restrict__ gu, int H, int I, int g_bytes, const float *__restrict__ hn, int M,
+                  const int32_t *__restrict__ experts, const uint32_t *__restrict__ masks, float *__restrict__ act,
+                  long long timeout_ns, int *err)
+{
+    extern __shared__ __align__(1024) uint8_t sm[];
+    uint8_t *const A0 = sm, *const B0 = sm + 2 * kTileA;   // buffer b at A0 + b kTileA, B0 + b kTileB
+    uint64_t *bar = reinterpret_cast<uint64_t *>(sm + 2 * kTileA + 2 * kTileB);
+    uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(bar + 2);
+    const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+    const int u = blockIdx.y, tile = blockIdx.x;
+    const int e = experts[u];
+    const uint32_t mask = masks[u];
+    const int nr = __popc(mask);
+
+    if (tid == 0) {
+        asm volatile("mbarrier.init.shared::cta.b64 [%0], 1;" ::"r"(su32(&bar[0])) : "memory");
+        asm volatile("mbarrier.init.shared::cta.b64 [%0], 1;" ::"r"(su32(&bar[1])) : "memory");
+        asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+    }
+    if (warp == 0) {
+        asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(su32(tmem_slot)),
+                     "r"(kTmemCols)
+                     : "memory");
+        asm volatile("tcgen05.relinquish_alloc_permit.cta_group::1.sync.aligned;" ::: "memory");
+    }
+    asm volatile("tcgen05.fence::before_thread_sync;" ::: "memory");
+    __syncthreads();
+    asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory");
+    const uint32_t taddr = *tmem_slot;
+
+    // this thread's half weight row (row tid / 2 of the tile, codes 32 (tid
+    // & 1) .. + 31 of each group) and its token-chunk share (B row tid / 4,
+    // inputs 16 (tid & 3) .. + 15 of each chunk)
+    const int arow = tid >> 1, ah = tid & 1;
+    const uint8_t *row = gu + ((size_t)e * 2 * I + (size_t)kTcRows * tile + arow) * (size_t)g_bytes;
+    const uint32_t *codes = reinterpret_cast<const uint32_t *>(row) + ah * BITS;   // + c * 2 BITS words
+    const uint32_t *sbp = reinterpret_cast<const uint32_t *>(row + (size_t)H * BITS / 8);
+    const int brow = tid >> 2, kq = (tid & 3) * 16;
+    const int tn = brow & (kTcTok - 1);
+    const bool lo_half = brow >= kTcTok;
+    int trow = tn < nr ? (int)__fns(mask, 0, tn + 1) : -1;
+    if (trow >= M) trow = -1;   // mask bits at or above M name no row
+    const float4 *hsrc = reinterpret_cast<const float4 *>(hn + (size_t)(trow < 0 ? 0 : trow) * H + kq);
+
+    const int G = H / kTcK;
+    // Loads run ahead of use: the codes and scale of chunk c + 2 and the
+    // inputs of chunk c + 1 are in flight while chunk c is converted.
+    uint32_t w0[BITS], w1[BITS], w2[BITS], sb0 = 0u, sb1 = 0u, sb2 = 0u;
+    float4 h0[4], h1[4];
+    auto load_codes = [&](int c, uint32_t (&w)[BITS], uint32_t &sb) {
+        if (c < G) {
+#pragma unroll
+            for (int i = 0; i < BITS; ++i) w[i] = __ldg(codes + c * 2 * BITS + i);
+            sb = __ldg(sbp + c);
+        }
+    };
+    auto load_inputs = [&](int c, float4 (&h)[4]) {
+#pragma unroll
+        for (int i = 0; i < 4; ++i) h[i] = make_float4(0.f, 0.f, 0.f, 0.f);
+        if (c < G && trow >= 0) {
+#pragma unroll
+            for (int i = 0; i < 4; ++i) h[i] = __ldg(hsrc + c * (kTcK / 4) + i);
+        }
+    };
+    load_codes(0, w0, sb0);
+    load_codes(1, w1, sb1);
+    load_inputs(0, h0);
+    bool ok = true;
+#pragma unroll 1
+    for (int c = 0; c < G; ++c) {
+        const int b = c & 1;
+        uint8_t *const Ab = A0 + b * kTileA, *const Bb = B0 + b * kTileB;
+        load_codes(c + 2, w2, sb2);
+        load_inputs(c + 1, h1);
+        // the MMAs that last read buffer b (chunk c - 2) must be done (a
+        // thread whose wait runs out still takes part in this chunk's
+        // barrier, after which the whole CTA stops)
+        if (c >= 2) ok = mbar_wait_bounded(su32(&bar[b]), (unsigned)((c - 2) >> 1) & 1u, timeout_ns);
+        // weights: 32 bf16 values of row arow, group c
+        {
+            const float sc = __uint_as_float(sb0 << 16), bb = __uint_as_float(sb0 & 0xFFFF0000u);
+#pragma unroll
+            for (int k8 = 0; k8 < 4; ++k8) {
+                uint32_t p[4];
+#pragma unroll
+                for (int j = 0; j < 4; ++j)
+                    p[j] = pack_bf16(fmaf((float)code_at<BITS>(w0, 8 * k8 + 2 * j), sc, bb),
+                                     fmaf((float)code_at<BITS>(w0, 8 * k8 + 2 * j + 1), sc, bb));
+                *reinterpret_cast<uint4 *>(Ab + canon(arow, 32 * ah + 8 * k8)) = make_uint4(p[0], p[1], p[2], p[3]);
+            }
+        }
+        // token rows: B row brow holds the high (or low) bf16 half of token
+        // row trow, inputs 64 c + kq .. + 15
+        {
+            float v[16];
+#pragma unroll
+            for (int i = 0; i < 4; ++i) {
+                v[4 * i] = h0[i].x; v[4 * i + 1] = h0[i].y; v[4 * i + 2] = h0[i].z; v[4 * i + 3] = h0[i].w;
+            }
+#pragma unroll
+            for (int i = 0; i < 16; ++i) {
+                const float hi = __bfloat162float(__float2bfloat16_rn(v[i]));
+                v[i] = lo_half ? v[i] - hi : hi;
+            }
+#pragma unroll
+            for (int k8 = 0; k8 < 2; ++k8)
+                *reinterpret_cast<uint4 *>(Bb + canon(brow, kq + 8 * k8)) =
+                    make_uint4(pack_bf16(v[8 * k8], v[8 * k8 + 1]), pack_bf16(v[8 * k8 + 2], v[8 * k8 + 3]),
+                               pack_bf16(v[8 * k8 + 4], v[8 * k8 + 5]), pack_bf16(v[8 * k8 + 6], v[8 * k8 + 7]));
+        }
+#pragma unroll
+        for (int i = 0; i < BITS; ++i) { w0[i] = w1[i]; w1[i] = w2[i]; }
+        sb0 = sb1;
+        sb1 = sb2;
+#pragma unroll
+        for (int i = 0; i < 4; ++i) h0[i] = h1[i];
+        // the generic-proxy stores above become visible to the tensor core
+        asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+        ok = __syncthreads_and(ok);
+        if (!ok) break;
+        if (tid == 0) {
+            asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory");
+#pragma unroll
+            for (int kk = 0; kk < kTcK / 16; ++kk) {
+                const uint64_t ad = smem_desc(su32(Ab) + kk * 256), bd = smem_desc(su32(Bb) + kk * 256);
+                const uint32_t accumulate = (c > 0 || kk > 0) ? 1u : 0u;
+                asm volatile("{\n\t.reg .pred p;\n\tsetp.ne.b32 p, %4, 0;\n\t"
+                             "tcgen05.mma.cta_group::1.kind::f16 [%0], %1, %2, %3, p;\n\t}" ::"r"(taddr),
+                             "l"(ad), "l"(bd), "r"(kIdesc), "r"(accumulate)
+                             : "memory");
+            }
+            asm volatile("tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];" ::"r"(
+                             su32(&bar[b]))
+                         : "memory");
+        }
+    }
+    // the last commit covers every MMA this CTA issued
+    if (ok && G > 0) ok = mbar_wait_bounded(su32(&bar[(G - 1) & 1]), (unsigned)((G - 1) >> 1) & 1u, timeout_ns);
+    ok = __syncthreads_and(ok);
+    asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory");
+    if (!ok) {
+        if (tid == 0) atomicExch(err, 1);
+    } else if (warp < 4) {
+        // warps 0-3: lane 32 warp + lane of tensor memory = tile row tid;
+        // columns n (high halves) and 32 + n (low halves) of token row n
+        float y[kTcTok];
+#pragma unroll
+        for (int part = 0; part < 2; ++part) {
+            uint32_t r[32];
+            const uint32_t a = taddr + ((uint32_t)(32 * warp) << 16) + (uint32_t)(32 * part);
+            asm volatile("tcgen05.ld.sync.aligned.32x32b.x32.b32 {%0, %1, %2, %3, %4, %5, %6, %7, %8, %9, %10, %11, "
+                         "%12, %13, %14, %15, %16, %17, %18, %19, %20, %21, %22, %23, %24, %25, %26, %27, %28, %29, "
+                         "%30, %31}, [%32];"
+                         : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]), "=r"(r[6]),
+                           "=r"(r[7]), "=r"(r[8]), "=r"(r[9]), "=r"(r[10]), "=r"(r[11]), "=r"(r[12]), "=r"(r[13]),
+                           "=r"(r[14]), "=r"(r[15]), "=r"(r[16]), "=r"(r[17]), "=r"(r[18]), "=r"(r[19]),
+                           "=r"(r[20]), "=r"(r[21]), "=r"(r[22]), "=r"(r[23]), "=r"(r[24]), "=r"(r[25]),
+                           "=r"(r[26]), "=r"(r[27]), "=r"(r[28]), "=r"(r[29]), "=r"(r[30]), "=r"(r[31])
+                         : "r"(a)
+                         : "memory");
+            asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory");
+#pragma unroll
+            for (int n = 0; n < kTcTok; ++n) y[n] = part ? y[n] + __uint_as_float(r[n]) : __uint_as_float(r[n]);
+        }
+        // rows 2j (gate) and 2j + 1 (up) of unit j = 64 tile + tid / 2
+        const int j = (kTcRows / 2) * tile + (tid >> 1);
+#pragma unroll 1
+        for (int n = 0; n < nr; ++n) {
+            float yn = 0.f;
+#pragma unroll
+            for (int t = 0; t < kTcTok; ++t) yn = t == n ? y[t] : yn;
+            const float other = __shfl_xor_sync(0xFFFFFFFFu, yn, 1);
+            const int m = (int)__fns(mask, 0, n + 1);
+            if ((tid & 1) == 0 && m < M) act[((size_t)u * M + m) * I + j] = yn / (1.0f + expf(-yn)) * other;
+        }
+        (void)lane;
+    }
+    asm volatile("tcgen05.fence::before_thread_sync;" ::: "memory");
+    __syncthreads();
+    if (warp == 0)
+        asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;" ::"r"(taddr), "r"(kTmemCols) : "memory");
+}
+
+}  // namespace
+
+int launch_gate_up_tc(const moe_layer &L, const float *hn, int M, const int32_t *experts, const uint32_t *masks, int U,
+                      float *act, int *err, long long timeout_ns, cudaStream_t stream)
+{
+    const Geo &g = L.geo;
+    const dim3 grid((unsigned)(2 * g.I / kTcRows), (unsigned)U);
+    cudaError_t e = cudaSuccess;
+    switch (g.rb) {
+    case 4:
+        e = cudaFuncSetAttribute(gate_up_tc_kernel<4>, cudaFuncAttributeMaxDynamicSharedMemorySize, kTcSmem);
+        if (e == cudaSuccess)
+            gate_up_tc_kernel<4><<<grid, kTcThreads, kTcSmem, stream>>>(L.ptrs.gu, g.H, g.I, g.g_bytes, hn, M, experts,
+                                                                        masks, act, timeout_ns, err);
+        break;
+    case 6:
+        e = cudaFuncSetAttribute(gate_up_tc_kernel<6>, cudaFuncAttributeMaxDynamicSharedMemorySize, kTcSmem);
+        if (e == cudaSuccess)
+            gate_up_tc_kernel<6><<<grid, kTcThreads, kTcSmem, stream>>>(L.ptrs.gu, g.H, g.I, g.g_bytes, hn, M, experts,
+                                                                        masks, act, timeout_ns, err);
+        break;
+    default:
+        e = cudaFuncSetAttribute(gate_up_tc_kernel<8>, cudaFuncAttributeMaxDynamicSharedMemorySize, kTcSmem);
+        if (e == cudaSuccess)
+            gate_up_tc_kernel<8><<<grid, kTcThreads, kTcSmem, stream>>>(L.ptrs.gu, g.H, g.I, g.g_bytes, hn, M, experts,
+                                                                        masks, act, timeout_ns, err);
+        break;
+    }
+    if (e == cudaSuccess) e = cudaGetLastError();
+    if (e != cudaSuccess) {
+        note_cuda_error((int)e);
+        return MOE_ERR_CUDA;
+    }
+    note_launch();
+    return MOE_OK;
+}
+
+}  // namespace moe

@@ -1,7 +1,8 @@
 """A small stack case for profiler captures: `--layers` distinct layer sets
 of the 35B-A3B shape (about 0.66 GB each) in one persistent launch at M rows,
 run `--forwards` times.  Prints one JSON line with the algorithmic bytes of
-one launch (from the experts the rows actually selected).
+one launch (from the experts the rows actually selected).  With --tc, the
+tensor-core grouped gate/up then runs on each layer's routing of the rows.
 
     python -m quantized_moe_decode_layer_gb300.profile_case --M 1 --layers 3
 """
@@ -17,6 +18,27 @@ if ROOT not in sys.path:
     sys.path.insert(0, ROOT)
 
 
+def tc_routing(layers, x, ws):
+    """Per layer along the chain of single-layer calls on x's rows: (distinct
+    experts int32 [U], their row masks int32 [U], the layer's input rows as
+    fp32 [M, H]).  The input rows stand in for the normalised rows of the
+    tensor-core gate/up calls that are timed or profiled with them."""
+    import numpy as np
+    import torch
+    import quantized_moe_decode_layer_gb300 as moe
+    out, h = [], x
+    for lyr in layers:
+        idx, _ = moe.router_topk(lyr, h, ws)
+        sel = idx.cpu().numpy()
+        ex = np.unique(sel)
+        masks = [sum(1 << m for m in range(sel.shape[0]) if e in sel[m]) for e in ex]
+        masks = [m - (1 << 32) if m >= (1 << 31) else m for m in masks]
+        out.append((torch.tensor(ex, dtype=torch.int32, device=x.device),
+                    torch.tensor(masks, dtype=torch.int32, device=x.device), h.float()))
+        h = moe.decode_layer(lyr, h, ws)
+    return out
+
+
 def main() -> None:
     p = argparse.ArgumentParser()
     p.add_argument("--M", type=int, default=1)
@@ -24,6 +46,8 @@ def main() -> None:
     p.add_argument("--forwards", type=int, default=4)
     p.add_argument("--shape", default="a35b")
     p.add_argument("--correlation", type=float, default=0.6)
+    p.add_argument("--tc", action="store_true",
+                   help="then run the tensor-core grouped gate/up (moe_gate_up_tc) on each layer's routing")
     a = p.parse_args()
 
     import torch
@@ -52,9 +76,21 @@ def main() -> None:
         st.forward(x, ws)
     torch.cuda.synchronize()
     assert ws.status() == 0
+    tc_calls = 0
+    if a.tc:
+        cases = tc_routing(layers, x, ws)
+        err = torch.zeros(1, dtype=torch.int32, device="cuda")
+        for _ in range(a.forwards):
+            for (ex, mk, hn), lyr in zip(cases, layers):
+                moe.gate_up_tc(lyr, hn, ex, mk, err=err)
+                tc_calls += 1
+        torch.cuda.synchronize()
+        assert int(err.item()) == 0
     print(json.dumps({"shape": shape.name, "M": a.M, "layers": a.layers, "U": Us,
                       "algorithmic_bytes_per_launch": sum(unique_bytes(shape, u, a.M) for u in Us),
-                      "launches": {"router_topk": a.layers, "decode_layer": a.layers, "stack": a.forwards}}))
+                      "launches": {"router_topk": a.layers, "decode_layer": a.layers, "stack": a.forwards,
+                                   "router_topk_tc_routing": a.layers if a.tc else 0,
+                                   "decode_layer_tc_routing": a.layers if a.tc else 0, "gate_up_tc": tc_calls}}))
 
 
 if __name__ == "__main__":

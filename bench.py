@@ -57,10 +57,15 @@ def unique_bytes(shape, U: int, M: int) -> int:
     return ub(shape, U, M)
 
 
+# The sources of moe_decode_kernel (the kernel the roofline and the traffic
+# figure describe): its translation unit and the headers it includes.
+KERNEL_SOURCES = ("moe_layer.cu", "moe_internal.h", "moe_unpack.cuh")
+
+
 def source_hash() -> str:
     h = hashlib.sha256()
     csrc = os.path.join(ROOT, "quantized_moe_decode_layer_gb300", "csrc")
-    for f in sorted(os.listdir(csrc)):
+    for f in KERNEL_SOURCES:
         h.update(open(os.path.join(csrc, f), "rb").read())
     return h.hexdigest()[:16]
 

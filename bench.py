@@ -214,24 +214,35 @@ def tc_measure(layers, desc, shape, dev, M, warmup):
         for (ex, mk, hn), act, lyr in zip(cases, acts, layers):
             moe.gate_up_tc(lyr, hn, ex, mk, act=act, err=err)
     torch.cuda.synchronize()
+    ys = [torch.zeros((int(ex.numel()), M, shape.H), dtype=torch.float32, device=dev) for ex, _, _ in cases]
+    for (ex, mk, _), act, y, lyr in zip(cases, acts, ys, layers):
+        moe.down_tc(lyr, act, ex, mk, y=y, err=err)
     reps = 5
-    a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    a, b, c = (torch.cuda.Event(enable_timing=True) for _ in range(3))
     a.record()
     for _ in range(reps):
         for (ex, mk, hn), act, lyr in zip(cases, acts, layers):
             moe.gate_up_tc(lyr, hn, ex, mk, act=act, err=err)
     b.record()
+    for _ in range(reps):
+        for (ex, mk, _), act, y, lyr in zip(cases, acts, ys, layers):
+            moe.down_tc(lyr, act, ex, mk, y=y, err=err)
+    c.record()
     torch.cuda.synchronize()
     assert int(err.item()) == 0
     per_call_s = a.elapsed_time(b) * 1e-3 / (reps * len(layers))
+    down_s = b.elapsed_time(c) * 1e-3 / (reps * len(layers))
     U = np.array([int(ex.numel()) for ex, _, _ in cases])
     pairs = np.array([sum(bin(int(m) & 0xFFFFFFFF).count("1") for m in mk.cpu().tolist()) for _, mk, _ in cases])
     unit_bytes = 2 * (shape.H * shape.routed_bits // 8 + shape.H // 64 * 4)
     bytes_call = float(np.mean(U)) * shape.I * unit_bytes
+    down_bytes = float(np.mean(U)) * shape.H * (shape.I * shape.routed_bits // 8 + shape.I // 64 * 4)
     flops_call = float(np.mean(pairs)) * 2 * (2 * shape.I) * shape.H
     return {"M": M, "us_per_call": round(per_call_s * 1e6, 3), "mean_U": round(float(np.mean(U)), 2),
             "rows_per_expert": round(float(np.mean(pairs / U)), 2),
             "gbs": round(bytes_call / per_call_s / 1e9, 1), "tflops": round(flops_call / per_call_s / 1e12, 2),
+            "down_us_per_call": round(down_s * 1e6, 3),
+            "down_gbs": round(down_bytes / down_s / 1e9, 1),
             "calls": reps * len(layers)}
 
 
@@ -337,6 +348,22 @@ def run_ours(args):
             sweep[str(M)] = {"tokens_per_s": round(M / s_step, 1), "us_per_layer": round(s_step * 1e6 / args.layers, 3),
                              "gbs": round(bm / s_step / 1e9, 1), "mean_U": round(float(np.mean(Um)), 2),
                              "launches_per_step": -(-M // min(8, 16384 // shape.H))}
+        # grouped mode (opt-in): above 8 rows, every expert read once per
+        # group of up to 32 rows and its products on the tensor cores
+        moe.set_grouped(9)
+        try:
+            for M in (16, 32):
+                xm = synth.make_rows(shape, 40 + M, M).to(dev)
+                Um = measure_U(layers, xm, wsw)
+                bm = sum(unique_bytes(shape, u, M) for u in Um)
+                sm = max(10, args.steps // 10)
+                tmm, perm, _ = time_stack(st, xm, wsw, sm, args.warmup, stream)
+                s_step = tmm / sm * 1e-3
+                sweep[f"{M}_grouped"] = {"tokens_per_s": round(M / s_step, 1),
+                                         "us_per_layer": round(s_step * 1e6 / args.layers, 3),
+                                         "gbs": round(bm / s_step / 1e9, 1), "mean_U": round(float(np.mean(Um)), 2)}
+        finally:
+            moe.set_grouped(0)
         del wsw
 
     # the grouped gate/up on the tensor cores (moe_gate_up_tc) for the M=32

@@ -236,6 +236,20 @@ int moe_debug_set(int skip_row, long long timeout_ns);
  * each layer goes (per phase, per CTA). */
 int moe_debug_trace(void *trace_dev, size_t bytes);
 
+/* Grouped mode for many rows (opt-in).  With min_rows > 0, moe_decode_layer
+ * and moe_stack_forward run calls of M >= min_rows rows that exceed one
+ * persistent launch (M > 8 at H = 2048) in groups of up to 32 rows per
+ * layer: routing by the persistent kernel in router mode (bit-exact, as
+ * for M = 1), then every selected expert read once for the group's rows, its
+ * products on the tensor cores (moe_gate_up_tc, moe_down_tc arithmetic), and
+ * a combine kernel.  Values are not row-exact and carry the tensor cores'
+ * fp32 accumulation error, which on outputs that are small differences of
+ * large terms can exceed the one-row path's tolerance.  min_rows = 0 (the
+ * default) keeps every M on the FMA path (launches of 8 rows).  The grouped
+ * regions of the workspace are included in moe_workspace_size whenever
+ * max_M > 8.  Process-wide; returns INVALID_ARG for min_rows < 0. */
+int moe_set_grouped(int min_rows);
+
 /* Grouped gate/up of routed experts on the tensor cores (tcgen05 MMAs,
  * fp32 accumulators in tensor memory): the first half of each selected
  * expert's FFN for every token row that chose it, when many rows share an
@@ -250,15 +264,28 @@ int moe_debug_trace(void *trace_dev, size_t bytes);
  * hn_dev: fp32 [M][H], rows already normalised (device).  experts_dev int32 [U]
  * and masks_dev uint32 [U] (device).  act_dev: fp32 [U][M][I] (device); entries
  * of rows outside a mask are not written (mask bits at or above M are
- * ignored).  M <= 32.  Arithmetic: each weight
- * is rounded once to bf16 (w = q * s + b in fp32, round to nearest even);
- * each input is split into two bf16 halves (hi = bf16(x), lo = bf16(x - hi));
- * products accumulate in fp32.  err_dev (device int) is set to 1 if a device
+ * ignored).  M <= 32.  Arithmetic: each weight w = q * s + b (fp32) and each
+ * input is split into two fp16 halves (hi = fp16(v), lo = fp16(v - hi)); the
+ * four half products accumulate in fp32, so every term keeps ~21 significant
+ * bits.  Inputs and weights must stay below 65504 in magnitude.  err_dev (device int) is set to 1 if a device
  * wait runs out (see moe_debug_set); the caller clears it.
  * Errors: INVALID_ARG (NULL pointer, M < 1, U < 0), UNSUPPORTED (M > 32),
  * CUDA (launch failed). */
 int moe_gate_up_tc(const moe_layer *layer, const float *hn_dev, int M, const int32_t *experts_dev,
                    const uint32_t *masks_dev, int U, float *act_dev, int *err_dev, moe_stream_t stream);
+
+/* The down projection of the same experts on the tensor cores, same
+ * arithmetic (flash-moe, "Metal Compute Shaders": dequant mat-vec of the
+ * down matrix; the weighted combine is not part of this call):
+ *
+ *   y_dev[(u * M + m) * H + h] = W_down,e[h] . act_dev[(u * M + m) * I ..]
+ *
+ * for u < U, e = experts_dev[u], each row m of masks_dev[u].  act_dev fp32
+ * [U][M][I] (moe_gate_up_tc's output), y_dev fp32 [U][M][H] (device); rows
+ * outside a mask are not read or written.  Errors: as moe_gate_up_tc, and
+ * UNSUPPORTED when H is not a multiple of 128. */
+int moe_down_tc(const moe_layer *layer, const float *act_dev, int M, const int32_t *experts_dev,
+                const uint32_t *masks_dev, int U, float *y_dev, int *err_dev, moe_stream_t stream);
 
 /* Human-readable name of a status code (static string). */
 const char *moe_status_str(int status);

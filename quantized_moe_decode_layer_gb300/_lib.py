@@ -21,7 +21,7 @@ SYMBOLS = ["moe_pack_size", "moe_pack_weights", "moe_layer_destroy", "moe_export
            "moe_workspace_size", "moe_workspace_init", "moe_router_topk", "moe_decode_layer",
            "moe_stack_create", "moe_stack_forward", "moe_stack_forward_host", "moe_stack_destroy",
            "moe_decode_layer_noalloc",
-           "moe_stream_status", "moe_debug_set", "moe_debug_trace", "moe_gate_up_tc", "moe_status_str",
+           "moe_stream_status", "moe_debug_set", "moe_debug_trace", "moe_set_grouped", "moe_gate_up_tc", "moe_down_tc", "moe_status_str",
            "moe_last_cuda_error",
            "moe_selftest_host", "moe_launch_count"]
 
@@ -80,6 +80,8 @@ def lib():
             "moe_debug_set": (i, [i, C.c_longlong]),
             "moe_debug_trace": (i, [vp, sz]),
             "moe_gate_up_tc": (i, [vp, vp, i, vp, vp, i, vp, vp, vp]),
+            "moe_down_tc": (i, [vp, vp, i, vp, vp, i, vp, vp, vp]),
+            "moe_set_grouped": (i, [i]),
             "moe_status_str": (C.c_char_p, [i]),
             "moe_last_cuda_error": (i, []),
             "moe_selftest_host": (i, []),

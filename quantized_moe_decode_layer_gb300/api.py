@@ -180,6 +180,12 @@ def decode_layer(layer: Layer, x: torch.Tensor, ws: Workspace, out=None, normed:
     return (out, on) if normed else out
 
 
+def set_grouped(min_rows: int) -> None:
+    """Grouped mode (tensor-core expert products) for calls of at least
+    min_rows rows above one launch's rows; 0 turns it off (moe_set_grouped)."""
+    check("moe_set_grouped", lib().moe_set_grouped(int(min_rows)))
+
+
 def gate_up_tc(layer: Layer, hn: torch.Tensor, experts: torch.Tensor, masks: torch.Tensor, act=None,
                err=None, stream=None):
     """Grouped gate/up + SwiGLU on the tensor cores (moe_gate_up_tc).
@@ -196,6 +202,22 @@ def gate_up_tc(layer: Layer, hn: torch.Tensor, experts: torch.Tensor, masks: tor
     check("moe_gate_up_tc", lib().moe_gate_up_tc(layer.handle, _ptr(hn.contiguous()), M, _ptr(experts), _ptr(masks),
                                                  U, _ptr(act), _ptr(err), _stream(stream)))
     return act, err
+
+
+def down_tc(layer: Layer, act: torch.Tensor, experts: torch.Tensor, masks: torch.Tensor, y=None, err=None,
+            stream=None):
+    """Grouped down projection on the tensor cores (moe_down_tc).
+
+    act fp32 [U, M, I], experts int32 [U], masks int32 [U] on the device.
+    Returns (y fp32 [U, M, H], err int32 [1])."""
+    U, M = act.shape[0], act.shape[1]
+    if y is None:
+        y = torch.zeros((U, M, layer.desc.H), dtype=torch.float32, device=act.device)
+    if err is None:
+        err = torch.zeros(1, dtype=torch.int32, device=act.device)
+    check("moe_down_tc", lib().moe_down_tc(layer.handle, _ptr(act.contiguous()), M, _ptr(experts), _ptr(masks), U,
+                                           _ptr(y), _ptr(err), _stream(stream)))
+    return y, err
 
 
 class Stack:

@@ -1,6 +1,6 @@
 """Build of the in-tree CUDA library libmoe.so for sm_103a.
 
-The four translation units compile in parallel with nvcc
+The five translation units compile in parallel with nvcc
 (-gencode arch=compute_103a,code=sm_103a) and link into
 quantized_moe_decode_layer_gb300/libmoe.so next to this file.  Objects go to
 _build/ at the repository root.
@@ -17,7 +17,7 @@ ROOT = os.path.dirname(HERE)
 CSRC = os.path.join(HERE, "csrc")
 OUT = os.path.join(HERE, "libmoe.so")
 OBJDIR = os.path.join(ROOT, "_build")
-SOURCES = ["moe_abi.cu", "moe_pack.cu", "moe_layer.cu", "moe_tc.cu"]
+SOURCES = ["moe_abi.cu", "moe_pack.cu", "moe_layer.cu", "moe_tc.cu", "moe_grouped.cu"]
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 
 

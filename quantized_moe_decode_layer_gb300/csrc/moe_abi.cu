@@ -16,6 +16,7 @@ thread_local long long t_launches = 0;
 int g_skip_row = -1;
 unsigned long long *g_trace = nullptr;
 long long g_timeout_ns = 2000000000LL;
+int g_grouped_min_rows = 0;   // grouped mode for M at or above this (0 = off)
 
 // Contraction widths 64 * 2^j up to 64 * 32 * kMaxGPL: a row splits into
 // whole groups over 1, 2, 4, ..., 32 lanes.
@@ -103,6 +104,28 @@ void make_ws_layout(const Geo &g, int max_M, WsLayout &w)
     w.off_y = put((size_t)R * g.k * g.H * 8);
     w.off_stage_in = put((size_t)max_M * g.H * 2);
     w.off_stage_out = put((size_t)max_M * g.H * 2);
+    w.grp_rows = w.grp_slots = 0;
+    w.off_g_hn = w.off_g_sigma = w.off_g_idx = w.off_g_w = w.off_g_slotof = w.off_g_experts = w.off_g_masks = 0;
+    w.off_g_count = w.off_g_act = w.off_g_act_s = w.off_g_y = w.off_g_ysh = w.off_g_ping = 0;
+    if (max_M > R) {
+        const int GR = max_M < kGroupRows ? max_M : kGroupRows;
+        const int GS = g.E < GR * g.k ? g.E : GR * g.k;
+        w.grp_rows = GR;
+        w.grp_slots = GS;
+        w.off_g_hn = put((size_t)GR * g.H * 4);
+        w.off_g_sigma = put((size_t)GR * 4);
+        w.off_g_idx = put((size_t)GR * g.k * 4);
+        w.off_g_w = put((size_t)GR * g.k * 4);
+        w.off_g_slotof = put((size_t)GR * g.k * 4);
+        w.off_g_experts = put((size_t)(GS + 1) * 4);   // + the shared expert's entry
+        w.off_g_masks = put((size_t)(GS + 1) * 4);
+        w.off_g_count = put(4);
+        w.off_g_act = put((size_t)GS * GR * g.I * 4);
+        w.off_g_act_s = put((size_t)GR * (g.Is ? g.Is : 1) * 4);
+        w.off_g_y = put((size_t)GS * GR * g.H * 4);
+        w.off_g_ysh = put((size_t)GR * g.H * 4);
+        w.off_g_ping = put((size_t)2 * GR * g.H * 2);
+    }
     w.total = align_up(o, 256);
 }
 
@@ -291,6 +314,9 @@ int moe_decode_layer(const moe_layer *layer, const uint16_t *x_dev, int M, uint1
     int R;
     int rc = prepare(layer, M, ws_dev, ws_bytes, kp, R);
     if (rc) return rc;
+    if (M > R && g_grouped_min_rows > 0 && M >= g_grouped_min_rows)   // grouped mode (moe_set_grouped)
+        return grouped_forward(&layer, 1, x_dev, M, out_dev, out_normed_dev, ws_dev, ws_bytes, g_timeout_ns,
+                               reinterpret_cast<cudaStream_t>(stream));
     kp.mode = kModeLayers;
     kp.L = 1;
     kp.layer[0] = layer->ptrs;
@@ -334,6 +360,9 @@ int moe_stack_forward(moe_stack *stack, const uint16_t *x_dev, int M, uint16_t *
     int R;
     int rc = prepare(stack->layers[0], M, ws_dev, ws_bytes, kp, R);
     if (rc) return rc;
+    if (M > R && g_grouped_min_rows > 0 && M >= g_grouped_min_rows)   // grouped mode, as in moe_decode_layer
+        return grouped_forward(stack->layers, stack->L, x_dev, M, out_dev, out_normed_dev, ws_dev, ws_bytes,
+                               g_timeout_ns, reinterpret_cast<cudaStream_t>(stream));
     kp.mode = kModeLayers;
     const int H = kp.g.H;
     for (int c0 = 0; c0 < M; c0 += R) {
@@ -436,6 +465,13 @@ int moe_decode_layer_noalloc(const moe_layer *layer, const uint16_t *x_dev, int 
     return moe_decode_layer(layer, x_dev, M, out_dev, out_normed_dev, ws, (size_t)MOE_NOALLOC_SCRATCH_BYTES, stream);
 }
 
+int moe_set_grouped(int min_rows)
+{
+    if (min_rows < 0) return MOE_ERR_INVALID_ARG;
+    g_grouped_min_rows = min_rows;
+    return MOE_OK;
+}
+
 int moe_debug_set(int skip_row, long long timeout_ns)
 {
     g_skip_row = skip_row;
@@ -457,11 +493,21 @@ int moe_gate_up_tc(const moe_layer *layer, const float *hn_dev, int M, const int
 {
     if (!layer || !hn_dev || !experts_dev || !masks_dev || !act_dev || !err_dev || M < 1 || U < 0)
         return MOE_ERR_INVALID_ARG;
-    if (M > 32 || layer->geo.I % 64 != 0 || layer->geo.H % 64 != 0 || !bits_ok(layer->geo.rb))
-        return MOE_ERR_UNSUPPORTED;
+    if (M > 32 || (2 * layer->geo.I) % 128 != 0 || !bits_ok(layer->geo.rb)) return MOE_ERR_UNSUPPORTED;
     if (U == 0) return MOE_OK;
     return launch_gate_up_tc(*layer, hn_dev, M, experts_dev, masks_dev, U, act_dev, err_dev, g_timeout_ns,
                              reinterpret_cast<cudaStream_t>(stream));
+}
+
+int moe_down_tc(const moe_layer *layer, const float *act_dev, int M, const int32_t *experts_dev,
+                const uint32_t *masks_dev, int U, float *y_dev, int *err_dev, moe_stream_t stream)
+{
+    if (!layer || !act_dev || !experts_dev || !masks_dev || !y_dev || !err_dev || M < 1 || U < 0)
+        return MOE_ERR_INVALID_ARG;
+    if (M > 32 || layer->geo.H % 128 != 0 || !bits_ok(layer->geo.rb)) return MOE_ERR_UNSUPPORTED;
+    if (U == 0) return MOE_OK;
+    return launch_down_tc(*layer, act_dev, M, experts_dev, masks_dev, U, y_dev, err_dev, g_timeout_ns,
+                          reinterpret_cast<cudaStream_t>(stream));
 }
 
 const char *moe_status_str(int status)

@@ -72,7 +72,15 @@ struct WsLayout {
     int max_slots;           // distinct routed experts per launch
     size_t off_logits, off_act, off_act_s, off_ping, off_y, off_stage_in, off_stage_out, total;
     int max_M;               // rows the host-staging area holds
+    // Grouped mode (M above maxr: the tensor-core expert path), sized for
+    // grp_rows = min(max_M, kGroupRows) rows and grp_slots = min(E, grp_rows k)
+    // distinct experts; all zero when max_M <= maxr.
+    int grp_rows, grp_slots;
+    size_t off_g_hn, off_g_sigma, off_g_idx, off_g_w, off_g_slotof, off_g_experts, off_g_masks, off_g_count;
+    size_t off_g_act, off_g_act_s, off_g_y, off_g_ysh, off_g_ping;
 };
+
+constexpr int kGroupRows = 32;      // token rows of one grouped pass (mask width)
 
 struct Ctrl {                // first kCtrlBytes of the workspace
     unsigned count;          // grid-barrier arrivals since the launch began (reset at its end)
@@ -143,14 +151,22 @@ struct moe_stack {
     moe_layer **layers;
 };
 
-// Host-side entry points of the kernels (moe_layer.cu, moe_pack.cu).
+// Host-side entry points of the kernels (moe_layer.cu, moe_pack.cu, moe_tc.cu,
+// moe_grouped.cu).
 namespace moe {
 int launch_decode(const KParams &kp, cudaStream_t stream);
 int launch_pack(const moe_layer &L, const moe_src_layer &src, cudaStream_t stream);
 int launch_export(const moe_layer &L, int tensor_id, int expert, uint8_t *codes, uint16_t *scales,
                   uint16_t *biases, cudaStream_t stream);
+int launch_grouped_tc(int bits, bool swiglu, const uint8_t *W, int rows, int K, int row_bytes, const float *in, int in_u,
+                      int M, const int32_t *experts, const uint32_t *masks, int U, const int *U_dev, float *out,
+                      int *err, long long timeout_ns, cudaStream_t stream);
 int launch_gate_up_tc(const moe_layer &L, const float *hn, int M, const int32_t *experts, const uint32_t *masks, int U,
                       float *act, int *err, long long timeout_ns, cudaStream_t stream);
+int launch_down_tc(const moe_layer &L, const float *act, int M, const int32_t *experts, const uint32_t *masks, int U,
+                   float *y, int *err, long long timeout_ns, cudaStream_t stream);
+int grouped_forward(const moe_layer *const *layers, int L, const uint16_t *x, int M, uint16_t *out, uint16_t *out_n,
+                    void *ws_dev, size_t ws_bytes, long long timeout_ns, cudaStream_t st);
 void note_cuda_error(int err);
 void note_launch();
 }  // namespace moe

@@ -1,26 +1,33 @@
-// Grouped gate/up projection of the routed experts on the 5th-generation
-// tensor cores (tcgen05, accumulators in tensor memory): the grouped-GEMM
-// regime that appears when many token rows share an expert.  Not on the decode
-// path: the decode kernel keeps every step on the FMA pipes, where each token
-// row's result is bitwise the one-row result; this kernel stands beside it
-// as a measured alternative for M up to 32.
+// Grouped products of the routed experts on the 5th-generation tensor cores
+// (tcgen05, accumulators in tensor memory): the grouped-GEMM regime that
+// appears when many token rows share an expert.  Not on the decode path: the
+// decode kernel keeps every step on the FMA pipes, where each token row's
+// result is bitwise the one-row result; these kernels stand beside it as a
+// measured alternative for M up to 32.
 //
-// What it computes (the expert FFN's first half as the pages state it:
-// dequantised weight w = q * s + b per group of 64 along the input axis, then
-// SwiGLU): for each listed expert e and each token row m in its mask,
-//   act[u][m][j] = silu(W_gate,e[j] . hn[m]) * (W_up,e[j] . hn[m]).
+// What they compute (an expert FFN as the pages state it: dequantised weight
+// w = q * s + b per group of 64 along the input axis, SwiGLU between the two
+// projections): for each listed expert e and each token row m in its mask,
+//   gate/up:  act[u][m][j] = silu(W_gate,e[j] . hn[m]) * (W_up,e[j] . hn[m])
+//   down:     y[u][m][h]   = W_down,e[h] . act[u][m]
 //
 // Layout and arithmetic:
-//   - One CTA per (expert, tile of 128 consecutive gate/up rows = 64 units).
-//     The tile is the MMA's M = 128 dimension.
-//   - The token rows are the N dimension: N = 64 = 32 rows of the high bf16
-//     halves of hn, then 32 rows of the low halves (hn - bf16(hn)), so the
-//     activations keep ~16 significant bits.  The weights are rounded once to
-//     bf16 (w = fma(q, s, b) in fp32, then round-to-nearest-even).
+//   - One CTA per (expert, tile of 128 consecutive weight rows; for gate/up
+//     64 units of gate and up rows).  The tile is the MMA's M = 128 dimension.
+//   - The token rows are the N dimension: N = 64 = 32 rows of the high fp16
+//     halves of the inputs, then 32 rows of the low halves (x - fp16(x)), so
+//     the inputs keep ~22 significant bits.  The weights are split the same
+//     way (w = fma(q, s, b) in fp32, then high and low fp16 halves, each an
+//     MMA into the same accumulator), so every product term keeps ~21 bits.
+//     (bf16 halves keep only ~16: with outputs that are small differences of
+//     terms in the thousands, as the synthetic 6-bit layers give, that
+//     missed the output tolerance.)  fp16 bounds the inputs and weights to
+//     |v| < 65504.
 //   - K runs over the input axis in chunks of 64 (one quantisation group):
 //     each of the CTA's 256 threads dequantises half a group of one tile row
 //     into shared memory and writes 16 inputs of the token-row chunk next to
-//     it, and one thread issues 4 MMAs of K = 16 into the same fp32
+//     it, and one thread issues 8 MMAs of K = 16 (high, then low weight
+//     halves) into the same fp32
 //     accumulator in tensor memory.  The codes of chunk c + 2 and the inputs
 //     of chunk c + 1 load while chunk c is converted.
 //     Two chunk buffers alternate; an MMA batch's commit arrives on the
@@ -29,13 +36,13 @@
 //     byte core matrices of 128 contiguous bytes, 128 B apart along K and
 //     1024 B apart along M/N.
 //   - Epilogue: warp w < 4 reads tensor-memory lanes 32w .. 32w + 31 (its rows),
-//     adds the high and low columns, and gate/up neighbours (rows 2j, 2j + 1)
+//     adds the high and low columns; for gate/up, the neighbours 2j, 2j + 1
 //     meet through one shuffle for SwiGLU.
 // Every wait is bounded; a wait that runs out sets *err and the CTA skips
 // the rest of its work, still freeing its tensor memory.
 
 #include <cuda_runtime.h>
-#include <cuda_bf16.h>
+#include <cuda_fp16.h>
 #include <stdint.h>
 
 #include "moe_internal.h"
@@ -48,14 +55,14 @@ constexpr int kTcTok = 32;        // token rows per call at most
 constexpr int kTcN = 2 * kTcTok;  // MMA N: high halves, then low halves
 constexpr int kTcK = 64;          // input elements per chunk (one group)
 constexpr int kTcThreads = 256;
-constexpr int kTileA = kTcRows * kTcK * 2;  // bytes of a weight chunk (16 KB)
+constexpr int kTileA = kTcRows * kTcK * 2;  // bytes of a weight chunk, one fp16 half (16 KB)
 constexpr int kTileB = kTcN * kTcK * 2;     // bytes of a token chunk (8 KB)
-constexpr int kTcSmem = 2 * kTileA + 2 * kTileB + 64;
+constexpr int kTcSmem = 4 * kTileA + 2 * kTileB + 64;   // 2 buffers of (A hi, A lo, B)
 constexpr uint32_t kTmemCols = 64;          // fp32 accumulator columns (= N)
 
 __device__ __forceinline__ uint32_t su32(const void *p) { return (uint32_t)__cvta_generic_to_shared(p); }
 
-// Byte offset of element (r, k) of a [rows x 64] bf16 tile in the no-swizzle
+// Byte offset of element (r, k) of a [rows x 64] fp16 tile in the no-swizzle
 // K-major layout (core matrix = 8 rows x 8 elements, 128 contiguous bytes).
 __device__ __forceinline__ uint32_t canon(int r, int k)
 {
@@ -71,9 +78,9 @@ __device__ __forceinline__ uint64_t smem_desc(uint32_t addr)
            (1ull << 46);
 }
 
-// Instruction descriptor of kind::f16: fp32 accumulator, bf16 A and B, both
+// Instruction descriptor of kind::f16: fp32 accumulator, fp16 A and B, both
 // K-major, N = kTcN, M = kTcRows.
-constexpr uint32_t kIdesc = (1u << 4) | (1u << 7) | (1u << 10) | ((uint32_t)(kTcN >> 3) << 17) |
+constexpr uint32_t kIdesc = (1u << 4) | (0u << 7) | (0u << 10) | ((uint32_t)(kTcN >> 3) << 17) |
                             ((uint32_t)(kTcRows >> 4) << 24);
 
 __device__ __forceinline__ bool mbar_wait_bounded(uint32_t bar, unsigned parity, long long timeout_ns)
@@ -94,10 +101,10 @@ __device__ __forceinline__ bool mbar_wait_bounded(uint32_t bar, unsigned parity,
     }
 }
 
-__device__ __forceinline__ uint32_t pack_bf16(float a, float b)
+__device__ __forceinline__ uint32_t pack_h(float a, float b)
 {
-    const uint32_t lo = __bfloat16_as_ushort(__float2bfloat16_rn(a));
-    const uint32_t hi = __bfloat16_as_ushort(__float2bfloat16_rn(b));
+    const uint32_t lo = __half_as_ushort(__float2half_rn(a));
+    const uint32_t hi = __half_as_ushort(__float2half_rn(b));
     return lo | (hi << 16);
 }
 
@@ -112,15 +119,25 @@ __device__ __forceinline__ uint32_t code_at(const uint32_t (&w)[BITS], int k)
     return v & ((1u << BITS) - 1u);
 }
 
-template <int BITS>
-__global__ void __launch_bounds__(kTcThreads, 1)
-gate_up_tc_kernel(const uint8_t *__restrict__ gu, int H, int I, int g_bytes, const float *__restrict__ hn, int M,
-                  const int32_t *__restrict__ experts, const uint32_t *__restrict__ masks, float *__restrict__ act,
-                  long long timeout_ns, int *err)
+// One grouped product: for slot u (expert experts[u]) and each token row m
+// of masks[u], the expert's `rows` weight rows (K inputs each, row_bytes per
+// packed row, rows e * rows .. of W) against input vector
+// in[(u * in_u + m) * K ..] (in_u = 0: one vector per row shared by every
+// slot; in_u = M: a vector per (slot, row)).  SWIGLU: rows 2j and 2j + 1 are
+// gate and up rows, out[(u * M + m) * rows / 2 + j] = silu(gate) * up; else
+// out[(u * M + m) * rows + r] = the dot product of row r.
+template <int BITS, bool SWIGLU>
+__global__ void __launch_bounds__(kTcThreads, 2)
+grouped_tc_kernel(const uint8_t *__restrict__ W, int rows, int K, int row_bytes, const float *__restrict__ in, int in_u,
+                  int M, const int32_t *__restrict__ experts, const uint32_t *__restrict__ masks,
+                  const int *__restrict__ U_dev, float *__restrict__ out, long long timeout_ns, int *err)
 {
+    // slots at or past a device-side count (when given) have nothing to do
+    if (U_dev && (int)blockIdx.y >= *U_dev) return;
     extern __shared__ __align__(1024) uint8_t sm[];
-    uint8_t *const A0 = sm, *const B0 = sm + 2 * kTileA;   // buffer b at A0 + b kTileA, B0 + b kTileB
-    uint64_t *bar = reinterpret_cast<uint64_t *>(sm + 2 * kTileA + 2 * kTileB);
+    // buffer b: weight halves at A0 + 2 b kTileA (high) and + kTileA (low), tokens at B0 + b kTileB
+    uint8_t *const A0 = sm, *const B0 = sm + 4 * kTileA;
+    uint64_t *bar = reinterpret_cast<uint64_t *>(sm + 4 * kTileA + 2 * kTileB);
     uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(bar + 2);
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
     const int u = blockIdx.y, tile = blockIdx.x;
@@ -148,17 +165,18 @@ gate_up_tc_kernel(const uint8_t *__restrict__ gu, int H, int I, int g_bytes, con
     // & 1) .. + 31 of each group) and its token-chunk share (B row tid / 4,
     // inputs 16 (tid & 3) .. + 15 of each chunk)
     const int arow = tid >> 1, ah = tid & 1;
-    const uint8_t *row = gu + ((size_t)e * 2 * I + (size_t)kTcRows * tile + arow) * (size_t)g_bytes;
+    const uint8_t *row = W + ((size_t)e * rows + (size_t)kTcRows * tile + arow) * (size_t)row_bytes;
     const uint32_t *codes = reinterpret_cast<const uint32_t *>(row) + ah * BITS;   // + c * 2 BITS words
-    const uint32_t *sbp = reinterpret_cast<const uint32_t *>(row + (size_t)H * BITS / 8);
+    const uint32_t *sbp = reinterpret_cast<const uint32_t *>(row + (size_t)K * BITS / 8);
     const int brow = tid >> 2, kq = (tid & 3) * 16;
     const int tn = brow & (kTcTok - 1);
     const bool lo_half = brow >= kTcTok;
     int trow = tn < nr ? (int)__fns(mask, 0, tn + 1) : -1;
     if (trow >= M) trow = -1;   // mask bits at or above M name no row
-    const float4 *hsrc = reinterpret_cast<const float4 *>(hn + (size_t)(trow < 0 ? 0 : trow) * H + kq);
+    const float4 *hsrc =
+        reinterpret_cast<const float4 *>(in + ((size_t)u * in_u + (trow < 0 ? 0 : trow)) * (size_t)K + kq);
 
-    const int G = H / kTcK;
+    const int G = K / kTcK;
     // Loads run ahead of use: the codes and scale of chunk c + 2 and the
     // inputs of chunk c + 1 are in flight while chunk c is converted.
     uint32_t w0[BITS], w1[BITS], w2[BITS], sb0 = 0u, sb1 = 0u, sb2 = 0u;
@@ -185,27 +203,34 @@ gate_up_tc_kernel(const uint8_t *__restrict__ gu, int H, int I, int g_bytes, con
 #pragma unroll 1
     for (int c = 0; c < G; ++c) {
         const int b = c & 1;
-        uint8_t *const Ab = A0 + b * kTileA, *const Bb = B0 + b * kTileB;
+        uint8_t *const Ab = A0 + 2 * b * kTileA, *const Alb = Ab + kTileA, *const Bb = B0 + b * kTileB;
         load_codes(c + 2, w2, sb2);
         load_inputs(c + 1, h1);
         // the MMAs that last read buffer b (chunk c - 2) must be done (a
         // thread whose wait runs out still takes part in this chunk's
         // barrier, after which the whole CTA stops)
         if (c >= 2) ok = mbar_wait_bounded(su32(&bar[b]), (unsigned)((c - 2) >> 1) & 1u, timeout_ns);
-        // weights: 32 bf16 values of row arow, group c
+        // weights: 32 values of row arow, group c, as high and low fp16 halves
         {
             const float sc = __uint_as_float(sb0 << 16), bb = __uint_as_float(sb0 & 0xFFFF0000u);
 #pragma unroll
             for (int k8 = 0; k8 < 4; ++k8) {
-                uint32_t p[4];
+                uint32_t ph[4], pl[4];
 #pragma unroll
-                for (int j = 0; j < 4; ++j)
-                    p[j] = pack_bf16(fmaf((float)code_at<BITS>(w0, 8 * k8 + 2 * j), sc, bb),
-                                     fmaf((float)code_at<BITS>(w0, 8 * k8 + 2 * j + 1), sc, bb));
-                *reinterpret_cast<uint4 *>(Ab + canon(arow, 32 * ah + 8 * k8)) = make_uint4(p[0], p[1], p[2], p[3]);
+                for (int j = 0; j < 4; ++j) {
+                    const float wa = fmaf((float)code_at<BITS>(w0, 8 * k8 + 2 * j), sc, bb);
+                    const float wb = fmaf((float)code_at<BITS>(w0, 8 * k8 + 2 * j + 1), sc, bb);
+                    const float ha = __half2float(__float2half_rn(wa));
+                    const float hb = __half2float(__float2half_rn(wb));
+                    ph[j] = pack_h(ha, hb);
+                    pl[j] = pack_h(wa - ha, wb - hb);
+                }
+                const uint32_t off = canon(arow, 32 * ah + 8 * k8);
+                *reinterpret_cast<uint4 *>(Ab + off) = make_uint4(ph[0], ph[1], ph[2], ph[3]);
+                *reinterpret_cast<uint4 *>(Alb + off) = make_uint4(pl[0], pl[1], pl[2], pl[3]);
             }
         }
-        // token rows: B row brow holds the high (or low) bf16 half of token
+        // token rows: B row brow holds the high (or low) fp16 half of token
         // row trow, inputs 64 c + kq .. + 15
         {
             float v[16];
@@ -215,14 +240,14 @@ gate_up_tc_kernel(const uint8_t *__restrict__ gu, int H, int I, int g_bytes, con
             }
 #pragma unroll
             for (int i = 0; i < 16; ++i) {
-                const float hi = __bfloat162float(__float2bfloat16_rn(v[i]));
+                const float hi = __half2float(__float2half_rn(v[i]));
                 v[i] = lo_half ? v[i] - hi : hi;
             }
 #pragma unroll
             for (int k8 = 0; k8 < 2; ++k8)
                 *reinterpret_cast<uint4 *>(Bb + canon(brow, kq + 8 * k8)) =
-                    make_uint4(pack_bf16(v[8 * k8], v[8 * k8 + 1]), pack_bf16(v[8 * k8 + 2], v[8 * k8 + 3]),
-                               pack_bf16(v[8 * k8 + 4], v[8 * k8 + 5]), pack_bf16(v[8 * k8 + 6], v[8 * k8 + 7]));
+                    make_uint4(pack_h(v[8 * k8], v[8 * k8 + 1]), pack_h(v[8 * k8 + 2], v[8 * k8 + 3]),
+                               pack_h(v[8 * k8 + 4], v[8 * k8 + 5]), pack_h(v[8 * k8 + 6], v[8 * k8 + 7]));
         }
 #pragma unroll
         for (int i = 0; i < BITS; ++i) { w0[i] = w1[i]; w1[i] = w2[i]; }
@@ -237,8 +262,11 @@ gate_up_tc_kernel(const uint8_t *__restrict__ gu, int H, int I, int g_bytes, con
         if (tid == 0) {
             asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory");
 #pragma unroll
-            for (int kk = 0; kk < kTcK / 16; ++kk) {
-                const uint64_t ad = smem_desc(su32(Ab) + kk * 256), bd = smem_desc(su32(Bb) + kk * 256);
+            for (int kk = 0; kk < 2 * (kTcK / 16); ++kk) {
+                // high weight halves, then low, into the same accumulator
+                const uint8_t *At = kk < kTcK / 16 ? Ab : Alb;
+                const int ks = kk % (kTcK / 16);
+                const uint64_t ad = smem_desc(su32(At) + ks * 256), bd = smem_desc(su32(Bb) + ks * 256);
                 const uint32_t accumulate = (c > 0 || kk > 0) ? 1u : 0u;
                 asm volatile("{\n\t.reg .pred p;\n\tsetp.ne.b32 p, %4, 0;\n\t"
                              "tcgen05.mma.cta_group::1.kind::f16 [%0], %1, %2, %3, p;\n\t}" ::"r"(taddr),
@@ -255,7 +283,7 @@ gate_up_tc_kernel(const uint8_t *__restrict__ gu, int H, int I, int g_bytes, con
     ok = __syncthreads_and(ok);
     asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory");
     if (!ok) {
-        if (tid == 0) atomicExch(err, 1);
+        if (tid == 0) atomicOr(err, kStatusTimeout);
     } else if (warp < 4) {
         // warps 0-3: lane 32 warp + lane of tensor memory = tile row tid;
         // columns n (high halves) and 32 + n (low halves) of token row n
@@ -278,16 +306,21 @@ gate_up_tc_kernel(const uint8_t *__restrict__ gu, int H, int I, int g_bytes, con
 #pragma unroll
             for (int n = 0; n < kTcTok; ++n) y[n] = part ? y[n] + __uint_as_float(r[n]) : __uint_as_float(r[n]);
         }
-        // rows 2j (gate) and 2j + 1 (up) of unit j = 64 tile + tid / 2
-        const int j = (kTcRows / 2) * tile + (tid >> 1);
+        const int r = kTcRows * tile + tid;
 #pragma unroll 1
         for (int n = 0; n < nr; ++n) {
             float yn = 0.f;
 #pragma unroll
             for (int t = 0; t < kTcTok; ++t) yn = t == n ? y[t] : yn;
-            const float other = __shfl_xor_sync(0xFFFFFFFFu, yn, 1);
             const int m = (int)__fns(mask, 0, n + 1);
-            if ((tid & 1) == 0 && m < M) act[((size_t)u * M + m) * I + j] = yn / (1.0f + expf(-yn)) * other;
+            if constexpr (SWIGLU) {
+                // rows 2j (gate) and 2j + 1 (up) of unit j = r / 2
+                const float other = __shfl_xor_sync(0xFFFFFFFFu, yn, 1);
+                if ((tid & 1) == 0 && m < M)
+                    out[((size_t)u * M + m) * (rows / 2) + (r >> 1)] = yn / (1.0f + expf(-yn)) * other;
+            } else {
+                if (m < M) out[((size_t)u * M + m) * rows + r] = yn;
+            }
         }
         (void)lane;
     }
@@ -299,31 +332,26 @@ gate_up_tc_kernel(const uint8_t *__restrict__ gu, int H, int I, int g_bytes, con
 
 }  // namespace
 
-int launch_gate_up_tc(const moe_layer &L, const float *hn, int M, const int32_t *experts, const uint32_t *masks, int U,
-                      float *act, int *err, long long timeout_ns, cudaStream_t stream)
+int launch_grouped_tc(int bits, bool swiglu, const uint8_t *W, int rows, int K, int row_bytes, const float *in, int in_u,
+                      int M, const int32_t *experts, const uint32_t *masks, int U, const int *U_dev, float *out,
+                      int *err, long long timeout_ns, cudaStream_t stream)
 {
-    const Geo &g = L.geo;
-    const dim3 grid((unsigned)(2 * g.I / kTcRows), (unsigned)U);
+    const dim3 grid((unsigned)(rows / kTcRows), (unsigned)U);
     cudaError_t e = cudaSuccess;
-    switch (g.rb) {
-    case 4:
-        e = cudaFuncSetAttribute(gate_up_tc_kernel<4>, cudaFuncAttributeMaxDynamicSharedMemorySize, kTcSmem);
+    auto go = [&](auto kernel) {
+        e = cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, kTcSmem);
         if (e == cudaSuccess)
-            gate_up_tc_kernel<4><<<grid, kTcThreads, kTcSmem, stream>>>(L.ptrs.gu, g.H, g.I, g.g_bytes, hn, M, experts,
-                                                                        masks, act, timeout_ns, err);
-        break;
-    case 6:
-        e = cudaFuncSetAttribute(gate_up_tc_kernel<6>, cudaFuncAttributeMaxDynamicSharedMemorySize, kTcSmem);
-        if (e == cudaSuccess)
-            gate_up_tc_kernel<6><<<grid, kTcThreads, kTcSmem, stream>>>(L.ptrs.gu, g.H, g.I, g.g_bytes, hn, M, experts,
-                                                                        masks, act, timeout_ns, err);
-        break;
-    default:
-        e = cudaFuncSetAttribute(gate_up_tc_kernel<8>, cudaFuncAttributeMaxDynamicSharedMemorySize, kTcSmem);
-        if (e == cudaSuccess)
-            gate_up_tc_kernel<8><<<grid, kTcThreads, kTcSmem, stream>>>(L.ptrs.gu, g.H, g.I, g.g_bytes, hn, M, experts,
-                                                                        masks, act, timeout_ns, err);
-        break;
+            kernel<<<grid, kTcThreads, kTcSmem, stream>>>(W, rows, K, row_bytes, in, in_u, M, experts, masks, U_dev,
+                                                          out, timeout_ns, err);
+    };
+    if (swiglu) {
+        if (bits == 4) go(grouped_tc_kernel<4, true>);
+        else if (bits == 6) go(grouped_tc_kernel<6, true>);
+        else go(grouped_tc_kernel<8, true>);
+    } else {
+        if (bits == 4) go(grouped_tc_kernel<4, false>);
+        else if (bits == 6) go(grouped_tc_kernel<6, false>);
+        else go(grouped_tc_kernel<8, false>);
     }
     if (e == cudaSuccess) e = cudaGetLastError();
     if (e != cudaSuccess) {
@@ -332,6 +360,22 @@ int launch_gate_up_tc(const moe_layer &L, const float *hn, int M, const int32_t 
     }
     note_launch();
     return MOE_OK;
+}
+
+int launch_gate_up_tc(const moe_layer &L, const float *hn, int M, const int32_t *experts, const uint32_t *masks, int U,
+                      float *act, int *err, long long timeout_ns, cudaStream_t stream)
+{
+    const Geo &g = L.geo;
+    return launch_grouped_tc(g.rb, true, L.ptrs.gu, 2 * g.I, g.H, g.g_bytes, hn, 0, M, experts, masks, U, nullptr, act,
+                             err, timeout_ns, stream);
+}
+
+int launch_down_tc(const moe_layer &L, const float *act, int M, const int32_t *experts, const uint32_t *masks, int U,
+                   float *y, int *err, long long timeout_ns, cudaStream_t stream)
+{
+    const Geo &g = L.geo;
+    return launch_grouped_tc(g.rb, false, L.ptrs.down, g.H, g.I, g.d_bytes, act, M, M, experts, masks, U, nullptr, y,
+                             err, timeout_ns, stream);
 }
 
 }  // namespace moe

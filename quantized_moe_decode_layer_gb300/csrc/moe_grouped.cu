@@ -6,20 +6,22 @@
 // expert make them a real contraction.
 //
 // Per layer and group of rows:
-//   1. routing by the persistent kernel in router mode (RMSNorm, router rows,
-//      softmax, top-k, renormalised weights: the same FMA-path routing as the
-//      one-row decode, so expert choices are bit-for-bit those of M = 1);
-//   2. rms_sigma_kernel: hn rows (fp32) and the shared-expert gate sigma;
+//   1. rms_sigma_kernel: hn rows (fp32) and the shared-expert gate sigma;
+//   2. router_kernel + topk_kernel: fp32 router logits (FMA pipes), the warp
+//      top-k per row (ties to the lower id) and the renormalised softmax
+//      weights;
 //   3. group_kernel: distinct experts in id order with their row masks;
 //   4. tensor-core gate/up + SwiGLU, then down, for the routed experts
 //      (slot count read on the device) and for the shared expert;
 //   5. combine_kernel: out = bf16(x + sum_i w_i y_i + sigma y_s) in expert-id
 //      order, and the fused next RMSNorm when asked for.
-// The expert products round weights to bf16 (see moe_tc.cu), so values
-// differ from the one-row path within the stated tolerance; routing does not.
+// The expert products carry the tensor cores' accumulation error (see
+// moe_tc.cu), so values are not row-exact; routing decisions are those of the
+// oracle wherever the top-k logit gap exceeds the fp32 rounding of the logits.
 
 #include <cuda_runtime.h>
 #include <cuda_bf16.h>
+#include <math.h>
 #include <stdint.h>
 
 #include "moe_internal.h"
@@ -89,6 +91,86 @@ __global__ void __launch_bounds__(kRowThreads) rms_sigma_kernel(const uint16_t *
         if (threadIdx.x == 0) sigma[m] = 1.0f / (1.0f + expf(-t));
     } else if (threadIdx.x == 0) {
         sigma[m] = 0.f;
+    }
+}
+
+// Router logits of M rows: one CTA per expert row e; the row is dequantised
+// into shared memory (w = q s + b per group of 64, or fp32), then warp w
+// takes token rows w, w + 8, ... with lane l summing inputs l, l + 32, ...
+// in fp32, and a butterfly over the lanes.  logits [M][E].
+__global__ void __launch_bounds__(kRowThreads) router_kernel(const uint8_t *__restrict__ router, int rr_bytes, int qb,
+                                                              int H, int E, const float *__restrict__ hn, int M,
+                                                              float *__restrict__ logits)
+{
+    extern __shared__ float wrow[];
+    const int e = blockIdx.x, lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+    const uint8_t *row = router + (size_t)e * rr_bytes;
+    for (int h = threadIdx.x; h < H; h += blockDim.x) {
+        if (qb == 0) {
+            wrow[h] = reinterpret_cast<const float *>(row)[h];
+        } else {
+            const uint32_t sb = reinterpret_cast<const uint32_t *>(row + (size_t)H * qb / 8)[h / kGroup];
+            wrow[h] = fmaf((float)code_of(row, h, qb), __uint_as_float(sb << 16), __uint_as_float(sb & 0xFFFF0000u));
+        }
+    }
+    __syncthreads();
+    for (int m = warp; m < M; m += kRowThreads / 32) {
+        const float *x = hn + (size_t)m * H;
+        float acc = 0.f;
+        for (int h = lane; h < H; h += 32) acc = fmaf(wrow[h], x[h], acc);
+#pragma unroll
+        for (int o = 16; o >= 1; o >>= 1) acc += __shfl_xor_sync(0xFFFFFFFFu, acc, o);
+        if (lane == 0) logits[(size_t)m * E + e] = acc;
+    }
+}
+
+// Top-k of each row's logits, one warp per row (E <= 512: up to 16 per
+// lane): k rounds of the warp-wide largest remaining logit, exact ties to the
+// lower expert id; then the softmax over the kept k (the full softmax's
+// probabilities divided by their top-k sum).  idx, w [M][k] in selection order.
+__global__ void __launch_bounds__(32) topk_kernel(const float *__restrict__ logits, int E, int k,
+                                                  int32_t *__restrict__ idx, float *__restrict__ w)
+{
+    const int m = blockIdx.x, lane = threadIdx.x;
+    constexpr int NPL = kMaxE / 32;
+    float v[NPL];
+#pragma unroll
+    for (int i = 0; i < NPL; ++i) {
+        const int e = lane + 32 * i;
+        v[i] = e < E ? logits[(size_t)m * E + e] : -INFINITY;
+    }
+    float top0 = 0.f, mine = 0.f;
+    int mine_e = -1;
+    for (int r = 0; r < k; ++r) {
+        // the lane's best (largest value, lowest index on ties)
+        float bv = -INFINITY;
+        int be = 0x7FFFFFFF;
+#pragma unroll
+        for (int i = 0; i < NPL; ++i) {
+            const int e = lane + 32 * i;
+            if (e < E && (v[i] > bv || (v[i] == bv && e < be))) { bv = v[i]; be = e; }
+        }
+#pragma unroll
+        for (int o = 16; o >= 1; o >>= 1) {
+            const float ov = __shfl_xor_sync(0xFFFFFFFFu, bv, o);
+            const int oe = __shfl_xor_sync(0xFFFFFFFFu, be, o);
+            if (ov > bv || (ov == bv && oe < be)) { bv = ov; be = oe; }
+        }
+        if (r == 0) top0 = bv;
+        if ((be & 31) == lane) {
+#pragma unroll
+            for (int i = 0; i < NPL; ++i)
+                if (lane + 32 * i == be) v[i] = -INFINITY;
+        }
+        if (lane == r) { mine = bv; mine_e = be; }
+    }
+    const float ev = lane < k ? expf(mine - top0) : 0.f;
+    float z = ev;
+#pragma unroll
+    for (int o = 16; o >= 1; o >>= 1) z += __shfl_xor_sync(0xFFFFFFFFu, z, o);
+    if (lane < k) {
+        idx[m * k + lane] = mine_e;
+        w[m * k + lane] = ev / z;
     }
 }
 
@@ -213,10 +295,17 @@ int grouped_layer(const moe_layer &L, const uint16_t *x, int mg, uint16_t *out, 
     float *ysh = reinterpret_cast<float *>(ws + w.off_g_ysh);
     int *err = &reinterpret_cast<Ctrl *>(ws)->status;
     const int Umax = g.E < mg * g.k ? g.E : mg * g.k;
-    int rc = moe_router_topk(&L, x, mg, idx, wt, ws, ws_bytes, reinterpret_cast<moe_stream_t>(st));
-    if (rc) return rc;
+    int rc;
     const uint8_t *sgate_row = g.has_shared ? L.ptrs.router + (size_t)g.E * g.rr_bytes : nullptr;
     rms_sigma_kernel<<<mg, kRowThreads, 0, st>>>(x, g.H, L.ptrs.gamma, g.eps, sgate_row, g.qb, hn, sigma);
+    if ((rc = check_launch())) return rc;
+    // routing: fp32 logits (into the routed-output buffer, free until the down
+    // projection), then the warp top-k per row
+    float *logits = y;
+    router_kernel<<<g.E, kRowThreads, (size_t)g.H * 4, st>>>(L.ptrs.router, g.rr_bytes, g.qb, g.H, g.E, hn, mg,
+                                                                 logits);
+    if ((rc = check_launch())) return rc;
+    topk_kernel<<<mg, 32, 0, st>>>(logits, g.E, g.k, idx, wt);
     if ((rc = check_launch())) return rc;
     group_kernel<<<1, 1024, 0, st>>>(idx, mg, g.k, g.E, w.grp_slots, experts, masks, count, slotof);
     if ((rc = check_launch())) return rc;

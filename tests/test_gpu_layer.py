@@ -339,10 +339,9 @@ def _rows_with_distinct_margin(shape, lay, seed, gamma=None, max_attempts=200):
 def test_router_topk_exact_ties(shape, period):
     """Repeated router rows make logits tie exactly; the top k must list tied
     experts by ascending id, as the oracle does.  Period 2 at a35b: experts
-    2j and 2j + 1 share a row (pairs of ties among few candidates).  Period 2
-    at tiny and 4 at a35b: expert e uses row e % period; at a35b every lane
-    of the routing warp then holds equal keys and 64 experts tie at the top
-    (the many-ties path)."""
+    2j and 2j + 1 share a row (pairs of ties).  Period 2 at tiny and 4 at
+    a35b: expert e uses row e % period; at a35b every lane of the routing
+    warp then holds equal keys and 64 experts tie at the top."""
     L = synth.make_layer(shape, 23, device=DEV)
     rw = L["router_w"]
     E = shape.E

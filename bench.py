@@ -331,39 +331,32 @@ def run_ours(args):
               "frac": round(bytes4 / (mean4 * 1e-3) / 1e9 / peaks["hbm_gbs"], 4),
               "mean_U": round(float(np.mean(U4)), 2), "bytes_per_step": bytes4}
 
-    # the stack over M in {1, 2, 4, 8, 32} independent token rows (M above 8
-    # runs as launches of 8 rows; the bytes are still each selected expert
-    # once per step, so re-reads across launches count against GB/s)
+    # the stack over M in {1, 2, 4, 8, 16, 32} independent token rows: up to 8
+    # rows one persistent launch per step; above, grouped mode (each selected
+    # expert read once per group of up to 32 rows, its products on the
+    # tensor cores); 32 rows also on the FMA path alone (4 launches of 8 rows)
     sweep = None
     if not args.no_m4:
         sweep = {}
         wsw = moe.Workspace(desc, 32)
-        for M in (1, 2, 4, 8, 32):
-            xm = synth.make_rows(shape, 40 + M, M).to(dev)
-            Um = measure_U(layers, xm, wsw)
-            bm = sum(unique_bytes(shape, u, M) for u in Um)
-            sm = max(10, args.steps // 10)
-            tmm, perm, _ = time_stack(st, xm, wsw, sm, args.warmup, stream)
-            s_step = tmm / sm * 1e-3
-            sweep[str(M)] = {"tokens_per_s": round(M / s_step, 1), "us_per_layer": round(s_step * 1e6 / args.layers, 3),
-                             "gbs": round(bm / s_step / 1e9, 1), "mean_U": round(float(np.mean(Um)), 2),
-                             "launches_per_step": -(-M // min(8, 16384 // shape.H))}
-        # grouped mode (opt-in): above 8 rows, every expert read once per
-        # group of up to 32 rows and its products on the tensor cores
-        moe.set_grouped(9)
-        try:
-            for M in (16, 32):
+        R = min(8, 16384 // shape.H)
+        for M, key, grouped in ((1, "1", 1), (2, "2", 1), (4, "4", 1), (8, "8", 1), (16, "16", 1),
+                                (16, "16_fma", 0), (32, "32", 1), (32, "32_fma", 0)):
+            moe.set_grouped(grouped)
+            try:
                 xm = synth.make_rows(shape, 40 + M, M).to(dev)
                 Um = measure_U(layers, xm, wsw)
                 bm = sum(unique_bytes(shape, u, M) for u in Um)
                 sm = max(10, args.steps // 10)
                 tmm, perm, _ = time_stack(st, xm, wsw, sm, args.warmup, stream)
-                s_step = tmm / sm * 1e-3
-                sweep[f"{M}_grouped"] = {"tokens_per_s": round(M / s_step, 1),
-                                         "us_per_layer": round(s_step * 1e6 / args.layers, 3),
-                                         "gbs": round(bm / s_step / 1e9, 1), "mean_U": round(float(np.mean(Um)), 2)}
-        finally:
-            moe.set_grouped(0)
+            finally:
+                moe.set_grouped(1)
+            s_step = tmm / sm * 1e-3
+            sweep[key] = {"tokens_per_s": round(M / s_step, 1), "us_per_layer": round(s_step * 1e6 / args.layers, 3),
+                          "gbs": round(bm / s_step / 1e9, 1), "mean_U": round(float(np.mean(Um)), 2),
+                          "mode": "grouped" if (M > R and grouped and M >= grouped) else "persistent",
+                          "launches_per_step": (-(-M // R) if not (M > R and grouped and M >= grouped)
+                                                else args.layers * (7 + 2 * int(shape.has_shared)) * -(-M // 32))}
         del wsw
 
     # the grouped gate/up on the tensor cores (moe_gate_up_tc) for the M=32

@@ -236,18 +236,20 @@ int moe_debug_set(int skip_row, long long timeout_ns);
  * each layer goes (per phase, per CTA). */
 int moe_debug_trace(void *trace_dev, size_t bytes);
 
-/* Grouped mode for many rows (opt-in).  With min_rows > 0, moe_decode_layer
- * and moe_stack_forward run calls of M >= min_rows rows that exceed one
- * persistent launch (M > 8 at H = 2048) in groups of up to 32 rows per
- * layer: routing by the persistent kernel in router mode (bit-exact, as
- * for M = 1), then every selected expert read once for the group's rows, its
- * products on the tensor cores (moe_gate_up_tc, moe_down_tc arithmetic), and
- * a combine kernel.  Values are not row-exact and carry the tensor cores'
- * fp32 accumulation error, which on outputs that are small differences of
- * large terms can exceed the one-row path's tolerance.  min_rows = 0 (the
- * default) keeps every M on the FMA path (launches of 8 rows).  The grouped
- * regions of the workspace are included in moe_workspace_size whenever
- * max_M > 8.  Process-wide; returns INVALID_ARG for min_rows < 0. */
+/* Grouped mode for many rows.  moe_decode_layer and moe_stack_forward run
+ * calls of more rows than one persistent launch holds (M > 8 at H = 2048),
+ * and of at least min_rows rows, in groups of up to 32 rows per layer:
+ * RMSNorm and fp32 router logits, the warp top-k per row (bit-exact routing
+ * wherever the top-k logit gap exceeds fp32 rounding), every selected
+ * expert read once for the group's rows with its products on the tensor
+ * cores (the arithmetic of moe_gate_up_tc and moe_down_tc), then the
+ * combine with the residual and the fused next RMSNorm.  Values are within
+ * the one-row path's tolerance but not bitwise equal to it.  The default,
+ * min_rows = 1, takes grouped mode whenever M exceeds one launch; min_rows = 0
+ * keeps every M on the FMA path (launches of 8 rows, each re-reading the
+ * experts its rows share).  The grouped regions of the workspace are included in
+ * moe_workspace_size whenever max_M exceeds one launch.  Process-wide;
+ * returns INVALID_ARG for min_rows < 0. */
 int moe_set_grouped(int min_rows);
 
 /* Grouped gate/up of routed experts on the tensor cores (tcgen05 MMAs,

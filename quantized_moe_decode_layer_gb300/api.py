@@ -182,7 +182,8 @@ def decode_layer(layer: Layer, x: torch.Tensor, ws: Workspace, out=None, normed:
 
 def set_grouped(min_rows: int) -> None:
     """Grouped mode (tensor-core expert products) for calls of at least
-    min_rows rows above one launch's rows; 0 turns it off (moe_set_grouped)."""
+    min_rows rows above one launch's rows (default 1); 0 turns it off
+    (moe_set_grouped)."""
     check("moe_set_grouped", lib().moe_set_grouped(int(min_rows)))
 
 

@@ -35,6 +35,10 @@
 //   - Shared-memory tiles use the no-swizzle K-major canonical layout: 8x16-
 //     byte core matrices of 128 contiguous bytes, 128 B apart along K and
 //     1024 B apart along M/N.
+//   - Each chunk's MMAs start a fresh sum in one of two accumulator blocks;
+//     warps 0-3 add the previous chunk's block into fp32 registers (round to
+//     nearest) while the next chunk converts, so the long sum over K is not
+//     accumulated inside the tensor core.
 //   - Epilogue: warp w < 4 reads tensor-memory lanes 32w .. 32w + 31 (its rows),
 //     adds the high and low columns; for gate/up, the neighbours 2j, 2j + 1
 //     meet through one shuffle for SwiGLU.
@@ -58,7 +62,7 @@ constexpr int kTcThreads = 256;
 constexpr int kTileA = kTcRows * kTcK * 2;  // bytes of a weight chunk, one fp16 half (16 KB)
 constexpr int kTileB = kTcN * kTcK * 2;     // bytes of a token chunk (8 KB)
 constexpr int kTcSmem = 4 * kTileA + 2 * kTileB + 64;   // 2 buffers of (A hi, A lo, B)
-constexpr uint32_t kTmemCols = 64;          // fp32 accumulator columns (= N)
+constexpr uint32_t kTmemCols = 2 * kTcN;    // two fp32 accumulator blocks of N columns
 
 __device__ __forceinline__ uint32_t su32(const void *p) { return (uint32_t)__cvta_generic_to_shared(p); }
 
@@ -117,6 +121,27 @@ __device__ __forceinline__ uint32_t code_at(const uint32_t (&w)[BITS], int k)
     uint32_t v = w[wi] >> off;
     if (off + BITS > 32) v |= w[wi + 1] << (32 - off);
     return v & ((1u << BITS) - 1u);
+}
+
+// y[n] += column n + column 32 + n of accumulator block `blk` (tensor-memory
+// lanes 32 warp .. + 31, one tile row per thread; warps 0-3 only).
+__device__ __forceinline__ void drain_block(uint32_t taddr, int warp, int blk, float (&y)[kTcTok])
+{
+#pragma unroll
+    for (int q = 0; q < 4; ++q) {
+        uint32_t r[16];
+        const uint32_t a = taddr + ((uint32_t)(32 * warp) << 16) + (uint32_t)(kTcN * blk + 16 * q);
+        asm volatile("tcgen05.ld.sync.aligned.32x32b.x16.b32 {%0, %1, %2, %3, %4, %5, %6, %7, %8, %9, %10, %11, "
+                     "%12, %13, %14, %15}, [%16];"
+                     : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]), "=r"(r[6]), "=r"(r[7]),
+                       "=r"(r[8]), "=r"(r[9]), "=r"(r[10]), "=r"(r[11]), "=r"(r[12]), "=r"(r[13]), "=r"(r[14]),
+                       "=r"(r[15])
+                     : "r"(a)
+                     : "memory");
+        asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory");
+#pragma unroll
+        for (int i = 0; i < 16; ++i) y[(16 * q + i) & (kTcTok - 1)] += __uint_as_float(r[i]);
+    }
 }
 
 // One grouped product: for slot u (expert experts[u]) and each token row m
@@ -200,6 +225,13 @@ grouped_tc_kernel(const uint8_t *__restrict__ W, int rows, int K, int row_bytes,
     load_codes(1, w1, sb1);
     load_inputs(0, h0);
     bool ok = true;
+    // Each chunk's MMAs start a fresh sum in accumulator block c & 1; warps
+    // 0-3 add the finished block of chunk c - 1 into these fp32 registers
+    // while chunk c is converted, so the long sums round to nearest here
+    // instead of accumulating inside the tensor core over all of K.
+    float y[kTcTok];
+#pragma unroll
+    for (int n = 0; n < kTcTok; ++n) y[n] = 0.f;
 #pragma unroll 1
     for (int c = 0; c < G; ++c) {
         const int b = c & 1;
@@ -210,6 +242,12 @@ grouped_tc_kernel(const uint8_t *__restrict__ W, int rows, int K, int row_bytes,
         // thread whose wait runs out still takes part in this chunk's
         // barrier, after which the whole CTA stops)
         if (c >= 2) ok = mbar_wait_bounded(su32(&bar[b]), (unsigned)((c - 2) >> 1) & 1u, timeout_ns);
+        if (c >= 1 && warp < 4) {
+            // chunk c - 1's sums (block b ^ 1), once its commit arrived
+            ok = mbar_wait_bounded(su32(&bar[b ^ 1]), (unsigned)((c - 1) >> 1) & 1u, timeout_ns) && ok;
+            asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory");
+            if (ok) drain_block(taddr, warp, b ^ 1, y);
+        }
         // weights: 32 values of row arow, group c, as high and low fp16 halves
         {
             const float sc = __uint_as_float(sb0 << 16), bb = __uint_as_float(sb0 & 0xFFFF0000u);
@@ -255,8 +293,10 @@ grouped_tc_kernel(const uint8_t *__restrict__ W, int rows, int K, int row_bytes,
         sb1 = sb2;
 #pragma unroll
         for (int i = 0; i < 4; ++i) h0[i] = h1[i];
-        // the generic-proxy stores above become visible to the tensor core
+        // the generic-proxy stores above become visible to the tensor core,
+        // and the tensor-memory reads above end before the next MMAs
         asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+        asm volatile("tcgen05.fence::before_thread_sync;" ::: "memory");
         ok = __syncthreads_and(ok);
         if (!ok) break;
         if (tid == 0) {
@@ -267,9 +307,9 @@ grouped_tc_kernel(const uint8_t *__restrict__ W, int rows, int K, int row_bytes,
                 const uint8_t *At = kk < kTcK / 16 ? Ab : Alb;
                 const int ks = kk % (kTcK / 16);
                 const uint64_t ad = smem_desc(su32(At) + ks * 256), bd = smem_desc(su32(Bb) + ks * 256);
-                const uint32_t accumulate = (c > 0 || kk > 0) ? 1u : 0u;
+                const uint32_t accumulate = kk > 0 ? 1u : 0u;
                 asm volatile("{\n\t.reg .pred p;\n\tsetp.ne.b32 p, %4, 0;\n\t"
-                             "tcgen05.mma.cta_group::1.kind::f16 [%0], %1, %2, %3, p;\n\t}" ::"r"(taddr),
+                             "tcgen05.mma.cta_group::1.kind::f16 [%0], %1, %2, %3, p;\n\t}" ::"r"(taddr + kTcN * b),
                              "l"(ad), "l"(bd), "r"(kIdesc), "r"(accumulate)
                              : "memory");
             }
@@ -278,7 +318,7 @@ grouped_tc_kernel(const uint8_t *__restrict__ W, int rows, int K, int row_bytes,
                          : "memory");
         }
     }
-    // the last commit covers every MMA this CTA issued
+    // the last chunk's sums
     if (ok && G > 0) ok = mbar_wait_bounded(su32(&bar[(G - 1) & 1]), (unsigned)((G - 1) >> 1) & 1u, timeout_ns);
     ok = __syncthreads_and(ok);
     asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory");
@@ -286,26 +326,8 @@ grouped_tc_kernel(const uint8_t *__restrict__ W, int rows, int K, int row_bytes,
         if (tid == 0) atomicOr(err, kStatusTimeout);
     } else if (warp < 4) {
         // warps 0-3: lane 32 warp + lane of tensor memory = tile row tid;
-        // columns n (high halves) and 32 + n (low halves) of token row n
-        float y[kTcTok];
-#pragma unroll
-        for (int part = 0; part < 2; ++part) {
-            uint32_t r[32];
-            const uint32_t a = taddr + ((uint32_t)(32 * warp) << 16) + (uint32_t)(32 * part);
-            asm volatile("tcgen05.ld.sync.aligned.32x32b.x32.b32 {%0, %1, %2, %3, %4, %5, %6, %7, %8, %9, %10, %11, "
-                         "%12, %13, %14, %15, %16, %17, %18, %19, %20, %21, %22, %23, %24, %25, %26, %27, %28, %29, "
-                         "%30, %31}, [%32];"
-                         : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]), "=r"(r[6]),
-                           "=r"(r[7]), "=r"(r[8]), "=r"(r[9]), "=r"(r[10]), "=r"(r[11]), "=r"(r[12]), "=r"(r[13]),
-                           "=r"(r[14]), "=r"(r[15]), "=r"(r[16]), "=r"(r[17]), "=r"(r[18]), "=r"(r[19]),
-                           "=r"(r[20]), "=r"(r[21]), "=r"(r[22]), "=r"(r[23]), "=r"(r[24]), "=r"(r[25]),
-                           "=r"(r[26]), "=r"(r[27]), "=r"(r[28]), "=r"(r[29]), "=r"(r[30]), "=r"(r[31])
-                         : "r"(a)
-                         : "memory");
-            asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory");
-#pragma unroll
-            for (int n = 0; n < kTcTok; ++n) y[n] = part ? y[n] + __uint_as_float(r[n]) : __uint_as_float(r[n]);
-        }
+        // y[n] = token row n's sum of high- and low-half columns over all chunks
+        if (G > 0) drain_block(taddr, warp, (G - 1) & 1, y);
         const int r = kTcRows * tile + tid;
 #pragma unroll 1
         for (int n = 0; n < nr; ++n) {

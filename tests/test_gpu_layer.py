@@ -119,7 +119,8 @@ def test_tiny_layer(M):
 
 
 def test_tiny_many_rows_chunked():
-    """M above the rows of one launch: rows are chunked, results unchanged."""
+    """M above the rows of one launch (19 rows): grouped mode by default;
+    routing bit-exact, outputs within the tolerance."""
     shape = synth.TINY
     L, layer, lay = cached(shape, 7)
     x = rows_with_margin(shape, lay, 555, 19)
@@ -158,48 +159,48 @@ def test_a35b_m8():
     check_layer(shape, L, layer, lay, x)
 
 
-def _grouped_close(got, ref, what):
-    """Grouped mode's bound: the one-row tolerance plus 2^-14 of the row's
-    largest |output| (the tensor cores' fp32 accumulation error grows with
-    the size of the terms, which the row's outputs bound; on outputs that are
-    small differences of terms in the thousands it exceeds the one-row
-    tolerance)."""
-    scale = np.abs(ref).max(axis=1, keepdims=True)
-    err = np.abs(got - ref)
-    tol = 2e-3 + 1e-2 * np.abs(ref) + 2.0 ** -14 * scale
-    bad = err > tol
-    assert not bad.any(), f"{what}: {bad.sum()} of {bad.size} outside the grouped-mode bound, max err {err.max()}"
+DEFAULT_GROUPED_MIN_ROWS = 1
 
 
 @pytest.fixture
-def grouped():
-    moe.set_grouped(9)
+def fma_only():
+    moe.set_grouped(0)
     try:
         yield
     finally:
-        moe.set_grouped(0)
+        moe.set_grouped(DEFAULT_GROUPED_MIN_ROWS)
 
 
-def test_a35b_m32_grouped(grouped):
-    """32 rows in grouped mode (tensor-core expert products, every expert read
-    once for the 32 rows): routing bit-exact, outputs within the grouped bound."""
+@pytest.fixture
+def grouped_always():
+    moe.set_grouped(1)
+    try:
+        yield
+    finally:
+        moe.set_grouped(DEFAULT_GROUPED_MIN_ROWS)
+
+
+def test_a35b_m32_grouped():
+    """32 rows: grouped mode (tensor-core expert products, every expert read
+    once for the 32 rows): routing bit-exact, outputs within the tolerance."""
     shape = synth.A35B
     L, layer, lay = cached(shape, 11)
     x = rows_with_margin(shape, lay, 4, 32, gamma=L["gamma"])
-    ws = moe.Workspace(layer.desc, 32)
-    out, on = moe.decode_layer(layer, x.to(DEV), ws, normed=True)
-    assert ws.status() == 0
-    ref = lay.forward(bits_np(x), normed=True)
-    _grouped_close(bf16_tensor_to_f64(out), ref["o"], "a35b grouped out")
-    _grouped_close(bf16_tensor_to_f64(on), ref["on"], "a35b grouped out_normed")
-    idx, w = moe.router_topk(layer, x.to(DEV), ws)
-    assert np.array_equal(idx.cpu().numpy(), ref["idx"])
+    check_layer(shape, L, layer, lay, x)
 
 
-def test_grouped_stack_equals_chained_layers(grouped):
+def test_a35b_m32_fma_chunks(fma_only):
+    """32 rows with grouped mode off: four 8-row launches of the FMA path."""
+    shape = synth.A35B
+    L, layer, lay = cached(shape, 11)
+    x = rows_with_margin(shape, lay, 5, 32, gamma=L["gamma"])
+    check_layer(shape, L, layer, lay, x)
+
+
+def test_grouped_stack_equals_chained_layers(grouped_always):
     """Grouped mode through a 3-layer stack (M = 12, tiny shape) gives the
     bits of chained single-layer grouped calls, and each layer is within the
-    grouped bound of the oracle on the GPU's own input (teacher-forced)."""
+    tolerance of the oracle on the GPU's own input (teacher-forced)."""
     shape = synth.TINY
     built = [build(shape, 300 + i) for i in range(3)]
     layers = [b[1] for b in built]
@@ -222,7 +223,7 @@ def test_grouped_stack_equals_chained_layers(grouped):
         ref = lay.forward(bits_np(h), normed=True)
         nxt = moe.decode_layer(lyr, h, ws)
         if ref["margin"].min() >= 1e-3:
-            _grouped_close(bf16_tensor_to_f64(nxt), ref["o"], f"grouped stack layer {i}")
+            assert_close(bf16_tensor_to_f64(nxt), ref["o"], f"grouped stack layer {i}")
         h = nxt
 
 

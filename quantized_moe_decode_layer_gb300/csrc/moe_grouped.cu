@@ -12,7 +12,8 @@
 //      weights;
 //   3. group_kernel: distinct experts in id order with their row masks;
 //   4. tensor-core gate/up + SwiGLU, then down, for the routed experts
-//      (slot count read on the device) and for the shared expert;
+//      (slot count read on the device) and the shared expert, one launch per
+//      projection;
 //   5. combine_kernel: out = bf16(x + sum_i w_i y_i + sigma y_s) in expert-id
 //      order, and the fused next RMSNorm when asked for.
 // The expert products carry the tensor cores' accumulation error (see
@@ -309,23 +310,27 @@ int grouped_layer(const moe_layer &L, const uint16_t *x, int mg, uint16_t *out, 
     if ((rc = check_launch())) return rc;
     group_kernel<<<1, 1024, 0, st>>>(idx, mg, g.k, g.E, w.grp_slots, experts, masks, count, slotof);
     if ((rc = check_launch())) return rc;
-    if ((rc = launch_grouped_tc(g.rb, true, L.ptrs.gu, 2 * g.I, g.H, g.g_bytes, hn, 0, mg, experts, masks, Umax, count,
-                                act, err, timeout_ns, st)))
+    // routed experts (set a, slot count on the device) and the shared expert
+    // (set b: its own weights, the one slot at entry grp_slots) in one launch
+    // per projection, so the shared expert's few tiles run beside the routed
+    // ones instead of after them
+    const int32_t *she = experts + w.grp_slots;
+    const uint32_t *shm = masks + w.grp_slots;
+    const TcSetHost gu_r{L.ptrs.gu, 2 * g.I, g.H, g.g_bytes, hn, 0, experts, masks, count, act};
+    const TcSetHost gu_s{L.ptrs.sgu, 2 * g.Is, g.H, g.sg_bytes, hn, 0, she, shm, nullptr, act_s};
+    const TcSetHost dn_r{L.ptrs.down, g.H, g.I, g.d_bytes, act, mg, experts, masks, count, y};
+    const TcSetHost dn_s{L.ptrs.sdown, g.H, g.Is, g.sd_bytes, act_s, mg, she, shm, nullptr, ysh};
+    const bool fused = g.has_shared && (g.sb == g.rb || g.sb == 8);
+    if ((rc = launch_grouped_tc2(true, g.rb, gu_r, Umax, g.sb, fused ? &gu_s : nullptr, 1, mg, err, timeout_ns, st)))
         return rc;
-    if ((rc = launch_grouped_tc(g.rb, false, L.ptrs.down, g.H, g.I, g.d_bytes, act, mg, mg, experts, masks, Umax,
-                                count, y, err, timeout_ns, st)))
+    if (g.has_shared && !fused &&
+        (rc = launch_grouped_tc2(true, g.sb, gu_s, 1, g.sb, nullptr, 0, mg, err, timeout_ns, st)))
         return rc;
-    if (g.has_shared) {
-        // the shared expert: its own weights, the one slot at entry grp_slots
-        const int32_t *she = experts + w.grp_slots;
-        const uint32_t *shm = masks + w.grp_slots;
-        if ((rc = launch_grouped_tc(g.sb, true, L.ptrs.sgu, 2 * g.Is, g.H, g.sg_bytes, hn, 0, mg, she, shm, 1, nullptr,
-                                    act_s, err, timeout_ns, st)))
-            return rc;
-        if ((rc = launch_grouped_tc(g.sb, false, L.ptrs.sdown, g.H, g.Is, g.sd_bytes, act_s, mg, mg, she, shm, 1,
-                                    nullptr, ysh, err, timeout_ns, st)))
-            return rc;
-    }
+    if ((rc = launch_grouped_tc2(false, g.rb, dn_r, Umax, g.sb, fused ? &dn_s : nullptr, 1, mg, err, timeout_ns, st)))
+        return rc;
+    if (g.has_shared && !fused &&
+        (rc = launch_grouped_tc2(false, g.sb, dn_s, 1, g.sb, nullptr, 0, mg, err, timeout_ns, st)))
+        return rc;
     combine_kernel<<<mg, kRowThreads, 0, st>>>(x, g.H, mg, g.k, wt, slotof, y, g.has_shared ? ysh : nullptr, sigma,
                                                L.ptrs.gamma_next, g.eps, out, out_n);
     return check_launch();

@@ -158,6 +158,22 @@ int launch_decode(const KParams &kp, cudaStream_t stream);
 int launch_pack(const moe_layer &L, const moe_src_layer &src, cudaStream_t stream);
 int launch_export(const moe_layer &L, int tensor_id, int expert, uint8_t *codes, uint16_t *scales,
                   uint16_t *biases, cudaStream_t stream);
+// One set of grouped tensor-core products (moe_tc.cu): slot u's expert
+// experts[u], rows of masks[u]; W rows e * rows .., K inputs, row_bytes per
+// packed row; inputs in[(u * in_u + m) * K ..]; U_dev a device-side slot
+// count or NULL.
+struct TcSetHost {
+    const uint8_t *W;
+    int rows, K, row_bytes;
+    const float *in;
+    int in_u;
+    const int32_t *experts;
+    const uint32_t *masks;
+    const int *U_dev;
+    float *out;
+};
+int launch_grouped_tc2(bool swiglu, int bits_a, const TcSetHost &a, int nA, int bits_b, const TcSetHost *b, int nB,
+                       int M, int *err, long long timeout_ns, cudaStream_t stream);
 int launch_grouped_tc(int bits, bool swiglu, const uint8_t *W, int rows, int K, int row_bytes, const float *in, int in_u,
                       int M, const int32_t *experts, const uint32_t *masks, int U, const int *U_dev, float *out,
                       int *err, long long timeout_ns, cudaStream_t stream);

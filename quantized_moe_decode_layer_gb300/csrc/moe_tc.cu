@@ -151,21 +151,36 @@ __device__ __forceinline__ void drain_block(uint32_t taddr, int warp, int blk, f
 // slot; in_u = M: a vector per (slot, row)).  SWIGLU: rows 2j and 2j + 1 are
 // gate and up rows, out[(u * M + m) * rows / 2 + j] = silu(gate) * up; else
 // out[(u * M + m) * rows + r] = the dot product of row r.
+struct TcSet {
+    const uint8_t *W;
+    int rows, K, row_bytes;
+    const float *in;
+    int in_u;
+    const int32_t *experts;
+    const uint32_t *masks;
+    const int *U_dev;   // device-side slot count, or NULL
+    float *out;
+};
+
 template <int BITS, bool SWIGLU>
-__global__ void __launch_bounds__(kTcThreads, 2)
-grouped_tc_kernel(const uint8_t *__restrict__ W, int rows, int K, int row_bytes, const float *__restrict__ in, int in_u,
-                  int M, const int32_t *__restrict__ experts, const uint32_t *__restrict__ masks,
-                  const int *__restrict__ U_dev, float *__restrict__ out, long long timeout_ns, int *err)
+__device__ __forceinline__ void grouped_tc_body(const TcSet &set, int u, int tile, int M, long long timeout_ns, int *err)
 {
-    // slots at or past a device-side count (when given) have nothing to do
-    if (U_dev && (int)blockIdx.y >= *U_dev) return;
+    const uint8_t *__restrict__ W = set.W;
+    const int rows = set.rows, K = set.K, row_bytes = set.row_bytes, in_u = set.in_u;
+    const float *__restrict__ in = set.in;
+    const int32_t *__restrict__ experts = set.experts;
+    const uint32_t *__restrict__ masks = set.masks;
+    float *__restrict__ out = set.out;
+    // tiles past this set's rows, and slots at or past a device-side count,
+    // have nothing to do
+    if (tile * kTcRows >= rows) return;
+    if (set.U_dev && u >= *set.U_dev) return;
     extern __shared__ __align__(1024) uint8_t sm[];
     // buffer b: weight halves at A0 + 2 b kTileA (high) and + kTileA (low), tokens at B0 + b kTileB
     uint8_t *const A0 = sm, *const B0 = sm + 4 * kTileA;
     uint64_t *bar = reinterpret_cast<uint64_t *>(sm + 4 * kTileA + 2 * kTileB);
     uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(bar + 2);
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
-    const int u = blockIdx.y, tile = blockIdx.x;
     const int e = experts[u];
     const uint32_t mask = masks[u];
     const int nr = __popc(mask);
@@ -352,28 +367,59 @@ grouped_tc_kernel(const uint8_t *__restrict__ W, int rows, int K, int row_bytes,
         asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;" ::"r"(taddr), "r"(kTmemCols) : "memory");
 }
 
+// Two product sets in one grid (a second set lets the shared expert, with
+// its own weights and code width, run beside the routed experts instead of
+// after them): blockIdx.y < nA are slots of set a, the rest of set b;
+// blockIdx.x is the 128-row tile.
+template <int BITS_A, int BITS_B, bool SWIGLU>
+__global__ void __launch_bounds__(kTcThreads, 2)
+grouped_tc_kernel(const TcSet a, const TcSet b, int nA, int M, long long timeout_ns, int *err)
+{
+    const int y = blockIdx.y;
+    if (y < nA) grouped_tc_body<BITS_A, SWIGLU>(a, y, blockIdx.x, M, timeout_ns, err);
+    else grouped_tc_body<BITS_B, SWIGLU>(b, y - nA, blockIdx.x, M, timeout_ns, err);
+}
+
 }  // namespace
 
-int launch_grouped_tc(int bits, bool swiglu, const uint8_t *W, int rows, int K, int row_bytes, const float *in, int in_u,
-                      int M, const int32_t *experts, const uint32_t *masks, int U, const int *U_dev, float *out,
-                      int *err, long long timeout_ns, cudaStream_t stream)
+int launch_grouped_tc2(bool swiglu, int bits_a, const TcSetHost &ha, int nA, int bits_b, const TcSetHost *hb, int nB,
+                       int M, int *err, long long timeout_ns, cudaStream_t stream)
 {
-    const dim3 grid((unsigned)(rows / kTcRows), (unsigned)U);
-    cudaError_t e = cudaSuccess;
+    auto to_set = [](const TcSetHost &h) {
+        return TcSet{h.W, h.rows, h.K, h.row_bytes, h.in, h.in_u, h.experts, h.masks, h.U_dev, h.out};
+    };
+    const TcSet a = to_set(ha);
+    const TcSet b = hb ? to_set(*hb) : a;
+    if (!hb) nB = 0;
+    int tiles = ha.rows / kTcRows;
+    if (hb && hb->rows / kTcRows > tiles) tiles = hb->rows / kTcRows;
+    const dim3 grid((unsigned)tiles, (unsigned)(nA + nB));
+    if (!hb) bits_b = bits_a;
+    cudaError_t e = cudaErrorInvalidValue;
     auto go = [&](auto kernel) {
         e = cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, kTcSmem);
-        if (e == cudaSuccess)
-            kernel<<<grid, kTcThreads, kTcSmem, stream>>>(W, rows, K, row_bytes, in, in_u, M, experts, masks, U_dev,
-                                                          out, timeout_ns, err);
+        if (e == cudaSuccess) kernel<<<grid, kTcThreads, kTcSmem, stream>>>(a, b, nA, M, timeout_ns, err);
     };
+    // (a, b) code widths: both the same, or a routed width with 8-bit shared weights
+    const int code = bits_a * 10 + bits_b;
     if (swiglu) {
-        if (bits == 4) go(grouped_tc_kernel<4, true>);
-        else if (bits == 6) go(grouped_tc_kernel<6, true>);
-        else go(grouped_tc_kernel<8, true>);
+        switch (code) {
+        case 44: go(grouped_tc_kernel<4, 4, true>); break;
+        case 66: go(grouped_tc_kernel<6, 6, true>); break;
+        case 88: go(grouped_tc_kernel<8, 8, true>); break;
+        case 48: go(grouped_tc_kernel<4, 8, true>); break;
+        case 68: go(grouped_tc_kernel<6, 8, true>); break;
+        default: return MOE_ERR_UNSUPPORTED;
+        }
     } else {
-        if (bits == 4) go(grouped_tc_kernel<4, false>);
-        else if (bits == 6) go(grouped_tc_kernel<6, false>);
-        else go(grouped_tc_kernel<8, false>);
+        switch (code) {
+        case 44: go(grouped_tc_kernel<4, 4, false>); break;
+        case 66: go(grouped_tc_kernel<6, 6, false>); break;
+        case 88: go(grouped_tc_kernel<8, 8, false>); break;
+        case 48: go(grouped_tc_kernel<4, 8, false>); break;
+        case 68: go(grouped_tc_kernel<6, 8, false>); break;
+        default: return MOE_ERR_UNSUPPORTED;
+        }
     }
     if (e == cudaSuccess) e = cudaGetLastError();
     if (e != cudaSuccess) {
@@ -382,6 +428,14 @@ int launch_grouped_tc(int bits, bool swiglu, const uint8_t *W, int rows, int K, 
     }
     note_launch();
     return MOE_OK;
+}
+
+int launch_grouped_tc(int bits, bool swiglu, const uint8_t *W, int rows, int K, int row_bytes, const float *in, int in_u,
+                      int M, const int32_t *experts, const uint32_t *masks, int U, const int *U_dev, float *out,
+                      int *err, long long timeout_ns, cudaStream_t stream)
+{
+    const TcSetHost h{W, rows, K, row_bytes, in, in_u, experts, masks, U_dev, out};
+    return launch_grouped_tc2(swiglu, bits, h, U, bits, nullptr, 0, M, err, timeout_ns, stream);
 }
 
 int launch_gate_up_tc(const moe_layer &L, const float *hn, int M, const int32_t *experts, const uint32_t *masks, int U,

@@ -221,9 +221,10 @@ __global__ void __launch_bounds__(1024) group_kernel(const int32_t *__restrict__
     }
 }
 
-// One CTA per row: out = bf16(x + sum_i w_i y[slot_i] + sigma y_s), the
-// choices summed in expert-id order; then, if asked, out_n =
-// bf16(RMSNorm(bf16 out) gamma_next).  x and out may alias.
+// CTA (m, part): out = bf16(x + sum_i w_i y[slot_i] + sigma y_s) for row m,
+// outputs part * H / gridDim.y .. (the choices summed in expert-id order);
+// then, with one part per row, if asked, out_n = bf16(RMSNorm(bf16 out)
+// gamma_next).  x and out may alias.
 __global__ void __launch_bounds__(kRowThreads) combine_kernel(
     const uint16_t *x, int H, int M, int k, const float *__restrict__ w, const int32_t *__restrict__ slotof,
     const float *__restrict__ y, const float *__restrict__ ysh, const float *__restrict__ sigma,
@@ -247,7 +248,9 @@ __global__ void __launch_bounds__(kRowThreads) combine_kernel(
     __syncthreads();
     const float sg = sigma[m];
     float ss = 0.f;
-    for (int h = threadIdx.x; h < H; h += blockDim.x) {
+    // a grid of several CTAs per row (no out_n) splits the row's H outputs
+    const int hs = H / (int)gridDim.y, h0 = hs * (int)blockIdx.y, h1 = h0 + hs;
+    for (int h = h0 + threadIdx.x; h < h1; h += blockDim.x) {
         float acc = 0.f;
         for (int i = 0; i < k; ++i) acc = fmaf(ow[i], y[((size_t)os[i] * M + m) * H + h], acc);
         if (ysh) acc = fmaf(sg, ysh[(size_t)m * H + h], acc);
@@ -331,8 +334,10 @@ int grouped_layer(const moe_layer &L, const uint16_t *x, int mg, uint16_t *out, 
     if (g.has_shared && !fused &&
         (rc = launch_grouped_tc2(false, g.sb, dn_s, 1, g.sb, nullptr, 0, mg, err, timeout_ns, st)))
         return rc;
-    combine_kernel<<<mg, kRowThreads, 0, st>>>(x, g.H, mg, g.k, wt, slotof, y, g.has_shared ? ysh : nullptr, sigma,
-                                               L.ptrs.gamma_next, g.eps, out, out_n);
+    // without the fused RMSNorm, 8 CTAs per row (each a whole number of 256-wide parts)
+    const int parts = (!out_n && g.H % (8 * kRowThreads) == 0) ? 8 : 1;
+    combine_kernel<<<dim3((unsigned)mg, (unsigned)parts), kRowThreads, 0, st>>>(
+        x, g.H, mg, g.k, wt, slotof, y, g.has_shared ? ysh : nullptr, sigma, L.ptrs.gamma_next, g.eps, out, out_n);
     return check_launch();
 }
 

@@ -28,17 +28,18 @@
 //     into shared memory and writes 16 inputs of the token-row chunk next to
 //     it, and one thread issues 8 MMAs of K = 16 (high, then low weight
 //     halves) into the same fp32
-//     accumulator in tensor memory.  The codes of chunk c + 2 and the inputs
-//     of chunk c + 1 load while chunk c is converted.
+//     accumulator in tensor memory.  Two register sets of codes, scales and
+//     inputs alternate between even and odd chunks; chunk c + 2's loads go
+//     out as soon as chunk c has been converted.
 //     Two chunk buffers alternate; an MMA batch's commit arrives on the
 //     buffer's mbarrier, which the next writers of that buffer wait on.
 //   - Shared-memory tiles use the no-swizzle K-major canonical layout: 8x16-
 //     byte core matrices of 128 contiguous bytes, 128 B apart along K and
 //     1024 B apart along M/N.
-//   - Each chunk's MMAs start a fresh sum in one of two accumulator blocks;
-//     warps 0-3 add the previous chunk's block into fp32 registers (round to
-//     nearest) while the next chunk converts, so the long sum over K is not
-//     accumulated inside the tensor core.
+//   - Each chunk's MMAs start a fresh sum in one of four accumulator blocks;
+//     two chunks later every warp adds the block into fp32 registers (round
+//     to nearest; warps 0-3 the high-half columns, warps 4-7 the low), so the
+//     long sum over K is not accumulated inside the tensor core.
 //   - Epilogue: warp w < 4 reads tensor-memory lanes 32w .. 32w + 31 (its rows),
 //     adds the high and low columns; for gate/up, the neighbours 2j, 2j + 1
 //     meet through one shuffle for SwiGLU.
@@ -62,7 +63,7 @@ constexpr int kTcThreads = 256;
 constexpr int kTileA = kTcRows * kTcK * 2;  // bytes of a weight chunk, one fp16 half (16 KB)
 constexpr int kTileB = kTcN * kTcK * 2;     // bytes of a token chunk (8 KB)
 constexpr int kTcSmem = 4 * kTileA + 2 * kTileB + 64;   // 2 buffers of (A hi, A lo, B)
-constexpr uint32_t kTmemCols = 2 * kTcN;    // two fp32 accumulator blocks of N columns
+constexpr uint32_t kTmemCols = 4 * kTcN;    // four fp32 accumulator blocks of N columns
 
 __device__ __forceinline__ uint32_t su32(const void *p) { return (uint32_t)__cvta_generic_to_shared(p); }
 
@@ -123,14 +124,16 @@ __device__ __forceinline__ uint32_t code_at(const uint32_t (&w)[BITS], int k)
     return v & ((1u << BITS) - 1u);
 }
 
-// y[n] += column n + column 32 + n of accumulator block `blk` (tensor-memory
-// lanes 32 warp .. + 31, one tile row per thread; warps 0-3 only).
+// y[n] += column n (warps 0-3: the high halves) or column 32 + n (warps 4-7:
+// the low halves) of accumulator block `blk`; warp w reads tensor-memory
+// lanes 32 (w % 4) .. + 31, one tile row per thread.
 __device__ __forceinline__ void drain_block(uint32_t taddr, int warp, int blk, float (&y)[kTcTok])
 {
 #pragma unroll
-    for (int q = 0; q < 4; ++q) {
+    for (int q = 0; q < 2; ++q) {
         uint32_t r[16];
-        const uint32_t a = taddr + ((uint32_t)(32 * warp) << 16) + (uint32_t)(kTcN * blk + 16 * q);
+        const uint32_t a = taddr + ((uint32_t)(32 * (warp & 3)) << 16) +
+                           (uint32_t)(kTcN * blk + kTcTok * (warp >> 2) + 16 * q);
         asm volatile("tcgen05.ld.sync.aligned.32x32b.x16.b32 {%0, %1, %2, %3, %4, %5, %6, %7, %8, %9, %10, %11, "
                      "%12, %13, %14, %15}, [%16];"
                      : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]), "=r"(r[6]), "=r"(r[7]),
@@ -140,7 +143,7 @@ __device__ __forceinline__ void drain_block(uint32_t taddr, int warp, int blk, f
                      : "memory");
         asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory");
 #pragma unroll
-        for (int i = 0; i < 16; ++i) y[(16 * q + i) & (kTcTok - 1)] += __uint_as_float(r[i]);
+        for (int i = 0; i < 16; ++i) y[16 * q + i] += __uint_as_float(r[i]);
     }
 }
 
@@ -217,51 +220,48 @@ __device__ __forceinline__ void grouped_tc_body(const TcSet &set, int u, int til
         reinterpret_cast<const float4 *>(in + ((size_t)u * in_u + (trow < 0 ? 0 : trow)) * (size_t)K + kq);
 
     const int G = K / kTcK;
-    // Loads run ahead of use: the codes and scale of chunk c + 2 and the
-    // inputs of chunk c + 1 are in flight while chunk c is converted.
-    uint32_t w0[BITS], w1[BITS], w2[BITS], sb0 = 0u, sb1 = 0u, sb2 = 0u;
-    float4 h0[4], h1[4];
-    auto load_codes = [&](int c, uint32_t (&w)[BITS], uint32_t &sb) {
+    // Two register sets of loaded codes, scale and inputs alternate between
+    // the even and the odd chunks; a set is refilled with chunk c + 2 as soon
+    // as chunk c has been converted from it, and is never copied (a copy
+    // would wait for the load), so each load has two chunks to land.
+    uint32_t wA[BITS], wB[BITS], sbA = 0u, sbB = 0u;
+    float4 hA[4], hB[4];
+    auto load_set = [&](int c, uint32_t (&w)[BITS], uint32_t &sb, float4 (&h)[4]) {
         if (c < G) {
 #pragma unroll
             for (int i = 0; i < BITS; ++i) w[i] = __ldg(codes + c * 2 * BITS + i);
             sb = __ldg(sbp + c);
+#pragma unroll
+            for (int i = 0; i < 4; ++i) h[i] = make_float4(0.f, 0.f, 0.f, 0.f);
+            if (trow >= 0) {
+#pragma unroll
+                for (int i = 0; i < 4; ++i) h[i] = __ldg(hsrc + c * (kTcK / 4) + i);
+            }
         }
     };
-    auto load_inputs = [&](int c, float4 (&h)[4]) {
-#pragma unroll
-        for (int i = 0; i < 4; ++i) h[i] = make_float4(0.f, 0.f, 0.f, 0.f);
-        if (c < G && trow >= 0) {
-#pragma unroll
-            for (int i = 0; i < 4; ++i) h[i] = __ldg(hsrc + c * (kTcK / 4) + i);
-        }
-    };
-    load_codes(0, w0, sb0);
-    load_codes(1, w1, sb1);
-    load_inputs(0, h0);
+    load_set(0, wA, sbA, hA);
+    load_set(1, wB, sbB, hB);
     bool ok = true;
-    // Each chunk's MMAs start a fresh sum in accumulator block c & 1; warps
-    // 0-3 add the finished block of chunk c - 1 into these fp32 registers
-    // while chunk c is converted, so the long sums round to nearest here
-    // instead of accumulating inside the tensor core over all of K.
+    // Each chunk's MMAs start a fresh sum in accumulator block c & 3; when
+    // chunk c starts, every warp adds chunk c - 2's finished block (warps 0-3
+    // its high-half columns, warps 4-7 its low-half columns) into these fp32
+    // registers, so the long sums round to nearest here instead of
+    // accumulating inside the tensor core over all of K, and the MMAs of
+    // chunk c - 1 still run meanwhile.
     float y[kTcTok];
 #pragma unroll
     for (int n = 0; n < kTcTok; ++n) y[n] = 0.f;
-#pragma unroll 1
-    for (int c = 0; c < G; ++c) {
+    auto step = [&](int c, uint32_t (&w0)[BITS], uint32_t &sb0, float4 (&h0)[4]) -> bool {
         const int b = c & 1;
         uint8_t *const Ab = A0 + 2 * b * kTileA, *const Alb = Ab + kTileA, *const Bb = B0 + b * kTileB;
-        load_codes(c + 2, w2, sb2);
-        load_inputs(c + 1, h1);
         // the MMAs that last read buffer b (chunk c - 2) must be done (a
         // thread whose wait runs out still takes part in this chunk's
         // barrier, after which the whole CTA stops)
-        if (c >= 2) ok = mbar_wait_bounded(su32(&bar[b]), (unsigned)((c - 2) >> 1) & 1u, timeout_ns);
-        if (c >= 1 && warp < 4) {
-            // chunk c - 1's sums (block b ^ 1), once its commit arrived
-            ok = mbar_wait_bounded(su32(&bar[b ^ 1]), (unsigned)((c - 1) >> 1) & 1u, timeout_ns) && ok;
+        if (c >= 2) {
+            ok = mbar_wait_bounded(su32(&bar[b]), (unsigned)((c - 2) >> 1) & 1u, timeout_ns);
+            // the same commit ends chunk c - 2's sums (block (c - 2) & 3)
             asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory");
-            if (ok) drain_block(taddr, warp, b ^ 1, y);
+            if (ok) drain_block(taddr, warp, (c - 2) & 3, y);
         }
         // weights: 32 values of row arow, group c, as high and low fp16 halves
         {
@@ -302,18 +302,13 @@ __device__ __forceinline__ void grouped_tc_body(const TcSet &set, int u, int til
                     make_uint4(pack_h(v[8 * k8], v[8 * k8 + 1]), pack_h(v[8 * k8 + 2], v[8 * k8 + 3]),
                                pack_h(v[8 * k8 + 4], v[8 * k8 + 5]), pack_h(v[8 * k8 + 6], v[8 * k8 + 7]));
         }
-#pragma unroll
-        for (int i = 0; i < BITS; ++i) { w0[i] = w1[i]; w1[i] = w2[i]; }
-        sb0 = sb1;
-        sb1 = sb2;
-#pragma unroll
-        for (int i = 0; i < 4; ++i) h0[i] = h1[i];
+        load_set(c + 2, w0, sb0, h0);
         // the generic-proxy stores above become visible to the tensor core,
         // and the tensor-memory reads above end before the next MMAs
         asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
         asm volatile("tcgen05.fence::before_thread_sync;" ::: "memory");
         ok = __syncthreads_and(ok);
-        if (!ok) break;
+        if (!ok) return false;
         if (tid == 0) {
             asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory");
 #pragma unroll
@@ -324,7 +319,7 @@ __device__ __forceinline__ void grouped_tc_body(const TcSet &set, int u, int til
                 const uint64_t ad = smem_desc(su32(At) + ks * 256), bd = smem_desc(su32(Bb) + ks * 256);
                 const uint32_t accumulate = kk > 0 ? 1u : 0u;
                 asm volatile("{\n\t.reg .pred p;\n\tsetp.ne.b32 p, %4, 0;\n\t"
-                             "tcgen05.mma.cta_group::1.kind::f16 [%0], %1, %2, %3, p;\n\t}" ::"r"(taddr + kTcN * b),
+                             "tcgen05.mma.cta_group::1.kind::f16 [%0], %1, %2, %3, p;\n\t}" ::"r"(taddr + kTcN * (c & 3)),
                              "l"(ad), "l"(bd), "r"(kIdesc), "r"(accumulate)
                              : "memory");
             }
@@ -332,17 +327,37 @@ __device__ __forceinline__ void grouped_tc_body(const TcSet &set, int u, int til
                              su32(&bar[b]))
                          : "memory");
         }
+        return true;
+    };
+#pragma unroll 1
+    for (int c = 0; c < G; c += 2) {
+        if (!step(c, wA, sbA, hA)) break;
+        if (c + 1 < G && !step(c + 1, wB, sbB, hB)) break;
     }
-    // the last chunk's sums
-    if (ok && G > 0) ok = mbar_wait_bounded(su32(&bar[(G - 1) & 1]), (unsigned)((G - 1) >> 1) & 1u, timeout_ns);
+    // the last two chunks' sums
+    for (int c = G - 2; c < G; ++c)
+        if (ok && c >= 0) ok = mbar_wait_bounded(su32(&bar[c & 1]), (unsigned)(c >> 1) & 1u, timeout_ns);
     ok = __syncthreads_and(ok);
     asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory");
+    if (ok) {
+        for (int c = G - 2; c < G; ++c)
+            if (c >= 0) drain_block(taddr, warp, c & 3, y);
+        // warps 4-7 hand their low-half sums to warps 0-3 (same tile rows)
+        // through the weight buffers, idle now that every MMA has finished
+        float *lo = reinterpret_cast<float *>(A0);
+        if (warp >= 4) {
+#pragma unroll
+            for (int n = 0; n < kTcTok; ++n) lo[n * kTcRows + (tid - kTcRows)] = y[n];
+        }
+    }
+    __syncthreads();
     if (!ok) {
         if (tid == 0) atomicOr(err, kStatusTimeout);
     } else if (warp < 4) {
-        // warps 0-3: lane 32 warp + lane of tensor memory = tile row tid;
-        // y[n] = token row n's sum of high- and low-half columns over all chunks
-        if (G > 0) drain_block(taddr, warp, (G - 1) & 1, y);
+        // warps 0-3: tile row tid; y[n] = token row n's sum over all chunks
+        const float *lo = reinterpret_cast<const float *>(A0);
+#pragma unroll
+        for (int n = 0; n < kTcTok; ++n) y[n] += lo[n * kTcRows + tid];
         const int r = kTcRows * tile + tid;
 #pragma unroll 1
         for (int n = 0; n < nr; ++n) {

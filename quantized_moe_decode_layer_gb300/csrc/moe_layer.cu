@@ -64,7 +64,6 @@ constexpr int NCW = kConsumerWarps;
 constexpr int NCT = NCW * 32;
 constexpr unsigned FULLMASK = 0xffffffffu;
 constexpr float kXScale = 0x1p100f;  // arranged vectors hold x * 2^100
-constexpr float kFmScale = 0x1p-77f; // (q 2^-23) (x 2^100) -> q x
 
 // ------------------------------------------------------------ shared layout
 
@@ -246,11 +245,6 @@ __device__ __forceinline__ void cbar() { asm volatile("bar.sync 1, %0;" ::"n"(NC
 __device__ __forceinline__ void red_release_add(unsigned *p, unsigned v)
 {
     asm volatile("red.release.gpu.global.add.u32 [%0], %1;" ::"l"(p), "r"(v) : "memory");
-}
-
-__device__ __forceinline__ void red_relaxed_add(unsigned *p, unsigned v)
-{
-    asm volatile("red.relaxed.gpu.global.add.u32 [%0], %1;" ::"l"(p), "r"(v) : "memory");
 }
 
 __device__ __forceinline__ unsigned atom_add_acqrel(unsigned *p, unsigned v)

@@ -189,6 +189,15 @@ def test_a35b_m32_grouped():
     check_layer(shape, L, layer, lay, x)
 
 
+def test_tiny_m40_two_groups():
+    """40 rows: grouped mode in two groups (32 + 8 rows); routing bit-exact,
+    outputs within the tolerance."""
+    shape = synth.TINY
+    L, layer, lay = cached(shape, 7)
+    x = rows_with_margin(shape, lay, 640, 40)
+    check_layer(shape, L, layer, lay, x)
+
+
 def test_a35b_m32_fma_chunks(fma_only):
     """32 rows with grouped mode off: four 8-row launches of the FMA path."""
     shape = synth.A35B

@@ -15,10 +15,12 @@
 //   - One CTA per (expert, tile of 128 consecutive weight rows; for gate/up
 //     64 units of gate and up rows).  The tile is the MMA's M = 128 dimension.
 //   - The token rows are the N dimension: N = 64 = 32 rows of the high fp16
-//     halves of the inputs, then 32 rows of the low halves (x - fp16(x)), so
+//     halves of the inputs (x with its 13 low mantissa bits cleared: exact in
+//     fp16), then 32 rows of the low halves (x - high, rounded to fp16), so
 //     the inputs keep ~22 significant bits.  The weights are split the same
-//     way (w = fma(q, s, b) in fp32, then high and low fp16 halves, each an
-//     MMA into the same accumulator), so every product term keeps ~21 bits.
+//     way (w = fma(q, s, b) in fp32, then the two halves, each an MMA into
+//     the same accumulator), so every product term keeps ~21 bits.  Only the
+//     final packing of two halves into one f16x2 word is a conversion.
 //     (bf16 halves keep only ~16: with outputs that are small differences of
 //     terms in the thousands, as the synthetic 6-bit layers give, that
 //     missed the output tolerance.)  fp16 bounds the inputs and weights to
@@ -106,12 +108,20 @@ __device__ __forceinline__ bool mbar_wait_bounded(uint32_t bar, unsigned parity,
     }
 }
 
+// Two floats as one f16x2 word (a in the low half), one paired conversion.
 __device__ __forceinline__ uint32_t pack_h(float a, float b)
 {
-    const uint32_t lo = __half_as_ushort(__float2half_rn(a));
-    const uint32_t hi = __half_as_ushort(__float2half_rn(b));
-    return lo | (hi << 16);
+    const __half2 h = __floats2half2_rn(a, b);
+    return *reinterpret_cast<const uint32_t *>(&h);
 }
+
+// The high fp16 half of v without a conversion: v with its 13 low mantissa
+// bits cleared has at most 11 significant bits, so it converts to fp16
+// exactly (inside fp16's range), and v - hi is exact in fp32.
+__device__ __forceinline__ float f16_hi(float v) { return __uint_as_float(__float_as_uint(v) & 0xFFFFE000u); }
+
+// A code (below 2^23) as a float without a conversion instruction.
+__device__ __forceinline__ float code_f(uint32_t q) { return __uint_as_float(q | 0x4B000000u) - 8388608.0f; }
 
 // Code k (0 .. 31) of half a group's LSB-first code stream, held in the
 // BITS words w (32 codes of BITS bits).
@@ -271,10 +281,9 @@ __device__ __forceinline__ void grouped_tc_body(const TcSet &set, int u, int til
                 uint32_t ph[4], pl[4];
 #pragma unroll
                 for (int j = 0; j < 4; ++j) {
-                    const float wa = fmaf((float)code_at<BITS>(w0, 8 * k8 + 2 * j), sc, bb);
-                    const float wb = fmaf((float)code_at<BITS>(w0, 8 * k8 + 2 * j + 1), sc, bb);
-                    const float ha = __half2float(__float2half_rn(wa));
-                    const float hb = __half2float(__float2half_rn(wb));
+                    const float wa = fmaf(code_f(code_at<BITS>(w0, 8 * k8 + 2 * j)), sc, bb);
+                    const float wb = fmaf(code_f(code_at<BITS>(w0, 8 * k8 + 2 * j + 1)), sc, bb);
+                    const float ha = f16_hi(wa), hb = f16_hi(wb);
                     ph[j] = pack_h(ha, hb);
                     pl[j] = pack_h(wa - ha, wb - hb);
                 }
@@ -293,7 +302,7 @@ __device__ __forceinline__ void grouped_tc_body(const TcSet &set, int u, int til
             }
 #pragma unroll
             for (int i = 0; i < 16; ++i) {
-                const float hi = __half2float(__float2half_rn(v[i]));
+                const float hi = f16_hi(v[i]);
                 v[i] = lo_half ? v[i] - hi : hi;
             }
 #pragma unroll

@@ -1,15 +1,18 @@
 // Grouped products of the routed experts on the 5th-generation tensor cores
 // (tcgen05, accumulators in tensor memory): the grouped-GEMM regime that
-// appears when many token rows share an expert.  Not on the decode path: the
-// decode kernel keeps every step on the FMA pipes, where each token row's
-// result is bitwise the one-row result; these kernels stand beside it as a
-// measured alternative for M up to 32.
+// appears when many token rows share an expert.  Grouped mode (moe_grouped.cu)
+// runs a layer's expert products here when a call has more rows than one
+// persistent launch holds; up to that the persistent kernel keeps every step
+// on the FMA pipes, where each token row's result is bitwise the one-row
+// result.
 //
 // What they compute (an expert FFN as the pages state it: dequantised weight
 // w = q * s + b per group of 64 along the input axis, SwiGLU between the two
 // projections): for each listed expert e and each token row m in its mask,
 //   gate/up:  act[u][m][j] = silu(W_gate,e[j] . hn[m]) * (W_up,e[j] . hn[m])
 //   down:     y[u][m][h]   = W_down,e[h] . act[u][m]
+// A launch can carry a second set of products (the shared expert, with its
+// own weights and code width) beside the first.
 //
 // Layout and arithmetic:
 //   - One CTA per (expert, tile of 128 consecutive weight rows; for gate/up
@@ -29,21 +32,21 @@
 //     each of the CTA's 256 threads dequantises half a group of one tile row
 //     into shared memory and writes 16 inputs of the token-row chunk next to
 //     it, and one thread issues 8 MMAs of K = 16 (high, then low weight
-//     halves) into the same fp32
-//     accumulator in tensor memory.  Two register sets of codes, scales and
-//     inputs alternate between even and odd chunks; chunk c + 2's loads go
-//     out as soon as chunk c has been converted.
-//     Two chunk buffers alternate; an MMA batch's commit arrives on the
-//     buffer's mbarrier, which the next writers of that buffer wait on.
+//     halves).  Two register sets of codes, scales and inputs alternate
+//     between even and odd chunks; chunk c + 2's loads go out as soon as
+//     chunk c has been converted.  Two chunk buffers alternate in shared
+//     memory; an MMA batch's commit arrives on the buffer's mbarrier, which
+//     the next writers of that buffer wait on.
 //   - Shared-memory tiles use the no-swizzle K-major canonical layout: 8x16-
 //     byte core matrices of 128 contiguous bytes, 128 B apart along K and
 //     1024 B apart along M/N.
-//   - Each chunk's MMAs start a fresh sum in one of four accumulator blocks;
-//     two chunks later every warp adds the block into fp32 registers (round
-//     to nearest; warps 0-3 the high-half columns, warps 4-7 the low), so the
-//     long sum over K is not accumulated inside the tensor core.
-//   - Epilogue: warp w < 4 reads tensor-memory lanes 32w .. 32w + 31 (its rows),
-//     adds the high and low columns; for gate/up, the neighbours 2j, 2j + 1
+//   - Each chunk's MMAs start a fresh fp32 sum in one of four accumulator
+//     blocks; two chunks later every warp adds the block into fp32 registers
+//     (round to nearest; warps 0-3 the high-half columns, warps 4-7 the low),
+//     so the long sum over K is not accumulated inside the tensor core (that
+//     drifted beyond the output tolerance on cancelling outputs).
+//   - Epilogue: warps 4-7 hand their low-half sums to warps 0-3 (the same
+//     tile rows) through shared memory; for gate/up the neighbours 2j, 2j + 1
 //     meet through one shuffle for SwiGLU.
 // Every wait is bounded; a wait that runs out sets *err and the CTA skips
 // the rest of its work, still freeing its tensor memory.

@@ -257,8 +257,8 @@ int moe_set_grouped(int min_rows);
  * expert's FFN for every token row that chose it, when many rows share an
  * expert (flash-moe, "Metal Compute Shaders": dequant mat-vec and SwiGLU;
  * PureDrive-35B-A3B model card, "How it works": one read of the weights for
- * all rows).  Not used by moe_decode_layer or the stack, which stay on the
- * FMA pipes; it is the measured alternative for many rows per expert.
+ * all rows).  Grouped mode (moe_set_grouped) computes a layer's expert
+ * products with these kernels; this call exposes the gate/up half alone.
  *
  *   for u < U, e = experts_dev[u], each row m < M with bit m of masks_dev[u]:
  *     act_dev[(u * M + m) * I + j] = silu(W_gate,e[j] . hn_m) * (W_up,e[j] . hn_m)

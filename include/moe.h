@@ -161,7 +161,9 @@ int moe_router_topk(const moe_layer *layer, const uint16_t *x_dev, int M, int32_
  * out_normed_dev [M, H] (needs gamma_next).  out_dev may alias x_dev.  Each
  * selected expert's weights are streamed from memory once for all the rows
  * that chose it (model card, "How it works": the verify pass reads its
- * weights once), and row m of the result does not depend on the other rows.
+ * weights once).  Up to one persistent launch's rows (8 at H = 2048) row m
+ * of the result is bitwise the one-row result; above, grouped mode runs
+ * (moe_set_grouped): the same routing, values within the tolerance.
  * Errors: INVALID_ARG, UNSUPPORTED, BUFFER_TOO_SMALL, CUDA. */
 int moe_decode_layer(const moe_layer *layer, const uint16_t *x_dev, int M, uint16_t *out_dev,
                      uint16_t *out_normed_dev, void *ws_dev, size_t ws_bytes, moe_stream_t stream);

@@ -217,14 +217,17 @@ __device__ __forceinline__ void grouped_tc_body(const TcSet &set, int u, int til
     asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory");
     const uint32_t taddr = *tmem_slot;
 
-    // this thread's half weight row (row tid / 2 of the tile, codes 32 (tid
-    // & 1) .. + 31 of each group) and its token-chunk share (B row tid / 4,
-    // inputs 16 (tid & 3) .. + 15 of each chunk)
-    const int arow = tid >> 1, ah = tid & 1;
+    // this thread's half weight row (codes 32 ah .. + 31 of each group of
+    // row arow) and its token-chunk share (inputs kq .. + 15 of each chunk of
+    // B row brow).  Each warp keeps 16 weight rows and 8 B rows; within every
+    // 8 consecutive lanes the row varies and the column does not, so their
+    // 16-byte stores fill one 128-byte core-matrix row set with no bank
+    // conflict.
+    const int arow = ((tid >> 4) << 3) | (tid & 7), ah = (tid >> 3) & 1;
     const uint8_t *row = W + ((size_t)e * rows + (size_t)kTcRows * tile + arow) * (size_t)row_bytes;
     const uint32_t *codes = reinterpret_cast<const uint32_t *>(row) + ah * BITS;   // + c * 2 BITS words
     const uint32_t *sbp = reinterpret_cast<const uint32_t *>(row + (size_t)K * BITS / 8);
-    const int brow = tid >> 2, kq = (tid & 3) * 16;
+    const int brow = ((tid >> 5) << 3) | (tid & 7), kq = ((tid >> 3) & 3) * 16;
     const int tn = brow & (kTcTok - 1);
     const bool lo_half = brow >= kTcTok;
     int trow = tn < nr ? (int)__fns(mask, 0, tn + 1) : -1;

@@ -108,6 +108,15 @@ def load_traffic():
     return None
 
 
+def traffic_for(record, layers: int):
+    """The record's DRAM bytes of one stack launch, scaled from its own layer
+    count to `layers` (at M=1 every layer reads the same bytes: U = 8 experts
+    per layer), or None without a record."""
+    if not record:
+        return None
+    return int(round(record["bytes_per_launch"] * layers / record.get("layers", LAYERS)))
+
+
 class Clocks:
     """nvidia-smi samples during the timed region."""
 
@@ -311,7 +320,7 @@ def run_ours(args):
     traffic = load_traffic()
     roof = {"bound": "hbm", "achieved": round(achieved, 1), "peak": peaks["hbm_gbs"], "unit": "GB/s",
             "frac": round(achieved / peaks["hbm_gbs"], 4), "peak_kind": peak_kind,
-            "traffic": (traffic["bytes_per_launch"] if traffic else None),
+            "traffic": traffic_for(traffic, args.layers),
             "algorithmic_bytes": bytes1, "launch_ms_mean": round(mean_ms, 5), "launch_ms_median": round(med_ms, 5)}
 
     # end to end through the C ABI with host buffers (copies inside the call)

@@ -50,3 +50,13 @@ def test_unique_bytes_by_hand():
 
 def test_flops():
     assert layer_flops(synth.A35B, 8, 1) == 8 * 6 * 512 * 2048 + 6 * 512 * 2048 + 2 * 257 * 2048
+
+
+def test_traffic_record_scales_with_layers():
+    """The bench's DRAM-traffic figure is per launch of the stack it ran: the
+    committed record (40 layers) scales with the launch's layer count."""
+    import bench
+    rec = {"bytes_per_launch": 992006827, "layers": 40}
+    assert bench.traffic_for(rec, 40) == 992006827
+    assert bench.traffic_for(rec, 8) == round(992006827 * 8 / 40)
+    assert bench.traffic_for(None, 8) is None

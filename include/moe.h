@@ -298,9 +298,11 @@ const char *moe_status_str(int status);
 int moe_last_cuda_error(void);
 
 /* Host-side checks (no GPU needed): the code-extraction tables the kernels
- * use, and the launch plans of the test shapes against the invariants the
- * kernel relies on (ring depth, stage and buffer sizes, shared-memory limit).
- * Returns the number of violations, 0 when consistent. */
+ * use; the launch plans of the test shapes against the invariants the
+ * kernel relies on (ring depth, stage and buffer sizes, shared-memory limit);
+ * and the workspace layouts for 1 to 100 rows (aligned, ordered regions, each
+ * large enough for what is written into it, grouped-mode regions only above
+ * one launch's rows).  Returns the number of violations, 0 when consistent. */
 int moe_selftest_host(void);
 
 /* Number of kernel launches the library enqueued on this host thread since

@@ -223,6 +223,78 @@ int plan_selftest_host()
     return bad;
 }
 
+// Host-side check of the workspace layouts over shapes and row counts: every
+// region 256-byte aligned, in order, large enough for what its users write
+// into it, and inside the total; the grouped regions sized for min(M, 32)
+// rows and min(E, rows k) experts, and absent from the persistent-only
+// layout.  Returns the number of violations.
+int ws_layout_selftest_host()
+{
+    const moe_layer_desc shapes[] = {
+        {256, 128, 16, 2, 4, 8, 0, 0, 0, 1e-6f},
+        {2048, 512, 256, 8, 6, 8, 8, 1, 512, 1e-6f},
+        {4096, 1024, 512, 10, 4, 8, 8, 1, 1024, 1e-6f},
+    };
+    const int rows[] = {1, 2, 4, 7, 8, 9, 16, 17, 31, 32, 33, 64, 100};
+    int bad = 0;
+    for (const moe_layer_desc &d : shapes) {
+        Geo g;
+        if (!make_geo(d, g)) { ++bad; continue; }
+        const size_t Is = g.Is ? (size_t)g.Is : 1;
+        for (int M : rows) {
+            WsLayout w, f;
+            make_ws_layout(g, M, w);
+            make_ws_layout_fma(g, M, f);
+            const int R = w.maxr;
+            // the persistent kernel's regions, in order, each holding its data
+            const size_t need[][2] = {
+                {w.off_logits, (size_t)kLogitCopies * R * g.Er * 8},
+                {w.off_act, (size_t)w.max_slots * R * g.I * 8},
+                {w.off_act_s, (size_t)R * Is * 8},
+                {w.off_ping, (size_t)2 * R * (g.H / 2) * 8},
+                {w.off_y, (size_t)R * g.k * g.H * 8},
+                {w.off_stage_in, (size_t)M * g.H * 2},
+                {w.off_stage_out, (size_t)M * g.H * 2},
+            };
+            size_t end = kCtrlBytes;
+            for (const auto &r : need) {
+                if (r[0] % 256 != 0 || r[0] < end) ++bad;
+                end = r[0] + r[1];
+            }
+            if (f.total < end || f.total > w.total || f.total % 256 != 0 || f.grp_rows != 0) ++bad;
+            if (w.max_slots != (g.E < R * g.k ? g.E : R * g.k)) ++bad;
+            if (M <= R) {
+                if (w.grp_rows != 0 || w.grp_slots != 0 || w.total != f.total) ++bad;
+                continue;
+            }
+            const int GR = M < kGroupRows ? M : kGroupRows;
+            const int GS = g.E < GR * g.k ? g.E : GR * g.k;
+            if (w.grp_rows != GR || w.grp_slots != GS) ++bad;
+            const size_t gneed[][2] = {
+                {w.off_g_hn, (size_t)GR * g.H * 4},
+                {w.off_g_sigma, (size_t)GR * 4},
+                {w.off_g_idx, (size_t)GR * g.k * 4},
+                {w.off_g_w, (size_t)GR * g.k * 4},
+                {w.off_g_slotof, (size_t)GR * g.k * 4},
+                {w.off_g_experts, (size_t)(GS + 1) * 4},
+                {w.off_g_masks, (size_t)(GS + 1) * 4},
+                {w.off_g_count, 4},
+                {w.off_g_act, (size_t)GS * GR * g.I * 4},
+                {w.off_g_act_s, (size_t)GR * Is * 4},
+                {w.off_g_y, (size_t)GS * GR * g.H * 4},
+                {w.off_g_ysh, (size_t)GR * g.H * 4},
+                {w.off_g_ping, (size_t)2 * GR * g.H * 2},
+            };
+            for (const auto &r : gneed) {
+                if (r[0] % 256 != 0 || r[0] < end) ++bad;
+                end = r[0] + r[1];
+            }
+            if (w.total < end || w.total % 256 != 0) ++bad;
+        }
+    }
+    return bad;
+}
+
 }  // namespace
 }  // namespace moe
 
@@ -562,6 +634,6 @@ long long moe_launch_count(int reset)
     return n;
 }
 
-int moe_selftest_host(void) { return unpack_selftest_host() + plan_selftest_host(); }
+int moe_selftest_host(void) { return unpack_selftest_host() + plan_selftest_host() + ws_layout_selftest_host(); }
 
 }  // extern "C"

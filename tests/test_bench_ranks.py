@@ -17,8 +17,11 @@ def _free_port() -> int:
 
 
 def _rank_main(rank, world, port, times, q):
+    import datetime
+
     import torch.distributed as td
-    td.init_process_group("gloo", init_method=f"tcp://127.0.0.1:{port}", rank=rank, world_size=world)
+    td.init_process_group("gloo", init_method=f"tcp://127.0.0.1:{port}", rank=rank, world_size=world,
+                          timeout=datetime.timedelta(seconds=60))
     try:
         t = bench.reduce_max(times[rank])
         v = bench.whole_job_gbs(world, 1_000_000_000, 10, t)

@@ -1,7 +1,6 @@
 """The bench's multi-rank host logic on CPU: two gloo ranks stand in for two
 GPU replicas.  The job's time is the slowest rank's, the job's throughput is
 every rank's bytes over that time, and only rank 0 of the reference arm runs."""
-import os
 import socket
 
 import pytest

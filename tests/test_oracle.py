@@ -295,3 +295,29 @@ def test_stack_is_chained_layers():
         assert np.array_equal(r["out"], res[i]["out"])
         x = r["out"]
     assert np.array_equal(res[-1]["out_n"], oracle.bf16_round_array(res[-1]["on"]))
+
+
+def test_expert_relabelling_invariance():
+    """Relabelling the experts (router row e and expert e's weights both moved
+    to id pi(e)) moves the selected ids to pi(idx) and leaves the weights and
+    the output unchanged: the router row and the weights of one expert stay
+    paired, whatever the labels."""
+    sh = synth.LayerShape("mini", 128, 64, 12, 3, 6, 8, 8, True, 128, True)
+    L = synth.make_layer(sh, 41)
+    pi = torch.randperm(sh.E, generator=torch.Generator().manual_seed(7))
+    inv = torch.argsort(pi)
+    P = dict(L)
+    P["router_w"] = L["router_w"][inv]
+    for key in ("gate", "up", "down"):
+        P[key] = {f: (v[inv] if isinstance(v, torch.Tensor) else v) for f, v in L[key].items()}
+    xb = synth.bf16_bits(synth.make_rows(sh, 42, 3, gamma=L["gamma"])).numpy().view(np.uint16)
+    r = oracle.Layer(L).forward(xb)
+    rp = oracle.Layer(P).forward(xb)
+    assert np.array_equal(rp["idx"], pi.numpy()[r["idx"]])
+    assert np.allclose(rp["w"], r["w"], rtol=1e-14, atol=0)
+    assert np.allclose(rp["o"], r["o"], rtol=1e-12, atol=1e-14)
+    # a label that is not carried over (the down weights left in place) changes the output
+    Q = dict(P)
+    Q["down"] = L["down"]
+    rq = oracle.Layer(Q).forward(xb)
+    assert not np.allclose(rq["o"], r["o"], rtol=1e-6, atol=1e-9)

@@ -13,7 +13,8 @@ from ._lib import LayerDesc, SrcLayer, SrcMatrix, check, lib
 def _ptr(t) -> int | None:
     if t is None:
         return None
-    assert t.is_cuda and t.is_contiguous(), "device tensors must be contiguous CUDA tensors"
+    if not (t.is_cuda and t.is_contiguous()):
+        raise ValueError("device tensors must be contiguous CUDA tensors")
     return t.data_ptr()
 
 
@@ -143,7 +144,8 @@ class Workspace:
     def __init__(self, desc: LayerDesc, max_M: int, device="cuda", stream=None):
         self.nbytes = workspace_size(desc, max_M)
         self.buf = torch.empty(self.nbytes, dtype=torch.uint8, device=device)
-        assert self.buf.data_ptr() % 256 == 0
+        if self.buf.data_ptr() % 256 != 0:
+            raise RuntimeError("workspace allocation is not 256-byte aligned")
         self.max_M = max_M
         self.init(stream)
 
@@ -241,7 +243,11 @@ class Stack:
 
     def forward_host(self, x_host: torch.Tensor, out_host: torch.Tensor, ws: Workspace, stream=None):
         """Host buffers in and out (copies inside the call); synchronises."""
-        assert not x_host.is_cuda and not out_host.is_cuda
+        for name, t in (("x_host", x_host), ("out_host", out_host)):
+            if t.is_cuda or not t.is_contiguous() or t.dtype != torch.bfloat16:
+                raise ValueError(f"{name} must be a contiguous bfloat16 host tensor")
+        if tuple(out_host.shape) != tuple(x_host.shape):
+            raise ValueError("out_host must have the shape of x_host")
         M = x_host.shape[0]
         check("moe_stack_forward_host",
               lib().moe_stack_forward_host(self.handle, _bits16(x_host).data_ptr(), M, _bits16(out_host).data_ptr(),

@@ -83,3 +83,16 @@ def test_argument_errors():
 def test_workspace_sizes_grow_with_rows():
     d = moe.desc_from_shape(synth.A35B)
     assert moe.workspace_size(d, 1) < moe.workspace_size(d, 8) < moe.workspace_size(d, 32)
+
+
+def test_binding_rejects_host_and_strided_tensors():
+    """The binding hands the library device pointers only: a host tensor, or
+    a strided view whose memory is not the logical layout, is refused before
+    any call."""
+    import torch
+    from quantized_moe_decode_layer_gb300 import api
+    assert api._ptr(None) is None
+    with pytest.raises(ValueError):
+        api._ptr(torch.zeros(4))
+    with pytest.raises(ValueError):
+        api._ptr(torch.zeros(4, 4).t())

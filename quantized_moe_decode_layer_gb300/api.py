@@ -18,6 +18,19 @@ def _ptr(t) -> int | None:
     return t.data_ptr()
 
 
+def _need(t, name: str, dtype, shape) -> None:
+    """Refuse, before any call, a tensor the library would read or write out
+    of its bounds: it must be a contiguous CUDA tensor of `dtype` and `shape`
+    (None in `shape` matches any extent)."""
+    ok = (isinstance(t, torch.Tensor) and t.is_cuda and t.is_contiguous() and t.dtype == dtype
+          and t.dim() == len(shape) and all(n is None or t.shape[i] == n for i, n in enumerate(shape)))
+    if not ok:
+        want = ", ".join("*" if n is None else str(n) for n in shape)
+        got = (f"{tuple(t.shape)} {t.dtype} on {t.device}, contiguous={t.is_contiguous()}"
+               if isinstance(t, torch.Tensor) else type(t).__name__)
+        raise ValueError(f"{name} must be a contiguous CUDA {dtype} tensor of shape [{want}]; got {got}")
+
+
 def _stream(stream=None) -> int:
     s = stream if stream is not None else torch.cuda.current_stream()
     return s.cuda_stream
@@ -162,6 +175,7 @@ class Workspace:
 
 
 def router_topk(layer: Layer, x: torch.Tensor, ws: Workspace, stream=None):
+    _need(x, "x", torch.bfloat16, (None, layer.desc.H))
     M = x.shape[0]
     idx = torch.empty((M, layer.desc.k), dtype=torch.int32, device=x.device)
     w = torch.empty((M, layer.desc.k), dtype=torch.float32, device=x.device)
@@ -172,9 +186,11 @@ def router_topk(layer: Layer, x: torch.Tensor, ws: Workspace, stream=None):
 
 def decode_layer(layer: Layer, x: torch.Tensor, ws: Workspace, out=None, normed: bool = False, stream=None):
     """out (and out_normed when normed) bf16 [M, H]."""
+    _need(x, "x", torch.bfloat16, (None, layer.desc.H))
     M = x.shape[0]
     if out is None:
         out = torch.empty_like(x)
+    _need(out, "out", torch.bfloat16, (M, layer.desc.H))
     on = torch.empty_like(x) if normed else None
     check("moe_decode_layer", lib().moe_decode_layer(layer.handle, _ptr(_bits16(x)), M, _ptr(_bits16(out)),
                                                      _ptr(_bits16(on)) if on is not None else None,
@@ -197,12 +213,17 @@ def gate_up_tc(layer: Layer, hn: torch.Tensor, experts: torch.Tensor, masks: tor
     = row m) on the device.  Returns (act fp32 [U, M, I], err int32 [1]);
     entries of rows outside a mask are left as they were in `act` (zeros when
     it is allocated here)."""
+    _need(hn, "hn", torch.float32, (None, layer.desc.H))
+    _need(experts, "experts", torch.int32, (None,))
     M, U, I = hn.shape[0], experts.shape[0], layer.desc.I
+    _need(masks, "masks", torch.int32, (U,))
     if act is None:
         act = torch.zeros((U, M, I), dtype=torch.float32, device=hn.device)
     if err is None:
         err = torch.zeros(1, dtype=torch.int32, device=hn.device)
-    check("moe_gate_up_tc", lib().moe_gate_up_tc(layer.handle, _ptr(hn.contiguous()), M, _ptr(experts), _ptr(masks),
+    _need(act, "act", torch.float32, (U, M, I))
+    _need(err, "err", torch.int32, (1,))
+    check("moe_gate_up_tc", lib().moe_gate_up_tc(layer.handle, _ptr(hn), M, _ptr(experts), _ptr(masks),
                                                  U, _ptr(act), _ptr(err), _stream(stream)))
     return act, err
 
@@ -213,12 +234,17 @@ def down_tc(layer: Layer, act: torch.Tensor, experts: torch.Tensor, masks: torch
 
     act fp32 [U, M, I], experts int32 [U], masks int32 [U] on the device.
     Returns (y fp32 [U, M, H], err int32 [1])."""
+    _need(act, "act", torch.float32, (None, None, layer.desc.I))
     U, M = act.shape[0], act.shape[1]
+    _need(experts, "experts", torch.int32, (U,))
+    _need(masks, "masks", torch.int32, (U,))
     if y is None:
         y = torch.zeros((U, M, layer.desc.H), dtype=torch.float32, device=act.device)
     if err is None:
         err = torch.zeros(1, dtype=torch.int32, device=act.device)
-    check("moe_down_tc", lib().moe_down_tc(layer.handle, _ptr(act.contiguous()), M, _ptr(experts), _ptr(masks), U,
+    _need(y, "y", torch.float32, (U, M, layer.desc.H))
+    _need(err, "err", torch.int32, (1,))
+    check("moe_down_tc", lib().moe_down_tc(layer.handle, _ptr(act), M, _ptr(experts), _ptr(masks), U,
                                            _ptr(y), _ptr(err), _stream(stream)))
     return y, err
 
@@ -232,9 +258,12 @@ class Stack:
         self.handle = h
 
     def forward(self, x: torch.Tensor, ws: Workspace, out=None, normed: bool = False, stream=None):
+        H = self.layers[0].desc.H
+        _need(x, "x", torch.bfloat16, (None, H))
         M = x.shape[0]
         if out is None:
             out = torch.empty_like(x)
+        _need(out, "out", torch.bfloat16, (M, H))
         on = torch.empty_like(x) if normed else None
         check("moe_stack_forward", lib().moe_stack_forward(self.handle, _ptr(_bits16(x)), M, _ptr(_bits16(out)),
                                                            _ptr(_bits16(on)) if on is not None else None,
@@ -246,8 +275,8 @@ class Stack:
         for name, t in (("x_host", x_host), ("out_host", out_host)):
             if t.is_cuda or not t.is_contiguous() or t.dtype != torch.bfloat16:
                 raise ValueError(f"{name} must be a contiguous bfloat16 host tensor")
-        if tuple(out_host.shape) != tuple(x_host.shape):
-            raise ValueError("out_host must have the shape of x_host")
+        if x_host.dim() != 2 or x_host.shape[1] != self.layers[0].desc.H or tuple(out_host.shape) != tuple(x_host.shape):
+            raise ValueError("x_host and out_host must both have shape [M, H]")
         M = x_host.shape[0]
         check("moe_stack_forward_host",
               lib().moe_stack_forward_host(self.handle, _bits16(x_host).data_ptr(), M, _bits16(out_host).data_ptr(),

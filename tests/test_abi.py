@@ -96,3 +96,7 @@ def test_binding_rejects_host_and_strided_tensors():
         api._ptr(torch.zeros(4))
     with pytest.raises(ValueError):
         api._ptr(torch.zeros(4, 4).t())
+    with pytest.raises(ValueError):
+        api._need(torch.zeros((2, 8), dtype=torch.bfloat16), "x", torch.bfloat16, (None, 8))
+    with pytest.raises(ValueError):
+        api._need([0.0] * 8, "x", torch.bfloat16, (None, 8))

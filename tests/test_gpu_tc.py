@@ -126,3 +126,9 @@ def test_gate_up_tc_rejects_bad_args():
     mk = torch.ones(1, dtype=torch.int32, device=DEV)
     with pytest.raises(moe.MoeError):
         moe.gate_up_tc(layer, hn, ex, mk)
+    # the binding refuses, before any launch, buffers the kernel would overrun
+    # or misread: an output smaller than [U, M, I], masks of another dtype
+    with pytest.raises(ValueError):
+        moe.gate_up_tc(layer, hn[:2], ex, mk, act=torch.zeros((1, 1, sh.I), dtype=torch.float32, device=DEV))
+    with pytest.raises(ValueError):
+        moe.gate_up_tc(layer, hn[:2], ex, mk.long())

@@ -198,6 +198,29 @@ def decode_layer(layer: Layer, x: torch.Tensor, ws: Workspace, out=None, normed:
     return (out, on) if normed else out
 
 
+def decode_layer_noalloc(layer: Layer, x: torch.Tensor, out=None, normed: bool = False, stream=None):
+    """moe_decode_layer_noalloc: decode_layer with the library's fixed
+    scratch instead of a workspace (no device allocation at the call; calls
+    must not overlap on the GPU).  Rows whose workspace would exceed the
+    scratch raise MoeError (MOE_ERR_BUFFER_TOO_SMALL)."""
+    _need(x, "x", torch.bfloat16, (None, layer.desc.H))
+    M = x.shape[0]
+    if out is None:
+        out = torch.empty_like(x)
+    _need(out, "out", torch.bfloat16, (M, layer.desc.H))
+    on = torch.empty_like(x) if normed else None
+    check("moe_decode_layer_noalloc",
+          lib().moe_decode_layer_noalloc(layer.handle, _ptr(_bits16(x)), M, _ptr(_bits16(out)),
+                                         _ptr(_bits16(on)) if on is not None else None, _stream(stream)))
+    return (out, on) if normed else out
+
+
+def selftest_host() -> int:
+    """moe_selftest_host: violations found by the library's host-side checks
+    (code tables, launch plans, workspace layouts); 0 when consistent."""
+    return int(lib().moe_selftest_host())
+
+
 def set_grouped(min_rows: int) -> None:
     """Grouped mode (tensor-core expert products) for calls of at least
     min_rows rows above one launch's rows (default 1); 0 turns it off

@@ -100,3 +100,16 @@ def test_binding_rejects_host_and_strided_tensors():
         api._need(torch.zeros((2, 8), dtype=torch.bfloat16), "x", torch.bfloat16, (None, 8))
     with pytest.raises(ValueError):
         api._need([0.0] * 8, "x", torch.bfloat16, (None, 8))
+
+
+def test_binding_wrappers_for_selftest_and_noalloc():
+    """The binding carries the ABI's names: the host selftest through it
+    finds no violation, and the no-alloc decode refuses host tensors before
+    calling the library."""
+    import types
+
+    import torch
+    assert moe.selftest_host() == 0
+    stand_in = types.SimpleNamespace(desc=types.SimpleNamespace(H=8))
+    with pytest.raises(ValueError):
+        moe.decode_layer_noalloc(stand_in, torch.zeros((1, 8), dtype=torch.bfloat16))

@@ -269,9 +269,11 @@ int moe_set_grouped(int min_rows);
  * and masks_dev uint32 [U] (device).  act_dev: fp32 [U][M][I] (device); entries
  * of rows outside a mask are not written (mask bits at or above M are
  * ignored).  M <= 32.  Arithmetic: each weight w = q * s + b (fp32) and each
- * input is split into two fp16 halves (hi = fp16(v), lo = fp16(v - hi)); the
- * four half products accumulate in fp32, so every term keeps ~21 significant
- * bits.  Inputs and weights must stay below 65504 in magnitude.  err_dev (device int) is set to 1 if a device
+ * input value v are split into two fp16 halves: hi is v with its 13 low
+ * mantissa bits cleared (exact in fp16), lo = fp16(v - hi).  The four half
+ * products accumulate in fp32, each chunk of 64 inputs in its own sum added
+ * into fp32 registers, so every term keeps ~21 significant bits.  Inputs and
+ * weights must stay below 65504 in magnitude.  err_dev (device int) is set to 1 if a device
  * wait runs out (see moe_debug_set); the caller clears it.
  * Errors: INVALID_ARG (NULL pointer, M < 1, U < 0), UNSUPPORTED (M > 32),
  * CUDA (launch failed). */

@@ -435,7 +435,8 @@ def run_ours(args):
                        "H": 2048, "E": 256, "k": 8, "I": 512, "I_shared": 512, "routed_bits": 6,
                        "shared_bits": 8, "router_bits": 8, "group": 64, "M": 1, "layers": args.layers,
                        "resident_weight_GB": round(sum(l.nbytes for l in layers) / 1e9, 2),
-                       "l2": "weights rotate over 40 layer sets (26 GB) > L2; no flush",
+                       "l2": (f"weights rotate over {args.layers} layer sets "
+                              f"({sum(l.nbytes for l in layers) / 1e9:.1f} GB) > L2; no flush"),
                        "parallelism": f"replicas x{world}"},
             "us_per_layer": round(us_layer, 3), "fraction_of_8TBs": round(value / world / 8000.0, 4),
             "single_layer_call_us": single, "m4": m4, "sweep": sweep, "tc_gate_up": tc, "b397": b397, "roofline": roof, "e2e": e2e,

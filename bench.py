@@ -513,7 +513,7 @@ def oracle_steps(shape, n_layers, steps, warmup, dev=None, prepared=4):
         done += ubytes[s % P]
     elapsed = time.perf_counter() - t0
     return {"value": round(done / elapsed / 1e9, 6), "unit": "GB/s", "cores": 1, "kind": "oracle",
-            "sample": f"{steps} timed steps of one a35b layer at M=1 each, cycling over the stack's first {P} "
+            "sample": f"{steps} timed steps of one {shape.name} layer at M=1 each, cycling over the stack's first {P} "
                       f"layer sets ({elapsed:.1f} s of oracle time, {warmup} untimed warm-up steps)",
             "s_per_step": elapsed / max(1, steps)}
 

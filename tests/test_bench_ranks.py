@@ -59,3 +59,13 @@ def test_reference_arm_runs_on_rank_zero_only(monkeypatch, capsys):
 
     assert bench.run_reference(Args()) is None
     assert capsys.readouterr().out == ""
+
+
+def test_oracle_steps_times_exactly_the_asked_steps():
+    """The reference arm's stepping on a small shape: W untimed steps, then K
+    timed ones over the prepared layer sets, reported in the bench's unit."""
+    import synth
+    r = bench.oracle_steps(synth.TINY, n_layers=3, steps=5, warmup=2, prepared=2)
+    assert r["kind"] == "oracle" and r["unit"] == "GB/s" and r["cores"] == 1
+    assert r["value"] > 0 and r["s_per_step"] > 0
+    assert r["sample"].startswith("5 timed steps") and "first 2 layer sets" in r["sample"]

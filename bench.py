@@ -41,6 +41,7 @@ def parse():
     p.add_argument("--layers", type=int, default=LAYERS)
     p.add_argument("--no-m4", action="store_true", help="M=1 only: no M=4 line and no M sweep")
     p.add_argument("--cpu-seconds", type=float, default=12.0)
+    p.add_argument("--routing-out", default=None, help="write per-layer routing statistics (JSON) here")
     return p.parse_args()
 
 
@@ -185,8 +186,9 @@ def build_stack(shape, n_layers, dev, seed0=1000):
     return desc, layers
 
 
-def measure_U(layers, x, ws):
-    """Distinct experts per layer along the stack for input x (untimed)."""
+def measure_U(layers, x, ws, selections=None):
+    """Distinct experts per layer along the stack for input x (untimed).  With
+    a list `selections`, appends each layer's expert ids [M, k] (numpy)."""
     import torch
     import quantized_moe_decode_layer_gb300 as moe
     Us = []
@@ -194,8 +196,32 @@ def measure_U(layers, x, ws):
     for lyr in layers:
         idx, _ = moe.router_topk(lyr, h, ws)
         Us.append(int(torch.unique(idx).numel()))
+        if selections is not None:
+            selections.append(idx.cpu().numpy())
         h = moe.decode_layer(lyr, h, ws)
     return Us
+
+
+def routing_stats(selections, E: int):
+    """Per-layer distinct experts U, the fraction of them chosen by two or
+    more rows, and the expert-selection histogram summed over the layers."""
+    import numpy as np
+    U, shared, hist = [], [], np.zeros(E, dtype=np.int64)
+    for idx in selections:
+        ids, counts = np.unique(idx, return_counts=True)
+        rows_per = np.array([int((idx == e).any(axis=1).sum()) for e in ids])
+        U.append(int(ids.size))
+        shared.append(round(float((rows_per >= 2).sum()) / ids.size, 3))
+        hist[ids] += counts
+    return {"U_per_layer": U, "shared_frac_per_layer": shared, "selection_hist": hist.tolist()}
+
+
+def percentiles(per_ms):
+    """p10 / median / p90 of per-step times (ms)."""
+    import numpy as np
+    a = np.asarray(per_ms)
+    return {"p10_ms": round(float(np.percentile(a, 10)), 5), "median_ms": round(float(np.percentile(a, 50)), 5),
+            "p90_ms": round(float(np.percentile(a, 90)), 5), "n": int(a.size)}
 
 
 def time_stack(st, x, ws, steps, warmup, stream):
@@ -299,7 +325,9 @@ def run_ours(args):
     # M = 1 (headline)
     x1 = synth.make_rows(shape, 5, 1, gamma=None).to(dev)
     ws = moe.Workspace(desc, 4)
-    U1 = measure_U(layers, x1, ws)
+    sel1 = []
+    U1 = measure_U(layers, x1, ws, sel1)
+    routing = {"M1": routing_stats(sel1, shape.E)}
     bytes1 = sum(unique_bytes(shape, u, 1) for u in U1)
     barrier()
     with Clocks(local) as clk:
@@ -321,7 +349,8 @@ def run_ours(args):
     roof = {"bound": "hbm", "achieved": round(achieved, 1), "peak": peaks["hbm_gbs"], "unit": "GB/s",
             "frac": round(achieved / peaks["hbm_gbs"], 4), "peak_kind": peak_kind,
             "traffic": traffic_for(traffic, args.layers),
-            "algorithmic_bytes": bytes1, "launch_ms_mean": round(mean_ms, 5), "launch_ms_median": round(med_ms, 5)}
+            "algorithmic_bytes": bytes1, "launch_ms_mean": round(mean_ms, 5), "launch_ms_median": round(med_ms, 5),
+            "launch_percentiles": percentiles(per)}
 
     # end to end through the C ABI with host buffers (copies inside the call)
     xh = x1.cpu().pin_memory()
@@ -343,15 +372,20 @@ def run_ours(args):
     m4 = None
     if not args.no_m4:
         x4 = synth.make_rows(shape, 6, 4, correlation=CORR_M4).to(dev)
-        U4 = measure_U(layers, x4, ws)
+        sel4 = []
+        U4 = measure_U(layers, x4, ws, sel4)
+        routing["M4"] = routing_stats(sel4, shape.E)
         bytes4 = sum(unique_bytes(shape, u, 4) for u in U4)
-        s4 = max(20, args.steps // 2)
-        tm4, per4, _ = time_stack(st, x4, ws, s4, args.warmup, stream)
+        s4 = max(200, args.steps // 2)
+        tm4, per4, l4 = time_stack(st, x4, ws, s4, args.warmup, stream)
         mean4 = sum(per4) / len(per4)
         m4 = {"us_per_layer": round(tm4 / s4 * 1e3 / args.layers, 3),
               "gbs": round(bytes4 / (mean4 * 1e-3) / 1e9, 1),
               "frac": round(bytes4 / (mean4 * 1e-3) / 1e9 / peaks["hbm_gbs"], 4),
-              "mean_U": round(float(np.mean(U4)), 2), "bytes_per_step": bytes4}
+              "mean_U": round(float(np.mean(U4)), 2), "bytes_per_step": bytes4,
+              "rows": "1 token + 3 draft rows, correlation %.1f at the stack input" % CORR_M4,
+              "shared_frac_layer0": routing["M4"]["shared_frac_per_layer"][0],
+              "launches_per_step": l4 / s4, "percentiles": percentiles(per4)}
 
     # the stack over M in {1, 2, 4, 8, 16, 32} independent token rows: up to 8
     # rows one persistent launch per step; above, grouped mode (each selected
@@ -367,18 +401,20 @@ def run_ours(args):
             moe.set_grouped(grouped)
             try:
                 xm = synth.make_rows(shape, 40 + M, M).to(dev)
-                Um = measure_U(layers, xm, wsw)
+                selm = []
+                Um = measure_U(layers, xm, wsw, selm)
+                if key == "32":
+                    routing["M32"] = routing_stats(selm, shape.E)
                 bm = sum(unique_bytes(shape, u, M) for u in Um)
                 sm = max(10, args.steps // 10)
-                tmm, perm, _ = time_stack(st, xm, wsw, sm, args.warmup, stream)
+                tmm, perm, lm = time_stack(st, xm, wsw, sm, args.warmup, stream)
             finally:
                 moe.set_grouped(1)
             s_step = tmm / sm * 1e-3
             sweep[key] = {"tokens_per_s": round(M / s_step, 1), "us_per_layer": round(s_step * 1e6 / args.layers, 3),
                           "gbs": round(bm / s_step / 1e9, 1), "mean_U": round(float(np.mean(Um)), 2),
                           "mode": "grouped" if (M > R and grouped and M >= grouped) else "persistent",
-                          "launches_per_step": (-(-M // R) if not (M > R and grouped and M >= grouped)
-                                                else args.layers * (7 + 2 * int(shape.has_shared)) * -(-M // 32))}
+                          "launches_per_step": lm / sm}
         del wsw
 
     # the grouped gate/up on the tensor cores (moe_gate_up_tc) for the M=32
@@ -425,6 +461,9 @@ def run_ours(args):
         torch.cuda.synchronize()
         single = round(a.elapsed_time(b) * 1e3 / (reps * len(layers)), 3)
 
+    if rank == 0 and args.routing_out:
+        with open(args.routing_out, "w") as f:
+            json.dump({"workload": f"a35b stack, {args.layers} layer sets", **routing}, f)
     cpu = cpu_baseline(args, shape, dev) if rank == 0 else None
     if rank == 0:
         line = {
@@ -440,7 +479,10 @@ def run_ours(args):
                        "parallelism": f"replicas x{world}"},
             "us_per_layer": round(us_layer, 3), "fraction_of_8TBs": round(value / world / 8000.0, 4),
             "single_layer_call_us": single, "m4": m4, "sweep": sweep, "tc_gate_up": tc, "b397": b397, "roofline": roof, "e2e": e2e,
-            "gpu_launches": launches, "clocks": clocks, "cpu_baseline": cpu,
+            "gpu_launches": launches, "launches_per_step": launches / args.steps, "clocks": clocks,
+            "cpu_baseline": cpu,
+            "routing": {k: {"mean_U": round(float(np.mean(v["U_per_layer"])), 2),
+                            "U_per_layer": v["U_per_layer"]} for k, v in routing.items()},
         }
         print(json.dumps(line), flush=True)
     if world > 1:
@@ -448,36 +490,77 @@ def run_ours(args):
         td.destroy_process_group()
 
 
-def cpu_baseline(args, shape, dev=None):
-    """The oracle, as it stands, on a bounded sample of the workload: whole
-    layers of the stack at M=1 (fp64, one host core)."""
+def host_cpu():
+    """(logical cores, CPU model name) of this host."""
+    model = None
+    try:
+        out = subprocess.run(["lscpu"], capture_output=True, text=True, timeout=10).stdout
+        for line in out.splitlines():
+            if line.lower().startswith("model name"):
+                model = line.split(":", 1)[1].strip()
+                break
+    except Exception:
+        pass
+    if model is None:
+        try:
+            for line in open("/proc/cpuinfo"):
+                if line.lower().startswith("model name"):
+                    model = line.split(":", 1)[1].strip()
+                    break
+        except Exception:
+            pass
+    return os.cpu_count(), model or "unknown"
+
+
+def _oracle_chain(shape, n_layers, t_budget, threads, dev=None):
+    """Whole chained layers of the a35b stack at M=1 through the oracle on
+    `threads` threads until `t_budget` seconds of oracle time are spent."""
     import numpy as np
     import torch
     import oracle
     import synth
-    t_budget = args.cpu_seconds
+    oracle.set_threads(threads)
     n_done, bytes_done, elapsed = 0, 0, 0.0
     x = synth.bf16_bits(synth.make_rows(shape, 5, 1)).numpy().view(np.uint16)
     l = 0
-    while elapsed < t_budget and l < args.layers:
-        L = synth.make_layer(shape, 1000 + l, device=dev if dev is not None else "cpu")
-        lay = oracle.Layer(L)
-        r = lay.route(x)
-        for e in set(int(v) for v in r["idx"].ravel()):
-            lay.expert(e)
-        del L
-        if dev is not None:
-            torch.cuda.empty_cache()
-        t0 = time.perf_counter()
-        res = lay.forward(x, normed=False)
-        elapsed += time.perf_counter() - t0
-        bytes_done += unique_bytes(shape, len(set(res["idx"].ravel().tolist())), 1)
-        n_done += 1
-        x = res["out"]
-        l += 1
-    return {"value": round(bytes_done / elapsed / 1e9, 6), "unit": "GB/s", "cores": 1, "kind": "oracle",
-            "sample": f"{n_done} chained layers of the a35b stack at M=1 ({elapsed:.1f} s of oracle time)",
-            "us_per_layer": round(elapsed / n_done * 1e6, 1)}
+    try:
+        while elapsed < t_budget and l < n_layers:
+            L = synth.make_layer(shape, 1000 + l, device=dev if dev is not None else "cpu")
+            lay = oracle.Layer(L)
+            r = lay.route(x)
+            for e in set(int(v) for v in r["idx"].ravel()):
+                lay.expert(e)
+            del L
+            if dev is not None:
+                torch.cuda.empty_cache()
+            t0 = time.perf_counter()
+            res = lay.forward(x, normed=False)
+            elapsed += time.perf_counter() - t0
+            bytes_done += unique_bytes(shape, len(set(res["idx"].ravel().tolist())), 1)
+            n_done += 1
+            x = res["out"]
+            l += 1
+    finally:
+        oracle.set_threads(1)
+    return n_done, bytes_done, elapsed
+
+
+def cpu_baseline(args, shape, dev=None):
+    """The oracle, as it stands, on a bounded sample of the workload: whole
+    chained layers of the stack at M=1 in fp64, first on one host core (the
+    parity reference), then with its mat-vec output rows spread over every
+    host core (OpenMP; the same bits)."""
+    import oracle
+    cores, model = host_cpu()
+    n1, b1, e1 = _oracle_chain(shape, args.layers, args.cpu_seconds * 2 / 3, 1, dev)
+    nthreads = oracle.max_threads()
+    nm, bm, em = _oracle_chain(shape, args.layers, args.cpu_seconds / 3, nthreads, dev)
+    return {"value": round(b1 / e1 / 1e9, 6), "unit": "GB/s", "cores": 1, "kind": "oracle",
+            "sample": f"{n1} chained layers of the a35b stack at M=1 ({e1:.1f} s of oracle time)",
+            "us_per_layer": round(e1 / n1 * 1e6, 1), "host_cores": cores, "cpu_model": model,
+            "all_cores": {"value": round(bm / em / 1e9, 6), "unit": "GB/s", "cores": nthreads,
+                          "sample": f"{nm} chained layers ({em:.1f} s of oracle time)",
+                          "us_per_layer": round(em / nm * 1e6, 1)}}
 
 
 def oracle_steps(shape, n_layers, steps, warmup, dev=None, prepared=4):

@@ -202,22 +202,40 @@ void moe_stack_destroy(moe_stack *stack);
  *
  * The scratch lives in a fixed array of MOE_NOALLOC_SCRATCH_BYTES of device
  * memory inside the library (every GPU that loads the library holds it
- * until the process exits).  Layers and row counts whose moe_workspace_size
- * exceeds it are rejected with MOE_ERR_BUFFER_TOO_SMALL before anything is
- * enqueued.  Inputs and outputs are as for moe_decode_layer.
+ * until the process exits).  The call always runs the persistent kernel in
+ * launches of one launch's rows (8 at H = 2048) and never grouped mode,
+ * whatever moe_set_grouped says; its bound is therefore that kernel's part
+ * of the workspace layout (moe_workspace_size without the grouped-mode
+ * regions, which only calls of more rows than one launch include).  Calls
+ * whose persistent-kernel layout exceeds the array are rejected with
+ * MOE_ERR_BUFFER_TOO_SMALL before anything is enqueued; so is every other
+ * argument error: a rejected call enqueues nothing.  Inputs and outputs are
+ * as for moe_decode_layer.
  *
  * - The first call on a device looks up the array's device address on that
- *   device (once); make that first call outside any stream capture.
- * - Each call clears the array's control block on `stream` before its
- *   kernels, so an earlier failed call does not affect it.
+ *   device (once, cudaGetSymbolAddress); make that first call outside any
+ *   stream capture.  The address is cached per device for the life of the
+ *   process; after cudaDeviceReset it is stale and the call must not be used.
+ * - Each accepted call clears the array's control block (status word,
+ *   barrier counters) on `stream` before its kernels, so an earlier failed
+ *   call does not affect it; the status word therefore describes the most
+ *   recent call only: read it with moe_noalloc_status before the next call.
  * - Every call on a device shares the one array: calls that can overlap on
  *   the GPU (different streams without ordering between them) race and give
  *   wrong results.  Order them on one stream.
  * - No device memory is allocated or freed by this call.
- * Errors: as moe_decode_layer, plus BUFFER_TOO_SMALL (scratch too small). */
+ * Errors: INVALID_ARG, UNSUPPORTED (shape, or a device index above 63),
+ * BUFFER_TOO_SMALL (scratch too small), CUDA; errors raised while the
+ * kernels run (a device wait that gave up) are read with moe_noalloc_status. */
 #define MOE_NOALLOC_SCRATCH_BYTES (4u << 20)
 int moe_decode_layer_noalloc(const moe_layer *layer, const uint16_t *x_dev, int M, uint16_t *out_dev,
                              uint16_t *out_normed_dev, moe_stream_t stream);
+
+/* Synchronises `stream` and returns the status of the latest
+ * moe_decode_layer_noalloc call on the current device: MOE_OK,
+ * MOE_ERR_TIMEOUT or MOE_ERR_DEVICE from the scratch array's status word
+ * (or MOE_ERR_CUDA).  The paper has no counterpart of this call either. */
+int moe_noalloc_status(moe_stream_t stream);
 
 /* Synchronises `stream` and returns MOE_OK, MOE_ERR_TIMEOUT or MOE_ERR_DEVICE
  * from the workspace status word (or MOE_ERR_CUDA). */

@@ -23,11 +23,17 @@ _lib = None
 
 
 def build(force: bool = False) -> str:
-    """Compile the oracle with gcc (host code only; no CUDA)."""
+    """Compile the oracle with gcc (host code only; no CUDA).  With OpenMP
+    when the compiler has it (the all-cores timing run); without, the oracle
+    runs on one thread."""
     if force or not os.path.exists(_LIB) or os.path.getmtime(_LIB) < os.path.getmtime(_SRC):
         tmp = _LIB + f".tmp{os.getpid()}"
-        subprocess.check_call(["gcc", "-O2", "-std=c11", "-Wall", "-Wextra", "-ffp-contract=off",
-                               "-fno-fast-math", "-fPIC", "-shared", "-o", tmp, _SRC, "-lm"])
+        base = ["gcc", "-O2", "-std=c11", "-Wall", "-Wextra", "-ffp-contract=off",
+                "-fno-fast-math", "-fPIC", "-shared", "-o", tmp, _SRC, "-lm"]
+        try:
+            subprocess.check_call(base[:1] + ["-fopenmp"] + base[1:], stderr=subprocess.DEVNULL)
+        except subprocess.CalledProcessError:
+            subprocess.check_call(base)
         os.replace(tmp, _LIB)
     return _LIB
 
@@ -58,6 +64,9 @@ def lib():
         _lib.oracle_weight.restype = C.c_double
         _lib.oracle_weight.argtypes = [C.POINTER(OqMatrix), C.c_int, C.c_int]
         _lib.oracle_layer.restype = C.c_int
+        _lib.oracle_set_threads.restype = None
+        _lib.oracle_set_threads.argtypes = [C.c_int]
+        _lib.oracle_max_threads.restype = C.c_int
         for name in ("oracle_pack_bits", "oracle_unpack_bits", "oracle_quantize_group",
                      "oracle_quantize_matrix", "oracle_rmsnorm", "oracle_topk",
                      "oracle_expert_ffn", "oracle_route"):
@@ -85,6 +94,17 @@ def _np(t, dtype=None):
         pass
     a = np.asarray(t)
     return np.ascontiguousarray(a if dtype is None else a.astype(dtype))
+
+
+def set_threads(n: int) -> None:
+    """Threads of the oracle's mat-vecs (1 = the parity reference; results
+    are the same bits for any count)."""
+    lib().oracle_set_threads(int(n))
+
+
+def max_threads() -> int:
+    """Host cores the oracle can use (1 when built without OpenMP)."""
+    return int(lib().oracle_max_threads())
 
 
 # ------------------------------------------------------------------ scalar ops

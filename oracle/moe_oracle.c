@@ -35,6 +35,9 @@
  * routines in fp64, brute force on tiny inputs).
  */
 #include <math.h>
+#ifdef _OPENMP
+#include <omp.h>
+#endif
 #include <stdint.h>
 #include <stdlib.h>
 #include <string.h>
@@ -172,9 +175,29 @@ static int matrix_present(const oq_matrix *m)
     return m->bits == 0 ? m->w != NULL : (m->codes && m->scales && m->biases);
 }
 
+/* Threads of the all-cores timing run (1 = the single-core parity
+ * reference).  Only the output rows of a mat-vec are spread over threads:
+ * each y[r] is still summed by one thread in column order, so any thread
+ * count gives the same bits. */
+static int g_threads = 1;
+
+void oracle_set_threads(int n) { g_threads = n < 1 ? 1 : n; }
+
+int oracle_max_threads(void)
+{
+#ifdef _OPENMP
+    return omp_get_num_procs();
+#else
+    return 1;
+#endif
+}
+
 /* y[r] = sum_c W[r, c] * x[c] */
 static void matvec(const oq_matrix *m, const double *x, double *y)
 {
+#ifdef _OPENMP
+#pragma omp parallel for num_threads(g_threads) if (g_threads > 1) schedule(static)
+#endif
     for (int r = 0; r < m->rows; ++r) {
         double acc = 0.0;
         for (int c = 0; c < m->cols; ++c) acc += oracle_weight(m, r, c) * x[c];

@@ -20,7 +20,7 @@ T_ROUTER, T_SGATE, T_GATE, T_UP, T_DOWN, T_SHARED_GATE, T_SHARED_UP, T_SHARED_DO
 SYMBOLS = ["moe_pack_size", "moe_pack_weights", "moe_layer_destroy", "moe_export_canonical",
            "moe_workspace_size", "moe_workspace_init", "moe_router_topk", "moe_decode_layer",
            "moe_stack_create", "moe_stack_forward", "moe_stack_forward_host", "moe_stack_destroy",
-           "moe_decode_layer_noalloc",
+           "moe_decode_layer_noalloc", "moe_noalloc_status",
            "moe_stream_status", "moe_debug_set", "moe_debug_trace", "moe_set_grouped", "moe_gate_up_tc", "moe_down_tc", "moe_status_str",
            "moe_last_cuda_error",
            "moe_selftest_host", "moe_launch_count"]
@@ -76,6 +76,7 @@ def lib():
             "moe_stack_forward_host": (i, [vp, vp, i, vp, vp, sz, vp]),
             "moe_stack_destroy": (None, [vp]),
             "moe_decode_layer_noalloc": (i, [vp, vp, i, vp, vp, vp]),
+            "moe_noalloc_status": (i, [vp]),
             "moe_stream_status": (i, [vp, sz, vp]),
             "moe_debug_set": (i, [i, C.c_longlong]),
             "moe_debug_trace": (i, [vp, sz]),

@@ -215,6 +215,12 @@ def decode_layer_noalloc(layer: Layer, x: torch.Tensor, out=None, normed: bool =
     return (out, on) if normed else out
 
 
+def noalloc_status(stream=None) -> int:
+    """moe_noalloc_status: synchronise and return the device status of the
+    latest decode_layer_noalloc call (0 = MOE_OK, 5 = a device wait gave up)."""
+    return int(lib().moe_noalloc_status(_stream(stream)))
+
+
 def selftest_host() -> int:
     """moe_selftest_host: violations found by the library's host-side checks
     (code tables, launch plans, workspace layouts); 0 when consistent."""

@@ -1,6 +1,7 @@
 // Host side of the C ABI declared in include/moe.h: argument checks,
 // blob/workspace layouts, row chunking and kernel launches.  No device
 // memory is allocated here.
+#include <atomic>
 #include <cstdio>
 #include <cstdlib>
 #include <cstring>
@@ -398,7 +399,8 @@ int moe_router_topk(const moe_layer *layer, const uint16_t *x_dev, int M, int32_
 namespace {
 
 int decode_layer_impl(const moe_layer *layer, const uint16_t *x_dev, int M, uint16_t *out_dev,
-                      uint16_t *out_normed_dev, void *ws_dev, size_t ws_bytes, moe_stream_t stream, bool allow_grouped)
+                      uint16_t *out_normed_dev, void *ws_dev, size_t ws_bytes, moe_stream_t stream, bool allow_grouped,
+                      bool clear_ctrl = false)
 {
     if (!x_dev || !out_dev || !aligned16(x_dev) || !aligned16(out_dev)) return MOE_ERR_INVALID_ARG;
     if (out_normed_dev && (!layer || !layer->ptrs.gamma_next)) return MOE_ERR_INVALID_ARG;
@@ -413,6 +415,18 @@ int decode_layer_impl(const moe_layer *layer, const uint16_t *x_dev, int M, uint
     kp.L = 1;
     kp.layer[0] = layer->ptrs;
     const int H = kp.g.H;
+    // every launch plan is made before anything is enqueued, so a call that
+    // fails its checks leaves the stream untouched
+    const int tail = M % R;
+    {
+        KParams probe = kp;
+        if ((rc = plan_for(probe, M < R ? M : R))) return rc;
+        if (tail && M > R && (rc = plan_for(probe, tail))) return rc;
+    }
+    if (clear_ctrl) {
+        cudaError_t e = cudaMemsetAsync(ws_dev, 0, kCtrlBytes, reinterpret_cast<cudaStream_t>(stream));
+        if (e != cudaSuccess) { note_cuda_error((int)e); return MOE_ERR_CUDA; }
+    }
     for (int c0 = 0; c0 < M; c0 += R) {
         const int mc = M - c0 < R ? M - c0 : R;
         if ((rc = plan_for(kp, mc))) return rc;
@@ -527,21 +541,25 @@ namespace {
 // runtime; the kernels get the device address looked up below.
 static __device__ __align__(256) uint8_t g_noalloc_scratch[MOE_NOALLOC_SCRATCH_BYTES];
 
-void *g_noalloc_ptr[64];
+constexpr int kMaxDevices = 64;
+std::atomic<void *> g_noalloc_ptr[kMaxDevices];
 
-// Device address of the array on the current device, looked up once per device.
+// Device address of the array on the current device, looked up once per
+// device (several host threads may look it up at once: they all store the
+// same address).
 int noalloc_scratch(void **out)
 {
     int dev = 0;
     cudaError_t e = cudaGetDevice(&dev);
-    if (e != cudaSuccess || dev < 0 || dev >= 64) { note_cuda_error((int)e); return MOE_ERR_CUDA; }
-    if (!g_noalloc_ptr[dev]) {
-        void *p = nullptr;
+    if (e != cudaSuccess) { note_cuda_error((int)e); return MOE_ERR_CUDA; }
+    if (dev < 0 || dev >= kMaxDevices) return MOE_ERR_UNSUPPORTED;
+    void *p = g_noalloc_ptr[dev].load(std::memory_order_acquire);
+    if (!p) {
         e = cudaGetSymbolAddress(&p, g_noalloc_scratch);
         if (e != cudaSuccess || !p) { note_cuda_error((int)e); return MOE_ERR_CUDA; }
-        g_noalloc_ptr[dev] = p;
+        g_noalloc_ptr[dev].store(p, std::memory_order_release);
     }
-    *out = g_noalloc_ptr[dev];
+    *out = p;
     return MOE_OK;
 }
 
@@ -552,18 +570,26 @@ extern "C" {
 int moe_decode_layer_noalloc(const moe_layer *layer, const uint16_t *x_dev, int M, uint16_t *out_dev,
                              uint16_t *out_normed_dev, moe_stream_t stream)
 {
-    if (!layer || M < 1) return MOE_ERR_INVALID_ARG;
+    if (!layer || M < 1 || !x_dev || !out_dev || !aligned16(x_dev) || !aligned16(out_dev)) return MOE_ERR_INVALID_ARG;
+    if (out_normed_dev && !layer->ptrs.gamma_next) return MOE_ERR_INVALID_ARG;
     WsLayout w;
     make_ws_layout_fma(layer->geo, M, w);   // the scratch array holds no grouped-mode regions
     if (w.total > (size_t)MOE_NOALLOC_SCRATCH_BYTES) return MOE_ERR_BUFFER_TOO_SMALL;
     void *ws = nullptr;
     int rc = noalloc_scratch(&ws);
     if (rc) return rc;
-    // the control block (barrier counters, status, ready counters) starts at zero
-    cudaError_t e = cudaMemsetAsync(ws, 0, kCtrlBytes, reinterpret_cast<cudaStream_t>(stream));
-    if (e != cudaSuccess) { note_cuda_error((int)e); return MOE_ERR_CUDA; }
+    // the control block (barrier counters, status word) is cleared on the
+    // stream once every check has passed, just before the first launch
     return decode_layer_impl(layer, x_dev, M, out_dev, out_normed_dev, ws, (size_t)MOE_NOALLOC_SCRATCH_BYTES, stream,
-                             false);
+                             false, true);
+}
+
+int moe_noalloc_status(moe_stream_t stream)
+{
+    void *ws = nullptr;
+    int rc = noalloc_scratch(&ws);
+    if (rc) return rc;
+    return moe_stream_status(ws, (size_t)MOE_NOALLOC_SCRATCH_BYTES, stream);
 }
 
 int moe_set_grouped(int min_rows)

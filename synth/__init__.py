@@ -16,9 +16,17 @@ hidden 4096, ~6.75 MB per 4-bit expert):
 
 Value recipe (one reading of the workload description):
   * expert codes uniform in [0, 2^b - 1];
-  * per-group scale |N(0, 0.02)| * 15 / (2^b - 1), bias N(0, 0.01), both
-    rounded to bf16 (the 15/(2^b-1) factor keeps the dequantised weight
-    distribution of the 4-bit case at every width);
+  * per-group scale |N(0, 0.02)| * 15 / (2^b - 1), both rounded to bf16 (the
+    15/(2^b-1) factor keeps the dequantised weight distribution of the 4-bit
+    case at every width);
+  * per-group bias N(0, 0.01) taken relative to the centre of the code grid:
+    b = N(0, 0.01) - s (2^b - 1) / 2, so that the dequantised weights q s + b
+    have mean zero as in an affine-quantised checkpoint, where the bias is the
+    group's minimum (grid="centred", the default).  grid="literal" draws
+    b = N(0, 0.01) as written; then every matrix carries a positive mean of
+    about 7.5 E[s] = 0.12, and a stack of layers amplifies that one direction
+    (the residual stream grows from rms 1 to ~1e7 within four 35B-A3B layers
+    and every token row routes to the same experts);
   * router and shared-gate vector fp32 N(0, 0.05) (quantised to 8 bits by the
     library's packer where the workload asks for an 8-bit router);
   * x bf16 N(0, 1); RMSNorm weights 1 + N(0, 0.1) in bf16;
@@ -80,15 +88,23 @@ def _scales(g, shape, bits, device):
     return s.to(torch.bfloat16)
 
 
-def _biases(g, shape, device):
-    return (torch.randn(shape, generator=g, device=device, dtype=torch.float32) * 0.01).to(torch.bfloat16)
+def _biases(g, shape, device, scales=None, bits=0):
+    b = torch.randn(shape, generator=g, device=device, dtype=torch.float32) * 0.01
+    if scales is not None:
+        b -= scales.float() * (((1 << bits) - 1) / 2.0)
+    return b.to(torch.bfloat16)
 
 
-def quant_matrix(g, rows_shape, K, bits, device):
+GRIDS = ("centred", "literal")
+
+
+def quant_matrix(g, rows_shape, K, bits, device, grid="centred"):
     """Canonical quantised matrix: codes u8 [..., K], scales/biases bf16 [..., K/64]."""
+    assert grid in GRIDS
     codes = _codes(g, tuple(rows_shape) + (K,), bits, device)
     scales = _scales(g, tuple(rows_shape) + (K // 64,), bits, device)
-    biases = _biases(g, tuple(rows_shape) + (K // 64,), device)
+    biases = _biases(g, tuple(rows_shape) + (K // 64,), device,
+                     scales if grid == "centred" else None, bits)
     return {"codes": codes, "scales": scales, "biases": biases, "bits": bits}
 
 
@@ -107,8 +123,9 @@ def zipf_direction(shape: LayerShape, seed: int):
     return u, c
 
 
-def make_layer(shape: LayerShape, seed: int, device="cpu") -> dict:
-    """Canonical weights of one layer (torch tensors on `device`).
+def make_layer(shape: LayerShape, seed: int, device="cpu", grid="centred") -> dict:
+    """Canonical weights of one layer (torch tensors on `device`); `grid`
+    chooses the bias distribution (see the module docstring).
 
     Keys: gate/up [E, I, H], down [E, H, I] (each a dict of codes/scales/biases),
     shared_gate/shared_up [I_s, H], shared_down [H, I_s] (when present),
@@ -117,15 +134,15 @@ def make_layer(shape: LayerShape, seed: int, device="cpu") -> dict:
     """
     g = _gen(seed, device)
     H, I, E = shape.H, shape.I, shape.E
-    L = {"shape": shape, "seed": seed}
-    L["gate"] = quant_matrix(g, (E, I), H, shape.routed_bits, device)
-    L["up"] = quant_matrix(g, (E, I), H, shape.routed_bits, device)
-    L["down"] = quant_matrix(g, (E, H), I, shape.routed_bits, device)
+    L = {"shape": shape, "seed": seed, "grid": grid}
+    L["gate"] = quant_matrix(g, (E, I), H, shape.routed_bits, device, grid)
+    L["up"] = quant_matrix(g, (E, I), H, shape.routed_bits, device, grid)
+    L["down"] = quant_matrix(g, (E, H), I, shape.routed_bits, device, grid)
     if shape.has_shared:
         Is = shape.I_shared
-        L["shared_gate"] = quant_matrix(g, (Is,), H, shape.shared_bits, device)
-        L["shared_up"] = quant_matrix(g, (Is,), H, shape.shared_bits, device)
-        L["shared_down"] = quant_matrix(g, (H,), Is, shape.shared_bits, device)
+        L["shared_gate"] = quant_matrix(g, (Is,), H, shape.shared_bits, device, grid)
+        L["shared_up"] = quant_matrix(g, (Is,), H, shape.shared_bits, device, grid)
+        L["shared_down"] = quant_matrix(g, (H,), Is, shape.shared_bits, device, grid)
     router = torch.randn((E, H), generator=g, device=device, dtype=torch.float32) * 0.05
     if shape.zipf:
         u, c = zipf_direction(shape, 0)

@@ -59,3 +59,44 @@ def assert_close(got: np.ndarray, ref: np.ndarray, what: str):
 
 def bf16_tensor_to_f64(t: torch.Tensor) -> np.ndarray:
     return t.detach().float().cpu().numpy().astype(np.float64)
+
+
+def teacher_forced(moe, layers, lays, x, ws, label: str, dev="cuda", min_frac: float = 0.75,
+                   normed_last: bool = True):
+    """Runs the layers one call at a time from x and compares every layer with
+    the oracle on the GPU's own bf16 input of that layer (teacher-forced).
+    Rows whose oracle top-k margin is below MARGIN are counted and not
+    compared (the GPU may then pick the other expert of a near tie); every
+    other row must have bit-exact expert ids and outputs within the
+    tolerance.  Fails if fewer than `min_frac` of all (layer, row) pairs
+    were compared.  Returns (outputs of each layer, compared, skipped)."""
+    M = x.shape[0]
+    h = x.to(dev)
+    outs = []
+    compared = skipped = 0
+    for i, (lyr, lay) in enumerate(zip(layers, lays)):
+        last = normed_last and i == len(layers) - 1
+        ref = lay.forward(bits_np(h), normed=last)
+        idx, _ = moe.router_topk(lyr, h, ws)
+        if last:
+            nxt, on = moe.decode_layer(lyr, h, ws, normed=True)
+        else:
+            nxt = moe.decode_layer(lyr, h, ws)
+        assert ws.status() == 0
+        idx = idx.cpu().numpy()
+        got = bf16_tensor_to_f64(nxt)
+        for m in range(M):
+            if ref["margin"][m] < MARGIN:
+                skipped += 1
+                continue
+            compared += 1
+            assert np.array_equal(idx[m], ref["idx"][m]), f"{label} layer {i} row {m}: expert ids differ"
+            assert_close(got[m], ref["o"][m], f"{label} layer {i} row {m} out")
+            if last:
+                assert_close(bf16_tensor_to_f64(on)[m], ref["on"][m], f"{label} layer {i} row {m} out_normed")
+        outs.append(nxt)
+        h = nxt
+    total = compared + skipped
+    print(f"{label}: {compared} of {total} (layer, row) pairs compared, {skipped} below the routing margin")
+    assert compared >= min_frac * total, f"{label}: only {compared} of {total} pairs above the routing margin"
+    return outs, compared, skipped

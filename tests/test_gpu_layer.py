@@ -13,7 +13,7 @@ import synth
 import quantized_moe_decode_layer_gb300 as moe
 from quantized_moe_decode_layer_gb300 import _lib
 
-from helpers import MARGIN, assert_close, bf16_tensor_to_f64, bits_np, rows_with_margin, to_device
+from helpers import MARGIN, assert_close, bf16_tensor_to_f64, bits_np, rows_with_margin, teacher_forced, to_device
 
 pytestmark = pytest.mark.gpu
 DEV = "cuda"
@@ -134,28 +134,48 @@ def test_a35b_m1():
     check_layer(shape, L, layer, lay, x)
 
 
+def rows_equal_one_row_calls(layer, x, out):
+    """Each row of an M-row call is bitwise the one-row call of that row."""
+    ws = moe.Workspace(layer.desc, 1)
+    for m in range(x.shape[0]):
+        o1 = moe.decode_layer(layer, x[m:m + 1].to(DEV), ws)
+        assert torch.equal(o1.view(torch.int16), out[m:m + 1].view(torch.int16)), f"row {m}"
+    assert ws.status() == 0
+
+
 def test_a35b_m4_rows_equal_m1_bitwise():
     """1 token + 3 correlated draft rows: every row equals the one-row call bit
-    for bit (PureDrive model card, "How it works": row-exact verify)."""
+    for bit (PureDrive model card, "How it works": row-exact verify), and the
+    rows share 30-60 % of their experts (the M=4 workload's correlation)."""
     shape = synth.A35B
     L, layer, lay = cached(shape, 11)
-    x = rows_with_margin(shape, lay, 2, 4, correlation=0.6, gamma=L["gamma"])
+    x = rows_with_margin(shape, lay, 3, 4, correlation=0.6, gamma=L["gamma"])
     out4, ref = check_layer(shape, L, layer, lay, x)
-    ws = moe.Workspace(layer.desc, 1)
-    for m in range(4):
-        o1 = moe.decode_layer(layer, x[m:m + 1].to(DEV), ws)
-        assert torch.equal(o1.view(torch.int16), out4[m:m + 1].view(torch.int16))
-    # experts chosen by two or more rows
+    rows_equal_one_row_calls(layer, x, out4)
+    # experts chosen by two or more rows, as a fraction of the distinct experts
     idx = ref["idx"]
     union = set(idx.ravel().tolist())
     shared = sum(1 for e in union if (idx == e).any(axis=1).sum() >= 2)
-    assert shared >= 1
+    assert 0.3 <= shared / len(union) <= 0.6, (shared, len(union))
 
 
 def test_a35b_m8():
+    """8 rows in one launch: parity, and every row bitwise the one-row call."""
     shape = synth.A35B
     L, layer, lay = cached(shape, 11)
     x = rows_with_margin(shape, lay, 3, 8, correlation=0.5, gamma=L["gamma"])
+    out, _ = check_layer(shape, L, layer, lay, x)
+    rows_equal_one_row_calls(layer, x, out)
+
+
+def test_tiny_literal_grid():
+    """The workload's bias distribution taken literally (b ~ N(0, 0.01), so
+    every dequantised matrix has a positive mean): parity holds as well."""
+    shape = synth.TINY
+    L = synth.make_layer(shape, 8, device=DEV, grid="literal")
+    layer = moe.Layer(moe.desc_from_shape(shape), moe.layer_src_from_synth(L))
+    lay = oracle.Layer(L)
+    x = rows_with_margin(shape, lay, 108, 3)
     check_layer(shape, L, layer, lay, x)
 
 
@@ -199,11 +219,14 @@ def test_tiny_m40_two_groups():
 
 
 def test_a35b_m32_fma_chunks(fma_only):
-    """32 rows with grouped mode off: four 8-row launches of the FMA path."""
+    """32 rows with grouped mode off: four 8-row launches of the FMA path;
+    every row is bitwise the one-row call (the mode a row-exact verify with
+    more than 8 rows uses)."""
     shape = synth.A35B
     L, layer, lay = cached(shape, 11)
     x = rows_with_margin(shape, lay, 5, 32, gamma=L["gamma"])
-    check_layer(shape, L, layer, lay, x)
+    out, _ = check_layer(shape, L, layer, lay, x)
+    rows_equal_one_row_calls(layer, x, out)
 
 
 def test_grouped_stack_equals_chained_layers(grouped_always):
@@ -227,13 +250,7 @@ def test_grouped_stack_equals_chained_layers(grouped_always):
             h = moe.decode_layer(lyr, h, ws)
     assert torch.equal(h.view(torch.int16), out.view(torch.int16))
     assert torch.equal(hn.view(torch.int16), on.view(torch.int16))
-    h = x.to(DEV)
-    for i, (lyr, lay) in enumerate(zip(layers, lays)):
-        ref = lay.forward(bits_np(h), normed=True)
-        nxt = moe.decode_layer(lyr, h, ws)
-        if ref["margin"].min() >= 1e-3:
-            assert_close(bf16_tensor_to_f64(nxt), ref["o"], f"grouped stack layer {i}")
-        h = nxt
+    teacher_forced(moe, layers, lays, x, ws, "tiny grouped stack M=12")
 
 
 def test_b397_m1():
@@ -286,13 +303,7 @@ def test_stack_equals_chained_layers_and_oracle():
     assert torch.equal(h.view(torch.int16), out.view(torch.int16))
     assert torch.equal(hn.view(torch.int16), on.view(torch.int16))
     # teacher-forced oracle: layer l on the GPU's bf16 input of layer l
-    h = x.to(DEV)
-    for i, (lyr, lay) in enumerate(zip(layers, lays)):
-        ref = lay.forward(bits_np(h), normed=True)
-        nxt = moe.decode_layer(lyr, h, ws)
-        if ref["margin"].min() >= 1e-3:
-            assert_close(bf16_tensor_to_f64(nxt), ref["o"], f"stack layer {i}")
-        h = nxt
+    teacher_forced(moe, layers, lays, x, ws, "tiny stack M=2")
 
 
 def test_stack_host_buffers():

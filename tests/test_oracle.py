@@ -321,3 +321,21 @@ def test_expert_relabelling_invariance():
     Q["down"] = L["down"]
     rq = oracle.Layer(Q).forward(xb)
     assert not np.allclose(rq["o"], r["o"], rtol=1e-6, atol=1e-9)
+
+
+def test_threads_give_the_same_bits():
+    """The all-cores oracle (mat-vec output rows over threads) equals the
+    single-core oracle bit for bit."""
+    L = synth.make_layer(synth.TINY, 41)
+    lay = oracle.Layer(L)
+    xb = synth.bf16_bits(synth.make_rows(synth.TINY, 42, 3)).numpy().view(np.uint16)
+    one = lay.forward(xb)
+    try:
+        oracle.set_threads(max(2, oracle.max_threads()))
+        many = lay.forward(xb)
+    finally:
+        oracle.set_threads(1)
+    for key in ("o", "on", "logits", "w", "sigma"):
+        assert np.array_equal(one[key], many[key]), key
+    for key in ("out", "out_n", "idx"):
+        assert np.array_equal(one[key], many[key]), key

@@ -53,9 +53,48 @@ def test_noalloc_matches_workspace_entry_point(shape, M):
     assert ws.status() == 0
     for _ in range(2):   # two calls in a row share the same scratch array
         out, on = call_noalloc(layer, x, normed=True)
-        torch.cuda.synchronize()
+        assert moe.noalloc_status() == 0
         close(out, ref, f"{shape.name} M={M} out")
         close(on, ref_n, f"{shape.name} M={M} out_normed")
+        # the same kernel with the same summation order: the bits agree too
+        assert torch.equal(out.view(torch.int16), ref.view(torch.int16))
+        assert torch.equal(on.view(torch.int16), ref_n.view(torch.int16))
+
+
+def test_noalloc_python_wrapper():
+    """The binding's decode_layer_noalloc gives the workspace call's result."""
+    shape = synth.A35B
+    L = synth.make_layer(shape, 64, device=DEV)
+    layer = moe.Layer(moe.desc_from_shape(shape), moe.layer_src_from_synth(L))
+    x = synth.make_rows(shape, 65, 2, gamma=L["gamma"], correlation=0.5).to(DEV)
+    ws = moe.Workspace(layer.desc, 2)
+    ref, ref_n = moe.decode_layer(layer, x, ws, normed=True)
+    out, on = moe.decode_layer_noalloc(layer, x, normed=True)
+    assert moe.noalloc_status() == 0
+    assert torch.equal(out.view(torch.int16), ref.view(torch.int16))
+    assert torch.equal(on.view(torch.int16), ref_n.view(torch.int16))
+
+
+def test_noalloc_reports_a_device_timeout():
+    """A device wait that runs out inside the no-alloc call is reported by
+    moe_noalloc_status (the router logit of one expert is left unpublished
+    through the debug switch, so every CTA's wait for it gives up after 50
+    ms); the next call starts clean and gives the right result again."""
+    shape = synth.TINY
+    L = synth.make_layer(shape, 66, device=DEV)
+    layer = moe.Layer(moe.desc_from_shape(shape), moe.layer_src_from_synth(L))
+    x = synth.make_rows(shape, 67, 1).to(DEV)
+    good, _ = call_noalloc(layer, x, normed=False)
+    assert moe.noalloc_status() == 0
+    try:
+        moe.debug_set(skip_row=3, timeout_ns=50_000_000)
+        call_noalloc(layer, x, normed=False)
+        assert moe.noalloc_status() == 5   # MOE_ERR_TIMEOUT
+    finally:
+        moe.debug_set(-1, 0)
+    again, _ = call_noalloc(layer, x, normed=False)
+    assert moe.noalloc_status() == 0
+    assert torch.equal(again.view(torch.int16), good.view(torch.int16))
 
 
 def test_noalloc_rejects_rows_beyond_the_scratch():

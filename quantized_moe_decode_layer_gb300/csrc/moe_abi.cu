@@ -3,6 +3,7 @@
 // memory is allocated here.
 #include <atomic>
 #include <cstdio>
+#include <mutex>
 #include <cstdlib>
 #include <cstring>
 
@@ -105,7 +106,6 @@ void make_ws_layout(const Geo &g, int max_M, WsLayout &w)
     w.off_act = put((size_t)w.max_slots * R * g.I * 8);
     w.off_act_s = put((size_t)R * (g.Is ? g.Is : 1) * 8);
     w.off_ping = put((size_t)2 * R * (g.H / 2) * 8);
-    w.off_y = put((size_t)R * g.k * g.H * 8);
     w.off_stage_in = put((size_t)max_M * g.H * 2);
     w.off_stage_out = put((size_t)max_M * g.H * 2);
     w.grp_rows = w.grp_slots = 0;
@@ -202,7 +202,7 @@ int plan_selftest_host()
         const int R = rows_per_launch(g.H);
         int maxi = 2 * g.g_bytes;
         if (g.d_bytes > maxi) maxi = g.d_bytes;
-        if (g.sg_bytes > maxi) maxi = g.sg_bytes;
+        if (2 * g.sg_bytes > maxi) maxi = 2 * g.sg_bytes;
         if (g.sd_bytes > maxi) maxi = g.sd_bytes;
         for (int sms : sm_counts)
             for (int mc = 1; mc <= R; ++mc) {
@@ -253,7 +253,6 @@ int ws_layout_selftest_host()
                 {w.off_act, (size_t)w.max_slots * R * g.I * 8},
                 {w.off_act_s, (size_t)R * Is * 8},
                 {w.off_ping, (size_t)2 * R * (g.H / 2) * 8},
-                {w.off_y, (size_t)R * g.k * g.H * 8},
                 {w.off_stage_in, (size_t)M * g.H * 2},
                 {w.off_stage_out, (size_t)M * g.H * 2},
             };
@@ -368,7 +367,9 @@ int moe_workspace_size(const moe_layer_desc *desc, int max_M, size_t *ws_bytes)
 int moe_workspace_init(void *ws_dev, size_t ws_bytes, moe_stream_t stream)
 {
     if (!ws_dev || ws_bytes < (size_t)kCtrlBytes) return MOE_ERR_INVALID_ARG;
-    cudaError_t e = cudaMemsetAsync(ws_dev, 0, kCtrlBytes, reinterpret_cast<cudaStream_t>(stream));
+    // the whole workspace: the control block (launch sequence, status) and
+    // every exchanged word (tag 0 is never a launch's tag)
+    cudaError_t e = cudaMemsetAsync(ws_dev, 0, ws_bytes, reinterpret_cast<cudaStream_t>(stream));
     if (e != cudaSuccess) { note_cuda_error((int)e); return MOE_ERR_CUDA; }
     return MOE_OK;
 }
@@ -400,7 +401,7 @@ namespace {
 
 int decode_layer_impl(const moe_layer *layer, const uint16_t *x_dev, int M, uint16_t *out_dev,
                       uint16_t *out_normed_dev, void *ws_dev, size_t ws_bytes, moe_stream_t stream, bool allow_grouped,
-                      bool clear_ctrl = false)
+                      bool clear_status = false)
 {
     if (!x_dev || !out_dev || !aligned16(x_dev) || !aligned16(out_dev)) return MOE_ERR_INVALID_ARG;
     if (out_normed_dev && (!layer || !layer->ptrs.gamma_next)) return MOE_ERR_INVALID_ARG;
@@ -423,8 +424,9 @@ int decode_layer_impl(const moe_layer *layer, const uint16_t *x_dev, int M, uint
         if ((rc = plan_for(probe, M < R ? M : R))) return rc;
         if (tail && M > R && (rc = plan_for(probe, tail))) return rc;
     }
-    if (clear_ctrl) {
-        cudaError_t e = cudaMemsetAsync(ws_dev, 0, kCtrlBytes, reinterpret_cast<cudaStream_t>(stream));
+    if (clear_status) {
+        cudaError_t e = cudaMemsetAsync(static_cast<uint8_t *>(ws_dev) + offsetof(Ctrl, status), 0, 2 * sizeof(int),
+                                        reinterpret_cast<cudaStream_t>(stream));
         if (e != cudaSuccess) { note_cuda_error((int)e); return MOE_ERR_CUDA; }
     }
     for (int c0 = 0; c0 < M; c0 += R) {
@@ -543,11 +545,12 @@ static __device__ __align__(256) uint8_t g_noalloc_scratch[MOE_NOALLOC_SCRATCH_B
 
 constexpr int kMaxDevices = 64;
 std::atomic<void *> g_noalloc_ptr[kMaxDevices];
+std::mutex g_noalloc_mu;
 
 // Device address of the array on the current device, looked up once per
-// device (several host threads may look it up at once: they all store the
-// same address).
-int noalloc_scratch(void **out)
+// device; the first lookup also zeroes the whole array on `stream` (the
+// launch sequence, the status word and every exchanged word start at zero).
+int noalloc_scratch(void **out, cudaStream_t stream)
 {
     int dev = 0;
     cudaError_t e = cudaGetDevice(&dev);
@@ -555,9 +558,15 @@ int noalloc_scratch(void **out)
     if (dev < 0 || dev >= kMaxDevices) return MOE_ERR_UNSUPPORTED;
     void *p = g_noalloc_ptr[dev].load(std::memory_order_acquire);
     if (!p) {
-        e = cudaGetSymbolAddress(&p, g_noalloc_scratch);
-        if (e != cudaSuccess || !p) { note_cuda_error((int)e); return MOE_ERR_CUDA; }
-        g_noalloc_ptr[dev].store(p, std::memory_order_release);
+        std::lock_guard<std::mutex> lock(g_noalloc_mu);
+        p = g_noalloc_ptr[dev].load(std::memory_order_acquire);
+        if (!p) {
+            e = cudaGetSymbolAddress(&p, g_noalloc_scratch);
+            if (e != cudaSuccess || !p) { note_cuda_error((int)e); return MOE_ERR_CUDA; }
+            e = cudaMemsetAsync(p, 0, MOE_NOALLOC_SCRATCH_BYTES, stream);
+            if (e != cudaSuccess) { note_cuda_error((int)e); return MOE_ERR_CUDA; }
+            g_noalloc_ptr[dev].store(p, std::memory_order_release);
+        }
     }
     *out = p;
     return MOE_OK;
@@ -576,10 +585,10 @@ int moe_decode_layer_noalloc(const moe_layer *layer, const uint16_t *x_dev, int 
     make_ws_layout_fma(layer->geo, M, w);   // the scratch array holds no grouped-mode regions
     if (w.total > (size_t)MOE_NOALLOC_SCRATCH_BYTES) return MOE_ERR_BUFFER_TOO_SMALL;
     void *ws = nullptr;
-    int rc = noalloc_scratch(&ws);
+    int rc = noalloc_scratch(&ws, reinterpret_cast<cudaStream_t>(stream));
     if (rc) return rc;
-    // the control block (barrier counters, status word) is cleared on the
-    // stream once every check has passed, just before the first launch
+    // the status word is cleared on the stream once every check has passed,
+    // just before the first launch
     return decode_layer_impl(layer, x_dev, M, out_dev, out_normed_dev, ws, (size_t)MOE_NOALLOC_SCRATCH_BYTES, stream,
                              false, true);
 }
@@ -587,7 +596,7 @@ int moe_decode_layer_noalloc(const moe_layer *layer, const uint16_t *x_dev, int 
 int moe_noalloc_status(moe_stream_t stream)
 {
     void *ws = nullptr;
-    int rc = noalloc_scratch(&ws);
+    int rc = noalloc_scratch(&ws, reinterpret_cast<cudaStream_t>(stream));
     if (rc) return rc;
     return moe_stream_status(ws, (size_t)MOE_NOALLOC_SCRATCH_BYTES, stream);
 }

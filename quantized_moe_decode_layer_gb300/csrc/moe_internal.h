@@ -70,7 +70,7 @@ struct LayerPtrs {
 struct WsLayout {
     int maxr;                // rows per launch
     int max_slots;           // distinct routed experts per launch
-    size_t off_logits, off_act, off_act_s, off_ping, off_y, off_stage_in, off_stage_out, total;
+    size_t off_logits, off_act, off_act_s, off_ping, off_stage_in, off_stage_out, total;
     int max_M;               // rows the host-staging area holds
     // Grouped mode (M above maxr: the tensor-core expert path), sized for
     // grp_rows = min(max_M, kGroupRows) rows and grp_slots = min(E, grp_rows k)
@@ -83,14 +83,19 @@ struct WsLayout {
 constexpr int kGroupRows = 32;      // token rows of one grouped pass (mask width)
 
 struct Ctrl {                // first kCtrlBytes of the workspace
-    unsigned count;          // grid-barrier arrivals since the launch began (reset at its end)
+    unsigned count;          // unused (kept zero)
     unsigned pad0[31];
-    unsigned exit;           // CTAs finished with their barriers (own 128-byte line)
+    unsigned exit;           // CTAs of the running launch that have finished (own 128-byte line)
     unsigned pad1[31];
     int status;              // kStatus* bits
     int where;               // debug: which wait gave up
-    int pad2[62];
+    int pad2[30];
+    unsigned seq;            // launches completed on this workspace (mod kSeqWrap): the tag range
+    unsigned pad3[31];       // of a launch is seq * 64 + 1 .. seq * 64 + 64
 };
+// seq wraps before seq * 64 + 64 passes 2^32; the launch that wraps clears
+// every tagged word of the workspace first, so no earlier word can match.
+constexpr unsigned kSeqWrap = 1u << 26;
 static_assert(sizeof(Ctrl) <= kCtrlBytes, "control block");
 
 // Launch plan of the persistent kernel.
@@ -100,7 +105,7 @@ struct Plan {
     int NS;                  // ring stages
     int maxr;                // rows per launch
     int max_slots;
-    int hrows;               // output rows per CTA (upper bound)
+    int hrows;               // output rows per CTA (upper bound, even)
     int pb_bytes;            // prefetch buffer (gamma, router rows, shared units of a layer)
     int act_pairs;           // (slot, row) activation vectors the staging buffer holds
     int smem_bytes;
@@ -124,7 +129,6 @@ struct KParams {
     WsLayout ws_l;
     long long timeout_ns;
     int skip_row;            // debug: router logit row left unpublished in layer 0 (-1 = none)
-    unsigned epoch;          // tags of this launch: epoch + layer + 1 (set at launch)
     unsigned long long *trace;   // optional per-CTA phase timestamps (ns), NULL = off
 };
 

@@ -46,13 +46,8 @@
 // only on the row itself, so row m of an M-row call equals a 1-row call.
 #include <cuda_bf16.h>
 
-#include <unistd.h>
-
-#include <atomic>
 #include <cfloat>
-#include <chrono>
 #include <climits>
-#include <mutex>
 
 #include "moe_internal.h"
 #include "moe_unpack.cuh"
@@ -87,7 +82,7 @@ constexpr int kShBytes = 512;
 
 struct SmemLayout {
     int shs, cplan, bar, flags, slot_e, slot_mask, slot_rowbase, sigma, eslot, emask, topv, tope, topw;
-    int row_w, row_pair, red, lscr, p1v, pair_src, xs, xsum, act, asum, ysh, pb, ring, total;
+    int row_w, row_pair, red, lscr, pair_src, xs, xsum, act, asum, ysh, yl, pb, ring, total;
 };
 
 __host__ __device__ inline int take(int &o, int bytes, int align)
@@ -125,13 +120,13 @@ __host__ __device__ inline SmemLayout carve(const Geo &g, const Plan &p)
     L.row_pair = take(o, kMaxRows * kMaxK * 4, 4);
     L.red = take(o, kMaxRows * (NCW + 1) * 4, 4);
     L.lscr = take(o, NCW * kMaxRows * 4, 4);
-    L.p1v = take(o, 2 * per_cta(g.Is > 0 ? g.Is : 1, p.P) * p.maxr * 4, 4);
     L.pair_src = take(o, p.act_pairs * 4, 4);
     L.xs = take(o, p.maxr * g.H * 4, 16);
     L.xsum = take(o, p.maxr * (g.H / kGroup) * 4, 16);
     L.act = take(o, p.act_pairs * Im * 4, 16);
     L.asum = take(o, p.act_pairs * (Im / kGroup) * 4, 16);
     L.ysh = take(o, p.hrows * kMaxRows * 4, 16);
+    L.yl = take(o, p.maxr * g.k * p.hrows * 4, 16);
     L.pb = take(o, p.pb_bytes, 128);
     L.ring = take(o, p.NS * p.S, 128);
     L.total = o;
@@ -242,23 +237,11 @@ __device__ __forceinline__ bool cbar_or(bool v)
 
 __device__ __forceinline__ void cbar() { asm volatile("bar.sync 1, %0;" ::"n"(NCT) : "memory"); }
 
-__device__ __forceinline__ void red_release_add(unsigned *p, unsigned v)
-{
-    asm volatile("red.release.gpu.global.add.u32 [%0], %1;" ::"l"(p), "r"(v) : "memory");
-}
-
 __device__ __forceinline__ unsigned atom_add_acqrel(unsigned *p, unsigned v)
 {
     unsigned old;
     asm volatile("atom.add.acq_rel.gpu.global.u32 %0, [%1], %2;" : "=r"(old) : "l"(p), "r"(v) : "memory");
     return old;
-}
-
-__device__ __forceinline__ unsigned ld_acquire(const unsigned *p)
-{
-    unsigned v;
-    asm volatile("ld.acquire.gpu.global.u32 %0, [%1];" : "=r"(v) : "l"(p) : "memory");
-    return v;
 }
 
 __device__ __forceinline__ void st_relaxed(unsigned *p, unsigned v)
@@ -270,7 +253,6 @@ __device__ __forceinline__ void st_relaxed(unsigned *p, unsigned v)
 // the 32-bit tag of the layer that wrote it, stored and loaded as one
 // 64-bit access.  A reader that sees its own layer's tag has the value; no
 // separate flag, counter or barrier is needed to publish data between CTAs.
-__device__ __forceinline__ unsigned layer_tag(const KParams &kp, int l) { return kp.epoch + (unsigned)l + 1u; }
 
 __device__ __forceinline__ void st_tag(uint64_t *p, uint32_t payload, unsigned tag)
 {
@@ -342,20 +324,27 @@ struct Sh {
     int *row_pair;
     float *red;          // [kMaxRows][NCW + 1] RMSNorm partial sums, then 1/rms
     float *lscr;         // [NCW][kMaxRows] a warp's router logits before they go out
-    float *p1v;          // [shared rows of this CTA][maxr] gate / up values
     int *pair_src;       // [act_pairs] slot * kMaxRows + row of each staged pair
     float4 *xs;          // [maxr][H / 4] arranged hn * 2^100
     float *xsum;         // [maxr][H / 64] group sums of hn
     float4 *act;         // [act_pairs][K / 4] arranged activations * 2^100
     float *asum;         // [act_pairs][K / 64]
     float *ysh;          // [hrows][kMaxRows] shared expert outputs
+    float *yl;           // [pairs][hrows] routed expert outputs of this CTA's output rows
     uint8_t *pb;
     uint8_t *ring;
     int NS, S, hrows, act_pairs;
     long long timeout_ns;
     Ctrl *ctrl;
+    unsigned epoch;      // tags of this launch: epoch + layer + 1 (epoch = launch sequence * 64)
 };
 static_assert(sizeof(Sh) <= kShBytes, "Sh does not fit its shared-memory slot");
+
+// Tag of the words layer l of this launch publishes.  The launch sequence
+// number lives in the workspace control block and advances when a launch
+// ends, so every launch has tags of its own even when its parameters are
+// the same as an earlier launch's (a replayed launch, a CUDA graph).
+__device__ __forceinline__ unsigned layer_tag(const Sh &sh, int l) { return sh.epoch + (unsigned)l + 1u; }
 
 
 __device__ __forceinline__ bool aborted(const Sh &sh) { return *(volatile int *)&sh.flags[0] != 0; }
@@ -466,75 +455,28 @@ __device__ __forceinline__ void poll_tag8(const Sh &sh, const uint64_t *pa, cons
     for (int j = 0; j < 4; ++j) { a[j] = (uint32_t)v[j]; b[j] = (uint32_t)v[4 + j]; }
 }
 
-// Four pairs of consecutive tagged words (each pointer 16-byte aligned; null
-// for none): payloads of (p0, p1) into a, of (p2, p3) into b.  All loaded
-// together; while some are missing, the first missing one is polled alone,
-// then all are loaded again.  Bounded (poll_more).
-__device__ __forceinline__ void poll_pairs4(const Sh &sh, const uint64_t *p0, const uint64_t *p1, const uint64_t *p2,
-                                            const uint64_t *p3, unsigned tag, int where, uint32_t (&a)[4],
-                                            uint32_t (&b)[4])
+// End of a launch for one CTA (thread 0, once its compute warps are done,
+// whether or not a wait gave up): the last CTA to finish advances the
+// workspace's launch sequence, so that the next launch's tags differ from
+// every tag of this one.  When the sequence wraps, that CTA first clears
+// every tagged word of the workspace (no CTA of this launch reads them any
+// more), so that no word an earlier launch wrote can carry a later tag.
+__device__ void kernel_exit(const KParams &kp, const Sh &sh)
 {
-    const uint64_t none = (uint64_t)tag << 32;
-    const uint64_t *const p[4] = {p0, p1, p2, p3};
-    uint64_t v[8];
-    unsigned long long t0 = 0;
-    unsigned it = 0;
+    Ctrl *ctrl = sh.ctrl;
+    const unsigned old = atom_add_acqrel(&ctrl->exit, 1u);
+    if (old != gridDim.x - 1) return;
+    st_relaxed(&ctrl->exit, 0u);
+    unsigned next = sh.epoch / 64u + 1u;
+    if (next >= kSeqWrap) {
+        uint4 *p = reinterpret_cast<uint4 *>(kp.ws + kp.ws_l.off_logits);
+        uint4 *const end = reinterpret_cast<uint4 *>(kp.ws + kp.ws_l.off_stage_in);
 #pragma unroll 1
-    for (;;) {
-#pragma unroll
-        for (int j = 0; j < 4; ++j) {
-            v[2 * j] = v[2 * j + 1] = none;
-            if (p[j]) ld_tag2(p[j], v[2 * j], v[2 * j + 1]);
-        }
-        const uint64_t *pm = nullptr;
-#pragma unroll
-        for (int j = 7; j >= 0; --j)
-            if ((unsigned)(v[j] >> 32) != tag) pm = p[j >> 1] + (j & 1);
-        if (!pm) break;
-        bool more = true;
-#pragma unroll 1
-        while ((more = poll_more(sh, ++it, t0, where)) && (unsigned)(ld_tag(pm) >> 32) != tag) {}
-        if (!more) break;
+        for (; p < end; ++p) *p = make_uint4(0u, 0u, 0u, 0u);
+        __threadfence();
+        next = 0u;
     }
-#pragma unroll
-    for (int j = 0; j < 4; ++j) { a[j] = (uint32_t)v[j]; b[j] = (uint32_t)v[4 + j]; }
-}
-
-// Grid-wide barrier over the compute warps of every CTA.  The arrival
-// counter grows monotonically during a launch (barrier b waits for
-// (b + 1) * gridDim.x arrivals) and is reset by the last CTA to finish.
-__device__ bool grid_sync(const KParams &kp, const Sh &sh, int &nsync)
-{
-    if (cbar_or(aborted(sh))) return false;
-    if (threadIdx.x == 0) {
-        Ctrl *ctrl = sh.ctrl;
-        const unsigned target = (unsigned)(nsync + 1) * gridDim.x;
-        red_release_add(&ctrl->count, 1u);
-        if (ld_acquire(&ctrl->count) < target) {
-            const unsigned long long t0 = now_ns();
-            for (unsigned it = 1;; ++it) {
-                if (ld_acquire(&ctrl->count) >= target) break;
-                if ((it & 63) == 0) {
-                    if (*(volatile int *)&ctrl->status != 0) { *(volatile int *)&sh.flags[0] = 1; break; }
-                    if (now_ns() - t0 > (unsigned long long)sh.timeout_ns) { raise_abort(sh, 100 + nsync); break; }
-                }
-            }
-        }
-    }
-    nsync += 1;
-    return !cbar_or(aborted(sh));
-}
-
-__device__ void kernel_exit(const Sh &sh)
-{
-    if (threadIdx.x == 0 && !aborted(sh)) {
-        Ctrl *ctrl = sh.ctrl;
-        const unsigned old = atom_add_acqrel(&ctrl->exit, 1u);
-        if (old == gridDim.x - 1) {
-            st_relaxed(&ctrl->count, 0u);
-            st_relaxed(&ctrl->exit, 0u);
-        }
-    }
+    st_relaxed(&ctrl->seq, next);
 }
 
 // Part c of P of n items: [n c / P, n (c + 1) / P).  n P < 2^32 (the host
@@ -591,16 +533,6 @@ __device__ __forceinline__ float ldsf1(uint32_t a)
     return v;
 }
 
-template <int BITS>
-__device__ __forceinline__ void load_group(uint32_t row, int g, uint32_t (&w)[2 * BITS])
-{
-#pragma unroll
-    for (int i = 0; i < BITS / 2; ++i) {
-        const uint4 v = lds4(row + g * 8 * BITS + 16 * i);
-        w[4 * i] = v.x; w[4 * i + 1] = v.y; w[4 * i + 2] = v.z; w[4 * i + 3] = v.w;
-    }
-}
-
 __device__ __forceinline__ void scale_bias(uint32_t row, int K, int bits, int g, float &s, float &b)
 {
     const uint32_t sbw = lds1(row + K * bits / 8 + g * 4);
@@ -640,384 +572,17 @@ __device__ __forceinline__ uint2 lds2(uint32_t a)
     return v;
 }
 
-// Visits the 4 sub-groups of group g of NROWS rows: f(sg, parity, words[n])
-// with words[n] the sub-group's BITS/2 code words of row n and parity a
-// compile-time visit parity (0, 1).  Two sub-groups per loop trip, the loop
-// not unrolled: the kernel's code then stays small enough to remain in the
-// instruction caches between layers.
-template <int BITS, int NROWS, typename F>
-__device__ __forceinline__ void for_subgroups(const uint32_t (&rp)[NROWS], int g, F &&f)
-{
-    if constexpr (BITS == 6) {
-        // 24 bytes (two sub-groups) per trip; lanes 8 .. 15 of each half warp
-        // start with the other pair so that 8-byte loads spread the banks
-        const int rot = (g >> 3) & 1;
-#pragma unroll 1
-        for (int j = 0; j < 2; ++j) {
-            const int jj = j ^ rot;
-            uint32_t w[NROWS][6];
-#pragma unroll
-            for (int n = 0; n < NROWS; ++n) {
-                const uint32_t a = rp[n] + g * 48 + 24 * jj;
-                const uint2 v0 = lds2(a), v1 = lds2(a + 8), v2 = lds2(a + 16);
-                w[n][0] = v0.x; w[n][1] = v0.y; w[n][2] = v1.x; w[n][3] = v1.y; w[n][4] = v2.x; w[n][5] = v2.y;
-            }
-            const uint32_t *w0[NROWS], *w1[NROWS];
-#pragma unroll
-            for (int n = 0; n < NROWS; ++n) { w0[n] = &w[n][0]; w1[n] = &w[n][3]; }
-            f(2 * jj, 0, w0);
-            f(2 * jj + 1, 1, w1);
-        }
-    } else if constexpr (BITS == 8) {
-        // one 16-byte chunk per sub-group, two per trip
-        const int rot = chunk_rot<8>(g);
-#pragma unroll 1
-        for (int j = 0; j < 2; ++j) {
-            const int c0 = (2 * j + rot) & 3, c1 = (2 * j + 1 + rot) & 3;
-            uint32_t w[NROWS][8];
-#pragma unroll
-            for (int n = 0; n < NROWS; ++n) {
-                const uint4 v0 = lds4(rp[n] + g * 64 + 16 * c0), v1 = lds4(rp[n] + g * 64 + 16 * c1);
-                w[n][0] = v0.x; w[n][1] = v0.y; w[n][2] = v0.z; w[n][3] = v0.w;
-                w[n][4] = v1.x; w[n][5] = v1.y; w[n][6] = v1.z; w[n][7] = v1.w;
-            }
-            const uint32_t *w0[NROWS], *w1[NROWS];
-#pragma unroll
-            for (int n = 0; n < NROWS; ++n) { w0[n] = &w[n][0]; w1[n] = &w[n][4]; }
-            f(c0, 0, w0);
-            f(c1, 1, w1);
-        }
-    } else {
-        // 4 bits: a 16-byte chunk holds two sub-groups
-        const int rot = chunk_rot<4>(g);
-#pragma unroll 1
-        for (int j = 0; j < 2; ++j) {
-            const int c = (j + rot) & 1;
-            uint32_t w[NROWS][4];
-#pragma unroll
-            for (int n = 0; n < NROWS; ++n) {
-                const uint4 v = lds4(rp[n] + g * 32 + 16 * c);
-                w[n][0] = v.x; w[n][1] = v.y; w[n][2] = v.z; w[n][3] = v.w;
-            }
-            const uint32_t *w0[NROWS], *w1[NROWS];
-#pragma unroll
-            for (int n = 0; n < NROWS; ++n) { w0[n] = &w[n][0]; w1[n] = &w[n][2]; }
-            f(2 * c, 0, w0);
-            f(2 * c + 1, 1, w1);
-        }
-    }
-}
-
-// acc[n][r] += dot(row n, group g) . x_r for NROWS weight rows and NR token
-// rows, with per-class accumulators (split by visit parity at 4 and 8 bits,
-// which have few classes, for more independent chains).  The codes are
-// extracted once for all token rows; each token row's arithmetic is the
-// same whatever NR is, so a row's result does not depend on the other rows
-// of the call (row-exact).
-template <int BITS, int NROWS, int NR>
-__device__ __forceinline__ void grp_cls(const uint32_t (&rp)[NROWS], int g, int K, int G, const uint32_t (&xq)[NR],
-                                        const float (&xsum)[NR], float (&acc)[NROWS][NR])
-{
-    using PT = Pairs<BITS>;
-    constexpr int NC = PT::NC, NA = BITS == 6 ? NC : 2 * NC;
-    float s[NROWS], b[NROWS];
-#pragma unroll
-    for (int n = 0; n < NROWS; ++n) scale_bias(rp[n], K, BITS, g, s[n], b[n]);
-    float2 A[NROWS][NR][NA];
-#pragma unroll
-    for (int n = 0; n < NROWS; ++n)
-#pragma unroll
-        for (int r = 0; r < NR; ++r)
-#pragma unroll
-            for (int c = 0; c < NA; ++c) A[n][r][c] = make_float2(0.f, 0.f);
-    const uint32_t G16 = G * 16;
-    for_subgroups<BITS, NROWS>(rp, g, [&](int sg, int step, const uint32_t *const (&ws)[NROWS]) {
-        float4 xv[NR][4];
-#pragma unroll
-        for (int r = 0; r < NR; ++r)
-#pragma unroll
-            for (int t = 0; t < 4; ++t) xv[r][t] = ldsf4(xq[r] + g * 16 + (4 * sg + t) * G16);
-        const int half = NA > NC ? step * NC : 0;
-#pragma unroll
-        for (int n = 0; n < NROWS; ++n)
-            PT::each(ws[n], [&](int i, float a, float bb) {
-                const float2 q = make_float2(a, bb);
-#pragma unroll
-                for (int r = 0; r < NR; ++r)
-                    A[n][r][PT::cls(i) + half] =
-                        __ffma2_rn(q, xpair(xv[r][i >> 1], i & 1), A[n][r][PT::cls(i) + half]);
-            });
-    });
-#pragma unroll
-    for (int n = 0; n < NROWS; ++n)
-#pragma unroll
-        for (int r = 0; r < NR; ++r) {
-            float t = 0.f;
-#pragma unroll
-            for (int c = 0; c < NA; ++c) {
-                const int i0 = first_of_class<PT>(c % NC);
-                t = fmaf(A[n][r][c].x, __uint_as_float(cls_bits(PT::pa(i0))), t);
-                t = fmaf(A[n][r][c].y, __uint_as_float(cls_bits(PT::pb(i0))), t);
-            }
-            acc[n][r] = fmaf(s[n], t, fmaf(b[n], xsum[r], acc[n][r]));
-        }
-}
-
-// fp32 rows (a router given in fp32): K floats per row.
-template <int NROWS, int NR>
-__device__ __forceinline__ void grp_f32(const uint32_t (&rp)[NROWS], int g, int G,
-                                        const uint32_t (&xq)[NR], float (&acc)[NROWS][NR])
-{
-#pragma unroll
-    for (int n = 0; n < NROWS; ++n) {
-        float S[NR];
-#pragma unroll
-        for (int r = 0; r < NR; ++r) S[r] = 0.f;
-#pragma unroll 4
-        for (int t = 0; t < 16; ++t) {
-            const float4 wq = ldsf4(rp[n] + (g * 16 + t) * 16);
-#pragma unroll
-            for (int r = 0; r < NR; ++r) {
-                const float4 x = ldsf4(xq[r] + (t * G + g) * 16);
-                S[r] = fmaf(wq.x, x.x, fmaf(wq.y, x.y, fmaf(wq.z, x.z, fmaf(wq.w, x.w, S[r]))));
-            }
-        }
-#pragma unroll
-        for (int r = 0; r < NR; ++r) acc[n][r] = fmaf(S[r], 0x1p-100f, acc[n][r]);
-    }
-}
-
-// A warp computes rows [0, nrows) (row i at base + i * rstride, K inputs
-// at BITS bits) against NR arranged token vectors.  Lanes split a row's
-// groups (LPR lanes per row, GPL groups per lane); each lane takes NROWS
-// consecutive rows.  emit(first_row, acc) runs on the first lane of each
-// row group with the complete sums of rows first_row .. first_row+NROWS-1
-// (rows at or past nrows hold repeats of the last row and must be ignored).
-template <int BITS, int NROWS, int NR, typename F>
-__device__ __forceinline__ void warp_rows(const uint8_t *base, int rstride, int nrows, int K,
-                                          const uint32_t (&xq)[NR], const float (&xsg)[NR][kMaxGPL],
-                                          F &&emit)
-{
-    const int lane = threadIdx.x & 31;
-    const uint32_t sbase = smem_u32(base);
-    // K and G are powers of two: shifts instead of divisions
-    const int G = K >> 6, lgG = ilog2(G), lgL = lgG < 5 ? lgG : 5;
-    const int LPR = 1 << lgL, GPL = G >> lgL, RPP = 32 >> lgL;
-    const int lg = lane & (LPR - 1), lr = lane >> lgL;
-    for (int r0 = 0; r0 < nrows; r0 += RPP * NROWS) {
-        const int rb = r0 + lr * NROWS;
-        uint32_t rp[NROWS];
-#pragma unroll
-        for (int n = 0; n < NROWS; ++n) rp[n] = sbase + (uint32_t)(min(rb + n, nrows - 1) * rstride);
-        float acc[NROWS][NR];
-#pragma unroll
-        for (int n = 0; n < NROWS; ++n)
-#pragma unroll
-            for (int r = 0; r < NR; ++r) acc[n][r] = 0.f;
-        if (rb < nrows) {
-            for (int j = 0; j < GPL; ++j) {
-                const int g = lg + LPR * j;
-                if constexpr (BITS == 0) {
-                    grp_f32<NROWS, NR>(rp, g, G, xq, acc);
-                } else {
-                    float xs[NR];
-#pragma unroll
-                    for (int r = 0; r < NR; ++r) xs[r] = xsg[r][j];
-                    grp_cls<BITS, NROWS, NR>(rp, g, K, G, xq, xs, acc);
-                }
-            }
-        }
-        for (int o = LPR >> 1; o >= 1; o >>= 1)
-#pragma unroll
-            for (int n = 0; n < NROWS; ++n)
-#pragma unroll
-                for (int r = 0; r < NR; ++r) acc[n][r] += __shfl_xor_sync(FULLMASK, acc[n][r], o);
-        if (lg == 0 && rb < nrows) emit(rb, acc);
-    }
-}
-
-// Per-lane group sums of NR arranged vectors (sums[soff[r] + g] layout).
-template <int NR>
-__device__ __forceinline__ void lane_gsums(uint32_t sums, const int (&soff)[NR], int K, float (&xsg)[NR][kMaxGPL])
-{
-    const int lane = threadIdx.x & 31;
-    const int G = K >> 6, lgG = ilog2(G), lgL = lgG < 5 ? lgG : 5;
-    const int LPR = 1 << lgL, GPL = G >> lgL, lg = lane & (LPR - 1);
-#pragma unroll
-    for (int r = 0; r < NR; ++r)
-#pragma unroll
-        for (int j = 0; j < kMaxGPL; ++j) xsg[r][j] = j < GPL ? ldsf1(sums + 4 * (soff[r] + lg + LPR * j)) : 0.f;
-}
-
-// Token rows first .. first + NR - 1 of a row mask (in set-bit order),
-// padded with the last one.
-template <int NR>
-__device__ __forceinline__ void rows_of_group(uint32_t mask, int first, int (&rows)[NR], int &nvalid)
-{
-    for (int i = 0; i < first; ++i) mask &= mask - 1;
-    nvalid = 0;
-    int last = 0;
-#pragma unroll
-    for (int r = 0; r < NR; ++r) {
-        if (mask) {
-            last = __ffs(mask) - 1;
-            mask &= mask - 1;
-            ++nvalid;
-        }
-        rows[r] = last;
-    }
-}
-
-// Row groups of a mask: pairs, then a single row.
-template <typename F>
-__device__ __forceinline__ void for_row_groups(uint32_t mask, F &&f)
-{
-    const int n = __popc(mask);
-    int g0 = 0;
-    for (; n - g0 >= 2; g0 += 2) f(g0, 2);
-    if (n - g0 == 1) f(g0, 1);
-}
-
-// The warp-level row kernels below are separate (not inlined) functions,
-// one per (bits, token rows): each gets its own register allocation, and a
-// call is made once per stage and row group, not per weight.
-
-// Gate/up units [0, cnt) at `units` (unit u: gate row then up row, row
-// bytes rowb, K = H inputs) for token rows g0 .. of `mask` against hn:
-// dst[m * ld + u] = silu(gate) * up.
-template <int B, int R>
-__device__ __forceinline__ void gu_k_body(const float4 *xs, const float *xsum, int H, const uint8_t *units, int cnt,
-                                  int rowb, uint32_t mask, int g0, uint64_t *dst, int ld, unsigned tag)
-{
-    const int G = H / kGroup;
-    int rows[R], nv;
-    rows_of_group<R>(mask, g0, rows, nv);
-    uint32_t xq[R];
-    int soff[R];
-#pragma unroll
-    for (int r = 0; r < R; ++r) { xq[r] = smem_u32(xs) + (uint32_t)(rows[r] * H * 4); soff[r] = rows[r] * G; }
-    float xsg[R][kMaxGPL];
-    lane_gsums<R>(smem_u32(xsum), soff, H, xsg);
-    constexpr int NROWS = R == 1 ? 4 : 2;   // whole units (gate and up row) per lane
-    warp_rows<B, NROWS, R>(units, rowb, 2 * cnt, H, xq, xsg, [&](int rb, const float (&acc)[NROWS][R]) {
-#pragma unroll
-        for (int k2 = 0; k2 < NROWS; k2 += 2) {
-            if (rb + k2 + 1 < 2 * cnt) {
-#pragma unroll
-                for (int r = 0; r < R; ++r)
-                    if (r < nv) {
-                        const float gt = acc[k2][r], up = acc[k2 + 1][r];
-                        st_tag(dst + (size_t)rows[r] * ld + ((rb + k2) >> 1),
-                               __float_as_uint(gt / (1.0f + expf(-gt)) * up), tag);
-                    }
-            }
-        }
-    });
-}
-
-// One row of K = H inputs (a router row, or a gate or up row of a shared
-// unit) for token rows g0 .. of `mask`: dst[m * ms] = row . hn_m.
-template <int B, int R>
-__device__ __forceinline__ void one_k_body(const float4 *xs, const float *xsum, int H, const uint8_t *row, uint32_t mask,
-                                   int g0, void *dst, int ms, unsigned tag)
-{
-    const int G = H / kGroup;
-    int rows[R], nv;
-    rows_of_group<R>(mask, g0, rows, nv);
-    uint32_t xq[R];
-    int soff[R];
-#pragma unroll
-    for (int r = 0; r < R; ++r) { xq[r] = smem_u32(xs) + (uint32_t)(rows[r] * H * 4); soff[r] = rows[r] * G; }
-    float xsg[R][kMaxGPL];
-    lane_gsums<R>(smem_u32(xsum), soff, H, xsg);
-    warp_rows<B, 1, R>(row, 0, 1, H, xq, xsg, [&](int, const float (&acc)[1][R]) {
-#pragma unroll
-        for (int r = 0; r < R; ++r)
-            if (r < nv) {
-                if (tag) st_tag(static_cast<uint64_t *>(dst) + (size_t)rows[r] * ms, __float_as_uint(acc[0][r]), tag);
-                else static_cast<float *>(dst)[(size_t)rows[r] * ms] = acc[0][r];
-            }
-    });
-}
-
-// Stores v at element i of dst: a plain fp32 array, or (tag != 0) tagged words.
-__device__ __forceinline__ void put_out(void *dst, size_t i, float v, unsigned tag)
-{
-    if (tag) st_tag(static_cast<uint64_t *>(dst) + i, __float_as_uint(v), tag);
-    else static_cast<float *>(dst)[i] = v;
-}
-
-// Down rows [0, cnt) (K inputs each) against the staged activation pairs
-// pair0 + t, t = g0 .. (t < popc(mask)): dst[h * hs + t * ts] (see put_out).
-template <int B, int R>
-__device__ __forceinline__ void dn_k_body(const float4 *act, const float *asum, int K, const uint8_t *rows0, int cnt,
-                                  int rowb, uint32_t mask, int pair0, int g0, void *dst, int hs, int ts, unsigned tag)
-{
-    const int Gi = K / kGroup, n = __popc(mask);
-    int tp[R];
-    int nv = 0;
-#pragma unroll
-    for (int r = 0; r < R; ++r) {
-        tp[r] = g0 + r < n ? g0 + r : n - 1;
-        nv += g0 + r < n ? 1 : 0;
-    }
-    uint32_t xq[R];
-    int soff[R];
-#pragma unroll
-    for (int r = 0; r < R; ++r) {
-        xq[r] = smem_u32(act) + (uint32_t)((pair0 + tp[r]) * K * 4);
-        soff[r] = (pair0 + tp[r]) * Gi;
-    }
-    float xsg[R][kMaxGPL];
-    lane_gsums<R>(smem_u32(asum), soff, K, xsg);
-    constexpr int NROWS = R == 1 ? 2 : 1;   // (down rows: any count)
-    warp_rows<B, NROWS, R>(rows0, rowb, cnt, K, xq, xsg, [&](int rb, const float (&acc)[NROWS][R]) {
-#pragma unroll
-        for (int k2 = 0; k2 < NROWS; ++k2)
-            if (rb + k2 < cnt) {
-#pragma unroll
-                for (int r = 0; r < R; ++r)
-                    if (r < nv) put_out(dst, (size_t)(rb + k2) * hs + (size_t)tp[r] * ts, acc[k2][r], tag);
-            }
-    });
-}
-
-// Out-of-line entry points of the row kernels (one per instantiation).
-template <int B, int R>
-__device__ __noinline__ void gu_k(const float4 *xs, const float *xsum, int H, const uint8_t *units, int cnt,
-                                  int rowb, uint32_t mask, int g0, uint64_t *dst, int ld, unsigned tag)
-{
-    gu_k_body<B, R>(xs, xsum, H, units, cnt, rowb, mask, g0, dst, ld, tag);
-}
-template <int B, int R>
-__device__ __noinline__ void one_k(const float4 *xs, const float *xsum, int H, const uint8_t *row, uint32_t mask,
-                                   int g0, void *dst, int ms, unsigned tag)
-{
-    one_k_body<B, R>(xs, xsum, H, row, mask, g0, dst, ms, tag);
-}
-template <int B, int R>
-__device__ __noinline__ void dn_k(const float4 *act, const float *asum, int K, const uint8_t *rows0, int cnt,
-                                  int rowb, uint32_t mask, int pair0, int g0, void *dst, int hs, int ts, unsigned tag)
-{
-    dn_k_body<B, R>(act, asum, K, rows0, cnt, rowb, mask, pair0, g0, dst, hs, ts, tag);
-}
-
-// ---------------------------------------------- one token vector in registers
-//
-// When a call has one token vector (one row of the mask) and a row has at
-// most 32 groups (K <= 2048), each lane of a row keeps its group's 64 inputs
-// in registers and the warp walks the rows: per row only the codes, scale and
-// bias are read from shared memory, and the loop body is small enough to run
-// from the innermost instruction cache after the first row.  The arithmetic
-// per row is that of grp_cls with NR = 1 (same sub-group visit order, same
-// class accumulators, same lane reduction), so a row's result is bit-for-bit
-// the one the general kernels give.
-
-// Sub-group of group g visited at position v (0 .. 3) by for_subgroups.
+// Sub-group of group g visited at position v (0 .. 3).  At 8 and 4 bits a
+// group is 64 or 32 bytes, so the same 16-byte chunk of neighbouring lanes'
+// groups falls on the same shared-memory banks; each lane starts at a
+// different chunk instead.  At 6 bits the 48-byte stride already spreads the
+// banks; lanes 8 .. 15 of each half warp start with the other pair of
+// sub-groups so that 8-byte loads spread them too.
 template <int BITS>
 __device__ __forceinline__ int visit_sg(int g, int v)
 {
-    if constexpr (BITS == 6) return 2 * ((v >> 1) ^ ((g >> 3) & 1)) + (v & 1);
+    if constexpr (BITS == 0) return v;
+    else if constexpr (BITS == 6) return 2 * ((v >> 1) ^ ((g >> 3) & 1)) + (v & 1);
     else if constexpr (BITS == 8) return (v + chunk_rot<8>(g)) & 3;
     else return 2 * (((v >> 1) + chunk_rot<4>(g)) & 1) + (v & 1);
 }
@@ -1035,188 +600,277 @@ __device__ __forceinline__ void load_x1(uint32_t xq, int g, int G, float4 (&x)[1
     }
 }
 
-// The lane's part of row . x (group g), before the reduction over the lanes
-// of the row: exactly grp_cls<BITS, 1, 1> on a zero accumulator.
+// The codes, scale and bias of one lane's group of one row, loaded into
+// registers ahead of the arithmetic (the next row's while the current one is
+// computed): w[v] holds the code words of the sub-group visited v-th.
+template <int BITS> struct GroupCodes {
+    uint32_t w[4][BITS == 0 ? 1 : BITS / 2];
+    uint32_t sb;   // scale (low half, bf16) | bias (high half, bf16)
+};
+
 template <int BITS>
-__device__ __forceinline__ float dot1(uint32_t row, int g, int K, const float4 (&x)[16], float xsum)
+__device__ __forceinline__ void load_codes(uint32_t row, int g, int K, GroupCodes<BITS> &c)
+{
+    if constexpr (BITS != 0) {
+#pragma unroll
+        for (int v = 0; v < 4; ++v) {
+            const int sg = visit_sg<BITS>(g, v);
+            if constexpr (BITS == 6) {
+                // 12 bytes at row + 48 g + 12 sg: 8-byte aligned for even sg
+                const uint32_t a = row + g * 48 + 12 * sg;
+                if (v & 1) {
+                    c.w[v][0] = lds1(a);
+                    const uint2 p = lds2(a + 4);
+                    c.w[v][1] = p.x; c.w[v][2] = p.y;
+                } else {
+                    const uint2 p = lds2(a);
+                    c.w[v][0] = p.x; c.w[v][1] = p.y;
+                    c.w[v][2] = lds1(a + 8);
+                }
+            } else if constexpr (BITS == 8) {
+                const uint4 p = lds4(row + g * 64 + 16 * sg);
+                c.w[v][0] = p.x; c.w[v][1] = p.y; c.w[v][2] = p.z; c.w[v][3] = p.w;
+            } else {
+                const uint2 p = lds2(row + g * 32 + 8 * sg);
+                c.w[v][0] = p.x; c.w[v][1] = p.y;
+            }
+        }
+        c.sb = lds1(row + K * BITS / 8 + g * 4);
+    }
+}
+
+// The lane's part of row . x for group g, before the reduction over the lanes
+// of the row: s * sum_j q_j x_j + b * sum_j x_j, with the code products
+// accumulated per bit position (class) and each class scaled back once (the
+// classes summed in two interleaved chains).
+template <int BITS>
+__device__ __forceinline__ float dot_codes(const GroupCodes<BITS> &c, const float4 (&x)[16], float xsum)
 {
     using PT = Pairs<BITS>;
     constexpr int NC = PT::NC, NA = BITS == 6 ? NC : 2 * NC;
-    float s, b;
-    scale_bias(row, K, BITS, g, s, b);
     float2 A[NA];
 #pragma unroll
-    for (int c = 0; c < NA; ++c) A[c] = make_float2(0.f, 0.f);
+    for (int k = 0; k < NA; ++k) A[k] = make_float2(0.f, 0.f);
 #pragma unroll
     for (int v = 0; v < 4; ++v) {
-        const int sg = visit_sg<BITS>(g, v);
-        uint32_t w[BITS / 2];
-        if constexpr (BITS == 6) {
-            // 12 bytes at row + 48 g + 12 sg: 8-byte aligned for even sg
-            const uint32_t a = row + g * 48 + 12 * sg;
-            if (sg & 1) {
-                w[0] = lds1(a);
-                const uint2 p = lds2(a + 4);
-                w[1] = p.x; w[2] = p.y;
-            } else {
-                const uint2 p = lds2(a);
-                w[0] = p.x; w[1] = p.y;
-                w[2] = lds1(a + 8);
-            }
-        } else if constexpr (BITS == 8) {
-            const uint4 p = lds4(row + g * 64 + 16 * sg);
-            w[0] = p.x; w[1] = p.y; w[2] = p.z; w[3] = p.w;
-        } else {
-            const uint2 p = lds2(row + g * 32 + 8 * sg);
-            w[0] = p.x; w[1] = p.y;
-        }
         const int half = NA > NC ? (v & 1) * NC : 0;
-        PT::each(w, [&](int i, float a, float bb) {
+        PT::each(c.w[v], [&](int i, float a, float bb) {
             A[PT::cls(i) + half] = __ffma2_rn(make_float2(a, bb), xpair(x[4 * v + (i >> 1)], i & 1), A[PT::cls(i) + half]);
         });
     }
-    float t = 0.f;
+    float t0 = 0.f, t1 = 0.f;
 #pragma unroll
-    for (int c = 0; c < NA; ++c) {
-        const int i0 = first_of_class<PT>(c % NC);
-        t = fmaf(A[c].x, __uint_as_float(cls_bits(PT::pa(i0))), t);
-        t = fmaf(A[c].y, __uint_as_float(cls_bits(PT::pb(i0))), t);
+    for (int k = 0; k < NA; ++k) {
+        const int i0 = first_of_class<PT>(k % NC);
+        t0 = fmaf(A[k].x, __uint_as_float(cls_bits(PT::pa(i0))), t0);
+        t1 = fmaf(A[k].y, __uint_as_float(cls_bits(PT::pb(i0))), t1);
     }
-    return fmaf(s, t, fmaf(b, xsum, 0.f));
+    const float s = __uint_as_float(c.sb << 16), b = __uint_as_float(c.sb & 0xFFFF0000u);
+    return fmaf(s, t0 + t1, b * xsum);
 }
 
-// Rows against one token vector: the warp takes rows r0 + RPP i (lanes
-// lg of a row group, RPP = 32 / LPR row groups) of nrows at rows + r * rstride
-// (shared memory), each of K inputs.  emit(r, value) runs on the first lane
-// of the row group with the complete dot product of row r.
-template <int BITS, typename F>
-__device__ __forceinline__ void rows1(uint32_t rows, int rstride, int nrows, int K, uint32_t xq, uint32_t xsq, F &&emit)
+// fp32 row (a router given in fp32): K floats; x holds the inputs times 2^100.
+__device__ __forceinline__ float dot_f32(uint32_t row, int g, const float4 (&x)[16])
+{
+    float S = 0.f;
+#pragma unroll
+    for (int q = 0; q < 16; ++q) {
+        const float4 w = ldsf4(row + (uint32_t)(g * 16 + q) * 16);
+        S = fmaf(w.x, x[q].x, fmaf(w.y, x[q].y, fmaf(w.z, x[q].z, fmaf(w.w, x[q].w, S))));
+    }
+    return S * 0x1p-100f;
+}
+
+// Stores v at element i of dst: a plain fp32 array, or (tag != 0) tagged words.
+__device__ __forceinline__ void put_out(void *dst, size_t i, float v, unsigned tag)
+{
+    if (tag) st_tag(static_cast<uint64_t *>(dst) + i, __float_as_uint(v), tag);
+    else static_cast<float *>(dst)[i] = v;
+}
+
+// ------------------------------------------------------------ row kernels
+//
+// Every dot product of the layer (router rows, gate/up rows, down rows) is a
+// packed row in shared memory against ONE arranged token vector (hn, or an
+// expert's activations, times 2^100, in shared memory).  A call with several
+// token rows runs the same kernel once per token row, so a row's result is
+// bitwise the same whatever the other rows of the call are (PureDrive model
+// card, "How it works": every row of the verify pass equals a one-row
+// decode).
+//
+// Lanes take whole 64-groups of a row: LPR = min(32, G) lanes per row, GPL =
+// G / LPR groups per lane, RPP = 32 / LPR rows side by side.  A lane keeps
+// the 64 inputs of its group in registers while the warp walks the rows, 8
+// row slots per lane at a time (a batch of 8 RPP rows, or units of a gate row
+// and an up row).  A batch is reduced over the LPR lanes of each row by a
+// transposing butterfly: at each exchange a lane keeps half of the values it
+// holds, adds its partner's copy of that half and sends the other half, so 8
+// slots cost 7 exchanges where one row at a time would cost 8 log2(LPR)
+// dependent ones.  Every row's lane partials are added in the same tree
+// (lanes l and l ^ LPR/2, then l ^ LPR/4, ...; a + b = b + a exactly) in
+// whichever slot of whichever batch it sits.
+
+template <int NA, int N>
+__device__ __forceinline__ void halve_slots(float (&v)[NA][8], int o, bool up)
+{
+#pragma unroll
+    for (int a = 0; a < NA; ++a)
+#pragma unroll
+        for (int i = 0; i < N / 2; ++i) {
+            const float keep = up ? v[a][i + N / 2] : v[a][i];
+            const float send = up ? v[a][i] : v[a][i + N / 2];
+            v[a][i] = keep + __shfl_xor_sync(FULLMASK, send, o);
+        }
+}
+
+// Reduces 8 slots per lane over the LPR lanes of each row.  Returns how many
+// slots this lane emits (0 on lanes whose copy is not the one kept); they are
+// v[a][0 ..) for slots slot0, slot0 + 1, ...
+template <int NA>
+__device__ __forceinline__ int reduce_slots(float (&v)[NA][8], int LPR, int lane, int &slot0)
+{
+    int o = LPR >> 1, held = 8;
+    slot0 = 0;
+    if (o) { const bool up = (lane & o) != 0; halve_slots<NA, 8>(v, o, up); slot0 += up ? 4 : 0; o >>= 1; held = 4; }
+    if (o) { const bool up = (lane & o) != 0; halve_slots<NA, 4>(v, o, up); slot0 += up ? 2 : 0; o >>= 1; held = 2; }
+    if (o) { const bool up = (lane & o) != 0; halve_slots<NA, 2>(v, o, up); slot0 += up ? 1 : 0; o >>= 1; held = 1; }
+    const int rest = o ? 2 * o - 1 : 0;
+#pragma unroll 1
+    for (; o; o >>= 1)
+#pragma unroll
+        for (int a = 0; a < NA; ++a) v[a][0] += __shfl_xor_sync(FULLMASK, v[a][0], o);
+    return (lane & rest) == 0 ? held : 0;
+}
+
+// Units [0, nunits) against one arranged vector (xq, group sums at xsq): unit
+// u is the row at rows + u * ustride (NA = 1), or the rows at rows + u *
+// ustride and rows + u * ustride + rstride (NA = 2: a gate row and its up
+// row).  emit(u, val) runs on one lane per unit with the complete products.
+template <int BITS, int NA, typename F>
+__device__ __forceinline__ void rows_dot(uint32_t rows, int ustride, int rstride, int nunits, int K, uint32_t xq,
+                                         uint32_t xsq, F &&emit)
 {
     const int lane = threadIdx.x & 31;
-    const int G = K >> 6, lgL = ilog2(G), LPR = 1 << lgL, RPP = 32 >> lgL;
-    const int g = lane & (LPR - 1), lr = lane >> lgL;
-    float4 x[16];
-    load_x1<BITS>(xq, g, G, x);
-    const float xsum = ldsf1(xsq + 4 * g);
+    const int G = K >> 6, lgG = ilog2(G), lgL = lgG < 5 ? lgG : 5;
+    const int LPR = 1 << lgL, RPP = 32 >> lgL, GPL = G >> lgL;
+    const int gl = lane & (LPR - 1), rg = lane >> lgL;
 #pragma unroll 1
-    for (int r0 = 0; r0 < nrows; r0 += RPP) {
-        const int r = r0 + lr;
-        float acc = dot1<BITS>(rows + (uint32_t)(min(r, nrows - 1) * rstride), g, K, x, xsum);
+    for (int u0 = 0; u0 < nunits; u0 += 8 * RPP) {
+        float v[NA][8];
+#pragma unroll
+        for (int a = 0; a < NA; ++a)
+#pragma unroll
+            for (int j = 0; j < 8; ++j) v[a][j] = 0.f;
+        const int nslots = min(8, (nunits - u0 + RPP - 1) / RPP);
 #pragma unroll 1
-        for (int o = LPR >> 1; o >= 1; o >>= 1) acc += __shfl_xor_sync(FULLMASK, acc, o);
-        if (g == 0 && r < nrows) emit(r, acc);
+        for (int gp = 0; gp < GPL; ++gp) {
+            const int g = gl + LPR * gp;
+            float4 x[16];
+            load_x1<BITS>(xq, g, G, x);
+            const float xs = BITS == 0 ? 0.f : ldsf1(xsq + 4 * g);
+#pragma unroll 1
+            for (int j = 0; j < nslots; ++j) {
+                const uint32_t r = rows + (uint32_t)(min(u0 + j * RPP + rg, nunits - 1) * ustride);
+                float d[NA];
+#pragma unroll
+                for (int a = 0; a < NA; ++a) {
+                    if constexpr (BITS == 0) {
+                        d[a] = dot_f32(r + (uint32_t)(a * rstride), g, x);
+                    } else {
+                        GroupCodes<BITS> c;
+                        load_codes<BITS>(r + (uint32_t)(a * rstride), g, K, c);
+                        d[a] = dot_codes<BITS>(c, x, xs);
+                    }
+                }
+                // into slot j without indexing the register array by a variable
+#pragma unroll
+                for (int a = 0; a < NA; ++a)
+#pragma unroll
+                    for (int jj = 0; jj < 8; ++jj) v[a][jj] = jj == j ? v[a][jj] + d[a] : v[a][jj];
+            }
+        }
+        int slot0;
+        const int held = reduce_slots<NA>(v, LPR, lane, slot0);
+#pragma unroll
+        for (int i = 0; i < 8; ++i)
+            if (i < held) {
+                const int u = u0 + (slot0 + i) * RPP + rg;
+                float val[NA];
+#pragma unroll
+                for (int a = 0; a < NA; ++a) val[a] = v[a][i];
+                if (u < nunits) emit(u, val);
+            }
     }
 }
 
-// Gate/up units [0, cnt) (unit u: gate row 2u, up row 2u + 1) against one
-// token vector: dst[u] = silu(gate) * up, tagged.  A row group takes a whole
-// unit.
+// Gate/up units [0, cnt) (unit u: gate row at units + 2 u rowb, up row next)
+// against hn of every token row m of `mask`: dst[m * ld + u] = silu(gate) *
+// up, as tagged words.
 template <int BITS>
-__device__ __noinline__ void gu1(uint32_t units, int cnt, int rowb, int H, uint32_t xq, uint32_t xsq, uint64_t *dst,
-                                 unsigned tag)
+__device__ __noinline__ void gu_rows(uint32_t units, int cnt, int rowb, int H, uint32_t xs, uint32_t xsum,
+                                     uint32_t mask, uint64_t *dst, int ld, unsigned tag)
 {
-    const int lane = threadIdx.x & 31;
-    const int G = H >> 6, lgL = ilog2(G), LPR = 1 << lgL, RPP = 32 >> lgL;
-    const int g = lane & (LPR - 1), lr = lane >> lgL;
-    float4 x[16];
-    load_x1<BITS>(xq, g, G, x);
-    const float xsum = ldsf1(xsq + 4 * g);
+    const int G = H / kGroup;
 #pragma unroll 1
-    for (int u0 = 0; u0 < cnt; u0 += RPP) {
-        const uint32_t ru = units + (uint32_t)(2 * min(u0 + lr, cnt - 1) * rowb);
-        float gt = 0.f, up = 0.f;
-#pragma unroll 1
-        for (int k = 0; k < 2; ++k) {
-            const float v = dot1<BITS>(ru + k * rowb, g, H, x, xsum);
-            if (k) up = v;
-            else gt = v;
-        }
-#pragma unroll 1
-        for (int o = LPR >> 1; o >= 1; o >>= 1) {
-            gt += __shfl_xor_sync(FULLMASK, gt, o);
-            up += __shfl_xor_sync(FULLMASK, up, o);
-        }
-        if (g == 0 && u0 + lr < cnt) st_tag(dst + u0 + lr, __float_as_uint(gt / (1.0f + expf(-gt)) * up), tag);
+    for (; mask; mask &= mask - 1u) {
+        const int m = __ffs(mask) - 1;
+        uint64_t *d = dst + (size_t)m * ld;
+        rows_dot<BITS, 2>(units, 2 * rowb, rowb, cnt, H, xs + (uint32_t)(m * H * 4), xsum + (uint32_t)(m * G * 4),
+                          [&](int u, const float (&v)[2]) {
+                              st_tag(d + u, __float_as_uint(v[0] / (1.0f + expf(-v[0])) * v[1]), tag);
+                          });
     }
 }
 
-// Rows [0, cnt) against one vector: dst[r * ds] = row r . x (see put_out).
+// Rows [0, cnt) (row bytes rowb, K inputs) against the vectors of the token
+// rows of `mask`: vector m (by_rank = 0: the vector of token row m) or
+// vector t (by_rank = 1: t = the rank of m in the mask) of vecs (stride K
+// floats, group sums at sums, stride K / 64):
+// dst[r * hs + (by_rank ? t : m) * ts] = row r . vector (see put_out).
 template <int BITS>
-__device__ __noinline__ void plain1(uint32_t rows, int cnt, int rowb, int K, uint32_t xq, uint32_t xsq, void *dst, int ds,
-                                    unsigned tag)
+__device__ __noinline__ void plain_rows(uint32_t rows, int cnt, int rowb, int K, uint32_t vecs, uint32_t sums,
+                                        uint32_t mask, int by_rank, void *dst, int hs, int ts, unsigned tag)
 {
-    rows1<BITS>(rows, rowb, cnt, K, xq, xsq, [&](int r, float v) { put_out(dst, (size_t)r * ds, v, tag); });
+    const int G = K / kGroup;
+#pragma unroll 1
+    for (int t = 0; mask; mask &= mask - 1u, ++t) {
+        const int m = __ffs(mask) - 1, vi = by_rank ? t : m;
+        rows_dot<BITS, 1>(rows, rowb, 0, cnt, K, vecs + (uint32_t)(vi * K * 4), sums + (uint32_t)(vi * G * 4),
+                          [&](int r, const float (&v)[1]) { put_out(dst, (size_t)r * hs + (size_t)vi * ts, v[0], tag); });
+    }
 }
-
-// Dispatch on (bits, row-group size): code = bits * 8 + nr.
-#define MOE_RK_CASES(FN, ARGS)                                                                   \
-    case 4 * 8 + 1: FN<4, 1> ARGS; break;                                                        \
-    case 4 * 8 + 2: FN<4, 2> ARGS; break;                                                        \
-    case 6 * 8 + 1: FN<6, 1> ARGS; break;                                                        \
-    case 6 * 8 + 2: FN<6, 2> ARGS; break;                                                        \
-    case 8 * 8 + 1: FN<8, 1> ARGS; break;                                                        \
-    case 8 * 8 + 2: FN<8, 2> ARGS; break;
 
 __device__ __noinline__ void gu_units(const Sh &sh, int H, int bits, const uint8_t *units, int cnt, int rowb,
-                                         uint32_t mask, uint64_t *dst, int ld, unsigned tag)
+                                      uint32_t mask, uint64_t *dst, int ld, unsigned tag)
 {
-    if (__popc(mask) == 1 && H <= 32 * kGroup && bits != 0) {
-        const int m = __ffs(mask) - 1;
-        const uint32_t xq = smem_u32(sh.xs) + (uint32_t)(m * H * 4), xsq = smem_u32(sh.xsum) + (uint32_t)(m * (H / kGroup) * 4);
-        uint64_t *d = dst + (size_t)m * ld;
-        if (bits == 6) gu1<6>(smem_u32(units), cnt, rowb, H, xq, xsq, d, tag);
-        else if (bits == 8) gu1<8>(smem_u32(units), cnt, rowb, H, xq, xsq, d, tag);
-        else gu1<4>(smem_u32(units), cnt, rowb, H, xq, xsq, d, tag);
-        return;
-    }
-    for_row_groups(mask, [&](int g0, int nr) {
-        switch (bits * 8 + nr) {
-            MOE_RK_CASES(gu_k, (sh.xs, sh.xsum, H, units, cnt, rowb, mask, g0, dst, ld, tag))
-        default: break;
-        }
-    });
+    const uint32_t u = smem_u32(units), xs = smem_u32(sh.xs), xsum = smem_u32(sh.xsum);
+    if (bits == 6) gu_rows<6>(u, cnt, rowb, H, xs, xsum, mask, dst, ld, tag);
+    else if (bits == 8) gu_rows<8>(u, cnt, rowb, H, xs, xsum, mask, dst, ld, tag);
+    else gu_rows<4>(u, cnt, rowb, H, xs, xsum, mask, dst, ld, tag);
 }
 
+// One row of K = H inputs (a router row) against hn of the token rows of
+// `mask`: dst[m * ms] = row . hn_m.
 __device__ __noinline__ void one_row(const Sh &sh, int H, int bits, const uint8_t *row, uint32_t mask,
-                                        void *dst, int ms, unsigned tag)
+                                     void *dst, int ms, unsigned tag)
 {
-    if (__popc(mask) == 1 && H <= 32 * kGroup && bits != 0 && tag == 0u) {
-        const int m = __ffs(mask) - 1;
-        const uint32_t xq = smem_u32(sh.xs) + (uint32_t)(m * H * 4), xsq = smem_u32(sh.xsum) + (uint32_t)(m * (H / kGroup) * 4);
-        float *d = static_cast<float *>(dst) + (size_t)m * ms;
-        if (bits == 6) plain1<6>(smem_u32(row), 1, 0, H, xq, xsq, d, 0, 0u);
-        else if (bits == 8) plain1<8>(smem_u32(row), 1, 0, H, xq, xsq, d, 0, 0u);
-        else plain1<4>(smem_u32(row), 1, 0, H, xq, xsq, d, 0, 0u);
-        return;
-    }
-    for_row_groups(mask, [&](int g0, int nr) {
-        switch (bits * 8 + nr) {
-            MOE_RK_CASES(one_k, (sh.xs, sh.xsum, H, row, mask, g0, dst, ms, tag))
-        case 0 * 8 + 1: one_k<0, 1>(sh.xs, sh.xsum, H, row, mask, g0, dst, ms, tag); break;
-        case 0 * 8 + 2: one_k<0, 2>(sh.xs, sh.xsum, H, row, mask, g0, dst, ms, tag); break;
-        default: break;
-        }
-    });
+    const uint32_t r = smem_u32(row), xs = smem_u32(sh.xs), xsum = smem_u32(sh.xsum);
+    if (bits == 6) plain_rows<6>(r, 1, 0, H, xs, xsum, mask, 0, dst, 0, ms, tag);
+    else if (bits == 8) plain_rows<8>(r, 1, 0, H, xs, xsum, mask, 0, dst, 0, ms, tag);
+    else if (bits == 4) plain_rows<4>(r, 1, 0, H, xs, xsum, mask, 0, dst, 0, ms, tag);
+    else plain_rows<0>(r, 1, 0, H, xs, xsum, mask, 0, dst, 0, ms, tag);
 }
 
-// dst[h * hs + t * ts] for down row h and the staged pair pair0 + t (t the
-// rank of a row in `mask`): plain fp32, or tagged words when tag != 0.
+// Down rows [0, cnt) (K inputs each) against the staged activation pairs
+// pair0 + t, t = the rank of a token row in `mask`: dst[h * hs + t * ts].
 __device__ __noinline__ void dn_rows(const Sh &sh, int bits, const uint8_t *rows0, int cnt, int rowb, int K,
-                                        uint32_t mask, int pair0, void *dst, int hs, int ts, unsigned tag)
+                                     uint32_t mask, int pair0, void *dst, int hs, int ts, unsigned tag)
 {
-    if (__popc(mask) == 1 && K <= 32 * kGroup && bits != 0) {
-        const uint32_t xq = smem_u32(sh.act) + (uint32_t)(pair0 * K * 4), xsq = smem_u32(sh.asum) + (uint32_t)(pair0 * (K / kGroup) * 4);
-        if (bits == 6) plain1<6>(smem_u32(rows0), cnt, rowb, K, xq, xsq, dst, hs, tag);
-        else if (bits == 8) plain1<8>(smem_u32(rows0), cnt, rowb, K, xq, xsq, dst, hs, tag);
-        else plain1<4>(smem_u32(rows0), cnt, rowb, K, xq, xsq, dst, hs, tag);
-        return;
-    }
-    for_row_groups(mask, [&](int g0, int nr) {
-        switch (bits * 8 + nr) {
-            MOE_RK_CASES(dn_k, (sh.act, sh.asum, K, rows0, cnt, rowb, mask, pair0, g0, dst, hs, ts, tag))
-        default: break;
-        }
-    });
+    const uint32_t r = smem_u32(rows0);
+    const uint32_t a = smem_u32(sh.act) + (uint32_t)(pair0 * K * 4), as = smem_u32(sh.asum) + (uint32_t)(pair0 * (K / kGroup) * 4);
+    if (bits == 6) plain_rows<6>(r, cnt, rowb, K, a, as, mask, 1, dst, hs, ts, tag);
+    else if (bits == 8) plain_rows<8>(r, cnt, rowb, K, a, as, mask, 1, dst, hs, ts, tag);
+    else plain_rows<4>(r, cnt, rowb, K, a, as, mask, 1, dst, hs, ts, tag);
 }
 
 // ------------------------------------------------------------ P0: RMSNorm
@@ -1410,7 +1064,7 @@ __device__ __noinline__ void topk_row_t(const KParams &kp, const Sh &sh, int m, 
         }
         if (!__any_sync(FULLMASK, pm != nullptr) || !__all_sync(FULLMASK, more)) break;
     }
-    if (threadIdx.x == 0) stamp(kp, (int)(tag - kp.epoch - 1u), 15);
+    if (threadIdx.x == 0) stamp(kp, (int)(tag - sh.epoch - 1u), 15);
     uint32_t key[NPL];
 #pragma unroll
     for (int i = 0; i < NPL; ++i) key[i] = lane + 32 * i < E ? fkey(__uint_as_float((uint32_t)v[i])) : 0u;
@@ -1480,7 +1134,7 @@ __device__ __forceinline__ void rbar(int nw) { asm volatile("bar.sync 2, %0;" ::
 // indices; ends by telling the producer that the table of layer l is ready.
 __device__ void route(const KParams &kp, const Sh &sh, const uint64_t *logits, int l)
 {
-    const unsigned tag = layer_tag(kp, l);
+    const unsigned tag = layer_tag(sh, l);
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     const int E = kp.g.E, k = kp.g.k, M = kp.M;
     topk_row(kp, sh, warp, logits, tag);
@@ -1568,8 +1222,7 @@ struct Ws {
     uint64_t *logits;   // [kLogitCopies][maxr][Er] fp32 (each CTA reads copy blockIdx % kLogitCopies)
     uint64_t *act;      // [max_slots][maxr][I] fp32
     uint64_t *act_s;    // [maxr][Is] fp32
-    uint64_t *ping[2];  // [maxr][H / 2] bf16 pairs: outputs of the layers before the last
-    uint64_t *y;        // [maxr * k][H] fp32 routed expert outputs, by pair
+    uint64_t *ping[2];  // [maxr][H / 2] bf16 pairs: layer outputs (tag of the layer that wrote them)
 };
 
 __device__ __forceinline__ Ws ws_views(const KParams &kp)
@@ -1580,7 +1233,6 @@ __device__ __forceinline__ Ws ws_views(const KParams &kp)
     w.act_s = reinterpret_cast<uint64_t *>(kp.ws + kp.ws_l.off_act_s);
     w.ping[0] = reinterpret_cast<uint64_t *>(kp.ws + kp.ws_l.off_ping);
     w.ping[1] = w.ping[0] + (size_t)kp.ws_l.maxr * (kp.g.H / 2);
-    w.y = reinterpret_cast<uint64_t *>(kp.ws + kp.ws_l.off_y);
     return w;
 }
 
@@ -1610,19 +1262,19 @@ __device__ void cta_plan(const KParams &kp, CtaPlan &b)
 // Ring stages of a layer, in order: P1 units that did not fit the prefetch
 // buffer, P2 routed gate/up units, P1b shared down rows that did not fit it,
 // P3 routed down rows.  `f` gets (src, bytes, slot-or-kind, first, count).
-// The P1 overflow is counted in shared-expert rows (row 2u is the gate row
-// of unit u, row 2u + 1 its up row); `first` is relative to the CTA's rows.
+// The P1 overflow is whole shared-expert units (gate row, up row); `first` is
+// the unit index relative to the CTA's first shared unit.
 template <typename F>
 __device__ __forceinline__ void sched_p1x(const KParams &kp, const Sh &sh, const LayerPtrs &Lp, F &&f)
 {
     const Geo &g = kp.g;
     if (kp.mode != kModeLayers || !g.has_shared || g.sg_bytes == 0) return;
     const CtaPlan &b = *sh.cp;
-    const int cr = max(1, sh.S / g.sg_bytes);
+    const int ub2 = 2 * g.sg_bytes, cu = max(1, sh.S / ub2);
 #pragma unroll 1
-    for (int r = 2 * (b.ua + b.upb); r < 2 * b.ub; r += cr) {
-        const int n = min(cr, 2 * b.ub - r);
-        f(Lp.sgu + (size_t)r * g.sg_bytes, n * g.sg_bytes, -2, r - 2 * b.ua, n);
+    for (int u = b.ua + b.upb; u < b.ub; u += cu) {
+        const int n = min(cu, b.ub - u);
+        f(Lp.sgu + (size_t)u * ub2, n * ub2, -2, u - b.ua, n);
     }
 }
 
@@ -1664,50 +1316,24 @@ __device__ __forceinline__ void sched_p2(const KParams &kp, const Sh &sh, const 
     }
 }
 
-// P3 of this CTA: the slots whose gate/up units it computed in P2 (one or
-// two: a CTA's unit range is shorter than an expert since U < P), and for
-// each the share of the slot's H down rows in proportion to the share of
-// the slot's units it computed (unit range [u0, u1) of I: rows
-// [H u0 / I, H u1 / I)), so that the activations a CTA waits for come from
-// the few CTAs that share its expert, not from every CTA, and the down work
-// follows the gate/up work.
-struct P3Part {
-    int s;        // slot
-    int r0, r1;   // down rows [r0, r1)
-};
-
-__device__ __forceinline__ int p3_parts(const KParams &kp, const Sh &sh, P3Part (&pt)[2])
-{
-    const int U = sh.flags[1], I = kp.g.I, H = kp.g.H, P = gridDim.x, c = blockIdx.x;
-    const int n = U * I;   // n P < 2^32 (the host plan checks it)
-    int a, b;
-    split(n, P, c, a, b);
-    int cnt = 0;
-#pragma unroll 1
-    for (int s = a / I; b > a && s <= (b - 1) / I && cnt < 2; ++s) {
-        const int u0 = max(a, s * I) - s * I, u1 = min(b, (s + 1) * I) - s * I;
-        const int r0 = (int)((unsigned)H * (unsigned)u0 / (unsigned)I), r1 = (int)((unsigned)H * (unsigned)u1 / (unsigned)I);
-        if (r1 > r0) pt[cnt++] = P3Part{s, r0, r1};
-    }
-    return cnt;
-}
-
+// P3 of this CTA: the down rows of its own output slice [h0, h0 + nh) of
+// every selected expert, in slot order (one or more stages per slot).  Each
+// CTA thus finishes its outputs itself (no exchange of expert outputs), and
+// needs the activations of every selected expert, from every CTA.
 template <typename F>
 __device__ __forceinline__ void sched_p3(const KParams &kp, const Sh &sh, const LayerPtrs &Lp, F &&f)
 {
     const Geo &g = kp.g;
-    P3Part pt[2];
-    const int np = p3_parts(kp, sh, pt);
-    // about one stage per compute warp over the layer
-    const int per_part = max(1, (NCW + np - 1) / max(1, np));
+    const int U = sh.flags[1], h0 = sh.cp->h0, nh = sh.cp->nh;
+    if (nh <= 0) return;
+    const int cd = max(1, min(sh.S / g.d_bytes, nh));
 #pragma unroll 1
-    for (int i = 0; i < np; ++i) {
-        const int e = sh.slot_e[pt[i].s], nr = pt[i].r1 - pt[i].r0;
-        const int cd = max(1, min(sh.S / g.d_bytes, (nr + per_part - 1) / per_part));
+    for (int s = 0; s < U; ++s) {
+        const int e = sh.slot_e[s];
 #pragma unroll 1
-        for (int r = pt[i].r0; r < pt[i].r1; r += cd) {
-            const int n = min(cd, pt[i].r1 - r);
-            f(Lp.down + ((size_t)e * g.H + r) * g.d_bytes, n * g.d_bytes, pt[i].s, r, n);
+        for (int r = 0; r < nh; r += cd) {
+            const int n = min(cd, nh - r);
+            f(Lp.down + ((size_t)e * g.H + h0 + r) * g.d_bytes, n * g.d_bytes, s, r, n);
         }
     }
 }
@@ -1897,49 +1523,50 @@ __device__ __forceinline__ void consume(const Sh &sh, Cursor &c, int where, F &&
 
 // P1 and routing.  With M at most half the compute warps, the first M warps
 // route (one token row each), waiting on every CTA's router logits, while
-// the other warps compute this CTA's router rows first and its shared
-// gate/up rows from the prefetch buffer after them (so that the logits every
-// CTA waits for go out first), then the SwiGLU of the CTA's shared units.
-// With more rows, every warp computes rows first and the first M route
-// after.  Shared rows past the buffer come through the ring; their stages go
-// to every compute warp in turn, so when there are any the SwiGLU waits for
-// the routing warps as well.
+// the other warps compute this CTA's router rows first (the logits every CTA
+// waits for go out first) and then its shared-expert gate/up units from the
+// prefetch buffer, one range of units per warp, publishing their SwiGLU
+// activations.  With more rows every warp computes first and the first M
+// route after.  Shared units past the buffer come through the ring, one stage
+// to each compute warp in turn.
 __device__ void phase1(const KParams &kp, const Sh &sh, const LayerPtrs &Lp, Cursor &q, const Ws &w, int l)
 {
     const Geo &g = kp.g;
     const uint32_t all = (1u << kp.M) - 1u;
-    const int warp = threadIdx.x >> 5, maxr = kp.p.maxr, M = kp.M;
+    const int warp = threadIdx.x >> 5, M = kp.M;
     const CtaPlan &b = *sh.cp;
-    const int nr = b.rb - b.ra, nrows = nr + 2 * b.upb;
-    const bool ring_rows = b.ub - b.ua > b.upb;
+    const int nr = b.rb - b.ra;
     const bool early = 2 * M <= NCW;
     const int w0 = early ? M : 0;   // first warp computing rows
+    const unsigned tag = layer_tag(sh, l);
     wstamp(kp, l, 14);
     if (early && warp < M) {
         route(kp, sh, w.logits, l);
     } else {
+        const int i0 = warp - w0, nw = NCW - w0;
 #pragma unroll 1
-        for (int i = warp - w0; i < nrows; i += NCW - w0) {
-            if (i < nr) {
-                // the M logits of router row e, then their copies out
-                const int e = b.ra + i;
-                float *lv = sh.lscr + warp * kMaxRows;
-                one_row(sh, g.H, g.qb, sh.pb + b.off_router + (size_t)i * g.rr_bytes, all, lv, 1, 0u);
-                __syncwarp();
-                const int lane = threadIdx.x & 31;
-                // (debug switch: one logit of layer 0 stays unpublished)
-                if (!(l == 0 && kp.skip_row == e))
+        for (int i = i0; i < nr; i += nw) {
+            // the M logits of router row e, then their copies out
+            const int e = b.ra + i;
+            float *lv = sh.lscr + warp * kMaxRows;
+            one_row(sh, g.H, g.qb, sh.pb + b.off_router + (size_t)i * g.rr_bytes, all, lv, 1, 0u);
+            __syncwarp();
+            const int lane = threadIdx.x & 31;
+            // (debug switch: one logit of layer 0 stays unpublished)
+            if (!(l == 0 && kp.skip_row == e))
 #pragma unroll 1
-                    for (int t = lane; t < kLogitCopies * M; t += 32) {
-                        const int c = t / M, m = t - c * M;
-                        st_tag(w.logits + ((size_t)c * kp.ws_l.maxr + m) * g.Er + e, __float_as_uint(lv[m]),
-                               layer_tag(kp, l));
-                    }
-                __syncwarp();
-            } else {
-                const int j = i - nr;   // gate row of unit j / 2, or its up row
-                one_row(sh, g.H, g.sb, sh.pb + b.off_units + (size_t)j * g.sg_bytes, all, sh.p1v + j * maxr, 1, 0u);
-            }
+                for (int t = lane; t < kLogitCopies * M; t += 32) {
+                    const int c = t / M, m = t - c * M;
+                    st_tag(w.logits + ((size_t)c * kp.ws_l.maxr + m) * g.Er + e, __float_as_uint(lv[m]), tag);
+                }
+            __syncwarp();
+        }
+        if (kp.mode == kModeLayers && b.upb > 0) {
+            int u0, u1;
+            split(b.upb, nw, i0, u0, u1);
+            if (u1 > u0)
+                gu_units(sh, g.H, g.sb, sh.pb + b.off_units + (size_t)u0 * 2 * g.sg_bytes, u1 - u0, g.sg_bytes, all,
+                         w.act_s + b.ua + u0, g.Is, tag);
         }
     }
     wstamp(kp, l, 15);
@@ -1948,33 +1575,12 @@ __device__ void phase1(const KParams &kp, const Sh &sh, const LayerPtrs &Lp, Cur
         if (warp < M) route(kp, sh, w.logits, l);
     }
     if (kp.mode != kModeLayers) return;
-    int t0 = w0 * 32, nt = NCT - w0 * 32;
-    if (ring_rows || !early) {
-        if (ring_rows) {
-            sched_p1x(kp, sh, Lp, [&](const uint8_t *, int, int, int first, int n) {
-                consume(sh, q, 10, [&](const uint8_t *st) {
-#pragma unroll 1
-                    for (int i = 0; i < n; ++i)
-                        one_row(sh, g.H, g.sb, st + (size_t)i * g.sg_bytes, all, sh.p1v + (first + i) * maxr, 1, 0u);
-                });
+    if (b.ub - b.ua > b.upb)
+        sched_p1x(kp, sh, Lp, [&](const uint8_t *, int, int, int first, int n) {
+            consume(sh, q, 10, [&](const uint8_t *st) {
+                gu_units(sh, g.H, g.sb, st, n, g.sg_bytes, all, w.act_s + b.ua + first, g.Is, tag);
             });
-            cbar();
-        }
-        t0 = 0;
-        nt = NCT;
-    } else {
-        if (warp < M) return;
-        asm volatile("bar.sync 3, %0;" ::"r"(nt) : "memory");
-    }
-    // SwiGLU of the CTA's shared units
-    const unsigned tag = layer_tag(kp, l);
-#pragma unroll 1
-    for (int m = 0; m < M; ++m)
-#pragma unroll 1
-        for (int u = (int)threadIdx.x - t0; u >= 0 && u < b.ub - b.ua; u += nt) {
-            const float gt = sh.p1v[(2 * u) * maxr + m], up = sh.p1v[(2 * u + 1) * maxr + m];
-            st_tag(w.act_s + (size_t)m * g.Is + b.ua + u, __float_as_uint(gt / (1.0f + expf(-gt)) * up), tag);
-        }
+        });
 }
 
 // The shared expert's down rows held in the prefetch buffer, by the `nw`
@@ -1986,7 +1592,7 @@ __device__ void shared_down_light(const KParams &kp, const Sh &sh, const Ws &w, 
 {
     const Geo &g = kp.g;
     const int M = kp.M, lane = threadIdx.x & 31;
-    stage_acts(sh, M, g.Is, rank * 32 + lane, nw * 32, layer_tag(kp, l),
+    stage_acts(sh, M, g.Is, rank * 32 + lane, nw * 32, layer_tag(sh, l),
                [&](int p) -> const uint64_t * { return w.act_s + (size_t)p * g.Is; });
     asm volatile("bar.sync 4, %0;" ::"r"(nw * 32) : "memory");
     const uint32_t all = (1u << M) - 1u;
@@ -2029,7 +1635,7 @@ __device__ void phase2(const KParams &kp, const Sh &sh, const LayerPtrs &Lp, Cur
 {
     const Geo &g = kp.g;
     const int maxr = kp.ws_l.maxr;
-    const unsigned tag = layer_tag(kp, l);
+    const unsigned tag = layer_tag(sh, l);
     StageTrace tr{kp.trace ? &kp : nullptr, l, 0, 2, 1};
     n2 = 0;
     turn0 = q.turn;
@@ -2042,35 +1648,46 @@ __device__ void phase2(const KParams &kp, const Sh &sh, const LayerPtrs &Lp, Cur
     });
 }
 
-// P3: per part (see p3_parts), the slot's activations from the CTAs that
-// computed them (tagged, waited for), then the part's down stages; the
-// outputs go to the workspace as tagged words, y[pair][h] for pair =
-// slot_rowbase[s] + rank of the row in the slot's mask.
+// P3: the routed down rows of this CTA's output slice.  The activations of
+// the selected experts (tagged words from the CTAs that computed them, waited
+// for) are staged in batches of whole slots, as many pairs as the staging
+// buffer holds; then each slot's down stage gives yl[pair][h] for the
+// slot's rows (pair = slot_rowbase[s] + rank of the row in the slot's mask).
 __device__ bool phase3(const KParams &kp, const Sh &sh, const LayerPtrs &Lp, Cursor &q, const Ws &w, int l)
 {
     const Geo &g = kp.g;
-    const int maxr = kp.ws_l.maxr;
-    const unsigned tag = layer_tag(kp, l);
+    const int maxr = kp.ws_l.maxr, U = sh.flags[1], hr = sh.hrows;
+    const unsigned tag = layer_tag(sh, l);
     StageTrace tr{kp.trace ? &kp : nullptr, l, 0, 7, 1};
-    P3Part pt[2];
-    const int np = p3_parts(kp, sh, pt);
+    int s0 = 0;
 #pragma unroll 1
-    for (int i = 0; i < np; ++i) {
-        const int s = pt[i].s;
-        const uint32_t mask = sh.slot_mask[s];
+    while (s0 < U) {
+        int s1 = s0;
+        const int p0 = sh.slot_rowbase[s0];
+        while (s1 < U && sh.slot_rowbase[s1 + 1] - p0 <= sh.act_pairs) ++s1;
+        const int np = sh.slot_rowbase[s1] - p0;
         cbar();
-        // pair p of the slot: token row __fns(mask, 0, p + 1)
-        stage_acts(sh, __popc(mask), g.I, threadIdx.x, NCT, tag, [&](int p) -> const uint64_t * {
-            return w.act + ((size_t)s * maxr + __fns(mask, 0, p + 1)) * g.I;
+        // staged pair p -> (slot, token row)
+#pragma unroll 1
+        for (int s = s0 + (int)threadIdx.x; s < s1; s += NCT) {
+            uint32_t mk = sh.slot_mask[s];
+#pragma unroll 1
+            for (int p = sh.slot_rowbase[s] - p0; mk; mk &= mk - 1u, ++p) sh.pair_src[p] = s * kMaxRows + __ffs(mk) - 1;
+        }
+        cbar();
+        stage_acts(sh, np, g.I, threadIdx.x, NCT, tag, [&](int p) -> const uint64_t * {
+            const int ps = sh.pair_src[p];
+            return w.act + ((size_t)(ps / kMaxRows) * maxr + ps % kMaxRows) * g.I;
         });
         if (cbar_or(aborted(sh))) return false;
-        uint64_t *y = w.y + (size_t)sh.slot_rowbase[s] * g.H;
-        sched_p3(kp, sh, Lp, [&](const uint8_t *, int, int ss, int first, int n) {
-            if (ss != s) return;
+        sched_p3(kp, sh, Lp, [&](const uint8_t *, int, int s, int first, int n) {
+            if (s < s0 || s >= s1) return;
             consume(sh, q, 30, [&](const uint8_t *st) {
-                dn_rows(sh, g.rb, st, n, g.d_bytes, g.I, mask, 0, y + first, 1, g.H, tag);
+                dn_rows(sh, g.rb, st, n, g.d_bytes, g.I, sh.slot_mask[s], sh.slot_rowbase[s] - p0,
+                        sh.yl + (size_t)sh.slot_rowbase[s] * hr + first, 1, hr, 0u);
             }, &tr);
         });
+        s0 = s1;
     }
     cbar();
     return true;
@@ -2078,40 +1695,26 @@ __device__ bool phase3(const KParams &kp, const Sh &sh, const LayerPtrs &Lp, Cur
 
 // out = x + sum_j w_j y_j (expert-id order) + sigma y_shared for this CTA's
 // outputs; thread t holds the row pair (2 pl, 2 pl + 1) of token row m,
-// t = pl * M + m, with residuals xr.  The routed outputs y_j come from the
-// CTAs that computed them (tagged words, waited for; eight experts' pairs
-// loaded at a time).  Outputs of layers before the last go out as tagged
-// bf16 pairs, the last one as plain bf16.
-__device__ void combine(const KParams &kp, const Sh &sh, const Ws &w, int l, const float (&xr)[2], uint64_t *tagged,
+// t = pl * M + m, with residuals xr.  Every y_j of these outputs was computed
+// by this CTA (P3).  The bf16 pairs go out as tagged words (the next layer's
+// input, or the input of the final RMSNorm) and, for the last layer, as
+// plain bf16 to `plain`.
+__device__ void combine(const KParams &kp, const Sh &sh, int l, const float (&xr)[2], uint64_t *tagged,
                         uint16_t *plain)
 {
     const Geo &g = kp.g;
-    const int M = kp.M, k = g.k, t = threadIdx.x;
+    const int M = kp.M, k = g.k, t = threadIdx.x, hr = sh.hrows;
     const int h0 = sh.cp->h0, np = sh.cp->nh / 2;
-    const unsigned tag = layer_tag(kp, l);
+    const unsigned tag = layer_tag(sh, l);
     if (t >= np * M) return;
     const int pl = t / M, m = t % M;
     float acc[2] = {0.f, 0.f};
 #pragma unroll 1
-    for (int j0 = 0; j0 < k; j0 += 8) {
-        const int nj = min(8, k - j0);
-        uint32_t a[4], b[4], c[4], d[4];
-        const uint64_t *p[8];
-#pragma unroll
-        for (int jj = 0; jj < 8; ++jj)
-            p[jj] = jj < nj ? w.y + (size_t)sh.row_pair[m * kMaxK + j0 + jj] * g.H + h0 + 2 * pl : nullptr;
-        // four experts' word pairs per poll: (p0, p1) and (p2, p3), then the next four
-        poll_pairs4(sh, p[0], p[1], p[2], p[3], tag, 47, a, b);
-        poll_pairs4(sh, p[4], p[5], p[6], p[7], tag, 47, c, d);
-        const uint32_t v[16] = {a[0], a[1], a[2], a[3], b[0], b[1], b[2], b[3],
-                                c[0], c[1], c[2], c[3], d[0], d[1], d[2], d[3]};
-#pragma unroll
-        for (int jj = 0; jj < 8; ++jj)
-            if (jj < nj) {
-                const float wv = sh.row_w[m * kMaxK + j0 + jj];
-                acc[0] = fmaf(wv, __uint_as_float(v[2 * jj]), acc[0]);
-                acc[1] = fmaf(wv, __uint_as_float(v[2 * jj + 1]), acc[1]);
-            }
+    for (int j = 0; j < k; ++j) {
+        const float wv = sh.row_w[m * kMaxK + j];
+        const float *y = sh.yl + (size_t)sh.row_pair[m * kMaxK + j] * hr + 2 * pl;
+        acc[0] = fmaf(wv, y[0], acc[0]);
+        acc[1] = fmaf(wv, y[1], acc[1]);
     }
     uint32_t o[2];
 #pragma unroll
@@ -2123,51 +1726,27 @@ __device__ void combine(const KParams &kp, const Sh &sh, const Ws &w, int l, con
     }
     const uint32_t pair = o[0] | (o[1] << 16);
     if (tagged) st_tag(tagged + (size_t)m * (g.H / 2) + h0 / 2 + pl, pair, tag);
-    else *reinterpret_cast<uint32_t *>(plain + (size_t)m * g.H + h0 + 2 * pl) = pair;
+    if (plain) *reinterpret_cast<uint32_t *>(plain + (size_t)m * g.H + h0 + 2 * pl) = pair;
 }
 
-// out_n = bf16(out * rinv * gamma_next) for this CTA's outputs.
-__device__ __noinline__ void write_normed(const KParams &kp, const Sh &sh, const uint16_t *out, const uint16_t *gamma_next)
+// out_n = bf16(out * rinv * gamma_next) for this CTA's outputs, with rinv from
+// every CTA's bf16 outputs (tagged words of the last layer): the same
+// computation as the next layer's RMSNorm (build_hn with gamma_next), of
+// which this CTA keeps its own slice.
+__device__ void final_normed(const KParams &kp, const Sh &sh, const uint64_t *xt, unsigned tag,
+                             const uint16_t *gamma_next)
 {
-    const Geo &g = kp.g;
-    const int H = g.H, M = kp.M, tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
-#pragma unroll 1
-    for (int m = lane; m < M; m += 32) sh.red[m * (NCW + 1) + warp] = 0.f;
-    __syncwarp();
-    const int per_row = H / 8, total = M * per_row;
-#pragma unroll 1
-    for (int base = 0; base < total; base += NCT) {
-        const int it = base + tid;
-        float ss = 0.f;
-        if (it < total) {
-            const int m = it / per_row;
-            const uint4 a = __ldcg(reinterpret_cast<const uint4 *>(out + (size_t)m * H) + it % per_row);
-            const uint32_t aw[4] = {a.x, a.y, a.z, a.w};
-#pragma unroll
-            for (int j = 0; j < 4; ++j) {
-                const float lo = __uint_as_float(aw[j] << 16), hi = __uint_as_float(aw[j] & 0xFFFF0000u);
-                ss = fmaf(lo, lo, fmaf(hi, hi, ss));
-            }
-        }
-        ss = warp_sum(ss);
-        const int wfirst = base + warp * 32;
-        if (lane == 0 && wfirst < total) sh.red[(wfirst / per_row) * (NCW + 1) + warp] += ss;
-    }
-    cbar();
-    if (tid < M) {
-        float t = 0.f;
-#pragma unroll 1
-        for (int w2 = 0; w2 < NCW; ++w2) t += sh.red[tid * (NCW + 1) + w2];
-        sh.red[tid * (NCW + 1) + NCW] = rsqrtf(t / (float)H + g.eps);
-    }
-    cbar();
+    const int H = kp.g.H, M = kp.M, G = H / kGroup;
+    build_hn(kp, sh, xt, tag, gamma_next);
+    if (cbar_or(aborted(sh))) return;
     const int h0 = sh.cp->h0, nh = sh.cp->nh;
 #pragma unroll 1
-    for (int t = tid; t < nh * M; t += NCT) {
-        const int hl = t / M, m = t % M;
-        const size_t idx = (size_t)m * H + h0 + hl;
-        const float v = bf2f(__ldcg(out + idx)) * sh.red[m * (NCW + 1) + NCW] * bf2f(gamma_next[h0 + hl]);
-        kp.out_normed[idx] = f2bf(v);
+    for (int t = threadIdx.x; t < nh * M; t += NCT) {
+        const int hl = t / M, m = t % M, h = h0 + hl;
+        // hn_m[h] * 2^100 in the arranged layout: group h / 64, quad (h % 64) / 4
+        const float4 v = sh.xs[(size_t)m * (H / 4) + ((h & 63) >> 2) * G + (h >> 6)];
+        const float c = (h & 3) == 0 ? v.x : (h & 3) == 1 ? v.y : (h & 3) == 2 ? v.z : v.w;
+        kp.out_normed[(size_t)m * H + h] = f2bf(c * 0x1p-100f);
     }
 }
 
@@ -2177,19 +1756,19 @@ __device__ __noinline__ void write_normed(const KParams &kp, const Sh &sh, const
 // (A word is rewritten only after every reader of its previous value is
 // done: CTA A writes layer l + 1's copy only after its P0 of layer l + 1,
 // which read every CTA's layer-l output, written after that CTA's last
-// read of layer l.)  One barrier remains, before the fused final RMSNorm.
+// read of layer l.)  The fused final RMSNorm reads the last layer's output
+// the same way.
 __device__ __forceinline__ void compute(const KParams &kp, const Sh &sh)
 {
     const Ws w = ws_views(kp);
     Cursor q = cursor0();
-    int nsync = 0;
     const int h0 = sh.cp->h0, np = sh.cp->nh / 2, M = kp.M, H = kp.g.H;
     const int warp = threadIdx.x >> 5;
 #pragma unroll 1
     for (int l = 0; l < kp.L; ++l) {
         const LayerPtrs &Lp = kp.layer[l];
         const bool last = l == kp.L - 1;
-        const unsigned xtag = l == 0 ? 0u : layer_tag(kp, l - 1);
+        const unsigned xtag = l == 0 ? 0u : layer_tag(sh, l - 1);
         const void *xin = l == 0 ? static_cast<const void *>(kp.x) : static_cast<const void *>(w.ping[(l - 1) & 1]);
         const bool t0 = threadIdx.x == 0;
         if (t0) stamp(kp, l, 0);
@@ -2233,7 +1812,7 @@ __device__ __forceinline__ void compute(const KParams &kp, const Sh &sh)
             const int nw = r0 == 0 ? NCW : NCW - r0;
             if (r0 == 0 || d >= r0) shared_down_light(kp, sh, w, l, r0 == 0 ? d : d - r0, nw);
         } else if (kp.g.has_shared) {
-            stage_acts(sh, M, kp.g.Is, threadIdx.x, NCT, layer_tag(kp, l),
+            stage_acts(sh, M, kp.g.Is, threadIdx.x, NCT, layer_tag(sh, l),
                        [&](int p) -> const uint64_t * { return w.act_s + (size_t)p * kp.g.Is; });
             cbar();
             shared_down_pb(kp, sh, 0);
@@ -2248,15 +1827,12 @@ __device__ __forceinline__ void compute(const KParams &kp, const Sh &sh)
         if (!phase3(kp, sh, Lp, q, w, l)) return;
         wstamp(kp, l, 10);
         if (cbar_or(aborted(sh))) return;
-        combine(kp, sh, w, l, xr, last ? nullptr : w.ping[l & 1], kp.out);
+        const bool normed = last && kp.out_normed;
+        combine(kp, sh, l, xr, last && !normed ? nullptr : w.ping[l & 1], last ? kp.out : nullptr);
         if (t0) stamp(kp, l, 7);
-        if (last && kp.out_normed) {
-            if (!grid_sync(kp, sh, nsync)) return;
-            write_normed(kp, sh, kp.out, Lp.gamma_next);
-        }
+        if (normed) final_normed(kp, sh, w.ping[l & 1], layer_tag(sh, l), Lp.gamma_next);
         if (t0) stamp(kp, l, 8);
     }
-    kernel_exit(sh);
 }
 
 __global__ void __launch_bounds__(kThreads, 1) moe_decode_kernel(const __grid_constant__ KParams kp)
@@ -2290,13 +1866,13 @@ __global__ void __launch_bounds__(kThreads, 1) moe_decode_kernel(const __grid_co
         sh.row_pair = reinterpret_cast<int *>(smem + L.row_pair);
         sh.red = reinterpret_cast<float *>(smem + L.red);
         sh.lscr = reinterpret_cast<float *>(smem + L.lscr);
-        sh.p1v = reinterpret_cast<float *>(smem + L.p1v);
         sh.pair_src = reinterpret_cast<int *>(smem + L.pair_src);
         sh.xs = reinterpret_cast<float4 *>(smem + L.xs);
         sh.xsum = reinterpret_cast<float *>(smem + L.xsum);
         sh.act = reinterpret_cast<float4 *>(smem + L.act);
         sh.asum = reinterpret_cast<float *>(smem + L.asum);
         sh.ysh = reinterpret_cast<float *>(smem + L.ysh);
+        sh.yl = reinterpret_cast<float *>(smem + L.yl);
         sh.pb = smem + L.pb;
         sh.ring = smem + L.ring;
         sh.NS = kp.p.NS;
@@ -2305,6 +1881,7 @@ __global__ void __launch_bounds__(kThreads, 1) moe_decode_kernel(const __grid_co
         sh.act_pairs = kp.p.act_pairs;
         sh.timeout_ns = kp.timeout_ns;
         sh.ctrl = reinterpret_cast<Ctrl *>(kp.ws);
+        sh.epoch = *reinterpret_cast<volatile unsigned *>(&sh.ctrl->seq) * 64u;
 #pragma unroll 1
         for (int i = 0; i < kp.p.NS; ++i) {
             mbar_init(&sh.full[i], 1);
@@ -2324,26 +1901,11 @@ __global__ void __launch_bounds__(kThreads, 1) moe_decode_kernel(const __grid_co
         return;
     }
     compute(kp, sh);
+    if (threadIdx.x == 0) kernel_exit(kp, sh);
 }
 
 int g_num_sms[64];
 bool g_attr_set[64];
-
-// Tag ranges of successive launches: 64 tags each (one per layer), from a
-// start drawn from the clock and the process id, so that words a previous
-// process left in reused device memory are unlikely to match.
-unsigned next_epoch()
-{
-    static std::atomic<unsigned> counter{0u};
-    static std::once_flag once;
-    std::call_once(once, [] {
-        const unsigned long long t = (unsigned long long)std::chrono::steady_clock::now().time_since_epoch().count();
-        counter.store((unsigned)((t ^ (t >> 32) ^ ((unsigned long long)getpid() << 16)) & ~63ull));
-    });
-    unsigned e = counter.fetch_add(64u);
-    if (e == 0u - 64u) e = counter.fetch_add(64u);   // tags epoch + 1 .. epoch + 64 never wrap to 0
-    return e;
-}
 
 }  // namespace
 
@@ -2362,7 +1924,7 @@ bool make_plan(const Geo &g, int maxr, int num_sms, Plan &p)
     int maxi = 2 * g.g_bytes;
     if (g.d_bytes > maxi) maxi = g.d_bytes;
     if (g.has_shared) {
-        if (g.sg_bytes > maxi) maxi = g.sg_bytes;
+        if (2 * g.sg_bytes > maxi) maxi = 2 * g.sg_bytes;   // one shared unit per stage at least
         if (g.sd_bytes > maxi) maxi = g.sd_bytes;
     }
     const int Im = imax_of(g);
@@ -2446,11 +2008,8 @@ int launch_decode(const KParams &kp, cudaStream_t stream)
     attr[0].val.cooperative = 1;
     cfg.attrs = attr;
     cfg.numAttrs = 1;
-    // a fresh tag range for this launch: words left in the workspace by
-    // earlier launches never carry one of its tags
-    KParams kl = kp;
-    kl.epoch = next_epoch();
-    e = cudaLaunchKernelEx(&cfg, moe_decode_kernel, kl);
+    // the launch's tags come from the workspace's launch sequence (device side)
+    e = cudaLaunchKernelEx(&cfg, moe_decode_kernel, kp);
     note_launch();
     if (e != cudaSuccess) { note_cuda_error((int)e); return MOE_ERR_CUDA; }
     return MOE_OK;

@@ -145,18 +145,32 @@ def rows_equal_one_row_calls(layer, x, out):
 
 def test_a35b_m4_rows_equal_m1_bitwise():
     """1 token + 3 correlated draft rows: every row equals the one-row call bit
-    for bit (PureDrive model card, "How it works": row-exact verify), and the
-    rows share 30-60 % of their experts (the M=4 workload's correlation)."""
+    for bit (PureDrive model card, "How it works": row-exact verify)."""
     shape = synth.A35B
     L, layer, lay = cached(shape, 11)
     x = rows_with_margin(shape, lay, 3, 4, correlation=0.6, gamma=L["gamma"])
     out4, ref = check_layer(shape, L, layer, lay, x)
     rows_equal_one_row_calls(layer, x, out4)
-    # experts chosen by two or more rows, as a fraction of the distinct experts
-    idx = ref["idx"]
-    union = set(idx.ravel().tolist())
-    shared = sum(1 for e in union if (idx == e).any(axis=1).sum() >= 2)
-    assert 0.3 <= shared / len(union) <= 0.6, (shared, len(union))
+
+
+def test_a35b_m4_shared_fraction():
+    """The M=4 workload (1 token + 3 draft rows at correlation 0.6): over 32
+    draws, the experts chosen by two or more rows make up 30-60 % of the
+    distinct experts on average (the GPU's routing)."""
+    shape = synth.A35B
+    L, layer, lay = cached(shape, 11)
+    ws = moe.Workspace(layer.desc, 4)
+    fr = []
+    for seed in range(32):
+        x = synth.make_rows(shape, 7000 + seed, 4, correlation=0.6, gamma=L["gamma"]).to(DEV)
+        idx, _ = moe.router_topk(layer, x, ws)
+        idx = idx.cpu().numpy()
+        union = set(idx.ravel().tolist())
+        shared = sum(1 for e in union if (idx == e).any(axis=1).sum() >= 2)
+        fr.append(shared / len(union))
+    assert ws.status() == 0
+    print(f"shared fraction at M=4: mean {np.mean(fr):.3f}, min {min(fr):.3f}, max {max(fr):.3f}")
+    assert 0.3 <= float(np.mean(fr)) <= 0.6
 
 
 def test_a35b_m8():

@@ -82,7 +82,7 @@ constexpr int kShBytes = 512;
 
 struct SmemLayout {
     int shs, cplan, bar, flags, slot_e, slot_mask, slot_rowbase, sigma, eslot, emask, topv, tope, topw;
-    int row_w, row_pair, red, lscr, pair_src, xs, xsum, act, asum, ysh, yl, pb, ring, total;
+    int row_w, row_pair, red, rred, lscr, pair_src, xs, xsum, act, asum, ysh, yl, pb, ring, total;
 };
 
 __host__ __device__ inline int take(int &o, int bytes, int align)
@@ -94,6 +94,10 @@ __host__ __device__ inline int take(int &o, int bytes, int align)
 }
 
 __host__ __device__ inline int imax_of(const Geo &g) { return g.Is > g.I ? g.Is : g.I; }
+
+// Router rows a CTA computes inside the RMSNorm pass (fp32 or 8-bit
+// routers, at most this many rows per CTA; otherwise P1 computes them).
+constexpr int kFusedRouterRows = 4;
 
 // Router rows / shared units taken by one CTA at most.
 __host__ __device__ inline int per_cta(int n, int P) { return (n + P - 1) / P; }
@@ -119,6 +123,7 @@ __host__ __device__ inline SmemLayout carve(const Geo &g, const Plan &p)
     L.row_w = take(o, kMaxRows * kMaxK * 4, 4);
     L.row_pair = take(o, kMaxRows * kMaxK * 4, 4);
     L.red = take(o, kMaxRows * (NCW + 1) * 4, 4);
+    L.rred = take(o, kMaxRows * kFusedRouterRows * NCW * 4, 4);
     L.lscr = take(o, NCW * kMaxRows * 4, 4);
     L.pair_src = take(o, p.act_pairs * 4, 4);
     L.xs = take(o, p.maxr * g.H * 4, 16);
@@ -323,6 +328,7 @@ struct Sh {
     float *row_w;        // [kMaxRows][kMaxK]  by expert id
     int *row_pair;
     float *red;          // [kMaxRows][NCW + 1] RMSNorm partial sums, then 1/rms
+    float *rred;         // [kMaxRows][kFusedRouterRows][NCW] router partial sums per warp
     float *lscr;         // [NCW][kMaxRows] a warp's router logits before they go out
     int *pair_src;       // [act_pairs] slot * kMaxRows + row of each staged pair
     float4 *xs;          // [maxr][H / 4] arranged hn * 2^100
@@ -418,41 +424,46 @@ __device__ __forceinline__ bool poll_more(const Sh &sh, unsigned it, unsigned lo
     return true;
 }
 
-// Two items of four consecutive tagged words each (pa, pb 16-byte aligned;
-// null for no item): payloads into a and b.  All eight words are loaded
-// together; while some are missing, the lane polls the first missing one
-// alone (many CTAs poll the same words: fewer requests while waiting) and
-// then loads all eight again.  Bounded (poll_more); payloads are 0 after a
-// timeout.
-__device__ __forceinline__ void poll_tag8(const Sh &sh, const uint64_t *pa, const uint64_t *pb, unsigned tag, int where,
-                                          uint32_t (&a)[4], uint32_t (&b)[4])
+// N items of four consecutive tagged words each (16-byte aligned; null for
+// no item): payloads into out[n].  All words are loaded together; while some
+// are missing, the lane polls the first missing one alone (many CTAs poll the
+// same words: fewer requests while waiting) and then loads all of them
+// again.  Bounded (poll_more); payloads are 0 after a timeout.
+template <int N>
+__device__ __forceinline__ void poll_items(const Sh &sh, const uint64_t *const (&p)[N], unsigned tag, int where,
+                                           uint32_t (&out)[N][4])
 {
     const uint64_t none = (uint64_t)tag << 32;
-    uint64_t v[8];
+    uint64_t v[N][4];
     unsigned long long t0 = 0;
     unsigned it = 0;
 #pragma unroll 1
     for (;;) {
 #pragma unroll
-        for (int j = 0; j < 8; ++j) v[j] = none;
-        if (pa) { ld_tag2(pa, v[0], v[1]); ld_tag2(pa + 2, v[2], v[3]); }
-        if (pb) { ld_tag2(pb, v[4], v[5]); ld_tag2(pb + 2, v[6], v[7]); }
+        for (int n = 0; n < N; ++n) {
+            v[n][0] = v[n][1] = v[n][2] = v[n][3] = none;
+            if (p[n]) { ld_tag2(p[n], v[n][0], v[n][1]); ld_tag2(p[n] + 2, v[n][2], v[n][3]); }
+        }
         const uint64_t *pm = nullptr;
 #pragma unroll
-        for (int j = 7; j >= 0; --j)
-            if ((unsigned)(v[j] >> 32) != tag) pm = j < 4 ? pa + j : pb + (j - 4);
+        for (int n = N - 1; n >= 0; --n)
+#pragma unroll
+            for (int j = 3; j >= 0; --j)
+                if ((unsigned)(v[n][j] >> 32) != tag) pm = p[n] + j;
         if (!pm) break;
         bool more = true;
 #pragma unroll 1
         while ((more = poll_more(sh, ++it, t0, where)) && (unsigned)(ld_tag(pm) >> 32) != tag) {}
         if (!more) {
 #pragma unroll
-            for (int j = 0; j < 8; ++j) v[j] = 0;
+            for (int n = 0; n < N; ++n) v[n][0] = v[n][1] = v[n][2] = v[n][3] = 0;
             break;
         }
     }
 #pragma unroll
-    for (int j = 0; j < 4; ++j) { a[j] = (uint32_t)v[j]; b[j] = (uint32_t)v[4 + j]; }
+    for (int n = 0; n < N; ++n)
+#pragma unroll
+        for (int j = 0; j < 4; ++j) out[n][j] = (uint32_t)v[n][j];
 }
 
 // End of a launch for one CTA (thread 0, once its compute warps are done,
@@ -533,6 +544,16 @@ __device__ __forceinline__ float ldsf1(uint32_t a)
     return v;
 }
 
+template <int BITS>
+__device__ __forceinline__ void load_group(uint32_t row, int g, uint32_t (&w)[2 * BITS])
+{
+#pragma unroll
+    for (int i = 0; i < BITS / 2; ++i) {
+        const uint4 v = lds4(row + g * 8 * BITS + 16 * i);
+        w[4 * i] = v.x; w[4 * i + 1] = v.y; w[4 * i + 2] = v.z; w[4 * i + 3] = v.w;
+    }
+}
+
 __device__ __forceinline__ void scale_bias(uint32_t row, int K, int bits, int g, float &s, float &b)
 {
     const uint32_t sbw = lds1(row + K * bits / 8 + g * 4);
@@ -572,17 +593,384 @@ __device__ __forceinline__ uint2 lds2(uint32_t a)
     return v;
 }
 
-// Sub-group of group g visited at position v (0 .. 3).  At 8 and 4 bits a
-// group is 64 or 32 bytes, so the same 16-byte chunk of neighbouring lanes'
-// groups falls on the same shared-memory banks; each lane starts at a
-// different chunk instead.  At 6 bits the 48-byte stride already spreads the
-// banks; lanes 8 .. 15 of each half warp start with the other pair of
-// sub-groups so that 8-byte loads spread them too.
+// Visits the 4 sub-groups of group g of NROWS rows: f(sg, parity, words[n])
+// with words[n] the sub-group's BITS/2 code words of row n and parity a
+// compile-time visit parity (0, 1).  Two sub-groups per loop trip, the loop
+// not unrolled: the kernel's code then stays small enough to remain in the
+// instruction caches between layers.
+template <int BITS, int NROWS, typename F>
+__device__ __forceinline__ void for_subgroups(const uint32_t (&rp)[NROWS], int g, F &&f)
+{
+    if constexpr (BITS == 6) {
+        // 24 bytes (two sub-groups) per trip; lanes 8 .. 15 of each half warp
+        // start with the other pair so that 8-byte loads spread the banks
+        const int rot = (g >> 3) & 1;
+#pragma unroll 1
+        for (int j = 0; j < 2; ++j) {
+            const int jj = j ^ rot;
+            uint32_t w[NROWS][6];
+#pragma unroll
+            for (int n = 0; n < NROWS; ++n) {
+                const uint32_t a = rp[n] + g * 48 + 24 * jj;
+                const uint2 v0 = lds2(a), v1 = lds2(a + 8), v2 = lds2(a + 16);
+                w[n][0] = v0.x; w[n][1] = v0.y; w[n][2] = v1.x; w[n][3] = v1.y; w[n][4] = v2.x; w[n][5] = v2.y;
+            }
+            const uint32_t *w0[NROWS], *w1[NROWS];
+#pragma unroll
+            for (int n = 0; n < NROWS; ++n) { w0[n] = &w[n][0]; w1[n] = &w[n][3]; }
+            f(2 * jj, 0, w0);
+            f(2 * jj + 1, 1, w1);
+        }
+    } else if constexpr (BITS == 8) {
+        // one 16-byte chunk per sub-group, two per trip
+        const int rot = chunk_rot<8>(g);
+#pragma unroll 1
+        for (int j = 0; j < 2; ++j) {
+            const int c0 = (2 * j + rot) & 3, c1 = (2 * j + 1 + rot) & 3;
+            uint32_t w[NROWS][8];
+#pragma unroll
+            for (int n = 0; n < NROWS; ++n) {
+                const uint4 v0 = lds4(rp[n] + g * 64 + 16 * c0), v1 = lds4(rp[n] + g * 64 + 16 * c1);
+                w[n][0] = v0.x; w[n][1] = v0.y; w[n][2] = v0.z; w[n][3] = v0.w;
+                w[n][4] = v1.x; w[n][5] = v1.y; w[n][6] = v1.z; w[n][7] = v1.w;
+            }
+            const uint32_t *w0[NROWS], *w1[NROWS];
+#pragma unroll
+            for (int n = 0; n < NROWS; ++n) { w0[n] = &w[n][0]; w1[n] = &w[n][4]; }
+            f(c0, 0, w0);
+            f(c1, 1, w1);
+        }
+    } else {
+        // 4 bits: a 16-byte chunk holds two sub-groups
+        const int rot = chunk_rot<4>(g);
+#pragma unroll 1
+        for (int j = 0; j < 2; ++j) {
+            const int c = (j + rot) & 1;
+            uint32_t w[NROWS][4];
+#pragma unroll
+            for (int n = 0; n < NROWS; ++n) {
+                const uint4 v = lds4(rp[n] + g * 32 + 16 * c);
+                w[n][0] = v.x; w[n][1] = v.y; w[n][2] = v.z; w[n][3] = v.w;
+            }
+            const uint32_t *w0[NROWS], *w1[NROWS];
+#pragma unroll
+            for (int n = 0; n < NROWS; ++n) { w0[n] = &w[n][0]; w1[n] = &w[n][2]; }
+            f(2 * c, 0, w0);
+            f(2 * c + 1, 1, w1);
+        }
+    }
+}
+
+// acc[n][r] += dot(row n, group g) . x_r for NROWS weight rows and NR token
+// rows, with per-class accumulators (split by visit parity at 4 and 8 bits,
+// which have few classes, for more independent chains).  The codes are
+// extracted once for all token rows; each token row's arithmetic is the
+// same whatever NR is, so a row's result does not depend on the other rows
+// of the call (row-exact).
+template <int BITS, int NROWS, int NR>
+__device__ __forceinline__ void grp_cls(const uint32_t (&rp)[NROWS], int g, int K, int G, const uint32_t (&xq)[NR],
+                                        const float (&xsum)[NR], float (&acc)[NROWS][NR])
+{
+    using PT = Pairs<BITS>;
+    constexpr int NC = PT::NC, NA = BITS == 6 ? NC : 2 * NC;
+    float s[NROWS], b[NROWS];
+#pragma unroll
+    for (int n = 0; n < NROWS; ++n) scale_bias(rp[n], K, BITS, g, s[n], b[n]);
+    float2 A[NROWS][NR][NA];
+#pragma unroll
+    for (int n = 0; n < NROWS; ++n)
+#pragma unroll
+        for (int r = 0; r < NR; ++r)
+#pragma unroll
+            for (int c = 0; c < NA; ++c) A[n][r][c] = make_float2(0.f, 0.f);
+    const uint32_t G16 = G * 16;
+    for_subgroups<BITS, NROWS>(rp, g, [&](int sg, int step, const uint32_t *const (&ws)[NROWS]) {
+        float4 xv[NR][4];
+#pragma unroll
+        for (int r = 0; r < NR; ++r)
+#pragma unroll
+            for (int t = 0; t < 4; ++t) xv[r][t] = ldsf4(xq[r] + g * 16 + (4 * sg + t) * G16);
+        const int half = NA > NC ? step * NC : 0;
+#pragma unroll
+        for (int n = 0; n < NROWS; ++n)
+            PT::each(ws[n], [&](int i, float a, float bb) {
+                const float2 q = make_float2(a, bb);
+#pragma unroll
+                for (int r = 0; r < NR; ++r)
+                    A[n][r][PT::cls(i) + half] =
+                        __ffma2_rn(q, xpair(xv[r][i >> 1], i & 1), A[n][r][PT::cls(i) + half]);
+            });
+    });
+#pragma unroll
+    for (int n = 0; n < NROWS; ++n)
+#pragma unroll
+        for (int r = 0; r < NR; ++r) {
+            float t = 0.f;
+#pragma unroll
+            for (int c = 0; c < NA; ++c) {
+                const int i0 = first_of_class<PT>(c % NC);
+                t = fmaf(A[n][r][c].x, __uint_as_float(cls_bits(PT::pa(i0))), t);
+                t = fmaf(A[n][r][c].y, __uint_as_float(cls_bits(PT::pb(i0))), t);
+            }
+            acc[n][r] = fmaf(s[n], t, fmaf(b[n], xsum[r], acc[n][r]));
+        }
+}
+
+// fp32 rows (a router given in fp32): K floats per row.
+template <int NROWS, int NR>
+__device__ __forceinline__ void grp_f32(const uint32_t (&rp)[NROWS], int g, int G,
+                                        const uint32_t (&xq)[NR], float (&acc)[NROWS][NR])
+{
+#pragma unroll
+    for (int n = 0; n < NROWS; ++n) {
+        float S[NR];
+#pragma unroll
+        for (int r = 0; r < NR; ++r) S[r] = 0.f;
+#pragma unroll 4
+        for (int t = 0; t < 16; ++t) {
+            const float4 wq = ldsf4(rp[n] + (g * 16 + t) * 16);
+#pragma unroll
+            for (int r = 0; r < NR; ++r) {
+                const float4 x = ldsf4(xq[r] + (t * G + g) * 16);
+                S[r] = fmaf(wq.x, x.x, fmaf(wq.y, x.y, fmaf(wq.z, x.z, fmaf(wq.w, x.w, S[r]))));
+            }
+        }
+#pragma unroll
+        for (int r = 0; r < NR; ++r) acc[n][r] = fmaf(S[r], 0x1p-100f, acc[n][r]);
+    }
+}
+
+// A warp computes rows [0, nrows) (row i at base + i * rstride, K inputs
+// at BITS bits) against NR arranged token vectors.  Lanes split a row's
+// groups (LPR lanes per row, GPL groups per lane); each lane takes NROWS
+// consecutive rows.  emit(first_row, acc) runs on the first lane of each
+// row group with the complete sums of rows first_row .. first_row+NROWS-1
+// (rows at or past nrows hold repeats of the last row and must be ignored).
+template <int BITS, int NROWS, int NR, typename F>
+__device__ __forceinline__ void warp_rows(const uint8_t *base, int rstride, int nrows, int K,
+                                          const uint32_t (&xq)[NR], const float (&xsg)[NR][kMaxGPL],
+                                          F &&emit)
+{
+    const int lane = threadIdx.x & 31;
+    const uint32_t sbase = smem_u32(base);
+    // K and G are powers of two: shifts instead of divisions
+    const int G = K >> 6, lgG = ilog2(G), lgL = lgG < 5 ? lgG : 5;
+    const int LPR = 1 << lgL, GPL = G >> lgL, RPP = 32 >> lgL;
+    const int lg = lane & (LPR - 1), lr = lane >> lgL;
+    for (int r0 = 0; r0 < nrows; r0 += RPP * NROWS) {
+        const int rb = r0 + lr * NROWS;
+        uint32_t rp[NROWS];
+#pragma unroll
+        for (int n = 0; n < NROWS; ++n) rp[n] = sbase + (uint32_t)(min(rb + n, nrows - 1) * rstride);
+        float acc[NROWS][NR];
+#pragma unroll
+        for (int n = 0; n < NROWS; ++n)
+#pragma unroll
+            for (int r = 0; r < NR; ++r) acc[n][r] = 0.f;
+        if (rb < nrows) {
+            for (int j = 0; j < GPL; ++j) {
+                const int g = lg + LPR * j;
+                if constexpr (BITS == 0) {
+                    grp_f32<NROWS, NR>(rp, g, G, xq, acc);
+                } else {
+                    float xs[NR];
+#pragma unroll
+                    for (int r = 0; r < NR; ++r) xs[r] = xsg[r][j];
+                    grp_cls<BITS, NROWS, NR>(rp, g, K, G, xq, xs, acc);
+                }
+            }
+        }
+        for (int o = LPR >> 1; o >= 1; o >>= 1)
+#pragma unroll
+            for (int n = 0; n < NROWS; ++n)
+#pragma unroll
+                for (int r = 0; r < NR; ++r) acc[n][r] += __shfl_xor_sync(FULLMASK, acc[n][r], o);
+        if (lg == 0 && rb < nrows) emit(rb, acc);
+    }
+}
+
+// Per-lane group sums of NR arranged vectors (sums[soff[r] + g] layout).
+template <int NR>
+__device__ __forceinline__ void lane_gsums(uint32_t sums, const int (&soff)[NR], int K, float (&xsg)[NR][kMaxGPL])
+{
+    const int lane = threadIdx.x & 31;
+    const int G = K >> 6, lgG = ilog2(G), lgL = lgG < 5 ? lgG : 5;
+    const int LPR = 1 << lgL, GPL = G >> lgL, lg = lane & (LPR - 1);
+#pragma unroll
+    for (int r = 0; r < NR; ++r)
+#pragma unroll
+        for (int j = 0; j < kMaxGPL; ++j) xsg[r][j] = j < GPL ? ldsf1(sums + 4 * (soff[r] + lg + LPR * j)) : 0.f;
+}
+
+// Token rows first .. first + NR - 1 of a row mask (in set-bit order),
+// padded with the last one.
+template <int NR>
+__device__ __forceinline__ void rows_of_group(uint32_t mask, int first, int (&rows)[NR], int &nvalid)
+{
+    for (int i = 0; i < first; ++i) mask &= mask - 1;
+    nvalid = 0;
+    int last = 0;
+#pragma unroll
+    for (int r = 0; r < NR; ++r) {
+        if (mask) {
+            last = __ffs(mask) - 1;
+            mask &= mask - 1;
+            ++nvalid;
+        }
+        rows[r] = last;
+    }
+}
+
+// Row groups of a mask: pairs, then a single row.
+template <typename F>
+__device__ __forceinline__ void for_row_groups(uint32_t mask, F &&f)
+{
+    const int n = __popc(mask);
+    int g0 = 0;
+    for (; n - g0 >= 2; g0 += 2) f(g0, 2);
+    if (n - g0 == 1) f(g0, 1);
+}
+
+// The warp-level row kernels below are separate (not inlined) functions,
+// one per (bits, token rows): each gets its own register allocation, and a
+// call is made once per stage and row group, not per weight.
+
+// Gate/up units [0, cnt) at `units` (unit u: gate row then up row, row
+// bytes rowb, K = H inputs) for token rows g0 .. of `mask` against hn:
+// dst[m * ld + u] = silu(gate) * up.
+template <int B, int R>
+__device__ __forceinline__ void gu_k_body(const float4 *xs, const float *xsum, int H, const uint8_t *units, int cnt,
+                                  int rowb, uint32_t mask, int g0, uint64_t *dst, int ld, unsigned tag)
+{
+    const int G = H / kGroup;
+    int rows[R], nv;
+    rows_of_group<R>(mask, g0, rows, nv);
+    uint32_t xq[R];
+    int soff[R];
+#pragma unroll
+    for (int r = 0; r < R; ++r) { xq[r] = smem_u32(xs) + (uint32_t)(rows[r] * H * 4); soff[r] = rows[r] * G; }
+    float xsg[R][kMaxGPL];
+    lane_gsums<R>(smem_u32(xsum), soff, H, xsg);
+    constexpr int NROWS = R == 1 ? 4 : 2;   // whole units (gate and up row) per lane
+    warp_rows<B, NROWS, R>(units, rowb, 2 * cnt, H, xq, xsg, [&](int rb, const float (&acc)[NROWS][R]) {
+#pragma unroll
+        for (int k2 = 0; k2 < NROWS; k2 += 2) {
+            if (rb + k2 + 1 < 2 * cnt) {
+#pragma unroll
+                for (int r = 0; r < R; ++r)
+                    if (r < nv) {
+                        const float gt = acc[k2][r], up = acc[k2 + 1][r];
+                        st_tag(dst + (size_t)rows[r] * ld + ((rb + k2) >> 1),
+                               __float_as_uint(gt / (1.0f + expf(-gt)) * up), tag);
+                    }
+            }
+        }
+    });
+}
+
+// One row of K = H inputs (a router row, or a gate or up row of a shared
+// unit) for token rows g0 .. of `mask`: dst[m * ms] = row . hn_m.
+template <int B, int R>
+__device__ __forceinline__ void one_k_body(const float4 *xs, const float *xsum, int H, const uint8_t *row, uint32_t mask,
+                                   int g0, void *dst, int ms, unsigned tag)
+{
+    const int G = H / kGroup;
+    int rows[R], nv;
+    rows_of_group<R>(mask, g0, rows, nv);
+    uint32_t xq[R];
+    int soff[R];
+#pragma unroll
+    for (int r = 0; r < R; ++r) { xq[r] = smem_u32(xs) + (uint32_t)(rows[r] * H * 4); soff[r] = rows[r] * G; }
+    float xsg[R][kMaxGPL];
+    lane_gsums<R>(smem_u32(xsum), soff, H, xsg);
+    warp_rows<B, 1, R>(row, 0, 1, H, xq, xsg, [&](int, const float (&acc)[1][R]) {
+#pragma unroll
+        for (int r = 0; r < R; ++r)
+            if (r < nv) {
+                if (tag) st_tag(static_cast<uint64_t *>(dst) + (size_t)rows[r] * ms, __float_as_uint(acc[0][r]), tag);
+                else static_cast<float *>(dst)[(size_t)rows[r] * ms] = acc[0][r];
+            }
+    });
+}
+
+// Stores v at element i of dst: a plain fp32 array, or (tag != 0) tagged words.
+__device__ __forceinline__ void put_out(void *dst, size_t i, float v, unsigned tag)
+{
+    if (tag) st_tag(static_cast<uint64_t *>(dst) + i, __float_as_uint(v), tag);
+    else static_cast<float *>(dst)[i] = v;
+}
+
+// Down rows [0, cnt) (K inputs each) against the staged activation pairs
+// pair0 + t, t = g0 .. (t < popc(mask)): dst[h * hs + t * ts] (see put_out).
+template <int B, int R>
+__device__ __forceinline__ void dn_k_body(const float4 *act, const float *asum, int K, const uint8_t *rows0, int cnt,
+                                  int rowb, uint32_t mask, int pair0, int g0, void *dst, int hs, int ts, unsigned tag)
+{
+    const int Gi = K / kGroup, n = __popc(mask);
+    int tp[R];
+    int nv = 0;
+#pragma unroll
+    for (int r = 0; r < R; ++r) {
+        tp[r] = g0 + r < n ? g0 + r : n - 1;
+        nv += g0 + r < n ? 1 : 0;
+    }
+    uint32_t xq[R];
+    int soff[R];
+#pragma unroll
+    for (int r = 0; r < R; ++r) {
+        xq[r] = smem_u32(act) + (uint32_t)((pair0 + tp[r]) * K * 4);
+        soff[r] = (pair0 + tp[r]) * Gi;
+    }
+    float xsg[R][kMaxGPL];
+    lane_gsums<R>(smem_u32(asum), soff, K, xsg);
+    constexpr int NROWS = R == 1 ? 2 : 1;   // (down rows: any count)
+    warp_rows<B, NROWS, R>(rows0, rowb, cnt, K, xq, xsg, [&](int rb, const float (&acc)[NROWS][R]) {
+#pragma unroll
+        for (int k2 = 0; k2 < NROWS; ++k2)
+            if (rb + k2 < cnt) {
+#pragma unroll
+                for (int r = 0; r < R; ++r)
+                    if (r < nv) put_out(dst, (size_t)(rb + k2) * hs + (size_t)tp[r] * ts, acc[k2][r], tag);
+            }
+    });
+}
+
+// Out-of-line entry points of the row kernels (one per instantiation).
+template <int B, int R>
+__device__ __noinline__ void gu_k(const float4 *xs, const float *xsum, int H, const uint8_t *units, int cnt,
+                                  int rowb, uint32_t mask, int g0, uint64_t *dst, int ld, unsigned tag)
+{
+    gu_k_body<B, R>(xs, xsum, H, units, cnt, rowb, mask, g0, dst, ld, tag);
+}
+template <int B, int R>
+__device__ __noinline__ void one_k(const float4 *xs, const float *xsum, int H, const uint8_t *row, uint32_t mask,
+                                   int g0, void *dst, int ms, unsigned tag)
+{
+    one_k_body<B, R>(xs, xsum, H, row, mask, g0, dst, ms, tag);
+}
+template <int B, int R>
+__device__ __noinline__ void dn_k(const float4 *act, const float *asum, int K, const uint8_t *rows0, int cnt,
+                                  int rowb, uint32_t mask, int pair0, int g0, void *dst, int hs, int ts, unsigned tag)
+{
+    dn_k_body<B, R>(act, asum, K, rows0, cnt, rowb, mask, pair0, g0, dst, hs, ts, tag);
+}
+
+// ---------------------------------------------- one token vector in registers
+//
+// When a call has one token vector (one row of the mask) and a row has at
+// most 32 groups (K <= 2048), each lane of a row keeps its group's 64 inputs
+// in registers and the warp walks the rows: per row only the codes, scale and
+// bias are read from shared memory, and the loop body is small enough to run
+// from the innermost instruction cache after the first row.  The arithmetic
+// per row is that of grp_cls with NR = 1 (same sub-group visit order, same
+// class accumulators, same lane reduction), so a row's result is bit-for-bit
+// the one the general kernels give.
+
+// Sub-group of group g visited at position v (0 .. 3) by for_subgroups.
 template <int BITS>
 __device__ __forceinline__ int visit_sg(int g, int v)
 {
-    if constexpr (BITS == 0) return v;
-    else if constexpr (BITS == 6) return 2 * ((v >> 1) ^ ((g >> 3) & 1)) + (v & 1);
+    if constexpr (BITS == 6) return 2 * ((v >> 1) ^ ((g >> 3) & 1)) + (v & 1);
     else if constexpr (BITS == 8) return (v + chunk_rot<8>(g)) & 3;
     else return 2 * (((v >> 1) + chunk_rot<4>(g)) & 1) + (v & 1);
 }
@@ -600,277 +988,188 @@ __device__ __forceinline__ void load_x1(uint32_t xq, int g, int G, float4 (&x)[1
     }
 }
 
-// The codes, scale and bias of one lane's group of one row, loaded into
-// registers ahead of the arithmetic (the next row's while the current one is
-// computed): w[v] holds the code words of the sub-group visited v-th.
-template <int BITS> struct GroupCodes {
-    uint32_t w[4][BITS == 0 ? 1 : BITS / 2];
-    uint32_t sb;   // scale (low half, bf16) | bias (high half, bf16)
-};
-
+// The lane's part of row . x (group g), before the reduction over the lanes
+// of the row: exactly grp_cls<BITS, 1, 1> on a zero accumulator.
 template <int BITS>
-__device__ __forceinline__ void load_codes(uint32_t row, int g, int K, GroupCodes<BITS> &c)
-{
-    if constexpr (BITS != 0) {
-#pragma unroll
-        for (int v = 0; v < 4; ++v) {
-            const int sg = visit_sg<BITS>(g, v);
-            if constexpr (BITS == 6) {
-                // 12 bytes at row + 48 g + 12 sg: 8-byte aligned for even sg
-                const uint32_t a = row + g * 48 + 12 * sg;
-                if (v & 1) {
-                    c.w[v][0] = lds1(a);
-                    const uint2 p = lds2(a + 4);
-                    c.w[v][1] = p.x; c.w[v][2] = p.y;
-                } else {
-                    const uint2 p = lds2(a);
-                    c.w[v][0] = p.x; c.w[v][1] = p.y;
-                    c.w[v][2] = lds1(a + 8);
-                }
-            } else if constexpr (BITS == 8) {
-                const uint4 p = lds4(row + g * 64 + 16 * sg);
-                c.w[v][0] = p.x; c.w[v][1] = p.y; c.w[v][2] = p.z; c.w[v][3] = p.w;
-            } else {
-                const uint2 p = lds2(row + g * 32 + 8 * sg);
-                c.w[v][0] = p.x; c.w[v][1] = p.y;
-            }
-        }
-        c.sb = lds1(row + K * BITS / 8 + g * 4);
-    }
-}
-
-// The lane's part of row . x for group g, before the reduction over the lanes
-// of the row: s * sum_j q_j x_j + b * sum_j x_j, with the code products
-// accumulated per bit position (class) and each class scaled back once (the
-// classes summed in two interleaved chains).
-template <int BITS>
-__device__ __forceinline__ float dot_codes(const GroupCodes<BITS> &c, const float4 (&x)[16], float xsum)
+__device__ __forceinline__ float dot1(uint32_t row, int g, int K, const float4 (&x)[16], float xsum)
 {
     using PT = Pairs<BITS>;
     constexpr int NC = PT::NC, NA = BITS == 6 ? NC : 2 * NC;
+    float s, b;
+    scale_bias(row, K, BITS, g, s, b);
     float2 A[NA];
 #pragma unroll
-    for (int k = 0; k < NA; ++k) A[k] = make_float2(0.f, 0.f);
+    for (int c = 0; c < NA; ++c) A[c] = make_float2(0.f, 0.f);
 #pragma unroll
     for (int v = 0; v < 4; ++v) {
+        const int sg = visit_sg<BITS>(g, v);
+        uint32_t w[BITS / 2];
+        if constexpr (BITS == 6) {
+            // 12 bytes at row + 48 g + 12 sg: 8-byte aligned for even sg
+            const uint32_t a = row + g * 48 + 12 * sg;
+            if (sg & 1) {
+                w[0] = lds1(a);
+                const uint2 p = lds2(a + 4);
+                w[1] = p.x; w[2] = p.y;
+            } else {
+                const uint2 p = lds2(a);
+                w[0] = p.x; w[1] = p.y;
+                w[2] = lds1(a + 8);
+            }
+        } else if constexpr (BITS == 8) {
+            const uint4 p = lds4(row + g * 64 + 16 * sg);
+            w[0] = p.x; w[1] = p.y; w[2] = p.z; w[3] = p.w;
+        } else {
+            const uint2 p = lds2(row + g * 32 + 8 * sg);
+            w[0] = p.x; w[1] = p.y;
+        }
         const int half = NA > NC ? (v & 1) * NC : 0;
-        PT::each(c.w[v], [&](int i, float a, float bb) {
+        PT::each(w, [&](int i, float a, float bb) {
             A[PT::cls(i) + half] = __ffma2_rn(make_float2(a, bb), xpair(x[4 * v + (i >> 1)], i & 1), A[PT::cls(i) + half]);
         });
     }
-    float t0 = 0.f, t1 = 0.f;
+    float t = 0.f;
 #pragma unroll
-    for (int k = 0; k < NA; ++k) {
-        const int i0 = first_of_class<PT>(k % NC);
-        t0 = fmaf(A[k].x, __uint_as_float(cls_bits(PT::pa(i0))), t0);
-        t1 = fmaf(A[k].y, __uint_as_float(cls_bits(PT::pb(i0))), t1);
+    for (int c = 0; c < NA; ++c) {
+        const int i0 = first_of_class<PT>(c % NC);
+        t = fmaf(A[c].x, __uint_as_float(cls_bits(PT::pa(i0))), t);
+        t = fmaf(A[c].y, __uint_as_float(cls_bits(PT::pb(i0))), t);
     }
-    const float s = __uint_as_float(c.sb << 16), b = __uint_as_float(c.sb & 0xFFFF0000u);
-    return fmaf(s, t0 + t1, b * xsum);
+    return fmaf(s, t, fmaf(b, xsum, 0.f));
 }
 
-// fp32 row (a router given in fp32): K floats; x holds the inputs times 2^100.
-__device__ __forceinline__ float dot_f32(uint32_t row, int g, const float4 (&x)[16])
-{
-    float S = 0.f;
-#pragma unroll
-    for (int q = 0; q < 16; ++q) {
-        const float4 w = ldsf4(row + (uint32_t)(g * 16 + q) * 16);
-        S = fmaf(w.x, x[q].x, fmaf(w.y, x[q].y, fmaf(w.z, x[q].z, fmaf(w.w, x[q].w, S))));
-    }
-    return S * 0x1p-100f;
-}
-
-// Stores v at element i of dst: a plain fp32 array, or (tag != 0) tagged words.
-__device__ __forceinline__ void put_out(void *dst, size_t i, float v, unsigned tag)
-{
-    if (tag) st_tag(static_cast<uint64_t *>(dst) + i, __float_as_uint(v), tag);
-    else static_cast<float *>(dst)[i] = v;
-}
-
-// ------------------------------------------------------------ row kernels
-//
-// Every dot product of the layer (router rows, gate/up rows, down rows) is a
-// packed row in shared memory against ONE arranged token vector (hn, or an
-// expert's activations, times 2^100, in shared memory).  A call with several
-// token rows runs the same kernel once per token row, so a row's result is
-// bitwise the same whatever the other rows of the call are (PureDrive model
-// card, "How it works": every row of the verify pass equals a one-row
-// decode).
-//
-// Lanes take whole 64-groups of a row: LPR = min(32, G) lanes per row, GPL =
-// G / LPR groups per lane, RPP = 32 / LPR rows side by side.  A lane keeps
-// the 64 inputs of its group in registers while the warp walks the rows, 8
-// row slots per lane at a time (a batch of 8 RPP rows, or units of a gate row
-// and an up row).  A batch is reduced over the LPR lanes of each row by a
-// transposing butterfly: at each exchange a lane keeps half of the values it
-// holds, adds its partner's copy of that half and sends the other half, so 8
-// slots cost 7 exchanges where one row at a time would cost 8 log2(LPR)
-// dependent ones.  Every row's lane partials are added in the same tree
-// (lanes l and l ^ LPR/2, then l ^ LPR/4, ...; a + b = b + a exactly) in
-// whichever slot of whichever batch it sits.
-
-template <int NA, int N>
-__device__ __forceinline__ void halve_slots(float (&v)[NA][8], int o, bool up)
-{
-#pragma unroll
-    for (int a = 0; a < NA; ++a)
-#pragma unroll
-        for (int i = 0; i < N / 2; ++i) {
-            const float keep = up ? v[a][i + N / 2] : v[a][i];
-            const float send = up ? v[a][i] : v[a][i + N / 2];
-            v[a][i] = keep + __shfl_xor_sync(FULLMASK, send, o);
-        }
-}
-
-// Reduces 8 slots per lane over the LPR lanes of each row.  Returns how many
-// slots this lane emits (0 on lanes whose copy is not the one kept); they are
-// v[a][0 ..) for slots slot0, slot0 + 1, ...
-template <int NA>
-__device__ __forceinline__ int reduce_slots(float (&v)[NA][8], int LPR, int lane, int &slot0)
-{
-    int o = LPR >> 1, held = 8;
-    slot0 = 0;
-    if (o) { const bool up = (lane & o) != 0; halve_slots<NA, 8>(v, o, up); slot0 += up ? 4 : 0; o >>= 1; held = 4; }
-    if (o) { const bool up = (lane & o) != 0; halve_slots<NA, 4>(v, o, up); slot0 += up ? 2 : 0; o >>= 1; held = 2; }
-    if (o) { const bool up = (lane & o) != 0; halve_slots<NA, 2>(v, o, up); slot0 += up ? 1 : 0; o >>= 1; held = 1; }
-    const int rest = o ? 2 * o - 1 : 0;
-#pragma unroll 1
-    for (; o; o >>= 1)
-#pragma unroll
-        for (int a = 0; a < NA; ++a) v[a][0] += __shfl_xor_sync(FULLMASK, v[a][0], o);
-    return (lane & rest) == 0 ? held : 0;
-}
-
-// Units [0, nunits) against one arranged vector (xq, group sums at xsq): unit
-// u is the row at rows + u * ustride (NA = 1), or the rows at rows + u *
-// ustride and rows + u * ustride + rstride (NA = 2: a gate row and its up
-// row).  emit(u, val) runs on one lane per unit with the complete products.
-template <int BITS, int NA, typename F>
-__device__ __forceinline__ void rows_dot(uint32_t rows, int ustride, int rstride, int nunits, int K, uint32_t xq,
-                                         uint32_t xsq, F &&emit)
+// Rows against one token vector: the warp takes rows r0 + RPP i (lanes
+// lg of a row group, RPP = 32 / LPR row groups) of nrows at rows + r * rstride
+// (shared memory), each of K inputs.  emit(r, value) runs on the first lane
+// of the row group with the complete dot product of row r.
+template <int BITS, typename F>
+__device__ __forceinline__ void rows1(uint32_t rows, int rstride, int nrows, int K, uint32_t xq, uint32_t xsq, F &&emit)
 {
     const int lane = threadIdx.x & 31;
-    const int G = K >> 6, lgG = ilog2(G), lgL = lgG < 5 ? lgG : 5;
-    const int LPR = 1 << lgL, RPP = 32 >> lgL, GPL = G >> lgL;
-    const int gl = lane & (LPR - 1), rg = lane >> lgL;
+    const int G = K >> 6, lgL = ilog2(G), LPR = 1 << lgL, RPP = 32 >> lgL;
+    const int g = lane & (LPR - 1), lr = lane >> lgL;
+    float4 x[16];
+    load_x1<BITS>(xq, g, G, x);
+    const float xsum = ldsf1(xsq + 4 * g);
 #pragma unroll 1
-    for (int u0 = 0; u0 < nunits; u0 += 8 * RPP) {
-        float v[NA][8];
-#pragma unroll
-        for (int a = 0; a < NA; ++a)
-#pragma unroll
-            for (int j = 0; j < 8; ++j) v[a][j] = 0.f;
-        const int nslots = min(8, (nunits - u0 + RPP - 1) / RPP);
+    for (int r0 = 0; r0 < nrows; r0 += RPP) {
+        const int r = r0 + lr;
+        float acc = dot1<BITS>(rows + (uint32_t)(min(r, nrows - 1) * rstride), g, K, x, xsum);
 #pragma unroll 1
-        for (int gp = 0; gp < GPL; ++gp) {
-            const int g = gl + LPR * gp;
-            float4 x[16];
-            load_x1<BITS>(xq, g, G, x);
-            const float xs = BITS == 0 ? 0.f : ldsf1(xsq + 4 * g);
+        for (int o = LPR >> 1; o >= 1; o >>= 1) acc += __shfl_xor_sync(FULLMASK, acc, o);
+        if (g == 0 && r < nrows) emit(r, acc);
+    }
+}
+
+// Gate/up units [0, cnt) (unit u: gate row 2u, up row 2u + 1) against one
+// token vector: dst[u] = silu(gate) * up, tagged.  A row group takes a whole
+// unit.
+template <int BITS>
+__device__ __noinline__ void gu1(uint32_t units, int cnt, int rowb, int H, uint32_t xq, uint32_t xsq, uint64_t *dst,
+                                 unsigned tag)
+{
+    const int lane = threadIdx.x & 31;
+    const int G = H >> 6, lgL = ilog2(G), LPR = 1 << lgL, RPP = 32 >> lgL;
+    const int g = lane & (LPR - 1), lr = lane >> lgL;
+    float4 x[16];
+    load_x1<BITS>(xq, g, G, x);
+    const float xsum = ldsf1(xsq + 4 * g);
 #pragma unroll 1
-            for (int j = 0; j < nslots; ++j) {
-                const uint32_t r = rows + (uint32_t)(min(u0 + j * RPP + rg, nunits - 1) * ustride);
-                float d[NA];
-#pragma unroll
-                for (int a = 0; a < NA; ++a) {
-                    if constexpr (BITS == 0) {
-                        d[a] = dot_f32(r + (uint32_t)(a * rstride), g, x);
-                    } else {
-                        GroupCodes<BITS> c;
-                        load_codes<BITS>(r + (uint32_t)(a * rstride), g, K, c);
-                        d[a] = dot_codes<BITS>(c, x, xs);
-                    }
-                }
-                // into slot j without indexing the register array by a variable
-#pragma unroll
-                for (int a = 0; a < NA; ++a)
-#pragma unroll
-                    for (int jj = 0; jj < 8; ++jj) v[a][jj] = jj == j ? v[a][jj] + d[a] : v[a][jj];
-            }
+    for (int u0 = 0; u0 < cnt; u0 += RPP) {
+        const uint32_t ru = units + (uint32_t)(2 * min(u0 + lr, cnt - 1) * rowb);
+        float gt = 0.f, up = 0.f;
+#pragma unroll 1
+        for (int k = 0; k < 2; ++k) {
+            const float v = dot1<BITS>(ru + k * rowb, g, H, x, xsum);
+            if (k) up = v;
+            else gt = v;
         }
-        int slot0;
-        const int held = reduce_slots<NA>(v, LPR, lane, slot0);
-#pragma unroll
-        for (int i = 0; i < 8; ++i)
-            if (i < held) {
-                const int u = u0 + (slot0 + i) * RPP + rg;
-                float val[NA];
-#pragma unroll
-                for (int a = 0; a < NA; ++a) val[a] = v[a][i];
-                if (u < nunits) emit(u, val);
-            }
+#pragma unroll 1
+        for (int o = LPR >> 1; o >= 1; o >>= 1) {
+            gt += __shfl_xor_sync(FULLMASK, gt, o);
+            up += __shfl_xor_sync(FULLMASK, up, o);
+        }
+        if (g == 0 && u0 + lr < cnt) st_tag(dst + u0 + lr, __float_as_uint(gt / (1.0f + expf(-gt)) * up), tag);
     }
 }
 
-// Gate/up units [0, cnt) (unit u: gate row at units + 2 u rowb, up row next)
-// against hn of every token row m of `mask`: dst[m * ld + u] = silu(gate) *
-// up, as tagged words.
+// Rows [0, cnt) against one vector: dst[r * ds] = row r . x (see put_out).
 template <int BITS>
-__device__ __noinline__ void gu_rows(uint32_t units, int cnt, int rowb, int H, uint32_t xs, uint32_t xsum,
-                                     uint32_t mask, uint64_t *dst, int ld, unsigned tag)
+__device__ __noinline__ void plain1(uint32_t rows, int cnt, int rowb, int K, uint32_t xq, uint32_t xsq, void *dst, int ds,
+                                    unsigned tag)
 {
-    const int G = H / kGroup;
-#pragma unroll 1
-    for (; mask; mask &= mask - 1u) {
-        const int m = __ffs(mask) - 1;
-        uint64_t *d = dst + (size_t)m * ld;
-        rows_dot<BITS, 2>(units, 2 * rowb, rowb, cnt, H, xs + (uint32_t)(m * H * 4), xsum + (uint32_t)(m * G * 4),
-                          [&](int u, const float (&v)[2]) {
-                              st_tag(d + u, __float_as_uint(v[0] / (1.0f + expf(-v[0])) * v[1]), tag);
-                          });
-    }
+    rows1<BITS>(rows, rowb, cnt, K, xq, xsq, [&](int r, float v) { put_out(dst, (size_t)r * ds, v, tag); });
 }
 
-// Rows [0, cnt) (row bytes rowb, K inputs) against the vectors of the token
-// rows of `mask`: vector m (by_rank = 0: the vector of token row m) or
-// vector t (by_rank = 1: t = the rank of m in the mask) of vecs (stride K
-// floats, group sums at sums, stride K / 64):
-// dst[r * hs + (by_rank ? t : m) * ts] = row r . vector (see put_out).
-template <int BITS>
-__device__ __noinline__ void plain_rows(uint32_t rows, int cnt, int rowb, int K, uint32_t vecs, uint32_t sums,
-                                        uint32_t mask, int by_rank, void *dst, int hs, int ts, unsigned tag)
-{
-    const int G = K / kGroup;
-#pragma unroll 1
-    for (int t = 0; mask; mask &= mask - 1u, ++t) {
-        const int m = __ffs(mask) - 1, vi = by_rank ? t : m;
-        rows_dot<BITS, 1>(rows, rowb, 0, cnt, K, vecs + (uint32_t)(vi * K * 4), sums + (uint32_t)(vi * G * 4),
-                          [&](int r, const float (&v)[1]) { put_out(dst, (size_t)r * hs + (size_t)vi * ts, v[0], tag); });
-    }
-}
+// Dispatch on (bits, row-group size): code = bits * 8 + nr.
+#define MOE_RK_CASES(FN, ARGS)                                                                   \
+    case 4 * 8 + 1: FN<4, 1> ARGS; break;                                                        \
+    case 4 * 8 + 2: FN<4, 2> ARGS; break;                                                        \
+    case 6 * 8 + 1: FN<6, 1> ARGS; break;                                                        \
+    case 6 * 8 + 2: FN<6, 2> ARGS; break;                                                        \
+    case 8 * 8 + 1: FN<8, 1> ARGS; break;                                                        \
+    case 8 * 8 + 2: FN<8, 2> ARGS; break;
 
 __device__ __noinline__ void gu_units(const Sh &sh, int H, int bits, const uint8_t *units, int cnt, int rowb,
-                                      uint32_t mask, uint64_t *dst, int ld, unsigned tag)
+                                         uint32_t mask, uint64_t *dst, int ld, unsigned tag)
 {
-    const uint32_t u = smem_u32(units), xs = smem_u32(sh.xs), xsum = smem_u32(sh.xsum);
-    if (bits == 6) gu_rows<6>(u, cnt, rowb, H, xs, xsum, mask, dst, ld, tag);
-    else if (bits == 8) gu_rows<8>(u, cnt, rowb, H, xs, xsum, mask, dst, ld, tag);
-    else gu_rows<4>(u, cnt, rowb, H, xs, xsum, mask, dst, ld, tag);
+    if (__popc(mask) == 1 && H <= 32 * kGroup && bits != 0) {
+        const int m = __ffs(mask) - 1;
+        const uint32_t xq = smem_u32(sh.xs) + (uint32_t)(m * H * 4), xsq = smem_u32(sh.xsum) + (uint32_t)(m * (H / kGroup) * 4);
+        uint64_t *d = dst + (size_t)m * ld;
+        if (bits == 6) gu1<6>(smem_u32(units), cnt, rowb, H, xq, xsq, d, tag);
+        else if (bits == 8) gu1<8>(smem_u32(units), cnt, rowb, H, xq, xsq, d, tag);
+        else gu1<4>(smem_u32(units), cnt, rowb, H, xq, xsq, d, tag);
+        return;
+    }
+    for_row_groups(mask, [&](int g0, int nr) {
+        switch (bits * 8 + nr) {
+            MOE_RK_CASES(gu_k, (sh.xs, sh.xsum, H, units, cnt, rowb, mask, g0, dst, ld, tag))
+        default: break;
+        }
+    });
 }
 
-// One row of K = H inputs (a router row) against hn of the token rows of
-// `mask`: dst[m * ms] = row . hn_m.
 __device__ __noinline__ void one_row(const Sh &sh, int H, int bits, const uint8_t *row, uint32_t mask,
-                                     void *dst, int ms, unsigned tag)
+                                        void *dst, int ms, unsigned tag)
 {
-    const uint32_t r = smem_u32(row), xs = smem_u32(sh.xs), xsum = smem_u32(sh.xsum);
-    if (bits == 6) plain_rows<6>(r, 1, 0, H, xs, xsum, mask, 0, dst, 0, ms, tag);
-    else if (bits == 8) plain_rows<8>(r, 1, 0, H, xs, xsum, mask, 0, dst, 0, ms, tag);
-    else if (bits == 4) plain_rows<4>(r, 1, 0, H, xs, xsum, mask, 0, dst, 0, ms, tag);
-    else plain_rows<0>(r, 1, 0, H, xs, xsum, mask, 0, dst, 0, ms, tag);
+    if (__popc(mask) == 1 && H <= 32 * kGroup && bits != 0 && tag == 0u) {
+        const int m = __ffs(mask) - 1;
+        const uint32_t xq = smem_u32(sh.xs) + (uint32_t)(m * H * 4), xsq = smem_u32(sh.xsum) + (uint32_t)(m * (H / kGroup) * 4);
+        float *d = static_cast<float *>(dst) + (size_t)m * ms;
+        if (bits == 6) plain1<6>(smem_u32(row), 1, 0, H, xq, xsq, d, 0, 0u);
+        else if (bits == 8) plain1<8>(smem_u32(row), 1, 0, H, xq, xsq, d, 0, 0u);
+        else plain1<4>(smem_u32(row), 1, 0, H, xq, xsq, d, 0, 0u);
+        return;
+    }
+    for_row_groups(mask, [&](int g0, int nr) {
+        switch (bits * 8 + nr) {
+            MOE_RK_CASES(one_k, (sh.xs, sh.xsum, H, row, mask, g0, dst, ms, tag))
+        case 0 * 8 + 1: one_k<0, 1>(sh.xs, sh.xsum, H, row, mask, g0, dst, ms, tag); break;
+        case 0 * 8 + 2: one_k<0, 2>(sh.xs, sh.xsum, H, row, mask, g0, dst, ms, tag); break;
+        default: break;
+        }
+    });
 }
 
-// Down rows [0, cnt) (K inputs each) against the staged activation pairs
-// pair0 + t, t = the rank of a token row in `mask`: dst[h * hs + t * ts].
+// dst[h * hs + t * ts] for down row h and the staged pair pair0 + t (t the
+// rank of a row in `mask`): plain fp32, or tagged words when tag != 0.
 __device__ __noinline__ void dn_rows(const Sh &sh, int bits, const uint8_t *rows0, int cnt, int rowb, int K,
-                                     uint32_t mask, int pair0, void *dst, int hs, int ts, unsigned tag)
+                                        uint32_t mask, int pair0, void *dst, int hs, int ts, unsigned tag)
 {
-    const uint32_t r = smem_u32(rows0);
-    const uint32_t a = smem_u32(sh.act) + (uint32_t)(pair0 * K * 4), as = smem_u32(sh.asum) + (uint32_t)(pair0 * (K / kGroup) * 4);
-    if (bits == 6) plain_rows<6>(r, cnt, rowb, K, a, as, mask, 1, dst, hs, ts, tag);
-    else if (bits == 8) plain_rows<8>(r, cnt, rowb, K, a, as, mask, 1, dst, hs, ts, tag);
-    else plain_rows<4>(r, cnt, rowb, K, a, as, mask, 1, dst, hs, ts, tag);
+    if (__popc(mask) == 1 && K <= 32 * kGroup && bits != 0) {
+        const uint32_t xq = smem_u32(sh.act) + (uint32_t)(pair0 * K * 4), xsq = smem_u32(sh.asum) + (uint32_t)(pair0 * (K / kGroup) * 4);
+        if (bits == 6) plain1<6>(smem_u32(rows0), cnt, rowb, K, xq, xsq, dst, hs, tag);
+        else if (bits == 8) plain1<8>(smem_u32(rows0), cnt, rowb, K, xq, xsq, dst, hs, tag);
+        else plain1<4>(smem_u32(rows0), cnt, rowb, K, xq, xsq, dst, hs, tag);
+        return;
+    }
+    for_row_groups(mask, [&](int g0, int nr) {
+        switch (bits * 8 + nr) {
+            MOE_RK_CASES(dn_k, (sh.act, sh.asum, K, rows0, cnt, rowb, mask, pair0, g0, dst, hs, ts, tag))
+        default: break;
+        }
+    });
 }
 
 // ------------------------------------------------------------ P0: RMSNorm
@@ -879,12 +1178,15 @@ __device__ __noinline__ void dn_rows(const Sh &sh, int bits, const uint8_t *rows
 // sums; 1 / rms of row m -> red[m * (NCW + 1) + NCW].  A thread item is 8
 // consecutive inputs (one 16-byte load); H / 8 is a multiple of 32, so the
 // 32 items of a warp belong to one row.
-__device__ void build_hn(const KParams &kp, const Sh &sh, const void *x, unsigned xtag, const uint16_t *gamma)
+__device__ void build_hn(const KParams &kp, const Sh &sh, const void *x, unsigned xtag, const uint16_t *gamma,
+                         const uint8_t *rrows = nullptr, int nr = 0)
 {
     const int H = kp.g.H, M = kp.M, G = H / kGroup, tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
     const int per_row = H / 8, lpr = ilog2(per_row), total = M * per_row;
 #pragma unroll 1
     for (int m = lane; m < M; m += 32) sh.red[m * (NCW + 1) + warp] = 0.f;
+#pragma unroll 1
+    for (int i = lane; i < M * kFusedRouterRows; i += 32) sh.rred[i * NCW + warp] = 0.f;
     __syncwarp();
     // pass 1: sums of squares per (row, warp); raw values into xs.  Two
     // items per thread and round, both loads in flight before either is used.
@@ -910,23 +1212,33 @@ __device__ void build_hn(const KParams &kp, const Sh &sh, const void *x, unsigne
         const int wfirst = it - lane;
         if (lane == 0 && wfirst < total) sh.red[(wfirst >> lpr) * (NCW + 1) + warp] += ss;
     };
+    constexpr int NI = 4;   // items per thread and round, all loads in flight before any is used
 #pragma unroll 1
-    for (int base = 0; base < total; base += 2 * NCT) {
-        const int ia = base + tid, ib = ia + NCT;
-        uint32_t a[4] = {0u, 0u, 0u, 0u}, b[4] = {0u, 0u, 0u, 0u};
+    for (int base = 0; base < total; base += NI * NCT) {
+        uint32_t a[NI][4];
         if (xtag) {
             // the previous layer's output: tagged bf16 pairs
             const uint64_t *xt = static_cast<const uint64_t *>(x);
-            const uint64_t *pa = ia < total ? xt + (size_t)(ia >> lpr) * (H / 2) + 4 * (ia & (per_row - 1)) : nullptr;
-            const uint64_t *pb = ib < total ? xt + (size_t)(ib >> lpr) * (H / 2) + 4 * (ib & (per_row - 1)) : nullptr;
-            poll_tag8(sh, pa, pb, xtag, 40, a, b);
+            const uint64_t *p[NI];
+#pragma unroll
+            for (int n = 0; n < NI; ++n) {
+                const int it = base + tid + n * NCT;
+                p[n] = it < total ? xt + (size_t)(it >> lpr) * (H / 2) + 4 * (it & (per_row - 1)) : nullptr;
+            }
+            poll_items<NI>(sh, p, xtag, 40, a);
         } else {
             const uint4 *xp = reinterpret_cast<const uint4 *>(x);
-            if (ia < total) { const uint4 v = __ldcg(xp + ia); a[0] = v.x; a[1] = v.y; a[2] = v.z; a[3] = v.w; }
-            if (ib < total) { const uint4 v = __ldcg(xp + ib); b[0] = v.x; b[1] = v.y; b[2] = v.z; b[3] = v.w; }
+#pragma unroll
+            for (int n = 0; n < NI; ++n) {
+                const int it = base + tid + n * NCT;
+                uint4 v = make_uint4(0u, 0u, 0u, 0u);
+                if (it < total) v = __ldcg(xp + it);
+                a[n][0] = v.x; a[n][1] = v.y; a[n][2] = v.z; a[n][3] = v.w;
+            }
         }
-        item(ia, a);
-        if (base + NCT < total) item(ib, b);
+#pragma unroll
+        for (int n = 0; n < NI; ++n)
+            if (n == 0 || base + n * NCT < total) item(base + tid + n * NCT, a[n]);
     }
     cbar();
     if (tid < M) {
@@ -936,11 +1248,19 @@ __device__ void build_hn(const KParams &kp, const Sh &sh, const void *x, unsigne
         sh.red[tid * (NCW + 1) + NCW] = rsqrtf(t / (float)H + kp.g.eps);
     }
     cbar();
-    // pass 2: scale by rinv * gamma * 2^100; group sums of hn
+    // pass 2: scale by rinv * gamma * 2^100; group sums of hn; and (rrows
+    // given) the CTA's router rows dotted with hn: per item of 8 inputs
+    // s * sum q h + b * sum h (8-bit rows) or sum w h (fp32 rows), summed
+    // over the warp and then, in warp order, over the CTA (the same order for
+    // every token row, whatever M is)
+    const int qb = kp.g.qb, rrb = kp.g.rr_bytes;
 #pragma unroll 1
     for (int base = 0; base < total; base += NCT) {
         const int it = base + tid;
         float gs = 0.f;
+        float rp[kFusedRouterRows];
+#pragma unroll
+        for (int r = 0; r < kFusedRouterRows; ++r) rp[r] = 0.f;
         if (it < total) {
             const int m = it >> lpr, c = it & (per_row - 1);
             const float rinv = sh.red[m * (NCW + 1) + NCW];
@@ -959,7 +1279,36 @@ __device__ void build_hn(const KParams &kp, const Sh &sh, const void *x, unsigne
             for (int j = 0; j < 8; ++j) gs += h[j];
             row[t * G + g] = make_float4(h[0] * kXScale, h[1] * kXScale, h[2] * kXScale, h[3] * kXScale);
             row[(t + 1) * G + g] = make_float4(h[4] * kXScale, h[5] * kXScale, h[6] * kXScale, h[7] * kXScale);
+#pragma unroll
+            for (int r = 0; r < kFusedRouterRows; ++r)
+                if (r < nr) {
+                    const uint8_t *rw = rrows + (size_t)r * rrb;
+                    if (qb == 8) {
+                        const uint2 cw = *reinterpret_cast<const uint2 *>(rw + 8 * c);
+                        const uint32_t sbw = *reinterpret_cast<const uint32_t *>(rw + H + g * 4);
+                        float qh = 0.f, hs = 0.f;
+#pragma unroll
+                        for (int j = 0; j < 8; ++j) {
+                            const uint32_t q = ((j < 4 ? cw.x : cw.y) >> (8 * (j & 3))) & 0xFFu;
+                            qh = fmaf((float)q, h[j], qh);
+                            hs += h[j];
+                        }
+                        rp[r] = fmaf(__uint_as_float(sbw << 16), qh, __uint_as_float(sbw & 0xFFFF0000u) * hs);
+                    } else {
+                        const float4 w0 = *reinterpret_cast<const float4 *>(rw + 32 * c);
+                        const float4 w1 = *reinterpret_cast<const float4 *>(rw + 32 * c + 16);
+                        rp[r] = fmaf(w0.x, h[0], fmaf(w0.y, h[1], fmaf(w0.z, h[2], fmaf(w0.w, h[3],
+                                fmaf(w1.x, h[4], fmaf(w1.y, h[5], fmaf(w1.z, h[6], w1.w * h[7])))))));
+                    }
+                }
         }
+#pragma unroll
+        for (int r = 0; r < kFusedRouterRows; ++r)
+            if (r < nr) {
+                const float v = warp_sum(rp[r]);
+                const int wfirst = it - lane;
+                if (lane == 0 && wfirst < total) sh.rred[((wfirst >> lpr) * kFusedRouterRows + r) * NCW + warp] += v;
+            }
         // 8 consecutive items make a group
         gs += __shfl_xor_sync(FULLMASK, gs, 4);
         gs += __shfl_xor_sync(FULLMASK, gs, 2);
@@ -1000,16 +1349,21 @@ __device__ __forceinline__ void stage_acts(const Sh &sh, int n, int K, int tid, 
             sh.asum[p * G + (c >> 4)] = gs;
         }
     };
-    // two items per thread and round, both loads in flight before either is used
+    // four items per thread and round, all loads in flight before any is used
+    constexpr int NI = 4;
 #pragma unroll 1
-    for (int base = 0; base < total; base += 2 * nt) {
-        const int ia = base + tid, ib = ia + nt;
-        const uint64_t *pa = ia < total ? src(ia >> lgp) + 4 * (ia & (per - 1)) : nullptr;
-        const uint64_t *pb = ib < total ? src(ib >> lgp) + 4 * (ib & (per - 1)) : nullptr;
-        uint32_t a[4], b[4];
-        poll_tag8(sh, pa, pb, tag, 41, a, b);
-        item(ia, a);
-        if (base + nt < total) item(ib, b);
+    for (int base = 0; base < total; base += NI * nt) {
+        const uint64_t *p[NI];
+#pragma unroll
+        for (int n = 0; n < NI; ++n) {
+            const int it = base + tid + n * nt;
+            p[n] = it < total ? src(it >> lgp) + 4 * (it & (per - 1)) : nullptr;
+        }
+        uint32_t a[NI][4];
+        poll_items<NI>(sh, p, tag, 41, a);
+#pragma unroll
+        for (int n = 0; n < NI; ++n)
+            if (n == 0 || base + n * nt < total) item(base + tid + n * nt, a[n]);
     }
 }
 
@@ -1521,6 +1875,34 @@ __device__ __forceinline__ void consume(const Sh &sh, Cursor &c, int where, F &&
     if ((threadIdx.x & 31) == 0) mbar_arrive(&sh.empty[slot], 1);
 }
 
+// True when this CTA's router rows are computed inside the RMSNorm pass
+// (fp32 or 8-bit router, few enough rows per CTA).
+__device__ __forceinline__ bool router_fused(const KParams &kp, const Sh &sh)
+{
+    return (kp.g.qb == 0 || kp.g.qb == 8) && sh.cp->rb - sh.cp->ra <= kFusedRouterRows;
+}
+
+// Logits of the router rows computed in the RMSNorm pass: the warps' partial
+// sums added in warp order, then the 8 copies of each out as tagged words.
+__device__ void publish_fused_logits(const KParams &kp, const Sh &sh, const Ws &w, int l)
+{
+    const CtaPlan &b = *sh.cp;
+    const int nr = b.rb - b.ra, M = kp.M, Er = kp.g.Er;
+    const unsigned tag = layer_tag(sh, l);
+#pragma unroll 1
+    for (int t = threadIdx.x; t < M * nr; t += NCT) {
+        const int m = t / nr, r = t - m * nr, e = b.ra + r;
+        float v = 0.f;
+#pragma unroll 1
+        for (int wp = 0; wp < NCW; ++wp) v += sh.rred[(m * kFusedRouterRows + r) * NCW + wp];
+        // (debug switch: one logit of layer 0 stays unpublished)
+        if (l == 0 && kp.skip_row == e) continue;
+#pragma unroll 1
+        for (int c = 0; c < kLogitCopies; ++c)
+            st_tag(w.logits + ((size_t)c * kp.ws_l.maxr + m) * Er + e, __float_as_uint(v), tag);
+    }
+}
+
 // P1 and routing.  With M at most half the compute warps, the first M warps
 // route (one token row each), waiting on every CTA's router logits, while
 // the other warps compute this CTA's router rows first (the logits every CTA
@@ -1535,7 +1917,7 @@ __device__ void phase1(const KParams &kp, const Sh &sh, const LayerPtrs &Lp, Cur
     const uint32_t all = (1u << kp.M) - 1u;
     const int warp = threadIdx.x >> 5, M = kp.M;
     const CtaPlan &b = *sh.cp;
-    const int nr = b.rb - b.ra;
+    const int nr = router_fused(kp, sh) ? 0 : b.rb - b.ra;   // router rows not done in the RMSNorm pass
     const bool early = 2 * M <= NCW;
     const int w0 = early ? M : 0;   // first warp computing rows
     const unsigned tag = layer_tag(sh, l);
@@ -1775,8 +2157,11 @@ __device__ __forceinline__ void compute(const KParams &kp, const Sh &sh)
         // layer l's gamma, router rows and shared units
         const bool pb_ok = wait_bar(sh, sh.pb_full, (unsigned)l & 1u, 5);
         if (cbar_or(!pb_ok)) return;
-        build_hn(kp, sh, xin, xtag, reinterpret_cast<const uint16_t *>(sh.pb));
+        const bool fused = router_fused(kp, sh);
+        build_hn(kp, sh, xin, xtag, reinterpret_cast<const uint16_t *>(sh.pb), fused ? sh.pb + sh.cp->off_router : nullptr,
+                 fused ? sh.cp->rb - sh.cp->ra : 0);
         if (cbar_or(aborted(sh))) return;
+        if (fused) publish_fused_logits(kp, sh, w, l);
         if (t0) stamp(kp, l, 1);
         phase1(kp, sh, Lp, q, w, l);
         if (t0) stamp(kp, l, 2);
@@ -1865,6 +2250,7 @@ __global__ void __launch_bounds__(kThreads, 1) moe_decode_kernel(const __grid_co
         sh.row_w = reinterpret_cast<float *>(smem + L.row_w);
         sh.row_pair = reinterpret_cast<int *>(smem + L.row_pair);
         sh.red = reinterpret_cast<float *>(smem + L.red);
+        sh.rred = reinterpret_cast<float *>(smem + L.rred);
         sh.lscr = reinterpret_cast<float *>(smem + L.lscr);
         sh.pair_src = reinterpret_cast<int *>(smem + L.pair_src);
         sh.xs = reinterpret_cast<float4 *>(smem + L.xs);
@@ -1948,6 +2334,19 @@ bool make_plan(const Geo &g, int maxr, int num_sms, Plan &p)
     const int fixed = carve(g, p).total;
     int room = kSmemMax - 2048 - fixed - pb_min - maxr * pair_bytes;
     if (room < NCW * maxi) return false;
+    // The staging buffer first: every activation pair of a launch, up to
+    // kActCap bytes (each CTA's down rows need the activations of every
+    // selected expert, and each batch of pairs costs a gather), keeping the
+    // smallest ring; then the ring up to ring_target, then the prefetch
+    // buffer, then the ring takes whatever is left.
+    constexpr int kActCap = 80 * 1024;
+    int more_pairs = pairs_all - maxr;
+    const int cap_pairs = (kActCap - maxr * pair_bytes) / pair_bytes;
+    if (more_pairs > cap_pairs) more_pairs = cap_pairs;
+    if (more_pairs > (room - NCW * maxi) / pair_bytes) more_pairs = (room - NCW * maxi) / pair_bytes;
+    if (more_pairs < 0) more_pairs = 0;
+    p.act_pairs = maxr + more_pairs;
+    room -= more_pairs * pair_bytes;
     const int ring_want = ring_target > NCW * maxi ? ring_target : NCW * maxi;
     int ring = room < ring_want ? room : ring_want;
     room -= ring;
@@ -1955,10 +2354,6 @@ bool make_plan(const Geo &g, int maxr, int num_sms, Plan &p)
     if (pb_extra > room) pb_extra = room;
     p.pb_bytes = pb_min + pb_extra;
     room -= pb_extra;
-    int more_pairs = room / pair_bytes;
-    if (more_pairs > pairs_all - maxr) more_pairs = pairs_all - maxr;
-    p.act_pairs = maxr + more_pairs;
-    room -= more_pairs * pair_bytes;
     ring += room;
     // Stages large enough that a CTA's gate/up units at the most slots fit
     // one stage per compute warp (a warp with two stages would hold up the

@@ -1648,11 +1648,12 @@ __device__ __forceinline__ void sched_p1b(const KParams &kp, const Sh &sh, const
     }
 }
 
+// The P2 stages of this CTA for U distinct experts: f(slot, first unit,
+// units), in ring order.
 template <typename F>
-__device__ __forceinline__ void sched_p2(const KParams &kp, const Sh &sh, const LayerPtrs &Lp, F &&f)
+__device__ __forceinline__ void p2_units(const KParams &kp, const Sh &sh, int U, F &&f)
 {
     const Geo &g = kp.g;
-    const int U = sh.flags[1];
     const int ub = 2 * g.g_bytes;
     int a, b;
     split(U * g.I, gridDim.x, blockIdx.x, a, b);
@@ -1663,11 +1664,20 @@ __device__ __forceinline__ void sched_p2(const KParams &kp, const Sh &sh, const 
 #pragma unroll 1
     for (int n = a; n < b;) {
         const int cnt = min(cu, min(b - n, g.I - j));
-        f(Lp.gu + ((size_t)sh.slot_e[s] * g.I + j) * ub, cnt * ub, s, j, cnt);
+        f(s, j, cnt);
         n += cnt;
         j += cnt;
         if (j == g.I) { j = 0; ++s; }
     }
+}
+
+template <typename F>
+__device__ __forceinline__ void sched_p2(const KParams &kp, const Sh &sh, const LayerPtrs &Lp, F &&f)
+{
+    const int ub = 2 * kp.g.g_bytes;
+    p2_units(kp, sh, sh.flags[1], [&](int s, int j, int cnt) {
+        f(Lp.gu + ((size_t)sh.slot_e[s] * kp.g.I + j) * ub, cnt * ub, s, j, cnt);
+    });
 }
 
 // P3 of this CTA: the down rows of its own output slice [h0, h0 + nh) of
@@ -1804,9 +1814,30 @@ __device__ __forceinline__ void producer(const KParams &kp, const Sh &sh, int la
             const LayerPtrs &Lp = kp.layer[l];
             if (!issue_pass(sh, c, lane, [&](auto &&f) { sched_p1x(kp, sh, Lp, f); })) break;
             if (lane == 0) stamp(kp, l, 9);
+            // With one token row the routing always yields k distinct experts,
+            // so each lane's gate/up stage (slot, units, ring position) is
+            // known before the routing ends; after it only the expert id is
+            // read and the copy goes out.
+            int my_s = 0, my_j = 0, my_n = 0, nst = 0;
+            if (kp.M == 1) p2_units(kp, sh, kp.g.k, [&](int s, int j, int n) {
+                if (nst == lane) { my_s = s; my_j = j; my_n = n; }
+                ++nst;
+            });
+            const bool fast = kp.M == 1 && nst <= sh.NS;
+            Cursor mine = c;
+#pragma unroll 1
+            for (int i = 0; fast && i < lane; ++i) cursor_next(mine, sh.NS);
             if (!wait_bar(sh, sh.route, (unsigned)l & 1u, 2)) break;
             if (lane == 0) stamp(kp, l, 10);
-            if (!issue_pass(sh, c, lane, [&](auto &&f) { sched_p2(kp, sh, Lp, f); })) break;
+            if (fast) {
+                const int ub = 2 * kp.g.g_bytes;
+                const uint8_t *src = lane < nst ? Lp.gu + ((size_t)sh.slot_e[my_s] * kp.g.I + my_j) * ub : nullptr;
+                if (!issue_batch(sh, lane < nst, mine.slot, mine.par, mine.reuse, src, my_n * ub)) break;
+#pragma unroll 1
+                for (int i = 0; i < nst; ++i) cursor_next(c, sh.NS);
+            } else if (!issue_pass(sh, c, lane, [&](auto &&f) { sched_p2(kp, sh, Lp, f); })) {
+                break;
+            }
             if (lane == 0) stamp(kp, l, 14);
             int turn = 0;
             sched_p3(kp, sh, Lp, [&](const uint8_t *src, int bytes, int, int, int) {

@@ -69,7 +69,7 @@ def lib():
         _lib.oracle_max_threads.restype = C.c_int
         for name in ("oracle_pack_bits", "oracle_unpack_bits", "oracle_quantize_group",
                      "oracle_quantize_matrix", "oracle_rmsnorm", "oracle_topk",
-                     "oracle_expert_ffn", "oracle_route"):
+                     "oracle_expert_ffn", "oracle_route", "oracle_qkv"):
             getattr(_lib, name).restype = None
     return _lib
 
@@ -319,6 +319,26 @@ class Layer:
             raise RuntimeError(f"oracle_layer: expert {-rc - 1} missing")
         return {"o": o, "out": out, "on": on, "out_n": out_n, "logits": logits, "idx": idx,
                 "w": w, "sigma": sigma, "margin": margin}
+
+
+def qkv(mats, x_bits: np.ndarray) -> np.ndarray:
+    """Fused projection of x bf16 patterns [M, H] by the matrices in `mats`
+    (Matrix objects of the same width, e.g. Q, K, V) stacked row-wise:
+    returns fp64 [M, sum of their rows]."""
+    x_bits = np.ascontiguousarray(x_bits, dtype=np.uint16)
+    M, H = x_bits.shape
+    parts = []
+    for m_ in mats:
+        assert m_.cols == H
+    if all(m_.bits == mats[0].bits for m_ in mats) and mats[0].bits != 0:
+        st = Matrix(mats[0].bits, np.concatenate([m_.codes for m_ in mats]),
+                    np.concatenate([m_.scales for m_ in mats]), np.concatenate([m_.biases for m_ in mats]))
+    else:
+        raise ValueError("qkv: the matrices must share one code width")
+    y = np.zeros((M, st.rows), np.float64)
+    s = st.struct()
+    lib().oracle_qkv(C.byref(s), _p(x_bits), C.c_int(M), _p(y))
+    return y
 
 
 def stack(layers, x_bits: np.ndarray, normed_last: bool = True):

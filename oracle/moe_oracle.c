@@ -205,6 +205,22 @@ static void matvec(const oq_matrix *m, const double *x, double *y)
     }
 }
 
+/* Fused Q/K/V (or Gated-DeltaNet input) projection of M token rows: the
+ * rows of Q, K and V stacked into one [rows, H] matrix, read once for the
+ * input row ("Qwen3.5-397B on M5 Max" (openclawradar), "効果的な最適化":
+ * fused QKV projection, the input read once).  x bf16 [M, H] is the layer's
+ * normalised input (the MoE layer's fused out_n); y[m, r] = sum_c W[r, c]
+ * x[m, c] in fp64. */
+void oracle_qkv(const oq_matrix *w, const uint16_t *x, int M, double *y)
+{
+    double *xd = (double *)malloc(sizeof(double) * (size_t)w->cols);
+    for (int m = 0; m < M; ++m) {
+        for (int c = 0; c < w->cols; ++c) xd[c] = oracle_bf16_to_double(x[(size_t)m * w->cols + c]);
+        matvec(w, xd, y + (size_t)m * w->rows);
+    }
+    free(xd);
+}
+
 /* --------------------------------------------------------------- layer */
 
 typedef struct {

@@ -339,3 +339,26 @@ def test_threads_give_the_same_bits():
         assert np.array_equal(one[key], many[key]), key
     for key in ("out", "out_n", "idx"):
         assert np.array_equal(one[key], many[key]), key
+
+
+@pytest.mark.parametrize("bits", [8, 4])
+def test_qkv_matches_dense_product(bits):
+    """The fused Q/K/V projection equals a dense fp64 product of the fully
+    dequantised stacked matrix (numpy, independent of the C code), and its
+    row blocks equal the three separate projections."""
+    g = torch.Generator().manual_seed(77 + bits)
+    H = 256
+    mats = [oracle.Matrix.from_canonical(synth.quant_matrix(g, (n,), H, bits, "cpu")) for n in (64, 32, 32)]
+    xb = synth.bf16_bits(synth.make_rows(synth.TINY, 5, 3)).numpy().view(np.uint16)
+    y = oracle.qkv(mats, xb)
+    x = oracle.bf16_patterns_to_double(xb)
+    dense = np.concatenate([m.dense() for m in mats])
+    assert y.shape == (3, 128)
+    assert np.allclose(y, x @ dense.T, rtol=1e-12, atol=1e-12)
+    off = 0
+    for m in mats:
+        alone = oracle.qkv([m], xb)
+        assert np.array_equal(alone, y[:, off:off + m.rows])
+        off += m.rows
+    # a transposed operand or a dropped bias would not match
+    assert not np.allclose(y, x @ (dense - dense.mean()).T, rtol=1e-6, atol=1e-6)

@@ -300,6 +300,59 @@ def tc_measure(layers, desc, shape, dev, M, warmup):
             "calls": reps * len(layers)}
 
 
+def qkv_measure(shape, dev, n_sets, warmup):
+    """Time moe_qkv_forward over n_sets distinct projections.  One pass over
+    the sets is captured in a CUDA graph (the calls are a few microseconds
+    each, shorter than a Python-side launch), replayed, and timed with CUDA
+    events; bytes = the packed rows of a call (read once) plus its input and
+    output."""
+    import torch
+    import quantized_moe_decode_layer_gb300 as moe
+    import synth
+    H, rows = shape.H, (4096, 512, 512)
+    sets = []
+    for i in range(n_sets):
+        g = torch.Generator(device=dev).manual_seed(7000 + i)
+        mats = [synth.quant_matrix(g, (n,), H, 8, dev) for n in rows]
+        sets.append(moe.QKV(H, *mats, bits=8))
+        del mats
+    torch.cuda.empty_cache()
+    res = {}
+    for M in (1, 4):
+        x = synth.make_rows(shape, 60 + M, M).to(dev)
+        y = torch.empty((M, sum(rows)), dtype=torch.float32, device=dev)
+        err = torch.zeros(1, dtype=torch.int32, device=dev)
+        side = torch.cuda.Stream()
+        with torch.cuda.stream(side):
+            for _ in range(max(1, warmup)):
+                for q in sets:
+                    q.forward(x, out=y, err=err)
+        torch.cuda.synchronize()
+        graph = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(graph):
+            for q in sets:
+                q.forward(x, out=y, err=err)
+        graph.replay()
+        torch.cuda.synchronize()
+        reps = 10
+        a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        a.record()
+        for _ in range(reps):
+            graph.replay()
+        b.record()
+        torch.cuda.synchronize()
+        assert int(err.item()) == 0
+        per = a.elapsed_time(b) * 1e-3 / (reps * len(sets))
+        nbytes = sets[0].nbytes + x.numel() * 2 + y.numel() * 4
+        res[str(M)] = {"us_per_call": round(per * 1e6, 3), "gbs": round(nbytes / per / 1e9, 1),
+                       "bytes_per_call": nbytes, "calls": reps * len(sets), "timing": "CUDA graph replay"}
+        del graph
+    res["shape"] = "H 2048, Q 4096 + K 512 + V 512 rows, 8-bit groups of 64"
+    del sets
+    torch.cuda.empty_cache()
+    return res
+
+
 def run_ours(args):
     import numpy as np
     import torch
@@ -430,6 +483,13 @@ def run_ours(args):
     if not args.no_m4:
         tc = {str(M): tc_measure(layers, desc, shape, dev, M, args.warmup) for M in (8, 32)}
 
+    # the fused Q/K/V projection (8-bit, Q 16 heads x 256, K and V 2 heads x
+    # 256 over H = 2048) over 40 distinct weight sets (445 MB, L2 cannot hold
+    # them), one call per set, at 1 and 4 rows
+    qkv = None
+    if not args.no_m4:
+        qkv = qkv_measure(shape, dev, args.layers, args.warmup)
+
     # the 397B-shaped layer at M=1: a stack over 15 distinct layer sets (55 GB)
     b397 = None
     if not args.no_m4:
@@ -484,7 +544,8 @@ def run_ours(args):
                               f"({sum(l.nbytes for l in layers) / 1e9:.1f} GB) > L2; no flush"),
                        "parallelism": f"replicas x{world}"},
             "us_per_layer": round(us_layer, 3), "fraction_of_8TBs": round(value / world / 8000.0, 4),
-            "single_layer_call_us": single, "m4": m4, "sweep": sweep, "tc_gate_up": tc, "b397": b397, "roofline": roof, "e2e": e2e,
+            "single_layer_call_us": single, "m4": m4, "sweep": sweep, "tc_gate_up": tc, "b397": b397, "qkv": qkv,
+            "roofline": roof, "e2e": e2e,
             "gpu_launches": launches, "launches_per_step": launches / args.steps, "clocks": clocks,
             "cpu_baseline": cpu,
             "routing": {k: {"mean_U": round(float(np.mean(v["U_per_layer"])), 2),

@@ -311,6 +311,54 @@ int moe_gate_up_tc(const moe_layer *layer, const float *hn_dev, int M, const int
 int moe_down_tc(const moe_layer *layer, const float *act_dev, int M, const int32_t *experts_dev,
                 const uint32_t *masks_dev, int U, float *y_dev, int *err_dev, moe_stream_t stream);
 
+/* ------------------------------------------------------------------ */
+/* Fused Q/K/V projection.  "Qwen3.5-397B on M5 Max" (openclawradar),
+ * 効果的な最適化: the attention's Q, K and V projections are fused so that
+ * the input row is read once; the PureDrive-35B-A3B-MLX model card,
+ * "Summary", keeps attention weights at 8 bits.  The input is the layer's
+ * normalised activations, e.g. the out_normed rows a moe_decode_layer or
+ * moe_stack_forward call writes:
+ *
+ *   y[m, r] = W[r] . x_m,  W = [W_q; W_k; W_v] stacked row-wise ([n, H], n =
+ *   n_q + n_k + n_v), every row in affine groups of 64 along H (w = q * s + b,
+ *   bf16 s and b), x bf16 [M, H], y fp32 [M, n]: Q in columns [0, n_q), K in
+ *   [n_q, n_q + n_k), V after.
+ *
+ * The kernel streams each row block from memory once for all M rows; the
+ * rows of y are bitwise independent of M. */
+typedef struct moe_qkv_desc {
+    int H;      /* input width (multiple of 64, >= 128) */
+    int n_q;    /* rows of the Q projection (heads x head dim) */
+    int n_k;    /* rows of the K projection */
+    int n_v;    /* rows of the V projection */
+    int bits;   /* 4, 6 or 8 */
+} moe_qkv_desc;
+
+typedef struct moe_qkv moe_qkv;
+
+/* Bytes of the packed projection (rows of moe_pack_size's row format).
+ * Errors: INVALID_ARG (NULL), UNSUPPORTED (sizes, bits). */
+int moe_qkv_pack_size(const moe_qkv_desc *desc, size_t *bytes);
+
+/* Packs the three matrices (each a moe_src_matrix of [n_x, H]: canonical
+ * codes/scales/biases, or fp32 weights that are quantised as for the layer)
+ * into dst_dev (>= moe_qkv_pack_size bytes, 256-byte aligned) on `stream`, and
+ * returns a handle that borrows dst_dev.  Errors: INVALID_ARG, UNSUPPORTED,
+ * BUFFER_TOO_SMALL, CUDA. */
+int moe_qkv_pack(const moe_qkv_desc *desc, const moe_src_matrix *q, const moe_src_matrix *k,
+                 const moe_src_matrix *v, void *dst_dev, size_t dst_bytes, moe_qkv **out, moe_stream_t stream);
+
+/* y_dev[M, n] (fp32) = the projection of x_dev [M, H] (bf16, 16-byte
+ * aligned), enqueued on `stream`.  err_dev (a device int the caller zeroes)
+ * is set to 1 if a device wait runs out (see moe_debug_set).  M >= 1 and small
+ * enough that the M input rows fit in shared memory (M * H <= 32768).
+ * Errors: INVALID_ARG, UNSUPPORTED, CUDA. */
+int moe_qkv_forward(const moe_qkv *qkv, const uint16_t *x_dev, int M, float *y_dev, int *err_dev,
+                    moe_stream_t stream);
+
+/* Frees the handle (not the packed rows).  NULL is a no-op. */
+void moe_qkv_destroy(moe_qkv *qkv);
+
 /* Human-readable name of a status code (static string). */
 const char *moe_status_str(int status);
 

@@ -21,6 +21,7 @@ SYMBOLS = ["moe_pack_size", "moe_pack_weights", "moe_layer_destroy", "moe_export
            "moe_workspace_size", "moe_workspace_init", "moe_router_topk", "moe_decode_layer",
            "moe_stack_create", "moe_stack_forward", "moe_stack_forward_host", "moe_stack_destroy",
            "moe_decode_layer_noalloc", "moe_noalloc_status",
+           "moe_qkv_pack_size", "moe_qkv_pack", "moe_qkv_forward", "moe_qkv_destroy",
            "moe_stream_status", "moe_debug_set", "moe_debug_trace", "moe_set_grouped", "moe_gate_up_tc", "moe_down_tc", "moe_status_str",
            "moe_last_cuda_error",
            "moe_selftest_host", "moe_launch_count"]
@@ -41,6 +42,10 @@ class LayerDesc(C.Structure):
 class SrcMatrix(C.Structure):
     _fields_ = [("codes_dev", C.c_void_p), ("scales_dev", C.c_void_p), ("biases_dev", C.c_void_p),
                 ("w_dev", C.c_void_p)]
+
+
+class QkvDesc(C.Structure):
+    _fields_ = [("H", C.c_int), ("n_q", C.c_int), ("n_k", C.c_int), ("n_v", C.c_int), ("bits", C.c_int)]
 
 
 class SrcLayer(C.Structure):
@@ -77,6 +82,11 @@ def lib():
             "moe_stack_destroy": (None, [vp]),
             "moe_decode_layer_noalloc": (i, [vp, vp, i, vp, vp, vp]),
             "moe_noalloc_status": (i, [vp]),
+            "moe_qkv_pack_size": (i, [C.POINTER(QkvDesc), C.POINTER(sz)]),
+            "moe_qkv_pack": (i, [C.POINTER(QkvDesc), C.POINTER(SrcMatrix), C.POINTER(SrcMatrix), C.POINTER(SrcMatrix),
+                                 vp, sz, C.POINTER(vp), vp]),
+            "moe_qkv_forward": (i, [vp, vp, i, vp, vp, vp]),
+            "moe_qkv_destroy": (None, [vp]),
             "moe_stream_status": (i, [vp, sz, vp]),
             "moe_debug_set": (i, [i, C.c_longlong]),
             "moe_debug_trace": (i, [vp, sz]),

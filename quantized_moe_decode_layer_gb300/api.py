@@ -7,7 +7,7 @@ import ctypes as C
 import torch
 
 from . import _lib
-from ._lib import LayerDesc, SrcLayer, SrcMatrix, check, lib
+from ._lib import LayerDesc, QkvDesc, SrcLayer, SrcMatrix, check, lib
 
 
 def _ptr(t) -> int | None:
@@ -316,6 +316,58 @@ class Stack:
         try:
             if getattr(self, "handle", None):
                 lib().moe_stack_destroy(self.handle)
+                self.handle = None
+        except Exception:
+            pass
+
+
+class QKV:
+    """A packed fused Q/K/V projection (moe_qkv_pack): q, k, v are canonical
+    dicts (codes [n, H] uint8, scales/biases bf16 [n, H/64]) or fp32 weights
+    [n, H]; the device blob is a torch uint8 tensor owned here."""
+
+    def __init__(self, H: int, q, k, v, bits: int = 8, device="cuda", stream=None):
+        mats = [q, k, v]
+        rows = [(m["codes"] if isinstance(m, dict) and m.get("codes") is not None else
+                 (m["w"] if isinstance(m, dict) else m)).shape[0] for m in mats]
+        self.desc = QkvDesc(H, rows[0], rows[1], rows[2], bits)
+        self.rows = sum(rows)
+        n = C.c_size_t()
+        check("moe_qkv_pack_size", lib().moe_qkv_pack_size(C.byref(self.desc), C.byref(n)))
+        self.nbytes = n.value
+        self.blob = torch.empty(self.nbytes, dtype=torch.uint8, device=device)
+        srcs, keep = [], []
+        for m in mats:
+            sm, kp = _src_matrix(m)
+            srcs.append(sm)
+            keep += kp
+        h = C.c_void_p()
+        check("moe_qkv_pack", lib().moe_qkv_pack(C.byref(self.desc), C.byref(srcs[0]), C.byref(srcs[1]),
+                                                 C.byref(srcs[2]), _ptr(self.blob), self.nbytes, C.byref(h),
+                                                 _stream(stream)))
+        self.handle = h
+        torch.cuda.current_stream().synchronize() if stream is None else stream.synchronize()
+        del keep
+
+    def forward(self, x: torch.Tensor, out=None, err=None, stream=None):
+        """y fp32 [M, n_q + n_k + n_v] for x bf16 [M, H] (moe_qkv_forward);
+        returns (y, err) with err an int32 [1] device flag (1 = a wait ran out)."""
+        _need(x, "x", torch.bfloat16, (None, self.desc.H))
+        M = x.shape[0]
+        if out is None:
+            out = torch.empty((M, self.rows), dtype=torch.float32, device=x.device)
+        _need(out, "out", torch.float32, (M, self.rows))
+        if err is None:
+            err = torch.zeros(1, dtype=torch.int32, device=x.device)
+        _need(err, "err", torch.int32, (1,))
+        check("moe_qkv_forward", lib().moe_qkv_forward(self.handle, _ptr(_bits16(x)), M, _ptr(out), _ptr(err),
+                                                       _stream(stream)))
+        return out, err
+
+    def __del__(self):
+        try:
+            if getattr(self, "handle", None):
+                lib().moe_qkv_destroy(self.handle)
                 self.handle = None
         except Exception:
             pass

@@ -646,6 +646,63 @@ int moe_down_tc(const moe_layer *layer, const float *act_dev, int M, const int32
                           reinterpret_cast<cudaStream_t>(stream));
 }
 
+namespace {
+bool qkv_desc_ok(const moe_qkv_desc &d)
+{
+    return d.H >= 128 && d.H % kGroup == 0 && d.n_q >= 0 && d.n_k >= 0 && d.n_v >= 0 && d.n_q + d.n_k + d.n_v >= 1 &&
+           bits_ok(d.bits) && (long long)d.n_q + d.n_k + d.n_v < (1ll << 30);
+}
+}  // namespace
+
+int moe_qkv_pack_size(const moe_qkv_desc *desc, size_t *bytes)
+{
+    if (!desc || !bytes) return MOE_ERR_INVALID_ARG;
+    if (!qkv_desc_ok(*desc)) return MOE_ERR_UNSUPPORTED;
+    *bytes = (size_t)(desc->n_q + desc->n_k + desc->n_v) * row_bytes(desc->H, desc->bits);
+    return MOE_OK;
+}
+
+int moe_qkv_pack(const moe_qkv_desc *desc, const moe_src_matrix *q, const moe_src_matrix *k, const moe_src_matrix *v,
+                 void *dst_dev, size_t dst_bytes, moe_qkv **out, moe_stream_t stream)
+{
+    if (!desc || !q || !k || !v || !dst_dev || !out) return MOE_ERR_INVALID_ARG;
+    *out = nullptr;
+    if (!qkv_desc_ok(*desc)) return MOE_ERR_UNSUPPORTED;
+    const int rb = row_bytes(desc->H, desc->bits), n = desc->n_q + desc->n_k + desc->n_v;
+    if (dst_bytes < (size_t)n * rb) return MOE_ERR_BUFFER_TOO_SMALL;
+    if ((reinterpret_cast<uintptr_t>(dst_dev) & 255) != 0) return MOE_ERR_INVALID_ARG;
+    uint8_t *base = static_cast<uint8_t *>(dst_dev);
+    cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
+    const moe_src_matrix *src[3] = {q, k, v};
+    const int rows[3] = {desc->n_q, desc->n_k, desc->n_v};
+    size_t off = 0;
+    for (int i = 0; i < 3; ++i) {
+        if (rows[i] > 0) {
+            const int rc = launch_pack_rows(*src[i], desc->bits, rows[i], desc->H, base + off, st);
+            if (rc) return rc;
+        }
+        off += (size_t)rows[i] * rb;
+    }
+    moe_qkv *h = static_cast<moe_qkv *>(calloc(1, sizeof(moe_qkv)));
+    if (!h) return MOE_ERR_INVALID_ARG;
+    h->desc = *desc;
+    h->rows = n;
+    h->row_bytes = rb;
+    h->base = base;
+    *out = h;
+    return MOE_OK;
+}
+
+int moe_qkv_forward(const moe_qkv *qkv, const uint16_t *x_dev, int M, float *y_dev, int *err_dev, moe_stream_t stream)
+{
+    if (!qkv || !x_dev || !y_dev || !err_dev || M < 1 || !aligned16(x_dev)) return MOE_ERR_INVALID_ARG;
+    if ((long long)M * qkv->desc.H > 32768) return MOE_ERR_UNSUPPORTED;
+    return launch_qkv(qkv->base, qkv->rows, qkv->desc.H, qkv->desc.bits, x_dev, M, y_dev, err_dev, g_timeout_ns,
+                      reinterpret_cast<cudaStream_t>(stream));
+}
+
+void moe_qkv_destroy(moe_qkv *qkv) { free(qkv); }
+
 const char *moe_status_str(int status)
 {
     switch (status) {

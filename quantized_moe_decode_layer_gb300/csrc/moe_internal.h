@@ -155,11 +155,23 @@ struct moe_stack {
     moe_layer **layers;
 };
 
+struct moe_qkv {
+    moe_qkv_desc desc;
+    int rows;          // n_q + n_k + n_v
+    int row_bytes;
+    uint8_t *base;     // packed rows (borrowed)
+};
+
 // Host-side entry points of the kernels (moe_layer.cu, moe_pack.cu, moe_tc.cu,
 // moe_grouped.cu).
 namespace moe {
 int launch_decode(const KParams &kp, cudaStream_t stream);
 int launch_pack(const moe_layer &L, const moe_src_layer &src, cudaStream_t stream);
+// rows of one matrix into consecutive packed rows at dst (moe_pack.cu)
+int launch_pack_rows(const moe_src_matrix &m, int bits, int rows, int K, uint8_t *dst, cudaStream_t stream);
+// fused Q/K/V projection (moe_layer.cu)
+int launch_qkv(const uint8_t *W, int rows, int K, int bits, const uint16_t *x, int M, float *y, int *err,
+               long long timeout_ns, cudaStream_t stream);
 int launch_export(const moe_layer &L, int tensor_id, int expert, uint8_t *codes, uint16_t *scales,
                   uint16_t *biases, cudaStream_t stream);
 // One set of grouped tensor-core products (moe_tc.cu): slot u's expert

@@ -2321,6 +2321,163 @@ __global__ void __launch_bounds__(kThreads, 1) moe_decode_kernel(const __grid_co
     if (threadIdx.x == 0) kernel_exit(kp, sh);
 }
 
+// ------------------------------------------------ fused Q/K/V projection
+//
+// y[m, r] = W[r] . x_m for the stacked rows of an attention's Q, K and V
+// projections (or a Gated-DeltaNet input projection): "Qwen3.5-397B on M5
+// Max" (openclawradar), 効果的な最適化: the Q/K/V projections fused so that
+// the input row is read once.  x is the layer's normalised input (the MoE
+// layer's fused out_n, bf16).  Each CTA streams its block of rows from HBM
+// once, in up to kQkvChunks bulk copies with an mbarrier each; it stages the
+// M input rows arranged and times 2^100 with their group sums, and its warps
+// take the block's rows with the layer's row kernels, two token rows at a
+// time (each code decoded once for both) or one; a row's arithmetic is the
+// same in both, so its result does not depend on M.
+constexpr int kQkvChunks = 4;
+constexpr int kQkvThreads = 256;
+
+struct QkvParams {
+    const uint8_t *W;    // rows of row_bytes(K, bits)
+    int rows, K, bits, rowb;
+    const uint16_t *x;   // [M, K] bf16
+    int M;
+    float *y;            // [M, rows]
+    int rows_per_cta;
+    long long timeout_ns;
+    int *err;            // set to 1 when a wait runs out (caller clears it)
+};
+
+__host__ __device__ inline size_t qkv_x_bytes(int M, int K) { return align_up((size_t)M * K * 4 + (size_t)M * (K / kGroup) * 4, 128); }
+
+__global__ void __launch_bounds__(kQkvThreads) qkv_kernel(const __grid_constant__ QkvParams q)
+{
+    extern __shared__ __align__(128) uint8_t smem[];
+    const int r0 = blockIdx.x * q.rows_per_cta;
+    const int nr = min(q.rows_per_cta, q.rows - r0);
+    if (nr <= 0) return;
+    const int K = q.K, G = K / kGroup, M = q.M, tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+    constexpr int NW = kQkvThreads / 32;
+    uint64_t *bars = reinterpret_cast<uint64_t *>(smem);
+    float4 *xs = reinterpret_cast<float4 *>(smem + 128);
+    float *xsum = reinterpret_cast<float *>(smem + 128 + (size_t)M * K * 4);
+    uint8_t *rows = smem + 128 + qkv_x_bytes(M, K);
+    const int cr = (nr + kQkvChunks - 1) / kQkvChunks;
+    if (tid == 0) {
+#pragma unroll 1
+        for (int c = 0; c < kQkvChunks; ++c) mbar_init(&bars[c], 1);
+        asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+    }
+    __syncthreads();
+    if (tid == 0) {
+#pragma unroll 1
+        for (int c = 0; c < kQkvChunks; ++c) {
+            const int a = c * cr, n = min(cr, nr - a);
+            if (n <= 0) break;
+            mbar_expect_tx(&bars[c], (unsigned)(n * q.rowb));
+            bulk_load(rows + (size_t)a * q.rowb, q.W + (size_t)(r0 + a) * q.rowb, (unsigned)(n * q.rowb), &bars[c]);
+        }
+    }
+    // the input rows: 8 consecutive inputs per thread item, arranged (float4
+    // t * G + g holds inputs 64 g + 4 t ..), times 2^100; group sums
+    const int per_row = K / 8, total = M * per_row;
+#pragma unroll 1
+    for (int base = 0; base < total; base += kQkvThreads) {
+        const int it = base + tid;
+        float gs = 0.f;
+        if (it < total) {
+            const int m = it / per_row, c = it - m * per_row;
+            const uint4 v = __ldg(reinterpret_cast<const uint4 *>(q.x) + it);
+            const uint32_t w[4] = {v.x, v.y, v.z, v.w};
+            float f[8];
+#pragma unroll
+            for (int j = 0; j < 4; ++j) {
+                f[2 * j] = __uint_as_float(w[j] << 16);
+                f[2 * j + 1] = __uint_as_float(w[j] & 0xFFFF0000u);
+            }
+#pragma unroll
+            for (int j = 0; j < 8; ++j) gs += f[j];
+            const int g = c >> 3, t = (c & 7) * 2;
+            float4 *row = xs + (size_t)m * (K / 4);
+            row[t * G + g] = make_float4(f[0] * kXScale, f[1] * kXScale, f[2] * kXScale, f[3] * kXScale);
+            row[(t + 1) * G + g] = make_float4(f[4] * kXScale, f[5] * kXScale, f[6] * kXScale, f[7] * kXScale);
+        }
+        gs += __shfl_xor_sync(FULLMASK, gs, 4);
+        gs += __shfl_xor_sync(FULLMASK, gs, 2);
+        gs += __shfl_xor_sync(FULLMASK, gs, 1);
+        if (it < total && (it & 7) == 0) {
+            const int m = it / per_row, c = it - m * per_row;
+            xsum[m * G + (c >> 3)] = gs;
+        }
+    }
+    __syncthreads();
+    const uint32_t xq0 = smem_u32(xs), xs0 = smem_u32(xsum);
+    // every chunk (they travel together), bounded: a wait that runs out sets
+    // the error word and the CTA leaves after its copies have landed
+    bool ok = true;
+#pragma unroll 1
+    for (int c = 0; c < kQkvChunks && ok; ++c) {
+        if (c * cr >= nr) break;
+        if (mbar_try_wait(&bars[c], 0u)) continue;
+        const unsigned long long t0 = now_ns();
+#pragma unroll 1
+        while (!(ok = mbar_try_wait_sleep(&bars[c], 0u, 2000)))
+            if (now_ns() - t0 > (unsigned long long)q.timeout_ns) break;
+    }
+    if (!__syncthreads_and(ok)) {
+        if (tid == 0) {
+            atomicExch(q.err, 1);
+#pragma unroll 1
+            for (int c2 = 0; c2 < kQkvChunks && c2 * cr < nr; ++c2) {
+                const unsigned long long t0 = now_ns();
+                while (!mbar_try_wait(&bars[c2], 0u) && now_ns() - t0 < (unsigned long long)q.timeout_ns) {}
+            }
+        }
+        return;
+    }
+    // warp w: rows w, w + NW, ... of the block; token rows two at a time
+    // (the codes decoded once for both), the last one alone; each row's
+    // arithmetic is the same in both kernels
+    const int cnt = (nr - warp + NW - 1) / NW;
+    if (cnt <= 0) return;
+    const uint8_t *rp = rows + (size_t)warp * q.rowb;
+    const uint32_t rbase = smem_u32(rp);
+    float *yb = q.y + r0 + warp;
+#pragma unroll 1
+    for (int m = 0; m < M; m += 2) {
+        if (m + 1 < M) {
+            const uint32_t xqa[2] = {xq0 + (uint32_t)(m * K * 4), xq0 + (uint32_t)((m + 1) * K * 4)};
+            const int soff[2] = {m * G, (m + 1) * G};
+            float xsg[2][kMaxGPL];
+            lane_gsums<2>(xs0, soff, K, xsg);
+            auto emit = [&](int rb, const float (&acc)[1][2]) {
+                yb[(size_t)m * q.rows + (size_t)rb * NW] = acc[0][0];
+                yb[(size_t)(m + 1) * q.rows + (size_t)rb * NW] = acc[0][1];
+            };
+            if (q.bits == 8) warp_rows<8, 1, 2>(rp, NW * q.rowb, cnt, K, xqa, xsg, emit);
+            else if (q.bits == 6) warp_rows<6, 1, 2>(rp, NW * q.rowb, cnt, K, xqa, xsg, emit);
+            else warp_rows<4, 1, 2>(rp, NW * q.rowb, cnt, K, xqa, xsg, emit);
+        } else {
+            const uint32_t xq = xq0 + (uint32_t)(m * K * 4), xsq = xs0 + (uint32_t)(m * G * 4);
+            float *dst = yb + (size_t)m * q.rows;
+            if (K <= 32 * kGroup) {
+                if (q.bits == 8) plain1<8>(rbase, cnt, NW * q.rowb, K, xq, xsq, dst, NW, 0u);
+                else if (q.bits == 6) plain1<6>(rbase, cnt, NW * q.rowb, K, xq, xsq, dst, NW, 0u);
+                else plain1<4>(rbase, cnt, NW * q.rowb, K, xq, xsq, dst, NW, 0u);
+            } else {
+                const uint32_t xqa[1] = {xq};
+                const int soff[1] = {m * G};
+                float xsg[1][kMaxGPL];
+                lane_gsums<1>(xs0, soff, K, xsg);
+                auto emit = [&](int rb, const float (&acc)[1][1]) { dst[(size_t)rb * NW] = acc[0][0]; };
+                if (q.bits == 8) warp_rows<8, 1, 1>(rp, NW * q.rowb, cnt, K, xqa, xsg, emit);
+                else if (q.bits == 6) warp_rows<6, 1, 1>(rp, NW * q.rowb, cnt, K, xqa, xsg, emit);
+                else warp_rows<4, 1, 1>(rp, NW * q.rowb, cnt, K, xqa, xsg, emit);
+            }
+        }
+    }
+    (void)lane;
+}
+
 int g_num_sms[64];
 bool g_attr_set[64];
 
@@ -2453,4 +2610,40 @@ int device_sms()
     return g_num_sms[dev];
 }
 
+int qkv_smem_bytes(int M, int K, int rows_per_cta, int rowb)
+{
+    return (int)(128 + qkv_x_bytes(M, K) + (size_t)rows_per_cta * rowb);
+}
+
+int launch_qkv(const uint8_t *W, int rows, int K, int bits, const uint16_t *x, int M, float *y, int *err,
+               long long timeout_ns, cudaStream_t stream)
+{
+    const int sms = device_sms();
+    if (sms <= 0) return MOE_ERR_CUDA;
+    const int rowb = row_bytes(K, bits);
+    // rows per CTA: an even share over the SMs, fewer if they do not fit in
+    // shared memory beside the staged input rows
+    int per = (rows + sms - 1) / sms;
+    const int room = kSmemMax - 128 - (int)qkv_x_bytes(M, K);
+    if (room < rowb) return MOE_ERR_UNSUPPORTED;
+    if (per * rowb > room) per = room / rowb;
+    static bool attr_set[64];
+    int dev = 0;
+    cudaError_t e = cudaGetDevice(&dev);
+    if (e != cudaSuccess || dev < 0 || dev >= 64) { note_cuda_error((int)e); return MOE_ERR_CUDA; }
+    if (!attr_set[dev]) {
+        e = cudaFuncSetAttribute(qkv_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, kSmemMax);
+        if (e != cudaSuccess) { note_cuda_error((int)e); return MOE_ERR_CUDA; }
+        attr_set[dev] = true;
+    }
+    QkvParams q{W, rows, K, bits, rowb, x, M, y, per, timeout_ns, err};
+    const int grid = (rows + per - 1) / per;
+    qkv_kernel<<<grid, kQkvThreads, qkv_smem_bytes(M, K, per, rowb), stream>>>(q);
+    note_launch();
+    e = cudaGetLastError();
+    if (e != cudaSuccess) { note_cuda_error((int)e); return MOE_ERR_CUDA; }
+    return MOE_OK;
+}
+
 }  // namespace moe
+

@@ -165,6 +165,11 @@ int pack_matrix(const moe_src_matrix &m, int bits, int rows, int K, PackDst dst,
 
 }  // namespace
 
+int launch_pack_rows(const moe_src_matrix &m, int bits, int rows, int K, uint8_t *dst, cudaStream_t st)
+{
+    return pack_matrix(m, bits, rows, K, PackDst{dst, (size_t)row_bytes(K, bits), 0}, st);
+}
+
 int launch_pack(const moe_layer &L, const moe_src_layer &src, cudaStream_t st)
 {
     const Geo &g = L.geo;

@@ -113,3 +113,24 @@ def test_binding_wrappers_for_selftest_and_noalloc():
     stand_in = types.SimpleNamespace(desc=types.SimpleNamespace(H=8))
     with pytest.raises(ValueError):
         moe.decode_layer_noalloc(stand_in, torch.zeros((1, 8), dtype=torch.bfloat16))
+
+
+def test_qkv_sizes_and_argument_errors():
+    """The fused projection's size query counts stacked packed rows; bad
+    descriptors and missing pointers are refused before any device work."""
+    L = moe.lib()
+    n = C.c_size_t()
+    d = _lib.QkvDesc(2048, 4096, 512, 512, 8)
+    assert L.moe_qkv_pack_size(C.byref(d), C.byref(n)) == 0
+    assert n.value == 5120 * (2048 + 32 * 4)        # codes + one scale/bias word per 64-group
+    d6 = _lib.QkvDesc(256, 64, 32, 32, 6)
+    assert L.moe_qkv_pack_size(C.byref(d6), C.byref(n)) == 0 and n.value == 128 * (192 + 16)
+    for bad in (_lib.QkvDesc(2048, 4096, 512, 512, 5), _lib.QkvDesc(100, 64, 0, 0, 8), _lib.QkvDesc(256, 0, 0, 0, 8)):
+        assert L.moe_qkv_pack_size(C.byref(bad), C.byref(n)) == 2
+    assert L.moe_qkv_pack_size(None, C.byref(n)) == 1
+    h = C.c_void_p()
+    m = _lib.SrcMatrix()
+    assert L.moe_qkv_pack(C.byref(d), C.byref(m), C.byref(m), C.byref(m), None, 0, C.byref(h), None) == 1
+    assert L.moe_qkv_pack(C.byref(d), C.byref(m), C.byref(m), C.byref(m), C.c_void_p(256), 16, C.byref(h), None) == 3
+    assert L.moe_qkv_forward(None, None, 1, None, None, None) == 1
+    L.moe_qkv_destroy(None)

@@ -248,6 +248,27 @@ int moe_stream_status(void *ws_dev, size_t ws_bytes, moe_stream_t stream);
  * returns MOE_ERR_TIMEOUT instead of hanging. */
 int moe_debug_set(int skip_row, long long timeout_ns);
 
+/* Build flags of the loaded library: MOE_BUILD_DEBUG_BOUNDS is set in the
+ * bounds-checked build (libmoe_debug.so, compiled with MOE_DEBUG_BOUNDS).
+ * In that build the persistent kernel compares every index it computes from
+ * data (the expert ids out of the top-k, slot and activation-pair numbers)
+ * with the size of the array it indexes before the access; an index out of
+ * range sets a bit of the workspace status word, is replaced by 0 so that
+ * the launch stays inside its buffers and runs to its end, and the call (or
+ * moe_stream_status) returns MOE_ERR_DEVICE.  The checked build computes the
+ * same results as the normal one when no check fails.  No CUDA call; never
+ * fails. */
+#define MOE_BUILD_DEBUG_BOUNDS 1
+int moe_build_flags(void);
+
+/* Test hook of the bounds-checked build: while expert >= 0, the next decode
+ * calls on the persistent kernel make token row 0 of their first layer
+ * report `expert` as its first routing choice, as a faulty top-k would;
+ * an id >= E is caught by the checks above (MOE_ERR_DEVICE).  expert < 0
+ * turns it off.  Host state only.  Returns MOE_ERR_UNSUPPORTED in the
+ * normal build, which has neither the hook nor the checks. */
+int moe_debug_inject(int expert);
+
 /* Diagnostic hook: while set, every decode launch records globaltimer
  * stamps (ns) into trace_dev: [CTA][layer][24] as uint64 for the first
  * min(layers, 64) layers of a launch, followed by a per-warp timeline of two

@@ -9,7 +9,10 @@ import ctypes as C
 import os
 
 HERE = os.path.dirname(os.path.abspath(__file__))
-LIB_PATH = os.path.join(HERE, "libmoe.so")
+# MOE_DEBUG_BOUNDS=1 in the environment selects the bounds-checked build
+# (libmoe_debug.so); it is read once, when the library is first loaded.
+DEBUG_BOUNDS = os.environ.get("MOE_DEBUG_BOUNDS", "0") not in ("", "0")
+LIB_PATH = os.path.join(HERE, "libmoe_debug.so" if DEBUG_BOUNDS else "libmoe.so")
 
 MOE_OK = 0
 STATUS = {0: "MOE_OK", 1: "MOE_ERR_INVALID_ARG", 2: "MOE_ERR_UNSUPPORTED", 3: "MOE_ERR_BUFFER_TOO_SMALL",
@@ -22,7 +25,7 @@ SYMBOLS = ["moe_pack_size", "moe_pack_weights", "moe_layer_destroy", "moe_export
            "moe_stack_create", "moe_stack_forward", "moe_stack_forward_host", "moe_stack_destroy",
            "moe_decode_layer_noalloc", "moe_noalloc_status",
            "moe_qkv_pack_size", "moe_qkv_pack", "moe_qkv_forward", "moe_qkv_destroy",
-           "moe_stream_status", "moe_debug_set", "moe_debug_trace", "moe_set_grouped", "moe_gate_up_tc", "moe_down_tc", "moe_status_str",
+           "moe_stream_status", "moe_build_flags", "moe_debug_inject", "moe_debug_set", "moe_debug_trace", "moe_set_grouped", "moe_gate_up_tc", "moe_down_tc", "moe_status_str",
            "moe_last_cuda_error",
            "moe_selftest_host", "moe_launch_count"]
 
@@ -89,6 +92,8 @@ def lib():
             "moe_qkv_destroy": (None, [vp]),
             "moe_stream_status": (i, [vp, sz, vp]),
             "moe_debug_set": (i, [i, C.c_longlong]),
+            "moe_build_flags": (i, []),
+            "moe_debug_inject": (i, [i]),
             "moe_debug_trace": (i, [vp, sz]),
             "moe_gate_up_tc": (i, [vp, vp, i, vp, vp, i, vp, vp, vp]),
             "moe_down_tc": (i, [vp, vp, i, vp, vp, i, vp, vp, vp]),

@@ -377,6 +377,16 @@ def debug_set(skip_row: int = -1, timeout_ns: int = 0) -> None:
     check("moe_debug_set", lib().moe_debug_set(skip_row, timeout_ns))
 
 
+def build_flags() -> int:
+    """moe_build_flags: MOE_BUILD_DEBUG_BOUNDS (1) in the bounds-checked build."""
+    return int(lib().moe_build_flags())
+
+
+def debug_inject(expert: int = -1) -> None:
+    """moe_debug_inject (bounds-checked build only; raises MoeError otherwise)."""
+    check("moe_debug_inject", lib().moe_debug_inject(expert))
+
+
 def launch_count(reset: bool = False) -> int:
     return int(lib().moe_launch_count(1 if reset else 0))
 

@@ -16,6 +16,7 @@ namespace {
 thread_local int t_last_cuda_error = 0;
 thread_local long long t_launches = 0;
 int g_skip_row = -1;
+int g_inject_e = -1;   // checked build only (moe_debug_inject)
 unsigned long long *g_trace = nullptr;
 long long g_timeout_ns = 2000000000LL;
 // Grouped mode for M above one launch's rows and at least this (0 = off).
@@ -162,6 +163,7 @@ int prepare(const moe_layer *layer, int M, void *ws, size_t ws_bytes, KParams &k
     kp.ws = reinterpret_cast<uint8_t *>(ws);
     kp.timeout_ns = g_timeout_ns;
     kp.skip_row = g_skip_row;
+    kp.inject_e = g_inject_e;
     kp.trace = g_trace;
     return MOE_OK;
 }
@@ -613,6 +615,26 @@ int moe_debug_set(int skip_row, long long timeout_ns)
     g_skip_row = skip_row;
     g_timeout_ns = timeout_ns > 0 ? timeout_ns : 2000000000LL;
     return MOE_OK;
+}
+
+int moe_build_flags(void)
+{
+#ifdef MOE_DEBUG_BOUNDS
+    return MOE_BUILD_DEBUG_BOUNDS;
+#else
+    return 0;
+#endif
+}
+
+int moe_debug_inject(int expert)
+{
+#ifdef MOE_DEBUG_BOUNDS
+    g_inject_e = expert < 0 ? -1 : expert;
+    return MOE_OK;
+#else
+    (void)expert;
+    return MOE_ERR_UNSUPPORTED;
+#endif
 }
 
 int moe_debug_trace(void *trace_dev, size_t bytes)

@@ -129,6 +129,7 @@ struct KParams {
     WsLayout ws_l;
     long long timeout_ns;
     int skip_row;            // debug: router logit row left unpublished in layer 0 (-1 = none)
+    int inject_e;            // checked build only: id row 0 of layer 0 reports as its first choice (-1 = none)
     unsigned long long *trace;   // optional per-CTA phase timestamps (ns), NULL = off
 };
 

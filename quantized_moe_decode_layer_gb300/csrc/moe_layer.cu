@@ -355,6 +355,29 @@ __device__ __forceinline__ unsigned layer_tag(const Sh &sh, int l) { return sh.e
 
 __device__ __forceinline__ bool aborted(const Sh &sh) { return *(volatile int *)&sh.flags[0] != 0; }
 
+// Bounds-checked build (compiled with MOE_DEBUG_BOUNDS): an index computed
+// from data (an expert id out of the top-k, a slot or pair number) is
+// compared with the size of what it indexes before it is used; one out of
+// range sets kStatusBounds in the status word, records 1000 + site in
+// `where`, and is replaced by 0 so that the access stays inside its array
+// and the launch runs to its end (the host then returns MOE_ERR_DEVICE).
+// In the normal build the check is the identity.
+#ifdef MOE_DEBUG_BOUNDS
+__device__ __noinline__ void bounds_fail(const Sh &sh, int site)
+{
+    atomicOr(&sh.ctrl->status, kStatusBounds);
+    atomicExch(&sh.ctrl->where, 1000 + site);
+}
+__device__ __forceinline__ int chk(const Sh &sh, int v, int lim, int site)
+{
+    if ((unsigned)v < (unsigned)lim) return v;
+    bounds_fail(sh, site);
+    return 0;
+}
+#else
+__device__ __forceinline__ int chk(const Sh &, int v, int, int) { return v; }
+#endif
+
 __device__ void raise_abort(const Sh &sh, int where)
 {
     *(volatile int *)&sh.flags[0] = 1;
@@ -1453,6 +1476,12 @@ __device__ __noinline__ void topk_row_t(const KParams &kp, const Sh &sh, int m, 
         }
     }
     __syncwarp();
+#ifdef MOE_DEBUG_BOUNDS
+    // test hook of the checked build: row 0 of the first layer reports the
+    // id set by moe_debug_inject as its first choice
+    if (kp.inject_e >= 0 && tag == layer_tag(sh, 0) && m == 0 && lane == 0) tope[0] = kp.inject_e;
+    __syncwarp();
+#endif
     // renormalised softmax weights over the k kept logits (the full softmax
     // probabilities divided by their top-k sum)
     const float ev = lane < k ? expf(topv[lane] - topv[0]) : 0.f;
@@ -1500,7 +1529,7 @@ __device__ void route(const KParams &kp, const Sh &sh, const uint64_t *logits, i
         // one row: the slots are its k experts in id order
 #pragma unroll 1
         for (int j = lane; j < k; j += 32) {
-            sh.slot_e[j] = sh.row_pair[j];
+            sh.slot_e[j] = chk(sh, sh.row_pair[j], E, 1);
             sh.slot_mask[j] = 1u;
             sh.slot_rowbase[j] = j;
             sh.row_pair[j] = j;
@@ -1510,7 +1539,7 @@ __device__ void route(const KParams &kp, const Sh &sh, const uint64_t *logits, i
 #pragma unroll 1
         for (int m = 0; m < M; ++m)
 #pragma unroll 1
-            for (int j = lane; j < k; j += 32) atomicOr(&sh.emask[sh.tope[m * kMaxK + j]], 1u << m);
+            for (int j = lane; j < k; j += 32) atomicOr(&sh.emask[chk(sh, sh.tope[m * kMaxK + j], E, 2)], 1u << m);
         __syncwarp();
         U = 0;
 #pragma unroll 1
@@ -1519,13 +1548,14 @@ __device__ void route(const KParams &kp, const Sh &sh, const uint64_t *logits, i
             const uint32_t em = e < E ? sh.emask[e] : 0u;
             const unsigned bal = __ballot_sync(FULLMASK, em != 0u);
             if (em) {
-                const int pos = U + __popc(bal & ((1u << lane) - 1u));
+                const int pos = chk(sh, U + __popc(bal & ((1u << lane) - 1u)), kp.ws_l.max_slots, 3);
                 sh.slot_e[pos] = e;
                 sh.slot_mask[pos] = em;
                 sh.eslot[e] = pos;
             }
             U += __popc(bal);
         }
+        U = min(U, kp.ws_l.max_slots);
         __syncwarp();
         // pair bases: prefix sums of popc(mask) over the slots
         npairs = 0;
@@ -1547,7 +1577,7 @@ __device__ void route(const KParams &kp, const Sh &sh, const uint64_t *logits, i
         for (int m = 0; m < M; ++m)
 #pragma unroll 1
             for (int j = lane; j < k; j += 32) {
-                const int s = sh.eslot[sh.row_pair[m * kMaxK + j]];
+                const int s = chk(sh, sh.eslot[chk(sh, sh.row_pair[m * kMaxK + j], E, 4)], U, 5);
                 sh.row_pair[m * kMaxK + j] = sh.slot_rowbase[s] + __popc(sh.slot_mask[s] & ((1u << m) - 1u));
             }
     }
@@ -1676,7 +1706,7 @@ __device__ __forceinline__ void sched_p2(const KParams &kp, const Sh &sh, const 
 {
     const int ub = 2 * kp.g.g_bytes;
     p2_units(kp, sh, sh.flags[1], [&](int s, int j, int cnt) {
-        f(Lp.gu + ((size_t)sh.slot_e[s] * kp.g.I + j) * ub, cnt * ub, s, j, cnt);
+        f(Lp.gu + ((size_t)chk(sh, sh.slot_e[s], kp.g.E, 6) * kp.g.I + j) * ub, cnt * ub, s, j, cnt);
     });
 }
 
@@ -1693,7 +1723,7 @@ __device__ __forceinline__ void sched_p3(const KParams &kp, const Sh &sh, const 
     const int cd = max(1, min(sh.S / g.d_bytes, nh));
 #pragma unroll 1
     for (int s = 0; s < U; ++s) {
-        const int e = sh.slot_e[s];
+        const int e = chk(sh, sh.slot_e[s], g.E, 8);
 #pragma unroll 1
         for (int r = 0; r < nh; r += cd) {
             const int n = min(cd, nh - r);
@@ -1831,7 +1861,8 @@ __device__ __forceinline__ void producer(const KParams &kp, const Sh &sh, int la
             if (lane == 0) stamp(kp, l, 10);
             if (fast) {
                 const int ub = 2 * kp.g.g_bytes;
-                const uint8_t *src = lane < nst ? Lp.gu + ((size_t)sh.slot_e[my_s] * kp.g.I + my_j) * ub : nullptr;
+                const uint8_t *src =
+                    lane < nst ? Lp.gu + ((size_t)chk(sh, sh.slot_e[my_s], kp.g.E, 7) * kp.g.I + my_j) * ub : nullptr;
                 if (!issue_batch(sh, lane < nst, mine.slot, mine.par, mine.reuse, src, my_n * ub)) break;
 #pragma unroll 1
                 for (int i = 0; i < nst; ++i) cursor_next(c, sh.NS);
@@ -2085,7 +2116,8 @@ __device__ bool phase3(const KParams &kp, const Sh &sh, const LayerPtrs &Lp, Cur
         for (int s = s0 + (int)threadIdx.x; s < s1; s += NCT) {
             uint32_t mk = sh.slot_mask[s];
 #pragma unroll 1
-            for (int p = sh.slot_rowbase[s] - p0; mk; mk &= mk - 1u, ++p) sh.pair_src[p] = s * kMaxRows + __ffs(mk) - 1;
+            for (int p = sh.slot_rowbase[s] - p0; mk; mk &= mk - 1u, ++p)
+                sh.pair_src[chk(sh, p, sh.act_pairs, 9)] = s * kMaxRows + __ffs(mk) - 1;
         }
         cbar();
         stage_acts(sh, np, g.I, threadIdx.x, NCT, tag, [&](int p) -> const uint64_t * {
@@ -2125,7 +2157,7 @@ __device__ void combine(const KParams &kp, const Sh &sh, int l, const float (&xr
 #pragma unroll 1
     for (int j = 0; j < k; ++j) {
         const float wv = sh.row_w[m * kMaxK + j];
-        const float *y = sh.yl + (size_t)sh.row_pair[m * kMaxK + j] * hr + 2 * pl;
+        const float *y = sh.yl + (size_t)chk(sh, sh.row_pair[m * kMaxK + j], sh.slot_rowbase[sh.flags[1]], 10) * hr + 2 * pl;
         acc[0] = fmaf(wv, y[0], acc[0]);
         acc[1] = fmaf(wv, y[1], acc[1]);
     }

@@ -134,3 +134,35 @@ def test_qkv_sizes_and_argument_errors():
     assert L.moe_qkv_pack(C.byref(d), C.byref(m), C.byref(m), C.byref(m), C.c_void_p(256), 16, C.byref(h), None) == 3
     assert L.moe_qkv_forward(None, None, 1, None, None, None) == 1
     L.moe_qkv_destroy(None)
+
+
+def _run_checked(code: str) -> str:
+    """Run `code` in a child interpreter that loads the bounds-checked build."""
+    import subprocess
+    import sys
+    from quantized_moe_decode_layer_gb300 import build as b
+    b.build(debug_bounds=True)
+    env = dict(os.environ, MOE_DEBUG_BOUNDS="1", PYTHONPATH=ROOT)
+    r = subprocess.run([sys.executable, "-c", code], env=env, capture_output=True, text=True, timeout=300, cwd=ROOT)
+    assert r.returncode == 0, r.stdout + r.stderr
+    return r.stdout
+
+
+def test_build_flags_of_both_builds():
+    """The normal build reports no flags and refuses the injection hook; the
+    checked build (selected by MOE_DEBUG_BOUNDS=1 at load time) reports
+    MOE_BUILD_DEBUG_BOUNDS, takes the hook, and exports the same symbols."""
+    assert moe.build_flags() == 0
+    assert not _lib.DEBUG_BOUNDS and _lib.LIB_PATH.endswith("libmoe.so")
+    with pytest.raises(moe.MoeError) as ei:
+        moe.debug_inject(3)
+    assert ei.value.code == 2
+    out = _run_checked(
+        "import quantized_moe_decode_layer_gb300 as m\n"
+        "from quantized_moe_decode_layer_gb300 import _lib\n"
+        "L = m.lib()\n"
+        "assert _lib.LIB_PATH.endswith('libmoe_debug.so')\n"
+        "missing = [n for n in _lib.SYMBOLS if not hasattr(L, n)]\n"
+        "m.debug_inject(7); m.debug_inject(-1)\n"
+        "print(m.build_flags(), len(missing), L.moe_selftest_host())\n")
+    assert out.split() == ["1", "0", "0"]

@@ -288,7 +288,9 @@ int moe_debug_trace(void *trace_dev, size_t bytes);
  * the one-row path's tolerance but not bitwise equal to it.  The default,
  * min_rows = 1, takes grouped mode whenever M exceeds one launch; min_rows = 0
  * keeps every M on the FMA path (launches of 8 rows, each re-reading the
- * experts its rows share).  The grouped regions of the workspace are included in
+ * experts its rows share), where every row of any M is bitwise its one-row
+ * result: a row-exact verify caller with more rows than one launch sets
+ * min_rows = 0.  The grouped regions of the workspace are included in
  * moe_workspace_size whenever max_M exceeds one launch.  Process-wide;
  * returns INVALID_ARG for min_rows < 0. */
 int moe_set_grouped(int min_rows);

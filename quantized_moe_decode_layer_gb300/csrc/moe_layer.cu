@@ -1264,6 +1264,7 @@ __device__ void build_hn(const KParams &kp, const Sh &sh, const void *x, unsigne
             if (n == 0 || base + n * NCT < total) item(base + tid + n * NCT, a[n]);
     }
     cbar();
+    if (tid == 0 && xtag) stamp(kp, (int)(xtag - sh.epoch), 19);
     if (tid < M) {
         float t = 0.f;
 #pragma unroll 1
@@ -1271,6 +1272,7 @@ __device__ void build_hn(const KParams &kp, const Sh &sh, const void *x, unsigne
         sh.red[tid * (NCW + 1) + NCW] = rsqrtf(t / (float)H + kp.g.eps);
     }
     cbar();
+    if (tid == 0 && xtag) stamp(kp, (int)(xtag - sh.epoch), 20);
     // pass 2: scale by rinv * gamma * 2^100; group sums of hn; and (rrows
     // given) the CTA's router rows dotted with hn: per item of 8 inputs
     // s * sum q h + b * sum h (8-bit rows) or sum w h (fp32 rows), summed
@@ -1341,9 +1343,11 @@ __device__ void build_hn(const KParams &kp, const Sh &sh, const void *x, unsigne
             sh.xsum[m * G + (c >> 3)] = gs;
         }
     }
+    if (tid == 0 && xtag) stamp(kp, (int)(xtag - sh.epoch), 21);
 #pragma unroll 1
     for (int e = tid; e < kp.g.E; e += NCT) sh.emask[e] = 0u;
     cbar();
+    if (tid == 0 && xtag) stamp(kp, (int)(xtag - sh.epoch), 22);
 }
 
 // Activations (fp32 rows in global memory) of `n` staged pairs: pair p =
@@ -2219,6 +2223,7 @@ __device__ __forceinline__ void compute(const KParams &kp, const Sh &sh)
         if (t0) stamp(kp, l, 0);
         // layer l's gamma, router rows and shared units
         const bool pb_ok = wait_bar(sh, sh.pb_full, (unsigned)l & 1u, 5);
+        if (t0) stamp(kp, l, 18);
         if (cbar_or(!pb_ok)) return;
         const bool fused = router_fused(kp, sh);
         build_hn(kp, sh, xin, xtag, reinterpret_cast<const uint16_t *>(sh.pb), fused ? sh.pb + sh.cp->off_router : nullptr,

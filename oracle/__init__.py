@@ -67,6 +67,7 @@ def lib():
         _lib.oracle_set_threads.restype = None
         _lib.oracle_set_threads.argtypes = [C.c_int]
         _lib.oracle_max_threads.restype = C.c_int
+        _lib.oracle_gqa_decode.restype = C.c_int
         for name in ("oracle_pack_bits", "oracle_unpack_bits", "oracle_quantize_group",
                      "oracle_quantize_matrix", "oracle_rmsnorm", "oracle_topk",
                      "oracle_expert_ffn", "oracle_route", "oracle_qkv"):
@@ -339,6 +340,27 @@ def qkv(mats, x_bits: np.ndarray) -> np.ndarray:
     s = st.struct()
     lib().oracle_qkv(C.byref(s), _p(x_bits), C.c_int(M), _p(y))
     return y
+
+
+def gqa_decode(q_bits: np.ndarray, k_bits: np.ndarray, vt_bits: np.ndarray, pos0: int):
+    """Decode attention with grouped query heads (oracle_gqa_decode).
+    q_bits [M, Hq, D], k_bits [Hkv, T_cap, D], vt_bits [Hkv, D, T_cap]: bf16
+    patterns (uint16).  Row m is at position pos0 + m and attends to keys
+    0 .. pos0 + m.  Returns (o, oabs), fp64 [M, Hq, D]."""
+    q_bits = np.ascontiguousarray(q_bits, dtype=np.uint16)
+    k_bits = np.ascontiguousarray(k_bits, dtype=np.uint16)
+    vt_bits = np.ascontiguousarray(vt_bits, dtype=np.uint16)
+    M, Hq, D = q_bits.shape
+    Hkv, T_cap, D2 = k_bits.shape
+    if D2 != D or vt_bits.shape != (Hkv, D, T_cap):
+        raise ValueError("gqa_decode: inconsistent shapes")
+    o = np.zeros((M, Hq, D), np.float64)
+    oabs = np.zeros((M, Hq, D), np.float64)
+    rc = lib().oracle_gqa_decode(_p(q_bits), _p(k_bits), _p(vt_bits), C.c_int(T_cap), C.c_int(pos0), C.c_int(M),
+                                 C.c_int(Hq), C.c_int(Hkv), C.c_int(D), _p(o), _p(oabs))
+    if rc != 0:
+        raise ValueError("gqa_decode: rejected arguments")
+    return o, oabs
 
 
 def stack(layers, x_bits: np.ndarray, normed_last: bool = True):

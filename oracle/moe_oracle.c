@@ -30,6 +30,10 @@
  * Everything is accumulated in fp64 with no intermediate rounding except the
  * quantiser, whose integer decisions are taken in fp32 like the kernel's.
  *
+ * The second workload, decode attention with grouped query heads
+ * (oracle_gqa_decode), is the plain softmax attention written out; see its
+ * comment.
+ *
  * Parity pins: every function here is pinned by tests/test_oracle.py
  * (hand-computed dequant, a hand-packed bit stream, closed forms, library
  * routines in fp64, brute force on tiny inputs).
@@ -393,5 +397,64 @@ int oracle_layer(const oq_layer *L, const uint16_t *x, int M,
     free(hn);
     free(y);
     free(ys);
+    return 0;
+}
+
+/* ------------------------------------------------ GQA decode attention */
+/*
+ * Decode-step attention over a bf16 key/value cache with grouped query
+ * heads ([MC] "How it works": one attention kernel serves the one-row decode
+ * and the multi-row verify, reading K/V once for all 8 query heads of a
+ * key/value head and all verify rows; "Beyond this checkpoint": 16 query
+ * heads, 2 key/value heads, head dimension 256).  The verify rows sit at
+ * consecutive positions: row m is at position pos0 + m and attends to keys
+ * 0 .. pos0 + m (its own included), the plain softmax attention
+ *     o[m][h] = sum_t softmax_t(q[m][h] . k[g][t] / sqrt(D)) v[g][t],
+ * g = h / (Hq / Hkv).  Layouts: q [M][Hq][D]; k [Hkv][T_cap][D]; v stored
+ * transposed, vt [Hkv][D][T_cap] (position fastest); o and oabs [M][Hq][D],
+ * oabs the same softmax-weighted sum of |v| (a scale for tolerances).
+ * fp64 throughout; the softmax subtracts the row maximum before exp.
+ * Returns 0, or -1 when the arguments are inconsistent or memory runs out.
+ */
+int oracle_gqa_decode(const uint16_t *q, const uint16_t *k, const uint16_t *vt, int T_cap, int pos0, int M,
+                      int Hq, int Hkv, int D, double *o, double *oabs)
+{
+    if (M < 1 || Hkv < 1 || Hq % Hkv != 0 || D < 1 || pos0 < 0 || pos0 + M > T_cap) return -1;
+    const int grp = Hq / Hkv, n_all = pos0 + M;
+    const double scale = 1.0 / sqrt((double)D);
+    double *s = (double *)malloc(sizeof(double) * (size_t)n_all);
+    if (!s) return -1;
+    for (int m = 0; m < M; ++m) {
+        const int n = pos0 + m + 1;
+        for (int h = 0; h < Hq; ++h) {
+            const int g = h / grp;
+            const uint16_t *qv = q + ((size_t)m * Hq + h) * D;
+            double mx = -INFINITY;
+            for (int t = 0; t < n; ++t) {
+                const uint16_t *kv = k + ((size_t)g * T_cap + t) * D;
+                double acc = 0.0;
+                for (int d = 0; d < D; ++d) acc += oracle_bf16_to_double(qv[d]) * oracle_bf16_to_double(kv[d]);
+                s[t] = acc * scale;
+                if (s[t] > mx) mx = s[t];
+            }
+            double z = 0.0;
+            for (int t = 0; t < n; ++t) {
+                s[t] = exp(s[t] - mx);
+                z += s[t];
+            }
+            for (int d = 0; d < D; ++d) {
+                const uint16_t *vrow = vt + ((size_t)g * D + d) * T_cap;
+                double acc = 0.0, aacc = 0.0;
+                for (int t = 0; t < n; ++t) {
+                    const double v = oracle_bf16_to_double(vrow[t]);
+                    acc += s[t] * v;
+                    aacc += s[t] * fabs(v);
+                }
+                o[((size_t)m * Hq + h) * D + d] = acc / z;
+                oabs[((size_t)m * Hq + h) * D + d] = aacc / z;
+            }
+        }
+    }
+    free(s);
     return 0;
 }

@@ -192,3 +192,25 @@ def bf16_bits(t: torch.Tensor) -> torch.Tensor:
     """View a bf16 tensor as its raw 16-bit patterns (int16)."""
     assert t.dtype == torch.bfloat16
     return t.contiguous().view(torch.int16)
+
+
+# ---------------------------------------------------------- decode attention
+#
+# The attention shape of the 35B-A3B model (16 query heads, 2 key/value
+# heads, head dimension 256) and its inputs: query rows and a bf16 cache of
+# keys [Hkv, T_cap, D] and values stored transposed [Hkv, D, T_cap], all
+# N(0, 1) in bf16, positions at or past the last valid one zero.
+
+ATTN_HQ, ATTN_HKV, ATTN_D = 16, 2, 256
+
+
+def make_attn(T_cap: int, n_valid: int, M: int, seed: int, device="cpu"):
+    """(q [M, 16, 256], k [2, T_cap, 256], vt [2, 256, T_cap]) bf16 with keys and
+    values at positions 0 .. n_valid - 1 drawn and the rest zero."""
+    g = _gen(seed * 7919 + 17, device)
+    q = torch.randn((M, ATTN_HQ, ATTN_D), generator=g, device=device, dtype=torch.float32)
+    k = torch.zeros((ATTN_HKV, T_cap, ATTN_D), device=device, dtype=torch.float32)
+    vt = torch.zeros((ATTN_HKV, ATTN_D, T_cap), device=device, dtype=torch.float32)
+    k[:, :n_valid] = torch.randn((ATTN_HKV, n_valid, ATTN_D), generator=g, device=device, dtype=torch.float32)
+    vt[:, :, :n_valid] = torch.randn((ATTN_HKV, ATTN_D, n_valid), generator=g, device=device, dtype=torch.float32)
+    return q.to(torch.bfloat16), k.to(torch.bfloat16), vt.to(torch.bfloat16)

@@ -362,3 +362,66 @@ def test_qkv_matches_dense_product(bits):
         off += m.rows
     # a transposed operand or a dropped bias would not match
     assert not np.allclose(y, x @ (dense - dense.mean()).T, rtol=1e-6, atol=1e-6)
+
+
+# ------------------------------------------------------ decode attention
+
+def _attn_bits(t):
+    return synth.bf16_bits(t).numpy().view(np.uint16)
+
+
+def test_gqa_single_key_returns_its_value():
+    """One key (position 0, one row): its softmax weight is 1, so every
+    query head of key/value head g returns v[g][:, 0]."""
+    q, k, vt = synth.make_attn(8, 1, 1, 3)
+    o, oabs = oracle.gqa_decode(_attn_bits(q), _attn_bits(k), _attn_bits(vt), 0)
+    v0 = vt[:, :, 0].double().numpy()
+    for h in range(16):
+        assert np.array_equal(o[0, h], v0[h // 8])
+        assert np.array_equal(oabs[0, h], np.abs(v0[h // 8]))
+
+
+def test_gqa_equal_keys_give_the_mean_of_the_values():
+    """All keys equal: every score of a row is the same, so the output is the
+    plain mean of the values the row sees (rows at positions 5, 6, 7)."""
+    T = 16
+    q, k, vt = synth.make_attn(T, 8, 3, 4)
+    k = k[:, :1].expand(2, T, 256).contiguous()
+    o, _ = oracle.gqa_decode(_attn_bits(q), _attn_bits(k), _attn_bits(vt), 5)
+    V = vt.double().numpy()
+    for m in range(3):
+        n = 5 + m + 1
+        for h in range(16):
+            np.testing.assert_allclose(o[m, h], V[h // 8, :, :n].mean(axis=1), rtol=1e-12, atol=1e-13)
+
+
+def test_gqa_matches_torch_sdpa():
+    """Against torch's scaled_dot_product_attention in fp64 with the key/value
+    heads repeated per query group and an explicit causal mask."""
+    T, n_valid, M = 96, 77, 4
+    pos0 = n_valid - M
+    q, k, vt = synth.make_attn(T, n_valid, M, 5)
+    o, oabs = oracle.gqa_decode(_attn_bits(q), _attn_bits(k), _attn_bits(vt), pos0)
+    Q = q.double().permute(1, 0, 2)                                   # [Hq, M, D]
+    K = k.double()[:, :n_valid].repeat_interleave(8, dim=0)          # [Hq, n, D]
+    V = vt.double()[:, :, :n_valid].transpose(1, 2).repeat_interleave(8, dim=0)
+    pos = torch.arange(n_valid)[None, :]
+    allowed = pos <= (pos0 + torch.arange(M))[:, None]                # [M, n]
+    ref = torch.nn.functional.scaled_dot_product_attention(Q, K, V, attn_mask=allowed)
+    np.testing.assert_allclose(o, ref.permute(1, 0, 2).numpy(), rtol=1e-10, atol=1e-12)
+    assert np.all(oabs >= np.abs(o) - 1e-12)
+
+
+def test_gqa_rows_equal_one_row_calls():
+    """Row m of an M-row call is the one-row call at position pos0 + m."""
+    q, k, vt = synth.make_attn(64, 50, 3, 6)
+    o, _ = oracle.gqa_decode(_attn_bits(q), _attn_bits(k), _attn_bits(vt), 47)
+    for m in range(3):
+        o1, _ = oracle.gqa_decode(_attn_bits(q[m:m + 1]), _attn_bits(k), _attn_bits(vt), 47 + m)
+        assert np.array_equal(o1[0], o[m])
+
+
+def test_gqa_rejects_rows_past_the_cache():
+    q, k, vt = synth.make_attn(16, 16, 2, 7)
+    with pytest.raises(ValueError):
+        oracle.gqa_decode(_attn_bits(q), _attn_bits(k), _attn_bits(vt), 15)

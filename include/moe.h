@@ -382,6 +382,55 @@ int moe_qkv_forward(const moe_qkv *qkv, const uint16_t *x_dev, int M, float *y_d
 /* Frees the handle (not the packed rows).  NULL is a no-op. */
 void moe_qkv_destroy(moe_qkv *qkv);
 
+/* ------------------------------------------------------------------------
+ * Decode attention with grouped query heads, split over the keys
+ * (PureDrive-35B-A3B-MLX model card, "How it works": one attention kernel
+ * for the one-row decode and the multi-row verify, reading K/V once for all
+ * query heads of a group and all verify rows, split flash-decoding style
+ * with split points and summation order that depend only on the row's
+ * position; "Beyond this checkpoint": 16 query heads, 2 KV heads, head
+ * dimension 256).  The shape is fixed at those sizes.
+ *
+ * Cache layout (caller-owned device memory, bf16):
+ *   k_cache  [2][T_cap][256]  key of position t of key/value head g at
+ *            (g * T_cap + t) * 256;
+ *   vt_cache [2][256][T_cap]  values stored transposed: value d of position t
+ *            of head g at (g * 256 + d) * T_cap + t.
+ * T_cap must be a multiple of 8 and both base addresses 16-byte aligned.
+ * Positions past the last valid one are never used.
+ *
+ * moe_attn_workspace_size: device scratch a call with this T_cap needs
+ * (the per-chunk partial results).  Errors: INVALID_ARG. */
+#define MOE_ATTN_Q_HEADS 16
+#define MOE_ATTN_KV_HEADS 2
+#define MOE_ATTN_HEAD_DIM 256
+#define MOE_ATTN_MAX_ROWS 8
+int moe_attn_workspace_size(int T_cap, size_t *bytes);
+
+/* Attention of M token rows (1 <= M <= 8) at positions pos0 .. pos0 + M - 1
+ * against the cache, whose positions 0 .. pos0 + M - 1 hold valid keys and
+ * values (the rows' own included, see moe_attn_append): row m attends to
+ * positions 0 .. pos0 + m,
+ *   o[m][h] = sum_t softmax_t(q[m][h] . k[g][t] / 16) v[g][t], g = h / 8.
+ * q_dev bf16 [M][16][256]; o_dev fp32 [M][16][256].  The keys are split into
+ * chunks of 512 positions, one CTA per (chunk, KV head) on the tensor cores
+ * (scores and weighted values in fp32, the softmax weights as two bf16
+ * halves), then a merge of each row's chunks in order: row m's result is
+ * bitwise the same for any M.  err_dev (int, device) is set to 1 if a device
+ * wait runs out of time; the caller clears it.  Two launches, asynchronous
+ * on `stream`.  Errors: INVALID_ARG (null or misaligned pointers, M or pos0
+ * out of range, T_cap not a multiple of 8), BUFFER_TOO_SMALL, UNSUPPORTED
+ * (no tensor-map encoder in the driver), CUDA. */
+int moe_attn_decode(const uint16_t *q_dev, const uint16_t *k_cache_dev, const uint16_t *vt_cache_dev, int T_cap,
+                    int pos0, int M, float *o_dev, void *ws_dev, size_t ws_bytes, int *err_dev,
+                    moe_stream_t stream);
+
+/* Writes the keys and values of M new rows (bf16 [M][2][256] each) into the
+ * cache at positions pos0 .. pos0 + M - 1 (values transposed).  One launch.
+ * Errors: INVALID_ARG, CUDA. */
+int moe_attn_append(const uint16_t *k_new_dev, const uint16_t *v_new_dev, int M, int pos0, uint16_t *k_cache_dev,
+                    uint16_t *vt_cache_dev, int T_cap, moe_stream_t stream);
+
 /* Human-readable name of a status code (static string). */
 const char *moe_status_str(int status);
 

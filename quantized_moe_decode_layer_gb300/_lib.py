@@ -25,6 +25,7 @@ SYMBOLS = ["moe_pack_size", "moe_pack_weights", "moe_layer_destroy", "moe_export
            "moe_stack_create", "moe_stack_forward", "moe_stack_forward_host", "moe_stack_destroy",
            "moe_decode_layer_noalloc", "moe_noalloc_status",
            "moe_qkv_pack_size", "moe_qkv_pack", "moe_qkv_forward", "moe_qkv_destroy",
+           "moe_attn_workspace_size", "moe_attn_decode", "moe_attn_append",
            "moe_stream_status", "moe_build_flags", "moe_debug_inject", "moe_debug_set", "moe_debug_trace", "moe_set_grouped", "moe_gate_up_tc", "moe_down_tc", "moe_status_str",
            "moe_last_cuda_error",
            "moe_selftest_host", "moe_launch_count"]
@@ -89,6 +90,9 @@ def lib():
             "moe_qkv_pack": (i, [C.POINTER(QkvDesc), C.POINTER(SrcMatrix), C.POINTER(SrcMatrix), C.POINTER(SrcMatrix),
                                  vp, sz, C.POINTER(vp), vp]),
             "moe_qkv_forward": (i, [vp, vp, i, vp, vp, vp]),
+            "moe_attn_workspace_size": (i, [i, C.POINTER(sz)]),
+            "moe_attn_decode": (i, [vp, vp, vp, i, i, i, vp, vp, sz, vp, vp]),
+            "moe_attn_append": (i, [vp, vp, i, i, vp, vp, i, vp]),
             "moe_qkv_destroy": (None, [vp]),
             "moe_stream_status": (i, [vp, sz, vp]),
             "moe_debug_set": (i, [i, C.c_longlong]),

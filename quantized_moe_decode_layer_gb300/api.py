@@ -373,6 +373,48 @@ class QKV:
             pass
 
 
+class AttnCache:
+    """A bf16 key/value cache of the decode attention (moe_attn_*): keys
+    [2, T_cap, 256] and values stored transposed [2, 256, T_cap], zeroed, with
+    the scratch the attention call needs."""
+
+    HQ, HKV, D = 16, 2, 256
+
+    def __init__(self, T_cap: int, device="cuda"):
+        if T_cap < 8 or T_cap % 8:
+            raise ValueError("T_cap must be a positive multiple of 8")
+        self.T_cap = T_cap
+        self.k = torch.zeros((self.HKV, T_cap, self.D), dtype=torch.bfloat16, device=device)
+        self.vt = torch.zeros((self.HKV, self.D, T_cap), dtype=torch.bfloat16, device=device)
+        n = C.c_size_t()
+        check("moe_attn_workspace_size", lib().moe_attn_workspace_size(T_cap, C.byref(n)))
+        self.ws = torch.empty(n.value, dtype=torch.uint8, device=device)
+
+    def append(self, k_new: torch.Tensor, v_new: torch.Tensor, pos0: int, stream=None) -> None:
+        """Keys and values of M new rows (bf16 [M, 2, 256]) at positions pos0 .. pos0 + M - 1."""
+        _need(k_new, "k_new", torch.bfloat16, (None, self.HKV, self.D))
+        M = k_new.shape[0]
+        _need(v_new, "v_new", torch.bfloat16, (M, self.HKV, self.D))
+        check("moe_attn_append", lib().moe_attn_append(_ptr(_bits16(k_new)), _ptr(_bits16(v_new)), M, pos0,
+                                                       _ptr(self.k), _ptr(self.vt), self.T_cap, _stream(stream)))
+
+    def attend(self, q: torch.Tensor, pos0: int, out=None, err=None, stream=None):
+        """o fp32 [M, 16, 256] of query rows q bf16 [M, 16, 256] at positions
+        pos0 .. pos0 + M - 1 (moe_attn_decode); returns (o, err)."""
+        _need(q, "q", torch.bfloat16, (None, self.HQ, self.D))
+        M = q.shape[0]
+        if out is None:
+            out = torch.empty((M, self.HQ, self.D), dtype=torch.float32, device=q.device)
+        _need(out, "out", torch.float32, (M, self.HQ, self.D))
+        if err is None:
+            err = torch.zeros(1, dtype=torch.int32, device=q.device)
+        _need(err, "err", torch.int32, (1,))
+        check("moe_attn_decode", lib().moe_attn_decode(_ptr(_bits16(q)), _ptr(self.k), _ptr(self.vt), self.T_cap,
+                                                       pos0, M, _ptr(out), _ptr(self.ws), self.ws.numel(),
+                                                       _ptr(err), _stream(stream)))
+        return out, err
+
+
 def debug_set(skip_row: int = -1, timeout_ns: int = 0) -> None:
     check("moe_debug_set", lib().moe_debug_set(skip_row, timeout_ns))
 

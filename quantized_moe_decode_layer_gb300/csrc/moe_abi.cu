@@ -725,6 +725,36 @@ int moe_qkv_forward(const moe_qkv *qkv, const uint16_t *x_dev, int M, float *y_d
 
 void moe_qkv_destroy(moe_qkv *qkv) { free(qkv); }
 
+int moe_attn_workspace_size(int T_cap, size_t *bytes)
+{
+    if (!bytes || T_cap < 1) return MOE_ERR_INVALID_ARG;
+    *bytes = attn_workspace_bytes(T_cap);
+    return MOE_OK;
+}
+
+int moe_attn_decode(const uint16_t *q_dev, const uint16_t *k_cache_dev, const uint16_t *vt_cache_dev, int T_cap,
+                    int pos0, int M, float *o_dev, void *ws_dev, size_t ws_bytes, int *err_dev, moe_stream_t stream)
+{
+    if (!q_dev || !k_cache_dev || !vt_cache_dev || !o_dev || !ws_dev || !err_dev) return MOE_ERR_INVALID_ARG;
+    if (M < 1 || M > MOE_ATTN_MAX_ROWS || pos0 < 0 || T_cap < 8 || T_cap % 8 != 0 || pos0 + M > T_cap)
+        return MOE_ERR_INVALID_ARG;
+    if ((reinterpret_cast<uintptr_t>(k_cache_dev) | reinterpret_cast<uintptr_t>(vt_cache_dev) |
+         reinterpret_cast<uintptr_t>(q_dev) | reinterpret_cast<uintptr_t>(ws_dev)) & 15u)
+        return MOE_ERR_INVALID_ARG;
+    if (ws_bytes < attn_workspace_bytes(T_cap)) return MOE_ERR_BUFFER_TOO_SMALL;
+    return launch_attn(q_dev, k_cache_dev, vt_cache_dev, T_cap, pos0, M, o_dev, ws_dev, err_dev, g_timeout_ns,
+                       reinterpret_cast<cudaStream_t>(stream));
+}
+
+int moe_attn_append(const uint16_t *k_new_dev, const uint16_t *v_new_dev, int M, int pos0, uint16_t *k_cache_dev,
+                    uint16_t *vt_cache_dev, int T_cap, moe_stream_t stream)
+{
+    if (!k_new_dev || !v_new_dev || !k_cache_dev || !vt_cache_dev) return MOE_ERR_INVALID_ARG;
+    if (M < 1 || M > MOE_ATTN_MAX_ROWS || pos0 < 0 || T_cap < 1 || pos0 + M > T_cap) return MOE_ERR_INVALID_ARG;
+    return launch_attn_append(k_new_dev, v_new_dev, M, pos0, k_cache_dev, vt_cache_dev, T_cap,
+                              reinterpret_cast<cudaStream_t>(stream));
+}
+
 const char *moe_status_str(int status)
 {
     switch (status) {

@@ -1,0 +1,659 @@
+// Decode attention with grouped query heads, split over the key axis, on the
+// 5th-generation tensor cores (tcgen05, accumulators in tensor memory), for
+// the attention shape of the 35B-A3B model: 16 query heads sharing 2
+// key/value heads (8 per group), head dimension 256, bf16 key/value cache
+// (PureDrive-35B-A3B-MLX model card, "How it works": one attention kernel for
+// the one-row decode and the multi-row verify that reads K/V once for all
+// query heads of a group and all verify rows, split over the keys
+// flash-decoding style, with split points and summation order that depend
+// only on the row's position; "Beyond this checkpoint": 16 query heads,
+// 2 KV heads, head dim 256).
+//
+// What it computes: token row m (m < M) is at position pos0 + m and attends
+// to keys 0 .. pos0 + m:
+//     o[m][h] = sum_t softmax_t(q[m][h] . k[g][t] / 16) v[g][t],  g = h / 8.
+//
+// Split: the keys are cut into chunks of 512 positions (chunk j = keys
+// 512 j .. 512 j + 511), the same for every row and every call; one CTA per
+// (chunk, key/value head) computes, for every query column q = 8 m + head in
+// group, the chunk's running maximum, the sum of exp(s - max) and the
+// unnormalised sum of exp(s - max) v.  A second kernel merges a row's chunks
+// in chunk order.  A row's result therefore depends only on its own position,
+// query and the cache, never on M or on the other rows.
+//
+// Per CTA, over the chunk's tiles of 128 keys (warp-specialised):
+//   - a TMA warp loads 16 KB boxes (128 rows x 64 bf16, 128-byte swizzle)
+//     into a ring: the tile's keys [128 keys x 256] in 4 boxes, then its
+//     values from the transposed cache [256 d x 128 keys] in 4 boxes;
+//   - an MMA warp issues S^T = K Q^T (M = 128 keys, N = the query columns,
+//     K = 256 over d; Q in shared memory, written once) into one of two
+//     tensor-memory score blocks, and O^T += V^T P^T (M = 128 values of d per
+//     half, K = 128 keys) into one of two output blocks, with P in two bf16
+//     halves (p = hi + lo, each an MMA into the same sum) so the weights keep
+//     ~16 significant bits;
+//   - eight softmax warps read the score block (thread = key, a half of the
+//     query columns each), mask keys past each row's position, take the
+//     tile's column maxima (redux.sync on order-preserving keys) and the new
+//     running maxima, write exp(s - max) as bf16 halves into shared memory
+//     for the MMA, and add the column sums; then they take the previous
+//     tile's output block into fp32 registers (thread = one d of one half),
+//     rescaled by exp(old max - new max) (online softmax).
+// Every wait is bounded; one that runs out sets *err, the roles stop, the
+// CTA waits (bounded) for its copies and MMAs and frees its tensor memory.
+#include <cuda.h>
+#include <cudaTypedefs.h>
+#include <cuda_bf16.h>
+#include <stdint.h>
+
+#include <cstring>
+#include <mutex>
+
+#include "moe_internal.h"
+
+namespace moe {
+namespace {
+
+constexpr int kAD = 256, kAHq = 16, kAHkv = 2, kAGrp = kAHq / kAHkv;
+constexpr int kAKeys = 128;                 // keys per tile (MMA M of the score product)
+constexpr int kATiles = 4;                  // tiles per chunk
+constexpr int kAChunk = kAKeys * kATiles;   // keys per chunk: the split points are multiples of this
+constexpr int kAMaxRows = 8;
+constexpr int kAMaxQ = kAGrp * kAMaxRows;   // query columns per key/value head
+constexpr int kABox = 16384;                // one TMA box: 128 rows of 128 bytes
+constexpr int kASoftWarps = 8;
+constexpr int kASoftThreads = kASoftWarps * 32;
+constexpr int kAThreads = kASoftThreads + 64;   // + TMA warp + MMA warp
+constexpr uint32_t kATmemCols = 512;
+// tensor-memory columns: score blocks at 0 and 64, output blocks (two
+// halves of d, 64 columns each) at 128 and 256
+__host__ __device__ constexpr uint32_t s_col(int b) { return 64u * (uint32_t)b; }
+__host__ __device__ constexpr uint32_t o_col(int b, int half) { return 128u + 128u * (uint32_t)b + 64u * (uint32_t)half; }
+
+struct AttnParams {
+    CUtensorMap tk;   // keys: dims {256, n_valid, 2}, box {64, 128, 1}
+    CUtensorMap tv;   // values, transposed: dims {n_valid, 256, 2}, box {64, 128, 1}
+    const uint16_t *q;    // [M][16][256]
+    float *part_o;        // [chunk][2][64][256]
+    float *part_ml;       // [chunk][2][64][2]: running maximum, sum
+    int M, pos0, n_valid, nq, nsub;
+    long long timeout_ns;
+    int *err;
+};
+
+// Shared-memory layout (offsets from a 1024-byte aligned base).
+struct ALayout {
+    int ring, q, p, red, bars, total;
+};
+__host__ __device__ inline ALayout attn_layout(int nq, int nsub)
+{
+    ALayout L;
+    L.ring = 0;
+    L.q = nsub * kABox;                       // Q: nq rows x 256, no swizzle, 4096 B per 8 rows
+    L.p = L.q + nq * kAD * 2;                 // P: [2 buffers][hi, lo] nq rows x 128 keys
+    L.red = L.p + 4 * nq * kAKeys * 2;        // reductions and running state
+    L.bars = L.red + 4 * kAMaxQ * 4 * 2 + 4 * kAMaxQ * 4;
+    L.total = L.bars + (2 * nsub + 11) * 8 + 16;
+    return L;
+}
+
+__device__ __forceinline__ uint32_t su32(const void *p) { return (uint32_t)__cvta_generic_to_shared(p); }
+
+__device__ __forceinline__ unsigned long long gtime()
+{
+    unsigned long long t;
+    asm volatile("mov.u64 %0, %%globaltimer;" : "=l"(t));
+    return t;
+}
+
+__device__ __forceinline__ void bar_init(uint32_t b, unsigned n)
+{
+    asm volatile("mbarrier.init.shared::cta.b64 [%0], %1;" ::"r"(b), "r"(n) : "memory");
+}
+__device__ __forceinline__ void bar_arrive(uint32_t b)
+{
+    asm volatile("{ .reg .b64 st; mbarrier.arrive.shared::cta.b64 st, [%0]; }" ::"r"(b) : "memory");
+}
+__device__ __forceinline__ void bar_expect(uint32_t b, unsigned bytes)
+{
+    asm volatile("{ .reg .b64 st; mbarrier.arrive.expect_tx.shared::cta.b64 st, [%0], %1; }" ::"r"(b), "r"(bytes)
+                 : "memory");
+}
+__device__ __forceinline__ bool bar_test(uint32_t b, unsigned parity)
+{
+    uint32_t done;
+    asm volatile("{ .reg .pred p; mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2; selp.u32 %0, 1, 0, p; }"
+                 : "=r"(done)
+                 : "r"(b), "r"(parity)
+                 : "memory");
+    return done != 0;
+}
+
+// Bounded wait on an mbarrier phase; gives up when the CTA's abort flag is
+// set, or sets it (and the error word) when the time runs out.
+__device__ __forceinline__ bool bar_wait(uint32_t b, unsigned parity, volatile int *abort, const AttnParams &p)
+{
+    if (bar_test(b, parity)) return true;
+    const unsigned long long t0 = gtime();
+#pragma unroll 1
+    for (;;) {
+        if (bar_test(b, parity)) return true;
+        if (*abort) return false;
+        if ((long long)(gtime() - t0) > p.timeout_ns) {
+            *abort = 1;
+            atomicOr(p.err, 1);
+            return false;
+        }
+    }
+}
+
+// Named barrier of the softmax warps with an AND over their flags.
+__device__ __forceinline__ bool soft_sync_and(bool ok)
+{
+    uint32_t r;
+    asm volatile("{ .reg .pred p, q; setp.ne.u32 p, %1, 0; barrier.red.and.pred q, 1, %2, p; selp.u32 %0, 1, 0, q; }"
+                 : "=r"(r)
+                 : "r"((uint32_t)ok), "r"(kASoftThreads)
+                 : "memory");
+    return r != 0;
+}
+__device__ __forceinline__ void soft_sync() { asm volatile("bar.sync 1, %0;" ::"r"(kASoftThreads) : "memory"); }
+
+// Matrix descriptors (tcgen05 shared-memory descriptor, version 1).
+// 128-byte swizzled K-major box (rows of 64 bf16, 8-row groups 1024 B apart):
+// the K step of 16 elements advances the start address by 32 bytes.
+__device__ __forceinline__ uint64_t desc_sw128(uint32_t addr)
+{
+    return (uint64_t)((addr & 0x3FFFFu) >> 4) | (1ull << 16) | ((uint64_t)(1024u >> 4) << 32) | (1ull << 46) |
+           (2ull << 61);
+}
+// No-swizzle K-major: 8 x 16-byte core matrices, 128 B apart along K, `sbo`
+// bytes apart between 8-row groups.
+__device__ __forceinline__ uint64_t desc_plain(uint32_t addr, uint32_t sbo)
+{
+    return (uint64_t)((addr & 0x3FFFFu) >> 4) | ((uint64_t)(128u >> 4) << 16) | ((uint64_t)(sbo >> 4) << 32) |
+           (1ull << 46);
+}
+// Instruction descriptor of kind::f16: fp32 accumulator, bf16 A and B, both
+// K-major, M = 128, N = nq.
+__device__ __forceinline__ uint32_t idesc_bf16(int nq)
+{
+    return (1u << 4) | (1u << 7) | (1u << 10) | ((uint32_t)(nq >> 3) << 17) | ((uint32_t)(128 >> 4) << 24);
+}
+__device__ __forceinline__ void umma(uint32_t d, uint64_t a, uint64_t b, uint32_t idesc, uint32_t acc)
+{
+    asm volatile("{ .reg .pred p; setp.ne.b32 p, %4, 0; tcgen05.mma.cta_group::1.kind::f16 [%0], %1, %2, %3, p; }" ::"r"(d),
+                 "l"(a), "l"(b), "r"(idesc), "r"(acc)
+                 : "memory");
+}
+__device__ __forceinline__ void umma_commit(uint32_t bar)
+{
+    asm volatile("tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];" ::"r"(bar) : "memory");
+}
+
+__device__ __forceinline__ void tmem_ld8(uint32_t a, float (&v)[8])
+{
+    uint32_t r[8];
+    asm volatile("tcgen05.ld.sync.aligned.32x32b.x8.b32 {%0, %1, %2, %3, %4, %5, %6, %7}, [%8];"
+                 : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]), "=r"(r[6]), "=r"(r[7])
+                 : "r"(a)
+                 : "memory");
+#pragma unroll
+    for (int i = 0; i < 8; ++i) v[i] = __uint_as_float(r[i]);
+}
+__device__ __forceinline__ void tmem_wait_ld() { asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory"); }
+
+__device__ __forceinline__ void tma_load3(uint32_t dst, const CUtensorMap *map, int c0, int c1, int c2, uint32_t bar)
+{
+    asm volatile(
+        "cp.async.bulk.tensor.3d.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1, {%2, %3, %4}], [%5];" ::"r"(
+            dst),
+        "l"(reinterpret_cast<uint64_t>(map)), "r"(c0), "r"(c1), "r"(c2), "r"(bar)
+        : "memory");
+}
+
+// Order-preserving map of a float to an unsigned key and back.
+__device__ __forceinline__ uint32_t fkey(float v)
+{
+    const uint32_t u = __float_as_uint(v);
+    return (u & 0x80000000u) ? ~u : (u | 0x80000000u);
+}
+__device__ __forceinline__ float unkey(uint32_t k) { return __uint_as_float((k & 0x80000000u) ? (k & 0x7FFFFFFFu) : ~k); }
+
+// Element (r, k) of a no-swizzle K-major tile with 8-row groups `sbo` apart.
+__device__ __forceinline__ uint32_t plain_off(int r, int k, uint32_t sbo)
+{
+    return (uint32_t)(r >> 3) * sbo + (uint32_t)(k >> 3) * 128u + (uint32_t)(r & 7) * 16u + (uint32_t)(k & 7) * 2u;
+}
+
+// The boxes of a chunk in ring order: tile 0's keys, then for each tile t
+// the keys of tile t + 1 (if any) and the values of tile t.  f(is_value,
+// tile, part): part = d chunk of 64 for keys, 2 * half + key half for values.
+template <typename F>
+__device__ __forceinline__ void for_boxes(int nt, F &&f)
+{
+#pragma unroll 1
+    for (int part = 0; part < 4; ++part) f(false, 0, part);
+#pragma unroll 1
+    for (int t = 0; t < nt; ++t) {
+        if (t + 1 < nt)
+#pragma unroll 1
+            for (int part = 0; part < 4; ++part) f(false, t + 1, part);
+#pragma unroll 1
+        for (int part = 0; part < 4; ++part) f(true, t, part);
+    }
+}
+
+__global__ void __launch_bounds__(kAThreads, 1) attn_chunk_kernel(const __grid_constant__ AttnParams p)
+{
+    extern __shared__ __align__(1024) uint8_t smem_raw[];
+    uint8_t *sm = reinterpret_cast<uint8_t *>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+    const int nq = p.nq, nsub = p.nsub, M = p.M;
+    const ALayout L = attn_layout(nq, nsub);
+    const int chunk = blockIdx.x, g = blockIdx.y;
+    const int k0 = chunk * kAChunk;
+    const int nkeys = min(kAChunk, p.n_valid - k0);
+    const int nt = (nkeys + kAKeys - 1) / kAKeys;
+    const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+
+    uint8_t *ring = sm + L.ring, *qs = sm + L.q, *ps = sm + L.p;
+    uint32_t *red_max = reinterpret_cast<uint32_t *>(sm + L.red);        // [4][64]
+    float *red_sum = reinterpret_cast<float *>(red_max + 4 * kAMaxQ);    // [4][64]
+    float *m_run = red_sum + 4 * kAMaxQ, *l_run = m_run + kAMaxQ;        // [64] each
+    float *alpha = l_run + kAMaxQ;                                       // [2][64]
+    uint64_t *bars = reinterpret_cast<uint64_t *>(sm + L.bars);
+    uint64_t *full = bars, *empty = bars + nsub;
+    uint64_t *s_full = bars + 2 * nsub, *s_free = s_full + 2, *p_full = s_free + 2, *o_full = p_full + 2,
+             *o_free = o_full + 2, *mma_done = o_free + 2;
+    uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(bars + 2 * nsub + 11);
+    volatile int *abort_flag = reinterpret_cast<volatile int *>(tmem_slot + 1);
+
+    if (tid == 0) {
+        for (int s = 0; s < nsub; ++s) {
+            bar_init(su32(&full[s]), 1);
+            bar_init(su32(&empty[s]), 1);
+        }
+        for (int b = 0; b < 2; ++b) {
+            bar_init(su32(&s_full[b]), 1);
+            bar_init(su32(&s_free[b]), kASoftWarps);
+            bar_init(su32(&p_full[b]), 1);
+            bar_init(su32(&o_full[b]), 1);
+            bar_init(su32(&o_free[b]), kASoftWarps);
+        }
+        bar_init(su32(mma_done), 1);
+        *abort_flag = 0;
+        asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+    }
+    if (warp == 0) {
+        asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(su32(tmem_slot)),
+                     "r"(kATmemCols)
+                     : "memory");
+        asm volatile("tcgen05.relinquish_alloc_permit.cta_group::1.sync.aligned;" ::: "memory");
+    }
+    // Q of this key/value head as the score product's B operand: row
+    // q = 8 m + head in group, zero past the last row
+    for (int i = tid; i < nq * (kAD / 8); i += kAThreads) {
+        const int qr = i / (kAD / 8), dc = i % (kAD / 8);
+        const int m = qr / kAGrp, hh = qr % kAGrp;
+        uint4 v = make_uint4(0u, 0u, 0u, 0u);
+        if (m < M) v = __ldg(reinterpret_cast<const uint4 *>(p.q + ((size_t)m * kAHq + g * kAGrp + hh) * kAD) + dc);
+        *reinterpret_cast<uint4 *>(qs + plain_off(qr, 8 * dc, 4096u)) = v;
+    }
+    for (int i = tid; i < kAMaxQ; i += kAThreads) {
+        m_run[i] = -INFINITY;
+        l_run[i] = 0.f;
+    }
+    asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+    asm volatile("tcgen05.fence::before_thread_sync;" ::: "memory");
+    __syncthreads();
+    asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory");
+    const uint32_t taddr = *tmem_slot;
+
+    if (warp == kASoftWarps) {
+        // ---------------------------------------------------------- TMA warp
+        if (lane == 0) {
+            int slot = 0, issued = 0;
+            unsigned ph = 0;
+            bool go = true;
+            for_boxes(nt, [&](bool is_v, int t, int part) {
+                if (!go) return;
+                if (issued >= nsub && !bar_wait(su32(&empty[slot]), ph ^ 1u, abort_flag, p)) {
+                    go = false;
+                    return;
+                }
+                const uint32_t dst = su32(ring + (size_t)slot * kABox), fb = su32(&full[slot]);
+                bar_expect(fb, kABox);
+                const int kb = k0 + kAKeys * t;
+                if (!is_v) tma_load3(dst, &p.tk, 64 * part, kb, g, fb);
+                else tma_load3(dst, &p.tv, kb + 64 * (part & 1), 128 * (part >> 1), g, fb);
+                ++issued;
+                if (++slot == nsub) { slot = 0; ph ^= 1u; }
+            });
+            // every box issued must have landed before the CTA can exit
+            const int last = issued;
+            for (int i = 0; i < nsub && i < last; ++i) {
+                const int q = last - 1 - i;                    // the i-th most recent box
+                const int s = q % nsub;
+                const unsigned par = (unsigned)(q / nsub) & 1u;
+                const unsigned long long t0 = gtime();
+                while (!bar_test(su32(&full[s]), par) && (long long)(gtime() - t0) <= p.timeout_ns) {}
+            }
+        }
+    } else if (warp == kASoftWarps + 1) {
+        // ---------------------------------------------------------- MMA warp
+        if (lane == 0) {
+            const uint32_t idesc = idesc_bf16(nq);
+            int slot = 0;
+            unsigned ph = 0;
+            bool go = true;
+            auto take = [&]() -> bool {
+                if (!go || !bar_wait(su32(&full[slot]), ph, abort_flag, p)) return go = false;
+                asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory");
+                return true;
+            };
+            auto release = [&]() {
+                umma_commit(su32(&empty[slot]));
+                if (++slot == nsub) { slot = 0; ph ^= 1u; }
+            };
+            auto scores = [&](int t) {
+                const int b = t & 1;
+                if (t >= 2 && !bar_wait(su32(&s_free[b]), (unsigned)((t - 2) >> 1) & 1u, abort_flag, p)) go = false;
+                asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory");
+                for (int part = 0; part < 4 && go; ++part) {
+                    if (!take()) break;
+                    const uint32_t a0 = su32(ring + (size_t)slot * kABox);
+#pragma unroll
+                    for (int k = 0; k < 4; ++k)
+                        umma(taddr + s_col(b), desc_sw128(a0 + 32u * k), desc_plain(su32(qs) + 256u * (4 * part + k), 4096u),
+                             idesc, (part | k) != 0 ? 1u : 0u);
+                    release();
+                }
+                if (go) umma_commit(su32(&s_full[b]));
+            };
+            auto values = [&](int t) {
+                const int b = t & 1;
+                if (!bar_wait(su32(&p_full[b]), (unsigned)(t >> 1) & 1u, abort_flag, p)) go = false;
+                if (go && t >= 2 && !bar_wait(su32(&o_free[b]), (unsigned)((t - 2) >> 1) & 1u, abort_flag, p)) go = false;
+                asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory");
+                const uint32_t phi = su32(ps) + (uint32_t)(2 * b) * (uint32_t)(nq * kAKeys * 2);
+                const uint32_t plo = phi + (uint32_t)(nq * kAKeys * 2);
+                for (int part = 0; part < 4 && go; ++part) {
+                    if (!take()) break;
+                    const int half = part >> 1, kh = part & 1;
+                    const uint32_t a0 = su32(ring + (size_t)slot * kABox);
+#pragma unroll
+                    for (int k = 0; k < 4; ++k) {
+                        const uint32_t koff = 256u * (4 * kh + k);
+                        umma(taddr + o_col(b, half), desc_sw128(a0 + 32u * k), desc_plain(phi + koff, 2048u), idesc,
+                             (kh | k) != 0 ? 1u : 0u);
+                        umma(taddr + o_col(b, half), desc_sw128(a0 + 32u * k), desc_plain(plo + koff, 2048u), idesc, 1u);
+                    }
+                    release();
+                }
+                if (go) umma_commit(su32(&o_full[b]));
+            };
+            scores(0);
+            for (int t = 0; t < nt && go; ++t) {
+                if (t + 1 < nt) scores(t + 1);
+                if (go) values(t);
+            }
+            // every MMA issued has finished before the tensor memory is freed
+            umma_commit(su32(mma_done));
+            const unsigned long long t0 = gtime();
+            while (!bar_test(su32(mma_done), 0u) && (long long)(gtime() - t0) <= p.timeout_ns) {}
+        }
+    } else {
+        // ------------------------------------------------------ softmax warps
+        const int qt = warp & 3, ch = warp >> 2;
+        const int ncol = nq >> 1;                 // query columns of this thread (multiple of 8)
+        const int key_local = 32 * qt + lane;
+        const int dl = 128 * ch + 32 * qt + lane;  // the d this thread accumulates
+        float oacc[kAMaxQ];
+#pragma unroll
+        for (int i = 0; i < kAMaxQ; ++i) oacc[i] = 0.f;
+        bool ok = true;
+        auto drain = [&](int t) {
+            const int b = t & 1;
+            ok = __all_sync(0xFFFFFFFFu, bar_wait(su32(&o_full[b]), (unsigned)(t >> 1) & 1u, abort_flag, p));
+            asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory");
+            if (!ok) return;
+            const uint32_t base = taddr + ((uint32_t)(32 * qt) << 16) + o_col(b, ch);
+#pragma unroll
+            for (int c8 = 0; c8 < kAMaxQ / 8; ++c8) {
+                if (8 * c8 < nq) {
+                    float v[8];
+                    tmem_ld8(base + 8u * c8, v);
+                    tmem_wait_ld();
+#pragma unroll
+                    for (int i = 0; i < 8; ++i) oacc[8 * c8 + i] = fmaf(oacc[8 * c8 + i], alpha[b * kAMaxQ + 8 * c8 + i], v[i]);
+                }
+            }
+            asm volatile("tcgen05.fence::before_thread_sync;" ::: "memory");
+            __syncwarp();
+            if (lane == 0) bar_arrive(su32(&o_free[b]));
+        };
+#pragma unroll 1
+        for (int t = 0; t < nt; ++t) {
+            const int b = t & 1;
+            const int key = k0 + kAKeys * t + key_local;
+            ok = __all_sync(0xFFFFFFFFu, bar_wait(su32(&s_full[b]), (unsigned)(t >> 1) & 1u, abort_flag, p));
+            asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory");
+            float s[kAMaxQ / 2];
+            if (ok) {
+                const uint32_t base = taddr + ((uint32_t)(32 * qt) << 16) + s_col(b) + (uint32_t)(ch * ncol);
+#pragma unroll
+                for (int c8 = 0; c8 < kAMaxQ / 16; ++c8)
+                    if (8 * c8 < ncol) {
+                        float v[8];
+                        tmem_ld8(base + 8u * c8, v);
+                        tmem_wait_ld();
+#pragma unroll
+                        for (int i = 0; i < 8; ++i) s[8 * c8 + i] = v[i];
+                    }
+                asm volatile("tcgen05.fence::before_thread_sync;" ::: "memory");
+                __syncwarp();
+                if (lane == 0) bar_arrive(su32(&s_free[b]));
+            }
+            if (!soft_sync_and(ok)) { ok = false; break; }
+            // scale and mask: column q = 8 m + head; key valid for row m when
+            // key <= pos0 + m
+#pragma unroll
+            for (int i = 0; i < kAMaxQ / 2; ++i) {
+                if (i < ncol) {
+                    const int q = ch * ncol + i, m = q >> 3;
+                    const bool valid = m < M && key <= p.pos0 + m && key < p.n_valid;
+                    s[i] = valid ? s[i] * 0.0625f : -INFINITY;
+                    const uint32_t mk = __reduce_max_sync(0xFFFFFFFFu, fkey(s[i]));
+                    if (lane == 0) red_max[qt * kAMaxQ + q] = mk;
+                }
+            }
+            soft_sync();
+            // exp(s - new max) as bf16 halves into P (the MMA's B operand:
+            // row q, key along K), and the column sums of what the MMA sees
+            uint8_t *phi = ps + (size_t)(2 * b) * (size_t)(nq * kAKeys * 2);
+            uint8_t *plo = phi + (size_t)(nq * kAKeys * 2);
+#pragma unroll
+            for (int i = 0; i < kAMaxQ / 2; ++i) {
+                if (i < ncol) {
+                    const int q = ch * ncol + i;
+                    uint32_t mk = red_max[q];
+#pragma unroll
+                    for (int w = 1; w < 4; ++w) mk = max(mk, red_max[w * kAMaxQ + q]);
+                    const float mnew = fmaxf(m_run[q], unkey(mk));
+                    const float e = s[i] == -INFINITY ? 0.f : expf(s[i] - mnew);
+                    const __nv_bfloat16 h = __float2bfloat16_rn(e);
+                    const float hf = __bfloat162float(h);
+                    const __nv_bfloat16 lo = __float2bfloat16_rn(e - hf);
+                    const uint32_t off = plain_off(q, key_local, 2048u);
+                    *reinterpret_cast<__nv_bfloat16 *>(phi + off) = h;
+                    *reinterpret_cast<__nv_bfloat16 *>(plo + off) = lo;
+                    float cs = hf + __bfloat162float(lo);
+#pragma unroll
+                    for (int o = 16; o >= 1; o >>= 1) cs += __shfl_xor_sync(0xFFFFFFFFu, cs, o);
+                    if (lane == 0) red_sum[qt * kAMaxQ + q] = cs;
+                }
+            }
+            asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+            soft_sync();
+            if (tid == 0) bar_arrive(su32(&p_full[b]));
+            if (tid < nq) {
+                const int q = tid;
+                uint32_t mk = red_max[q];
+#pragma unroll
+                for (int w = 1; w < 4; ++w) mk = max(mk, red_max[w * kAMaxQ + q]);
+                const float mold = m_run[q], mnew = fmaxf(mold, unkey(mk));
+                const float a = mnew == -INFINITY ? 1.f : expf(mold - mnew);
+                const float lt = ((red_sum[q] + red_sum[kAMaxQ + q]) + red_sum[2 * kAMaxQ + q]) + red_sum[3 * kAMaxQ + q];
+                l_run[q] = fmaf(l_run[q], a, lt);
+                m_run[q] = mnew;
+                alpha[b * kAMaxQ + q] = a;
+            }
+            if (t >= 1) {
+                drain(t - 1);
+                if (!soft_sync_and(ok)) { ok = false; break; }
+            }
+        }
+        if (ok && nt >= 1) {
+            soft_sync();   // the last tile's alpha is written
+            drain(nt - 1);
+        }
+        ok = soft_sync_and(ok);
+        if (ok) {
+            const size_t cg = (size_t)chunk * kAHkv + g;
+#pragma unroll
+            for (int q = 0; q < kAMaxQ; ++q)
+                if (q < 8 * M) p.part_o[(cg * kAMaxQ + q) * kAD + dl] = oacc[q];
+            if (tid < 8 * M) {
+                p.part_ml[(cg * kAMaxQ + tid) * 2] = m_run[tid];
+                p.part_ml[(cg * kAMaxQ + tid) * 2 + 1] = l_run[tid];
+            }
+        }
+    }
+    asm volatile("tcgen05.fence::before_thread_sync;" ::: "memory");
+    __syncthreads();
+    if (warp == 0)
+        asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;" ::"r"(taddr), "r"(kATmemCols) : "memory");
+}
+
+// Merge of a row's chunks, in chunk order: o = sum_j e^(m_j - M) O_j /
+// sum_j e^(m_j - M) l_j with M the largest chunk maximum.  One CTA per
+// (row, query head), thread = d.
+__global__ void __launch_bounds__(kAD) attn_combine_kernel(const float *part_o, const float *part_ml, int pos0, float *o)
+{
+    const int m = blockIdx.x / kAHq, h = blockIdx.x % kAHq, g = h / kAGrp, q = kAGrp * m + h % kAGrp;
+    const int d = threadIdx.x;
+    const int J = (pos0 + m + 1 + kAChunk - 1) / kAChunk;
+    float mx = -INFINITY;
+#pragma unroll 1
+    for (int j = 0; j < J; ++j) mx = fmaxf(mx, __ldg(part_ml + (((size_t)j * kAHkv + g) * kAMaxQ + q) * 2));
+    float lsum = 0.f, acc = 0.f;
+#pragma unroll 1
+    for (int j = 0; j < J; ++j) {
+        const size_t c = ((size_t)j * kAHkv + g) * kAMaxQ + q;
+        const float w = expf(__ldg(part_ml + 2 * c) - mx);
+        lsum = fmaf(__ldg(part_ml + 2 * c + 1), w, lsum);
+        acc = fmaf(__ldg(part_o + c * kAD + d), w, acc);
+    }
+    o[((size_t)m * kAHq + h) * kAD + d] = acc / lsum;
+}
+
+// New rows' keys and values into the cache: row m at position pos0 + m;
+// values go to the transposed cache.  One CTA per (row, key/value head).
+__global__ void __launch_bounds__(kAD) attn_append_kernel(const uint16_t *kn, const uint16_t *vn, int pos0,
+                                                          uint16_t *kc, uint16_t *vtc, int T_cap)
+{
+    const int m = blockIdx.x / kAHkv, g = blockIdx.x % kAHkv, d = threadIdx.x, t = pos0 + m;
+    kc[((size_t)g * T_cap + t) * kAD + d] = kn[((size_t)m * kAHkv + g) * kAD + d];
+    vtc[((size_t)g * kAD + d) * T_cap + t] = vn[((size_t)m * kAHkv + g) * kAD + d];
+}
+
+PFN_cuTensorMapEncodeTiled_v12000 encode_fn()
+{
+    static std::once_flag once;
+    static PFN_cuTensorMapEncodeTiled_v12000 fn = nullptr;
+    std::call_once(once, [] {
+        void *ptr = nullptr;
+        cudaDriverEntryPointQueryResult qr;
+        if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &ptr, 12000, cudaEnableDefault, &qr) ==
+                cudaSuccess &&
+            qr == cudaDriverEntryPointSuccess)
+            fn = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(ptr);
+    });
+    return fn;
+}
+
+}  // namespace
+
+size_t attn_workspace_bytes(int T_cap)
+{
+    const size_t nchunks = (size_t)(T_cap + kAChunk - 1) / kAChunk;
+    return align_up(nchunks * kAHkv * kAMaxQ * 2 * sizeof(float), 256) + nchunks * kAHkv * kAMaxQ * kAD * sizeof(float);
+}
+
+int launch_attn(const uint16_t *q, const uint16_t *k, const uint16_t *vt, int T_cap, int pos0, int M, float *o,
+                void *ws, int *err, long long timeout_ns, cudaStream_t stream)
+{
+    PFN_cuTensorMapEncodeTiled_v12000 enc = encode_fn();
+    if (!enc) return MOE_ERR_UNSUPPORTED;
+    const int n_valid = pos0 + M, nchunks = (n_valid + kAChunk - 1) / kAChunk;
+    AttnParams P;
+    memset(&P, 0, sizeof P);
+    {
+        const cuuint64_t dims[3] = {(cuuint64_t)kAD, (cuuint64_t)n_valid, (cuuint64_t)kAHkv};
+        const cuuint64_t strides[2] = {(cuuint64_t)kAD * 2, (cuuint64_t)T_cap * kAD * 2};
+        const cuuint32_t box[3] = {64, (cuuint32_t)kAKeys, 1}, es[3] = {1, 1, 1};
+        if (enc(&P.tk, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, const_cast<uint16_t *>(k), dims, strides, box, es,
+                CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) != CUDA_SUCCESS)
+            return MOE_ERR_INVALID_ARG;
+    }
+    {
+        const cuuint64_t dims[3] = {(cuuint64_t)n_valid, (cuuint64_t)kAD, (cuuint64_t)kAHkv};
+        const cuuint64_t strides[2] = {(cuuint64_t)T_cap * 2, (cuuint64_t)kAD * T_cap * 2};
+        const cuuint32_t box[3] = {64, 128, 1}, es[3] = {1, 1, 1};
+        if (enc(&P.tv, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, const_cast<uint16_t *>(vt), dims, strides, box, es,
+                CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) != CUDA_SUCCESS)
+            return MOE_ERR_INVALID_ARG;
+    }
+    const size_t nchunks_cap = (size_t)(T_cap + kAChunk - 1) / kAChunk;
+    P.q = q;
+    P.part_ml = static_cast<float *>(ws);
+    P.part_o = reinterpret_cast<float *>(static_cast<uint8_t *>(ws) +
+                                         align_up(nchunks_cap * kAHkv * kAMaxQ * 2 * sizeof(float), 256));
+    P.M = M;
+    P.pos0 = pos0;
+    P.n_valid = n_valid;
+    P.nq = 16 * ((kAGrp * M + 15) / 16);
+    P.nsub = attn_layout(P.nq, 8).total + 1024 <= kSmemMax ? 8 : 6;
+    P.timeout_ns = timeout_ns;
+    P.err = err;
+    const int smem = attn_layout(P.nq, P.nsub).total + 1024;
+    if (smem > kSmemMax) return MOE_ERR_UNSUPPORTED;
+    static std::once_flag attr_once[64];
+    int dev = 0;
+    cudaError_t e = cudaGetDevice(&dev);
+    if (e != cudaSuccess || dev < 0 || dev >= 64) { note_cuda_error((int)e); return MOE_ERR_CUDA; }
+    std::call_once(attr_once[dev], [&] {
+        e = cudaFuncSetAttribute(attn_chunk_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, kSmemMax);
+    });
+    if (e != cudaSuccess) { note_cuda_error((int)e); return MOE_ERR_CUDA; }
+    attn_chunk_kernel<<<dim3(nchunks, kAHkv), kAThreads, smem, stream>>>(P);
+    note_launch();
+    attn_combine_kernel<<<M * kAHq, kAD, 0, stream>>>(P.part_o, P.part_ml, pos0, o);
+    note_launch();
+    e = cudaGetLastError();
+    if (e != cudaSuccess) { note_cuda_error((int)e); return MOE_ERR_CUDA; }
+    return MOE_OK;
+}
+
+int launch_attn_append(const uint16_t *kn, const uint16_t *vn, int M, int pos0, uint16_t *kc, uint16_t *vtc, int T_cap,
+                       cudaStream_t stream)
+{
+    attn_append_kernel<<<M * kAHkv, kAD, 0, stream>>>(kn, vn, pos0, kc, vtc, T_cap);
+    note_launch();
+    const cudaError_t e = cudaGetLastError();
+    if (e != cudaSuccess) { note_cuda_error((int)e); return MOE_ERR_CUDA; }
+    return MOE_OK;
+}
+
+}  // namespace moe

@@ -173,6 +173,12 @@ int launch_pack_rows(const moe_src_matrix &m, int bits, int rows, int K, uint8_t
 // fused Q/K/V projection (moe_layer.cu)
 int launch_qkv(const uint8_t *W, int rows, int K, int bits, const uint16_t *x, int M, float *y, int *err,
                long long timeout_ns, cudaStream_t stream);
+// split-K decode attention with grouped query heads (moe_attn.cu)
+size_t attn_workspace_bytes(int T_cap);
+int launch_attn(const uint16_t *q, const uint16_t *k, const uint16_t *vt, int T_cap, int pos0, int M, float *o,
+                void *ws, int *err, long long timeout_ns, cudaStream_t stream);
+int launch_attn_append(const uint16_t *kn, const uint16_t *vn, int M, int pos0, uint16_t *kc, uint16_t *vtc, int T_cap,
+                       cudaStream_t stream);
 int launch_export(const moe_layer &L, int tensor_id, int expert, uint8_t *codes, uint16_t *scales,
                   uint16_t *biases, cudaStream_t stream);
 // One set of grouped tensor-core products (moe_tc.cu): slot u's expert

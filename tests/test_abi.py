@@ -166,3 +166,28 @@ def test_build_flags_of_both_builds():
         "m.debug_inject(7); m.debug_inject(-1)\n"
         "print(m.build_flags(), len(missing), L.moe_selftest_host())\n")
     assert out.split() == ["1", "0", "0"]
+
+
+def test_attention_sizes_and_argument_errors():
+    """Workspace size of the decode attention (per 512-position chunk: 2 KV
+    heads x 64 query columns x (256 + 2) floats, the maxima and sums first,
+    256-aligned) and its argument checks, which reject before any launch."""
+    L = moe.lib()
+    n = C.c_size_t()
+    assert L.moe_attn_workspace_size(4096, C.byref(n)) == 0
+    chunks = 8
+    ml = chunks * 2 * 64 * 2 * 4
+    assert n.value == ((ml + 255) // 256) * 256 + chunks * 2 * 64 * 256 * 4
+    assert L.moe_attn_workspace_size(0, C.byref(n)) == 1
+    fake = 1 << 20   # never dereferenced: every call below is rejected first
+    err = fake
+    # M out of range, T_cap not a multiple of 8, rows past the cache, null pointers
+    assert L.moe_attn_decode(fake, fake, fake, 64, 0, 0, fake, fake, 1 << 30, err, None) == 1
+    assert L.moe_attn_decode(fake, fake, fake, 64, 0, 9, fake, fake, 1 << 30, err, None) == 1
+    assert L.moe_attn_decode(fake, fake, fake, 60, 0, 1, fake, fake, 1 << 30, err, None) == 1
+    assert L.moe_attn_decode(fake, fake, fake, 64, 63, 2, fake, fake, 1 << 30, err, None) == 1
+    assert L.moe_attn_decode(None, fake, fake, 64, 0, 1, fake, fake, 1 << 30, err, None) == 1
+    assert L.moe_attn_decode(fake + 8, fake, fake, 64, 0, 1, fake, fake, 1 << 30, err, None) == 1
+    assert L.moe_attn_decode(fake, fake, fake, 64, 0, 1, fake, fake, 16, err, None) == 3
+    assert L.moe_attn_append(fake, fake, 0, 0, fake, fake, 64, None) == 1
+    assert L.moe_attn_append(fake, fake, 2, 63, fake, fake, 64, None) == 1

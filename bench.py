@@ -353,6 +353,59 @@ def qkv_measure(shape, dev, n_sets, warmup):
     return res
 
 
+def attn_measure(dev, peaks, warmup):
+    """Time moe_attn_decode (16 query heads, 2 KV heads, head dim 256, bf16
+    cache) at a 32K-position cache (64 MB of keys and values: L2 could hold
+    it, so a 256 MB buffer is written before every call) and at 128K
+    positions (256 MB, above L2), for 1 and 3 rows.  Each call is timed with
+    CUDA events on its own stream; bytes = the valid keys and values (read
+    once) plus the queries and the fp32 output."""
+    import torch
+    import quantized_moe_decode_layer_gb300 as moe
+    import synth
+    res = {}
+    flush = torch.empty(256 << 20, dtype=torch.uint8, device=dev)
+    st = torch.cuda.Stream()
+    for T, do_flush, calls in ((32768, True, 40), (131072, False, 40)):
+        q_all, k, vt = synth.make_attn(T, T, 3, 5, device=dev)
+        cache = moe.AttnCache(T, device=dev)
+        cache.k.copy_(k)
+        cache.vt.copy_(vt)
+        del k, vt
+        for M in (1, 3):
+            q = q_all[:M].contiguous()
+            out = torch.empty((M, 16, 256), dtype=torch.float32, device=dev)
+            err = torch.zeros(1, dtype=torch.int32, device=dev)
+            with torch.cuda.stream(st):
+                for _ in range(max(3, warmup)):
+                    cache.attend(q, T - M, out=out, err=err, stream=st)
+            st.synchronize()
+            evs = []
+            with torch.cuda.stream(st):
+                for _ in range(calls):
+                    if do_flush:
+                        flush.fill_(1)
+                    a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+                    a.record(st)
+                    cache.attend(q, T - M, out=out, err=err, stream=st)
+                    b.record(st)
+                    evs.append((a, b))
+            st.synchronize()
+            assert int(err.item()) == 0
+            ts = sorted(a.elapsed_time(b) * 1e-3 for a, b in evs)
+            per = sum(ts) / len(ts)
+            nbytes = T * 2 * 256 * 2 * 2 + M * 16 * 256 * (2 + 4)
+            res[f"T{T}_M{M}"] = {"us_per_call": round(per * 1e6, 2), "median_us": round(ts[len(ts) // 2] * 1e6, 2),
+                                 "gbs": round(nbytes / per / 1e9, 1),
+                                 "frac": round(nbytes / per / 1e9 / peaks["hbm_gbs"], 4),
+                                 "bytes_per_call": nbytes, "calls": calls,
+                                 "l2": "256 MB written before each call" if do_flush else "cache > L2"}
+        del cache
+        torch.cuda.empty_cache()
+    res["shape"] = "16 query heads, 2 KV heads, head dim 256, bf16 cache, chunks of 512 positions"
+    return res
+
+
 def run_ours(args):
     import numpy as np
     import torch
@@ -490,6 +543,11 @@ def run_ours(args):
     if not args.no_m4:
         qkv = qkv_measure(shape, dev, args.layers, args.warmup)
 
+    # the split-K decode attention with grouped query heads
+    attn = None
+    if not args.no_m4:
+        attn = attn_measure(dev, peaks, args.warmup)
+
     # the 397B-shaped layer at M=1: a stack over 15 distinct layer sets (55 GB)
     b397 = None
     if not args.no_m4:
@@ -545,6 +603,7 @@ def run_ours(args):
                        "parallelism": f"replicas x{world}"},
             "us_per_layer": round(us_layer, 3), "fraction_of_8TBs": round(value / world / 8000.0, 4),
             "single_layer_call_us": single, "m4": m4, "sweep": sweep, "tc_gate_up": tc, "b397": b397, "qkv": qkv,
+            "attn": attn,
             "roofline": roof, "e2e": e2e,
             "gpu_launches": launches, "launches_per_step": launches / args.steps, "clocks": clocks,
             "cpu_baseline": cpu,

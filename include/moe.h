@@ -396,8 +396,9 @@ void moe_qkv_destroy(moe_qkv *qkv);
  *            (g * T_cap + t) * 256;
  *   vt_cache [2][256][T_cap]  values stored transposed: value d of position t
  *            of head g at (g * 256 + d) * T_cap + t.
- * T_cap must be a multiple of 8 and both base addresses 16-byte aligned.
- * Positions past the last valid one are never used.
+ * T_cap must be a multiple of 8, at most MOE_ATTN_MAX_POSITIONS, and both
+ * base addresses 16-byte aligned.  Positions past the last valid one are
+ * never used.
  *
  * moe_attn_workspace_size: device scratch a call with this T_cap needs
  * (the per-chunk partial results).  Errors: INVALID_ARG. */
@@ -405,6 +406,7 @@ void moe_qkv_destroy(moe_qkv *qkv);
 #define MOE_ATTN_KV_HEADS 2
 #define MOE_ATTN_HEAD_DIM 256
 #define MOE_ATTN_MAX_ROWS 8
+#define MOE_ATTN_MAX_POSITIONS (1 << 19)
 int moe_attn_workspace_size(int T_cap, size_t *bytes);
 
 /* Attention of M token rows (1 <= M <= 8) at positions pos0 .. pos0 + M - 1

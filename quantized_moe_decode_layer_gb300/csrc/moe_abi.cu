@@ -727,7 +727,7 @@ void moe_qkv_destroy(moe_qkv *qkv) { free(qkv); }
 
 int moe_attn_workspace_size(int T_cap, size_t *bytes)
 {
-    if (!bytes || T_cap < 1) return MOE_ERR_INVALID_ARG;
+    if (!bytes || T_cap < 1 || T_cap > attn_max_positions()) return MOE_ERR_INVALID_ARG;
     *bytes = attn_workspace_bytes(T_cap);
     return MOE_OK;
 }
@@ -736,7 +736,8 @@ int moe_attn_decode(const uint16_t *q_dev, const uint16_t *k_cache_dev, const ui
                     int pos0, int M, float *o_dev, void *ws_dev, size_t ws_bytes, int *err_dev, moe_stream_t stream)
 {
     if (!q_dev || !k_cache_dev || !vt_cache_dev || !o_dev || !ws_dev || !err_dev) return MOE_ERR_INVALID_ARG;
-    if (M < 1 || M > MOE_ATTN_MAX_ROWS || pos0 < 0 || T_cap < 8 || T_cap % 8 != 0 || pos0 + M > T_cap)
+    if (M < 1 || M > MOE_ATTN_MAX_ROWS || pos0 < 0 || T_cap < 8 || T_cap % 8 != 0 || pos0 + M > T_cap ||
+        T_cap > attn_max_positions())
         return MOE_ERR_INVALID_ARG;
     if ((reinterpret_cast<uintptr_t>(k_cache_dev) | reinterpret_cast<uintptr_t>(vt_cache_dev) |
          reinterpret_cast<uintptr_t>(q_dev) | reinterpret_cast<uintptr_t>(ws_dev)) & 15u)

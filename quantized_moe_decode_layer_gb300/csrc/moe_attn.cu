@@ -23,21 +23,25 @@
 //
 // Per CTA, over the chunk's tiles of 128 keys (warp-specialised):
 //   - a TMA warp loads 16 KB boxes (128 rows x 64 bf16, 128-byte swizzle)
-//     into a ring: the tile's keys [128 keys x 256] in 4 boxes, then its
-//     values from the transposed cache [256 d x 128 keys] in 4 boxes;
+//     into a ring, one lane per box so that the boxes of a round go out
+//     together: the tile's keys [128 keys x 256] in 4 boxes, then its values
+//     from the transposed cache [256 d x 128 keys] in 4 boxes;
 //   - an MMA warp issues S^T = K Q^T (M = 128 keys, N = the query columns,
 //     K = 256 over d; Q in shared memory, written once) into one of two
 //     tensor-memory score blocks, and O^T += V^T P^T (M = 128 values of d per
-//     half, K = 128 keys) into one of two output blocks, with P in two bf16
-//     halves (p = hi + lo, each an MMA into the same sum) so the weights keep
-//     ~16 significant bits;
-//   - eight softmax warps read the score block (thread = key, a half of the
-//     query columns each), mask keys past each row's position, take the
+//     half, K = 128 keys) into the output block, with P in two bf16 halves
+//     (p = hi + lo) stacked as the product's N columns (one instruction for
+//     both: a tensor-core instruction of M = 128 costs about the same at any
+//     N up to 256), so the weights keep ~16 significant bits;
+//   - eight softmax warps read the score block (thread = key, every other
+//     query column each, all columns' steps interleaved), mask keys past each row's position, take the
 //     tile's column maxima (redux.sync on order-preserving keys) and the new
-//     running maxima, write exp(s - max) as bf16 halves into shared memory
-//     for the MMA, and add the column sums; then they take the previous
-//     tile's output block into fp32 registers (thread = one d of one half),
-//     rescaled by exp(old max - new max) (online softmax).
+//     running maxima, and write exp(s - max) as bf16 halves into shared
+//     memory for the MMA, which also multiplies them by a tile of ones: the
+//     column sums of exactly the weights it used; then they take the
+//     previous tile's output block into fp32 registers (thread = one d of
+//     one half) and its column sums into the running sums, both rescaled by
+//     exp(old max - new max) (online softmax).
 // Every wait is bounded; one that runs out sets *err, the roles stop, the
 // CTA waits (bounded) for its copies and MMAs and frees its tensor memory.
 #include <cuda.h>
@@ -58,16 +62,20 @@ constexpr int kAKeys = 128;                 // keys per tile (MMA M of the score
 constexpr int kATiles = 4;                  // tiles per chunk
 constexpr int kAChunk = kAKeys * kATiles;   // keys per chunk: the split points are multiples of this
 constexpr int kAMaxRows = 8;
+constexpr int kAMaxPos = 1 << 19;           // cache positions at most (1024 chunks)
 constexpr int kAMaxQ = kAGrp * kAMaxRows;   // query columns per key/value head
 constexpr int kABox = 16384;                // one TMA box: 128 rows of 128 bytes
 constexpr int kASoftWarps = 8;
 constexpr int kASoftThreads = kASoftWarps * 32;
 constexpr int kAThreads = kASoftThreads + 64;   // + TMA warp + MMA warp
 constexpr uint32_t kATmemCols = 512;
-// tensor-memory columns: score blocks at 0 and 64, output blocks (two
-// halves of d, 64 columns each) at 128 and 256
+// tensor-memory columns: score blocks (up to 64 query columns) at 0 and
+// 64, the output block (two halves of d, up to 128 columns each: the query
+// columns of the high, then of the low weight halves) at 128 and 256, and
+// the column sums of the weights (ones times P, the same columns) at 384
 __host__ __device__ constexpr uint32_t s_col(int b) { return 64u * (uint32_t)b; }
-__host__ __device__ constexpr uint32_t o_col(int b, int half) { return 128u + 128u * (uint32_t)b + 64u * (uint32_t)half; }
+__host__ __device__ constexpr uint32_t o_col(int, int half) { return 128u + 128u * (uint32_t)half; }
+constexpr uint32_t kSumCol = 384u;
 
 struct AttnParams {
     CUtensorMap tk;   // keys: dims {256, n_valid, 2}, box {64, 128, 1}
@@ -82,7 +90,7 @@ struct AttnParams {
 
 // Shared-memory layout (offsets from a 1024-byte aligned base).
 struct ALayout {
-    int ring, q, p, red, bars, total;
+    int ring, q, p, ones, red, bars, total;
 };
 __host__ __device__ inline ALayout attn_layout(int nq, int nsub)
 {
@@ -90,7 +98,8 @@ __host__ __device__ inline ALayout attn_layout(int nq, int nsub)
     L.ring = 0;
     L.q = nsub * kABox;                       // Q: nq rows x 256, no swizzle, 4096 B per 8 rows
     L.p = L.q + nq * kAD * 2;                 // P: [2 buffers][hi, lo] nq rows x 128 keys
-    L.red = L.p + 4 * nq * kAKeys * 2;        // reductions and running state
+    L.ones = L.p + 4 * nq * kAKeys * 2;       // a 128 x 64 tile of bf16 ones (1024-aligned: P is)
+    L.red = L.ones + kABox;                   // reductions and running state
     L.bars = L.red + 4 * kAMaxQ * 4 * 2 + 4 * kAMaxQ * 4;
     L.total = L.bars + (2 * nsub + 11) * 8 + 16;
     return L;
@@ -225,34 +234,31 @@ __device__ __forceinline__ uint32_t plain_off(int r, int k, uint32_t sbo)
     return (uint32_t)(r >> 3) * sbo + (uint32_t)(k >> 3) * 128u + (uint32_t)(r & 7) * 16u + (uint32_t)(k & 7) * 2u;
 }
 
-// The boxes of a chunk in ring order: tile 0's keys, then for each tile t
-// the keys of tile t + 1 (if any) and the values of tile t.  f(is_value,
-// tile, part): part = d chunk of 64 for keys, 2 * half + key half for values.
-template <typename F>
-__device__ __forceinline__ void for_boxes(int nt, F &&f)
+// Box j of a chunk of nt tiles, in ring order: tile 0's keys (4 boxes of
+// 64 d), then for each tile t the keys of tile t + 1 (if any) and the
+// values of tile t (4 boxes: half of d, then key half).
+__device__ __forceinline__ void box_of(int j, int nt, bool &is_v, int &t, int &part)
 {
-#pragma unroll 1
-    for (int part = 0; part < 4; ++part) f(false, 0, part);
-#pragma unroll 1
-    for (int t = 0; t < nt; ++t) {
-        if (t + 1 < nt)
-#pragma unroll 1
-            for (int part = 0; part < 4; ++part) f(false, t + 1, part);
-#pragma unroll 1
-        for (int part = 0; part < 4; ++part) f(true, t, part);
-    }
+    if (j < 4) { is_v = false; t = 0; part = j; return; }
+    j -= 4;
+    t = j >> 3;
+    const int w = j & 7;
+    if (t + 1 < nt && w < 4) { is_v = false; part = w; t = t + 1; }
+    else { is_v = true; part = t + 1 < nt ? w - 4 : w; }
 }
 
+template <int NQ>
 __global__ void __launch_bounds__(kAThreads, 1) attn_chunk_kernel(const __grid_constant__ AttnParams p)
 {
+    constexpr int NC = NQ / 2;   // query columns of a softmax thread: q = 2 i + ch
     extern __shared__ __align__(1024) uint8_t smem_raw[];
     uint8_t *sm = reinterpret_cast<uint8_t *>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
-    const int nq = p.nq, nsub = p.nsub, M = p.M;
-    const ALayout L = attn_layout(nq, nsub);
+    const int nsub = p.nsub, M = p.M, nreal = kAGrp * p.M;
+    const ALayout L = attn_layout(NQ, nsub);
     const int chunk = blockIdx.x, g = blockIdx.y;
     const int k0 = chunk * kAChunk;
     const int nkeys = min(kAChunk, p.n_valid - k0);
-    const int nt = (nkeys + kAKeys - 1) / kAKeys;
+    const int nt = (nkeys + kAKeys - 1) / kAKeys, nbox = 8 * nt;
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
 
     uint8_t *ring = sm + L.ring, *qs = sm + L.q, *ps = sm + L.p;
@@ -263,7 +269,7 @@ __global__ void __launch_bounds__(kAThreads, 1) attn_chunk_kernel(const __grid_c
     uint64_t *bars = reinterpret_cast<uint64_t *>(sm + L.bars);
     uint64_t *full = bars, *empty = bars + nsub;
     uint64_t *s_full = bars + 2 * nsub, *s_free = s_full + 2, *p_full = s_free + 2, *o_full = p_full + 2,
-             *o_free = o_full + 2, *mma_done = o_free + 2;
+             *o_free = o_full + 1, *mma_done = o_free + 1;
     uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(bars + 2 * nsub + 11);
     volatile int *abort_flag = reinterpret_cast<volatile int *>(tmem_slot + 1);
 
@@ -276,9 +282,9 @@ __global__ void __launch_bounds__(kAThreads, 1) attn_chunk_kernel(const __grid_c
             bar_init(su32(&s_full[b]), 1);
             bar_init(su32(&s_free[b]), kASoftWarps);
             bar_init(su32(&p_full[b]), 1);
-            bar_init(su32(&o_full[b]), 1);
-            bar_init(su32(&o_free[b]), kASoftWarps);
         }
+        bar_init(su32(o_full), 1);
+        bar_init(su32(o_free), kASoftWarps);
         bar_init(su32(mma_done), 1);
         *abort_flag = 0;
         asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
@@ -291,7 +297,7 @@ __global__ void __launch_bounds__(kAThreads, 1) attn_chunk_kernel(const __grid_c
     }
     // Q of this key/value head as the score product's B operand: row
     // q = 8 m + head in group, zero past the last row
-    for (int i = tid; i < nq * (kAD / 8); i += kAThreads) {
+    for (int i = tid; i < NQ * (kAD / 8); i += kAThreads) {
         const int qr = i / (kAD / 8), dc = i % (kAD / 8);
         const int m = qr / kAGrp, hh = qr % kAGrp;
         uint4 v = make_uint4(0u, 0u, 0u, 0u);
@@ -302,6 +308,8 @@ __global__ void __launch_bounds__(kAThreads, 1) attn_chunk_kernel(const __grid_c
         m_run[i] = -INFINITY;
         l_run[i] = 0.f;
     }
+    for (int i = tid; i < kABox / 16; i += kAThreads)
+        reinterpret_cast<uint4 *>(sm + L.ones)[i] = make_uint4(0x3F803F80u, 0x3F803F80u, 0x3F803F80u, 0x3F803F80u);
     asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
     asm volatile("tcgen05.fence::before_thread_sync;" ::: "memory");
     __syncthreads();
@@ -310,38 +318,43 @@ __global__ void __launch_bounds__(kAThreads, 1) attn_chunk_kernel(const __grid_c
 
     if (warp == kASoftWarps) {
         // ---------------------------------------------------------- TMA warp
-        if (lane == 0) {
-            int slot = 0, issued = 0;
-            unsigned ph = 0;
-            bool go = true;
-            for_boxes(nt, [&](bool is_v, int t, int part) {
-                if (!go) return;
-                if (issued >= nsub && !bar_wait(su32(&empty[slot]), ph ^ 1u, abort_flag, p)) {
-                    go = false;
-                    return;
-                }
-                const uint32_t dst = su32(ring + (size_t)slot * kABox), fb = su32(&full[slot]);
+        // batches of nsub boxes, one per lane: each lane waits for its own
+        // slot to be released and issues, so the boxes go out together
+        bool go = true;
+#pragma unroll 1
+        for (int base = 0; base < nbox && go; base += nsub) {
+            const int j = base + lane;
+            bool pending = lane < nsub && j < nbox;
+            if (pending && base > 0 && !bar_wait(su32(&empty[lane]), (unsigned)((base / nsub) - 1) & 1u, abort_flag, p))
+                pending = false;
+            if (pending) {
+                bool is_v;
+                int t, part;
+                box_of(j, nt, is_v, t, part);
+                const uint32_t dst = su32(ring + (size_t)lane * kABox), fb = su32(&full[lane]);
                 bar_expect(fb, kABox);
                 const int kb = k0 + kAKeys * t;
                 if (!is_v) tma_load3(dst, &p.tk, 64 * part, kb, g, fb);
                 else tma_load3(dst, &p.tv, kb + 64 * (part & 1), 128 * (part >> 1), g, fb);
-                ++issued;
-                if (++slot == nsub) { slot = 0; ph ^= 1u; }
-            });
-            // every box issued must have landed before the CTA can exit
-            const int last = issued;
-            for (int i = 0; i < nsub && i < last; ++i) {
-                const int q = last - 1 - i;                    // the i-th most recent box
-                const int s = q % nsub;
-                const unsigned par = (unsigned)(q / nsub) & 1u;
+            }
+            go = !__any_sync(0xFFFFFFFFu, *abort_flag != 0);
+        }
+        // every box issued must have landed before the CTA can exit: box j
+        // of the last round of slot s
+        const int rounds = (nbox + nsub - 1) / nsub;
+        if (lane < nsub) {
+            int last = -1;
+            for (int r = rounds - 1; r >= 0 && last < 0; --r)
+                if (r * nsub + lane < nbox) last = r;
+            if (last >= 0) {
                 const unsigned long long t0 = gtime();
-                while (!bar_test(su32(&full[s]), par) && (long long)(gtime() - t0) <= p.timeout_ns) {}
+                while (!bar_test(su32(&full[lane]), (unsigned)last & 1u) && (long long)(gtime() - t0) <= p.timeout_ns) {}
             }
         }
     } else if (warp == kASoftWarps + 1) {
         // ---------------------------------------------------------- MMA warp
         if (lane == 0) {
-            const uint32_t idesc = idesc_bf16(nq);
+            const uint32_t id_s = idesc_bf16(NQ), id_o = idesc_bf16(2 * NQ), ones = su32(sm + L.ones);
             int slot = 0;
             unsigned ph = 0;
             bool go = true;
@@ -364,32 +377,33 @@ __global__ void __launch_bounds__(kAThreads, 1) attn_chunk_kernel(const __grid_c
 #pragma unroll
                     for (int k = 0; k < 4; ++k)
                         umma(taddr + s_col(b), desc_sw128(a0 + 32u * k), desc_plain(su32(qs) + 256u * (4 * part + k), 4096u),
-                             idesc, (part | k) != 0 ? 1u : 0u);
+                             id_s, (part | k) != 0 ? 1u : 0u);
                     release();
                 }
                 if (go) umma_commit(su32(&s_full[b]));
             };
+            // O^T += V^T [P_hi; P_lo]^T: the two halves of the weights are the
+            // columns 0 .. NQ - 1 and NQ .. 2 NQ - 1 of one product
             auto values = [&](int t) {
                 const int b = t & 1;
                 if (!bar_wait(su32(&p_full[b]), (unsigned)(t >> 1) & 1u, abort_flag, p)) go = false;
-                if (go && t >= 2 && !bar_wait(su32(&o_free[b]), (unsigned)((t - 2) >> 1) & 1u, abort_flag, p)) go = false;
+                if (go && t >= 1 && !bar_wait(su32(o_free), (unsigned)(t - 1) & 1u, abort_flag, p)) go = false;
                 asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory");
-                const uint32_t phi = su32(ps) + (uint32_t)(2 * b) * (uint32_t)(nq * kAKeys * 2);
-                const uint32_t plo = phi + (uint32_t)(nq * kAKeys * 2);
+                const uint32_t pb = su32(ps) + (uint32_t)b * (uint32_t)(2 * NQ * kAKeys * 2);
                 for (int part = 0; part < 4 && go; ++part) {
                     if (!take()) break;
                     const int half = part >> 1, kh = part & 1;
                     const uint32_t a0 = su32(ring + (size_t)slot * kABox);
 #pragma unroll
                     for (int k = 0; k < 4; ++k) {
-                        const uint32_t koff = 256u * (4 * kh + k);
-                        umma(taddr + o_col(b, half), desc_sw128(a0 + 32u * k), desc_plain(phi + koff, 2048u), idesc,
-                             (kh | k) != 0 ? 1u : 0u);
-                        umma(taddr + o_col(b, half), desc_sw128(a0 + 32u * k), desc_plain(plo + koff, 2048u), idesc, 1u);
+                        const uint64_t bd = desc_plain(pb + 256u * (4 * kh + k), 2048u);
+                        umma(taddr + o_col(0, half), desc_sw128(a0 + 32u * k), bd, id_o, (kh | k) != 0 ? 1u : 0u);
+                        // the column sums of the weights: a tile of ones times P
+                        if (half == 0) umma(taddr + kSumCol, desc_sw128(ones + 32u * k), bd, id_o, (kh | k) != 0 ? 1u : 0u);
                     }
                     release();
                 }
-                if (go) umma_commit(su32(&o_full[b]));
+                if (go) umma_commit(su32(o_full));
             };
             scores(0);
             for (int t = 0; t < nt && go; ++t) {
@@ -403,33 +417,50 @@ __global__ void __launch_bounds__(kAThreads, 1) attn_chunk_kernel(const __grid_c
         }
     } else {
         // ------------------------------------------------------ softmax warps
+        // thread = key 32 qt + lane of a tile (columns q = 2 i + ch), and, for
+        // the output, d = 128 ch + 32 qt + lane
         const int qt = warp & 3, ch = warp >> 2;
-        const int ncol = nq >> 1;                 // query columns of this thread (multiple of 8)
         const int key_local = 32 * qt + lane;
-        const int dl = 128 * ch + 32 * qt + lane;  // the d this thread accumulates
-        float oacc[kAMaxQ];
+        const int dl = 128 * ch + 32 * qt + lane;
+        float oacc[NQ];
 #pragma unroll
-        for (int i = 0; i < kAMaxQ; ++i) oacc[i] = 0.f;
+        for (int i = 0; i < NQ; ++i) oacc[i] = 0.f;
         bool ok = true;
         auto drain = [&](int t) {
-            const int b = t & 1;
-            ok = __all_sync(0xFFFFFFFFu, bar_wait(su32(&o_full[b]), (unsigned)(t >> 1) & 1u, abort_flag, p));
+            ok = __all_sync(0xFFFFFFFFu, bar_wait(su32(o_full), (unsigned)t & 1u, abort_flag, p));
             asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory");
             if (!ok) return;
-            const uint32_t base = taddr + ((uint32_t)(32 * qt) << 16) + o_col(b, ch);
+            const uint32_t base = taddr + ((uint32_t)(32 * qt) << 16) + o_col(0, ch);
+            const float *al = alpha + (t & 1) * kAMaxQ;
+            // columns q (high halves) and NQ + q (low halves), 8 at a time
 #pragma unroll
-            for (int c8 = 0; c8 < kAMaxQ / 8; ++c8) {
-                if (8 * c8 < nq) {
-                    float v[8];
-                    tmem_ld8(base + 8u * c8, v);
+            for (int c8 = 0; c8 < NQ / 8; ++c8) {
+                float hi[8], lo[8];
+                tmem_ld8(base + 8u * c8, hi);
+                tmem_ld8(base + (uint32_t)NQ + 8u * c8, lo);
+                tmem_wait_ld();
+#pragma unroll
+                for (int i = 0; i < 8; ++i) oacc[8 * c8 + i] = fmaf(oacc[8 * c8 + i], al[8 * c8 + i], hi[i] + lo[i]);
+            }
+            if (warp == 0) {
+                // every lane of the sums block holds the same column sums;
+                // lane i of each group of 8 keeps column 8 c8 + i
+                const uint32_t sb = taddr + kSumCol;
+#pragma unroll
+                for (int c8 = 0; c8 < NQ / 8; ++c8) {
+                    float hs[8], ls[8];
+                    tmem_ld8(sb + 8u * c8, hs);
+                    tmem_ld8(sb + (uint32_t)NQ + 8u * c8, ls);
                     tmem_wait_ld();
+                    float mine = 0.f;
 #pragma unroll
-                    for (int i = 0; i < 8; ++i) oacc[8 * c8 + i] = fmaf(oacc[8 * c8 + i], alpha[b * kAMaxQ + 8 * c8 + i], v[i]);
+                    for (int i = 0; i < 8; ++i) mine = (lane & 7) == i ? hs[i] + ls[i] : mine;
+                    if (lane < 8) l_run[8 * c8 + lane] = fmaf(l_run[8 * c8 + lane], al[8 * c8 + lane], mine);
                 }
             }
             asm volatile("tcgen05.fence::before_thread_sync;" ::: "memory");
             __syncwarp();
-            if (lane == 0) bar_arrive(su32(&o_free[b]));
+            if (lane == 0) bar_arrive(su32(o_free));
         };
 #pragma unroll 1
         for (int t = 0; t < nt; ++t) {
@@ -437,75 +468,78 @@ __global__ void __launch_bounds__(kAThreads, 1) attn_chunk_kernel(const __grid_c
             const int key = k0 + kAKeys * t + key_local;
             ok = __all_sync(0xFFFFFFFFu, bar_wait(su32(&s_full[b]), (unsigned)(t >> 1) & 1u, abort_flag, p));
             asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory");
-            float s[kAMaxQ / 2];
+            float sv[NC];
             if (ok) {
-                const uint32_t base = taddr + ((uint32_t)(32 * qt) << 16) + s_col(b) + (uint32_t)(ch * ncol);
+                const uint32_t base = taddr + ((uint32_t)(32 * qt) << 16) + s_col(b);
+                // 16 columns at a time, keeping every other one (q = 2 i + ch)
 #pragma unroll
-                for (int c8 = 0; c8 < kAMaxQ / 16; ++c8)
-                    if (8 * c8 < ncol) {
-                        float v[8];
-                        tmem_ld8(base + 8u * c8, v);
-                        tmem_wait_ld();
+                for (int c16 = 0; c16 < NQ / 16; ++c16) {
+                    float w0[8], w1[8];
+                    tmem_ld8(base + 16u * c16, w0);
+                    tmem_ld8(base + 16u * c16 + 8u, w1);
+                    tmem_wait_ld();
 #pragma unroll
-                        for (int i = 0; i < 8; ++i) s[8 * c8 + i] = v[i];
+                    for (int i = 0; i < 4; ++i) {
+                        sv[8 * c16 + i] = w0[2 * i + ch];
+                        sv[8 * c16 + 4 + i] = w1[2 * i + ch];
                     }
+                }
                 asm volatile("tcgen05.fence::before_thread_sync;" ::: "memory");
                 __syncwarp();
                 if (lane == 0) bar_arrive(su32(&s_free[b]));
             }
             if (!soft_sync_and(ok)) { ok = false; break; }
-            // scale and mask: column q = 8 m + head; key valid for row m when
-            // key <= pos0 + m
+            // scale and mask (key valid for row m when key <= pos0 + m), then
+            // the tile's column maxima over the warp's keys
+            uint32_t mk[NC];
 #pragma unroll
-            for (int i = 0; i < kAMaxQ / 2; ++i) {
-                if (i < ncol) {
-                    const int q = ch * ncol + i, m = q >> 3;
-                    const bool valid = m < M && key <= p.pos0 + m && key < p.n_valid;
-                    s[i] = valid ? s[i] * 0.0625f : -INFINITY;
-                    const uint32_t mk = __reduce_max_sync(0xFFFFFFFFu, fkey(s[i]));
-                    if (lane == 0) red_max[qt * kAMaxQ + q] = mk;
-                }
+            for (int i = 0; i < NC; ++i) {
+                const int q = 2 * i + ch, m = q >> 3;
+                const bool valid = q < nreal && key <= p.pos0 + m && key < p.n_valid;
+                sv[i] = valid ? sv[i] * 0.0625f : -INFINITY;
+                mk[i] = fkey(sv[i]);
+            }
+            // (every column, padding included: branches around the
+            // reductions would keep them from overlapping)
+#pragma unroll
+            for (int i = 0; i < NC; ++i) mk[i] = __reduce_max_sync(0xFFFFFFFFu, mk[i]);
+            if (lane == 0) {
+#pragma unroll
+                for (int i = 0; i < NC; ++i) red_max[qt * kAMaxQ + 2 * i + ch] = mk[i];
             }
             soft_sync();
-            // exp(s - new max) as bf16 halves into P (the MMA's B operand:
-            // row q, key along K), and the column sums of what the MMA sees
-            uint8_t *phi = ps + (size_t)(2 * b) * (size_t)(nq * kAKeys * 2);
-            uint8_t *plo = phi + (size_t)(nq * kAKeys * 2);
+            // new running maxima, then exp(s - max) as bf16 halves into P
+            // (rows q and NQ + q of the value product's B operand, key along
+            // K) and the column sums of what the MMA sees
+            float mnew[NC];
 #pragma unroll
-            for (int i = 0; i < kAMaxQ / 2; ++i) {
-                if (i < ncol) {
-                    const int q = ch * ncol + i;
-                    uint32_t mk = red_max[q];
+            for (int i = 0; i < NC; ++i) {
+                const int q = 2 * i + ch;
+                const uint32_t a = max(red_max[q], red_max[kAMaxQ + q]);
+                const uint32_t c = max(red_max[2 * kAMaxQ + q], red_max[3 * kAMaxQ + q]);
+                mnew[i] = fmaxf(m_run[q], unkey(max(a, c)));
+            }
+            uint8_t *pbuf = ps + (size_t)b * (size_t)(2 * NQ * kAKeys * 2);
 #pragma unroll
-                    for (int w = 1; w < 4; ++w) mk = max(mk, red_max[w * kAMaxQ + q]);
-                    const float mnew = fmaxf(m_run[q], unkey(mk));
-                    const float e = s[i] == -INFINITY ? 0.f : expf(s[i] - mnew);
-                    const __nv_bfloat16 h = __float2bfloat16_rn(e);
-                    const float hf = __bfloat162float(h);
-                    const __nv_bfloat16 lo = __float2bfloat16_rn(e - hf);
-                    const uint32_t off = plain_off(q, key_local, 2048u);
-                    *reinterpret_cast<__nv_bfloat16 *>(phi + off) = h;
-                    *reinterpret_cast<__nv_bfloat16 *>(plo + off) = lo;
-                    float cs = hf + __bfloat162float(lo);
-#pragma unroll
-                    for (int o = 16; o >= 1; o >>= 1) cs += __shfl_xor_sync(0xFFFFFFFFu, cs, o);
-                    if (lane == 0) red_sum[qt * kAMaxQ + q] = cs;
-                }
+            for (int i = 0; i < NC; ++i) {
+                const int q = 2 * i + ch;
+                const float e = sv[i] == -INFINITY ? 0.f : expf(sv[i] - mnew[i]);
+                const __nv_bfloat16 h = __float2bfloat16_rn(e);
+                const __nv_bfloat16 lo = __float2bfloat16_rn(e - __bfloat162float(h));
+                *reinterpret_cast<__nv_bfloat16 *>(pbuf + plain_off(q, key_local, 2048u)) = h;
+                *reinterpret_cast<__nv_bfloat16 *>(pbuf + plain_off(NQ + q, key_local, 2048u)) = lo;
             }
             asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
             soft_sync();
             if (tid == 0) bar_arrive(su32(&p_full[b]));
-            if (tid < nq) {
+            if (tid < NQ) {
                 const int q = tid;
-                uint32_t mk = red_max[q];
-#pragma unroll
-                for (int w = 1; w < 4; ++w) mk = max(mk, red_max[w * kAMaxQ + q]);
-                const float mold = m_run[q], mnew = fmaxf(mold, unkey(mk));
-                const float a = mnew == -INFINITY ? 1.f : expf(mold - mnew);
-                const float lt = ((red_sum[q] + red_sum[kAMaxQ + q]) + red_sum[2 * kAMaxQ + q]) + red_sum[3 * kAMaxQ + q];
-                l_run[q] = fmaf(l_run[q], a, lt);
-                m_run[q] = mnew;
-                alpha[b * kAMaxQ + q] = a;
+                const uint32_t a = max(red_max[q], red_max[kAMaxQ + q]);
+                const uint32_t c = max(red_max[2 * kAMaxQ + q], red_max[3 * kAMaxQ + q]);
+                const float mold = m_run[q], mn = fmaxf(mold, unkey(max(a, c)));
+                const float al = mn == -INFINITY ? 1.f : expf(mold - mn);
+                m_run[q] = mn;
+                alpha[b * kAMaxQ + q] = al;
             }
             if (t >= 1) {
                 drain(t - 1);
@@ -520,9 +554,9 @@ __global__ void __launch_bounds__(kAThreads, 1) attn_chunk_kernel(const __grid_c
         if (ok) {
             const size_t cg = (size_t)chunk * kAHkv + g;
 #pragma unroll
-            for (int q = 0; q < kAMaxQ; ++q)
-                if (q < 8 * M) p.part_o[(cg * kAMaxQ + q) * kAD + dl] = oacc[q];
-            if (tid < 8 * M) {
+            for (int q = 0; q < NQ; ++q)
+                if (q < nreal) p.part_o[(cg * kAMaxQ + q) * kAD + dl] = oacc[q];
+            if (tid < nreal) {
                 p.part_ml[(cg * kAMaxQ + tid) * 2] = m_run[tid];
                 p.part_ml[(cg * kAMaxQ + tid) * 2 + 1] = l_run[tid];
             }
@@ -536,20 +570,37 @@ __global__ void __launch_bounds__(kAThreads, 1) attn_chunk_kernel(const __grid_c
 
 // Merge of a row's chunks, in chunk order: o = sum_j e^(m_j - M) O_j /
 // sum_j e^(m_j - M) l_j with M the largest chunk maximum.  One CTA per
-// (row, query head), thread = d.
+// (row, query head), thread = d.  The chunk maxima and weights go through
+// shared memory (all threads load them together), then each thread's loads
+// of its d from every chunk are independent and overlap.
+constexpr int kACombineChunks = kAMaxPos / kAChunk;
 __global__ void __launch_bounds__(kAD) attn_combine_kernel(const float *part_o, const float *part_ml, int pos0, float *o)
 {
+    __shared__ float wsh[kACombineChunks];
+    __shared__ float red[kAD / 32];
     const int m = blockIdx.x / kAHq, h = blockIdx.x % kAHq, g = h / kAGrp, q = kAGrp * m + h % kAGrp;
-    const int d = threadIdx.x;
-    const int J = (pos0 + m + 1 + kAChunk - 1) / kAChunk;
+    const int d = threadIdx.x, lane = d & 31, warp = d >> 5;
+    const int J = (pos0 + m + 1 + kAChunk - 1) / kAChunk;   // <= kACombineChunks (host check)
     float mx = -INFINITY;
-#pragma unroll 1
-    for (int j = 0; j < J; ++j) mx = fmaxf(mx, __ldg(part_ml + (((size_t)j * kAHkv + g) * kAMaxQ + q) * 2));
-    float lsum = 0.f, acc = 0.f;
-#pragma unroll 1
+    for (int j = d; j < J; j += kAD) {
+        const float v = __ldg(part_ml + (((size_t)j * kAHkv + g) * kAMaxQ + q) * 2);
+        wsh[j] = v;
+        mx = fmaxf(mx, v);
+    }
+#pragma unroll
+    for (int off = 16; off >= 1; off >>= 1) mx = fmaxf(mx, __shfl_xor_sync(0xFFFFFFFFu, mx, off));
+    if (lane == 0) red[warp] = mx;
+    __syncthreads();
+    mx = red[0];
+#pragma unroll
+    for (int w = 1; w < kAD / 32; ++w) mx = fmaxf(mx, red[w]);
+    for (int j = d; j < J; j += kAD) wsh[j] = expf(wsh[j] - mx);
+    __syncthreads();
+    float acc = 0.f, lsum = 0.f;
+#pragma unroll 8
     for (int j = 0; j < J; ++j) {
         const size_t c = ((size_t)j * kAHkv + g) * kAMaxQ + q;
-        const float w = expf(__ldg(part_ml + 2 * c) - mx);
+        const float w = wsh[j];
         lsum = fmaf(__ldg(part_ml + 2 * c + 1), w, lsum);
         acc = fmaf(__ldg(part_o + c * kAD + d), w, acc);
     }
@@ -582,6 +633,8 @@ PFN_cuTensorMapEncodeTiled_v12000 encode_fn()
 }
 
 }  // namespace
+
+int attn_max_positions() { return kAMaxPos; }
 
 size_t attn_workspace_bytes(int T_cap)
 {
@@ -634,10 +687,19 @@ int launch_attn(const uint16_t *q, const uint16_t *k, const uint16_t *vt, int T_
     cudaError_t e = cudaGetDevice(&dev);
     if (e != cudaSuccess || dev < 0 || dev >= 64) { note_cuda_error((int)e); return MOE_ERR_CUDA; }
     std::call_once(attr_once[dev], [&] {
-        e = cudaFuncSetAttribute(attn_chunk_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, kSmemMax);
+        const void *fns[4] = {(const void *)attn_chunk_kernel<16>, (const void *)attn_chunk_kernel<32>,
+                              (const void *)attn_chunk_kernel<48>, (const void *)attn_chunk_kernel<64>};
+        for (int i = 0; i < 4 && e == cudaSuccess; ++i)
+            e = cudaFuncSetAttribute(fns[i], cudaFuncAttributeMaxDynamicSharedMemorySize, kSmemMax);
     });
     if (e != cudaSuccess) { note_cuda_error((int)e); return MOE_ERR_CUDA; }
-    attn_chunk_kernel<<<dim3(nchunks, kAHkv), kAThreads, smem, stream>>>(P);
+    const dim3 grid(nchunks, kAHkv);
+    switch (P.nq) {
+    case 16: attn_chunk_kernel<16><<<grid, kAThreads, smem, stream>>>(P); break;
+    case 32: attn_chunk_kernel<32><<<grid, kAThreads, smem, stream>>>(P); break;
+    case 48: attn_chunk_kernel<48><<<grid, kAThreads, smem, stream>>>(P); break;
+    default: attn_chunk_kernel<64><<<grid, kAThreads, smem, stream>>>(P); break;
+    }
     note_launch();
     attn_combine_kernel<<<M * kAHq, kAD, 0, stream>>>(P.part_o, P.part_ml, pos0, o);
     note_launch();

@@ -175,6 +175,7 @@ int launch_qkv(const uint8_t *W, int rows, int K, int bits, const uint16_t *x, i
                long long timeout_ns, cudaStream_t stream);
 // split-K decode attention with grouped query heads (moe_attn.cu)
 size_t attn_workspace_bytes(int T_cap);
+int attn_max_positions();
 int launch_attn(const uint16_t *q, const uint16_t *k, const uint16_t *vt, int T_cap, int pos0, int M, float *o,
                 void *ws, int *err, long long timeout_ns, cudaStream_t stream);
 int launch_attn_append(const uint16_t *kn, const uint16_t *vn, int M, int pos0, uint16_t *kc, uint16_t *vtc, int T_cap,

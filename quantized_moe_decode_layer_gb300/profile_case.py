@@ -3,8 +3,11 @@ of the 35B-A3B shape (about 0.66 GB each) in one persistent launch at M rows,
 run `--forwards` times.  Prints one JSON line with the algorithmic bytes of
 one launch (from the experts the rows actually selected).  With --tc, the
 tensor-core grouped gate/up then runs on each layer's routing of the rows.
+With --attn T, instead: the decode attention (moe_attn_decode) over a cache
+of T positions at M rows, run `--forwards` times.
 
     python -m quantized_moe_decode_layer_gb300.profile_case --M 1 --layers 3
+    python -m quantized_moe_decode_layer_gb300.profile_case --attn 32768 --M 3
 """
 from __future__ import annotations
 
@@ -39,6 +42,26 @@ def tc_routing(layers, x, ws):
     return out
 
 
+def attn_case(a) -> None:
+    import torch
+    import synth
+    import quantized_moe_decode_layer_gb300 as moe
+    T, M = a.attn, a.M
+    q, k, vt = synth.make_attn(T, T, M, 5, device="cuda")
+    cache = moe.AttnCache(T, device="cuda")
+    cache.k.copy_(k)
+    cache.vt.copy_(vt)
+    del k, vt
+    out = torch.empty((M, 16, 256), dtype=torch.float32, device="cuda")
+    err = torch.zeros(1, dtype=torch.int32, device="cuda")
+    for _ in range(a.forwards):
+        cache.attend(q, T - M, out=out, err=err)
+    torch.cuda.synchronize()
+    assert int(err.item()) == 0
+    print(json.dumps({"case": "attn", "T": T, "M": M, "forwards": a.forwards,
+                      "bytes_per_call": T * 2 * 256 * 2 * 2 + M * 16 * 256 * 6}))
+
+
 def main() -> None:
     p = argparse.ArgumentParser()
     p.add_argument("--M", type=int, default=1)
@@ -48,7 +71,11 @@ def main() -> None:
     p.add_argument("--correlation", type=float, default=0.6)
     p.add_argument("--tc", action="store_true",
                    help="then run the tensor-core grouped gate/up (moe_gate_up_tc) on each layer's routing")
+    p.add_argument("--attn", type=int, default=0, help="run the decode attention over a cache of this many positions")
     a = p.parse_args()
+    if a.attn:
+        attn_case(a)
+        return
 
     import torch
     import synth

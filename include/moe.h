@@ -58,7 +58,8 @@ typedef enum moe_status {
     MOE_ERR_BUFFER_TOO_SMALL = 3, /* weight blob or workspace smaller than the *_size query */
     MOE_ERR_CUDA = 4,             /* a CUDA runtime call failed; see moe_last_cuda_error() */
     MOE_ERR_TIMEOUT = 5,          /* a device-side wait gave up (the kernel returned early) */
-    MOE_ERR_DEVICE = 6            /* a device-side check failed (bounds build) */
+    MOE_ERR_DEVICE = 6,           /* a device-side check failed (bounds build) */
+    MOE_ERR_NOT_RESIDENT = 7      /* a streamed layer's selected expert was not in its cache */
 } moe_status;
 
 /* Shape and storage of one layer. */
@@ -432,6 +433,75 @@ int moe_attn_decode(const uint16_t *q_dev, const uint16_t *k_cache_dev, const ui
  * Errors: INVALID_ARG, CUDA. */
 int moe_attn_append(const uint16_t *k_new_dev, const uint16_t *v_new_dev, int M, int pos0, uint16_t *k_cache_dev,
                     uint16_t *vt_cache_dev, int T_cap, moe_stream_t stream);
+
+/* ------------------------------------------------------------------------
+ * Streamed layers: the routed experts of a layer live in host memory (the
+ * Grace side of a GB300, over NVLink-C2C) and only the experts the router
+ * selects are copied into an HBM cache of n_slots expert slots, least
+ * recently used evicted first (flash-moe, "SSD Expert Streaming" and
+ * "Trust the OS": only the selected experts are loaded, an LRU cache keeps
+ * the popular ones; AiiStream Q3.6 article: the next layer's experts are
+ * predicted and loaded ahead; "Qwen3.5-397B on M5 Max": temporal expert
+ * prediction).  The router, norm weights and shared expert stay in HBM.
+ * A streamed layer decodes with the same kernel as a resident one and gives
+ * the same bits; it runs on the persistent path only (never grouped mode,
+ * and the tensor-core product calls refuse it).
+ *
+ * moe_streamed_size: device bytes of a streamed layer with n_slots slots
+ * (k <= n_slots <= E): the resident parts, the cache and the slot map.
+ * Errors: INVALID_ARG, UNSUPPORTED. */
+typedef struct moe_streamed moe_streamed;
+int moe_streamed_size(const moe_layer_desc *desc, int n_slots, size_t *dev_bytes);
+
+/* Makes a streamed layer from a packed one: the whole blob is copied to
+ * host_blob (host memory the caller allocated, pinned for asynchronous
+ * copies, at least moe_pack_size bytes, kept alive by the caller), the
+ * resident parts to dev_buf (256-byte aligned, moe_streamed_size bytes);
+ * the cache starts empty.  Synchronises `stream`; afterwards the packed
+ * layer and its device memory may be released.  Errors: INVALID_ARG,
+ * BUFFER_TOO_SMALL, CUDA. */
+int moe_streamed_create(const moe_layer *packed, void *host_blob, size_t host_bytes, void *dev_buf, size_t dev_bytes,
+                        int n_slots, moe_streamed **out, moe_stream_t stream);
+
+/* The layer handle to pass to moe_decode_layer / moe_router_topk /
+ * moe_stack_create.  A decode whose routing selects an expert without a
+ * cache slot reports MOE_ERR_NOT_RESIDENT (moe_stream_status) and its
+ * output is not defined. */
+const moe_layer *moe_streamed_layer(const moe_streamed *s);
+
+/* Makes experts expert_ids[0 .. n) (host array, repeats allowed) resident:
+ * the missing ones are copied from host memory on `stream` (two copies per
+ * expert: its gate/up units and its down rows), evicting the least
+ * recently used slots that hold none of the listed experts, then the slot
+ * map is updated on `stream`.  *fetched (may be NULL) = experts copied.
+ * Counts hits and misses.  Errors: INVALID_ARG (an id outside 0 .. E - 1),
+ * BUFFER_TOO_SMALL (more distinct ids than slots), CUDA. */
+int moe_streamed_prepare(moe_streamed *s, const int32_t *expert_ids, int n, moe_stream_t stream, int *fetched);
+
+/* Counters since creation: hits and misses of moe_streamed_prepare and of
+ * the routing in moe_streamed_forward, experts fetched and their bytes (also
+ * by prefetches), experts predicted for this layer and how many of the
+ * selected experts the prediction named.  Any pointer may be NULL. */
+int moe_streamed_stats(const moe_streamed *s, long long *hits, long long *misses, long long *fetched,
+                       long long *bytes, long long *predicted, long long *predicted_used);
+
+void moe_streamed_destroy(moe_streamed *s);
+
+/* One forward of M rows (M <= one persistent launch's rows) through L
+ * streamed layers of one shape, in the library's runtime: for each layer,
+ * route it on its input (moe_router_topk), wait for the routing on the
+ * host, make its selected experts resident, decode it (out_dev; layer l > 0
+ * reads and overwrites out_dev; the last layer also writes out_normed_dev
+ * when given).  With predict != 0, layer l + 1's router also runs on layer
+ * l's input, and the experts it names are copied into layer l + 1's cache
+ * on copy_stream while layer l is decoded (the copy waits for the last
+ * decode that read that cache; layer l + 1's decode waits for the copy).
+ * Kernels run on `stream` only.  route_dev: device scratch of at least
+ * 16 * M * k bytes.  Errors: as the calls above; UNSUPPORTED for M above
+ * one launch. */
+int moe_streamed_forward(moe_streamed *const *layers, int L, const uint16_t *x_dev, int M, uint16_t *out_dev,
+                         uint16_t *out_normed_dev, void *ws_dev, size_t ws_bytes, void *route_dev, size_t route_bytes,
+                         int predict, moe_stream_t stream, moe_stream_t copy_stream);
 
 /* Human-readable name of a status code (static string). */
 const char *moe_status_str(int status);

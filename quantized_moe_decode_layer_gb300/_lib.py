@@ -16,7 +16,7 @@ LIB_PATH = os.path.join(HERE, "libmoe_debug.so" if DEBUG_BOUNDS else "libmoe.so"
 
 MOE_OK = 0
 STATUS = {0: "MOE_OK", 1: "MOE_ERR_INVALID_ARG", 2: "MOE_ERR_UNSUPPORTED", 3: "MOE_ERR_BUFFER_TOO_SMALL",
-          4: "MOE_ERR_CUDA", 5: "MOE_ERR_TIMEOUT", 6: "MOE_ERR_DEVICE"}
+          4: "MOE_ERR_CUDA", 5: "MOE_ERR_TIMEOUT", 6: "MOE_ERR_DEVICE", 7: "MOE_ERR_NOT_RESIDENT"}
 T_ROUTER, T_SGATE, T_GATE, T_UP, T_DOWN, T_SHARED_GATE, T_SHARED_UP, T_SHARED_DOWN = range(8)
 
 # every symbol include/moe.h declares
@@ -26,6 +26,8 @@ SYMBOLS = ["moe_pack_size", "moe_pack_weights", "moe_layer_destroy", "moe_export
            "moe_decode_layer_noalloc", "moe_noalloc_status",
            "moe_qkv_pack_size", "moe_qkv_pack", "moe_qkv_forward", "moe_qkv_destroy",
            "moe_attn_workspace_size", "moe_attn_decode", "moe_attn_append",
+           "moe_streamed_size", "moe_streamed_create", "moe_streamed_layer", "moe_streamed_prepare",
+           "moe_streamed_stats", "moe_streamed_destroy", "moe_streamed_forward",
            "moe_stream_status", "moe_build_flags", "moe_debug_inject", "moe_debug_set", "moe_debug_trace", "moe_set_grouped", "moe_gate_up_tc", "moe_down_tc", "moe_status_str",
            "moe_last_cuda_error",
            "moe_selftest_host", "moe_launch_count"]
@@ -93,6 +95,13 @@ def lib():
             "moe_attn_workspace_size": (i, [i, C.POINTER(sz)]),
             "moe_attn_decode": (i, [vp, vp, vp, i, i, i, vp, vp, sz, vp, vp]),
             "moe_attn_append": (i, [vp, vp, i, i, vp, vp, i, vp]),
+            "moe_streamed_size": (i, [C.POINTER(LayerDesc), i, C.POINTER(sz)]),
+            "moe_streamed_create": (i, [vp, vp, sz, vp, sz, i, C.POINTER(vp), vp]),
+            "moe_streamed_layer": (vp, [vp]),
+            "moe_streamed_prepare": (i, [vp, vp, i, vp, C.POINTER(i)]),
+            "moe_streamed_stats": (i, [vp] + [C.POINTER(C.c_longlong)] * 6),
+            "moe_streamed_destroy": (None, [vp]),
+            "moe_streamed_forward": (i, [vp, i, vp, i, vp, vp, vp, sz, vp, sz, i, vp, vp]),
             "moe_qkv_destroy": (None, [vp]),
             "moe_stream_status": (i, [vp, sz, vp]),
             "moe_debug_set": (i, [i, C.c_longlong]),

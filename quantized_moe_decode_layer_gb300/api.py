@@ -373,6 +373,72 @@ class QKV:
             pass
 
 
+class StreamedLayer:
+    """A layer whose routed experts live in pinned host memory, with an HBM
+    cache of n_slots experts (moe_streamed_*).  Built from a packed Layer,
+    which may be dropped afterwards; usable wherever a Layer is (decode_layer,
+    router_topk, Stack), and by streamed_forward."""
+
+    def __init__(self, layer: Layer, n_slots: int, stream=None):
+        self.desc = layer.desc
+        n = C.c_size_t()
+        check("moe_streamed_size", lib().moe_streamed_size(C.byref(self.desc), n_slots, C.byref(n)))
+        self.host = torch.empty(layer.nbytes, dtype=torch.uint8, pin_memory=True)
+        self.dev = torch.empty(n.value, dtype=torch.uint8, device=layer.blob.device)
+        h = C.c_void_p()
+        check("moe_streamed_create", lib().moe_streamed_create(layer.handle, self.host.data_ptr(), layer.nbytes,
+                                                               _ptr(self.dev), n.value, n_slots, C.byref(h),
+                                                               _stream(stream)))
+        self.sh = h
+        self.handle = C.c_void_p(lib().moe_streamed_layer(h))
+        self.n_slots = n_slots
+        self.nbytes = n.value
+
+    def prepare(self, expert_ids, stream=None) -> int:
+        """Make the listed experts resident; returns how many were copied."""
+        ids = (C.c_int32 * len(expert_ids))(*[int(e) for e in expert_ids])
+        f = C.c_int()
+        check("moe_streamed_prepare", lib().moe_streamed_prepare(self.sh, ids, len(expert_ids), _stream(stream),
+                                                                 C.byref(f)))
+        return f.value
+
+    def stats(self) -> dict:
+        v = [C.c_longlong() for _ in range(6)]
+        check("moe_streamed_stats", lib().moe_streamed_stats(self.sh, *[C.byref(x) for x in v]))
+        return dict(zip(("hits", "misses", "fetched", "bytes", "predicted", "predicted_used"), (x.value for x in v)))
+
+    def __del__(self):
+        try:
+            if getattr(self, "sh", None):
+                lib().moe_streamed_destroy(self.sh)
+                self.sh = None
+        except Exception:
+            pass
+
+
+def streamed_forward(layers, x: torch.Tensor, ws: Workspace, out=None, normed: bool = False, predict: bool = True,
+                     stream=None, copy_stream=None):
+    """One forward of x bf16 [M, H] through StreamedLayers (moe_streamed_forward)."""
+    H = layers[0].desc.H
+    _need(x, "x", torch.bfloat16, (None, H))
+    M = x.shape[0]
+    k = layers[0].desc.k
+    if out is None:
+        out = torch.empty_like(x)
+    _need(out, "out", torch.bfloat16, (M, H))
+    on = torch.empty_like(x) if normed else None
+    route = torch.empty(16 * M * k, dtype=torch.uint8, device=x.device)
+    if predict and copy_stream is None:
+        copy_stream = torch.cuda.Stream(device=x.device)
+    arr = (C.c_void_p * len(layers))(*[l.sh.value for l in layers])
+    check("moe_streamed_forward",
+          lib().moe_streamed_forward(arr, len(layers), _ptr(_bits16(x)), M, _ptr(_bits16(out)),
+                                     _ptr(_bits16(on)) if on is not None else None, ws.ptr, ws.nbytes,
+                                     _ptr(route), route.numel(), 1 if predict else 0, _stream(stream),
+                                     copy_stream.cuda_stream if copy_stream is not None else None))
+    return (out, on) if normed else out
+
+
 class AttnCache:
     """A bf16 key/value cache of the decode attention (moe_attn_*): keys
     [2, T_cap, 256] and values stored transposed [2, 256, T_cap], zeroed, with

@@ -42,6 +42,7 @@ int check_status_word(void *ws)
                                cudaMemcpyDeviceToHost);
     if (e != cudaSuccess) { note_cuda_error((int)e); return MOE_ERR_CUDA; }
     if (st & kStatusTimeout) return MOE_ERR_TIMEOUT;
+    if (st & kStatusNotResident) return MOE_ERR_NOT_RESIDENT;
     if (st) return MOE_ERR_DEVICE;
     return MOE_OK;
 }
@@ -411,7 +412,9 @@ int decode_layer_impl(const moe_layer *layer, const uint16_t *x_dev, int M, uint
     int R;
     int rc = prepare(layer, M, ws_dev, ws_bytes, kp, R);
     if (rc) return rc;
-    if (allow_grouped && use_grouped(M, R))   // grouped mode (moe_set_grouped)
+    // grouped mode (moe_set_grouped); never for a streamed layer, whose
+    // experts are reached through its cache's slot map
+    if (allow_grouped && !layer->ptrs.slot_of && use_grouped(M, R))
         return grouped_forward(&layer, 1, x_dev, M, out_dev, out_normed_dev, ws_dev, ws_bytes, g_timeout_ns,
                                reinterpret_cast<cudaStream_t>(stream));
     kp.mode = kModeLayers;
@@ -478,7 +481,9 @@ int moe_stack_forward(moe_stack *stack, const uint16_t *x_dev, int M, uint16_t *
     int R;
     int rc = prepare(stack->layers[0], M, ws_dev, ws_bytes, kp, R);
     if (rc) return rc;
-    if (use_grouped(M, R))   // grouped mode, as in moe_decode_layer
+    bool streamed = false;
+    for (int l = 0; l < stack->L; ++l) streamed = streamed || stack->layers[l]->ptrs.slot_of != nullptr;
+    if (!streamed && use_grouped(M, R))   // grouped mode, as in moe_decode_layer
         return grouped_forward(stack->layers, stack->L, x_dev, M, out_dev, out_normed_dev, ws_dev, ws_bytes,
                                g_timeout_ns, reinterpret_cast<cudaStream_t>(stream));
     kp.mode = kModeLayers;
@@ -651,6 +656,7 @@ int moe_gate_up_tc(const moe_layer *layer, const float *hn_dev, int M, const int
 {
     if (!layer || !hn_dev || !experts_dev || !masks_dev || !act_dev || !err_dev || M < 1 || U < 0)
         return MOE_ERR_INVALID_ARG;
+    if (layer->ptrs.slot_of) return MOE_ERR_UNSUPPORTED;   // a streamed layer's experts are not at their ids
     if (M > 32 || (2 * layer->geo.I) % 128 != 0 || !bits_ok(layer->geo.rb)) return MOE_ERR_UNSUPPORTED;
     if (U == 0) return MOE_OK;
     return launch_gate_up_tc(*layer, hn_dev, M, experts_dev, masks_dev, U, act_dev, err_dev, g_timeout_ns,
@@ -662,6 +668,7 @@ int moe_down_tc(const moe_layer *layer, const float *act_dev, int M, const int32
 {
     if (!layer || !act_dev || !experts_dev || !masks_dev || !y_dev || !err_dev || M < 1 || U < 0)
         return MOE_ERR_INVALID_ARG;
+    if (layer->ptrs.slot_of) return MOE_ERR_UNSUPPORTED;
     if (M > 32 || layer->geo.H % 128 != 0 || !bits_ok(layer->geo.rb)) return MOE_ERR_UNSUPPORTED;
     if (U == 0) return MOE_OK;
     return launch_down_tc(*layer, act_dev, M, experts_dev, masks_dev, U, y_dev, err_dev, g_timeout_ns,
@@ -766,6 +773,7 @@ const char *moe_status_str(int status)
     case MOE_ERR_CUDA: return "MOE_ERR_CUDA";
     case MOE_ERR_TIMEOUT: return "MOE_ERR_TIMEOUT";
     case MOE_ERR_DEVICE: return "MOE_ERR_DEVICE";
+    case MOE_ERR_NOT_RESIDENT: return "MOE_ERR_NOT_RESIDENT";
     default: return "MOE_ERR_UNKNOWN";
     }
 }

@@ -28,6 +28,7 @@ constexpr int kSmemMax = 232448;    // dynamic shared memory per CTA on sm_100-c
 // Status word bits (workspace control block).
 constexpr int kStatusTimeout = 1;
 constexpr int kStatusBounds = 2;
+constexpr int kStatusNotResident = 4;   // a selected expert had no cache slot (streamed layers)
 
 __host__ __device__ constexpr size_t align_up(size_t v, size_t a) { return (v + a - 1) / a * a; }
 
@@ -64,6 +65,11 @@ struct LayerPtrs {
     const uint8_t *sdown;    // H rows
     const uint16_t *gamma;
     const uint16_t *gamma_next;  // NULL when absent
+    // Streamed layers (moe_streamed_*): the routed experts live in host
+    // memory and gu / down are an HBM cache of n_slots experts; slot_of[e]
+    // is expert e's slot (or -1).  NULL for a resident layer.
+    const int32_t *slot_of;
+    int n_slots;
 };
 
 // Workspace layout (offsets from the workspace base).

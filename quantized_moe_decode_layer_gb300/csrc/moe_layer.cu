@@ -1585,6 +1585,23 @@ __device__ void route(const KParams &kp, const Sh &sh, const uint64_t *logits, i
                 sh.row_pair[m * kMaxK + j] = sh.slot_rowbase[s] + __popc(sh.slot_mask[s] & ((1u << m) - 1u));
             }
     }
+    // a streamed layer's experts are read from its HBM cache: the slot table
+    // carries their cache slots in place of their ids (the ids keep ordering
+    // the combine through row_pair); an expert with no slot is reported and
+    // slot 0 read instead, so every access stays inside the cache
+    const LayerPtrs &Lr = kp.layer[l];
+    if (Lr.slot_of && kp.mode == kModeLayers) {
+#pragma unroll 1
+        for (int s = lane; s < U; s += 32) {
+            int c = __ldg(Lr.slot_of + sh.slot_e[s]);
+            if ((unsigned)c >= (unsigned)Lr.n_slots) {
+                atomicOr(&sh.ctrl->status, kStatusNotResident);
+                c = 0;
+            }
+            sh.slot_e[s] = c;
+        }
+        __syncwarp();
+    }
     if (kp.mode == kModeRouter && blockIdx.x == 0) {
 #pragma unroll 1
         for (int m = 0; m < M; ++m)
@@ -1682,6 +1699,13 @@ __device__ __forceinline__ void sched_p1b(const KParams &kp, const Sh &sh, const
     }
 }
 
+// Expert blocks in a layer's gu / down regions: E, or a streamed layer's
+// cache slots.
+__device__ __forceinline__ int expert_blocks(const KParams &kp, const LayerPtrs &Lp)
+{
+    return Lp.slot_of ? Lp.n_slots : kp.g.E;
+}
+
 // The P2 stages of this CTA for U distinct experts: f(slot, first unit,
 // units), in ring order.
 template <typename F>
@@ -1710,7 +1734,7 @@ __device__ __forceinline__ void sched_p2(const KParams &kp, const Sh &sh, const 
 {
     const int ub = 2 * kp.g.g_bytes;
     p2_units(kp, sh, sh.flags[1], [&](int s, int j, int cnt) {
-        f(Lp.gu + ((size_t)chk(sh, sh.slot_e[s], kp.g.E, 6) * kp.g.I + j) * ub, cnt * ub, s, j, cnt);
+        f(Lp.gu + ((size_t)chk(sh, sh.slot_e[s], expert_blocks(kp, Lp), 6) * kp.g.I + j) * ub, cnt * ub, s, j, cnt);
     });
 }
 
@@ -1727,7 +1751,7 @@ __device__ __forceinline__ void sched_p3(const KParams &kp, const Sh &sh, const 
     const int cd = max(1, min(sh.S / g.d_bytes, nh));
 #pragma unroll 1
     for (int s = 0; s < U; ++s) {
-        const int e = chk(sh, sh.slot_e[s], g.E, 8);
+        const int e = chk(sh, sh.slot_e[s], expert_blocks(kp, Lp), 8);
 #pragma unroll 1
         for (int r = 0; r < nh; r += cd) {
             const int n = min(cd, nh - r);
@@ -1866,7 +1890,8 @@ __device__ __forceinline__ void producer(const KParams &kp, const Sh &sh, int la
             if (fast) {
                 const int ub = 2 * kp.g.g_bytes;
                 const uint8_t *src =
-                    lane < nst ? Lp.gu + ((size_t)chk(sh, sh.slot_e[my_s], kp.g.E, 7) * kp.g.I + my_j) * ub : nullptr;
+                    lane < nst ? Lp.gu + ((size_t)chk(sh, sh.slot_e[my_s], expert_blocks(kp, Lp), 7) * kp.g.I + my_j) * ub
+                               : nullptr;
                 if (!issue_batch(sh, lane < nst, mine.slot, mine.par, mine.reuse, src, my_n * ub)) break;
 #pragma unroll 1
                 for (int i = 0; i < nst; ++i) cursor_next(c, sh.NS);

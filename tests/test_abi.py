@@ -191,3 +191,24 @@ def test_attention_sizes_and_argument_errors():
     assert L.moe_attn_decode(fake, fake, fake, 64, 0, 1, fake, fake, 16, err, None) == 3
     assert L.moe_attn_append(fake, fake, 0, 0, fake, fake, 64, None) == 1
     assert L.moe_attn_append(fake, fake, 2, 63, fake, fake, 64, None) == 1
+
+
+def test_streamed_sizes_and_argument_errors():
+    """A streamed layer's device bytes: the resident parts (router, gammas,
+    shared expert) plus n_slots experts plus the slot map, 256-aligned; slot
+    counts below k or above E and null handles are refused."""
+    L = moe.lib()
+    d = moe.desc_from_shape(synth.A35B)
+    n16, n8 = C.c_size_t(), C.c_size_t()
+    assert L.moe_streamed_size(C.byref(d), 16, C.byref(n16)) == 0
+    assert L.moe_streamed_size(C.byref(d), 8, C.byref(n8)) == 0
+    assert n16.value - n8.value == 8 * 2_555_904             # eight more experts of 2,555,904 bytes
+    assert n16.value < moe.pack_size(d)
+    assert L.moe_streamed_size(C.byref(d), 7, C.byref(n8)) == 1      # fewer slots than k
+    assert L.moe_streamed_size(C.byref(d), 257, C.byref(n8)) == 1    # more slots than experts
+    h = C.c_void_p()
+    assert L.moe_streamed_create(None, 1, 1, 1, 1, 16, C.byref(h), None) == 1
+    assert L.moe_streamed_prepare(None, None, 0, None, None) == 1
+    assert L.moe_streamed_stats(None, None, None, None, None, None, None) == 1
+    assert L.moe_streamed_forward(None, 1, None, 1, None, None, None, 0, None, 0, 0, None, None) == 1
+    assert L.moe_streamed_layer(None) is None

@@ -406,6 +406,64 @@ def attn_measure(dev, peaks, warmup):
     return res
 
 
+def streamed_measure(shape, dev, peaks, n_layers=8, n_slots=16, tokens=24, warm_tokens=4, corr=0.6):
+    """moe_streamed_forward over n_layers streamed layers (experts in pinned
+    host memory, an HBM cache of n_slots experts per layer) for a sequence of
+    token rows, x_{t+1} = a x_t + sqrt(1 - a^2) n_t (a = corr), with and
+    without next-layer prediction.  Reports wall time per layer (the runtime
+    waits for each layer's routing on the host), cache hits, the bytes
+    fetched over the host link and their rate, and the share of selected
+    experts the prediction named."""
+    import math
+    import torch
+    import quantized_moe_decode_layer_gb300 as moe
+    import synth
+    desc = moe.desc_from_shape(shape)
+    res = {"layers": n_layers, "slots_per_layer": n_slots, "tokens": tokens, "token_correlation": corr,
+           "host_blob_GB": None}
+    g = torch.Generator().manual_seed(123)
+    xs = [torch.randn(shape.H, generator=g)]
+    for _ in range(warm_tokens + tokens - 1):
+        xs.append(corr * xs[-1] + math.sqrt(1 - corr * corr) * torch.randn(shape.H, generator=g))
+    zc = synth.zipf_component(shape).float()
+    xs = [(x + zc).to(torch.bfloat16).view(1, -1).to(dev) for x in xs]
+    ws = moe.Workspace(desc, 1)
+    cs = torch.cuda.Stream()
+    for predict in (False, True):
+        st = []
+        for l in range(n_layers):
+            lay = moe.Layer(desc, moe.layer_src_from_synth(synth.make_layer(shape, 5000 + l, device=dev)))
+            st.append(moe.StreamedLayer(lay, n_slots=n_slots))
+            del lay
+        torch.cuda.synchronize()
+        torch.cuda.empty_cache()
+        res["host_blob_GB"] = round(sum(s.host.numel() for s in st) / 1e9, 2)
+        out = torch.empty_like(xs[0])
+        for t in range(warm_tokens):
+            moe.streamed_forward(st, xs[t], ws, out=out, predict=predict, copy_stream=cs)
+        torch.cuda.synchronize()
+        before = [s.stats() for s in st]
+        t0 = time.perf_counter()
+        for t in range(warm_tokens, warm_tokens + tokens):
+            moe.streamed_forward(st, xs[t], ws, out=out, predict=predict, copy_stream=cs)
+        torch.cuda.synchronize()
+        dt = time.perf_counter() - t0
+        assert ws.status() == 0
+        after = [s.stats() for s in st]
+        d = {k: sum(a[k] - b[k] for a, b in zip(after, before)) for k in after[0]}
+        sel = d["hits"] + d["misses"]
+        res["predict" if predict else "lru_only"] = {
+            "us_per_layer": round(dt / (tokens * n_layers) * 1e6, 2),
+            "tokens_per_s": round(tokens / dt, 1),
+            "hit_rate": round(d["hits"] / max(1, sel), 4),
+            "fetched_experts_per_token": round(d["fetched"] / tokens, 2),
+            "fetched_GB_per_s": round(d["bytes"] / dt / 1e9, 2),
+            "prediction_named": round(d["predicted_used"] / max(1, sel), 4) if predict else None}
+        del st
+        torch.cuda.empty_cache()
+    return res
+
+
 def run_ours(args):
     import numpy as np
     import torch
@@ -548,6 +606,11 @@ def run_ours(args):
     if not args.no_m4:
         attn = attn_measure(dev, peaks, args.warmup)
 
+    # streamed layers: experts in host memory behind an HBM cache
+    streamed = None
+    if not args.no_m4:
+        streamed = streamed_measure(shape, dev, peaks)
+
     # the 397B-shaped layer at M=1: a stack over 15 distinct layer sets (55 GB)
     b397 = None
     if not args.no_m4:
@@ -603,7 +666,7 @@ def run_ours(args):
                        "parallelism": f"replicas x{world}"},
             "us_per_layer": round(us_layer, 3), "fraction_of_8TBs": round(value / world / 8000.0, 4),
             "single_layer_call_us": single, "m4": m4, "sweep": sweep, "tc_gate_up": tc, "b397": b397, "qkv": qkv,
-            "attn": attn,
+            "attn": attn, "streamed": streamed,
             "roofline": roof, "e2e": e2e,
             "gpu_launches": launches, "launches_per_step": launches / args.steps, "clocks": clocks,
             "cpu_baseline": cpu,

@@ -16,9 +16,12 @@
 //
 // The host side here keeps, per layer, the slot of every expert (a host
 // mirror of the device slot map), the expert held by every slot and a use
-// stamp per slot (least recently used evicted first), and copies missing
-// experts with one host-to-device copy for the gate/up units and one for
-// the down rows (each expert's rows are contiguous in the packed blob).
+// stamp per slot (least recently used evicted first), and fetches missing
+// experts (each expert's gate/up units and its down rows are contiguous in
+// the packed blob): with pinned host memory, one gather kernel reads them
+// all over the host link (about 200 GB/s measured on GB300, against about
+// 150 for copy-engine copies of expert-sized pieces); otherwise one copy per
+// piece.
 // moe_streamed_forward runs a token through a stack of such layers: route
 // layer l, copy its missing experts, decode it; with prediction, layer
 // l + 1's router also runs on layer l's input, and the experts it names are
@@ -39,7 +42,8 @@
 struct moe_streamed {
     moe_layer layer;                 // resident parts and cache in dev_buf; ptrs.slot_of set
     const uint8_t *host;             // the whole packed blob, host memory
-    size_t off_cache_gu, off_cache_down, off_shared, off_map;
+    size_t off_cache_gu, off_cache_down, off_shared, off_map, off_jobs;
+    bool host_mapped;                // the device can read `host` directly (pinned host memory)
     int n_slots;
     int32_t *slot_of_dev;
     std::vector<int32_t> slot_of;    // expert -> slot, or -1
@@ -56,8 +60,39 @@ namespace moe {
 namespace {
 
 struct StreamedLayout {
-    size_t cache_gu, cache_down, shared, map, total;
+    size_t cache_gu, cache_down, shared, map, jobs, total;
 };
+
+// One copy of the gather kernel: n16 16-byte words from src (host memory
+// the device can read) to dst (device memory).
+struct CopyJob {
+    const uint4 *src;
+    uint4 *dst;
+    unsigned long long n16;
+    unsigned long long pad;
+};
+constexpr int kGatherCtasPerJob = 16;
+
+// The experts' rows from host memory into their cache slots: CTA (x, j)
+// takes every gridDim.x-th stretch of job j, four 16-byte loads in flight
+// per thread (the host link is latency-bound otherwise); loads bypass L1.
+__global__ void __launch_bounds__(256) gather_kernel(const CopyJob *jobs)
+{
+    const CopyJob j = jobs[blockIdx.y];
+    const unsigned long long stride = (unsigned long long)gridDim.x * blockDim.x;
+    unsigned long long i = (unsigned long long)blockIdx.x * blockDim.x + threadIdx.x;
+#pragma unroll 1
+    for (; i + 3 * stride < j.n16; i += 4 * stride) {
+        const uint4 a = __ldcs(j.src + i), b = __ldcs(j.src + i + stride), c = __ldcs(j.src + i + 2 * stride),
+                    d = __ldcs(j.src + i + 3 * stride);
+        j.dst[i] = a;
+        j.dst[i + stride] = b;
+        j.dst[i + 2 * stride] = c;
+        j.dst[i + 3 * stride] = d;
+    }
+#pragma unroll 1
+    for (; i < j.n16; i += stride) j.dst[i] = __ldcs(j.src + i);
+}
 
 StreamedLayout streamed_layout(const Geo &g, int n_slots)
 {
@@ -71,6 +106,8 @@ StreamedLayout streamed_layout(const Geo &g, int n_slots)
     o = align_up(o + (g.total - g.off_sgu), 256);
     s.map = o;
     o = align_up(o + (size_t)g.E * 4, 256);
+    s.jobs = o;
+    o = align_up(o + (size_t)2 * n_slots * sizeof(CopyJob), 256);
     s.total = o;
     return s;
 }
@@ -106,6 +143,8 @@ int make_resident(moe_streamed *s, const int32_t *ids, int n, cudaStream_t st, b
         if (s->slot_of[e] >= 0) s->stamp[s->slot_of[e]] = now;
     int fetched = 0;
     bool changed = false;
+    std::vector<CopyJob> jobs;
+    uint8_t *dev = s->layer.base;
     for (int e : want) {
         if (s->slot_of[e] >= 0) {
             if (count) ++s->hits;
@@ -117,15 +156,18 @@ int make_resident(moe_streamed *s, const int32_t *ids, int n, cudaStream_t st, b
             if (s->stamp[c] != now && (victim < 0 || s->stamp[c] < s->stamp[victim])) victim = c;
         if (victim < 0) return MOE_ERR_BUFFER_TOO_SMALL;
         if (s->owner[victim] >= 0) s->slot_of[s->owner[victim]] = -1;
-        uint8_t *dev = s->layer.base;
-        cudaError_t err = cudaMemcpyAsync(dev + s->off_cache_gu + (size_t)victim * expert_gu_bytes(g),
-                                          s->host + g.off_gu + (size_t)e * expert_gu_bytes(g), expert_gu_bytes(g),
-                                          cudaMemcpyHostToDevice, st);
-        if (err == cudaSuccess)
-            err = cudaMemcpyAsync(dev + s->off_cache_down + (size_t)victim * expert_down_bytes(g),
-                                  s->host + g.off_down + (size_t)e * expert_down_bytes(g), expert_down_bytes(g),
-                                  cudaMemcpyHostToDevice, st);
-        if (err != cudaSuccess) return cuda_fail(err);
+        uint8_t *dgu = dev + s->off_cache_gu + (size_t)victim * expert_gu_bytes(g);
+        uint8_t *ddn = dev + s->off_cache_down + (size_t)victim * expert_down_bytes(g);
+        const uint8_t *hgu = s->host + g.off_gu + (size_t)e * expert_gu_bytes(g);
+        const uint8_t *hdn = s->host + g.off_down + (size_t)e * expert_down_bytes(g);
+        if (s->host_mapped) {
+            jobs.push_back({reinterpret_cast<const uint4 *>(hgu), reinterpret_cast<uint4 *>(dgu), expert_gu_bytes(g) / 16, 0});
+            jobs.push_back({reinterpret_cast<const uint4 *>(hdn), reinterpret_cast<uint4 *>(ddn), expert_down_bytes(g) / 16, 0});
+        } else {
+            cudaError_t err = cudaMemcpyAsync(dgu, hgu, expert_gu_bytes(g), cudaMemcpyHostToDevice, st);
+            if (err == cudaSuccess) err = cudaMemcpyAsync(ddn, hdn, expert_down_bytes(g), cudaMemcpyHostToDevice, st);
+            if (err != cudaSuccess) return cuda_fail(err);
+        }
         s->owner[victim] = e;
         s->slot_of[e] = victim;
         s->stamp[victim] = now;
@@ -133,6 +175,16 @@ int make_resident(moe_streamed *s, const int32_t *ids, int n, cudaStream_t st, b
         ++s->fetched;
         ++fetched;
         changed = true;
+    }
+    if (!jobs.empty()) {
+        // one launch reads every missing expert over the host link (the job
+        // table's pageable source is staged before the call returns)
+        CopyJob *jd = reinterpret_cast<CopyJob *>(dev + s->off_jobs);
+        cudaError_t err = cudaMemcpyAsync(jd, jobs.data(), jobs.size() * sizeof(CopyJob), cudaMemcpyHostToDevice, st);
+        if (err != cudaSuccess) return cuda_fail(err);
+        gather_kernel<<<dim3(kGatherCtasPerJob, (unsigned)jobs.size()), 256, 0, st>>>(jd);
+        note_launch();
+        if ((err = cudaGetLastError()) != cudaSuccess) return cuda_fail(err);
     }
     if (changed) {
         // pageable source: the runtime stages it before returning, so the
@@ -183,7 +235,16 @@ int moe_streamed_create(const moe_layer *packed, void *host_blob, size_t host_by
     s->off_cache_down = sl.cache_down;
     s->off_shared = sl.shared;
     s->off_map = sl.map;
+    s->off_jobs = sl.jobs;
     s->n_slots = n_slots;
+    {
+        // pinned (or registered) host memory is read by the gather kernel;
+        // any other host memory goes through copies
+        cudaPointerAttributes pa;
+        s->host_mapped = cudaPointerGetAttributes(&pa, host_blob) == cudaSuccess && pa.type == cudaMemoryTypeHost &&
+                         pa.devicePointer == host_blob && (reinterpret_cast<uintptr_t>(host_blob) & 15) == 0;
+        cudaGetLastError();
+    }
     s->slot_of.assign(g.E, -1);
     s->owner.assign(n_slots, -1);
     s->stamp.assign(n_slots, 0);

@@ -195,14 +195,16 @@ def test_attention_sizes_and_argument_errors():
 
 def test_streamed_sizes_and_argument_errors():
     """A streamed layer's device bytes: the resident parts (router, gammas,
-    shared expert) plus n_slots experts plus the slot map, 256-aligned; slot
+    shared expert) plus n_slots experts plus the slot map and a table of two
+    fetch jobs (32 bytes each) per slot, 256-aligned; slot
     counts below k or above E and null handles are refused."""
     L = moe.lib()
     d = moe.desc_from_shape(synth.A35B)
     n16, n8 = C.c_size_t(), C.c_size_t()
     assert L.moe_streamed_size(C.byref(d), 16, C.byref(n16)) == 0
     assert L.moe_streamed_size(C.byref(d), 8, C.byref(n8)) == 0
-    assert n16.value - n8.value == 8 * 2_555_904             # eight more experts of 2,555,904 bytes
+    # eight more experts of 2,555,904 bytes, and 8 more 512-byte pairs of gather jobs
+    assert n16.value - n8.value == 8 * 2_555_904 + 512
     assert n16.value < moe.pack_size(d)
     assert L.moe_streamed_size(C.byref(d), 7, C.byref(n8)) == 1      # fewer slots than k
     assert L.moe_streamed_size(C.byref(d), 257, C.byref(n8)) == 1    # more slots than experts

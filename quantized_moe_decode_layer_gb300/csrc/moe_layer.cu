@@ -1327,17 +1327,24 @@ __device__ void build_hn(const KParams &kp, const Sh &sh, const void *x, unsigne
                     }
                 }
         }
+        // the warp's sums of the router dots (the tree of warp_sum) and the
+        // group sums (8 consecutive items make a group), all reductions'
+        // levels interleaved with no branch between them so that the
+        // independent shuffles overlap; rows past nr add zeros
 #pragma unroll
-        for (int r = 0; r < kFusedRouterRows; ++r)
-            if (r < nr) {
-                const float v = warp_sum(rp[r]);
-                const int wfirst = it - lane;
-                if (lane == 0 && wfirst < total) sh.rred[((wfirst >> lpr) * kFusedRouterRows + r) * NCW + warp] += v;
+        for (int o = 16; o >= 1; o >>= 1) {
+#pragma unroll
+            for (int r = 0; r < kFusedRouterRows; ++r) rp[r] += __shfl_xor_sync(FULLMASK, rp[r], o);
+            if (o <= 4) gs += __shfl_xor_sync(FULLMASK, gs, o);
+        }
+        {
+            const int wfirst = it - lane;
+            if (lane == 0 && wfirst < total) {
+#pragma unroll
+                for (int r = 0; r < kFusedRouterRows; ++r)
+                    if (r < nr) sh.rred[((wfirst >> lpr) * kFusedRouterRows + r) * NCW + warp] += rp[r];
             }
-        // 8 consecutive items make a group
-        gs += __shfl_xor_sync(FULLMASK, gs, 4);
-        gs += __shfl_xor_sync(FULLMASK, gs, 2);
-        gs += __shfl_xor_sync(FULLMASK, gs, 1);
+        }
         if (it < total && (it & 7) == 0) {
             const int m = it >> lpr, c = it & (per_row - 1);
             sh.xsum[m * G + (c >> 3)] = gs;
@@ -1359,7 +1366,8 @@ template <typename F>
 __device__ __forceinline__ void stage_acts(const Sh &sh, int n, int K, int tid, int nt, unsigned tag, F &&src)
 {
     const int per = K / 4, lgp = ilog2(per), G = K / kGroup, total = n * per;
-    auto item = [&](int it, const uint32_t (&u)[4]) {
+    // an item's 4 inputs into the staging buffer; returns their sum
+    auto item = [&](int it, const uint32_t (&u)[4]) -> float {
         float gs = 0.f;
         if (it < total) {
             const int p = it >> lgp, c = it & (per - 1);
@@ -1369,12 +1377,7 @@ __device__ __forceinline__ void stage_acts(const Sh &sh, int n, int K, int tid, 
             sh.act[(size_t)p * per + (c & 15) * G + (c >> 4)] =
                 make_float4(v.x * kXScale, v.y * kXScale, v.z * kXScale, v.w * kXScale);
         }
-#pragma unroll
-        for (int o = 8; o >= 1; o >>= 1) gs += __shfl_xor_sync(FULLMASK, gs, o);
-        if (it < total && (it & 15) == 0) {
-            const int p = it >> lgp, c = it & (per - 1);
-            sh.asum[p * G + (c >> 4)] = gs;
-        }
+        return gs;
     };
     // four items per thread and round, all loads in flight before any is used
     constexpr int NI = 4;
@@ -1388,9 +1391,20 @@ __device__ __forceinline__ void stage_acts(const Sh &sh, int n, int K, int tid, 
         }
         uint32_t a[NI][4];
         poll_items<NI>(sh, p, tag, 41, a);
+        // group sums (16 consecutive items make a group), the items'
+        // reductions interleaved
+        float gs[NI];
 #pragma unroll
-        for (int n = 0; n < NI; ++n)
-            if (n == 0 || base + n * nt < total) item(base + tid + n * nt, a[n]);
+        for (int n = 0; n < NI; ++n) gs[n] = item(base + tid + n * nt, a[n]);
+#pragma unroll
+        for (int o = 8; o >= 1; o >>= 1)
+#pragma unroll
+            for (int n = 0; n < NI; ++n) gs[n] += __shfl_xor_sync(FULLMASK, gs[n], o);
+#pragma unroll
+        for (int n = 0; n < NI; ++n) {
+            const int it = base + tid + n * nt;
+            if (it < total && (it & 15) == 0) sh.asum[(it >> lgp) * G + ((it & (per - 1)) >> 4)] = gs[n];
+        }
     }
 }
 

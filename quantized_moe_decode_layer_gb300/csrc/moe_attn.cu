@@ -36,12 +36,14 @@
 //   - eight softmax warps read the score block (thread = key, every other
 //     query column each, all columns' steps interleaved), mask keys past each row's position, take the
 //     tile's column maxima (redux.sync on order-preserving keys) and the new
-//     running maxima, and write exp(s - max) as bf16 halves into shared
-//     memory for the MMA, which also multiplies them by a tile of ones: the
-//     column sums of exactly the weights it used; then they take the
+//     running maxima, write exp(s - max) as bf16 halves into shared memory
+//     for the MMA and sum exactly those halves per column (all columns'
+//     reductions interleaved, no branch between them); then they take the
 //     previous tile's output block into fp32 registers (thread = one d of
-//     one half) and its column sums into the running sums, both rescaled by
-//     exp(old max - new max) (online softmax).
+//     one half), rescaled by exp(old max - new max) (online softmax).
+//     (A tile of ones times the weights on the tensor core gave the column
+//     sums too; it cost more in MMA instructions, the pipe that bounds a
+//     tile, than the shuffles cost the softmax warps.)
 // Every wait is bounded; one that runs out sets *err, the roles stop, the
 // CTA waits (bounded) for its copies and MMAs and frees its tensor memory.
 #include <cuda.h>
@@ -71,11 +73,9 @@ constexpr int kAThreads = kASoftThreads + 64;   // + TMA warp + MMA warp
 constexpr uint32_t kATmemCols = 512;
 // tensor-memory columns: score blocks (up to 64 query columns) at 0 and
 // 64, the output block (two halves of d, up to 128 columns each: the query
-// columns of the high, then of the low weight halves) at 128 and 256, and
-// the column sums of the weights (ones times P, the same columns) at 384
+// columns of the high, then of the low weight halves) at 128 and 256
 __host__ __device__ constexpr uint32_t s_col(int b) { return 64u * (uint32_t)b; }
 __host__ __device__ constexpr uint32_t o_col(int, int half) { return 128u + 128u * (uint32_t)half; }
-constexpr uint32_t kSumCol = 384u;
 
 struct AttnParams {
     CUtensorMap tk;   // keys: dims {256, n_valid, 2}, box {64, 128, 1}
@@ -90,7 +90,7 @@ struct AttnParams {
 
 // Shared-memory layout (offsets from a 1024-byte aligned base).
 struct ALayout {
-    int ring, q, p, ones, red, bars, total;
+    int ring, q, p, red, bars, total;
 };
 __host__ __device__ inline ALayout attn_layout(int nq, int nsub)
 {
@@ -98,8 +98,7 @@ __host__ __device__ inline ALayout attn_layout(int nq, int nsub)
     L.ring = 0;
     L.q = nsub * kABox;                       // Q: nq rows x 256, no swizzle, 4096 B per 8 rows
     L.p = L.q + nq * kAD * 2;                 // P: [2 buffers][hi, lo] nq rows x 128 keys
-    L.ones = L.p + 4 * nq * kAKeys * 2;       // a 128 x 64 tile of bf16 ones (1024-aligned: P is)
-    L.red = L.ones + kABox;                   // reductions and running state
+    L.red = L.p + 4 * nq * kAKeys * 2;        // reductions and running state
     L.bars = L.red + 4 * kAMaxQ * 4 * 2 + 4 * kAMaxQ * 4;
     L.total = L.bars + (2 * nsub + 11) * 8 + 16;
     return L;
@@ -308,8 +307,6 @@ __global__ void __launch_bounds__(kAThreads, 1) attn_chunk_kernel(const __grid_c
         m_run[i] = -INFINITY;
         l_run[i] = 0.f;
     }
-    for (int i = tid; i < kABox / 16; i += kAThreads)
-        reinterpret_cast<uint4 *>(sm + L.ones)[i] = make_uint4(0x3F803F80u, 0x3F803F80u, 0x3F803F80u, 0x3F803F80u);
     asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
     asm volatile("tcgen05.fence::before_thread_sync;" ::: "memory");
     __syncthreads();
@@ -354,7 +351,7 @@ __global__ void __launch_bounds__(kAThreads, 1) attn_chunk_kernel(const __grid_c
     } else if (warp == kASoftWarps + 1) {
         // ---------------------------------------------------------- MMA warp
         if (lane == 0) {
-            const uint32_t id_s = idesc_bf16(NQ), id_o = idesc_bf16(2 * NQ), ones = su32(sm + L.ones);
+            const uint32_t id_s = idesc_bf16(NQ), id_o = idesc_bf16(2 * NQ);
             int slot = 0;
             unsigned ph = 0;
             bool go = true;
@@ -398,8 +395,6 @@ __global__ void __launch_bounds__(kAThreads, 1) attn_chunk_kernel(const __grid_c
                     for (int k = 0; k < 4; ++k) {
                         const uint64_t bd = desc_plain(pb + 256u * (4 * kh + k), 2048u);
                         umma(taddr + o_col(0, half), desc_sw128(a0 + 32u * k), bd, id_o, (kh | k) != 0 ? 1u : 0u);
-                        // the column sums of the weights: a tile of ones times P
-                        if (half == 0) umma(taddr + kSumCol, desc_sw128(ones + 32u * k), bd, id_o, (kh | k) != 0 ? 1u : 0u);
                     }
                     release();
                 }
@@ -441,22 +436,6 @@ __global__ void __launch_bounds__(kAThreads, 1) attn_chunk_kernel(const __grid_c
                 tmem_wait_ld();
 #pragma unroll
                 for (int i = 0; i < 8; ++i) oacc[8 * c8 + i] = fmaf(oacc[8 * c8 + i], al[8 * c8 + i], hi[i] + lo[i]);
-            }
-            if (warp == 0) {
-                // every lane of the sums block holds the same column sums;
-                // lane i of each group of 8 keeps column 8 c8 + i
-                const uint32_t sb = taddr + kSumCol;
-#pragma unroll
-                for (int c8 = 0; c8 < NQ / 8; ++c8) {
-                    float hs[8], ls[8];
-                    tmem_ld8(sb + 8u * c8, hs);
-                    tmem_ld8(sb + (uint32_t)NQ + 8u * c8, ls);
-                    tmem_wait_ld();
-                    float mine = 0.f;
-#pragma unroll
-                    for (int i = 0; i < 8; ++i) mine = (lane & 7) == i ? hs[i] + ls[i] : mine;
-                    if (lane < 8) l_run[8 * c8 + lane] = fmaf(l_run[8 * c8 + lane], al[8 * c8 + lane], mine);
-                }
             }
             asm volatile("tcgen05.fence::before_thread_sync;" ::: "memory");
             __syncwarp();
@@ -528,6 +507,15 @@ __global__ void __launch_bounds__(kAThreads, 1) attn_chunk_kernel(const __grid_c
                 const __nv_bfloat16 lo = __float2bfloat16_rn(e - __bfloat162float(h));
                 *reinterpret_cast<__nv_bfloat16 *>(pbuf + plain_off(q, key_local, 2048u)) = h;
                 *reinterpret_cast<__nv_bfloat16 *>(pbuf + plain_off(NQ + q, key_local, 2048u)) = lo;
+                sv[i] = __bfloat162float(h) + __bfloat162float(lo);
+            }
+#pragma unroll
+            for (int o = 16; o >= 1; o >>= 1)
+#pragma unroll
+                for (int i = 0; i < NC; ++i) sv[i] += __shfl_xor_sync(0xFFFFFFFFu, sv[i], o);
+            if (lane == 0) {
+#pragma unroll
+                for (int i = 0; i < NC; ++i) red_sum[qt * kAMaxQ + 2 * i + ch] = sv[i];
             }
             asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
             soft_sync();
@@ -538,6 +526,8 @@ __global__ void __launch_bounds__(kAThreads, 1) attn_chunk_kernel(const __grid_c
                 const uint32_t c = max(red_max[2 * kAMaxQ + q], red_max[3 * kAMaxQ + q]);
                 const float mold = m_run[q], mn = fmaxf(mold, unkey(max(a, c)));
                 const float al = mn == -INFINITY ? 1.f : expf(mold - mn);
+                const float lt = ((red_sum[q] + red_sum[kAMaxQ + q]) + red_sum[2 * kAMaxQ + q]) + red_sum[3 * kAMaxQ + q];
+                l_run[q] = fmaf(l_run[q], al, lt);
                 m_run[q] = mn;
                 alpha[b * kAMaxQ + q] = al;
             }

@@ -285,6 +285,11 @@ __device__ __forceinline__ uint16_t f2bf(float v)
     return *reinterpret_cast<uint16_t *>(&h);
 }
 
+// A code below 2^23 as a float without an int-to-float conversion: placed
+// in the mantissa of 2^23 and 2^23 subtracted (the magic-number conversion
+// of quantised GEMM kernels, e.g. Kim et al. 2022).  Exact.
+__device__ __forceinline__ float code_float(uint32_t q) { return __uint_as_float(q | 0x4B000000u) - 8388608.0f; }
+
 __device__ __forceinline__ float warp_sum(float v)
 {
 #pragma unroll
@@ -1315,7 +1320,7 @@ __device__ void build_hn(const KParams &kp, const Sh &sh, const void *x, unsigne
 #pragma unroll
                         for (int j = 0; j < 8; ++j) {
                             const uint32_t q = ((j < 4 ? cw.x : cw.y) >> (8 * (j & 3))) & 0xFFu;
-                            qh = fmaf((float)q, h[j], qh);
+                            qh = fmaf(code_float(q), h[j], qh);
                             hs += h[j];
                         }
                         rp[r] = fmaf(__uint_as_float(sbw << 16), qh, __uint_as_float(sbw & 0xFFFF0000u) * hs);

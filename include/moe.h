@@ -296,6 +296,15 @@ int moe_debug_trace(void *trace_dev, size_t bytes);
  * returns INVALID_ARG for min_rows < 0. */
 int moe_set_grouped(int min_rows);
 
+/* Grouped mode's expert products: 0 (the default) on the FMA pipes, each
+ * selected expert's rows read once and dotted with each of its token rows
+ * by the persistent kernel's one-vector row kernel (about 1.7 token rows per
+ * expert at 32 rows with top-8 of 256 experts, where the tensor-core tiles
+ * would be mostly padding); 1 on the tensor cores (the products of
+ * moe_gate_up_tc and moe_down_tc).  Widths above 2048 always use the tensor
+ * cores.  Process-wide; INVALID_ARG for other values. */
+int moe_set_grouped_products(int tensor_cores);
+
 /* Grouped gate/up of routed experts on the tensor cores (tcgen05 MMAs,
  * fp32 accumulators in tensor memory): the first half of each selected
  * expert's FFN for every token row that chose it, when many rows share an

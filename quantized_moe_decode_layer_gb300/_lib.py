@@ -28,7 +28,7 @@ SYMBOLS = ["moe_pack_size", "moe_pack_weights", "moe_layer_destroy", "moe_export
            "moe_attn_workspace_size", "moe_attn_decode", "moe_attn_append",
            "moe_streamed_size", "moe_streamed_create", "moe_streamed_layer", "moe_streamed_prepare",
            "moe_streamed_stats", "moe_streamed_destroy", "moe_streamed_forward",
-           "moe_stream_status", "moe_build_flags", "moe_debug_inject", "moe_debug_set", "moe_debug_trace", "moe_set_grouped", "moe_gate_up_tc", "moe_down_tc", "moe_status_str",
+           "moe_stream_status", "moe_build_flags", "moe_debug_inject", "moe_debug_set", "moe_debug_trace", "moe_set_grouped", "moe_set_grouped_products", "moe_gate_up_tc", "moe_down_tc", "moe_status_str",
            "moe_last_cuda_error",
            "moe_selftest_host", "moe_launch_count"]
 
@@ -106,6 +106,7 @@ def lib():
             "moe_stream_status": (i, [vp, sz, vp]),
             "moe_debug_set": (i, [i, C.c_longlong]),
             "moe_build_flags": (i, []),
+            "moe_set_grouped_products": (i, [i]),
             "moe_debug_inject": (i, [i]),
             "moe_debug_trace": (i, [vp, sz]),
             "moe_gate_up_tc": (i, [vp, vp, i, vp, vp, i, vp, vp, vp]),

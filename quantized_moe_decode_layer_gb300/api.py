@@ -485,6 +485,12 @@ def debug_set(skip_row: int = -1, timeout_ns: int = 0) -> None:
     check("moe_debug_set", lib().moe_debug_set(skip_row, timeout_ns))
 
 
+def set_grouped_products(tensor_cores: bool) -> None:
+    """moe_set_grouped_products: grouped mode's expert products on the tensor
+    cores (True) or the FMA pipes (False, the default)."""
+    check("moe_set_grouped_products", lib().moe_set_grouped_products(1 if tensor_cores else 0))
+
+
 def build_flags() -> int:
     """moe_build_flags: MOE_BUILD_DEBUG_BOUNDS (1) in the bounds-checked build."""
     return int(lib().moe_build_flags())

@@ -23,6 +23,7 @@ long long g_timeout_ns = 2000000000LL;
 // On the 35B shape the 40-layer stack runs 16 rows grouped in 240 us per
 // layer against 259 in two 8-row launches, and 32 rows in 265 against 470.
 int g_grouped_min_rows = 1;
+std::atomic<int> g_grouped_tc{0};   // grouped mode's products: 0 FMA, 1 tensor cores
 
 // Contraction widths 64 * 2^j up to 64 * 32 * kMaxGPL: a row splits into
 // whole groups over 1, 2, 4, ..., 32 lanes.
@@ -49,6 +50,7 @@ int check_status_word(void *ws)
 }  // namespace
 
 void note_cuda_error(int err) { t_last_cuda_error = err; }
+bool grouped_products_tc() { return g_grouped_tc.load(std::memory_order_relaxed) != 0; }
 void note_launch() { ++t_launches; }
 
 int rows_per_launch(int H)
@@ -612,6 +614,13 @@ int moe_set_grouped(int min_rows)
 {
     if (min_rows < 0) return MOE_ERR_INVALID_ARG;
     g_grouped_min_rows = min_rows;
+    return MOE_OK;
+}
+
+int moe_set_grouped_products(int tensor_cores)
+{
+    if (tensor_cores != 0 && tensor_cores != 1) return MOE_ERR_INVALID_ARG;
+    g_grouped_tc.store(tensor_cores, std::memory_order_relaxed);
     return MOE_OK;
 }
 

@@ -323,6 +323,16 @@ int grouped_layer(const moe_layer &L, const uint16_t *x, int mg, uint16_t *out, 
     const TcSetHost gu_s{L.ptrs.sgu, 2 * g.Is, g.H, g.sg_bytes, hn, 0, she, shm, nullptr, act_s};
     const TcSetHost dn_r{L.ptrs.down, g.H, g.I, g.d_bytes, act, mg, experts, masks, count, y};
     const TcSetHost dn_s{L.ptrs.sdown, g.H, g.Is, g.sd_bytes, act_s, mg, she, shm, nullptr, ysh};
+    // the FMA products (each slot's rows read once, one pass per token row of
+    // the slot) unless the tensor-core products are asked for or the widths
+    // exceed the one-vector kernel's
+    if (!grouped_products_tc() && g.H <= 2048 && g.I <= 2048 && g.H % 128 == 0 && g.I % 128 == 0 &&
+        (!g.has_shared || g.Is % 128 == 0)) {
+        const TcSetHost *gs = g.has_shared ? &gu_s : nullptr;
+        const TcSetHost *ds = g.has_shared ? &dn_s : nullptr;
+        if ((rc = launch_grouped_fma(true, g.rb, gu_r, Umax, g.sb, gs, 1, mg, err, timeout_ns, st))) return rc;
+        if ((rc = launch_grouped_fma(false, g.rb, dn_r, Umax, g.sb, ds, 1, mg, err, timeout_ns, st))) return rc;
+    } else {
     const bool fused = g.has_shared && (g.sb == g.rb || g.sb == 8);
     if ((rc = launch_grouped_tc2(true, g.rb, gu_r, Umax, g.sb, fused ? &gu_s : nullptr, 1, mg, err, timeout_ns, st)))
         return rc;
@@ -334,6 +344,7 @@ int grouped_layer(const moe_layer &L, const uint16_t *x, int mg, uint16_t *out, 
     if (g.has_shared && !fused &&
         (rc = launch_grouped_tc2(false, g.sb, dn_s, 1, g.sb, nullptr, 0, mg, err, timeout_ns, st)))
         return rc;
+    }
     // without the fused RMSNorm, 8 CTAs per row (each a whole number of 256-wide parts)
     const int parts = (!out_n && g.H % (8 * kRowThreads) == 0) ? 8 : 1;
     combine_kernel<<<dim3((unsigned)mg, (unsigned)parts), kRowThreads, 0, st>>>(

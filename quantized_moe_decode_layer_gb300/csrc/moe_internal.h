@@ -204,6 +204,8 @@ struct TcSetHost {
 };
 int launch_grouped_tc2(bool swiglu, int bits_a, const TcSetHost &a, int nA, int bits_b, const TcSetHost *b, int nB,
                        int M, int *err, long long timeout_ns, cudaStream_t stream);
+int launch_grouped_fma(bool swiglu, int bits_a, const TcSetHost &a, int nA, int bits_b, const TcSetHost *b, int nB,
+                       int M, int *err, long long timeout_ns, cudaStream_t stream);
 int launch_grouped_tc(int bits, bool swiglu, const uint8_t *W, int rows, int K, int row_bytes, const float *in, int in_u,
                       int M, const int32_t *experts, const uint32_t *masks, int U, const int *U_dev, float *out,
                       int *err, long long timeout_ns, cudaStream_t stream);
@@ -215,4 +217,5 @@ int grouped_forward(const moe_layer *const *layers, int L, const uint16_t *x, in
                     void *ws_dev, size_t ws_bytes, long long timeout_ns, cudaStream_t st);
 void note_cuda_error(int err);
 void note_launch();
+bool grouped_products_tc();   // moe_set_grouped_products
 }  // namespace moe

@@ -48,6 +48,8 @@
 
 #include <cfloat>
 #include <climits>
+#include <cstring>
+#include <mutex>
 
 #include "moe_internal.h"
 #include "moe_unpack.cuh"
@@ -2430,6 +2432,175 @@ struct QkvParams {
 
 __host__ __device__ inline size_t qkv_x_bytes(int M, int K) { return align_up((size_t)M * K * 4 + (size_t)M * (K / kGroup) * 4, 128); }
 
+// ------------------------------------------------- grouped FMA products
+//
+// Grouped mode's expert products on the FMA pipes: slot u's expert over the
+// token rows of its mask, the same dequantised dot products as the
+// persistent kernel's row kernels (the one-vector plain1, or two token rows
+// at a time with the codes decoded once for both: the same arithmetic per
+// row).  One CTA per (block of rows, slot, group of up to 4 of the slot's
+// token rows): its rows come in with one bulk copy (read once per group of
+// token rows; a popular expert chosen by many rows gets several CTAs rather
+// than one long one), then for each pair of token rows the input vectors
+// are staged (arranged, times 2^100, group sums) and the warps split the
+// rows.  Gate/up rows come in units (gate row, up row) and leave as
+// silu(gate) * up.  With realistic routing a slot has one or two token rows,
+// where the tensor-core products spend most of their work on padding.
+struct FmaSet {
+    const uint8_t *W;
+    int rows, K, row_bytes, bits;
+    const float *in;
+    int in_u;
+    const int32_t *experts;
+    const uint32_t *masks;
+    const int *U_dev;
+    float *out;
+};
+struct FmaParams {
+    FmaSet s[2];
+    int nA, M, swiglu, block;   // block: units (gate/up) or rows per CTA
+    long long timeout_ns;
+    int *err;
+};
+constexpr int kFmaThreads = 256;
+
+constexpr int kFmaRowGroup = 4;   // token rows of a slot per CTA (popular experts get several CTAs)
+
+__host__ __device__ inline size_t fma_smem_bytes(int K, int block_bytes, int block_rows)
+{
+    return 128 + align_up((size_t)block_bytes, 128) + 2 * ((size_t)K * 4 + (size_t)(K / kGroup) * 4) +
+           2 * (size_t)block_rows * 4;
+}
+
+__global__ void __launch_bounds__(kFmaThreads) grouped_fma_kernel(const __grid_constant__ FmaParams p)
+{
+    extern __shared__ __align__(128) uint8_t smem[];
+    const int y = blockIdx.y;
+    const FmaSet &S = y < p.nA ? p.s[0] : p.s[1];
+    const int u = y < p.nA ? y : y - p.nA;
+    if (S.U_dev && u >= *S.U_dev) return;
+    const int rpu = p.swiglu ? 2 : 1;                 // rows per unit
+    const int units = S.rows / rpu;
+    const int a0 = blockIdx.x * p.block;
+    if (a0 >= units) return;
+    const uint32_t mask = S.masks[u];
+    // this CTA's token rows: set bits z * kFmaRowGroup .. + kFmaRowGroup - 1
+    const int popc = __popc(mask), z = blockIdx.z;
+    if (z * kFmaRowGroup >= popc) return;
+    uint32_t mk = mask;
+#pragma unroll 1
+    for (int i = 0; i < z * kFmaRowGroup; ++i) mk &= mk - 1u;
+    int left = min(kFmaRowGroup, popc - z * kFmaRowGroup);
+    const int n = min(p.block, units - a0), nrows = n * rpu;
+    const int e = S.experts[u];
+    const int K = S.K, G = K / kGroup, tid = threadIdx.x, warp = tid >> 5;
+    constexpr int NW = kFmaThreads / 32;
+    uint64_t *bar = reinterpret_cast<uint64_t *>(smem);
+    uint8_t *rows = smem + 128;
+    float4 *xs = reinterpret_cast<float4 *>(rows + align_up((size_t)p.block * rpu * S.row_bytes, 128));  // [2][K / 4]
+    float *xsum = reinterpret_cast<float *>(xs + 2 * (K / 4));                                          // [2][G]
+    float *tmp = xsum + 2 * G;                                                                          // [2][nrows]
+    if (tid == 0) {
+        mbar_init(bar, 1);
+        asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+    }
+    __syncthreads();
+    if (tid == 0) {
+        const unsigned bytes = (unsigned)(nrows * S.row_bytes);
+        mbar_expect_tx(bar, bytes);
+        bulk_load(rows, S.W + ((size_t)e * S.rows + (size_t)a0 * rpu) * S.row_bytes, bytes, bar);
+    }
+    bool ok = true, landed = false;
+    // warp w: block rows w, w + NW, ...
+    const int cw = nrows > warp ? (nrows - warp + NW - 1) / NW : 0;
+    const uint32_t rq = smem_u32(rows) + (uint32_t)(warp * S.row_bytes);
+    const int rstride = NW * S.row_bytes;
+#pragma unroll 1
+    while (left > 0) {
+        const int np = min(2, left);
+        int ms[2];
+        ms[0] = __ffs(mk) - 1;
+        mk &= mk - 1u;
+        ms[1] = ms[0];
+        if (np == 2) {
+            ms[1] = __ffs(mk) - 1;
+            mk &= mk - 1u;
+        }
+        left -= np;
+        if (ms[np - 1] >= p.M) break;
+        // the np token rows' inputs: quads arranged (float4 t * G + g holds
+        // inputs 64 g + 4 t ..), times 2^100; group sums over 16 quads
+#pragma unroll 1
+        for (int c = tid; c < np * (K / 4); c += kFmaThreads) {
+            const int r = c / (K / 4), cc = c - r * (K / 4);
+            const float4 v = __ldg(reinterpret_cast<const float4 *>(S.in + ((size_t)u * S.in_u + ms[r]) * K) + cc);
+            float gs = (v.x + v.y) + (v.z + v.w);
+#pragma unroll
+            for (int o = 8; o >= 1; o >>= 1) gs += __shfl_xor_sync(FULLMASK, gs, o);
+            xs[r * (K / 4) + (cc & 15) * G + (cc >> 4)] =
+                make_float4(v.x * kXScale, v.y * kXScale, v.z * kXScale, v.w * kXScale);
+            if ((cc & 15) == 0) xsum[r * G + (cc >> 4)] = gs;
+        }
+        if (!landed) {
+            // the rows' copy, waited for once (bounded)
+            if (!mbar_try_wait(bar, 0u)) {
+                const unsigned long long t0 = now_ns();
+#pragma unroll 1
+                while (!(ok = mbar_try_wait_sleep(bar, 0u, 2000)))
+                    if (now_ns() - t0 > (unsigned long long)p.timeout_ns) break;
+            }
+            landed = true;
+        }
+        if (!__syncthreads_and(ok)) break;
+        if (cw > 0) {
+            // two token rows: the codes decoded once for both; one: the
+            // one-vector kernel (the same arithmetic per row)
+            if (np == 2) {
+                const uint32_t xqa[2] = {smem_u32(xs), smem_u32(xs + K / 4)};
+                const int soff[2] = {0, G};
+                float xsg[2][kMaxGPL];
+                lane_gsums<2>(smem_u32(xsum), soff, K, xsg);
+                auto emit = [&](int rb, const float (&acc)[1][2]) {
+                    tmp[rb * NW + warp] = acc[0][0];
+                    tmp[nrows + rb * NW + warp] = acc[0][1];
+                };
+                const uint8_t *rp = rows + (size_t)warp * S.row_bytes;
+                if (S.bits == 6) warp_rows<6, 1, 2>(rp, rstride, cw, K, xqa, xsg, emit);
+                else if (S.bits == 8) warp_rows<8, 1, 2>(rp, rstride, cw, K, xqa, xsg, emit);
+                else warp_rows<4, 1, 2>(rp, rstride, cw, K, xqa, xsg, emit);
+            } else {
+                if (S.bits == 6) plain1<6>(rq, cw, rstride, K, smem_u32(xs), smem_u32(xsum), tmp + warp, NW, 0u);
+                else if (S.bits == 8) plain1<8>(rq, cw, rstride, K, smem_u32(xs), smem_u32(xsum), tmp + warp, NW, 0u);
+                else plain1<4>(rq, cw, rstride, K, smem_u32(xs), smem_u32(xsum), tmp + warp, NW, 0u);
+            }
+        }
+        __syncthreads();
+#pragma unroll 1
+        for (int r = 0; r < np; ++r) {
+            float *o = S.out + ((size_t)u * p.M + ms[r]) * units + a0;
+            const float *t = tmp + (size_t)r * nrows;
+#pragma unroll 1
+            for (int i = tid; i < n; i += kFmaThreads) {
+                if (p.swiglu) {
+                    const float gt = t[2 * i], up = t[2 * i + 1];
+                    o[i] = gt / (1.0f + expf(-gt)) * up;
+                } else {
+                    o[i] = t[i];
+                }
+            }
+        }
+        __syncthreads();
+    }
+    if (!ok) {
+        if (tid == 0) atomicOr(p.err, kStatusTimeout);
+    }
+    if (tid == 0 && (!ok || !landed)) {
+        // the copy lands before the CTA exits
+        const unsigned long long t0 = now_ns();
+        while (!mbar_try_wait(bar, 0u) && now_ns() - t0 < (unsigned long long)p.timeout_ns) {}
+    }
+}
+
 __global__ void __launch_bounds__(kQkvThreads) qkv_kernel(const __grid_constant__ QkvParams q)
 {
     extern __shared__ __align__(128) uint8_t smem[];
@@ -2694,6 +2865,59 @@ int device_sms()
 int qkv_smem_bytes(int M, int K, int rows_per_cta, int rowb)
 {
     return (int)(128 + qkv_x_bytes(M, K) + (size_t)rows_per_cta * rowb);
+}
+
+// Grouped mode's products on the FMA pipes (see grouped_fma_kernel): set a
+// over its nA slots and set b (if given) over its nB, in one launch.  Sets
+// with K above 2048 (the one-vector kernel's limit) are refused
+// (MOE_ERR_UNSUPPORTED): the caller uses the tensor-core products there.
+int launch_grouped_fma(bool swiglu, int bits_a, const TcSetHost &a, int nA, int bits_b, const TcSetHost *b, int nB,
+                       int M, int *err, long long timeout_ns, cudaStream_t stream)
+{
+    const TcSetHost *sets[2] = {&a, b};
+    const int bits[2] = {bits_a, bits_b};
+    FmaParams P;
+    memset(&P, 0, sizeof P);
+    int Kmax = 0, rowb_max = 0;
+    for (int i = 0; i < 2; ++i) {
+        if (!sets[i]) continue;
+        const TcSetHost &t = *sets[i];
+        // (K a multiple of 128: the staging's shuffles run on whole warps)
+        if (t.K > 32 * kGroup || t.K % 128 || !(bits[i] == 4 || bits[i] == 6 || bits[i] == 8))
+            return MOE_ERR_UNSUPPORTED;
+        P.s[i] = FmaSet{t.W, t.rows, t.K, t.row_bytes, bits[i], t.in, t.in_u, t.experts, t.masks, t.U_dev, t.out};
+        Kmax = max(Kmax, t.K);
+        rowb_max = max(rowb_max, t.row_bytes);
+    }
+    const int rpu = swiglu ? 2 : 1;
+    // rows per CTA: about 80 KB of them (two CTAs per SM), whole units
+    int block = max(1, (80 * 1024) / (rpu * rowb_max));
+    if (block > 1024 / rpu) block = 1024 / rpu;
+    P.nA = nA;
+    P.M = M;
+    P.swiglu = swiglu ? 1 : 0;
+    P.block = block;
+    P.timeout_ns = timeout_ns;
+    P.err = err;
+    const size_t smem = fma_smem_bytes(Kmax, block * rpu * rowb_max, block * rpu);
+    static std::once_flag attr_once[64];
+    int dev = 0;
+    cudaError_t e = cudaGetDevice(&dev);
+    if (e != cudaSuccess || dev < 0 || dev >= 64) { note_cuda_error((int)e); return MOE_ERR_CUDA; }
+    std::call_once(attr_once[dev], [&] {
+        e = cudaFuncSetAttribute(grouped_fma_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, kSmemMax);
+    });
+    if (e != cudaSuccess) { note_cuda_error((int)e); return MOE_ERR_CUDA; }
+    int units_max = 0;
+    for (int i = 0; i < 2; ++i)
+        if (sets[i]) units_max = max(units_max, sets[i]->rows / rpu);
+    const dim3 grid((unsigned)((units_max + block - 1) / block), (unsigned)(nA + (b ? nB : 0)),
+                    (unsigned)((M + kFmaRowGroup - 1) / kFmaRowGroup));
+    grouped_fma_kernel<<<grid, kFmaThreads, smem, stream>>>(P);
+    note_launch();
+    e = cudaGetLastError();
+    if (e != cudaSuccess) { note_cuda_error((int)e); return MOE_ERR_CUDA; }
+    return MOE_OK;
 }
 
 int launch_qkv(const uint8_t *W, int rows, int K, int bits, const uint16_t *x, int M, float *y, int *err,

@@ -214,13 +214,40 @@ def grouped_always():
         moe.set_grouped(DEFAULT_GROUPED_MIN_ROWS)
 
 
-def test_a35b_m32_grouped():
-    """32 rows: grouped mode (tensor-core expert products, every expert read
-    once for the 32 rows): routing bit-exact, outputs within the tolerance."""
+@pytest.fixture(params=["fma", "tc"])
+def grouped_products(request):
+    moe.set_grouped_products(request.param == "tc")
+    try:
+        yield request.param
+    finally:
+        moe.set_grouped_products(False)
+
+
+def test_a35b_m32_grouped(grouped_products):
+    """32 rows: grouped mode (every expert read once for the 32 rows), with
+    its products on the FMA pipes (the default) and on the tensor cores:
+    routing bit-exact, outputs within the tolerance."""
     shape = synth.A35B
     L, layer, lay = cached(shape, 11)
     x = rows_with_margin(shape, lay, 4, 32, gamma=L["gamma"])
     check_layer(shape, L, layer, lay, x)
+
+
+def test_grouped_fma_products_match_one_row_products():
+    """The grouped FMA products run the persistent kernel's one-vector row
+    kernel: with grouped mode on, a 12-row tiny call's rows are within the
+    tolerance and each expert's products do not depend on the other rows
+    (two calls sharing row 0 give row 0 the same output bits)."""
+    shape = synth.TINY
+    L, layer, lay = cached(shape, 7)
+    x = rows_with_margin(shape, lay, 777, 12)
+    out, _ = check_layer(shape, L, layer, lay, x)
+    y = rows_with_margin(shape, lay, 778, 12)
+    y[0] = x[0]
+    ws = moe.Workspace(layer.desc, 12)
+    out2 = moe.decode_layer(layer, y.to(DEV), ws)
+    assert ws.status() == 0
+    assert torch.equal(out[0].view(torch.int16), out2[0].view(torch.int16))
 
 
 def test_tiny_m40_two_groups():

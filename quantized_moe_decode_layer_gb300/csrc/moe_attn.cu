@@ -70,12 +70,21 @@ constexpr int kABox = 16384;                // one TMA box: 128 rows of 128 byte
 constexpr int kASoftWarps = 8;
 constexpr int kASoftThreads = kASoftWarps * 32;
 constexpr int kAThreads = kASoftThreads + 64;   // + TMA warp + MMA warp
-constexpr uint32_t kATmemCols = 512;
-// tensor-memory columns: score blocks (up to 64 query columns) at 0 and
-// 64, the output block (two halves of d, up to 128 columns each: the query
-// columns of the high, then of the low weight halves) at 128 and 256
-__host__ __device__ constexpr uint32_t s_col(int b) { return 64u * (uint32_t)b; }
-__host__ __device__ constexpr uint32_t o_col(int, int half) { return 128u + 128u * (uint32_t)half; }
+// Tensor-memory columns: two score blocks of nq columns, then the output
+// block (two halves of d, 2 nq columns each: the query columns of the high,
+// then of the low weight halves). Up to 32 query columns this packs into 256
+// columns, so that two CTAs fit on one SM; above, blocks sit at multiples of
+// 64 and 128 in all 512.
+__host__ __device__ constexpr bool tmem_compact(int nq) { return nq <= 32; }
+__host__ __device__ constexpr uint32_t tmem_cols(int nq) { return tmem_compact(nq) ? 256u : 512u; }
+__host__ __device__ constexpr uint32_t s_col(int nq, int b)
+{
+    return tmem_compact(nq) ? (uint32_t)(nq * b) : 64u * (uint32_t)b;
+}
+__host__ __device__ constexpr uint32_t o_col(int nq, int half)
+{
+    return tmem_compact(nq) ? (uint32_t)(2 * nq + 2 * nq * half) : 128u + 128u * (uint32_t)half;
+}
 
 struct AttnParams {
     CUtensorMap tk;   // keys: dims {256, n_valid, 2}, box {64, 128, 1}
@@ -246,8 +255,10 @@ __device__ __forceinline__ void box_of(int j, int nt, bool &is_v, int &t, int &p
     else { is_v = true; part = t + 1 < nt ? w - 4 : w; }
 }
 
-template <int NQ>
-__global__ void __launch_bounds__(kAThreads, 1) attn_chunk_kernel(const __grid_constant__ AttnParams p)
+// MINB = 2: two CTAs per SM (at most 32 query columns, a shallower ring,
+// registers capped at 96), for grids of more chunks than SMs.
+template <int NQ, int MINB>
+__global__ void __launch_bounds__(kAThreads, MINB) attn_chunk_kernel(const __grid_constant__ AttnParams p)
 {
     constexpr int NC = NQ / 2;   // query columns of a softmax thread: q = 2 i + ch
     extern __shared__ __align__(1024) uint8_t smem_raw[];
@@ -290,7 +301,7 @@ __global__ void __launch_bounds__(kAThreads, 1) attn_chunk_kernel(const __grid_c
     }
     if (warp == 0) {
         asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(su32(tmem_slot)),
-                     "r"(kATmemCols)
+                     "r"(tmem_cols(NQ))
                      : "memory");
         asm volatile("tcgen05.relinquish_alloc_permit.cta_group::1.sync.aligned;" ::: "memory");
     }
@@ -373,7 +384,7 @@ __global__ void __launch_bounds__(kAThreads, 1) attn_chunk_kernel(const __grid_c
                     const uint32_t a0 = su32(ring + (size_t)slot * kABox);
 #pragma unroll
                     for (int k = 0; k < 4; ++k)
-                        umma(taddr + s_col(b), desc_sw128(a0 + 32u * k), desc_plain(su32(qs) + 256u * (4 * part + k), 4096u),
+                        umma(taddr + s_col(NQ, b), desc_sw128(a0 + 32u * k), desc_plain(su32(qs) + 256u * (4 * part + k), 4096u),
                              id_s, (part | k) != 0 ? 1u : 0u);
                     release();
                 }
@@ -394,7 +405,7 @@ __global__ void __launch_bounds__(kAThreads, 1) attn_chunk_kernel(const __grid_c
 #pragma unroll
                     for (int k = 0; k < 4; ++k) {
                         const uint64_t bd = desc_plain(pb + 256u * (4 * kh + k), 2048u);
-                        umma(taddr + o_col(0, half), desc_sw128(a0 + 32u * k), bd, id_o, (kh | k) != 0 ? 1u : 0u);
+                        umma(taddr + o_col(NQ, half), desc_sw128(a0 + 32u * k), bd, id_o, (kh | k) != 0 ? 1u : 0u);
                     }
                     release();
                 }
@@ -425,7 +436,7 @@ __global__ void __launch_bounds__(kAThreads, 1) attn_chunk_kernel(const __grid_c
             ok = __all_sync(0xFFFFFFFFu, bar_wait(su32(o_full), (unsigned)t & 1u, abort_flag, p));
             asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory");
             if (!ok) return;
-            const uint32_t base = taddr + ((uint32_t)(32 * qt) << 16) + o_col(0, ch);
+            const uint32_t base = taddr + ((uint32_t)(32 * qt) << 16) + o_col(NQ, ch);
             const float *al = alpha + (t & 1) * kAMaxQ;
             // columns q (high halves) and NQ + q (low halves), 8 at a time
 #pragma unroll
@@ -449,7 +460,7 @@ __global__ void __launch_bounds__(kAThreads, 1) attn_chunk_kernel(const __grid_c
             asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory");
             float sv[NC];
             if (ok) {
-                const uint32_t base = taddr + ((uint32_t)(32 * qt) << 16) + s_col(b);
+                const uint32_t base = taddr + ((uint32_t)(32 * qt) << 16) + s_col(NQ, b);
                 // 16 columns at a time, keeping every other one (q = 2 i + ch)
 #pragma unroll
                 for (int c16 = 0; c16 < NQ / 16; ++c16) {
@@ -555,7 +566,7 @@ __global__ void __launch_bounds__(kAThreads, 1) attn_chunk_kernel(const __grid_c
     asm volatile("tcgen05.fence::before_thread_sync;" ::: "memory");
     __syncthreads();
     if (warp == 0)
-        asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;" ::"r"(taddr), "r"(kATmemCols) : "memory");
+        asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;" ::"r"(taddr), "r"(tmem_cols(NQ)) : "memory");
 }
 
 // Merge of a row's chunks, in chunk order: o = sum_j e^(m_j - M) O_j /
@@ -667,28 +678,47 @@ int launch_attn(const uint16_t *q, const uint16_t *k, const uint16_t *vt, int T_
     P.pos0 = pos0;
     P.n_valid = n_valid;
     P.nq = 16 * ((kAGrp * M + 15) / 16);
-    P.nsub = attn_layout(P.nq, 8).total + 1024 <= kSmemMax ? 8 : 6;
     P.timeout_ns = timeout_ns;
     P.err = err;
-    const int smem = attn_layout(P.nq, P.nsub).total + 1024;
-    if (smem > kSmemMax) return MOE_ERR_UNSUPPORTED;
     static std::once_flag attr_once[64];
+    static int sm_count[64];
     int dev = 0;
     cudaError_t e = cudaGetDevice(&dev);
     if (e != cudaSuccess || dev < 0 || dev >= 64) { note_cuda_error((int)e); return MOE_ERR_CUDA; }
     std::call_once(attr_once[dev], [&] {
-        const void *fns[4] = {(const void *)attn_chunk_kernel<16>, (const void *)attn_chunk_kernel<32>,
-                              (const void *)attn_chunk_kernel<48>, (const void *)attn_chunk_kernel<64>};
-        for (int i = 0; i < 4 && e == cudaSuccess; ++i)
+        const void *fns[6] = {(const void *)attn_chunk_kernel<16, 1>, (const void *)attn_chunk_kernel<32, 1>,
+                              (const void *)attn_chunk_kernel<48, 1>, (const void *)attn_chunk_kernel<64, 1>,
+                              (const void *)attn_chunk_kernel<16, 2>, (const void *)attn_chunk_kernel<32, 2>};
+        for (int i = 0; i < 6 && e == cudaSuccess; ++i) {
             e = cudaFuncSetAttribute(fns[i], cudaFuncAttributeMaxDynamicSharedMemorySize, kSmemMax);
+            if (e == cudaSuccess)
+                e = cudaFuncSetAttribute(fns[i], cudaFuncAttributePreferredSharedMemoryCarveout,
+                                         (int)cudaSharedmemCarveoutMaxShared);
+        }
+        if (e == cudaSuccess) e = cudaDeviceGetAttribute(&sm_count[dev], cudaDevAttrMultiProcessorCount, dev);
     });
     if (e != cudaSuccess) { note_cuda_error((int)e); return MOE_ERR_CUDA; }
+    // More chunk CTAs than SMs: two per SM when the tensor memory and a
+    // shallower ring allow it (16 query columns: 5 boxes, 32: 3, within
+    // half of the SM's shared memory); otherwise one per SM with 8 boxes.
+    const bool two_per_sm = tmem_compact(P.nq) && (long long)nchunks * kAHkv > sm_count[dev];
+    if (two_per_sm)
+        P.nsub = P.nq <= 16 ? 5 : 3;
+    else
+        P.nsub = attn_layout(P.nq, 8).total + 1024 <= kSmemMax ? 8 : 6;
+    const int smem = attn_layout(P.nq, P.nsub).total + 1024;
+    if (smem > kSmemMax) return MOE_ERR_UNSUPPORTED;
     const dim3 grid(nchunks, kAHkv);
-    switch (P.nq) {
-    case 16: attn_chunk_kernel<16><<<grid, kAThreads, smem, stream>>>(P); break;
-    case 32: attn_chunk_kernel<32><<<grid, kAThreads, smem, stream>>>(P); break;
-    case 48: attn_chunk_kernel<48><<<grid, kAThreads, smem, stream>>>(P); break;
-    default: attn_chunk_kernel<64><<<grid, kAThreads, smem, stream>>>(P); break;
+    if (two_per_sm) {
+        if (P.nq == 16) attn_chunk_kernel<16, 2><<<grid, kAThreads, smem, stream>>>(P);
+        else attn_chunk_kernel<32, 2><<<grid, kAThreads, smem, stream>>>(P);
+    } else {
+        switch (P.nq) {
+        case 16: attn_chunk_kernel<16, 1><<<grid, kAThreads, smem, stream>>>(P); break;
+        case 32: attn_chunk_kernel<32, 1><<<grid, kAThreads, smem, stream>>>(P); break;
+        case 48: attn_chunk_kernel<48, 1><<<grid, kAThreads, smem, stream>>>(P); break;
+        default: attn_chunk_kernel<64, 1><<<grid, kAThreads, smem, stream>>>(P); break;
+        }
     }
     note_launch();
     attn_combine_kernel<<<M * kAHq, kAD, 0, stream>>>(P.part_o, P.part_ml, pos0, o);

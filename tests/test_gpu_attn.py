@@ -69,16 +69,22 @@ def check(T_cap, n_valid, M, seed):
 
 
 @pytest.mark.parametrize("T_cap,n_valid,M", [(64, 1, 1), (256, 200, 1), (1024, 700, 3), (2048, 1537, 8),
-                                             (4096, 4096, 4), (640, 129, 2)])
+                                             (4096, 4096, 4), (640, 129, 2), (40960, 40000, 1),
+                                             (65536, 50001, 4)])
 def test_attention_matches_oracle(T_cap, n_valid, M):
     """Single key; ragged tiles and chunks (700 = 512 + 188, 1537 = 3 * 512 + 1,
-    129 = 128 + 1); the cache full to its end; 1, 2, 3, 4 and 8 rows."""
+    129 = 128 + 1); the cache full to its end; 1, 2, 3, 4 and 8 rows; more
+    chunk CTAs than SMs (79 and 98 chunks per KV head), where 16 and 32
+    query columns run two CTAs per SM."""
     check(T_cap, n_valid, M, 11 + M)
 
 
-def test_attention_rows_equal_one_row_calls():
-    """Row m of an 8-row call is bitwise the one-row call at position pos0 + m."""
-    T_cap, n_valid, M = 2048, 1800, 8
+@pytest.mark.parametrize("T_cap,n_valid", [(2048, 1800), (45056, 40000)])
+def test_attention_rows_equal_one_row_calls(T_cap, n_valid):
+    """Row m of an 8-row call is bitwise the one-row call at position pos0 + m
+    (at 40000 positions the one-row calls run two CTAs per SM, the 8-row call
+    one)."""
+    M = 8
     q, cache, o = check(T_cap, n_valid, M, 21)
     pos0 = n_valid - M
     for m in range(M):

@@ -78,6 +78,7 @@ bool make_geo(const moe_layer_desc &d, Geo &g)
     g.sb = d.has_shared ? d.shared_bits : 8;
     g.qb = d.router_bits;
     g.Er = d.E + d.has_shared;
+    g.Erp = (int)align_up((size_t)g.Er, 16);
     g.eps = d.eps;
     g.rr_bytes = row_bytes(g.H, g.qb);
     g.g_bytes = row_bytes(g.H, g.rb);
@@ -89,6 +90,8 @@ bool make_geo(const moe_layer_desc &d, Geo &g)
     g.off_router = put((size_t)g.Er * g.rr_bytes);
     g.off_gamma = put((size_t)g.H * 2);
     g.off_gamma_next = put((size_t)g.H * 2);
+    g.off_router_t = put(router_t_bytes(g.H, g.Erp, g.qb));
+    g.rt_sb = (size_t)g.H * g.Erp;
     g.off_gu = put((size_t)g.E * g.I * 2 * g.g_bytes);
     g.off_down = put((size_t)g.E * g.H * g.d_bytes);
     g.off_sgu = put(d.has_shared ? (size_t)g.Is * 2 * g.sg_bytes : 0);
@@ -106,10 +109,15 @@ void make_ws_layout(const Geo &g, int max_M, WsLayout &w)
     size_t o = kCtrlBytes;
     auto put = [&](size_t bytes) { o = align_up(o, 256); size_t r = o; o += bytes; return r; };
     // buffers CTAs exchange hold tagged 8-byte words (value | tag << 32)
-    w.off_logits = put((size_t)kLogitCopies * R * g.Er * 8);
+    // router logits before the RMSNorm scale, and (last) the row's sum of
+    // squares: [kLogitCopies][R][Er + 1]
+    w.off_logits = put((size_t)kLogitCopies * R * (g.Er + 1) * 8);
     w.off_act = put((size_t)w.max_slots * R * g.I * 8);
     w.off_act_s = put((size_t)R * (g.Is ? g.Is : 1) * 8);
     w.off_ping = put((size_t)2 * R * (g.H / 2) * 8);
+    // partial router dots and sums of squares: [row][Er + 1][CTA], for the
+    // rows of one launch
+    w.off_part = put((size_t)kMaxCtas * (max_M < R ? max_M : R) * (g.Er + 1) * 8);
     w.off_stage_in = put((size_t)max_M * g.H * 2);
     w.off_stage_out = put((size_t)max_M * g.H * 2);
     w.grp_rows = w.grp_slots = 0;
@@ -187,9 +195,10 @@ bool aligned16(const void *p) { return (reinterpret_cast<uintptr_t>(p) & 15) == 
 // checked against what the kernel relies on: the ring depth a multiple of
 // the compute warps and within one producer batch, stages that hold any
 // single bulk copy, the shared-memory limit, a staging buffer that holds
-// every row of a slot, a prefetch buffer that holds gamma and the router
-// rows, whole output row pairs per CTA, and 32-bit products in the work
-// split.  Returns the number of violations.
+// every row of a slot, a prefetch buffer that holds gamma and the CTA's
+// slice of the input-major router, at most kRouterRowsCta router rows and at
+// most one group of output rows per CTA, whole output row pairs per CTA, and
+// 32-bit products in the work split.  Returns the number of violations.
 int plan_selftest_host()
 {
     const moe_layer_desc shapes[] = {
@@ -199,7 +208,7 @@ int plan_selftest_host()
         {2048, 512, 256, 8, 8, 8, 8, 1, 512, 1e-6f},
         {4096, 1024, 512, 10, 4, 8, 8, 1, 1024, 1e-6f},
     };
-    const int sm_counts[] = {132, 148, 152, 160, 170};
+    const int sm_counts[] = {132, 148, 152, 160};
     int bad = 0;
     for (const moe_layer_desc &d : shapes) {
         Geo g;
@@ -217,8 +226,9 @@ int plan_selftest_host()
                 if (p.S % 16 != 0 || p.S < maxi) ++bad;
                 if (p.smem_bytes > kSmemMax) ++bad;
                 if (p.act_pairs < p.maxr) ++bad;
-                const int rows_cta = (g.Er + sms - 1) / sms;
-                if (p.pb_bytes < (int)align_up((size_t)g.H * 2, 16) + rows_cta * g.rr_bytes) ++bad;
+                const int rows_cta = (g.Er + 1 + sms - 1) / sms;
+                if (rows_cta > kRouterRowsCta || sms > kMaxCtas || p.hrows > kGroup) ++bad;
+                if (p.pb_bytes < (int)align_up((size_t)g.H * 2, 16) + router_slice_bytes(p.hrows, 2, g.Erp, g.qb)) ++bad;
                 if (p.hrows % 2 != 0 || (long long)p.hrows * sms < g.H) ++bad;
                 const long long lim = 1ll << 32;
                 const long long ns[] = {g.Er, g.Is, (long long)p.max_slots * g.I, g.H / 2};
@@ -254,10 +264,11 @@ int ws_layout_selftest_host()
             const int R = w.maxr;
             // the persistent kernel's regions, in order, each holding its data
             const size_t need[][2] = {
-                {w.off_logits, (size_t)kLogitCopies * R * g.Er * 8},
+                {w.off_logits, (size_t)kLogitCopies * R * (g.Er + 1) * 8},
                 {w.off_act, (size_t)w.max_slots * R * g.I * 8},
                 {w.off_act_s, (size_t)R * Is * 8},
                 {w.off_ping, (size_t)2 * R * (g.H / 2) * 8},
+                {w.off_part, (size_t)kMaxCtas * (M < R ? M : R) * (g.Er + 1) * 8},
                 {w.off_stage_in, (size_t)M * g.H * 2},
                 {w.off_stage_out, (size_t)M * g.H * 2},
             };
@@ -333,6 +344,7 @@ int moe_pack_weights(const moe_layer_desc *desc, const moe_src_layer *src, void 
     L->base = static_cast<uint8_t *>(dst_dev);
     L->bytes = dst_bytes;
     L->ptrs.router = L->base + g.off_router;
+    L->ptrs.router_t = L->base + g.off_router_t;
     L->ptrs.gu = L->base + g.off_gu;
     L->ptrs.down = L->base + g.off_down;
     L->ptrs.sgu = g.has_shared ? L->base + g.off_sgu : nullptr;

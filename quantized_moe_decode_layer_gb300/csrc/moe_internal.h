@@ -22,6 +22,8 @@ constexpr int kMaxE = 512;
 constexpr int kMaxK = 32;
 constexpr int kMaxGPL = 4;          // 64-groups per lane of a row: K <= 32 * 64 * kMaxGPL
 constexpr int kLogitCopies = 8;     // copies of the router logits in the workspace (readers spread over them)
+constexpr int kMaxCtas = 160;       // CTAs of a persistent launch (one per SM) at most
+constexpr int kRouterRowsCta = 4;   // router rows one CTA reduces and publishes, at most
 constexpr int kCtrlBytes = 2048;    // control block at the start of the workspace
 constexpr int kSmemMax = 232448;    // dynamic shared memory per CTA on sm_100-class parts
 
@@ -41,11 +43,30 @@ __host__ __device__ constexpr int row_bytes(int K, int bits)
                      : (int)align_up((size_t)K * bits / 8 + (size_t)(K / kGroup) * 4, 16);
 }
 
+// Input-major copy of the router (the persistent kernel's partial logits:
+// each CTA dots every router row with its own slice of the input, so it
+// reads a range of input columns of all rows).  Er rows padded to Erp, a
+// multiple of 16.  Quantised routers: one code byte per (column, row),
+// [H][Erp], then one word (scale | bias << 16) per (group, row), [H/64][Erp].
+// fp32 routers: [H][Erp] floats.
+__host__ __device__ constexpr size_t router_t_bytes(int H, int Erp, int bits)
+{
+    return bits == 0 ? (size_t)H * Erp * 4 : (size_t)H * Erp + (size_t)(H / kGroup) * Erp * 4;
+}
+
+// Bytes of a CTA's slice of that copy: nh columns of every row and the
+// scale/bias words of the ng groups they touch (multiples of 16 bytes).
+__host__ __device__ constexpr int router_slice_bytes(int nh, int ng, int Erp, int bits)
+{
+    return bits == 0 ? nh * Erp * 4 : nh * Erp + ng * Erp * 4;
+}
+
 // Geometry of a layer: sizes, row sizes, blob offsets, launch plan.
 struct Geo {
     int H, I, E, k, Is;
     int has_shared, rb, sb, qb;     // routed / shared / router bits
     int Er;                         // router rows = E + has_shared (last = shared gate)
+    int Erp;                        // Er rounded up to 16 (rows of the input-major router copy)
     int rr_bytes;                   // router row
     int g_bytes;                    // routed gate (or up) row, K = H
     int d_bytes;                    // routed down row, K = I
@@ -53,12 +74,14 @@ struct Geo {
     int sd_bytes;                   // shared down row, K = Is
     float eps;
     // blob offsets (bytes)
-    size_t off_router, off_gamma, off_gamma_next, off_gu, off_down, off_sgu, off_sdown, total;
+    size_t off_router, off_gamma, off_gamma_next, off_router_t, off_gu, off_down, off_sgu, off_sdown, total;
+    size_t rt_sb;                   // scale/bias words inside the input-major router copy (H * Erp)
 };
 
 // Per-layer device pointers inside the packed blob.
 struct LayerPtrs {
     const uint8_t *router;
+    const uint8_t *router_t; // input-major router copy (router_t_bytes)
     const uint8_t *gu;       // E * I units of (gate row, up row)
     const uint8_t *down;     // E * H rows
     const uint8_t *sgu;      // I_shared units
@@ -76,7 +99,7 @@ struct LayerPtrs {
 struct WsLayout {
     int maxr;                // rows per launch
     int max_slots;           // distinct routed experts per launch
-    size_t off_logits, off_act, off_act_s, off_ping, off_stage_in, off_stage_out, total;
+    size_t off_logits, off_act, off_act_s, off_ping, off_part, off_stage_in, off_stage_out, total;
     int max_M;               // rows the host-staging area holds
     // Grouped mode (M above maxr: the tensor-core expert path), sized for
     // grp_rows = min(max_M, kGroupRows) rows and grp_slots = min(E, grp_rows k)

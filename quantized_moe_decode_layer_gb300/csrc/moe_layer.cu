@@ -61,21 +61,29 @@ constexpr int NCW = kConsumerWarps;
 constexpr int NCT = NCW * 32;
 constexpr unsigned FULLMASK = 0xffffffffu;
 constexpr float kXScale = 0x1p100f;  // arranged vectors hold x * 2^100
+// RMSNorm sums of squares: one slot per 256 inputs of a row (H <= 8192),
+// then 1 / rms
+constexpr int kSsChunks = 32;
+constexpr int kRed = kSsChunks + 1;
 
 // ------------------------------------------------------------ shared layout
 
 // Per-CTA constants of a launch, computed once into shared memory: this
 // CTA's router rows, shared gate/up units and output slice, and what its
 // prefetch buffer holds.  The prefetch buffer of a layer is gamma, the
-// router rows, the shared expert's down rows of the output slice (when they
+// CTA's slice of the input-major router (the columns of its output slice,
+// every row), the shared expert's down rows of the output slice (when they
 // fit) and as many of the shared units as fit; the rest go through the ring.
 struct CtaPlan {
-    int ra, rb;        // router rows
+    int ra, rb;        // router rows (row Er: the sum of squares) this CTA sums and publishes
     int ua, ub;        // shared units of this CTA
     int upb;           // units held in the buffer: [ua, ua + upb)
     int h0, nh;        // output slice (whole row pairs): rows h0 .. h0 + nh
     int dpb;           // shared down rows held in the buffer: nh or 0
-    int off_router, off_sdown, off_units, bytes;
+    int g0, ng;        // groups the slice touches: g0 .. g0 + ng
+    int off_router;    // router codes (or fp32 values) of the slice: [nh][Erp]
+    int off_rsb;       // their scale/bias words: [ng][Erp]
+    int off_sdown, off_units, bytes;
 };
 
 // Bytes reserved for the CTA's Sh (pointers into shared memory and launch
@@ -84,7 +92,7 @@ constexpr int kShBytes = 512;
 
 struct SmemLayout {
     int shs, cplan, bar, flags, slot_e, slot_mask, slot_rowbase, sigma, eslot, emask, topv, tope, topw;
-    int row_w, row_pair, red, rred, lscr, pair_src, xs, xsum, act, asum, ysh, yl, pb, ring, total;
+    int row_w, row_pair, red, ru, pair_src, xs, xsum, act, asum, ysh, yl, pb, ring, total;
 };
 
 __host__ __device__ inline int take(int &o, int bytes, int align)
@@ -96,10 +104,6 @@ __host__ __device__ inline int take(int &o, int bytes, int align)
 }
 
 __host__ __device__ inline int imax_of(const Geo &g) { return g.Is > g.I ? g.Is : g.I; }
-
-// Router rows a CTA computes inside the RMSNorm pass (fp32 or 8-bit
-// routers, at most this many rows per CTA; otherwise P1 computes them).
-constexpr int kFusedRouterRows = 4;
 
 // Router rows / shared units taken by one CTA at most.
 __host__ __device__ inline int per_cta(int n, int P) { return (n + P - 1) / P; }
@@ -124,9 +128,8 @@ __host__ __device__ inline SmemLayout carve(const Geo &g, const Plan &p)
     L.topw = take(o, kMaxRows * kMaxK * 4, 4);
     L.row_w = take(o, kMaxRows * kMaxK * 4, 4);
     L.row_pair = take(o, kMaxRows * kMaxK * 4, 4);
-    L.red = take(o, kMaxRows * (NCW + 1) * 4, 4);
-    L.rred = take(o, kMaxRows * kFusedRouterRows * NCW * 4, 4);
-    L.lscr = take(o, NCW * kMaxRows * 4, 4);
+    L.red = take(o, kMaxRows * kRed * 4, 4);
+    L.ru = take(o, 2 * kMaxRows * p.hrows * 4, 16);
     L.pair_src = take(o, p.act_pairs * 4, 4);
     L.xs = take(o, p.maxr * g.H * 4, 16);
     L.xsum = take(o, p.maxr * (g.H / kGroup) * 4, 16);
@@ -334,9 +337,8 @@ struct Sh {
     float *topw;
     float *row_w;        // [kMaxRows][kMaxK]  by expert id
     int *row_pair;
-    float *red;          // [kMaxRows][NCW + 1] RMSNorm partial sums, then 1/rms
-    float *rred;         // [kMaxRows][kFusedRouterRows][NCW] router partial sums per warp
-    float *lscr;         // [NCW][kMaxRows] a warp's router logits before they go out
+    float *red;          // [kMaxRows][kRed] RMSNorm sums of 256-input chunks, then 1/rms
+    float *ru;           // [2][kMaxRows][hrows] the CTA's input slice: gamma * x, then x
     int *pair_src;       // [act_pairs] slot * kMaxRows + row of each staged pair
     float4 *xs;          // [maxr][H / 4] arranged hn * 2^100
     float *xsum;         // [maxr][H / 64] group sums of hn
@@ -407,35 +409,6 @@ __device__ bool wait_bar(const Sh &sh, uint64_t *bar, unsigned parity, int where
             }
         }
     }
-}
-
-// Loads tagged word p until it carries `tag`; returns its payload.  Bounded:
-// on timeout (or when another thread gave up) raises the abort flag and
-// returns 0; callers check aborted() at their next CTA barrier.  Kept out of
-// line: it runs only for data that is not there at the first look.
-__device__ __noinline__ uint32_t poll_tag_slow(const Sh &sh, const uint64_t *p, unsigned tag, int where)
-{
-    const unsigned long long t0 = now_ns();
-#pragma unroll 1
-    for (unsigned it = 1;; ++it) {
-        const uint64_t v = ld_tag(p);
-        if ((unsigned)(v >> 32) == tag) return (uint32_t)v;
-        __nanosleep(32);
-        if ((it & 15) == 0) {
-            if (aborted(sh)) return 0u;
-            if (now_ns() - t0 > (unsigned long long)sh.timeout_ns) {
-                raise_abort(sh, where);
-                return 0u;
-            }
-        }
-    }
-}
-
-__device__ __forceinline__ uint32_t poll_tag(const Sh &sh, const uint64_t *p, unsigned tag, int where)
-{
-    const uint64_t v = ld_tag(p);
-    if ((unsigned)(v >> 32) == tag) return (uint32_t)v;
-    return poll_tag_slow(sh, p, tag, where);
 }
 
 // Bookkeeping of a bounded poll: false once the wait ran out (the abort flag
@@ -898,31 +871,6 @@ __device__ __forceinline__ void gu_k_body(const float4 *xs, const float *xsum, i
     });
 }
 
-// One row of K = H inputs (a router row, or a gate or up row of a shared
-// unit) for token rows g0 .. of `mask`: dst[m * ms] = row . hn_m.
-template <int B, int R>
-__device__ __forceinline__ void one_k_body(const float4 *xs, const float *xsum, int H, const uint8_t *row, uint32_t mask,
-                                   int g0, void *dst, int ms, unsigned tag)
-{
-    const int G = H / kGroup;
-    int rows[R], nv;
-    rows_of_group<R>(mask, g0, rows, nv);
-    uint32_t xq[R];
-    int soff[R];
-#pragma unroll
-    for (int r = 0; r < R; ++r) { xq[r] = smem_u32(xs) + (uint32_t)(rows[r] * H * 4); soff[r] = rows[r] * G; }
-    float xsg[R][kMaxGPL];
-    lane_gsums<R>(smem_u32(xsum), soff, H, xsg);
-    warp_rows<B, 1, R>(row, 0, 1, H, xq, xsg, [&](int, const float (&acc)[1][R]) {
-#pragma unroll
-        for (int r = 0; r < R; ++r)
-            if (r < nv) {
-                if (tag) st_tag(static_cast<uint64_t *>(dst) + (size_t)rows[r] * ms, __float_as_uint(acc[0][r]), tag);
-                else static_cast<float *>(dst)[(size_t)rows[r] * ms] = acc[0][r];
-            }
-    });
-}
-
 // Stores v at element i of dst: a plain fp32 array, or (tag != 0) tagged words.
 __device__ __forceinline__ void put_out(void *dst, size_t i, float v, unsigned tag)
 {
@@ -971,12 +919,6 @@ __device__ __noinline__ void gu_k(const float4 *xs, const float *xsum, int H, co
                                   int rowb, uint32_t mask, int g0, uint64_t *dst, int ld, unsigned tag)
 {
     gu_k_body<B, R>(xs, xsum, H, units, cnt, rowb, mask, g0, dst, ld, tag);
-}
-template <int B, int R>
-__device__ __noinline__ void one_k(const float4 *xs, const float *xsum, int H, const uint8_t *row, uint32_t mask,
-                                   int g0, void *dst, int ms, unsigned tag)
-{
-    one_k_body<B, R>(xs, xsum, H, row, mask, g0, dst, ms, tag);
 }
 template <int B, int R>
 __device__ __noinline__ void dn_k(const float4 *act, const float *asum, int K, const uint8_t *rows0, int cnt,
@@ -1160,28 +1102,6 @@ __device__ __noinline__ void gu_units(const Sh &sh, int H, int bits, const uint8
     });
 }
 
-__device__ __noinline__ void one_row(const Sh &sh, int H, int bits, const uint8_t *row, uint32_t mask,
-                                        void *dst, int ms, unsigned tag)
-{
-    if (__popc(mask) == 1 && H <= 32 * kGroup && bits != 0 && tag == 0u) {
-        const int m = __ffs(mask) - 1;
-        const uint32_t xq = smem_u32(sh.xs) + (uint32_t)(m * H * 4), xsq = smem_u32(sh.xsum) + (uint32_t)(m * (H / kGroup) * 4);
-        float *d = static_cast<float *>(dst) + (size_t)m * ms;
-        if (bits == 6) plain1<6>(smem_u32(row), 1, 0, H, xq, xsq, d, 0, 0u);
-        else if (bits == 8) plain1<8>(smem_u32(row), 1, 0, H, xq, xsq, d, 0, 0u);
-        else plain1<4>(smem_u32(row), 1, 0, H, xq, xsq, d, 0, 0u);
-        return;
-    }
-    for_row_groups(mask, [&](int g0, int nr) {
-        switch (bits * 8 + nr) {
-            MOE_RK_CASES(one_k, (sh.xs, sh.xsum, H, row, mask, g0, dst, ms, tag))
-        case 0 * 8 + 1: one_k<0, 1>(sh.xs, sh.xsum, H, row, mask, g0, dst, ms, tag); break;
-        case 0 * 8 + 2: one_k<0, 2>(sh.xs, sh.xsum, H, row, mask, g0, dst, ms, tag); break;
-        default: break;
-        }
-    });
-}
-
 // dst[h * hs + t * ts] for down row h and the staged pair pair0 + t (t the
 // rank of a row in `mask`): plain fp32, or tagged words when tag != 0.
 __device__ __noinline__ void dn_rows(const Sh &sh, int bits, const uint8_t *rows0, int cnt, int rowb, int K,
@@ -1205,21 +1125,21 @@ __device__ __noinline__ void dn_rows(const Sh &sh, int bits, const uint8_t *rows
 // ------------------------------------------------------------ P0: RMSNorm
 
 // hn rows of x (bf16 [M, H], global) -> xs (arranged, * 2^100) and group
-// sums; 1 / rms of row m -> red[m * (NCW + 1) + NCW].  A thread item is 8
+// sums; 1 / rms of row m -> red[m * kRed + kSsChunks].  A thread item is 8
 // consecutive inputs (one 16-byte load); H / 8 is a multiple of 32, so the
-// 32 items of a warp belong to one row.
+// 32 items of a warp are one aligned chunk of 256 inputs of one row.  The
+// sum of squares is the chunks' warp sums added in chunk order: the same
+// for every row whatever M is and however many warps take part.  Run by compute warps w0 .. NCW - 1
+// (the first w0 route meanwhile), which meet at their own named barrier.
 __device__ void build_hn(const KParams &kp, const Sh &sh, const void *x, unsigned xtag, const uint16_t *gamma,
-                         const uint8_t *rrows = nullptr, int nr = 0)
+                         int w0)
 {
-    const int H = kp.g.H, M = kp.M, G = H / kGroup, tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+    const int H = kp.g.H, M = kp.M, G = H / kGroup, lane = threadIdx.x & 31;
+    const int tid = threadIdx.x - 32 * w0, nt = 32 * (NCW - w0);
     const int per_row = H / 8, lpr = ilog2(per_row), total = M * per_row;
-#pragma unroll 1
-    for (int m = lane; m < M; m += 32) sh.red[m * (NCW + 1) + warp] = 0.f;
-#pragma unroll 1
-    for (int i = lane; i < M * kFusedRouterRows; i += 32) sh.rred[i * NCW + warp] = 0.f;
-    __syncwarp();
-    // pass 1: sums of squares per (row, warp); raw values into xs.  Two
-    // items per thread and round, both loads in flight before either is used.
+    auto bar = [nt]() { asm volatile("bar.sync 5, %0;" ::"r"(nt) : "memory"); };
+    // pass 1: sums of squares per (row, warp); raw values into xs.  Several
+    // items per thread and round, all loads in flight before any is used.
     auto item = [&](int it, const uint32_t (&aw)[4]) {
         float ss = 0.f;
         if (it < total) {
@@ -1240,11 +1160,11 @@ __device__ void build_hn(const KParams &kp, const Sh &sh, const void *x, unsigne
         }
         ss = warp_sum(ss);
         const int wfirst = it - lane;
-        if (lane == 0 && wfirst < total) sh.red[(wfirst >> lpr) * (NCW + 1) + warp] += ss;
+        if (lane == 0 && wfirst < total) sh.red[(wfirst >> lpr) * kRed + ((wfirst & (per_row - 1)) >> 5)] = ss;
     };
-    constexpr int NI = 4;   // items per thread and round, all loads in flight before any is used
+    constexpr int NI = 4;   // items per thread and round
 #pragma unroll 1
-    for (int base = 0; base < total; base += NI * NCT) {
+    for (int base = 0; base < total; base += NI * nt) {
         uint32_t a[NI][4];
         if (xtag) {
             // the previous layer's output: tagged bf16 pairs
@@ -1252,7 +1172,7 @@ __device__ void build_hn(const KParams &kp, const Sh &sh, const void *x, unsigne
             const uint64_t *p[NI];
 #pragma unroll
             for (int n = 0; n < NI; ++n) {
-                const int it = base + tid + n * NCT;
+                const int it = base + tid + n * nt;
                 p[n] = it < total ? xt + (size_t)(it >> lpr) * (H / 2) + 4 * (it & (per_row - 1)) : nullptr;
             }
             poll_items<NI>(sh, p, xtag, 40, a);
@@ -1260,7 +1180,7 @@ __device__ void build_hn(const KParams &kp, const Sh &sh, const void *x, unsigne
             const uint4 *xp = reinterpret_cast<const uint4 *>(x);
 #pragma unroll
             for (int n = 0; n < NI; ++n) {
-                const int it = base + tid + n * NCT;
+                const int it = base + tid + n * nt;
                 uint4 v = make_uint4(0u, 0u, 0u, 0u);
                 if (it < total) v = __ldcg(xp + it);
                 a[n][0] = v.x; a[n][1] = v.y; a[n][2] = v.z; a[n][3] = v.w;
@@ -1268,34 +1188,27 @@ __device__ void build_hn(const KParams &kp, const Sh &sh, const void *x, unsigne
         }
 #pragma unroll
         for (int n = 0; n < NI; ++n)
-            if (n == 0 || base + n * NCT < total) item(base + tid + n * NCT, a[n]);
+            if (n == 0 || base + n * nt < total) item(base + tid + n * nt, a[n]);
     }
-    cbar();
-    if (tid == 0 && xtag) stamp(kp, (int)(xtag - sh.epoch), 19);
+    bar();
+    if (tid == 0 && xtag) stamp(kp, (int)(xtag - sh.epoch), 16);
     if (tid < M) {
         float t = 0.f;
 #pragma unroll 1
-        for (int w = 0; w < NCW; ++w) t += sh.red[tid * (NCW + 1) + w];
-        sh.red[tid * (NCW + 1) + NCW] = rsqrtf(t / (float)H + kp.g.eps);
+        for (int c = 0; c < per_row / 32; ++c) t += sh.red[tid * kRed + c];
+        sh.red[tid * kRed + kSsChunks] = rsqrtf(t / (float)H + kp.g.eps);
     }
-    cbar();
+    bar();
     if (tid == 0 && xtag) stamp(kp, (int)(xtag - sh.epoch), 20);
-    // pass 2: scale by rinv * gamma * 2^100; group sums of hn; and (rrows
-    // given) the CTA's router rows dotted with hn: per item of 8 inputs
-    // s * sum q h + b * sum h (8-bit rows) or sum w h (fp32 rows), summed
-    // over the warp and then, in warp order, over the CTA (the same order for
-    // every token row, whatever M is)
-    const int qb = kp.g.qb, rrb = kp.g.rr_bytes;
+    // pass 2: scale by rinv * gamma * 2^100, and the group sums of hn (8
+    // consecutive items make a group)
 #pragma unroll 1
-    for (int base = 0; base < total; base += NCT) {
+    for (int base = 0; base < total; base += nt) {
         const int it = base + tid;
         float gs = 0.f;
-        float rp[kFusedRouterRows];
-#pragma unroll
-        for (int r = 0; r < kFusedRouterRows; ++r) rp[r] = 0.f;
         if (it < total) {
             const int m = it >> lpr, c = it & (per_row - 1);
-            const float rinv = sh.red[m * (NCW + 1) + NCW];
+            const float rinv = sh.red[m * kRed + kSsChunks];
             const uint4 gv = *reinterpret_cast<const uint4 *>(gamma + c * 8);
             const uint32_t gw[4] = {gv.x, gv.y, gv.z, gv.w};
             const int g = c >> 3, t = (c & 7) * 2;
@@ -1311,57 +1224,157 @@ __device__ void build_hn(const KParams &kp, const Sh &sh, const void *x, unsigne
             for (int j = 0; j < 8; ++j) gs += h[j];
             row[t * G + g] = make_float4(h[0] * kXScale, h[1] * kXScale, h[2] * kXScale, h[3] * kXScale);
             row[(t + 1) * G + g] = make_float4(h[4] * kXScale, h[5] * kXScale, h[6] * kXScale, h[7] * kXScale);
-#pragma unroll
-            for (int r = 0; r < kFusedRouterRows; ++r)
-                if (r < nr) {
-                    const uint8_t *rw = rrows + (size_t)r * rrb;
-                    if (qb == 8) {
-                        const uint2 cw = *reinterpret_cast<const uint2 *>(rw + 8 * c);
-                        const uint32_t sbw = *reinterpret_cast<const uint32_t *>(rw + H + g * 4);
-                        float qh = 0.f, hs = 0.f;
-#pragma unroll
-                        for (int j = 0; j < 8; ++j) {
-                            const uint32_t q = ((j < 4 ? cw.x : cw.y) >> (8 * (j & 3))) & 0xFFu;
-                            qh = fmaf(code_float(q), h[j], qh);
-                            hs += h[j];
-                        }
-                        rp[r] = fmaf(__uint_as_float(sbw << 16), qh, __uint_as_float(sbw & 0xFFFF0000u) * hs);
-                    } else {
-                        const float4 w0 = *reinterpret_cast<const float4 *>(rw + 32 * c);
-                        const float4 w1 = *reinterpret_cast<const float4 *>(rw + 32 * c + 16);
-                        rp[r] = fmaf(w0.x, h[0], fmaf(w0.y, h[1], fmaf(w0.z, h[2], fmaf(w0.w, h[3],
-                                fmaf(w1.x, h[4], fmaf(w1.y, h[5], fmaf(w1.z, h[6], w1.w * h[7])))))));
-                    }
-                }
         }
-        // the warp's sums of the router dots (the tree of warp_sum) and the
-        // group sums (8 consecutive items make a group), all reductions'
-        // levels interleaved with no branch between them so that the
-        // independent shuffles overlap; rows past nr add zeros
 #pragma unroll
-        for (int o = 16; o >= 1; o >>= 1) {
-#pragma unroll
-            for (int r = 0; r < kFusedRouterRows; ++r) rp[r] += __shfl_xor_sync(FULLMASK, rp[r], o);
-            if (o <= 4) gs += __shfl_xor_sync(FULLMASK, gs, o);
-        }
-        {
-            const int wfirst = it - lane;
-            if (lane == 0 && wfirst < total) {
-#pragma unroll
-                for (int r = 0; r < kFusedRouterRows; ++r)
-                    if (r < nr) sh.rred[((wfirst >> lpr) * kFusedRouterRows + r) * NCW + warp] += rp[r];
-            }
-        }
+        for (int o = 4; o >= 1; o >>= 1) gs += __shfl_xor_sync(FULLMASK, gs, o);
         if (it < total && (it & 7) == 0) {
             const int m = it >> lpr, c = it & (per_row - 1);
             sh.xsum[m * G + (c >> 3)] = gs;
         }
     }
     if (tid == 0 && xtag) stamp(kp, (int)(xtag - sh.epoch), 21);
+    bar();
+}
+
+// Partial router dots (every compute warp, at the start of a layer): the
+// CTA dots every router row with gamma * x over its own output slice of the
+// layer input, and adds up x^2 over the slice, for each token row m, and
+// publishes the Er + 1 sums as tagged words part[m][e][CTA] (e = Er: the
+// squares).  The logit of router row e is rinv_m times the sum over CTAs of
+// part[m][e][.], rinv_m = 1 / sqrt(sum over CTAs of part[m][Er][.] / H +
+// eps) (reduce_logits sums, top-k scales): the RMSNorm's scale is a common
+// factor of the row's products (flash-moe, "Metal Compute Shaders": RMS
+// normalisation; PureDrive model card, "Summary": the router of 256 experts
+// plus the shared expert's gate), so no CTA needs the whole input first.
+// The slice of x is the CTA's own output of the previous layer, which
+// combine left in shared memory (layer 0: the caller's rows).  Quantised
+// rows: each weight dequantised as s q + b (fp32) before its product.
+__device__ void router_partials(const KParams &kp, const Sh &sh, const uint64_t *part, int l)
+{
+    const Geo &g = kp.g;
+    const CtaPlan &b = *sh.cp;
+    const int M = kp.M, H = g.H, nh = b.nh, h0 = b.h0, Er = g.Er, E1 = Er + 1, Erp = g.Erp, P = gridDim.x;
+    const int hr = sh.hrows, tid = threadIdx.x;
+    const unsigned tag = layer_tag(sh, l);
+    const uint16_t *gamma = reinterpret_cast<const uint16_t *>(sh.pb);
+    float *u = sh.ru, *xv = sh.ru + kMaxRows * hr;
 #pragma unroll 1
-    for (int e = tid; e < kp.g.E; e += NCT) sh.emask[e] = 0u;
+    for (int t = tid; t < M * nh; t += NCT) {
+        const int m = t / nh, j = t - m * nh;
+        if (l == 0) xv[m * hr + j] = bf2f(kp.x[(size_t)m * H + h0 + j]);
+        u[m * hr + j] = xv[m * hr + j] * bf2f(gamma[h0 + j]);
+    }
     cbar();
-    if (tid == 0 && xtag) stamp(kp, (int)(xtag - sh.epoch), 22);
+    if (tid == 0) stamp(kp, l, 17);
+    const uint8_t *codes = sh.pb + b.off_router;
+    const uint32_t *sbw = reinterpret_cast<const uint32_t *>(sh.pb + b.off_rsb);
+    const float *wf = reinterpret_cast<const float *>(sh.pb + b.off_router);
+    // columns from js on belong to the slice's second group
+    const int js = b.ng > 1 ? (b.g0 + 1) * kGroup - h0 : nh;
+    uint64_t *dst = const_cast<uint64_t *>(part) + blockIdx.x;
+    // items rotated by the routing warps' threads, so that items past the
+    // first NCT go to the other warps and the routing warps start reducing
+    // first
+    const int rot = (tid + 32 * M) % NCT;
+#pragma unroll 1
+    for (int t = rot; t < M * E1; t += NCT) {
+        const int m = t / E1, e = t - m * E1;
+        const float *um = u + m * hr;
+        float acc = 0.f;
+        if (e == Er) {
+            const float *xm = xv + m * hr;
+#pragma unroll 4
+            for (int j = 0; j < nh; ++j) acc = fmaf(xm[j], xm[j], acc);
+        } else if (g.qb) {
+            const uint32_t w0 = sbw[e], w1 = b.ng > 1 ? sbw[Erp + e] : w0;
+            const float s0 = __uint_as_float(w0 << 16), b0 = __uint_as_float(w0 & 0xFFFF0000u);
+            const float s1 = __uint_as_float(w1 << 16), b1 = __uint_as_float(w1 & 0xFFFF0000u);
+#pragma unroll 4
+            for (int j = 0; j < nh; ++j) {
+                const bool hi = j >= js;
+                const float wt = fmaf(hi ? s1 : s0, code_float(codes[j * Erp + e]), hi ? b1 : b0);
+                acc = fmaf(wt, um[j], acc);
+            }
+        } else {
+#pragma unroll 4
+            for (int j = 0; j < nh; ++j) acc = fmaf(wf[j * Erp + e], um[j], acc);
+        }
+        st_tag(dst + (size_t)t * P, __float_as_uint(acc), tag);
+    }
+}
+
+// The logits of this CTA's router rows [ra, rb) for token row m, before
+// the RMSNorm scale, or (row Er) the row's sum of squares (one warp): every
+// CTA's partial sums, each lane adding
+// CTAs lane, lane + 32, ... in turn and the lanes then combined by a
+// butterfly (every lane ends with the same sums; the order depends on
+// nothing but the row), published as tagged words, kLogitCopies copies
+// each.  The words of a router row are read by this CTA alone.
+__device__ __noinline__ void reduce_logits(const KParams &kp, const Sh &sh, const uint64_t *part, uint64_t *logits,
+                                           int m, int l)
+{
+    const Geo &g = kp.g;
+    const CtaPlan &b = *sh.cp;
+    const int lane = threadIdx.x & 31, E1 = g.Er + 1, nr = b.rb - b.ra, P = gridDim.x;
+    const unsigned tag = layer_tag(sh, l);
+    if (nr <= 0) return;
+    constexpr int NC = (kMaxCtas + 31) / 32;
+    const uint64_t *rows = part + ((size_t)m * E1 + b.ra) * P;
+    // all words of the lane's CTAs requested together, then every missing
+    // one again in each round until all are there (each word has this one
+    // reader); the rounds are the whole warp's, so that no lane's wait is
+    // serialised behind another's (bounded: zeros after a timeout)
+    uint64_t v[NC][kRouterRowsCta];
+#pragma unroll
+    for (int i = 0; i < NC; ++i)
+#pragma unroll
+        for (int r = 0; r < kRouterRowsCta; ++r) {
+            const int c = lane + 32 * i;
+            v[i][r] = c < P && r < nr ? ld_tag(rows + (size_t)r * P + c) : (uint64_t)tag << 32;
+        }
+    unsigned long long t0 = 0;
+    unsigned it = 0;
+#pragma unroll 1
+    for (;;) {
+        bool missing = false;
+#pragma unroll
+        for (int i = 0; i < NC; ++i)
+#pragma unroll
+            for (int r = 0; r < kRouterRowsCta; ++r) missing |= (unsigned)(v[i][r] >> 32) != tag;
+        if (!__any_sync(FULLMASK, missing)) break;
+        if (!__all_sync(FULLMASK, poll_more(sh, ++it, t0, 45))) {
+#pragma unroll
+            for (int i = 0; i < NC; ++i)
+#pragma unroll
+                for (int r = 0; r < kRouterRowsCta; ++r) v[i][r] = (uint64_t)tag << 32;
+            break;
+        }
+#pragma unroll
+        for (int i = 0; i < NC; ++i)
+#pragma unroll
+            for (int r = 0; r < kRouterRowsCta; ++r)
+                if ((unsigned)(v[i][r] >> 32) != tag) v[i][r] = ld_tag(rows + (size_t)r * P + lane + 32 * i);
+    }
+    if (threadIdx.x == 0) stamp(kp, l, 23);
+    float acc[kRouterRowsCta];
+#pragma unroll
+    for (int r = 0; r < kRouterRowsCta; ++r) {
+        acc[r] = 0.f;
+#pragma unroll
+        for (int i = 0; i < NC; ++i)
+            if (lane + 32 * i < P && r < nr) acc[r] += __uint_as_float((uint32_t)v[i][r]);
+    }
+#pragma unroll
+    for (int o = 16; o >= 1; o >>= 1)
+#pragma unroll
+        for (int r = 0; r < kRouterRowsCta; ++r) acc[r] += __shfl_xor_sync(FULLMASK, acc[r], o);
+#pragma unroll
+    for (int r = 0; r < kRouterRowsCta; ++r) {
+        const int e = b.ra + r;
+        // (debug switch: one logit of layer 0 stays unpublished)
+        if (r < nr && lane < kLogitCopies && !(l == 0 && kp.skip_row == e))
+            st_tag(logits + ((size_t)lane * kp.ws_l.maxr + m) * E1 + e, __float_as_uint(acc[r]), tag);
+    }
 }
 
 // Activations (fp32 rows in global memory) of `n` staged pairs: pair p =
@@ -1440,14 +1453,15 @@ template <int NPL>
 __device__ __noinline__ void topk_row_t(const KParams &kp, const Sh &sh, int m, const uint64_t *logits, unsigned tag)
 {
     const int lane = threadIdx.x & 31;
-    const int E = kp.g.E, k = kp.g.k;
+    const int E = kp.g.E, k = kp.g.k, Er = kp.g.Er;
     // this CTA's copy of the logits
-    const uint64_t *row = logits + ((size_t)(blockIdx.x % kLogitCopies) * kp.ws_l.maxr + m) * kp.g.Er;
-    // the lane's logits and the shared expert's gate logit, all loaded
-    // together; while some are missing the lane polls the first missing one
-    // alone (every CTA polls these words), then loads them all again
+    const uint64_t *row = logits + ((size_t)(blockIdx.x % kLogitCopies) * kp.ws_l.maxr + m) * (Er + 1);
+    // the lane's logits, the shared expert's gate logit and the row's sum of
+    // squares, all loaded together; while some are missing the lane polls
+    // the first missing one alone (every CTA polls these words), then loads
+    // them all again
     const uint64_t none = (uint64_t)tag << 32;
-    uint64_t v[NPL + 1];
+    uint64_t v[NPL + 2];
     unsigned long long t0 = 0;
     unsigned it = 0;
 #pragma unroll 1
@@ -1455,10 +1469,11 @@ __device__ __noinline__ void topk_row_t(const KParams &kp, const Sh &sh, int m, 
 #pragma unroll
         for (int i = 0; i < NPL; ++i) v[i] = lane + 32 * i < E ? ld_tag(row + lane + 32 * i) : none;
         v[NPL] = kp.g.has_shared ? ld_tag(row + E) : none;
+        v[NPL + 1] = ld_tag(row + Er);
         const uint64_t *pm = nullptr;
 #pragma unroll
-        for (int i = NPL; i >= 0; --i)
-            if ((unsigned)(v[i] >> 32) != tag) pm = i < NPL ? row + lane + 32 * i : row + E;
+        for (int i = NPL + 1; i >= 0; --i)
+            if ((unsigned)(v[i] >> 32) != tag) pm = i < NPL ? row + lane + 32 * i : i == NPL ? row + E : row + Er;
         bool more = true;
         if (pm) {
 #pragma unroll 1
@@ -1468,9 +1483,12 @@ __device__ __noinline__ void topk_row_t(const KParams &kp, const Sh &sh, int m, 
     }
     if (threadIdx.x == 0) stamp(kp, (int)(tag - sh.epoch - 1u), 15);
     uint32_t key[NPL];
+    // the published logits are the router dots before the RMSNorm scale
+    const float rinv = rsqrtf(__uint_as_float((uint32_t)v[NPL + 1]) / (float)kp.g.H + kp.g.eps);
 #pragma unroll
-    for (int i = 0; i < NPL; ++i) key[i] = lane + 32 * i < E ? fkey(__uint_as_float((uint32_t)v[i])) : 0u;
-    const float lsg = __uint_as_float((uint32_t)v[NPL]);
+    for (int i = 0; i < NPL; ++i)
+        key[i] = lane + 32 * i < E ? fkey(__uint_as_float((uint32_t)v[i]) * rinv) : 0u;
+    const float lsg = __uint_as_float((uint32_t)v[NPL]) * rinv;
     float *topv = sh.topv + m * kMaxK;
     int *tope = sh.tope + m * kMaxK;
 #pragma unroll 1
@@ -1545,6 +1563,10 @@ __device__ void route(const KParams &kp, const Sh &sh, const uint64_t *logits, i
     const unsigned tag = layer_tag(sh, l);
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     const int E = kp.g.E, k = kp.g.k, M = kp.M;
+    if (M > 1 && warp == 0) {
+#pragma unroll 1
+        for (int e = lane; e < E; e += 32) sh.emask[e] = 0u;
+    }
     topk_row(kp, sh, warp, logits, tag);
     if (threadIdx.x == 0) stamp(kp, l, 12);
     if (M > 1) rbar(M);
@@ -1649,6 +1671,7 @@ struct Ws {
     uint64_t *act;      // [max_slots][maxr][I] fp32
     uint64_t *act_s;    // [maxr][Is] fp32
     uint64_t *ping[2];  // [maxr][H / 2] bf16 pairs: layer outputs (tag of the layer that wrote them)
+    uint64_t *part;     // [M][Er][CTA] fp32 partial router dots
 };
 
 __device__ __forceinline__ Ws ws_views(const KParams &kp)
@@ -1659,6 +1682,7 @@ __device__ __forceinline__ Ws ws_views(const KParams &kp)
     w.act_s = reinterpret_cast<uint64_t *>(kp.ws + kp.ws_l.off_act_s);
     w.ping[0] = reinterpret_cast<uint64_t *>(kp.ws + kp.ws_l.off_ping);
     w.ping[1] = w.ping[0] + (size_t)kp.ws_l.maxr * (kp.g.H / 2);
+    w.part = reinterpret_cast<uint64_t *>(kp.ws + kp.ws_l.off_part);
     return w;
 }
 
@@ -1668,15 +1692,18 @@ __device__ __forceinline__ Ws ws_views(const KParams &kp)
 __device__ void cta_plan(const KParams &kp, CtaPlan &b)
 {
     const Geo &g = kp.g;
-    split(g.Er, gridDim.x, blockIdx.x, b.ra, b.rb);
+    split(g.Er + 1, gridDim.x, blockIdx.x, b.ra, b.rb);
     int h1;
     hslice(g.H, b.h0, h1);
     b.nh = h1 - b.h0;
     b.ua = b.ub = 0;
     const bool sh_on = kp.mode == kModeLayers && g.has_shared;
     if (sh_on) split(g.Is, gridDim.x, blockIdx.x, b.ua, b.ub);
+    b.g0 = b.h0 / kGroup;
+    b.ng = b.nh > 0 ? (b.h0 + b.nh - 1) / kGroup - b.g0 + 1 : 0;
     b.off_router = (int)align_up((size_t)g.H * 2, 16);
-    b.off_sdown = b.off_router + (b.rb - b.ra) * g.rr_bytes;
+    b.off_rsb = b.off_router + router_slice_bytes(b.nh, 0, g.Erp, g.qb);
+    b.off_sdown = b.off_router + router_slice_bytes(b.nh, b.ng, g.Erp, g.qb);
     b.dpb = sh_on && b.off_sdown + b.nh * g.sd_bytes <= kp.p.pb_bytes ? b.nh : 0;
     b.off_units = b.off_sdown + b.dpb * g.sd_bytes;
     const int ub2 = 2 * g.sg_bytes;
@@ -1864,9 +1891,14 @@ __device__ __forceinline__ void pb_issue(const KParams &kp, const Sh &sh, int l)
     const LayerPtrs &Lp = kp.layer[l];
     mbar_expect_tx(sh.pb_full, (unsigned)b.bytes);
     bulk_load(sh.pb, Lp.gamma, (unsigned)(g.H * 2), sh.pb_full);
-    if (b.rb > b.ra)
-        bulk_load(sh.pb + b.off_router, Lp.router + (size_t)b.ra * g.rr_bytes, (unsigned)((b.rb - b.ra) * g.rr_bytes),
+    if (b.nh > 0) {
+        const size_t esz = g.qb ? 1 : 4;
+        bulk_load(sh.pb + b.off_router, Lp.router_t + (size_t)b.h0 * g.Erp * esz, (unsigned)(b.nh * g.Erp * esz),
                   sh.pb_full);
+        if (g.qb)
+            bulk_load(sh.pb + b.off_rsb, Lp.router_t + g.rt_sb + (size_t)b.g0 * g.Erp * 4, (unsigned)(b.ng * g.Erp * 4),
+                      sh.pb_full);
+    }
     if (b.dpb > 0)
         bulk_load(sh.pb + b.off_sdown, Lp.sdown + (size_t)b.h0 * g.sd_bytes, (unsigned)(b.dpb * g.sd_bytes), sh.pb_full);
     if (b.upb > 0)
@@ -1987,74 +2019,37 @@ __device__ __forceinline__ void consume(const Sh &sh, Cursor &c, int where, F &&
     if ((threadIdx.x & 31) == 0) mbar_arrive(&sh.empty[slot], 1);
 }
 
-// True when this CTA's router rows are computed inside the RMSNorm pass
-// (fp32 or 8-bit router, few enough rows per CTA).
-__device__ __forceinline__ bool router_fused(const KParams &kp, const Sh &sh)
-{
-    return (kp.g.qb == 0 || kp.g.qb == 8) && sh.cp->rb - sh.cp->ra <= kFusedRouterRows;
-}
-
-// Logits of the router rows computed in the RMSNorm pass: the warps' partial
-// sums added in warp order, then the 8 copies of each out as tagged words.
-__device__ void publish_fused_logits(const KParams &kp, const Sh &sh, const Ws &w, int l)
-{
-    const CtaPlan &b = *sh.cp;
-    const int nr = b.rb - b.ra, M = kp.M, Er = kp.g.Er;
-    const unsigned tag = layer_tag(sh, l);
-#pragma unroll 1
-    for (int t = threadIdx.x; t < M * nr; t += NCT) {
-        const int m = t / nr, r = t - m * nr, e = b.ra + r;
-        float v = 0.f;
-#pragma unroll 1
-        for (int wp = 0; wp < NCW; ++wp) v += sh.rred[(m * kFusedRouterRows + r) * NCW + wp];
-        // (debug switch: one logit of layer 0 stays unpublished)
-        if (l == 0 && kp.skip_row == e) continue;
-#pragma unroll 1
-        for (int c = 0; c < kLogitCopies; ++c)
-            st_tag(w.logits + ((size_t)c * kp.ws_l.maxr + m) * Er + e, __float_as_uint(v), tag);
-    }
-}
-
-// P1 and routing.  With M at most half the compute warps, the first M warps
-// route (one token row each), waiting on every CTA's router logits, while
-// the other warps compute this CTA's router rows first (the logits every CTA
-// waits for go out first) and then its shared-expert gate/up units from the
-// prefetch buffer, one range of units per warp, publishing their SwiGLU
-// activations.  With more rows every warp computes first and the first M
-// route after.  Shared units past the buffer come through the ring, one stage
-// to each compute warp in turn.
-__device__ void phase1(const KParams &kp, const Sh &sh, const LayerPtrs &Lp, Cursor &q, const Ws &w, int l)
+// P0 and P1 (after router_partials).  With M at most half the compute
+// warps, the first M warps each take one token row: they sum the CTA's
+// router logits of that row from every CTA's partials, publish them and
+// route (waiting on every CTA's logits), while the other warps build hn
+// (the RMSNorm of the whole input, gathered from every CTA's outputs) and
+// then compute the CTA's shared-expert gate/up units from the prefetch
+// buffer, one range of units per warp, publishing their SwiGLU activations.
+// With more rows every warp builds hn, the first M publish logits, every
+// warp computes the shared units and the first M route after.  Shared units
+// past the buffer come through the ring, one stage to each compute warp in
+// turn.
+__device__ void phase1(const KParams &kp, const Sh &sh, const LayerPtrs &Lp, Cursor &q, const Ws &w, int l,
+                       const void *xin, unsigned xtag)
 {
     const Geo &g = kp.g;
     const uint32_t all = (1u << kp.M) - 1u;
     const int warp = threadIdx.x >> 5, M = kp.M;
     const CtaPlan &b = *sh.cp;
-    const int nr = router_fused(kp, sh) ? 0 : b.rb - b.ra;   // router rows not done in the RMSNorm pass
     const bool early = 2 * M <= NCW;
-    const int w0 = early ? M : 0;   // first warp computing rows
+    const int w0 = early ? M : 0;   // first warp building hn
     const unsigned tag = layer_tag(sh, l);
     wstamp(kp, l, 14);
     if (early && warp < M) {
+        reduce_logits(kp, sh, w.part, w.logits, warp, l);
+        if (threadIdx.x == 0) stamp(kp, l, 22);
         route(kp, sh, w.logits, l);
     } else {
+        build_hn(kp, sh, xin, xtag, reinterpret_cast<const uint16_t *>(sh.pb), w0);
+        if (threadIdx.x == 32 * w0) stamp(kp, l, 1);
+        if (!early && warp < M) reduce_logits(kp, sh, w.part, w.logits, warp, l);
         const int i0 = warp - w0, nw = NCW - w0;
-#pragma unroll 1
-        for (int i = i0; i < nr; i += nw) {
-            // the M logits of router row e, then their copies out
-            const int e = b.ra + i;
-            float *lv = sh.lscr + warp * kMaxRows;
-            one_row(sh, g.H, g.qb, sh.pb + b.off_router + (size_t)i * g.rr_bytes, all, lv, 1, 0u);
-            __syncwarp();
-            const int lane = threadIdx.x & 31;
-            // (debug switch: one logit of layer 0 stays unpublished)
-            if (!(l == 0 && kp.skip_row == e))
-#pragma unroll 1
-                for (int t = lane; t < kLogitCopies * M; t += 32) {
-                    const int c = t / M, m = t - c * M;
-                    st_tag(w.logits + ((size_t)c * kp.ws_l.maxr + m) * g.Er + e, __float_as_uint(lv[m]), tag);
-                }
-            __syncwarp();
-        }
         if (kp.mode == kModeLayers && b.upb > 0) {
             int u0, u1;
             split(b.upb, nw, i0, u0, u1);
@@ -2064,10 +2059,10 @@ __device__ void phase1(const KParams &kp, const Sh &sh, const LayerPtrs &Lp, Cur
         }
     }
     wstamp(kp, l, 15);
-    if (!early) {
-        cbar();
-        if (warp < M) route(kp, sh, w.logits, l);
-    }
+    // hn complete (the routing warps go on to shared units that came through
+    // the ring, which read it)
+    cbar();
+    if (!early && warp < M) route(kp, sh, w.logits, l);
     if (kp.mode != kModeLayers) return;
     if (b.ub - b.ua > b.upb)
         sched_p1x(kp, sh, Lp, [&](const uint8_t *, int, int, int first, int n) {
@@ -2222,6 +2217,11 @@ __device__ void combine(const KParams &kp, const Sh &sh, int l, const float (&xr
     const uint32_t pair = o[0] | (o[1] << 16);
     if (tagged) st_tag(tagged + (size_t)m * (g.H / 2) + h0 / 2 + pl, pair, tag);
     if (plain) *reinterpret_cast<uint32_t *>(plain + (size_t)m * g.H + h0 + 2 * pl) = pair;
+    // the CTA's slice of the next layer's input, for its partial router dots
+    // and residuals
+    float *xv = sh.ru + kMaxRows * hr + m * hr + 2 * pl;
+    xv[0] = bf2f((uint16_t)o[0]);
+    xv[1] = bf2f((uint16_t)o[1]);
 }
 
 // out_n = bf16(out * rinv * gamma_next) for this CTA's outputs, with rinv from
@@ -2232,7 +2232,7 @@ __device__ void final_normed(const KParams &kp, const Sh &sh, const uint64_t *xt
                              const uint16_t *gamma_next)
 {
     const int H = kp.g.H, M = kp.M, G = H / kGroup;
-    build_hn(kp, sh, xt, tag, gamma_next);
+    build_hn(kp, sh, xt, tag, gamma_next, 0);
     if (cbar_or(aborted(sh))) return;
     const int h0 = sh.cp->h0, nh = sh.cp->nh;
 #pragma unroll 1
@@ -2257,7 +2257,7 @@ __device__ __forceinline__ void compute(const KParams &kp, const Sh &sh)
 {
     const Ws w = ws_views(kp);
     Cursor q = cursor0();
-    const int h0 = sh.cp->h0, np = sh.cp->nh / 2, M = kp.M, H = kp.g.H;
+    const int np = sh.cp->nh / 2, M = kp.M;
     const int warp = threadIdx.x >> 5;
 #pragma unroll 1
     for (int l = 0; l < kp.L; ++l) {
@@ -2271,13 +2271,9 @@ __device__ __forceinline__ void compute(const KParams &kp, const Sh &sh)
         const bool pb_ok = wait_bar(sh, sh.pb_full, (unsigned)l & 1u, 5);
         if (t0) stamp(kp, l, 18);
         if (cbar_or(!pb_ok)) return;
-        const bool fused = router_fused(kp, sh);
-        build_hn(kp, sh, xin, xtag, reinterpret_cast<const uint16_t *>(sh.pb), fused ? sh.pb + sh.cp->off_router : nullptr,
-                 fused ? sh.cp->rb - sh.cp->ra : 0);
-        if (cbar_or(aborted(sh))) return;
-        if (fused) publish_fused_logits(kp, sh, w, l);
-        if (t0) stamp(kp, l, 1);
-        phase1(kp, sh, Lp, q, w, l);
+        router_partials(kp, sh, w.part, l);
+        if (t0) stamp(kp, l, 19);
+        phase1(kp, sh, Lp, q, w, l, xin, xtag);
         if (t0) stamp(kp, l, 2);
         if (t0) stamp(kp, l, 3);
         if (cbar_or(aborted(sh))) return;
@@ -2289,12 +2285,11 @@ __device__ __forceinline__ void compute(const KParams &kp, const Sh &sh)
         // residuals of this thread's output pair
         float xr[2] = {0.f, 0.f};
         if ((int)threadIdx.x < np * M) {
+            // this CTA's slice of the layer input, kept in shared memory
             const int pl = threadIdx.x / M, m = threadIdx.x % M;
-            uint32_t pair;
-            if (l == 0) pair = *reinterpret_cast<const uint32_t *>(kp.x + (size_t)m * H + h0 + 2 * pl);
-            else pair = poll_tag(sh, w.ping[(l - 1) & 1] + (size_t)m * (H / 2) + h0 / 2 + pl, xtag, 43);
-            xr[0] = bf2f((uint16_t)(pair & 0xFFFFu));
-            xr[1] = bf2f((uint16_t)(pair >> 16));
+            const float *xv = sh.ru + kMaxRows * sh.hrows + m * sh.hrows + 2 * pl;
+            xr[0] = xv[0];
+            xr[1] = xv[1];
         }
         wstamp(kp, l, 0);
         wstamp(kp, l, 1);
@@ -2364,8 +2359,7 @@ __global__ void __launch_bounds__(kThreads, 1) moe_decode_kernel(const __grid_co
         sh.row_w = reinterpret_cast<float *>(smem + L.row_w);
         sh.row_pair = reinterpret_cast<int *>(smem + L.row_pair);
         sh.red = reinterpret_cast<float *>(smem + L.red);
-        sh.rred = reinterpret_cast<float *>(smem + L.rred);
-        sh.lscr = reinterpret_cast<float *>(smem + L.lscr);
+        sh.ru = reinterpret_cast<float *>(smem + L.ru);
         sh.pair_src = reinterpret_cast<int *>(smem + L.pair_src);
         sh.xs = reinterpret_cast<float4 *>(smem + L.xs);
         sh.xsum = reinterpret_cast<float *>(smem + L.xsum);
@@ -2755,7 +2749,8 @@ bool make_plan(const Geo &g, int maxr, int num_sms, Plan &p)
     }
     const int Im = imax_of(g);
     const int pair_bytes = Im * 4 + (Im / kGroup) * 4 + 4;
-    const int pb_min = (int)align_up((size_t)g.H * 2, 16) + per_cta(g.Er, num_sms) * g.rr_bytes;
+    if (num_sms > kMaxCtas || per_cta(g.Er + 1, num_sms) > kRouterRowsCta || p.hrows > kGroup) return false;
+    const int pb_min = (int)align_up((size_t)g.H * 2, 16) + router_slice_bytes(p.hrows, 2, g.Erp, g.qb);
     // plus the CTA's shared down rows and shared gate/up units: with all of
     // them at hand, P1 needs no ring stages
     const int pb_all = pb_min + (g.has_shared ? p.hrows * g.sd_bytes + per_cta(g.Is, num_sms) * 2 * g.sg_bytes : 0);

@@ -137,10 +137,57 @@ __global__ void export_kernel(const uint8_t *base, size_t stride, size_t offset,
     }
 }
 
+// The input-major router copy (router_t_bytes) from the packed router rows:
+// code (column h, row e) as one byte at h * Erp + e, and row e's scale/bias
+// word of group g at H * Erp + g * Erp + e (fp32 routers: the value at
+// h * Erp + e).  Consecutive threads take consecutive rows of one column.
+// Rows Er .. Erp - 1 stay as the caller cleared them (zero).
+template <int BITS>
+__global__ void router_t_kernel(const uint8_t *rows, int rr_bytes, int Er, int H, int Erp, uint8_t *dst)
+{
+    const long long total = (long long)Er * H;
+    for (long long t = blockIdx.x * (long long)blockDim.x + threadIdx.x; t < total;
+         t += (long long)gridDim.x * blockDim.x) {
+        const int e = (int)(t % Er), h = (int)(t / Er);
+        const uint8_t *row = rows + (size_t)e * rr_bytes;
+        if constexpr (BITS == 0) {
+            reinterpret_cast<float *>(dst)[(size_t)h * Erp + e] = reinterpret_cast<const float *>(row)[h];
+        } else {
+            const uint32_t *dw = reinterpret_cast<const uint32_t *>(row);
+            const int o = h * BITS, wi = o >> 5, sh = o & 31;
+            uint32_t v = dw[wi] >> sh;
+            if (sh + BITS > 32) v |= dw[wi + 1] << (32 - sh);
+            dst[(size_t)h * Erp + e] = (uint8_t)(v & ((1u << BITS) - 1u));
+            if ((h & (kGroup - 1)) == 0) {
+                const uint32_t sbw = reinterpret_cast<const uint32_t *>(row + (size_t)H * BITS / 8)[h / kGroup];
+                reinterpret_cast<uint32_t *>(dst + (size_t)H * Erp)[(size_t)(h / kGroup) * Erp + e] = sbw;
+            }
+        }
+    }
+}
+
 int grid_for(long long work)
 {
     long long b = (work + 255) / 256;
     return (int)(b < 1 ? 1 : (b > 4096 ? 4096 : b));
+}
+
+int router_t_fill(const Geo &g, uint8_t *b, cudaStream_t st)
+{
+    const int grid = grid_for((long long)g.Er * g.H);
+    const uint8_t *rows = b + g.off_router;
+    uint8_t *dst = b + g.off_router_t;
+    switch (g.qb) {
+    case 0: router_t_kernel<0><<<grid, 256, 0, st>>>(rows, g.rr_bytes, g.Er, g.H, g.Erp, dst); break;
+    case 4: router_t_kernel<4><<<grid, 256, 0, st>>>(rows, g.rr_bytes, g.Er, g.H, g.Erp, dst); break;
+    case 6: router_t_kernel<6><<<grid, 256, 0, st>>>(rows, g.rr_bytes, g.Er, g.H, g.Erp, dst); break;
+    case 8: router_t_kernel<8><<<grid, 256, 0, st>>>(rows, g.rr_bytes, g.Er, g.H, g.Erp, dst); break;
+    default: return MOE_ERR_UNSUPPORTED;
+    }
+    note_launch();
+    cudaError_t e = cudaGetLastError();
+    if (e != cudaSuccess) { note_cuda_error((int)e); return MOE_ERR_CUDA; }
+    return MOE_OK;
 }
 
 int pack_matrix(const moe_src_matrix &m, int bits, int rows, int K, PackDst dst, cudaStream_t st)
@@ -191,6 +238,7 @@ int launch_pack(const moe_layer &L, const moe_src_layer &src, cudaStream_t st)
                               PackDst{b + g.off_router + (size_t)g.E * g.rr_bytes, (size_t)g.rr_bytes, 0}, st)))
             return rc;
     }
+    if ((rc = router_t_fill(g, b, st))) return rc;
     e = cudaMemcpyAsync(b + g.off_gamma, src.gamma_dev, (size_t)g.H * 2, cudaMemcpyDeviceToDevice, st);
     if (e == cudaSuccess && src.gamma_next_dev)
         e = cudaMemcpyAsync(b + g.off_gamma_next, src.gamma_next_dev, (size_t)g.H * 2, cudaMemcpyDeviceToDevice, st);

@@ -97,7 +97,7 @@ __global__ void __launch_bounds__(256) gather_kernel(const CopyJob *jobs)
 StreamedLayout streamed_layout(const Geo &g, int n_slots)
 {
     StreamedLayout s;
-    size_t o = align_up(g.off_gu, 256);   // router, gamma, gamma_next at their blob offsets
+    size_t o = align_up(g.off_gu, 256);   // router (both copies), gamma, gamma_next at their blob offsets
     s.cache_gu = o;
     o = align_up(o + (size_t)n_slots * g.I * 2 * g.g_bytes, 256);
     s.cache_down = o;
@@ -272,6 +272,7 @@ int moe_streamed_create(const moe_layer *packed, void *host_blob, size_t host_by
     s->layer.bytes = dev_bytes;
     LayerPtrs &p = s->layer.ptrs;
     p.router = dev + g.off_router;
+    p.router_t = dev + g.off_router_t;
     p.gamma = reinterpret_cast<const uint16_t *>(dev + g.off_gamma);
     p.gamma_next = packed->ptrs.gamma_next ? reinterpret_cast<const uint16_t *>(dev + g.off_gamma_next) : nullptr;
     p.gu = dev + sl.cache_gu;

@@ -228,7 +228,7 @@ void moe_stack_destroy(moe_stack *stack);
  * Errors: INVALID_ARG, UNSUPPORTED (shape, or a device index above 63),
  * BUFFER_TOO_SMALL (scratch too small), CUDA; errors raised while the
  * kernels run (a device wait that gave up) are read with moe_noalloc_status. */
-#define MOE_NOALLOC_SCRATCH_BYTES (4u << 20)
+#define MOE_NOALLOC_SCRATCH_BYTES (16u << 20)
 int moe_decode_layer_noalloc(const moe_layer *layer, const uint16_t *x_dev, int M, uint16_t *out_dev,
                              uint16_t *out_normed_dev, moe_stream_t stream);
 

@@ -112,8 +112,13 @@ void make_ws_layout(const Geo &g, int max_M, WsLayout &w)
     // router logits before the RMSNorm scale, and (last) the row's sum of
     // squares: [kLogitCopies][R][Er + 1]
     w.off_logits = put((size_t)kLogitCopies * R * (g.Er + 1) * 8);
-    w.off_act = put((size_t)w.max_slots * R * g.I * 8);
-    w.off_act_s = put((size_t)R * (g.Is ? g.Is : 1) * 8);
+    // activations: [kActCopies][slot][row][I] and [kActCopies][row][Is],
+    // rows of one launch (at most min(max_M, R))
+    const int Mr = max_M < R ? max_M : R;
+    w.act_cs = (size_t)(g.E < Mr * g.k ? g.E : Mr * g.k) * Mr * g.I;
+    w.act_s_cs = (size_t)Mr * (g.Is ? g.Is : 1);
+    w.off_act = put((size_t)kActCopies * w.act_cs * 8);
+    w.off_act_s = put((size_t)kActCopies * w.act_s_cs * 8);
     w.off_ping = put((size_t)2 * R * (g.H / 2) * 8);
     // partial router dots and sums of squares: [row][Er + 1][CTA], for the
     // rows of one launch
@@ -265,8 +270,9 @@ int ws_layout_selftest_host()
             // the persistent kernel's regions, in order, each holding its data
             const size_t need[][2] = {
                 {w.off_logits, (size_t)kLogitCopies * R * (g.Er + 1) * 8},
-                {w.off_act, (size_t)w.max_slots * R * g.I * 8},
-                {w.off_act_s, (size_t)R * Is * 8},
+                {w.off_act, (size_t)kActCopies * (g.E < (M < R ? M : R) * g.k ? g.E : (M < R ? M : R) * g.k) *
+                                (M < R ? M : R) * g.I * 8},
+                {w.off_act_s, (size_t)kActCopies * (M < R ? M : R) * Is * 8},
                 {w.off_ping, (size_t)2 * R * (g.H / 2) * 8},
                 {w.off_part, (size_t)kMaxCtas * (M < R ? M : R) * (g.Er + 1) * 8},
                 {w.off_stage_in, (size_t)M * g.H * 2},

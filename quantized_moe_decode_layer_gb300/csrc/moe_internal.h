@@ -24,6 +24,7 @@ constexpr int kMaxGPL = 4;          // 64-groups per lane of a row: K <= 32 * 64
 constexpr int kLogitCopies = 8;     // copies of the router logits in the workspace (readers spread over them)
 constexpr int kMaxCtas = 160;       // CTAs of a persistent launch (one per SM) at most
 constexpr int kRouterRowsCta = 4;   // router rows one CTA reduces and publishes, at most
+constexpr int kActCopies = 1;       // copies of the exchanged activations (more copies measured slower)
 constexpr int kCtrlBytes = 2048;    // control block at the start of the workspace
 constexpr int kSmemMax = 232448;    // dynamic shared memory per CTA on sm_100-class parts
 
@@ -100,6 +101,7 @@ struct WsLayout {
     int maxr;                // rows per launch
     int max_slots;           // distinct routed experts per launch
     size_t off_logits, off_act, off_act_s, off_ping, off_part, off_stage_in, off_stage_out, total;
+    size_t act_cs, act_s_cs; // words of one copy of the routed / shared activations
     int max_M;               // rows the host-staging area holds
     // Grouped mode (M above maxr: the tensor-core expert path), sized for
     // grp_rows = min(max_M, kGroupRows) rows and grp_slots = min(E, grp_rows k)

@@ -428,40 +428,44 @@ __device__ __forceinline__ bool poll_more(const Sh &sh, unsigned it, unsigned lo
 }
 
 // N items of four consecutive tagged words each (16-byte aligned; null for
-// no item): payloads into out[n].  All words are loaded together; while some
-// are missing, the lane polls the first missing one alone (many CTAs poll the
-// same words: fewer requests while waiting) and then loads all of them
-// again.  Bounded (poll_more); payloads are 0 after a timeout.
+// no item): payloads into out[n].  All words are loaded together, then in
+// each round the warp loads again every pair of words that is still
+// missing, until no lane misses any: the rounds are the whole warp's, one
+// memory round trip each, so that no lane's wait is serialised behind
+// another's.  Every lane of the warp takes part.  Bounded (poll_more);
+// payloads are 0 after a timeout.
 template <int N>
 __device__ __forceinline__ void poll_items(const Sh &sh, const uint64_t *const (&p)[N], unsigned tag, int where,
                                            uint32_t (&out)[N][4])
 {
     const uint64_t none = (uint64_t)tag << 32;
     uint64_t v[N][4];
+#pragma unroll
+    for (int n = 0; n < N; ++n) {
+        v[n][0] = v[n][1] = v[n][2] = v[n][3] = none;
+        if (p[n]) { ld_tag2(p[n], v[n][0], v[n][1]); ld_tag2(p[n] + 2, v[n][2], v[n][3]); }
+    }
     unsigned long long t0 = 0;
     unsigned it = 0;
 #pragma unroll 1
     for (;;) {
+        bool missing = false;
 #pragma unroll
-        for (int n = 0; n < N; ++n) {
-            v[n][0] = v[n][1] = v[n][2] = v[n][3] = none;
-            if (p[n]) { ld_tag2(p[n], v[n][0], v[n][1]); ld_tag2(p[n] + 2, v[n][2], v[n][3]); }
-        }
-        const uint64_t *pm = nullptr;
+        for (int n = 0; n < N; ++n)
 #pragma unroll
-        for (int n = N - 1; n >= 0; --n)
-#pragma unroll
-            for (int j = 3; j >= 0; --j)
-                if ((unsigned)(v[n][j] >> 32) != tag) pm = p[n] + j;
-        if (!pm) break;
-        bool more = true;
-#pragma unroll 1
-        while ((more = poll_more(sh, ++it, t0, where)) && (unsigned)(ld_tag(pm) >> 32) != tag) {}
-        if (!more) {
+            for (int j = 0; j < 4; ++j) missing |= (unsigned)(v[n][j] >> 32) != tag;
+        if (!__any_sync(FULLMASK, missing)) break;
+        if (!__all_sync(FULLMASK, poll_more(sh, ++it, t0, where))) {
 #pragma unroll
             for (int n = 0; n < N; ++n) v[n][0] = v[n][1] = v[n][2] = v[n][3] = 0;
             break;
         }
+#pragma unroll
+        for (int n = 0; n < N; ++n)
+#pragma unroll
+            for (int j = 0; j < 4; j += 2)
+                if ((unsigned)(v[n][j] >> 32) != tag || (unsigned)(v[n][j + 1] >> 32) != tag)
+                    ld_tag2(p[n] + j, v[n][j], v[n][j + 1]);
     }
 #pragma unroll
     for (int n = 0; n < N; ++n)
@@ -843,7 +847,7 @@ __device__ __forceinline__ void for_row_groups(uint32_t mask, F &&f)
 // dst[m * ld + u] = silu(gate) * up.
 template <int B, int R>
 __device__ __forceinline__ void gu_k_body(const float4 *xs, const float *xsum, int H, const uint8_t *units, int cnt,
-                                  int rowb, uint32_t mask, int g0, uint64_t *dst, int ld, unsigned tag)
+                                  int rowb, uint32_t mask, int g0, uint64_t *dst, int ld, size_t cs, unsigned tag)
 {
     const int G = H / kGroup;
     int rows[R], nv;
@@ -863,8 +867,10 @@ __device__ __forceinline__ void gu_k_body(const float4 *xs, const float *xsum, i
                 for (int r = 0; r < R; ++r)
                     if (r < nv) {
                         const float gt = acc[k2][r], up = acc[k2 + 1][r];
-                        st_tag(dst + (size_t)rows[r] * ld + ((rb + k2) >> 1),
-                               __float_as_uint(gt / (1.0f + expf(-gt)) * up), tag);
+                        const uint32_t a = __float_as_uint(gt / (1.0f + expf(-gt)) * up);
+#pragma unroll
+                        for (int c = 0; c < kActCopies; ++c)
+                            st_tag(dst + c * cs + (size_t)rows[r] * ld + ((rb + k2) >> 1), a, tag);
                     }
             }
         }
@@ -916,9 +922,9 @@ __device__ __forceinline__ void dn_k_body(const float4 *act, const float *asum, 
 // Out-of-line entry points of the row kernels (one per instantiation).
 template <int B, int R>
 __device__ __noinline__ void gu_k(const float4 *xs, const float *xsum, int H, const uint8_t *units, int cnt,
-                                  int rowb, uint32_t mask, int g0, uint64_t *dst, int ld, unsigned tag)
+                                  int rowb, uint32_t mask, int g0, uint64_t *dst, int ld, size_t cs, unsigned tag)
 {
-    gu_k_body<B, R>(xs, xsum, H, units, cnt, rowb, mask, g0, dst, ld, tag);
+    gu_k_body<B, R>(xs, xsum, H, units, cnt, rowb, mask, g0, dst, ld, cs, tag);
 }
 template <int B, int R>
 __device__ __noinline__ void dn_k(const float4 *act, const float *asum, int K, const uint8_t *rows0, int cnt,
@@ -1038,7 +1044,7 @@ __device__ __forceinline__ void rows1(uint32_t rows, int rstride, int nrows, int
 // unit.
 template <int BITS>
 __device__ __noinline__ void gu1(uint32_t units, int cnt, int rowb, int H, uint32_t xq, uint32_t xsq, uint64_t *dst,
-                                 unsigned tag)
+                                 size_t cs, unsigned tag)
 {
     const int lane = threadIdx.x & 31;
     const int G = H >> 6, lgL = ilog2(G), LPR = 1 << lgL, RPP = 32 >> lgL;
@@ -1061,7 +1067,11 @@ __device__ __noinline__ void gu1(uint32_t units, int cnt, int rowb, int H, uint3
             gt += __shfl_xor_sync(FULLMASK, gt, o);
             up += __shfl_xor_sync(FULLMASK, up, o);
         }
-        if (g == 0 && u0 + lr < cnt) st_tag(dst + u0 + lr, __float_as_uint(gt / (1.0f + expf(-gt)) * up), tag);
+        if (g == 0 && u0 + lr < cnt) {
+            const uint32_t a = __float_as_uint(gt / (1.0f + expf(-gt)) * up);
+#pragma unroll
+            for (int c = 0; c < kActCopies; ++c) st_tag(dst + c * cs + u0 + lr, a, tag);
+        }
     }
 }
 
@@ -1083,20 +1093,20 @@ __device__ __noinline__ void plain1(uint32_t rows, int cnt, int rowb, int K, uin
     case 8 * 8 + 2: FN<8, 2> ARGS; break;
 
 __device__ __noinline__ void gu_units(const Sh &sh, int H, int bits, const uint8_t *units, int cnt, int rowb,
-                                         uint32_t mask, uint64_t *dst, int ld, unsigned tag)
+                                         uint32_t mask, uint64_t *dst, int ld, size_t cs, unsigned tag)
 {
     if (__popc(mask) == 1 && H <= 32 * kGroup && bits != 0) {
         const int m = __ffs(mask) - 1;
         const uint32_t xq = smem_u32(sh.xs) + (uint32_t)(m * H * 4), xsq = smem_u32(sh.xsum) + (uint32_t)(m * (H / kGroup) * 4);
         uint64_t *d = dst + (size_t)m * ld;
-        if (bits == 6) gu1<6>(smem_u32(units), cnt, rowb, H, xq, xsq, d, tag);
-        else if (bits == 8) gu1<8>(smem_u32(units), cnt, rowb, H, xq, xsq, d, tag);
-        else gu1<4>(smem_u32(units), cnt, rowb, H, xq, xsq, d, tag);
+        if (bits == 6) gu1<6>(smem_u32(units), cnt, rowb, H, xq, xsq, d, cs, tag);
+        else if (bits == 8) gu1<8>(smem_u32(units), cnt, rowb, H, xq, xsq, d, cs, tag);
+        else gu1<4>(smem_u32(units), cnt, rowb, H, xq, xsq, d, cs, tag);
         return;
     }
     for_row_groups(mask, [&](int g0, int nr) {
         switch (bits * 8 + nr) {
-            MOE_RK_CASES(gu_k, (sh.xs, sh.xsum, H, units, cnt, rowb, mask, g0, dst, ld, tag))
+            MOE_RK_CASES(gu_k, (sh.xs, sh.xsum, H, units, cnt, rowb, mask, g0, dst, ld, cs, tag))
         default: break;
         }
     });
@@ -1457,29 +1467,27 @@ __device__ __noinline__ void topk_row_t(const KParams &kp, const Sh &sh, int m, 
     // this CTA's copy of the logits
     const uint64_t *row = logits + ((size_t)(blockIdx.x % kLogitCopies) * kp.ws_l.maxr + m) * (Er + 1);
     // the lane's logits, the shared expert's gate logit and the row's sum of
-    // squares, all loaded together; while some are missing the lane polls
-    // the first missing one alone (every CTA polls these words), then loads
-    // them all again
+    // squares, all loaded together, then in each round of the whole warp
+    // every word still missing again
     const uint64_t none = (uint64_t)tag << 32;
     uint64_t v[NPL + 2];
+    auto addr = [&](int i) { return i < NPL ? row + lane + 32 * i : i == NPL ? row + E : row + Er; };
+#pragma unroll
+    for (int i = 0; i < NPL; ++i) v[i] = lane + 32 * i < E ? ld_tag(addr(i)) : none;
+    v[NPL] = kp.g.has_shared ? ld_tag(addr(NPL)) : none;
+    v[NPL + 1] = ld_tag(addr(NPL + 1));
     unsigned long long t0 = 0;
     unsigned it = 0;
 #pragma unroll 1
     for (;;) {
+        bool missing = false;
 #pragma unroll
-        for (int i = 0; i < NPL; ++i) v[i] = lane + 32 * i < E ? ld_tag(row + lane + 32 * i) : none;
-        v[NPL] = kp.g.has_shared ? ld_tag(row + E) : none;
-        v[NPL + 1] = ld_tag(row + Er);
-        const uint64_t *pm = nullptr;
+        for (int i = 0; i < NPL + 2; ++i) missing |= (unsigned)(v[i] >> 32) != tag;
+        if (!__any_sync(FULLMASK, missing)) break;
+        if (!__all_sync(FULLMASK, poll_more(sh, ++it, t0, 42))) break;
 #pragma unroll
-        for (int i = NPL + 1; i >= 0; --i)
-            if ((unsigned)(v[i] >> 32) != tag) pm = i < NPL ? row + lane + 32 * i : i == NPL ? row + E : row + Er;
-        bool more = true;
-        if (pm) {
-#pragma unroll 1
-            while ((more = poll_more(sh, ++it, t0, 42)) && (unsigned)(ld_tag(pm) >> 32) != tag) {}
-        }
-        if (!__any_sync(FULLMASK, pm != nullptr) || !__all_sync(FULLMASK, more)) break;
+        for (int i = 0; i < NPL + 2; ++i)
+            if ((unsigned)(v[i] >> 32) != tag) v[i] = ld_tag(addr(i));
     }
     if (threadIdx.x == 0) stamp(kp, (int)(tag - sh.epoch - 1u), 15);
     uint32_t key[NPL];
@@ -1668,8 +1676,8 @@ __device__ void route(const KParams &kp, const Sh &sh, const uint64_t *logits, i
 // Workspace buffers shared between CTAs, all of tagged words.
 struct Ws {
     uint64_t *logits;   // [kLogitCopies][maxr][Er] fp32 (each CTA reads copy blockIdx % kLogitCopies)
-    uint64_t *act;      // [max_slots][maxr][I] fp32
-    uint64_t *act_s;    // [maxr][Is] fp32
+    uint64_t *act;      // [kActCopies][slot][M][I] fp32 (each CTA reads copy blockIdx % kActCopies)
+    uint64_t *act_s;    // [kActCopies][M][Is] fp32
     uint64_t *ping[2];  // [maxr][H / 2] bf16 pairs: layer outputs (tag of the layer that wrote them)
     uint64_t *part;     // [M][Er][CTA] fp32 partial router dots
 };
@@ -2055,7 +2063,7 @@ __device__ void phase1(const KParams &kp, const Sh &sh, const LayerPtrs &Lp, Cur
             split(b.upb, nw, i0, u0, u1);
             if (u1 > u0)
                 gu_units(sh, g.H, g.sb, sh.pb + b.off_units + (size_t)u0 * 2 * g.sg_bytes, u1 - u0, g.sg_bytes, all,
-                         w.act_s + b.ua + u0, g.Is, tag);
+                         w.act_s + b.ua + u0, g.Is, kp.ws_l.act_s_cs, tag);
         }
     }
     wstamp(kp, l, 15);
@@ -2067,7 +2075,7 @@ __device__ void phase1(const KParams &kp, const Sh &sh, const LayerPtrs &Lp, Cur
     if (b.ub - b.ua > b.upb)
         sched_p1x(kp, sh, Lp, [&](const uint8_t *, int, int, int first, int n) {
             consume(sh, q, 10, [&](const uint8_t *st) {
-                gu_units(sh, g.H, g.sb, st, n, g.sg_bytes, all, w.act_s + b.ua + first, g.Is, tag);
+                gu_units(sh, g.H, g.sb, st, n, g.sg_bytes, all, w.act_s + b.ua + first, g.Is, kp.ws_l.act_s_cs, tag);
             });
         });
 }
@@ -2082,7 +2090,9 @@ __device__ void shared_down_light(const KParams &kp, const Sh &sh, const Ws &w, 
     const Geo &g = kp.g;
     const int M = kp.M, lane = threadIdx.x & 31;
     stage_acts(sh, M, g.Is, rank * 32 + lane, nw * 32, layer_tag(sh, l),
-               [&](int p) -> const uint64_t * { return w.act_s + (size_t)p * g.Is; });
+               [&](int p) -> const uint64_t * {
+                   return w.act_s + (blockIdx.x % kActCopies) * kp.ws_l.act_s_cs + (size_t)p * g.Is;
+               });
     asm volatile("bar.sync 4, %0;" ::"r"(nw * 32) : "memory");
     const uint32_t all = (1u << M) - 1u;
     const CtaPlan &b = *sh.cp;
@@ -2123,7 +2133,6 @@ __device__ void phase2(const KParams &kp, const Sh &sh, const LayerPtrs &Lp, Cur
                        int &turn0)
 {
     const Geo &g = kp.g;
-    const int maxr = kp.ws_l.maxr;
     const unsigned tag = layer_tag(sh, l);
     StageTrace tr{kp.trace ? &kp : nullptr, l, 0, 2, 1};
     n2 = 0;
@@ -2131,8 +2140,8 @@ __device__ void phase2(const KParams &kp, const Sh &sh, const LayerPtrs &Lp, Cur
     sched_p2(kp, sh, Lp, [&](const uint8_t *, int, int s, int first, int n) {
         ++n2;
         consume(sh, q, 20, [&](const uint8_t *st) {
-            uint64_t *act = w.act + (size_t)s * maxr * g.I;
-            gu_units(sh, g.H, g.rb, st, n, g.g_bytes, sh.slot_mask[s], act + first, g.I, tag);
+            uint64_t *act = w.act + (size_t)s * kp.M * g.I;
+            gu_units(sh, g.H, g.rb, st, n, g.g_bytes, sh.slot_mask[s], act + first, g.I, kp.ws_l.act_cs, tag);
         }, &tr);
     });
 }
@@ -2145,7 +2154,7 @@ __device__ void phase2(const KParams &kp, const Sh &sh, const LayerPtrs &Lp, Cur
 __device__ bool phase3(const KParams &kp, const Sh &sh, const LayerPtrs &Lp, Cursor &q, const Ws &w, int l)
 {
     const Geo &g = kp.g;
-    const int maxr = kp.ws_l.maxr, U = sh.flags[1], hr = sh.hrows;
+    const int U = sh.flags[1], hr = sh.hrows;
     const unsigned tag = layer_tag(sh, l);
     StageTrace tr{kp.trace ? &kp : nullptr, l, 0, 7, 1};
     int s0 = 0;
@@ -2167,7 +2176,8 @@ __device__ bool phase3(const KParams &kp, const Sh &sh, const LayerPtrs &Lp, Cur
         cbar();
         stage_acts(sh, np, g.I, threadIdx.x, NCT, tag, [&](int p) -> const uint64_t * {
             const int ps = sh.pair_src[p];
-            return w.act + ((size_t)(ps / kMaxRows) * maxr + ps % kMaxRows) * g.I;
+            return w.act + (blockIdx.x % kActCopies) * kp.ws_l.act_cs +
+                   ((size_t)(ps / kMaxRows) * kp.M + ps % kMaxRows) * g.I;
         });
         if (cbar_or(aborted(sh))) return false;
         sched_p3(kp, sh, Lp, [&](const uint8_t *, int, int s, int first, int n) {
@@ -2307,7 +2317,9 @@ __device__ __forceinline__ void compute(const KParams &kp, const Sh &sh)
             if (r0 == 0 || d >= r0) shared_down_light(kp, sh, w, l, r0 == 0 ? d : d - r0, nw);
         } else if (kp.g.has_shared) {
             stage_acts(sh, M, kp.g.Is, threadIdx.x, NCT, layer_tag(sh, l),
-                       [&](int p) -> const uint64_t * { return w.act_s + (size_t)p * kp.g.Is; });
+                       [&](int p) -> const uint64_t * {
+                           return w.act_s + (blockIdx.x % kActCopies) * kp.ws_l.act_s_cs + (size_t)p * kp.g.Is;
+                       });
             cbar();
             shared_down_pb(kp, sh, 0);
             phase1b(kp, sh, Lp, q, l);

@@ -7,18 +7,24 @@
 // routed experts (and shared-expert rows that do not fit elsewhere), each
 // stage consumed by one compute warp, issued one lane per stage so that the
 // copies of a layer go out together; and a prefetch buffer with the next
-// layer's RMSNorm weight, router rows and shared-expert rows, which do not
-// depend on routing and are therefore loaded while the current layer still
+// layer's RMSNorm weight, the CTA's column slice of the router and
+// shared-expert rows, which do not depend on routing and are therefore loaded while the current layer still
 // runs.  Per layer:
 //
-//   P0  every CTA: RMSNorm of the M input rows into shared memory
-//       (flash-moe, "Metal Compute Shaders": RMS normalisation)
-//   P1  this CTA's router rows (plus the shared-expert gate row), published
-//       first, then its shared-expert gate/up units and their SwiGLU; the
-//       first M warps meanwhile wait for every CTA's logits and route:
-//       softmax + top-k + renormalisation per row and the list of distinct
-//       selected experts with the rows that chose each (PureDrive model
-//       card, "Summary": the full top-8 of 256 is kept)
+//   P0  every CTA: partial router dots -- every router row dotted with
+//       gamma * x over the CTA's own output slice of the layer input (its
+//       own output of the previous layer), and x^2 summed over the slice --
+//       published as tagged words (flash-moe, "Metal Compute Shaders": RMS
+//       normalisation; PureDrive model card, "Summary": 256 experts plus
+//       the shared expert's gate)
+//   P1  the first M warps, one token row each: the CTA's router rows summed
+//       over every CTA's partials and published, then softmax + top-k +
+//       renormalisation on every CTA's logits scaled by the row's
+//       1 / rms, and the list of distinct selected experts with the rows
+//       that chose each (model card, "Summary": the full top-8 of 256 is
+//       kept); meanwhile the other warps gather the whole input, build its
+//       RMSNorm into shared memory and compute this CTA's shared-expert
+//       gate/up units and their SwiGLU
 //   P2  gate/up units of the selected experts, each expert streamed once for
 //       all the rows that chose it (model card, "How it works": the verify
 //       pass reads its weights once), SwiGLU
@@ -29,9 +35,10 @@
 //   N   the fused next RMSNorm of the bf16 output (model card: fused
 //       add+RMSNorm), or the next layer's P0.
 //
-// CTAs exchange data (router logits, activations, layer outputs) as tagged
-// words in global memory that readers poll; there is no grid barrier
-// between phases or layers.
+// CTAs exchange data (partial router dots, router logits, activations,
+// layer outputs) as tagged words in global memory that readers poll, a
+// whole warp's missing words per round; there is no grid barrier between
+// phases or layers.
 //
 // Dequantisation (moe_unpack.cuh).  A lane takes one 64-code group of a
 // weight row.  A masked code read as a float is the subnormal

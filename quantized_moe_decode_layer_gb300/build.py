@@ -1,6 +1,6 @@
 """Build of the in-tree CUDA library libmoe.so for sm_103a.
 
-The seven translation units compile in parallel with nvcc
+The eight translation units compile in parallel with nvcc
 (-gencode arch=compute_103a,code=sm_103a) and link into
 quantized_moe_decode_layer_gb300/libmoe.so next to this file.  Objects go to
 _build/ at the repository root.  build(debug_bounds=True) makes the
@@ -20,7 +20,8 @@ CSRC = os.path.join(HERE, "csrc")
 OUT = os.path.join(HERE, "libmoe.so")
 OUT_DEBUG = os.path.join(HERE, "libmoe_debug.so")
 OBJDIR = os.path.join(ROOT, "_build")
-SOURCES = ["moe_abi.cu", "moe_pack.cu", "moe_layer.cu", "moe_tc.cu", "moe_grouped.cu", "moe_attn.cu", "moe_stream.cu"]
+SOURCES = ["moe_abi.cu", "moe_pack.cu", "moe_layer.cu", "moe_layer_w8.cu", "moe_tc.cu", "moe_grouped.cu", "moe_attn.cu",
+           "moe_stream.cu"]
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 
 

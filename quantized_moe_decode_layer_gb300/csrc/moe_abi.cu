@@ -188,7 +188,7 @@ int plan_for(KParams &kp, int mc)
 {
     const int sms = device_sms();
     if (sms <= 0) return MOE_ERR_CUDA;
-    if (!make_plan(kp.g, mc, sms, kp.p)) return MOE_ERR_UNSUPPORTED;
+    if (!decode_plan(kp.g, mc, sms, kp.p)) return MOE_ERR_UNSUPPORTED;
     kp.M = mc;
     return MOE_OK;
 }
@@ -226,8 +226,8 @@ int plan_selftest_host()
         for (int sms : sm_counts)
             for (int mc = 1; mc <= R; ++mc) {
                 Plan p;
-                if (!make_plan(g, mc, sms, p)) { ++bad; continue; }
-                if (p.NS % kConsumerWarps != 0 || p.NS > 32 || p.NS > kMaxStages) ++bad;
+                if (!decode_plan(g, mc, sms, p)) { ++bad; continue; }
+                if (p.ncw != decode_warps(g) || p.NS % p.ncw != 0 || p.NS > 32 || p.NS > kMaxStages) ++bad;
                 if (p.S % 16 != 0 || p.S < maxi) ++bad;
                 if (p.smem_bytes > kSmemMax) ++bad;
                 if (p.act_pairs < p.maxr) ++bad;
@@ -415,7 +415,7 @@ int moe_router_topk(const moe_layer *layer, const uint16_t *x_dev, int M, int32_
         kp.x = x_dev + (size_t)c0 * H;
         kp.idx_out = idx_dev + (size_t)c0 * k;
         kp.w_out = w_dev + (size_t)c0 * k;
-        if ((rc = launch_decode(kp, reinterpret_cast<cudaStream_t>(stream)))) return rc;
+        if ((rc = decode_launch(kp, reinterpret_cast<cudaStream_t>(stream)))) return rc;
     }
     return MOE_OK;
 }
@@ -460,7 +460,7 @@ int decode_layer_impl(const moe_layer *layer, const uint16_t *x_dev, int M, uint
         kp.x = x_dev + (size_t)c0 * H;
         kp.out = out_dev + (size_t)c0 * H;
         kp.out_normed = out_normed_dev ? out_normed_dev + (size_t)c0 * H : nullptr;
-        if ((rc = launch_decode(kp, reinterpret_cast<cudaStream_t>(stream)))) return rc;
+        if ((rc = decode_launch(kp, reinterpret_cast<cudaStream_t>(stream)))) return rc;
     }
     return MOE_OK;
 }
@@ -519,7 +519,7 @@ int moe_stack_forward(moe_stack *stack, const uint16_t *x_dev, int M, uint16_t *
             kp.out = out_dev + (size_t)c0 * H;
             const bool final_group = l0 + nl == stack->L;
             kp.out_normed = final_group && out_normed_dev ? out_normed_dev + (size_t)c0 * H : nullptr;
-            if ((rc = launch_decode(kp, reinterpret_cast<cudaStream_t>(stream)))) return rc;
+            if ((rc = decode_launch(kp, reinterpret_cast<cudaStream_t>(stream)))) return rc;
         }
     }
     return MOE_OK;

@@ -13,8 +13,6 @@ namespace moe {
 
 constexpr int kGroup = 64;          // affine group along the contraction axis
 constexpr int kSub = 16;            // codes per sub-group (one lane step)
-constexpr int kConsumerWarps = 8;   // compute warps per CTA (9 warps in all: up to 224 registers per thread)
-constexpr int kThreads = (kConsumerWarps + 1) * 32;  // + one TMA producer warp
 constexpr int kMaxRows = 8;         // token rows per launch (larger M is chunked)
 constexpr int kMaxLayers = 64;      // layers per persistent launch
 constexpr int kMaxStages = 64;      // ring stages (mbarrier pairs)
@@ -140,6 +138,7 @@ struct Plan {
     int pb_bytes;            // prefetch buffer (gamma, router rows, shared units of a layer)
     int act_pairs;           // (slot, row) activation vectors the staging buffer holds
     int smem_bytes;
+    int ncw;                 // compute warps of the kernel build the plan is for
 };
 
 enum Mode { kModeLayers = 0, kModeRouter = 1 };
@@ -168,7 +167,20 @@ constexpr int kTraceEvents = 24; // events recorded per (CTA, layer)
 
 bool make_geo(const moe_layer_desc &d, Geo &g);
 void make_ws_layout(const Geo &g, int max_M, WsLayout &w);
+// The decode kernel is built for two numbers of compute warps (each CTA has
+// one more, the producer): 11 for rows of at most 2048 inputs, where more
+// warps hide more of the row kernels' latency, and 8 for wider rows, whose
+// gate/up units would otherwise be cut into twice as many ring stages (bulk
+// copies).  Registers are given to warps in fours, so both builds get 168
+// per thread.  make_plan / launch_decode are the 11-warp build, the _w8
+// entries the 8-warp one; decode_plan / decode_launch pick.
+inline int decode_warps(const Geo &g) { return g.H <= 2048 ? 11 : 8; }
 bool make_plan(const Geo &g, int maxr, int num_sms, Plan &p);
+bool make_plan_w8(const Geo &g, int maxr, int num_sms, Plan &p);
+inline bool decode_plan(const Geo &g, int maxr, int num_sms, Plan &p)
+{
+    return decode_warps(g) == 8 ? make_plan_w8(g, maxr, num_sms, p) : make_plan(g, maxr, num_sms, p);
+}
 int rows_per_launch(int H);
 int device_sms();
 
@@ -198,6 +210,11 @@ struct moe_qkv {
 // moe_grouped.cu).
 namespace moe {
 int launch_decode(const KParams &kp, cudaStream_t stream);
+int launch_decode_w8(const KParams &kp, cudaStream_t stream);
+inline int decode_launch(const KParams &kp, cudaStream_t stream)
+{
+    return kp.p.ncw == 8 ? launch_decode_w8(kp, stream) : launch_decode(kp, stream);
+}
 int launch_pack(const moe_layer &L, const moe_src_layer &src, cudaStream_t stream);
 // rows of one matrix into consecutive packed rows at dst (moe_pack.cu)
 int launch_pack_rows(const moe_src_matrix &m, int bits, int rows, int K, uint8_t *dst, cudaStream_t stream);

@@ -64,8 +64,18 @@
 namespace moe {
 namespace {
 
-constexpr int NCW = kConsumerWarps;
+// Compute warps of this build (the library builds 11 and 8: decode_plan).
+#ifndef MOE_NCW
+#define MOE_NCW 11
+#endif
+#if MOE_NCW == 11
+#define MOE_WBUILD(name) name
+#else
+#define MOE_WBUILD(name) name##_w8
+#endif
+constexpr int NCW = MOE_NCW;
 constexpr int NCT = NCW * 32;
+constexpr int kThreads = (NCW + 1) * 32;   // + the producer warp
 constexpr unsigned FULLMASK = 0xffffffffu;
 constexpr float kXScale = 0x1p100f;  // arranged vectors hold x * 2^100
 // RMSNorm sums of squares: one slot per 256 inputs of a row (H <= 8192),
@@ -1778,9 +1788,12 @@ __device__ __forceinline__ void p2_units(const KParams &kp, const Sh &sh, int U,
     const int ub = 2 * g.g_bytes;
     int a, b;
     split(U * g.I, gridDim.x, blockIdx.x, a, b);
-    // about one stage per compute warp, an even number of units (a lane
-    // takes two at a time) where the stage size allows
-    const int cu = max(1, min(sh.S / ub, 2 * ((b - a + 2 * NCW - 1) / (2 * NCW))));
+    // about one stage per compute warp where the stage size allows: with one
+    // token row and K <= 2048 (the one-vector kernel, a unit per pass) any
+    // number of units, otherwise an even number (the general kernel's lanes
+    // take two at a time)
+    const bool one = kp.M == 1 && g.H <= 32 * kGroup && g.rb != 0;
+    const int cu = max(1, min(sh.S / ub, one ? (b - a + NCW - 1) / NCW : 2 * ((b - a + 2 * NCW - 1) / (2 * NCW))));
     int s = (int)((unsigned)a / (unsigned)g.I), j = a - s * g.I;
 #pragma unroll 1
     for (int n = a; n < b;) {
@@ -2754,10 +2767,11 @@ bool g_attr_set[64];
 // at one SM's share of the bandwidth), then the prefetch buffer up to one
 // layer's P1 rows, then staging pairs up to every pair of a launch, then
 // the ring takes whatever is left.
-bool make_plan(const Geo &g, int maxr, int num_sms, Plan &p)
+bool MOE_WBUILD(make_plan)(const Geo &g, int maxr, int num_sms, Plan &p)
 {
     p.P = num_sms;
     p.maxr = maxr;
+    p.ncw = NCW;
     p.max_slots = g.E < maxr * g.k ? g.E : maxr * g.k;
     p.hrows = 2 * ((g.H / 2 + num_sms - 1) / num_sms);   // whole row pairs per CTA
     int maxi = 2 * g.g_bytes;
@@ -2837,8 +2851,9 @@ bool make_plan(const Geo &g, int maxr, int num_sms, Plan &p)
     return false;
 }
 
-int launch_decode(const KParams &kp, cudaStream_t stream)
+int MOE_WBUILD(launch_decode)(const KParams &kp, cudaStream_t stream)
 {
+    if (kp.p.ncw != NCW) return MOE_ERR_INVALID_ARG;
     int dev = 0;
     cudaError_t e = cudaGetDevice(&dev);
     if (e != cudaSuccess || dev < 0 || dev >= 64) { note_cuda_error((int)e); return MOE_ERR_CUDA; }
@@ -2864,6 +2879,8 @@ int launch_decode(const KParams &kp, cudaStream_t stream)
     return MOE_OK;
 }
 
+#if MOE_NCW == 11
+// (once in the library: the 8-warp build leaves these out)
 int device_sms()
 {
     int dev = 0;
@@ -2963,6 +2980,8 @@ int launch_qkv(const uint8_t *W, int rows, int K, int bits, const uint16_t *x, i
     if (e != cudaSuccess) { note_cuda_error((int)e); return MOE_ERR_CUDA; }
     return MOE_OK;
 }
+
+#endif  // MOE_NCW == 11
 
 }  // namespace moe
 

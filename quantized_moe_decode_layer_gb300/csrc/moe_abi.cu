@@ -227,7 +227,7 @@ int plan_selftest_host()
             for (int mc = 1; mc <= R; ++mc) {
                 Plan p;
                 if (!decode_plan(g, mc, sms, p)) { ++bad; continue; }
-                if (p.ncw != decode_warps(g) || p.NS % p.ncw != 0 || p.NS > 32 || p.NS > kMaxStages) ++bad;
+                if (p.ncw != decode_warps(g, mc) || p.NS % p.ncw != 0 || p.NS > 32 || p.NS > kMaxStages) ++bad;
                 if (p.S % 16 != 0 || p.S < maxi) ++bad;
                 if (p.smem_bytes > kSmemMax) ++bad;
                 if (p.act_pairs < p.maxr) ++bad;

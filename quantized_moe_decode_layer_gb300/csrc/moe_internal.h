@@ -168,18 +168,20 @@ constexpr int kTraceEvents = 24; // events recorded per (CTA, layer)
 bool make_geo(const moe_layer_desc &d, Geo &g);
 void make_ws_layout(const Geo &g, int max_M, WsLayout &w);
 // The decode kernel is built for two numbers of compute warps (each CTA has
-// one more, the producer): 11 for rows of at most 2048 inputs, where more
-// warps hide more of the row kernels' latency, and 8 for wider rows, whose
-// gate/up units would otherwise be cut into twice as many ring stages (bulk
-// copies).  Registers are given to warps in fours, so both builds get 168
+// one more, the producer): 11 for launches of at most 4 token rows of at
+// most 2048 inputs, where more warps hide more of the row kernels' latency,
+// and 8 otherwise: wider rows' gate/up units would be cut into twice as
+// many ring stages (bulk copies), and with more rows the staging buffer
+// leaves the 22-stage ring too little room (8 rows: 351 against 190 us per
+// layer).  Registers are given to warps in fours, so both builds get 168
 // per thread.  make_plan / launch_decode are the 11-warp build, the _w8
 // entries the 8-warp one; decode_plan / decode_launch pick.
-inline int decode_warps(const Geo &g) { return g.H <= 2048 ? 11 : 8; }
+inline int decode_warps(const Geo &g, int maxr) { return g.H <= 2048 && maxr <= 4 ? 11 : 8; }
 bool make_plan(const Geo &g, int maxr, int num_sms, Plan &p);
 bool make_plan_w8(const Geo &g, int maxr, int num_sms, Plan &p);
 inline bool decode_plan(const Geo &g, int maxr, int num_sms, Plan &p)
 {
-    return decode_warps(g) == 8 ? make_plan_w8(g, maxr, num_sms, p) : make_plan(g, maxr, num_sms, p);
+    return decode_warps(g, maxr) == 8 ? make_plan_w8(g, maxr, num_sms, p) : make_plan(g, maxr, num_sms, p);
 }
 int rows_per_launch(int H);
 int device_sms();

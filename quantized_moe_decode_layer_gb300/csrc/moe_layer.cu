@@ -1,7 +1,9 @@
 // Persistent decode kernel of the quantized MoE FFN layer (and of a stack of
 // such layers) for sm_103a.
 //
-// One CTA per SM: eight compute warps and one producer warp.  The producer
+// One CTA per SM: eleven compute warps (launches of at most 4 rows of at
+// most 2048 inputs) or eight (this source compiled with MOE_NCW=8), and one
+// producer warp.  The producer
 // streams weights into shared memory with 1-D bulk copies
 // (cp.async.bulk ... mbarrier::complete_tx): a ring of stages holding the
 // routed experts (and shared-expert rows that do not fit elsewhere), each

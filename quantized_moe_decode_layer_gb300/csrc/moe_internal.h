@@ -135,7 +135,7 @@ struct Plan {
     int maxr;                // rows per launch
     int max_slots;
     int hrows;               // output rows per CTA (upper bound, even)
-    int pb_bytes;            // prefetch buffer (gamma, router rows, shared units of a layer)
+    int pb_bytes;            // prefetch buffer (gamma, the CTA's router slice, shared units of a layer)
     int act_pairs;           // (slot, row) activation vectors the staging buffer holds
     int smem_bytes;
     int ncw;                 // compute warps of the kernel build the plan is for

@@ -124,7 +124,7 @@ __host__ __device__ inline int take(int &o, int bytes, int align)
 
 __host__ __device__ inline int imax_of(const Geo &g) { return g.Is > g.I ? g.Is : g.I; }
 
-// Router rows / shared units taken by one CTA at most.
+// Router rows (logits summed) / shared units taken by one CTA at most.
 __host__ __device__ inline int per_cta(int n, int P) { return (n + P - 1) / P; }
 
 __host__ __device__ inline SmemLayout carve(const Geo &g, const Plan &p)
@@ -2299,7 +2299,7 @@ __device__ __forceinline__ void compute(const KParams &kp, const Sh &sh)
         const void *xin = l == 0 ? static_cast<const void *>(kp.x) : static_cast<const void *>(w.ping[(l - 1) & 1]);
         const bool t0 = threadIdx.x == 0;
         if (t0) stamp(kp, l, 0);
-        // layer l's gamma, router rows and shared units
+        // layer l's gamma, router slice and shared units
         const bool pb_ok = wait_bar(sh, sh.pb_full, (unsigned)l & 1u, 5);
         if (t0) stamp(kp, l, 18);
         if (cbar_or(!pb_ok)) return;

@@ -113,7 +113,9 @@ enum {
 };
 
 /* Bytes of the packed device blob of one layer (codes as LSB-first bit
- * streams, per-group bf16 scale and bias, rows padded to 16 bytes).
+ * streams, per-group bf16 scale and bias, rows padded to 16 bytes; the
+ * router also input-major, one code byte per weight, so that the decode
+ * kernel's CTAs can each fetch a column slice of every router row).
  * Errors: MOE_ERR_INVALID_ARG (NULL), MOE_ERR_UNSUPPORTED (sizes/bits). */
 int moe_pack_size(const moe_layer_desc *desc, size_t *weight_bytes);
 
@@ -138,14 +140,16 @@ int moe_export_canonical(const moe_layer *layer, int tensor_id, int expert, uint
                          uint16_t *scales_dev, uint16_t *biases_dev, moe_stream_t stream);
 
 /* Scratch bytes needed by the decode calls for up to max_M rows per call
- * (logits, expert activations, inter-layer activations and a control block).
+ * (partial router dots, logits, expert activations, inter-layer activations
+ * and a control block).
  * The same workspace serves every call on one stream; calls that run at the
  * same time on the GPU need separate workspaces. */
 int moe_workspace_size(const moe_layer_desc *desc, int max_M, size_t *ws_bytes);
 
-/* Zeroes the workspace control block (grid-barrier state and status word).
- * Call once after allocating a workspace, and again after any call reported
- * MOE_ERR_TIMEOUT or MOE_ERR_DEVICE. */
+/* Zeroes the workspace: the control block (launch counter, status word)
+ * and every word the kernels exchange.  Call once after allocating a
+ * workspace, and again after any call reported MOE_ERR_TIMEOUT or
+ * MOE_ERR_DEVICE. */
 int moe_workspace_init(void *ws_dev, size_t ws_bytes, moe_stream_t stream);
 
 /* Router only (RMSNorm, router mat-vec, softmax, top-k, renormalisation) for

@@ -301,6 +301,17 @@ def test_b397_m1():
     check_layer(shape, L, layer, lay, x)
 
 
+def test_b397_m3_rows_equal_m1_bitwise():
+    """397B shape (rows of 4096 inputs: the 8-compute-warp build), 3 rows with
+    the routing warps beside the RMSNorm: parity, and every row bitwise the
+    one-row call."""
+    shape = synth.B397
+    L, layer, lay = cached(shape, 13)
+    x = rows_with_margin(shape, lay, 5, 3, correlation=0.6, gamma=L["gamma"])
+    out, _ = check_layer(shape, L, layer, lay, x)
+    rows_equal_one_row_calls(layer, x, out)
+
+
 def test_deterministic_repeat():
     shape = synth.TINY
     L, layer, lay = cached(shape, 7)
@@ -309,6 +320,34 @@ def test_deterministic_repeat():
     a = moe.decode_layer(layer, x, ws)
     b = moe.decode_layer(layer, x, ws)
     assert torch.equal(a.view(torch.int16), b.view(torch.int16))
+
+
+def test_tiny_m5_rows_equal_m1_bitwise():
+    """5 rows: more routing rows than half the compute warps, so every warp
+    builds hn before the first five route (the 8-warp build); each row
+    bitwise the one-row call."""
+    shape = synth.TINY
+    L, layer, lay = cached(shape, 7)
+    x = rows_with_margin(shape, lay, 78, 5)
+    out, _ = check_layer(shape, L, layer, lay, x)
+    rows_equal_one_row_calls(layer, x, out)
+
+
+def test_a35b_m4_deterministic_repeat():
+    """35B shape, 1 token + 3 correlated draft rows (shared experts, and
+    shared-expert units that come through the ring): repeated calls on one
+    workspace and a call on a fresh one are bitwise equal (no race between
+    the warps that route and those that build hn)."""
+    shape = synth.A35B
+    L, layer, lay = cached(shape, 11)
+    x = synth.make_rows(shape, 61, 4, correlation=0.6, gamma=L["gamma"]).to(DEV)
+    ws = moe.Workspace(layer.desc, 4)
+    outs = [moe.decode_layer(layer, x, ws) for _ in range(3)]
+    outs.append(moe.decode_layer(layer, x, moe.Workspace(layer.desc, 4)))
+    torch.cuda.synchronize()
+    assert ws.status() == 0
+    for o in outs[1:]:
+        assert torch.equal(o.view(torch.int16), outs[0].view(torch.int16))
 
 
 def test_out_aliases_x():

@@ -92,6 +92,7 @@ struct AttnParams {
     const uint16_t *q;    // [M][16][256]
     float *part_o;        // [chunk][2][64][256]
     float *part_ml;       // [chunk][2][64][2]: running maximum, sum
+    unsigned *seg_cnt;    // [M * 16] combine segments done (cleared by chunk CTA (0, 0))
     int M, pos0, n_valid, nq, nsub;
     long long timeout_ns;
     int *err;
@@ -270,6 +271,9 @@ __global__ void __launch_bounds__(kAThreads, MINB) attn_chunk_kernel(const __gri
     const int nkeys = min(kAChunk, p.n_valid - k0);
     const int nt = (nkeys + kAKeys - 1) / kAKeys, nbox = 8 * nt;
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+    // the combine's segment counters of this call start at zero (the
+    // combine kernel runs after this one on the stream)
+    if (chunk == 0 && g == 0 && tid < M * kAHq) p.seg_cnt[tid] = 0u;
 
     uint8_t *ring = sm + L.ring, *qs = sm + L.q, *ps = sm + L.p;
     uint32_t *red_max = reinterpret_cast<uint32_t *>(sm + L.red);        // [4][64]
@@ -575,19 +579,31 @@ __global__ void __launch_bounds__(kAThreads, MINB) attn_chunk_kernel(const __gri
 // shared memory (all threads load them together), then each thread's loads
 // of its d from every chunk are independent and overlap.
 constexpr int kACombineChunks = kAMaxPos / kAChunk;
-__global__ void __launch_bounds__(kAD) attn_combine_kernel(const float *part_o, const float *part_ml, int pos0, float *o)
+constexpr int kASeg = 16;                               // chunks per combine segment
+
+// The chunks of row m, head h merged: every chunk's output rescaled by
+// exp(its running maximum - the maximum over all chunks) and summed, and
+// divided by the sum of its rescaled sums.  One CTA per (row, head, segment
+// of kASeg chunks): each sums its segment in chunk order (thread = d); the
+// last CTA of a (row, head) to finish (a counter, after a memory fence)
+// adds the segments' sums in segment order.  The order depends only on the
+// row's position, so a row's result does not depend on M.
+__global__ void __launch_bounds__(kAD) attn_combine_kernel(const float *part_o, const float *part_ml, int pos0,
+                                                           float *o, float *seg_o, float *seg_l, unsigned *seg_cnt,
+                                                           int smax)
 {
-    __shared__ float wsh[kACombineChunks];
+    __shared__ float wsh[kASeg];
     __shared__ float red[kAD / 32];
-    const int m = blockIdx.x / kAHq, h = blockIdx.x % kAHq, g = h / kAGrp, q = kAGrp * m + h % kAGrp;
+    __shared__ int last;
+    const int mh = blockIdx.x, seg = blockIdx.y;
+    const int m = mh / kAHq, h = mh % kAHq, g = h / kAGrp, q = kAGrp * m + h % kAGrp;
     const int d = threadIdx.x, lane = d & 31, warp = d >> 5;
     const int J = (pos0 + m + 1 + kAChunk - 1) / kAChunk;   // <= kACombineChunks (host check)
+    const int S = (J + kASeg - 1) / kASeg;
+    if (seg >= S) return;
+    auto ml = [&](int j) { return part_ml + (((size_t)j * kAHkv + g) * kAMaxQ + q) * 2; };
     float mx = -INFINITY;
-    for (int j = d; j < J; j += kAD) {
-        const float v = __ldg(part_ml + (((size_t)j * kAHkv + g) * kAMaxQ + q) * 2);
-        wsh[j] = v;
-        mx = fmaxf(mx, v);
-    }
+    for (int j = d; j < J; j += kAD) mx = fmaxf(mx, __ldg(ml(j)));
 #pragma unroll
     for (int off = 16; off >= 1; off >>= 1) mx = fmaxf(mx, __shfl_xor_sync(0xFFFFFFFFu, mx, off));
     if (lane == 0) red[warp] = mx;
@@ -595,17 +611,38 @@ __global__ void __launch_bounds__(kAD) attn_combine_kernel(const float *part_o, 
     mx = red[0];
 #pragma unroll
     for (int w = 1; w < kAD / 32; ++w) mx = fmaxf(mx, red[w]);
-    for (int j = d; j < J; j += kAD) wsh[j] = expf(wsh[j] - mx);
+    const int j0 = seg * kASeg, nj = min(kASeg, J - j0);
+    if (d < nj) wsh[d] = expf(__ldg(ml(j0 + d)) - mx);
     __syncthreads();
     float acc = 0.f, lsum = 0.f;
-#pragma unroll 8
-    for (int j = 0; j < J; ++j) {
-        const size_t c = ((size_t)j * kAHkv + g) * kAMaxQ + q;
-        const float w = wsh[j];
-        lsum = fmaf(__ldg(part_ml + 2 * c + 1), w, lsum);
-        acc = fmaf(__ldg(part_o + c * kAD + d), w, acc);
+#pragma unroll
+    for (int jj = 0; jj < kASeg; ++jj)
+        if (jj < nj) {
+            const size_t c = ((size_t)(j0 + jj) * kAHkv + g) * kAMaxQ + q;
+            const float w = wsh[jj];
+            lsum = fmaf(__ldg(part_ml + 2 * c + 1), w, lsum);
+            acc = fmaf(__ldg(part_o + c * kAD + d), w, acc);
+        }
+    float *out = o + ((size_t)m * kAHq + h) * kAD + d;
+    if (S == 1) {
+        *out = acc / lsum;
+        return;
     }
-    o[((size_t)m * kAHq + h) * kAD + d] = acc / lsum;
+    seg_o[((size_t)mh * smax + seg) * kAD + d] = acc;
+    if (d == 0) seg_l[(size_t)mh * smax + seg] = lsum;
+    __threadfence();
+    __syncthreads();
+    if (d == 0) last = atomicAdd(seg_cnt + mh, 1u) == (unsigned)(S - 1);
+    __syncthreads();
+    if (!last) return;
+    __threadfence();
+    float a = 0.f, l = 0.f;
+#pragma unroll 4
+    for (int s2 = 0; s2 < S; ++s2) {
+        a += __ldcg(seg_o + ((size_t)mh * smax + s2) * kAD + d);
+        l += __ldcg(seg_l + (size_t)mh * smax + s2);
+    }
+    *out = a / l;
 }
 
 // New rows' keys and values into the cache: row m at position pos0 + m;
@@ -637,11 +674,30 @@ PFN_cuTensorMapEncodeTiled_v12000 encode_fn()
 
 int attn_max_positions() { return kAMaxPos; }
 
-size_t attn_workspace_bytes(int T_cap)
+// Workspace: per-chunk maxima and sums [chunk][2][64][2], per-chunk outputs
+// [chunk][2][64][256], the combine's segment sums [8 * 16][seg] and segment
+// outputs [8 * 16][seg][256], and its counters [8 * 16] (fp32 / u32, each
+// region 256-byte aligned).
+struct AWs {
+    size_t ml, po, sl, so, cnt, total;
+    int smax;
+};
+AWs attn_ws_layout(int T_cap)
 {
+    AWs w;
     const size_t nchunks = (size_t)(T_cap + kAChunk - 1) / kAChunk;
-    return align_up(nchunks * kAHkv * kAMaxQ * 2 * sizeof(float), 256) + nchunks * kAHkv * kAMaxQ * kAD * sizeof(float);
+    w.smax = (int)((nchunks + kASeg - 1) / kASeg);
+    const size_t mh = (size_t)kAMaxRows * kAHq;
+    w.ml = 0;
+    w.po = align_up(nchunks * kAHkv * kAMaxQ * 2 * sizeof(float), 256);
+    w.sl = align_up(w.po + nchunks * kAHkv * kAMaxQ * kAD * sizeof(float), 256);
+    w.so = align_up(w.sl + mh * w.smax * sizeof(float), 256);
+    w.cnt = align_up(w.so + mh * w.smax * kAD * sizeof(float), 256);
+    w.total = align_up(w.cnt + mh * sizeof(unsigned), 256);
+    return w;
 }
+
+size_t attn_workspace_bytes(int T_cap) { return attn_ws_layout(T_cap).total; }
 
 int launch_attn(const uint16_t *q, const uint16_t *k, const uint16_t *vt, int T_cap, int pos0, int M, float *o,
                 void *ws, int *err, long long timeout_ns, cudaStream_t stream)
@@ -671,6 +727,8 @@ int launch_attn(const uint16_t *q, const uint16_t *k, const uint16_t *vt, int T_
     }
     const size_t nchunks_cap = (size_t)(T_cap + kAChunk - 1) / kAChunk;
     P.q = q;
+    const AWs aw = attn_ws_layout(T_cap);
+    P.seg_cnt = reinterpret_cast<unsigned *>(static_cast<uint8_t *>(ws) + aw.cnt);
     P.part_ml = static_cast<float *>(ws);
     P.part_o = reinterpret_cast<float *>(static_cast<uint8_t *>(ws) +
                                          align_up(nchunks_cap * kAHkv * kAMaxQ * 2 * sizeof(float), 256));
@@ -721,7 +779,15 @@ int launch_attn(const uint16_t *q, const uint16_t *k, const uint16_t *vt, int T_
         }
     }
     note_launch();
-    attn_combine_kernel<<<M * kAHq, kAD, 0, stream>>>(P.part_o, P.part_ml, pos0, o);
+    {
+        // segments of the last row (the most chunks); other rows' CTAs past
+        // their own segments return at once
+        const int Jmax = (pos0 + M + kAChunk - 1) / kAChunk;
+        const dim3 cgrid(M * kAHq, (Jmax + kASeg - 1) / kASeg);
+        attn_combine_kernel<<<cgrid, kAD, 0, stream>>>(
+            P.part_o, P.part_ml, pos0, o, reinterpret_cast<float *>(static_cast<uint8_t *>(ws) + aw.so),
+            reinterpret_cast<float *>(static_cast<uint8_t *>(ws) + aw.sl), P.seg_cnt, aw.smax);
+    }
     note_launch();
     e = cudaGetLastError();
     if (e != cudaSuccess) { note_cuda_error((int)e); return MOE_ERR_CUDA; }

@@ -175,14 +175,24 @@ def test_build_flags_of_both_builds():
 
 def test_attention_sizes_and_argument_errors():
     """Workspace size of the decode attention (per 512-position chunk: 2 KV
-    heads x 64 query columns x (256 + 2) floats, the maxima and sums first,
-    256-aligned) and its argument checks, which reject before any launch."""
+    heads x 64 query columns x (256 + 2) floats, the maxima and sums first;
+    then for the merge, per (row, query head) of 8 x 16 and segment of 16
+    chunks, a sum and 256 outputs, and a counter per (row, head); each
+    region 256-aligned) and its argument checks, which reject before any
+    launch."""
     L = moe.lib()
     n = C.c_size_t()
-    assert L.moe_attn_workspace_size(4096, C.byref(n)) == 0
-    chunks = 8
-    ml = chunks * 2 * 64 * 2 * 4
-    assert n.value == ((ml + 255) // 256) * 256 + chunks * 2 * 64 * 256 * 4
+
+    def a256(v):
+        return (v + 255) // 256 * 256
+    for T_cap, chunks in ((4096, 8), (40960, 80)):
+        assert L.moe_attn_workspace_size(T_cap, C.byref(n)) == 0
+        segs = (chunks + 15) // 16
+        po = a256(chunks * 2 * 64 * 2 * 4)
+        sl = a256(po + chunks * 2 * 64 * 256 * 4)
+        so = a256(sl + 128 * segs * 4)
+        cnt = a256(so + 128 * segs * 256 * 4)
+        assert n.value == a256(cnt + 128 * 4)
     assert L.moe_attn_workspace_size(0, C.byref(n)) == 1
     fake = 1 << 20   # never dereferenced: every call below is rejected first
     err = fake

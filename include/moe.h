@@ -416,7 +416,8 @@ void moe_qkv_destroy(moe_qkv *qkv);
  *
  * moe_attn_workspace_size: device scratch a call with this T_cap needs
  * (the per-chunk partial results and the merge's per-segment sums and
- * counters; no initialisation needed).  Errors: INVALID_ARG. */
+ * counters; no initialisation needed).  Calls that can run at the same time
+ * on the GPU need separate scratch.  Errors: INVALID_ARG. */
 #define MOE_ATTN_Q_HEADS 16
 #define MOE_ATTN_KV_HEADS 2
 #define MOE_ATTN_HEAD_DIM 256
